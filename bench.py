@@ -1,0 +1,321 @@
+"""Benchmark of the varlen gated-delta-net layer forward through the C ABI.
+
+One step = one gdn_varlen_forward over one packed batch (scheduler + conv +
+recurrence + state write-back, every kernel of the path).  The default
+workload is the 256-request decode batch (one token per request, all with a
+past, 16 k-heads / 32 v-heads, d_k = d_v = 128, K = 4, bf16 activations, fp32
+states, 512-block pool); its state traffic (1 GiB per step) is far larger
+than L2, so no flush is needed between steps.
+
+Prints one JSON line: tokens/s of the whole job, the roofline of the dominant
+(compute) kernel timed live with CUDA events on the launching stream, the
+end-to-end number with host<->device copies from pinned memory inside the
+timed region, SM clocks sampled during the timed region, and the fp64 CPU
+oracle timed on the host cores on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica of the batch on its
+own GPU (requests are independent: no collective on the data path); value is
+the tokens of all ranks over the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN varlen layer tokens/s (prefill, decode); decode state HBM GB/s vs peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = float(d.get("hbm_gbs") or d.get("hbm_GBs") or d["hbm"])
+        bf16 = float(d.get("bf16_tflops"))
+        bf16s = float(d.get("bf16_tflops_sustained", bf16))
+        return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16s,
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def decode_bytes(wl) -> int:
+    """Algorithmic HBM bytes of one decode forward: per request the recurrent
+    state read + write, the conv state read + write, x, a, b and out; the conv
+    weight, A_log and dt_bias once."""
+    d = wl.dims
+    act = 4 if d.act == "f32" else 2
+    per_req = (2 * d.Hv * d.dk * d.dv * 4 + 2 * (d.K - 1) * d.C * act + d.C * act
+               + 2 * d.Hv * act + d.Hv * d.dv * act)
+    weights = d.C * d.K * act + 2 * d.Hv * 4
+    return wl.N * per_req + weights
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        entry = rec[kernel_file]
+        src = os.path.join(ROOT, "continuous_linear_attention_gb300", "csrc", kernel_file)
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if entry.get("source_sha256_16") != digest:
+            return None
+        return entry["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def cpu_baseline(wl, budget_s: float = 12.0):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of
+    the workload (its first requests), scaled to tokens/s."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    import oracle
+    cu = wl.cu_seqlens.tolist()
+    n = min(wl.N, 64)
+    T = cu[n]
+    sub = dataclasses.replace(wl, x=wl.x[:T], a=wl.a[:T], b=wl.b[:T],
+                              cu_seqlens=wl.cu_seqlens[:n + 1].clone(),
+                              block_idx=wl.block_idx[:n], has_past=wl.has_past[:n])
+    reps, t0, threads = 0, time.perf_counter(), 1
+    while True:
+        res = oracle.forward(sub)
+        threads = res["threads"]
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": reps * T / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {wl.N} requests ({T} tokens), {reps} passes, "
+                      f"{el:.1f} s wall, fp64 token-by-token"}
+
+
+def run_reference(args, rank, world):
+    """The oracle (fp64, host cores) as the reference arm."""
+    if rank != 0:
+        return
+    from continuous_linear_attention_gb300 import synth
+    wl = synth.decode_batch()
+    cb = cpu_baseline(wl, budget_s=max(2.0, 20.0 / max(1, args.steps + args.warmup)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_256req_bf16act_fp32state", "requests": wl.N,
+                   "Hk": wl.dims.Hk, "Hv": wl.dims.Hv, "d": wl.dims.dk, "K": wl.dims.K},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from continuous_linear_attention_gb300 import harness, synth
+
+    wl = synth.decode_batch(seed=1 + rank)
+    run = harness.DeviceRun(wl, device=f"cuda:{local_rank}")
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for _ in range(args.warmup):
+        run.run(stream)
+    torch.cuda.synchronize()
+
+    # per-step events around the compute kernels (inside the C-ABI call)
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in kb + ka:
+        e.record(stream)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            run.pool.set_timing_events(kb[i], ka[i])
+            run.run(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    run.pool.set_timing_events(None, None)
+    elapsed_ms = start.elapsed_time(stop)
+    kern_ms = [kb[i].elapsed_time(ka[i]) for i in range(args.steps)]
+    flags = run.pool.error_flags()
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during the bench")
+
+    # end to end: inputs from pinned host memory in, out back, every step
+    host_in = {k: getattr(run, k).cpu().pin_memory() for k in
+               ("x", "a", "b", "cu", "idx", "has_past")}
+    host_out = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    for _ in range(args.warmup):
+        for k, t in host_in.items():
+            getattr(run, k).copy_(t, non_blocking=True)
+        run.run(stream)
+        host_out.copy_(run.out, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for k, t in host_in.items():
+            getattr(run, k).copy_(t, non_blocking=True)
+        run.run(stream)
+        host_out.copy_(run.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # max over ranks
+    t = torch.tensor([elapsed_ms, e2e_ms, statistics.mean(kern_ms)], device=f"cuda:{local_rank}")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms, kern_mean_ms = [float(v) for v in t.tolist()]
+
+    if rank == 0:
+        pk = peaks()
+        tokens = wl.T * world * args.steps
+        value = tokens / (elapsed_ms / 1e3)
+        alg_bytes = decode_bytes(wl)
+        achieved = alg_bytes / (kern_mean_ms / 1e3) / 1e9
+        traffic = traffic_record("gdn_recurrent.cu")
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "decode_256req_bf16act_fp32state", "requests_per_gpu": wl.N,
+                       "tokens_per_gpu": wl.T, "Hk": wl.dims.Hk, "Hv": wl.dims.Hv,
+                       "d_k": wl.dims.dk, "d_v": wl.dims.dv, "K": wl.dims.K,
+                       "act": wl.dims.act, "state": "fp32", "pool_blocks": wl.num_blocks,
+                       "l2": "no flush: 1 GiB of state traffic per step, > 129 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": traffic, "peak_source": pk["source"],
+                         "kernel": "compute kernels of gdn_varlen_forward (decode)",
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "kernel_ms_mean": kern_mean_ms},
+            "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    run.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

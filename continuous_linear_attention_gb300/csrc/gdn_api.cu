@@ -1,0 +1,286 @@
+// C ABI of libgdn: the paged state pool, host-side validation and the launch
+// sequence of one layer forward.  The operations follow the pages on
+// continuous batching for linear attention layers (per-request state block,
+// zeroed trash block, in-place overwrite, 128-byte sub-state alignment) and
+// the gated delta rule; see include/gdn.h for the full contract.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "gdn.h"
+#include "gdn_internal.cuh"
+
+struct gdn_pool {
+  int num_blocks, num_layers, Hk, Hv, dk, dv, K, act;
+  size_t stride, conv_off, rec_off, total;
+  unsigned char* base;
+  bool owns;
+  int device;
+  int32_t* work;  // num_layers * WorkArea::words(num_blocks) words
+  cudaEvent_t ev_before, ev_after;  // optional timing events (caller-owned)
+};
+
+namespace {
+
+size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+bool is_pow2(size_t v) { return v && !(v & (v - 1)); }
+
+int check_dims(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv, int K, int act,
+               size_t block_align) {
+  if (num_blocks < 2 || num_layers < 1) return GDN_ERR_RANGE;
+  if (Hk < 1 || Hv < 1 || Hv % Hk != 0) return GDN_ERR_DIMS;
+  const int ratio = Hv / Hk;
+  if (ratio > 2) return GDN_ERR_DIMS;
+  if (dk != dv || (dk != 32 && dk != 64 && dk != 128)) return GDN_ERR_DIMS;
+  if (K < 2 || K > gdn::kMaxConvK) return GDN_ERR_DIMS;
+  if (act != GDN_F32 && act != GDN_BF16) return GDN_ERR_DIMS;
+  if (block_align != 0 && (block_align < 128 || !is_pow2(block_align))) return GDN_ERR_DIMS;
+  // every block byte offset must fit comfortably in size_t and indices in int
+  if ((long long)num_blocks * num_layers > (1ll << 30)) return GDN_ERR_RANGE;
+  return GDN_OK;
+}
+
+struct Layout {
+  size_t stride, conv_off, rec_off, total;
+};
+
+Layout layout_of(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv, int K, int act,
+                 size_t block_align) {
+  const size_t C = 2 * (size_t)Hk * dk + (size_t)Hv * dv;
+  const size_t act_bytes = act == GDN_F32 ? 4 : 2;
+  const size_t conv_bytes = (size_t)(K - 1) * C * act_bytes;
+  const size_t rec_bytes = (size_t)Hv * dk * dv * sizeof(float);
+  Layout l;
+  l.conv_off = 0;
+  l.rec_off = roundup(conv_bytes, 128);
+  size_t align = block_align > 128 ? block_align : 128;
+  l.stride = roundup(l.rec_off + rec_bytes, align);
+  l.total = l.stride * (size_t)num_blocks * (size_t)num_layers;
+  return l;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_NULL: return "a required pointer is NULL";
+    case GDN_ERR_DIMS: return "dimensions inconsistent or unsupported";
+    case GDN_ERR_RANGE: return "argument out of range";
+    case GDN_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case GDN_ERR_CUDA: return "CUDA runtime error";
+    case GDN_ERR_NOMEM: return "out of device memory or buffer too small";
+    case GDN_ERR_DEVICE: return "current device differs from the pool's device";
+    default: return "unknown status";
+  }
+}
+
+int gdn_state_pool_layout_for(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv,
+                              int K, int act, size_t block_align, size_t* block_stride,
+                              size_t* conv_off, size_t* rec_off, size_t* total_bytes) {
+  int st = check_dims(num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align);
+  if (st != GDN_OK) return st;
+  Layout l = layout_of(num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align);
+  if (block_stride) *block_stride = l.stride;
+  if (conv_off) *conv_off = l.conv_off;
+  if (rec_off) *rec_off = l.rec_off;
+  if (total_bytes) *total_bytes = l.total;
+  return GDN_OK;
+}
+
+int gdn_state_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int Hk, int Hv,
+                          int dk, int dv, int K, int act, size_t block_align, void* device_mem,
+                          size_t device_bytes) {
+  if (!out) return GDN_ERR_NULL;
+  *out = nullptr;
+  int st = check_dims(num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align);
+  if (st != GDN_OK) return st;
+  Layout l = layout_of(num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align);
+  if (device_mem) {
+    if (device_bytes < l.total) return GDN_ERR_NOMEM;
+    if (((uintptr_t)device_mem & 255u) != 0) return GDN_ERR_ALIGN;
+  }
+  gdn_pool* p = new (std::nothrow) gdn_pool();
+  if (!p) return GDN_ERR_NOMEM;
+  p->num_blocks = num_blocks;
+  p->num_layers = num_layers;
+  p->Hk = Hk;
+  p->Hv = Hv;
+  p->dk = dk;
+  p->dv = dv;
+  p->K = K;
+  p->act = act;
+  p->stride = l.stride;
+  p->conv_off = l.conv_off;
+  p->rec_off = l.rec_off;
+  p->total = l.total;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return GDN_ERR_CUDA;
+  }
+  if (device_mem) {
+    p->base = (unsigned char*)device_mem;
+    p->owns = false;
+  } else {
+    if (cudaMalloc((void**)&p->base, l.total) != cudaSuccess) {
+      cudaGetLastError();
+      delete p;
+      return GDN_ERR_NOMEM;
+    }
+    p->owns = true;
+  }
+  const size_t work_bytes = gdn::WorkArea::words(num_blocks) * num_layers * sizeof(int32_t);
+  if (cudaMalloc((void**)&p->work, work_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    if (p->owns) cudaFree(p->base);
+    delete p;
+    return GDN_ERR_NOMEM;
+  }
+  if (cudaMemset(p->base, 0, l.total) != cudaSuccess ||
+      cudaMemset(p->work, 0, work_bytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    if (p->owns) cudaFree(p->base);
+    cudaFree(p->work);
+    delete p;
+    return GDN_ERR_CUDA;
+  }
+  *out = p;
+  return GDN_OK;
+}
+
+int gdn_state_pool_destroy(gdn_pool_t* p) {
+  if (!p) return GDN_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  if (p->owns) cudaFree(p->base);
+  cudaFree(p->work);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete p;
+  return GDN_OK;
+}
+
+int gdn_state_pool_layout(const gdn_pool_t* p, size_t* block_stride, size_t* conv_off,
+                          size_t* rec_off, void** base) {
+  if (!p) return GDN_ERR_NULL;
+  if (block_stride) *block_stride = p->stride;
+  if (conv_off) *conv_off = p->conv_off;
+  if (rec_off) *rec_off = p->rec_off;
+  if (base) *base = p->base;
+  return GDN_OK;
+}
+
+int gdn_state_pool_copy_block(gdn_pool_t* p, int layer, int src, int dst, void* stream) {
+  if (!p) return GDN_ERR_NULL;
+  if (layer < 0 || layer >= p->num_layers) return GDN_ERR_RANGE;
+  if (src < 0 || src >= p->num_blocks || dst <= 0 || dst >= p->num_blocks) return GDN_ERR_RANGE;
+  if (src == dst) return GDN_OK;
+  unsigned char* page = p->base + (size_t)layer * p->num_blocks * p->stride;
+  cudaError_t e = cudaMemcpyAsync(page + (size_t)dst * p->stride, page + (size_t)src * p->stride,
+                                  p->stride, cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* a, const void* b,
+                       const int32_t* cu_seqlens, const int32_t* state_block_idx,
+                       const uint8_t* has_past, const gdn_weights_t* w, void* out, int T, int N,
+                       int max_seqlen_hint, void* stream) {
+  (void)max_seqlen_hint;
+  if (!p || !w) return GDN_ERR_NULL;
+  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0) return GDN_ERR_RANGE;
+  if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
+  if (!cu_seqlens || !state_block_idx || !has_past || !w->conv_w || !w->A_log || !w->dt_bias)
+    return GDN_ERR_NULL;
+  if (T > 0 && (!x_qkv || !a || !b || !out)) return GDN_ERR_NULL;
+  const int C = 2 * p->Hk * p->dk + p->Hv * p->dv;
+  const size_t act_bytes = p->act == GDN_F32 ? 4 : 2;
+  if ((long long)T * C > (1ll << 40)) return GDN_ERR_RANGE;
+  if (T > 0 && (!aligned16(x_qkv) || !aligned16(a) || !aligned16(b) || !aligned16(out)))
+    return GDN_ERR_ALIGN;
+  if (!aligned16(w->conv_w) || ((size_t)C * act_bytes) % 16 != 0 ||
+      ((size_t)p->dv * act_bytes) % 16 != 0)
+    return GDN_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev != p->device) return GDN_ERR_DEVICE;
+
+  gdn::FwdParams fp;
+  fp.x = x_qkv;
+  fp.a = a;
+  fp.b = b;
+  fp.cu = cu_seqlens;
+  fp.blk = state_block_idx;
+  fp.has_past = has_past;
+  fp.conv_w = w->conv_w;
+  fp.A_log = w->A_log;
+  fp.dt_bias = w->dt_bias;
+  fp.out = out;
+  fp.layer_base = p->base + (size_t)layer * p->num_blocks * p->stride;
+  fp.stride = p->stride;
+  fp.rec_off = p->rec_off;
+  fp.T = T;
+  fp.N = N;
+  fp.Hk = p->Hk;
+  fp.Hv = p->Hv;
+  fp.C = C;
+  fp.K = p->K;
+  fp.num_blocks = p->num_blocks;
+  fp.work.base = p->work + (size_t)layer * gdn::WorkArea::words(p->num_blocks);
+  fp.work.num_blocks = p->num_blocks;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (T == 0) {
+    if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+  }
+  // at most one active sequence per non-trash block, and at most T non-empty ones
+  int max_items = N;
+  if (max_items > p->num_blocks - 1) max_items = p->num_blocks - 1;
+  if (max_items > T) max_items = T;
+  if (gdn::launch_recurrent(fp, p->dk, p->act, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+int gdn_pool_set_timing_events(gdn_pool_t* p, void* before, void* after) {
+  if (!p) return GDN_ERR_NULL;
+  if ((before == nullptr) != (after == nullptr)) return GDN_ERR_NULL;
+  p->ev_before = (cudaEvent_t)before;
+  p->ev_after = (cudaEvent_t)after;
+  return GDN_OK;
+}
+
+int gdn_get_error(gdn_pool_t* p, int layer, uint32_t* flags, int reset, void* stream) {
+  if (!p || !flags) return GDN_ERR_NULL;
+  if (layer >= p->num_layers) return GDN_ERR_RANGE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t words = gdn::WorkArea::words(p->num_blocks);
+  uint32_t acc = 0;
+  for (int l = 0; l < p->num_layers; ++l) {
+    if (layer >= 0 && l != layer) continue;
+    uint32_t v = 0;
+    int32_t* word = p->work + (size_t)l * words + gdn::kErr;
+    if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+    acc |= v;
+    if (reset && cudaMemsetAsync(word, 0, sizeof(uint32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  if (reset && cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  *flags = acc;
+  return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Internal declarations shared by the CUDA translation units of libgdn.
+// Nothing here is part of the C ABI (include/gdn.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr float kL2Eps = 1e-6f;  // inside the root of the L2 norm of q and k
+constexpr int kMaxConvK = 4;
+
+// Per-layer work area, library-owned, laid out as int32 words:
+//   [0]            error word (uint32, OR of GDN_FLAG_*)
+//   [1 .. 15]      counters, see Cnt
+//   then           blk_count[num_blocks]   block-use counts (duplicate check)
+//                  items[num_blocks]       active sequences (any length)
+//                  dec[num_blocks]         active sequences of length 1
+//                  pre_tmp[num_blocks]     active sequences of length > 1, unsorted
+//                  pre[num_blocks]         the same, longest first
+enum Cnt : int {
+  kErr = 0,
+  kNItems = 1,
+  kNDec = 2,
+  kNPre = 3,
+  kPreTokens = 4,  // total tokens of the length>1 sequences
+  kWorkHead = 5,   // dynamic work counter of persistent kernels (reset by the scheduler)
+  kHeaderWords = 16,
+};
+
+struct WorkArea {
+  int32_t* base;  // kHeaderWords + 5 * num_blocks words
+  int num_blocks;
+  __host__ __device__ int32_t* header() const { return base; }
+  __host__ __device__ int32_t* blk_count() const { return base + kHeaderWords; }
+  __host__ __device__ int32_t* items() const { return base + kHeaderWords + 1 * num_blocks; }
+  __host__ __device__ int32_t* dec() const { return base + kHeaderWords + 2 * num_blocks; }
+  __host__ __device__ int32_t* pre_tmp() const { return base + kHeaderWords + 3 * num_blocks; }
+  __host__ __device__ int32_t* pre() const { return base + kHeaderWords + 4 * num_blocks; }
+  static size_t words(int num_blocks) { return kHeaderWords + 5 * (size_t)num_blocks; }
+};
+
+// Everything a forward kernel needs, passed by value.
+struct FwdParams {
+  const void* x;        // [T][C] act
+  const void* a;        // [T][Hv] act
+  const void* b;        // [T][Hv] act
+  const int32_t* cu;    // [N+1]
+  const int32_t* blk;   // [N]
+  const uint8_t* has_past;  // [N]
+  const void* conv_w;   // [C][K] act
+  const float* A_log;   // [Hv]
+  const float* dt_bias; // [Hv]
+  void* out;            // [T][Hv][dv] act
+  unsigned char* layer_base;  // first byte of this layer's page
+  size_t stride;        // block stride (bytes)
+  size_t rec_off;       // recurrent sub-state offset inside a block (bytes)
+  int T, N, Hk, Hv, C, K, num_blocks;
+  WorkArea work;
+};
+
+// Launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// softplus(x) = log(1 + e^x) without overflow: x + log1p(e^-x) for x > 0.
+__device__ __forceinline__ float softplus_f32(float x) {
+  return x > 0.f ? x + log1pf(__expf(-x)) : log1pf(__expf(x));
+}
+__device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + __expf(-x)); }
+__device__ __forceinline__ float silu_f32(float y) { return y / (1.f + __expf(-y)); }
+
+}  // namespace gdn

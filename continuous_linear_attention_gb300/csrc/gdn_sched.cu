@@ -1,0 +1,112 @@
+// Device-side scheduler: turns cu_seqlens / block indices into work lists
+// without a host round trip, so the whole forward stays capturable in a CUDA
+// graph (the pages note that a chunked kernel which syncs with the host keeps
+// accelerator graphs off on the varlen path; this removes that sync).
+//
+// One CTA.  It validates the batch the way the pool's contract demands (one
+// block per request, never shared, the trash block never written, cu_seqlens
+// monotonic and ending at T), raises GDN_FLAG_* bits in the layer's error word
+// and writes:
+//   items[] all active sequences, dec[] the length-1 ones, pre[] the longer
+//   ones sorted longest first (ties by sequence id), their counts and the
+//   total prefill tokens, and resets the persistent-kernel work counter.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kSchedThreads = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads)
+schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk, int N, int T,
+                int num_blocks, WorkArea work) {
+  __shared__ int s_bad;
+  __shared__ int s_n_items, s_n_dec, s_n_pre, s_pre_tokens;
+  __shared__ unsigned s_flags;
+  const int tid = threadIdx.x;
+  int32_t* hdr = work.header();
+  int32_t* blk_count = work.blk_count();
+  if (tid == 0) {
+    s_bad = (cu[0] != 0 || cu[N] != T) ? 1 : 0;
+    s_n_items = s_n_dec = s_n_pre = s_pre_tokens = 0;
+    s_flags = 0u;
+  }
+  for (int i = tid; i < num_blocks; i += kSchedThreads) blk_count[i] = 0;
+  __syncthreads();
+  for (int s = tid; s < N; s += kSchedThreads)
+    if (cu[s + 1] < cu[s]) s_bad = 1;
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_SEQLENS);
+      hdr[kNItems] = hdr[kNDec] = hdr[kNPre] = hdr[kPreTokens] = 0;
+      hdr[kWorkHead] = 0;
+    }
+    return;
+  }
+  // Count how many active sequences name each block.
+  for (int s = tid; s < N; s += kSchedThreads) {
+    const int len = cu[s + 1] - cu[s];
+    const int b = blk[s];
+    if (b < 0 || len <= 0) continue;  // padding entry or empty sequence: no-op
+    if (b >= num_blocks) {
+      atomicOr(&s_flags, GDN_FLAG_BLOCK_RANGE);
+    } else if (b == 0) {
+      atomicOr(&s_flags, GDN_FLAG_TRASH_WRITE);
+    } else {
+      atomicAdd(&blk_count[b], 1);
+    }
+  }
+  __syncthreads();
+  int32_t* items = work.items();
+  int32_t* dec = work.dec();
+  int32_t* pre_tmp = work.pre_tmp();
+  for (int s = tid; s < N; s += kSchedThreads) {
+    const int len = cu[s + 1] - cu[s];
+    const int b = blk[s];
+    if (b <= 0 || b >= num_blocks || len <= 0) continue;
+    if (atomicAdd(&blk_count[b], 0) > 1) {
+      atomicOr(&s_flags, GDN_FLAG_DUPLICATE);
+      continue;
+    }
+    items[atomicAdd(&s_n_items, 1)] = s;
+    if (len == 1) {
+      dec[atomicAdd(&s_n_dec, 1)] = s;
+    } else {
+      pre_tmp[atomicAdd(&s_n_pre, 1)] = s;
+      atomicAdd(&s_pre_tokens, len);
+    }
+  }
+  __syncthreads();
+  // Rank sort of the prefill sequences: longest first, ties by sequence id.
+  const int n_pre = s_n_pre;
+  int32_t* pre = work.pre();
+  for (int i = tid; i < n_pre; i += kSchedThreads) {
+    const int si = pre_tmp[i];
+    const int li = cu[si + 1] - cu[si];
+    int rank = 0;
+    for (int j = 0; j < n_pre; ++j) {
+      const int sj = pre_tmp[j];
+      const int lj = cu[sj + 1] - cu[sj];
+      rank += (lj > li) || (lj == li && sj < si);
+    }
+    pre[rank] = si;
+  }
+  if (tid == 0) {
+    if (s_flags) atomicOr((unsigned*)&hdr[kErr], s_flags);
+    hdr[kNItems] = s_n_items;
+    hdr[kNDec] = s_n_dec;
+    hdr[kNPre] = n_pre;
+    hdr[kPreTokens] = s_pre_tokens;
+    hdr[kWorkHead] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream) {
+  schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p.cu, p.blk, p.N, p.T, p.num_blocks, p.work);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,174 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) library for the continuous-batching
+ * forward of a gated delta net layer: a varlen causal depthwise conv1d + SiLU
+ * continued from each request's conv state, then the gated delta rule over
+ * cu_seqlens continued from each request's recurrent state, both states held
+ * in one block per request of a paged state pool.
+ *
+ * Sources of the operations (pages on continuous batching for linear attention
+ * layers, and the gated delta rule):
+ *  - "Continuous batching for linear attention layers" (PR description): a
+ *    linear attention layer keeps a fixed-size state per request (the last
+ *    inputs of its causal convolution and its recurrent state); an allocator
+ *    keeps it in one block per request for the request's whole life, read from
+ *    the zeroed trash block while the request has no past and overwritten in
+ *    place by every forward; indices hold one entry per sequence; the packed
+ *    batch runs as one row through a varlen convolution and kernels taking the
+ *    per-sequence states through cu_seqlens.  The commit that makes layers
+ *    declare their states: any number of declared states per block, each on a
+ *    128-byte boundary.
+ *  - transformers generation/continuous_batching/input_ouputs.py
+ *    (prepare_batch_tensors, get_model_kwargs): cu_seqlens are int32
+ *    cumulative query lengths [0, l0, l0+l1, ...]; graph padding repeats the
+ *    last value, i.e. adds zero-length sequences.
+ *  - Gated delta rule (Gated Delta Networks, Yang et al.):
+ *      g_t = -exp(A_log) * softplus(a_t + dt_bias), beta_t = sigmoid(b_t),
+ *      S_t = e^{g_t} S_{t-1} + beta_t (v_t - e^{g_t} S_{t-1} k_t) k_t^T,
+ *      o_t = S_t q_t, q and k L2-normalised (eps 1e-6 inside the root), q
+ *      scaled by 1/sqrt(d_k).
+ *
+ * Conventions common to every entry point:
+ *  - Every tensor pointer is DEVICE memory owned by the caller, except where
+ *    stated.  Nothing is retained after a call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and is stream-ordered: the caller must not rewrite an input until
+ *    the stream has reached the call (the engine's warmup race, where a
+ *    forward read cu_seqlens that were being rewritten, is exactly this).
+ *  - Return value: GDN_OK (0) or a negative GDN_ERR_* code; on error nothing
+ *    was launched and nothing was written.
+ *  - No entry point except gdn_get_error synchronises with the device, so
+ *    gdn_varlen_forward can be captured in a CUDA graph.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GDN_OK 0
+#define GDN_ERR_NULL (-1)        /* a required pointer is NULL */
+#define GDN_ERR_DIMS (-2)        /* dimensions inconsistent or unsupported */
+#define GDN_ERR_RANGE (-3)       /* T, N, layer, block or size out of range */
+#define GDN_ERR_ALIGN (-4)       /* a pointer or row pitch is not 16-byte aligned */
+#define GDN_ERR_CUDA (-5)        /* a CUDA runtime call failed */
+#define GDN_ERR_NOMEM (-6)       /* device allocation failed / buffer too small */
+#define GDN_ERR_DEVICE (-7)      /* called with a different current device than the pool's */
+
+/* Activation dtypes (x_qkv, a, b, conv weight, conv state, out). */
+#define GDN_F32 0
+#define GDN_BF16 1
+
+/* Bits of the device error word (see gdn_get_error).  A flagged sequence is
+ * skipped: nothing is read for it, its block and its out rows are untouched. */
+#define GDN_FLAG_SEQLENS 0x1u     /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] != T: whole batch skipped */
+#define GDN_FLAG_BLOCK_RANGE 0x2u /* block index >= num_blocks */
+#define GDN_FLAG_TRASH_WRITE 0x4u /* block index 0 (the trash block) given as a write target */
+#define GDN_FLAG_DUPLICATE 0x8u   /* two active sequences name the same block: both skipped */
+
+typedef struct gdn_pool gdn_pool_t;
+
+/* Layer weights, all device pointers.
+ *   conv_w  : [C][K] activation dtype, C = 2*Hk*d_k + Hv*d_v channels in the
+ *             order q | k | v, head-major within each part; w[c][K-1]
+ *             multiplies the current token (PyTorch depthwise conv1d taps);
+ *   A_log   : [Hv] fp32;  dt_bias : [Hv] fp32. */
+typedef struct {
+  const void* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+} gdn_weights_t;
+
+/* Byte layout of a pool with these dimensions, without allocating.
+ * Block b of layer l starts at base + (l*num_blocks + b) * block_stride.
+ * Inside a block: conv state [K-1][C] (activation dtype, oldest row first) at
+ * conv_off = 0; recurrent state [Hv][d_k][d_v] fp32 at rec_off =
+ * roundup(conv bytes, 128), element S_h[v][k] at ((h*d_k)+k)*d_v+v;
+ * block_stride = roundup(rec_off + rec bytes, max(128, block_align)).
+ * Any output pointer may be NULL.  Returns GDN_ERR_DIMS for unsupported
+ * dimensions (see gdn_state_pool_create). */
+int gdn_state_pool_layout_for(int num_blocks, int num_layers, int num_k_heads, int num_v_heads,
+                              int d_k, int d_v, int conv_k, int act_dtype, size_t block_align,
+                              size_t* block_stride, size_t* conv_off, size_t* rec_off,
+                              size_t* total_bytes);
+
+/* Create a state pool on the current CUDA device: num_layers pages of
+ * num_blocks blocks, block 0 of each page is the trash block.
+ * Supported: num_blocks >= 2, num_layers >= 1, d_k == d_v in {32, 64, 128},
+ * num_v_heads equal to num_k_heads or twice it,
+ * 2 <= conv_k <= 4, act_dtype GDN_F32 or GDN_BF16, block_align 0 (= 128) or
+ * a power of two >= 128.
+ * device_mem: NULL -> the library allocates (cudaMalloc) and frees at
+ * destroy; otherwise caller-owned device memory of device_bytes >= the
+ * layout's total_bytes, 256-byte aligned, which must outlive the pool.
+ * The whole pool memory is zeroed at creation (synchronously), so every trash
+ * block reads zeros; it is never written afterwards.  The pool also holds a
+ * small library-allocated work area (scheduler lists and error words).
+ * *out receives the handle. */
+int gdn_state_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int num_k_heads,
+                          int num_v_heads, int d_k, int d_v, int conv_k, int act_dtype,
+                          size_t block_align, void* device_mem, size_t device_bytes);
+
+/* Free the pool's library-owned memory (synchronises the device first).
+ * NULL is accepted. */
+int gdn_state_pool_destroy(gdn_pool_t* pool);
+
+/* Layout of an existing pool and its base device address (any output may be
+ * NULL).  For views and byte-exact tests. */
+int gdn_state_pool_layout(const gdn_pool_t* pool, size_t* block_stride, size_t* conv_off,
+                          size_t* rec_off, void** base);
+
+/* Copy block src to block dst of one layer (a fork: a block is copied on fork
+ * and never shared).  dst must not be 0 (the trash block).  Stream-ordered. */
+int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, void* stream);
+
+/* Forward of one gated-delta-net layer over a packed batch.
+ *   x_qkv           : [T][C] activation dtype, the packed pre-convolution q|k|v rows
+ *   a, b            : [T][Hv] activation dtype, gate and beta pre-activations
+ *   cu_seqlens      : [N+1] int32 device, cumulative starts, cu_seqlens[N] == T
+ *   state_block_idx : [N] int32 device, the block of each sequence; < 0 marks a
+ *                     padding entry (skipped: nothing read or written)
+ *   has_past        : [N] uint8 device; 0 -> the sequence starts from the trash
+ *                     block (zeros); nonzero -> from its own block
+ *   weights         : host struct of device pointers (see gdn_weights_t)
+ *   out             : [T][Hv][d_v] activation dtype; rows of skipped or
+ *                     padding sequences are not written
+ *   T, N            : host ints, T >= 0, N >= 0
+ *   max_seqlen_hint : host hint of the longest sequence (0 = unknown); only
+ *                     used to pick kernels, never trusted for indexing
+ * Each active sequence reads its conv and recurrent state from block
+ * (has_past ? idx : 0) and overwrites block idx with the new ones.
+ * Zero-length sequences are no-ops.  Bad data in the device arrays (see
+ * GDN_FLAG_*) is flagged in the layer's error word and the affected sequences
+ * are skipped.  x_qkv, a, b, out and conv_w must be 16-byte aligned.
+ * Never synchronises; graph-capturable.  Calls on the same layer must be
+ * ordered on one stream (they share the layer's scheduler work area). */
+int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const void* a,
+                       const void* b, const int32_t* cu_seqlens, const int32_t* state_block_idx,
+                       const uint8_t* has_past, const gdn_weights_t* weights, void* out, int T,
+                       int N, int max_seqlen_hint, void* stream);
+
+/* Read (and optionally clear) the OR of GDN_FLAG_* raised by earlier forwards
+ * on one layer (layer < 0: OR over all layers).  Synchronises `stream`; not
+ * for the hot path. */
+int gdn_get_error(gdn_pool_t* pool, int layer, uint32_t* flags, int reset, void* stream);
+
+/* Profiling aid: while set, every later gdn_varlen_forward on this pool
+ * records cudaEvent_t `before` on its stream right after the scheduler kernel
+ * and `after` right after the last compute kernel, so the caller can time the
+ * compute kernels alone (cudaEventElapsedTime).  NULL, NULL turns it off.
+ * The events are caller-owned; recording them does not synchronise. */
+int gdn_pool_set_timing_events(gdn_pool_t* pool, void* before, void* after);
+
+/* Static string for a status code. */
+const char* gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,81 @@
+"""The C-ABI library loads and exports every entry point its header declares;
+host-only entry points (layout, status strings, argument checks) behave as
+documented.  No GPU needed: nothing here launches work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from continuous_linear_attention_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "gdn.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = binding.load()
+    names = _declared()
+    assert "gdn_varlen_forward" in names and "gdn_state_pool_create" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(binding.EXPORTED) == names
+
+
+@pytest.mark.parametrize("dims", [
+    (512, 1, 16, 32, 128, 128, 4, "bf16", 0),
+    (8, 1, 2, 4, 32, 32, 4, "f32", 0),
+    (1024, 3, 16, 32, 128, 128, 4, "bf16", 4096),
+    (4, 2, 1, 1, 64, 64, 2, "bf16", 0),
+    (4, 2, 2, 2, 32, 32, 3, "bf16", 1 << 16),
+])
+def test_layout_matches_the_stated_layout(dims):
+    nb, nl, Hk, Hv, dk, dv, K, act, align = dims
+    stride, conv_off, rec_off, total = binding.layout_for(nb, nl, Hk, Hv, dk, dv, K, act, align)
+    spec = oracle.pool_layout(nb, nl, Hk, Hv, dk, dv, K, 4 if act == "f32" else 2, align)
+    assert (stride, conv_off, rec_off, total) == (spec["stride"], spec["conv_off"],
+                                                  spec["rec_off"], spec["total"])
+    assert rec_off % 128 == 0 and stride % 128 == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(dk=48, dv=48), dict(dk=64, dv=128), dict(Hv=3), dict(Hv=64), dict(K=1), dict(K=5),
+    dict(align=100), dict(align=64),
+])
+def test_layout_rejects_unsupported_dims(bad):
+    args = dict(nb=8, nl=1, Hk=2, Hv=4, dk=32, dv=32, K=4, act="f32", align=0)
+    args.update(bad)
+    with pytest.raises(binding.GdnError) as e:
+        binding.layout_for(args["nb"], args["nl"], args["Hk"], args["Hv"], args["dk"], args["dv"],
+                           args["K"], args["act"], args["align"])
+    assert e.value.status == -2
+
+
+def test_layout_rejects_small_pools():
+    with pytest.raises(binding.GdnError) as e:
+        binding.layout_for(1, 1, 2, 4, 32, 32, 4, "f32", 0)
+    assert e.value.status == -3
+
+
+def test_status_strings():
+    for code in range(-7, 1):
+        assert binding.status_string(code) != "unknown status"
+    assert binding.status_string(-99) == "unknown status"
+
+
+def test_null_arguments_are_rejected_without_device_work():
+    lib = binding.load()
+    assert lib.gdn_state_pool_create(None, 8, 1, 2, 4, 32, 32, 4, 0, 0, None, 0) == -1
+    w = binding.Weights(None, None, None)
+    assert lib.gdn_varlen_forward(None, 0, None, None, None, None, None, None, ctypes.byref(w),
+                                  None, 0, 0, 0, None) == -1
+    v = ctypes.c_uint32()
+    assert lib.gdn_get_error(None, 0, ctypes.byref(v), 0, None) == -1
+    assert lib.gdn_state_pool_destroy(None) == 0
+    assert lib.gdn_state_pool_layout(None, None, None, None, None) == -1

@@ -1,0 +1,266 @@
+"""GPU parity of the C-ABI forward against the fp64 oracle, and the invariants
+of continuous batching checked on the GPU path (all calls go through the C
+ABI via the ctypes binding)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from continuous_linear_attention_gb300 import binding, harness, synth
+
+from gpu_check import TOL, check_against_oracle, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _slice(wl, seqs):
+    cu = wl.cu_seqlens.tolist()
+    rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs]).astype(np.int64)
+    ncu = np.zeros(len(seqs) + 1, dtype=np.int32)
+    ncu[1:] = np.cumsum([cu[s + 1] - cu[s] for s in seqs])
+    idx = torch.from_numpy(rows)
+    return dataclasses.replace(wl, x=wl.x[idx], a=wl.a[idx], b=wl.b[idx],
+                               cu_seqlens=torch.from_numpy(ncu),
+                               block_idx=wl.block_idx[list(seqs)],
+                               has_past=wl.has_past[list(seqs)])
+
+
+# ----------------------------------------------------------------------------
+# The standard cases.
+
+def test_tiny_packed_fp32():
+    errs = check_against_oracle(synth.tiny_packed(0))
+    assert errs["out"] <= 1e-5
+
+
+def test_tiny_packed_fp32_slow_decay():
+    check_against_oracle(synth.tiny_packed(0, slow_decay=True))
+
+
+@pytest.mark.parametrize("seed", [0, 5])
+def test_tiny_dims_bf16_mixed(seed):
+    dims = dataclasses.replace(synth.TINY_DIMS, act="bf16")
+    wl = synth.make_workload("tiny_bf16", dims, [70, 1, 1, 129, 3], [1, 1, 0, 0, 1], 16, seed)
+    check_against_oracle(wl)
+
+
+@pytest.mark.parametrize("d", [64])
+def test_head_dim_64(d):
+    dims = synth.Dims(Hk=2, Hv=4, dk=d, dv=d, K=4, act="bf16")
+    wl = synth.make_workload("d64", dims, [65, 1, 130], [0, 1, 1], 8, 3)
+    check_against_oracle(wl)
+
+
+def test_equal_heads_ratio_one():
+    dims = synth.Dims(Hk=3, Hv=3, dk=32, dv=32, K=3, act="f32")
+    wl = synth.make_workload("r1", dims, [9, 1, 66], [1, 1, 0], 8, 4)
+    check_against_oracle(wl)
+
+
+def test_decode_batch_full():
+    """256 decode requests, bf16 activations, fp32 states, 512-block pool."""
+    check_against_oracle(synth.decode_batch())
+
+
+def test_prefill_full_dims_ragged():
+    """Full head dims, lengths spanning several 64-token chunks and ragged tails."""
+    wl = synth.make_workload("prefill_small", synth.FULL_DIMS, [130, 64, 257, 2, 1, 65],
+                             [0, 1, 0, 1, 1, 1], 16, 7)
+    check_against_oracle(wl)
+
+
+def test_prefill_full_size_sampled():
+    """The ~16k-token packed prefill at full size; the oracle checks the two
+    shortest sequences (a packed batch equals each sequence alone)."""
+    wl = synth.packed_prefill()
+    lens = wl.seqlens()
+    pick = sorted(range(wl.N), key=lambda s: lens[s])[:2]
+    ref = oracle.forward(_slice(wl, pick))
+    run = harness.DeviceRun(wl)
+    before = run.mem.clone()
+    run.run()
+    torch.cuda.synchronize()
+    # map the sliced oracle back onto the full batch's rows
+    cu = wl.cu_seqlens.tolist()
+    full_out = np.full((wl.T, wl.dims.Hv, wl.dims.dv), np.nan)
+    off = 0
+    for s in pick:
+        L = cu[s + 1] - cu[s]
+        full_out[cu[s]:cu[s + 1]] = ref["out"][off:off + L]
+        off += L
+    ref_full = dict(ref, out=full_out, skip=[False] * wl.N)
+    check_against_oracle(wl, run=run, seqs=pick, ref=ref_full)
+    # nothing outside the written sub-states moved
+    from gpu_check import mask_written, written_blocks
+    wb = written_blocks(wl, [False] * wl.N)
+    assert torch.equal(mask_written(before, run, wb), mask_written(run.mem, run, wb))
+
+
+def test_mixed_batch_full():
+    """64 decodes + 6 prefill continuations with past, 8192 tokens, 1024 blocks."""
+    check_against_oracle(synth.mixed_batch())
+
+
+def test_long_context_split_equals_single_pass():
+    """4 x 32768 tokens then a 4096-token continuation from the saved states
+    equals one 36864-token pass; the oracle checks a prefix of sequence 0."""
+    first, cont, whole = synth.long_context()
+    # split run
+    run = harness.DeviceRun(first)
+    run.run()
+    run.set_inputs(cont)
+    run.run()
+    torch.cuda.synchronize()
+    assert run.pool.error_flags() == 0
+    out_cont = run.out.float().cpu()
+    # first part's out again (set_inputs replaced it): rerun on a fresh pool
+    run1 = harness.DeviceRun(first)
+    run1.run()
+    torch.cuda.synchronize()
+    out_first = run1.out.float().cpu()
+    # single pass
+    single = harness.DeviceRun(whole)
+    single.run()
+    torch.cuda.synchronize()
+    n, L1, L2 = 4, 32768, 4096
+    d = whole.dims
+    out_single = single.out.float().cpu().view(n, L1 + L2, d.Hv, d.dv)
+    split = torch.cat([out_first.view(n, L1, d.Hv, d.dv), out_cont.view(n, L2, d.Hv, d.dv)], 1)
+    assert rel_l2(split.numpy(), out_single.numpy()) <= TOL["bf16"]
+    for s in range(n):
+        blk = int(whole.block_idx[s])
+        assert rel_l2(run.rec_view(blk).cpu().numpy(), single.rec_view(blk).cpu().numpy()) <= 1e-3
+        assert torch.equal(run.conv_view(blk).cpu(), single.conv_view(blk).cpu())
+    # oracle on the first 2048 tokens of sequence 0
+    pre = dataclasses.replace(_slice(first, [0]), x=first.x[:2048], a=first.a[:2048],
+                              b=first.b[:2048], cu_seqlens=torch.tensor([0, 2048], dtype=torch.int32))
+    ref = oracle.forward(pre)
+    assert rel_l2(out_first[:2048].numpy(), ref["out"]) <= TOL["bf16"]
+
+
+# ----------------------------------------------------------------------------
+# Edge cases of the batch description.
+
+def test_padding_and_empty_sequences():
+    dims = synth.TINY_DIMS
+    wl = synth.make_workload("pad", dims, [4, 0, 1, 0, 7, 2], [1, 0, 1, 1, 0, 0], 12, 8,
+                             block_idx=[3, 5, -1, -1, 6, 9])
+    check_against_oracle(wl)
+
+
+def test_zero_tokens():
+    dims = synth.TINY_DIMS
+    wl = synth.make_workload("empty", dims, [0, 0], [0, 0], 4, 9, block_idx=[1, 2])
+    check_against_oracle(wl)
+
+
+@pytest.mark.parametrize("blocks,flag", [
+    ([2, 2, 5], binding.FLAG_DUPLICATE),
+    ([0, 3, 5], binding.FLAG_TRASH_WRITE),
+    ([2, 3, 99], binding.FLAG_BLOCK_RANGE),
+])
+def test_bad_block_indices_are_flagged_and_skipped(blocks, flag):
+    dims = synth.TINY_DIMS
+    wl = synth.make_workload("bad", dims, [3, 1, 4], [1, 1, 0], 8, 10, block_idx=blocks)
+    check_against_oracle(wl, expect_flags=flag)
+
+
+def test_bad_cu_seqlens_skip_everything():
+    dims = synth.TINY_DIMS
+    wl = synth.make_workload("badcu", dims, [3, 1, 4], [1, 1, 0], 8, 11)
+    wl = dataclasses.replace(wl, cu_seqlens=torch.tensor([0, 3, 2, 8], dtype=torch.int32))
+    run = harness.DeviceRun(wl)
+    before = run.mem.clone()
+    run.run()
+    torch.cuda.synchronize()
+    assert run.pool.error_flags() == binding.FLAG_SEQLENS
+    assert torch.equal(before, run.mem)
+    assert (run.out.float() == harness.OUT_SENTINEL).all()
+
+
+def test_host_argument_errors_launch_nothing():
+    wl = synth.tiny_packed(0)
+    run = harness.DeviceRun(wl)
+    with pytest.raises(binding.GdnError):
+        binding.varlen_forward(run.pool, 1, run.x, run.a, run.b, run.cu, run.idx, run.has_past,
+                               run.conv_w, run.A_log, run.dt_bias, run.out, wl.T, wl.N)
+    with pytest.raises(binding.GdnError):
+        binding.varlen_forward(run.pool, 0, run.x.data_ptr() + 4, run.a, run.b, run.cu, run.idx,
+                               run.has_past, run.conv_w, run.A_log, run.dt_bias, run.out, wl.T,
+                               wl.N)
+    torch.cuda.synchronize()
+    assert (run.out.float() == harness.OUT_SENTINEL).all()
+
+
+# ----------------------------------------------------------------------------
+# Invariants on the GPU path.
+
+def test_packed_equals_each_alone_gpu():
+    dims = dataclasses.replace(synth.FULL_DIMS)
+    wl = synth.make_workload("pack", dims, [70, 1, 129, 1, 3], [0, 1, 1, 1, 0], 8, 12)
+    run = harness.DeviceRun(wl)
+    run.run()
+    torch.cuda.synchronize()
+    cu = wl.cu_seqlens.tolist()
+    for s in range(wl.N):
+        one = harness.DeviceRun(_slice(wl, [s]))
+        one.run()
+        torch.cuda.synchronize()
+        assert torch.equal(one.out, run.out[cu[s]:cu[s + 1]])
+        blk = int(wl.block_idx[s])
+        assert torch.equal(one.rec_view(blk), run.rec_view(blk))
+        assert torch.equal(one.conv_view(blk), run.conv_view(blk))
+
+
+def test_beta_zero_only_decays_gpu():
+    wl = synth.make_workload("beta0", synth.FULL_DIMS, [5, 1, 66], [1, 1, 1], 8, 13)
+    wl = dataclasses.replace(wl, b=torch.full_like(wl.b, -1000.0))
+    check_against_oracle(wl)
+
+
+def test_graph_capture_replays_the_same_result():
+    wl = synth.make_workload("graph", synth.FULL_DIMS, [1, 1, 200, 1, 67], [1, 1, 1, 1, 0], 16, 14)
+    eager = harness.DeviceRun(wl)
+    eager.run()
+    torch.cuda.synchronize()
+    graphed = harness.DeviceRun(wl)
+    snapshot = graphed.mem.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graphed.run(stream=s)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graphed.mem.copy_(snapshot)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        graphed.run()
+    graphed.mem.copy_(snapshot)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(graphed.out, eager.out)
+    assert torch.equal(graphed.mem, eager.mem)
+
+
+def test_inputs_rewritten_after_stream_order_are_safe():
+    """Batch buffers reused across calls on one stream (the warmup race: a
+    forward must see the inputs as they were when it was enqueued)."""
+    wls = [synth.make_workload(f"r{i}", synth.TINY_DIMS, [3, 1, 6], [0, 1, 0], 8, 20 + i,
+                               block_idx=[1, 2, 3]) for i in range(3)]
+    run = harness.DeviceRun(wls[0])
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for wl in wls:
+            run.x.copy_(wl.x.to(run.device, non_blocking=False))
+            run.run(stream=s)
+            outs.append(run.out.clone())
+    torch.cuda.synchronize()
+    ref = harness.DeviceRun(wls[0])
+    for i, wl in enumerate(wls):
+        ref.x.copy_(wl.x.cuda())
+        ref.run()
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref.out)
