@@ -92,6 +92,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.05)
+
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -190,8 +195,11 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--requests", type=int, default=256,
+                    help="decode requests per GPU (256 is the standard batch; smaller "
+                         "batches are for profiler captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -215,13 +223,16 @@ def main():
     __graft_entry__.build()
     from continuous_linear_attention_gb300 import harness, synth
 
-    wl = synth.decode_batch(seed=1 + rank)
+    wl = synth.decode_batch(seed=1 + rank, n_req=args.requests,
+                            num_blocks=max(512, 2 * args.requests))
     run = harness.DeviceRun(wl, device=f"cuda:{local_rank}")
     stream = torch.cuda.current_stream()
 
     # warm-up
+    # every request of this batch has one new token: the decode fast path
+    hint = 1
     for _ in range(args.warmup):
-        run.run(stream)
+        run.run(stream, max_seqlen_hint=hint)
     torch.cuda.synchronize()
 
     # per-step events around the compute kernels (inside the C-ABI call)
@@ -236,10 +247,11 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        clk.wait_first()
         start.record(stream)
         for i in range(args.steps):
             run.pool.set_timing_events(kb[i], ka[i])
-            run.run(stream)
+            run.run(stream, max_seqlen_hint=hint)
         stop.record(stream)
         torch.cuda.synchronize()
     run.pool.set_timing_events(None, None)
@@ -258,7 +270,7 @@ def main():
     for _ in range(args.warmup):
         for k, t in host_in.items():
             getattr(run, k).copy_(t, non_blocking=True)
-        run.run(stream)
+        run.run(stream, max_seqlen_hint=hint)
         host_out.copy_(run.out, non_blocking=True)
     torch.cuda.synchronize()
     if world > 1:
@@ -268,7 +280,7 @@ def main():
     for _ in range(args.steps):
         for k, t in host_in.items():
             getattr(run, k).copy_(t, non_blocking=True)
-        run.run(stream)
+        run.run(stream, max_seqlen_hint=hint)
         host_out.copy_(run.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -301,7 +313,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                          "traffic": traffic, "peak_source": pk["source"],
-                         "kernel": "compute kernels of gdn_varlen_forward (decode)",
+                         "kernel": "decode_kernel (the only compute kernel of a decode batch)",
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "kernel_ms_mean": kern_mean_ms},
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",

@@ -22,6 +22,8 @@ FLAG_SEQLENS = 0x1
 FLAG_BLOCK_RANGE = 0x2
 FLAG_TRASH_WRITE = 0x4
 FLAG_DUPLICATE = 0x8
+FLAG_TIMEOUT = 0x10
+FLAG_HINT = 0x20
 
 EXPORTED = [
     "gdn_state_pool_layout_for",

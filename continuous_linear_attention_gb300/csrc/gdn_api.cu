@@ -195,9 +195,9 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
                        const int32_t* cu_seqlens, const int32_t* state_block_idx,
                        const uint8_t* has_past, const gdn_weights_t* w, void* out, int T, int N,
                        int max_seqlen_hint, void* stream) {
-  (void)max_seqlen_hint;
   if (!p || !w) return GDN_ERR_NULL;
-  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0) return GDN_ERR_RANGE;
+  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
+    return GDN_ERR_RANGE;
   if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
   if (!cu_seqlens || !state_block_idx || !has_past || !w->conv_w || !w->A_log || !w->dt_bias)
     return GDN_ERR_NULL;
@@ -235,6 +235,7 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
   fp.C = C;
   fp.K = p->K;
   fp.num_blocks = p->num_blocks;
+  fp.max_seqlen_hint = max_seqlen_hint;
   fp.work.base = p->work + (size_t)layer * gdn::WorkArea::words(p->num_blocks);
   fp.work.num_blocks = p->num_blocks;
 
@@ -249,7 +250,18 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
   int max_items = N;
   if (max_items > p->num_blocks - 1) max_items = p->num_blocks - 1;
   if (max_items > T) max_items = T;
-  if (gdn::launch_recurrent(fp, p->dk, p->act, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (gdn::decode_supported(p->dk, p->act, p->Hk, p->Hv, p->K)) {
+    // length-1 sequences: persistent HBM-streaming decode kernel; longer ones
+    // (at most T/2 of them): token-serial kernel
+    if (gdn::launch_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+    int max_long = max_items < T / 2 ? max_items : T / 2;
+    if (max_seqlen_hint == 1) max_long = 0;  // longer sequences are flagged, never listed
+    if (gdn::launch_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess)
+      return GDN_ERR_CUDA;
+  } else {
+    if (gdn::launch_recurrent(fp, p->dk, p->act, max_items, false, s) != cudaSuccess)
+      return GDN_ERR_CUDA;
+  }
   if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;
 }

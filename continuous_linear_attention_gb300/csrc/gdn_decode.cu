@@ -1,0 +1,316 @@
+// Decode kernel: one new token per request (the engine's decode fast path,
+// "Continuous batching for linear attention layers").  The step is bound by
+// HBM: every v-head's d_k x d_v fp32 state (64 KiB at d = 128) is read once
+// and written once, which is ~97% of the bytes of the call.
+//
+// Design (GB300): a persistent grid of one CTA per SM, warp-specialised.
+//  - Work units are (request, k-head group).  A unit owns the q/k conv
+//    channels of its k-head and the v channels and states of its v-heads, so
+//    reading the old conv/recurrent state and overwriting it in place needs no
+//    cross-CTA ordering.  Units are dealt round-robin over the CTAs.
+//  - One producer warp streams, kStages heads ahead, each v-head's state
+//    (64 KiB) into a ring of shared-memory buffers with bulk (TMA) copies, and
+//    with the first head of a unit also that unit's conv inputs (its x row,
+//    conv-state rows, conv taps, gate rows).  It resolves the request's block
+//    indices itself, so the compute warps never wait on a global load.
+//  - Eight compute warps read a state buffer once into registers (releasing
+//    it to the producer at once), reduce S k and S q across warps, and write
+//    the new state straight from registers to HBM with 16-byte stores.
+//
+// Per token (v-head h, k-head h / (Hv/Hk)), as in the gated delta rule:
+//   y = SiLU(conv over [conv state ; x]),  q, k L2-normalised, q /= sqrt(d_k)
+//   g = -exp(A_log) softplus(a + dt_bias),  beta = sigmoid(b)
+//   p = S k, r = S q,  u = beta (v - e^g p),  o = e^g r + (k.q) u,
+//   S <- e^g S + u k^T.
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int D = 128;                 // d_k = d_v
+constexpr int KC = 4;                  // conv taps
+constexpr int kConsumers = 256;        // 8 compute warps
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 3;
+constexpr int kCV = D / 4;             // float4 columns of a state row
+constexpr int kG = kConsumers / kCV;   // row groups (8)
+constexpr int kRows = D / kG;          // rows per thread (16)
+constexpr uint32_t kHeadBytes = D * D * sizeof(float);
+constexpr int R = 2;                   // v-heads per k-head
+constexpr int kUnitCh = (2 + R) * D;   // conv channels of a unit (512)
+constexpr int kMaxHv = 64;
+
+// Conv inputs of one unit, bf16, channel order q | k | v of the unit.
+struct ConvIn {
+  __nv_bfloat16 x[kUnitCh];
+  __nv_bfloat16 tail[KC - 1][kUnitCh];
+  __nv_bfloat16 w[kUnitCh][KC];
+  __nv_bfloat16 a[kMaxHv];
+  __nv_bfloat16 b[kMaxHv];
+};
+
+struct Meta {
+  int row;   // packed row of the token
+  int wblk;  // block written
+  int pad0, pad1;
+};
+
+struct DecodeSmem {
+  float buf[kStages][D * D];  // state ring
+  ConvIn cin[2];              // conv inputs, double-buffered by unit
+  float part[2][kG][D];       // partial S k and S q
+  float y[kUnitCh];           // conv + SiLU outputs of the unit
+  float u[D];
+  float red[4];
+  float gate[R][2];           // e^g, beta
+  Meta meta[kStages];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t cempty[2];
+  int ok;
+};
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int Hk = p.Hk, Hv = p.Hv, C = p.C;
+  const int n_units = p.work.header()[kNDec] * Hk;
+  const int my_units = n_units > (int)blockIdx.x
+                           ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int n_stages = my_units * R;
+  if (n_stages == 0) return;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kConsumers / 32);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&sm.cempty[i], kConsumers / 32);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (tid >= kConsumers) {
+    // ======================= producer warp =======================
+    if (tid != kConsumers) return;
+    const int* dec = p.work.dec();
+    for (int n = 0; n < n_stages; ++n) {
+      const int st = n % kStages;
+      if (n >= kStages && !mbar_wait_bounded(&sm.empty[st], ((n / kStages) - 1) & 1)) {
+        atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+        return;
+      }
+      const int k = n / R, jh = n % R;
+      const int unit = blockIdx.x + k * gridDim.x;
+      const int s = dec[unit / Hk];
+      const int kh = unit % Hk;
+      const int h = kh * R + jh;
+      const int row = p.cu[s];
+      const int wblk = p.blk[s];
+      const int rblk = p.has_past[s] ? wblk : 0;
+      sm.meta[st].row = row;
+      sm.meta[st].wblk = wblk;
+      const unsigned char* rbase = p.layer_base + (size_t)rblk * p.stride;
+      const float* src = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * D * D;
+      uint32_t bytes = kHeadBytes;
+      ConvIn* ci = nullptr;
+      if (jh == 0) {
+        const int cb = k & 1;
+        if (k >= 2 && !mbar_wait_bounded(&sm.cempty[cb], ((k >> 1) - 1) & 1)) {
+          atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+          return;
+        }
+        ci = &sm.cin[cb];
+        bytes += (uint32_t)(KC * kUnitCh * 2 + kUnitCh * KC * 2 + 2 * Hv * 2);
+      }
+      mbar_arrive_expect_tx(&sm.full[st], bytes);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        bulk_g2s(sm.buf[st] + c * (D * D / 4), src + c * (D * D / 4), kHeadBytes / 4,
+                 &sm.full[st]);
+      if (ci) {
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x) + (size_t)row * C;
+        const __nv_bfloat16* tail = reinterpret_cast<const __nv_bfloat16*>(rbase);
+        const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
+        const int cq = kh * D, ck = Hk * D + kh * D, cv = 2 * Hk * D + kh * R * D;
+        bulk_g2s(ci->x, x + cq, D * 2, &sm.full[st]);
+        bulk_g2s(ci->x + D, x + ck, D * 2, &sm.full[st]);
+        bulk_g2s(ci->x + 2 * D, x + cv, R * D * 2, &sm.full[st]);
+        for (int j = 0; j < KC - 1; ++j) {
+          bulk_g2s(ci->tail[j], tail + (size_t)j * C + cq, D * 2, &sm.full[st]);
+          bulk_g2s(ci->tail[j] + D, tail + (size_t)j * C + ck, D * 2, &sm.full[st]);
+          bulk_g2s(ci->tail[j] + 2 * D, tail + (size_t)j * C + cv, R * D * 2, &sm.full[st]);
+        }
+        bulk_g2s(ci->w[0], w + (size_t)cq * KC, D * KC * 2, &sm.full[st]);
+        bulk_g2s(ci->w[D], w + (size_t)ck * KC, D * KC * 2, &sm.full[st]);
+        bulk_g2s(ci->w[2 * D], w + (size_t)cv * KC, R * D * KC * 2, &sm.full[st]);
+        bulk_g2s(ci->a, reinterpret_cast<const __nv_bfloat16*>(p.a) + (size_t)row * Hv, Hv * 2,
+                 &sm.full[st]);
+        bulk_g2s(ci->b, reinterpret_cast<const __nv_bfloat16*>(p.b) + (size_t)row * Hv, Hv * 2,
+                 &sm.full[st]);
+      }
+    }
+    return;
+  }
+
+  // ======================= compute warps =======================
+  __nv_bfloat16* __restrict__ out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  const float inv_sqrt_d = rsqrtf((float)D);
+  const int cv = tid % kCV;
+  const int rg = tid / kCV;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  for (int n = 0; n < n_stages; ++n) {
+    const int st = n % kStages;
+    const int k = n / R, jh = n % R;
+    const int unit = blockIdx.x + k * gridDim.x;
+    const int kh = unit % Hk;
+    const int h = kh * R + jh;
+
+    if (tid == 0) sm.ok = mbar_wait_bounded(&sm.full[st], (n / kStages) & 1) ? 1 : 0;
+    consumer_sync();
+    if (!sm.ok) {
+      if (tid == 0) {
+        atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+        for (int m = n + 1; m < n_stages && m < n + kStages; ++m)
+          mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1);
+      }
+      return;
+    }
+    const int row = sm.meta[st].row;
+    const int wblk = sm.meta[st].wblk;
+    unsigned char* wbase = p.layer_base + (size_t)wblk * p.stride;
+
+    if (jh == 0) {
+      // ---- conv + SiLU of the unit's channels; new conv state; gates
+      const ConvIn& ci = sm.cin[k & 1];
+      __nv_bfloat16* tail_w = reinterpret_cast<__nv_bfloat16*>(wbase);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int lc = tid + c * kConsumers;
+        const float xv = __bfloat162float(ci.x[lc]);
+        float acc = __bfloat162float(ci.w[lc][KC - 1]) * xv;
+#pragma unroll
+        for (int j = 0; j < KC - 1; ++j)
+          acc += __bfloat162float(ci.w[lc][j]) * __bfloat162float(ci.tail[j][lc]);
+        sm.y[lc] = silu_f32(acc);
+        const int ch = lc < D ? kh * D + lc
+                              : (lc < 2 * D ? Hk * D + kh * D + (lc - D)
+                                            : 2 * Hk * D + kh * R * D + (lc - 2 * D));
+        // new conv state: the last K-1 inputs of [old state ; x]
+#pragma unroll
+        for (int j = 0; j < KC - 2; ++j) tail_w[(size_t)j * C + ch] = ci.tail[j + 1][lc];
+        tail_w[(size_t)(KC - 2) * C + ch] = ci.x[lc];
+      }
+      if (tid < R) {
+        const int hh = kh * R + tid;
+        const float araw = __bfloat162float(ci.a[hh]) + p.dt_bias[hh];
+        const float g = -__expf(p.A_log[hh]) * softplus_f32(araw);
+        sm.gate[tid][0] = __expf(g);
+        sm.gate[tid][1] = sigmoid_f32(__bfloat162float(ci.b[hh]));
+      }
+      consumer_sync();
+      if (lane == 0) mbar_arrive(&sm.cempty[k & 1]);
+      if (tid < 96) {
+        float acc = 0.f;
+        for (int i = lane; i < D; i += 32) {
+          const float qv = sm.y[i], kv = sm.y[D + i];
+          acc += warp == 0 ? qv * qv : (warp == 1 ? kv * kv : qv * kv);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) sm.red[warp] = acc;
+      }
+      consumer_sync();
+    }
+    const float qs = rsqrtf(sm.red[0] + kL2Eps) * inv_sqrt_d;
+    const float ks = rsqrtf(sm.red[1] + kL2Eps);
+    const float decay = sm.gate[jh][0];
+    const float beta = sm.gate[jh][1];
+    const float* buf = sm.buf[st];
+
+    // ---- pass 1: state rows into registers, partial S k and S q
+    float4 S[kRows];
+    float kr[kRows];
+    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const int r = rg + kG * i;
+      S[i] = *reinterpret_cast<const float4*>(buf + r * D + 4 * cv);
+      kr[i] = sm.y[D + r] * ks;
+      const float qr = sm.y[r] * qs;
+      pk.x += S[i].x * kr[i]; pk.y += S[i].y * kr[i]; pk.z += S[i].z * kr[i]; pk.w += S[i].w * kr[i];
+      pq.x += S[i].x * qr; pq.y += S[i].y * qr; pq.z += S[i].z * qr; pq.w += S[i].w * qr;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[st]);  // this warp is done with the buffer
+    *reinterpret_cast<float4*>(&sm.part[0][rg][4 * cv]) = pk;
+    *reinterpret_cast<float4*>(&sm.part[1][rg][4 * cv]) = pq;
+    consumer_sync();
+    if (tid < D) {
+      float sk = 0.f, sq = 0.f;
+#pragma unroll
+      for (int g2 = 0; g2 < kG; ++g2) {
+        sk += sm.part[0][g2][tid];
+        sq += sm.part[1][g2][tid];
+      }
+      const float vv = sm.y[2 * D + jh * D + tid];
+      const float u = beta * (vv - decay * sk);
+      sm.u[tid] = u;
+      out[((size_t)row * Hv + h) * D + tid] =
+          __float2bfloat16_rn(decay * sq + sm.red[2] * qs * ks * u);
+    }
+    consumer_sync();
+    // ---- pass 2: S <- e^g S + u k^T from registers, straight to the write block
+    float* S_w = reinterpret_cast<float*>(wbase + p.rec_off) + (size_t)h * D * D;
+    const float4 u4 = *reinterpret_cast<const float4*>(&sm.u[4 * cv]);
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const int r = rg + kG * i;
+      float4 s4 = S[i];
+      s4.x = decay * s4.x + u4.x * kr[i];
+      s4.y = decay * s4.y + u4.y * kr[i];
+      s4.z = decay * s4.z + u4.z * kr[i];
+      s4.w = decay * s4.w + u4.w * kr[i];
+      *reinterpret_cast<float4*>(S_w + (size_t)r * D + 4 * cv) = s4;
+    }
+  }
+}
+
+int g_num_sms = 0;
+
+}  // namespace
+
+bool decode_supported(int d, int act, int Hk, int Hv, int K) {
+  return d == D && act == GDN_BF16 && Hv == R * Hk && K == KC && Hv % 8 == 0 && Hv <= kMaxHv;
+}
+
+cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {
+  if (max_dec <= 0) return cudaSuccess;
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 1;
+  }
+  const long long max_units = (long long)max_dec * p.Hk;
+  const int grid = (int)(max_units < g_num_sms ? max_units : g_num_sms);
+  const size_t smem = sizeof(DecodeSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -60,12 +60,20 @@ struct FwdParams {
   size_t stride;        // block stride (bytes)
   size_t rec_off;       // recurrent sub-state offset inside a block (bytes)
   int T, N, Hk, Hv, C, K, num_blocks;
+  int max_seqlen_hint;  // 0 = unknown; else longer sequences are flagged and skipped
   WorkArea work;
 };
 
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
-cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, cudaStream_t stream);
+// The token-serial kernel runs over all active sequences (long_only = false)
+// or only over those longer than one token (long_only = true).
+cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, bool long_only,
+                             cudaStream_t stream);
+// The persistent decode kernel (length-1 sequences): d_k = d_v = 128, bf16
+// activations, Hv = 2 Hk, K = 4.
+bool decode_supported(int d, int act, int Hk, int Hv, int K);
+cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

@@ -30,16 +30,16 @@ constexpr int kHeadThreads = 256;  // threads per v-head
 
 template <int D, typename Act>
 __global__ void __launch_bounds__(2 * kHeadThreads)
-recurrent_kernel(FwdParams p) {
+recurrent_kernel(FwdParams p, bool long_only) {
   constexpr int CV = D / 4;                 // float4 columns per state row
   constexpr int G = kHeadThreads / CV;      // row groups
   constexpr int NJ = D / G;                 // rows per thread
   static_assert(NJ * G == D, "row split");
   const int R = p.Hv / p.Hk;                // v-heads per k-head (1 or 2)
   const WorkArea& wk = p.work;
-  const int n_items = wk.header()[kNItems];
+  const int n_items = wk.header()[long_only ? kNPre : kNItems];
   if ((int)blockIdx.x >= n_items) return;
-  const int s = wk.items()[blockIdx.x];
+  const int s = (long_only ? wk.pre() : wk.items())[blockIdx.x];
   const int kh = blockIdx.y;
   const int t0 = p.cu[s];
   const int L = p.cu[s + 1] - t0;
@@ -203,28 +203,28 @@ recurrent_kernel(FwdParams p) {
 }
 
 template <int D, typename Act>
-cudaError_t launch_rec(const FwdParams& p, int max_items, cudaStream_t stream) {
+cudaError_t launch_rec(const FwdParams& p, int max_items, bool long_only, cudaStream_t stream) {
   const int R = p.Hv / p.Hk;
   constexpr int G = kHeadThreads / (D / 4);
   const size_t smem = sizeof(float) * (4 * D + 2 * 2 * G * D + 2 * D + 4 + 4);
   dim3 grid(max_items, p.Hk);
-  recurrent_kernel<D, Act><<<grid, R * kHeadThreads, smem, stream>>>(p);
+  recurrent_kernel<D, Act><<<grid, R * kHeadThreads, smem, stream>>>(p, long_only);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items,
+cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, bool long_only,
                              cudaStream_t stream) {
   if (max_items <= 0) return cudaSuccess;
   if (act == GDN_F32) {
-    if (d == 32) return launch_rec<32, float>(p, max_items, stream);
-    if (d == 64) return launch_rec<64, float>(p, max_items, stream);
-    return launch_rec<128, float>(p, max_items, stream);
+    if (d == 32) return launch_rec<32, float>(p, max_items, long_only, stream);
+    if (d == 64) return launch_rec<64, float>(p, max_items, long_only, stream);
+    return launch_rec<128, float>(p, max_items, long_only, stream);
   }
-  if (d == 32) return launch_rec<32, __nv_bfloat16>(p, max_items, stream);
-  if (d == 64) return launch_rec<64, __nv_bfloat16>(p, max_items, stream);
-  return launch_rec<128, __nv_bfloat16>(p, max_items, stream);
+  if (d == 32) return launch_rec<32, __nv_bfloat16>(p, max_items, long_only, stream);
+  if (d == 64) return launch_rec<64, __nv_bfloat16>(p, max_items, long_only, stream);
+  return launch_rec<128, __nv_bfloat16>(p, max_items, long_only, stream);
 }
 
 }  // namespace gdn

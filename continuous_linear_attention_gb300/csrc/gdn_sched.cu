@@ -19,7 +19,7 @@ constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
 schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk, int N, int T,
-                int num_blocks, WorkArea work) {
+                int num_blocks, int hint, WorkArea work) {
   __shared__ int s_bad;
   __shared__ int s_n_items, s_n_dec, s_n_pre, s_pre_tokens;
   __shared__ unsigned s_flags;
@@ -69,6 +69,10 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
       atomicOr(&s_flags, GDN_FLAG_DUPLICATE);
       continue;
     }
+    if (hint > 0 && len > hint) {
+      atomicOr(&s_flags, GDN_FLAG_HINT);
+      continue;
+    }
     items[atomicAdd(&s_n_items, 1)] = s;
     if (len == 1) {
       dec[atomicAdd(&s_n_dec, 1)] = s;
@@ -105,7 +109,8 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
 }  // namespace
 
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream) {
-  schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p.cu, p.blk, p.N, p.T, p.num_blocks, p.work);
+  schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p.cu, p.blk, p.N, p.T, p.num_blocks,
+                                                   p.max_seqlen_hint, p.work);
   return cudaGetLastError();
 }
 

@@ -69,6 +69,8 @@ extern "C" {
 #define GDN_FLAG_BLOCK_RANGE 0x2u /* block index >= num_blocks */
 #define GDN_FLAG_TRASH_WRITE 0x4u /* block index 0 (the trash block) given as a write target */
 #define GDN_FLAG_DUPLICATE 0x8u   /* two active sequences name the same block: both skipped */
+#define GDN_FLAG_TIMEOUT 0x10u    /* a kernel's bounded wait gave up (its results are incomplete) */
+#define GDN_FLAG_HINT 0x20u       /* a sequence is longer than max_seqlen_hint: it was skipped */
 
 typedef struct gdn_pool gdn_pool_t;
 
@@ -138,8 +140,10 @@ int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, voi
  *   out             : [T][Hv][d_v] activation dtype; rows of skipped or
  *                     padding sequences are not written
  *   T, N            : host ints, T >= 0, N >= 0
- *   max_seqlen_hint : host hint of the longest sequence (0 = unknown); only
- *                     used to pick kernels, never trusted for indexing
+ *   max_seqlen_hint : host bound on the sequence lengths (0 = unknown).  With 1
+ *                     (a pure decode batch) only the decode path is launched.
+ *                     Never trusted: an active sequence longer than a nonzero
+ *                     hint is skipped and GDN_FLAG_HINT raised
  * Each active sequence reads its conv and recurrent state from block
  * (has_past ? idx : 0) and overwrites block idx with the new ones.
  * Zero-length sequences are no-ops.  Bad data in the device arrays (see

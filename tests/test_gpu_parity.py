@@ -167,6 +167,26 @@ def test_bad_block_indices_are_flagged_and_skipped(blocks, flag):
     check_against_oracle(wl, expect_flags=flag)
 
 
+def test_decode_hint_skips_and_flags_longer_sequences():
+    """max_seqlen_hint = 1 launches only the decode path; a longer sequence is
+    skipped (block and out rows untouched) and flagged, the others match."""
+    wl = synth.make_workload("hint", synth.FULL_DIMS, [1, 5, 1, 1], [1, 1, 0, 1], 8, 15)
+    run = harness.DeviceRun(wl)
+    before = run.mem.clone()
+    run.run(max_seqlen_hint=1)
+    torch.cuda.synchronize()
+    assert run.pool.error_flags() == binding.FLAG_HINT
+    blk = int(wl.block_idx[1])
+    assert torch.equal(run.rec_view(blk), before[run.block_offset(blk) + run.rec_off:][
+        :run.rec_bytes].view(torch.float32).view(run.rec_view(blk).shape))
+    assert (run.out[1:6].float() == harness.OUT_SENTINEL).all()
+    keep = [0, 2, 3]
+    ref = oracle.forward(_slice(wl, keep))
+    cu = wl.cu_seqlens.tolist()
+    got = torch.cat([run.out[cu[s]:cu[s + 1]] for s in keep]).double().cpu().numpy()
+    assert rel_l2(got, ref["out"]) <= TOL["bf16"]
+
+
 def test_bad_cu_seqlens_skip_everything():
     dims = synth.TINY_DIMS
     wl = synth.make_workload("badcu", dims, [3, 1, 4], [1, 1, 0], 8, 11)
