@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
                                        I, I, I, P]
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
+    lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, P]
+    lib.gdn_diag_umma_gemm.restype = I
     lib.gdn_status_string.argtypes = [I]
     lib.gdn_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -187,3 +189,11 @@ def varlen_forward(pool: Pool, layer: int, x_qkv, a, b, cu_seqlens, state_block_
                                      _ptr(cu_seqlens), _ptr(state_block_idx), _ptr(has_past),
                                      ctypes.byref(w), _ptr(out), T, N, max_seqlen_hint,
                                      _stream(stream)), "gdn_varlen_forward")
+
+
+def diag_umma_gemm(A, B, C, D, stream=None) -> None:
+    """gdn_diag_umma_gemm: D = (C or 0) + A @ B^T on the tensor cores
+    (A [128][K], B [N][K] bf16; C, D [128][N] fp32; device tensors)."""
+    N, K = B.shape
+    _check(load().gdn_diag_umma_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K, _stream(stream)),
+           "gdn_diag_umma_gemm")

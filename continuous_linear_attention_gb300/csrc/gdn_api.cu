@@ -256,8 +256,11 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
     if (gdn::launch_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
     int max_long = max_items < T / 2 ? max_items : T / 2;
     if (max_seqlen_hint == 1) max_long = 0;  // longer sequences are flagged, never listed
-    if (gdn::launch_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess)
+    if (gdn::chunk_supported(p->dk, p->act, p->K)) {
+      if (gdn::launch_chunk(fp, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;
+    } else if (gdn::launch_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess) {
       return GDN_ERR_CUDA;
+    }
   } else {
     if (gdn::launch_recurrent(fp, p->dk, p->act, max_items, false, s) != cudaSuccess)
       return GDN_ERR_CUDA;

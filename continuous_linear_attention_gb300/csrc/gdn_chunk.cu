@@ -1,0 +1,500 @@
+// Chunked prefill kernel: the gated delta rule over sequences longer than one
+// token, in chunks of C = 64 tokens with the WY / UT-transform form, the dense
+// intra-chunk and state products on the 5th-generation tensor cores
+// (tcgen05.mma, bf16 operands from 128-byte-swizzled shared tiles, fp32
+// accumulators in tensor memory).  The recurrent state stays in tensor memory
+// (fp32) for the whole sequence; only the final state is written back.
+//
+// One CTA (4 warps) per (sequence, v-head) chain, longest sequences first.
+// Per chunk, with G_i the inclusive cumulative gate inside the chunk, beta_i
+// the write strength, q~/k~ the normalised rows and S0 the state at the chunk
+// start (S is d_v x d_k, S[v][k]):
+//   prep (CUDA cores): conv + SiLU + L2 norms + gates; bf16 tiles
+//        [q~ ; k~], [q~ e^G ; k~ beta e^G], (k~ e^{G_C - G})^T, fp32 beta v
+//   state hand-over: S0 -> bf16 tile; TMEM S <- e^{G_C} S0
+//   MMA  X  = [q~ ; k~] k~^T                     (QK^T and KK^T, 128 x 64)
+//   MMA  [Oacc | Y] = S0 [q~ e^G ; k~ beta e^G]^T (128 x 128)
+//   CUDA A_ij = beta_i e^{G_i-G_j} (k~_i.k~_j) (j<i);  P_ij = (q~_i.k~_j) e^{G_i-G_j} (j<=i)
+//        R^T = (beta v)^T - Y;  T = (I + A)^{-1} (forward substitution)
+//   MMA  U^T = R^T T^T          (the per-token updates u_i, 128 x 64)
+//   MMA  Oacc += U^T P^T        (o_i = e^{G_i} S0 q~_i + sum_{j<=i} e^{G_i-G_j}(q~_i.k~_j) u_j)
+//   MMA  S    += U^T (k~ e^{G_C-G})  (S_C = e^{G_C} S0 + sum_j e^{G_C-G_j} u_j k~_j^T)
+// Every exponent is of a non-positive number.  Tokens past the end of a
+// partial chunk get zero q/k/v, beta = 0 and g = 0, which leaves everything
+// unchanged.  This is the chunked form of the gated delta rule (Gated Delta
+// Networks); "Continuous batching for linear attention layers" runs such a
+// kernel over cu_seqlens with per-sequence initial and final states.
+//
+// The conv state is only read here; the new conv states of these sequences
+// are written by tail_update_kernel, launched after this kernel, so no chain
+// can see another chain's write.
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int D = 128;
+constexpr int CH = 64;        // chunk
+constexpr int KC = 4;         // conv taps
+constexpr int kThreads = 128;
+constexpr int kLocalCh = 3 * D;  // q, k of the k-head and v of the v-head
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]   2 x (128 rows x 128 B)
+constexpr uint32_t OFF_QKH = 32768;    // [q^ ; k^]   2 x (128 x 128 B)
+constexpr uint32_t OFF_S0 = 65536;     // S0 bf16     2 x (128 x 128 B)
+constexpr uint32_t OFF_KPT = 98304;    // k'^T        128 x 128 B
+constexpr uint32_t OFF_P = 114688;     // P           64 x 128 B
+constexpr uint32_t OFF_T = 122880;     // T           64 x 128 B
+constexpr uint32_t OFF_RU = 131072;    // R^T, then U^T   128 x 128 B
+constexpr uint32_t OFF_BV = 147456;    // beta v fp32 [64][128]
+constexpr uint32_t OFF_AM = 180224;    // A fp32 [64][64]
+constexpr uint32_t OFF_G = 196608;     // G fp32 [64]
+constexpr uint32_t OFF_BETA = 196864;  // beta fp32 [64]
+constexpr uint32_t OFF_W = 197120;     // conv taps fp32 [4][384]
+constexpr uint32_t OFF_TOT = 203264;   // scan partials [2]
+constexpr uint32_t SMEM_BYTES = 203392 + 1024;
+constexpr uint32_t KB_STRIDE = 16384;  // bytes between K-blocks of a 128-row tile
+
+// tensor memory columns
+constexpr uint32_t TM_X = 0, TM_OACC = 64, TM_Y = 128, TM_UT = 192, TM_S = 256;
+constexpr uint32_t TM_COLS = 512;
+
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
+  if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity) ? 1 : 0;
+  __syncthreads();
+  return *flag != 0;
+}
+
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* v) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __bfloat1622float2(h[j]);
+    v[2 * j] = f.x;
+    v[2 * j + 1] = f.y;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int flag;
+
+  __shared__ int s_chain;
+  const int tid = threadIdx.x;
+  const int Hk = p.Hk, Hv = p.Hv, C = p.C;
+  const int R = Hv / Hk;
+  int32_t* hdr = p.work.header();
+  const int n_chains = hdr[kNPre] * Hv;
+  if ((int)blockIdx.x >= n_chains) return;
+  const __nv_bfloat16* __restrict__ x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+  const __nv_bfloat16* __restrict__ wconv = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
+  const __nv_bfloat16* __restrict__ av = reinterpret_cast<const __nv_bfloat16*>(p.a);
+  const __nv_bfloat16* __restrict__ bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
+  __nv_bfloat16* __restrict__ out = reinterpret_cast<__nv_bfloat16*>(p.out);
+
+  float* G = reinterpret_cast<float*>(sm + OFF_G);
+  float* BETA = reinterpret_cast<float*>(sm + OFF_BETA);
+  float* WS = reinterpret_cast<float*>(sm + OFF_W);
+  float* BV = reinterpret_cast<float*>(sm + OFF_BV);
+  float* AM = reinterpret_cast<float*>(sm + OFF_AM);
+  float* TOT = reinterpret_cast<float*>(sm + OFF_TOT);
+  const uint32_t sbase = smem_u32(sm);
+
+  // ---- set-up: barrier, TMEM (kept for every chain this CTA runs)
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane = (uint32_t)(tid & ~31) << 16;  // this warp's TMEM lane base
+  uint32_t phase = 0;
+  const float inv_sqrt_d = rsqrtf((float)D);
+  bool failed = false;
+
+  // ---- chains, longest sequences first, pulled from the scheduler's counter
+  for (;;) {
+  if (tid == 0) s_chain = atomicAdd(&hdr[kWorkHead], 1);
+  __syncthreads();
+  const int chain = s_chain;
+  if (chain >= n_chains) break;
+  const int s = p.work.pre()[chain / Hv];
+  const int h = chain % Hv;
+  const int kh = h / R;
+  const int seq0 = p.cu[s];
+  const int L = p.cu[s + 1] - seq0;
+  const int wblk = p.blk[s];
+  const int rblk = p.has_past[s] ? wblk : 0;
+  const unsigned char* rbase = p.layer_base + (size_t)rblk * p.stride;
+  unsigned char* wbase = p.layer_base + (size_t)wblk * p.stride;
+  const __nv_bfloat16* __restrict__ tail_r = reinterpret_cast<const __nv_bfloat16*>(rbase);
+
+  // global channel of local channel lc (q | k of the k-head, v of the v-head)
+  auto gch = [&](int lc) {
+    return lc < D ? kh * D + lc : (lc < 2 * D ? Hk * D + kh * D + (lc - D) : 2 * Hk * D + h * D + (lc - 2 * D));
+  };
+  for (int lc = tid; lc < kLocalCh; lc += kThreads) {
+    const int gc = gch(lc);
+#pragma unroll
+    for (int j = 0; j < KC; ++j) WS[j * kLocalCh + lc] = __bfloat162float(wconv[(size_t)gc * KC + j]);
+  }
+  const float A_neg = -__expf(p.A_log[h]);
+  const float dtb = p.dt_bias[h];
+  __syncthreads();
+
+  const int n_chunks = (L + CH - 1) / CH;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int c0 = c * CH;                 // chunk start inside the sequence
+    const int n = min(CH, L - c0);         // valid tokens
+    // ---------------- prep: gates and their in-chunk cumulative sum
+    if (tid < CH) {
+      float g = 0.f, beta = 0.f;
+      if (tid < n) {
+        const size_t row = (size_t)(seq0 + c0 + tid);
+        g = A_neg * softplus_f32(__bfloat162float(av[row * Hv + h]) + dtb);
+        beta = sigmoid_f32(__bfloat162float(bv[row * Hv + h]));
+      }
+      // inclusive scan inside each warp, then across the two warps
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, g, o);
+        if ((tid & 31) >= o) g += t;
+      }
+      if ((tid & 31) == 31) TOT[tid >> 5] = g;
+      G[tid] = g;
+      BETA[tid] = beta;
+    }
+    __syncthreads();
+    if (tid >= 32 && tid < CH) G[tid] += TOT[0];
+    __syncthreads();
+    const float GC = G[CH - 1];
+
+    // ---------------- prep: conv + SiLU + norms -> bf16 tiles
+    {
+      const int i = tid & (CH - 1);
+      const int half = tid >> 6;  // 0: q and v[0:64), 1: k and v[64:128)
+      const bool valid = i < n;
+      const int pos = c0 + i;     // position inside the sequence
+      const float Gi = G[i];
+      const float bi = BETA[i];
+      float qk[D];
+      float ss = 0.f;
+      const int lbase = half ? D : 0;
+#pragma unroll
+      for (int g8 = 0; g8 < D / 8; ++g8) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        if (valid) {
+          const int lc0 = lbase + g8 * 8;
+          const int gc0 = gch(lc0);
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            const int pp = pos - (KC - 1) + j;
+            const __nv_bfloat16* src = pp >= 0 ? x + (size_t)(seq0 + pp) * C + gc0
+                                                : tail_r + (size_t)(KC - 1 + pp) * C + gc0;
+            float xv[8];
+            load8_bf16(src, xv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += WS[j * kLocalCh + lc0 + e] * xv[e];
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float yv = valid ? silu_f32(acc[e]) : 0.f;
+          qk[g8 * 8 + e] = yv;
+          ss += yv * yv;
+        }
+      }
+      const float scale = valid ? rsqrtf(ss + kL2Eps) * (half ? 1.f : inv_sqrt_d) : 0.f;
+#pragma unroll
+      for (int e = 0; e < D; ++e) qk[e] *= scale;
+      // [q~ ; k~] rows, [q^ ; k^] rows
+      const int trow = half * CH + i;
+      const float rs = half ? bi * __expf(Gi) : __expf(Gi);
+#pragma unroll
+      for (int g8 = 0; g8 < D / 8; ++g8) {
+        float v8[8], h8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          v8[e] = qk[g8 * 8 + e];
+          h8[e] = v8[e] * rs;
+        }
+        const int kb = g8 >> 3, k0 = (g8 & 7) * 8;
+        tc::sw128_store8(sm + OFF_QK + kb * KB_STRIDE, trow, k0, v8);
+        tc::sw128_store8(sm + OFF_QKH + kb * KB_STRIDE, trow, k0, h8);
+      }
+      if (half) {
+        // (k~ e^{G_C - G_i})^T : column i of a 128-row tile
+        const float ds = __expf(GC - Gi);
+#pragma unroll
+        for (int e = 0; e < D; ++e) tc::sw128_store1(sm + OFF_KPT, e, i, qk[e] * ds);
+      }
+      // beta * v for this thread's 64 v channels
+      const int v0 = half * 64;
+#pragma unroll 2
+      for (int g8 = 0; g8 < 8; ++g8) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        if (valid) {
+          const int lc0 = 2 * D + v0 + g8 * 8;
+          const int gc0 = gch(lc0);
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            const int pp = pos - (KC - 1) + j;
+            const __nv_bfloat16* src = pp >= 0 ? x + (size_t)(seq0 + pp) * C + gc0
+                                                : tail_r + (size_t)(KC - 1 + pp) * C + gc0;
+            float xv[8];
+            load8_bf16(src, xv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += WS[j * kLocalCh + lc0 + e] * xv[e];
+          }
+        }
+        float4 o0, o1;
+        o0.x = valid ? bi * silu_f32(acc[0]) : 0.f;
+        o0.y = valid ? bi * silu_f32(acc[1]) : 0.f;
+        o0.z = valid ? bi * silu_f32(acc[2]) : 0.f;
+        o0.w = valid ? bi * silu_f32(acc[3]) : 0.f;
+        o1.x = valid ? bi * silu_f32(acc[4]) : 0.f;
+        o1.y = valid ? bi * silu_f32(acc[5]) : 0.f;
+        o1.z = valid ? bi * silu_f32(acc[6]) : 0.f;
+        o1.w = valid ? bi * silu_f32(acc[7]) : 0.f;
+        *reinterpret_cast<float4*>(BV + i * D + v0 + g8 * 8) = o0;
+        *reinterpret_cast<float4*>(BV + i * D + v0 + g8 * 8 + 4) = o1;
+      }
+    }
+
+    // ---------------- state hand-over: S0 -> bf16 tile, TMEM S <- e^{G_C} S0
+    {
+      const int v = tid;
+      float srow[D];
+      if (c == 0) {
+        const float* S_r = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * D * D;
+#pragma unroll
+        for (int k = 0; k < D; ++k) srow[k] = S_r[(size_t)k * D + v];
+      } else {
+#pragma unroll
+        for (int c32 = 0; c32 < D / 32; ++c32) tc::tmem_ld32(tmem + lane + TM_S + c32 * 32, srow + c32 * 32);
+        tc::tmem_wait_ld();
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < D / 8; ++g8)
+        tc::sw128_store8(sm + OFF_S0 + (g8 >> 3) * KB_STRIDE, v, (g8 & 7) * 8, srow + g8 * 8);
+      const float dc = __expf(GC);
+#pragma unroll
+      for (int k = 0; k < D; ++k) srow[k] *= dc;
+#pragma unroll
+      for (int c32 = 0; c32 < D / 32; ++c32) tc::tmem_st32(tmem + lane + TM_S + c32 * 32, srow + c32 * 32);
+      tc::tmem_wait_st();
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_tile(tmem + TM_X, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
+                   tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_tile(tmem + TM_OACC, sbase + OFF_S0, KB_STRIDE, sbase + OFF_QKH, KB_STRIDE, 2,
+                   tc::idesc_bf16_f32(128, 128), false);
+      tc::commit(&bar);
+    }
+    if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
+    phase ^= 1;
+    tc::fence_after_sync();
+
+    // ---------------- A, P from X; R^T from Y
+    {
+      float xr[CH];
+      tc::tmem_ld32(tmem + lane + TM_X, xr);
+      tc::tmem_ld32(tmem + lane + TM_X + 32, xr + 32);
+      tc::tmem_wait_ld();
+      if (tid < CH) {
+        const int i = tid;
+        const float Gi = G[i];
+#pragma unroll
+        for (int g8 = 0; g8 < CH / 8; ++g8) {
+          float v8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = g8 * 8 + e;
+            v8[e] = j <= i ? xr[j] * __expf(Gi - G[j]) : 0.f;
+          }
+          tc::sw128_store8(sm + OFF_P, i, g8 * 8, v8);
+        }
+      } else {
+        const int i = tid - CH;
+        const float Gi = G[i], bi = BETA[i];
+#pragma unroll
+        for (int j4 = 0; j4 < CH / 4; ++j4) {
+          float4 a4;
+          const int j = j4 * 4;
+          a4.x = j + 0 < i ? bi * __expf(Gi - G[j + 0]) * xr[j + 0] : 0.f;
+          a4.y = j + 1 < i ? bi * __expf(Gi - G[j + 1]) * xr[j + 1] : 0.f;
+          a4.z = j + 2 < i ? bi * __expf(Gi - G[j + 2]) * xr[j + 2] : 0.f;
+          a4.w = j + 3 < i ? bi * __expf(Gi - G[j + 3]) * xr[j + 3] : 0.f;
+          *reinterpret_cast<float4*>(AM + i * CH + j) = a4;
+        }
+      }
+      float yr[CH];
+      tc::tmem_ld32(tmem + lane + TM_Y, yr);
+      tc::tmem_ld32(tmem + lane + TM_Y + 32, yr + 32);
+      tc::tmem_wait_ld();
+      const int v = tid;
+#pragma unroll
+      for (int g8 = 0; g8 < CH / 8; ++g8) {
+        float v8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = g8 * 8 + e;
+          v8[e] = BV[i * D + v] - yr[i];
+        }
+        tc::sw128_store8(sm + OFF_RU, v, g8 * 8, v8);
+      }
+    }
+    __syncthreads();
+    // ---------------- T = (I + A)^{-1}, column m per thread
+    if (tid < CH) {
+      const int m = tid;
+      float col[CH];
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        float acc = i == m ? 1.f : 0.f;
+        const float* arow = AM + i * CH;
+#pragma unroll
+        for (int j = 0; j < i; ++j) acc -= arow[j] * col[j];
+        col[i] = acc;
+      }
+#pragma unroll
+      for (int i = 0; i < CH; ++i) tc::sw128_store1(sm + OFF_T, i, m, col[i]);
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_tile(tmem + TM_UT, sbase + OFF_RU, 0, sbase + OFF_T, 0, 1, tc::idesc_bf16_f32(128, 64),
+                   false);
+      tc::commit(&bar);
+    }
+    if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
+    phase ^= 1;
+    tc::fence_after_sync();
+    // ---------------- U^T -> bf16 tile (over R^T, which MMA-D has consumed)
+    {
+      float ur[CH];
+      tc::tmem_ld32(tmem + lane + TM_UT, ur);
+      tc::tmem_ld32(tmem + lane + TM_UT + 32, ur + 32);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int g8 = 0; g8 < CH / 8; ++g8) tc::sw128_store8(sm + OFF_RU, tid, g8 * 8, ur + g8 * 8);
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_tile(tmem + TM_OACC, sbase + OFF_RU, 0, sbase + OFF_P, 0, 1, tc::idesc_bf16_f32(128, 64),
+                   true);
+      tc::mma_tile(tmem + TM_S, sbase + OFF_RU, 0, sbase + OFF_KPT, 0, 1,
+                   tc::idesc_bf16_f32(128, 128), true);
+      tc::commit(&bar);
+    }
+    if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
+    phase ^= 1;
+    tc::fence_after_sync();
+    // ---------------- outputs of the chunk
+    {
+      float orow[CH];
+      tc::tmem_ld32(tmem + lane + TM_OACC, orow);
+      tc::tmem_ld32(tmem + lane + TM_OACC + 32, orow + 32);
+      tc::tmem_wait_ld();
+      const int v = tid;
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+        if (i < n) out[((size_t)(seq0 + c0 + i) * Hv + h) * D + v] = __float2bfloat16_rn(orow[i]);
+    }
+  }
+
+  if (failed) break;
+  {
+    // ---- final state -> the write block, S[v][k] at (h*D + k)*D + v
+    float srow[D];
+#pragma unroll
+    for (int c32 = 0; c32 < D / 32; ++c32) tc::tmem_ld32(tmem + lane + TM_S + c32 * 32, srow + c32 * 32);
+    tc::tmem_wait_ld();
+    float* S_w = reinterpret_cast<float*>(wbase + p.rec_off) + (size_t)h * D * D;
+#pragma unroll
+    for (int k = 0; k < D; ++k) S_w[(size_t)k * D + tid] = srow[k];
+  }
+  __syncthreads();  // s_chain, WS and the tiles are reused by the next chain
+  }  // chains
+  if (failed && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+}
+
+// New conv states of the length > 1 sequences: the last K-1 inputs of
+// [old conv state ; x_seq], written after every chain has read the old one.
+__global__ void __launch_bounds__(256) tail_update_kernel(FwdParams p) {
+  const int n_pre = p.work.header()[kNPre];
+  if ((int)blockIdx.x >= n_pre) return;
+  const int s = p.work.pre()[blockIdx.x];
+  const int seq0 = p.cu[s];
+  const int L = p.cu[s + 1] - seq0;
+  const int wblk = p.blk[s];
+  const int rblk = p.has_past[s] ? wblk : 0;
+  const int C = p.C;
+  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+  const __nv_bfloat16* tail_r =
+      reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
+  __nv_bfloat16* tail_w = reinterpret_cast<__nv_bfloat16*>(p.layer_base + (size_t)wblk * p.stride);
+  for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
+    __nv_bfloat16 nv[KC - 1];
+#pragma unroll
+    for (int j = 0; j < KC - 1; ++j) {
+      const int pp = L - (KC - 1) + j;
+      nv[j] = pp >= 0 ? x[(size_t)(seq0 + pp) * C + ch] : tail_r[(size_t)(KC - 1 + pp) * C + ch];
+    }
+#pragma unroll
+    for (int j = 0; j < KC - 1; ++j) tail_w[(size_t)j * C + ch] = nv[j];
+  }
+}
+
+}  // namespace
+
+bool chunk_supported(int d, int act, int K) { return d == D && act == GDN_BF16 && K == KC; }
+
+cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
+  if (max_pre <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (num_sms <= 0) num_sms = 1;
+  }
+  const long long chains = (long long)max_pre * p.Hv;
+  const int grid = (int)(chains < num_sms ? chains : num_sms);
+  chunk_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  tail_update_kernel<<<max_pre, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

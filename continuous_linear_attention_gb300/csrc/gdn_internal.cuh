@@ -74,6 +74,10 @@ cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, 
 // activations, Hv = 2 Hk, K = 4.
 bool decode_supported(int d, int act, int Hk, int Hv, int K);
 cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
+// The tcgen05 chunked prefill kernel (length > 1 sequences) and the conv-state
+// update that follows it: d_k = d_v = 128, bf16 activations, K = 4.
+bool chunk_supported(int d, int act, int K);
+cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

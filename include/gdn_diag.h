@@ -1,0 +1,30 @@
+/*
+ * gdn_diag.h -- diagnostic entry point of libgdn, outside the forward path.
+ *
+ * gdn_diag_umma_gemm runs the tensor-core building blocks of the chunked
+ * prefill kernel on plain matrices, so a test can check them against a
+ * library GEMM: one CTA stages A and B into 128-byte-swizzled K-major shared
+ * tiles, optionally preloads C into tensor memory with tcgen05.st, issues
+ * tcgen05.mma (kind::f16, bf16 inputs, fp32 accumulator in tensor memory) and
+ * reads the result back with tcgen05.ld:
+ *     D[128][N] = (C ? C : 0) + A[128][K] * B[N][K]^T
+ * A, B: bf16 row-major device arrays; C, D: fp32 row-major device arrays
+ * (C may be NULL).  N in {64, 128, 192, 256}, K in {64, 128}.  Returns GDN_OK
+ * or GDN_ERR_NULL / GDN_ERR_DIMS / GDN_ERR_ALIGN / GDN_ERR_CUDA (nothing
+ * launched on error).  Stream-ordered, no synchronisation.
+ */
+#ifndef GDN_DIAG_H_
+#define GDN_DIAG_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, int N, int K,
+                       void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_DIAG_H_ */

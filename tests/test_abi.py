@@ -10,11 +10,11 @@ import pytest
 import oracle
 from continuous_linear_attention_gb300 import binding
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "gdn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 
 
-def _declared():
-    src = open(HEADER).read()
+def _declared(headers=("gdn.h", "gdn_diag.h")):
+    src = "".join(open(os.path.join(INCLUDE, h)).read() for h in headers)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", src)))
 
@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported():
     assert "gdn_varlen_forward" in names and "gdn_state_pool_create" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert sorted(binding.EXPORTED) == names
+    assert sorted(binding.EXPORTED + ["gdn_diag_umma_gemm"]) == names
 
 
 @pytest.mark.parametrize("dims", [

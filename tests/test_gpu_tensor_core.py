@@ -1,0 +1,23 @@
+"""The tensor-core building blocks (swizzled shared tiles, descriptors,
+tcgen05.mma, TMEM loads/stores) against torch's GEMM."""
+import pytest
+import torch
+
+from continuous_linear_attention_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N", [64, 128, 192, 256])
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("acc", [False, True])
+def test_umma_gemm_matches_torch(N, K, acc):
+    g = torch.Generator(device="cuda").manual_seed(N * 1000 + K + acc)
+    A = torch.randn(128, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    C = torch.randn(128, N, device="cuda", generator=g) if acc else None
+    D = torch.full((128, N), float("nan"), device="cuda")
+    binding.diag_umma_gemm(A, B, C, D)
+    torch.cuda.synchronize()
+    ref = A.float() @ B.float().T + (C if acc else 0)
+    torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
