@@ -143,6 +143,63 @@ def traffic_record(kernel_file: str):
         return None
 
 
+def prefill_flops(wl, chunk: int = 64) -> float:
+    """Algorithmic flops of the chunked form for the tokens of sequences longer
+    than one token: per token and v-head 2C(3 d_k + 2 d_v) + 6 d_k d_v (the
+    intra-chunk products K K^T, Q K^T, the T-weighted k and v, the P-weighted
+    updates; the state products W S^T, Q S^T, U^T K), triangular solve
+    excluded."""
+    d = wl.dims
+    per = 2 * chunk * (3 * d.dk + 2 * d.dv) + 6 * d.dk * d.dv
+    toks = sum(L for L in wl.seqlens() if L > 1)
+    return float(d.Hv * per * toks)
+
+
+def time_secondary(harness, wl, steps, device, pk):
+    """Tokens/s and the compute kernels' roofline for another workload (the
+    ~16k-token prefill, the mixed batch), timed like the main line."""
+    import torch
+    run = harness.DeviceRun(wl, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        run.run(stream)
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in kb + ka:
+        e.record(stream)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        run.pool.set_timing_events(kb[i], ka[i])
+        run.run(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    run.pool.set_timing_events(None, None)
+    ms = start.elapsed_time(stop) / steps
+    kms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(steps))
+    flags = run.pool.error_flags()
+    run.close()
+    fl = prefill_flops(wl)
+    tf = fl / (kms / 1e3) / 1e12
+    return {"workload": wl.name, "tokens": wl.T, "ms_per_step": ms,
+            "tokens_per_s": wl.T / (ms / 1e3), "compute_kernels_ms": kms,
+            "prefill_tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
+            "algorithmic_flops": fl, "error_flags": flags}
+
+
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity when not
+    distributed): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def cpu_baseline(wl, budget_s: float = 12.0):
     """The fp64 oracle as it stands, on the host cores, on a bounded sample of
     the workload (its first requests), scaled to tokens/s."""
@@ -202,6 +259,8 @@ def main():
                          "batches are for profiler captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the prefill / mixed-batch measurements")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -287,10 +346,8 @@ def main():
     e2e_ms = e0.elapsed_time(e1)
 
     # max over ranks
-    t = torch.tensor([elapsed_ms, e2e_ms, statistics.mean(kern_ms)], device=f"cuda:{local_rank}")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms, kern_mean_ms = [float(v) for v in t.tolist()]
+    elapsed_ms, e2e_ms, kern_mean_ms = max_over_ranks(
+        [elapsed_ms, e2e_ms, statistics.mean(kern_ms)], device=f"cuda:{local_rank}")
 
     if rank == 0:
         pk = peaks()
@@ -321,6 +378,11 @@ def main():
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
         }
+        if not args.no_secondary:
+            line["secondary"] = [
+                time_secondary(harness, synth.packed_prefill(), 20, f"cuda:{local_rank}", pk),
+                time_secondary(harness, synth.mixed_batch(), 20, f"cuda:{local_rank}", pk),
+            ]
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(line), flush=True)
