@@ -24,6 +24,7 @@ FLAG_TRASH_WRITE = 0x4
 FLAG_DUPLICATE = 0x8
 FLAG_TIMEOUT = 0x10
 FLAG_HINT = 0x20
+FLAG_RANGE = 0x40
 
 EXPORTED = [
     "gdn_state_pool_layout_for",
@@ -76,7 +77,7 @@ def load() -> ctypes.CDLL:
                                        I, I, I, P]
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
-    lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, P]
+    lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, I, P]
     lib.gdn_diag_umma_gemm.restype = I
     lib.gdn_status_string.argtypes = [I]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -191,9 +192,10 @@ def varlen_forward(pool: Pool, layer: int, x_qkv, a, b, cu_seqlens, state_block_
                                      _stream(stream)), "gdn_varlen_forward")
 
 
-def diag_umma_gemm(A, B, C, D, stream=None) -> None:
+def diag_umma_gemm(A, B, C, D, operand_f16=False, stream=None) -> None:
     """gdn_diag_umma_gemm: D = (C or 0) + A @ B^T on the tensor cores
     (A [128][K], B [N][K] bf16; C, D [128][N] fp32; device tensors)."""
     N, K = B.shape
-    _check(load().gdn_diag_umma_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K, _stream(stream)),
+    _check(load().gdn_diag_umma_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K,
+                                     1 if operand_f16 else 0, _stream(stream)),
            "gdn_diag_umma_gemm")

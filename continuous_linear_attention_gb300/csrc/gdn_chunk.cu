@@ -5,20 +5,25 @@
 // accumulators in tensor memory).  The recurrent state stays in tensor memory
 // (fp32) for the whole sequence; only the final state is written back.
 //
-// One CTA (4 warps) per (sequence, v-head) chain, longest sequences first.
+// Persistent CTAs (8 warps, one per SM) pull (sequence, v-head) chains,
+// longest sequences first.
 // Per chunk, with G_i the inclusive cumulative gate inside the chunk, beta_i
 // the write strength, q~/k~ the normalised rows and S0 the state at the chunk
 // start (S is d_v x d_k, S[v][k]):
-//   prep (CUDA cores): conv + SiLU + L2 norms + gates; bf16 tiles
+//   prep (CUDA cores): conv + SiLU + L2 norms + gates; fp16 tiles
 //        [q~ ; k~], [q~ e^G ; k~ beta e^G], (k~ e^{G_C - G})^T, fp32 beta v
-//   state hand-over: S0 -> bf16 tile; TMEM S <- e^{G_C} S0
+//   state hand-over: S0 -> fp16 tile; TMEM S <- e^{G_C} S0
 //   MMA  X  = [q~ ; k~] k~^T                     (QK^T and KK^T, 128 x 64)
 //   MMA  [Oacc | Y] = S0 [q~ e^G ; k~ beta e^G]^T (128 x 128)
 //   CUDA A_ij = beta_i e^{G_i-G_j} (k~_i.k~_j) (j<i);  P_ij = (q~_i.k~_j) e^{G_i-G_j} (j<=i)
-//        R^T = (beta v)^T - Y;  T = (I + A)^{-1} (forward substitution)
+//        R^T = (beta v)^T - Y;  T = (I + A)^{-1} (blocked forward substitution:
+//        16 x 16 diagonal blocks, then the off-diagonal blocks level by level)
 //   MMA  U^T = R^T T^T          (the per-token updates u_i, 128 x 64)
 //   MMA  Oacc += U^T P^T        (o_i = e^{G_i} S0 q~_i + sum_{j<=i} e^{G_i-G_j}(q~_i.k~_j) u_j)
 //   MMA  S    += U^T (k~ e^{G_C-G})  (S_C = e^{G_C} S0 + sum_j e^{G_C-G_j} u_j k~_j^T)
+// MMA operands are fp16 (same tensor-core rate as bf16, 3 more mantissa bits:
+// the bf16 version of this kernel sat at ~4.5e-3 relative error on slowly
+// decaying states).  An operand outside the fp16 range raises GDN_FLAG_RANGE.
 // Every exponent is of a non-positive number.  Tokens past the end of a
 // partial chunk get zero q/k/v, beta = 0 and g = 0, which leaves everything
 // unchanged.  This is the chunked form of the gated delta rule (Gated Delta
@@ -35,27 +40,31 @@
 namespace gdn {
 namespace {
 
+using E = __half;             // MMA operand type
 constexpr int D = 128;
 constexpr int CH = 64;        // chunk
 constexpr int KC = 4;         // conv taps
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kLocalCh = 3 * D;  // q, k of the k-head and v of the v-head
+constexpr float kF16Max = 65000.f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]   2 x (128 rows x 128 B)
 constexpr uint32_t OFF_QKH = 32768;    // [q^ ; k^]   2 x (128 x 128 B)
-constexpr uint32_t OFF_S0 = 65536;     // S0 bf16     2 x (128 x 128 B)
+constexpr uint32_t OFF_S0 = 65536;     // S0          2 x (128 x 128 B)
 constexpr uint32_t OFF_KPT = 98304;    // k'^T        128 x 128 B
 constexpr uint32_t OFF_P = 114688;     // P           64 x 128 B
 constexpr uint32_t OFF_T = 122880;     // T           64 x 128 B
 constexpr uint32_t OFF_RU = 131072;    // R^T, then U^T   128 x 128 B
 constexpr uint32_t OFF_BV = 147456;    // beta v fp32 [64][128]
-constexpr uint32_t OFF_AM = 180224;    // A fp32 [64][64]
-constexpr uint32_t OFF_G = 196608;     // G fp32 [64]
-constexpr uint32_t OFF_BETA = 196864;  // beta fp32 [64]
-constexpr uint32_t OFF_W = 197120;     // conv taps fp32 [4][384]
-constexpr uint32_t OFF_TOT = 203264;   // scan partials [2]
-constexpr uint32_t SMEM_BYTES = 203392 + 1024;
+constexpr uint32_t OFF_AM = 180224;    // A fp32 [64][64]; then the out tile bf16 [64][128]
+constexpr uint32_t OFF_TS = 196608;    // T fp32 [64][64]
+constexpr uint32_t OFF_Z = 212992;     // blocked-solve scratch fp32 [3][16][16]
+constexpr uint32_t OFF_G = 216064;     // G fp32 [64]
+constexpr uint32_t OFF_BETA = 216320;  // beta fp32 [64]
+constexpr uint32_t OFF_TOT = 216576;   // scan partials [2]
+constexpr uint32_t OFF_W = 216832;     // conv taps fp32 [4][384]
+constexpr uint32_t SMEM_BYTES = 222976 + 1024;
 constexpr uint32_t KB_STRIDE = 16384;  // bytes between K-blocks of a 128-row tile
 
 // tensor memory columns
@@ -79,14 +88,21 @@ __device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* v) {
   }
 }
 
+__device__ __forceinline__ bool out_of_f16(const float* v, int n) {
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < n; ++e) bad |= !(fabsf(v[e]) <= kF16Max);
+  return bad;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
-
   __shared__ int s_chain;
+
   const int tid = threadIdx.x;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
   const int R = Hv / Hk;
@@ -104,6 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
   float* WS = reinterpret_cast<float*>(sm + OFF_W);
   float* BV = reinterpret_cast<float*>(sm + OFF_BV);
   float* AM = reinterpret_cast<float*>(sm + OFF_AM);
+  __nv_bfloat16* OT = reinterpret_cast<__nv_bfloat16*>(sm + OFF_AM);
+  float* TS = reinterpret_cast<float*>(sm + OFF_TS);
+  float* Z = reinterpret_cast<float*>(sm + OFF_Z);
   float* TOT = reinterpret_cast<float*>(sm + OFF_TOT);
   const uint32_t sbase = smem_u32(sm);
 
@@ -117,10 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane = (uint32_t)(tid & ~31) << 16;  // this warp's TMEM lane base
+  // TMEM lane quarter of this warp (warps w and w + 4 share lanes 32 (w % 4) ..)
+  const uint32_t lane = (uint32_t)(tid & 96) << 16;
+  const int r128 = tid & 127;  // TMEM row (lane) of this thread
+  const int chalf = tid >> 7;  // which half of the columns this thread handles
   uint32_t phase = 0;
   const float inv_sqrt_d = rsqrtf((float)D);
   bool failed = false;
+  bool range_bad = false;
 
   // ---- chains, longest sequences first, pulled from the scheduler's counter
   for (;;) {
@@ -141,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
 
   // global channel of local channel lc (q | k of the k-head, v of the v-head)
   auto gch = [&](int lc) {
-    return lc < D ? kh * D + lc : (lc < 2 * D ? Hk * D + kh * D + (lc - D) : 2 * Hk * D + h * D + (lc - 2 * D));
+    return lc < D ? kh * D + lc
+                  : (lc < 2 * D ? Hk * D + kh * D + (lc - D) : 2 * Hk * D + h * D + (lc - 2 * D));
   };
   for (int lc = tid; lc < kLocalCh; lc += kThreads) {
     const int gc = gch(lc);
@@ -164,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
         g = A_neg * softplus_f32(__bfloat162float(av[row * Hv + h]) + dtb);
         beta = sigmoid_f32(__bfloat162float(bv[row * Hv + h]));
       }
-      // inclusive scan inside each warp, then across the two warps
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float t = __shfl_up_sync(0xffffffffu, g, o);
@@ -179,19 +202,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     __syncthreads();
     const float GC = G[CH - 1];
 
-    // ---------------- prep: conv + SiLU + norms -> bf16 tiles
+    // ---------------- prep: conv + SiLU + norms -> fp16 tiles (4 threads per token)
     {
-      const int i = tid & (CH - 1);
-      const int half = tid >> 6;  // 0: q and v[0:64), 1: k and v[64:128)
+      const int i = tid >> 2;
+      const int part = tid & 3;     // 0,1: q halves, 2,3: k halves; each also 32 v channels
+      const bool isk = part >= 2;
+      const int hsel = part & 1;
       const bool valid = i < n;
-      const int pos = c0 + i;     // position inside the sequence
+      const int pos = c0 + i;       // position inside the sequence
       const float Gi = G[i];
       const float bi = BETA[i];
-      float qk[D];
+      const int lbase = (isk ? D : 0) + hsel * 64;
+      float qk[64];
       float ss = 0.f;
-      const int lbase = half ? D : 0;
 #pragma unroll
-      for (int g8 = 0; g8 < D / 8; ++g8) {
+      for (int g8 = 0; g8 < 8; ++g8) {
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -216,39 +241,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
           ss += yv * yv;
         }
       }
-      const float scale = valid ? rsqrtf(ss + kL2Eps) * (half ? 1.f : inv_sqrt_d) : 0.f;
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      const float scale = valid ? rsqrtf(ss + kL2Eps) * (isk ? 1.f : inv_sqrt_d) : 0.f;
 #pragma unroll
-      for (int e = 0; e < D; ++e) qk[e] *= scale;
-      // [q~ ; k~] rows, [q^ ; k^] rows
-      const int trow = half * CH + i;
-      const float rs = half ? bi * __expf(Gi) : __expf(Gi);
+      for (int e = 0; e < 64; ++e) qk[e] *= scale;
+      const int trow = (isk ? CH : 0) + i;
+      const float rs = isk ? bi * __expf(Gi) : __expf(Gi);
 #pragma unroll
-      for (int g8 = 0; g8 < D / 8; ++g8) {
-        float v8[8], h8[8];
+      for (int g8 = 0; g8 < 8; ++g8) {
+        float h8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v8[e] = qk[g8 * 8 + e];
-          h8[e] = v8[e] * rs;
-        }
-        const int kb = g8 >> 3, k0 = (g8 & 7) * 8;
-        tc::sw128_store8(sm + OFF_QK + kb * KB_STRIDE, trow, k0, v8);
-        tc::sw128_store8(sm + OFF_QKH + kb * KB_STRIDE, trow, k0, h8);
+        for (int e = 0; e < 8; ++e) h8[e] = qk[g8 * 8 + e] * rs;
+        tc::sw128_store8<E>(sm + OFF_QK + hsel * KB_STRIDE, trow, g8 * 8, qk + g8 * 8);
+        tc::sw128_store8<E>(sm + OFF_QKH + hsel * KB_STRIDE, trow, g8 * 8, h8);
       }
-      if (half) {
-        // (k~ e^{G_C - G_i})^T : column i of a 128-row tile
+      if (isk) {
+        // (k~ e^{G_C - G_i})^T : column i of the 128-row tile
         const float ds = __expf(GC - Gi);
 #pragma unroll
-        for (int e = 0; e < D; ++e) tc::sw128_store1(sm + OFF_KPT, e, i, qk[e] * ds);
+        for (int e = 0; e < 64; ++e) tc::sw128_store1<E>(sm + OFF_KPT, hsel * 64 + e, i, qk[e] * ds);
       }
-      // beta * v for this thread's 64 v channels
-      const int v0 = half * 64;
-#pragma unroll 2
-      for (int g8 = 0; g8 < 8; ++g8) {
+      // beta * v for this thread's 32 v channels
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        const int vc = part * 32 + g8 * 8;
         if (valid) {
-          const int lc0 = 2 * D + v0 + g8 * 8;
+          const int lc0 = 2 * D + vc;
           const int gc0 = gch(lc0);
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
@@ -270,32 +291,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
         o1.y = valid ? bi * silu_f32(acc[5]) : 0.f;
         o1.z = valid ? bi * silu_f32(acc[6]) : 0.f;
         o1.w = valid ? bi * silu_f32(acc[7]) : 0.f;
-        *reinterpret_cast<float4*>(BV + i * D + v0 + g8 * 8) = o0;
-        *reinterpret_cast<float4*>(BV + i * D + v0 + g8 * 8 + 4) = o1;
+        *reinterpret_cast<float4*>(BV + i * D + vc) = o0;
+        *reinterpret_cast<float4*>(BV + i * D + vc + 4) = o1;
       }
     }
 
-    // ---------------- state hand-over: S0 -> bf16 tile, TMEM S <- e^{G_C} S0
+    // ---------------- state hand-over: S0 -> fp16 tile, TMEM S <- e^{G_C} S0
     {
-      const int v = tid;
-      float srow[D];
+      const int v = r128;
+      float srow[64];
       if (c == 0) {
         const float* S_r = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * D * D;
 #pragma unroll
-        for (int k = 0; k < D; ++k) srow[k] = S_r[(size_t)k * D + v];
+        for (int k = 0; k < 64; ++k) srow[k] = S_r[(size_t)(chalf * 64 + k) * D + v];
       } else {
-#pragma unroll
-        for (int c32 = 0; c32 < D / 32; ++c32) tc::tmem_ld32(tmem + lane + TM_S + c32 * 32, srow + c32 * 32);
+        tc::tmem_ld32(tmem + lane + TM_S + chalf * 64, srow);
+        tc::tmem_ld32(tmem + lane + TM_S + chalf * 64 + 32, srow + 32);
         tc::tmem_wait_ld();
       }
+      range_bad |= out_of_f16(srow, 64);
 #pragma unroll
-      for (int g8 = 0; g8 < D / 8; ++g8)
-        tc::sw128_store8(sm + OFF_S0 + (g8 >> 3) * KB_STRIDE, v, (g8 & 7) * 8, srow + g8 * 8);
+      for (int g8 = 0; g8 < 8; ++g8)
+        tc::sw128_store8<E>(sm + OFF_S0 + chalf * KB_STRIDE, v, g8 * 8, srow + g8 * 8);
       const float dc = __expf(GC);
 #pragma unroll
-      for (int k = 0; k < D; ++k) srow[k] *= dc;
-#pragma unroll
-      for (int c32 = 0; c32 < D / 32; ++c32) tc::tmem_st32(tmem + lane + TM_S + c32 * 32, srow + c32 * 32);
+      for (int k = 0; k < 64; ++k) srow[k] *= dc;
+      tc::tmem_st32(tmem + lane + TM_S + chalf * 64, srow);
+      tc::tmem_st32(tmem + lane + TM_S + chalf * 64 + 32, srow + 32);
       tc::tmem_wait_st();
     }
     tc::fence_proxy_async_smem();
@@ -304,140 +326,185 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_tile(tmem + TM_X, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
-                   tc::idesc_bf16_f32(128, 64), false);
+                   tc::idesc_f16_f32(128, 64), false);
       tc::mma_tile(tmem + TM_OACC, sbase + OFF_S0, KB_STRIDE, sbase + OFF_QKH, KB_STRIDE, 2,
-                   tc::idesc_bf16_f32(128, 128), false);
+                   tc::idesc_f16_f32(128, 128), false);
       tc::commit(&bar);
     }
     if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
     phase ^= 1;
     tc::fence_after_sync();
 
-    // ---------------- A, P from X; R^T from Y
+    // ---------------- A, P from X; R^T from Y (each thread: one row, 32 columns)
     {
-      float xr[CH];
-      tc::tmem_ld32(tmem + lane + TM_X, xr);
-      tc::tmem_ld32(tmem + lane + TM_X + 32, xr + 32);
+      float xr[32];
+      tc::tmem_ld32(tmem + lane + TM_X + chalf * 32, xr);
       tc::tmem_wait_ld();
-      if (tid < CH) {
-        const int i = tid;
+      if (r128 < CH) {
+        const int i = r128;
         const float Gi = G[i];
 #pragma unroll
-        for (int g8 = 0; g8 < CH / 8; ++g8) {
+        for (int g8 = 0; g8 < 4; ++g8) {
           float v8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int j = g8 * 8 + e;
-            v8[e] = j <= i ? xr[j] * __expf(Gi - G[j]) : 0.f;
+            const int j = chalf * 32 + g8 * 8 + e;
+            v8[e] = j <= i ? xr[g8 * 8 + e] * __expf(Gi - G[j]) : 0.f;
           }
-          tc::sw128_store8(sm + OFF_P, i, g8 * 8, v8);
+          tc::sw128_store8<E>(sm + OFF_P, i, chalf * 32 + g8 * 8, v8);
         }
       } else {
-        const int i = tid - CH;
+        const int i = r128 - CH;
         const float Gi = G[i], bi = BETA[i];
 #pragma unroll
-        for (int j4 = 0; j4 < CH / 4; ++j4) {
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const int j = chalf * 32 + j4 * 4;
           float4 a4;
-          const int j = j4 * 4;
-          a4.x = j + 0 < i ? bi * __expf(Gi - G[j + 0]) * xr[j + 0] : 0.f;
-          a4.y = j + 1 < i ? bi * __expf(Gi - G[j + 1]) * xr[j + 1] : 0.f;
-          a4.z = j + 2 < i ? bi * __expf(Gi - G[j + 2]) * xr[j + 2] : 0.f;
-          a4.w = j + 3 < i ? bi * __expf(Gi - G[j + 3]) * xr[j + 3] : 0.f;
+          a4.x = j + 0 < i ? bi * __expf(Gi - G[j + 0]) * xr[j4 * 4 + 0] : 0.f;
+          a4.y = j + 1 < i ? bi * __expf(Gi - G[j + 1]) * xr[j4 * 4 + 1] : 0.f;
+          a4.z = j + 2 < i ? bi * __expf(Gi - G[j + 2]) * xr[j4 * 4 + 2] : 0.f;
+          a4.w = j + 3 < i ? bi * __expf(Gi - G[j + 3]) * xr[j4 * 4 + 3] : 0.f;
           *reinterpret_cast<float4*>(AM + i * CH + j) = a4;
         }
       }
-      float yr[CH];
-      tc::tmem_ld32(tmem + lane + TM_Y, yr);
-      tc::tmem_ld32(tmem + lane + TM_Y + 32, yr + 32);
+      float yr[32];
+      tc::tmem_ld32(tmem + lane + TM_Y + chalf * 32, yr);
       tc::tmem_wait_ld();
-      const int v = tid;
+      const int v = r128;
 #pragma unroll
-      for (int g8 = 0; g8 < CH / 8; ++g8) {
+      for (int g8 = 0; g8 < 4; ++g8) {
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int i = g8 * 8 + e;
-          v8[e] = BV[i * D + v] - yr[i];
+          const int i = chalf * 32 + g8 * 8 + e;
+          v8[e] = BV[i * D + v] - yr[g8 * 8 + e];
         }
-        tc::sw128_store8(sm + OFF_RU, v, g8 * 8, v8);
+        range_bad |= out_of_f16(v8, 8);
+        tc::sw128_store8<E>(sm + OFF_RU, v, chalf * 32 + g8 * 8, v8);
       }
     }
     __syncthreads();
-    // ---------------- T = (I + A)^{-1}, column m per thread
+    // ---------------- T = (I + A)^{-1}: diagonal 16 x 16 blocks, column per thread
     if (tid < CH) {
-      const int m = tid;
-      float col[CH];
+      const int b = tid >> 4, m = tid & 15;
+      const float* Ab = AM + (16 * b) * CH + 16 * b;
+      float col[16];
 #pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        float acc = i == m ? 1.f : 0.f;
-        const float* arow = AM + i * CH;
+      for (int r = 0; r < 16; ++r) {
+        float acc = r == m ? 1.f : 0.f;
 #pragma unroll
-        for (int j = 0; j < i; ++j) acc -= arow[j] * col[j];
-        col[i] = acc;
+        for (int j = 0; j < r; ++j) acc -= Ab[r * CH + j] * col[j];
+        col[r] = acc;
       }
 #pragma unroll
-      for (int i = 0; i < CH; ++i) tc::sw128_store1(sm + OFF_T, i, m, col[i]);
+      for (int r = 0; r < 16; ++r) TS[(16 * b + r) * CH + 16 * b + m] = col[r];
+    }
+    __syncthreads();
+    // off-diagonal blocks, level L = i - j: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+    for (int Lv = 1; Lv < 4; ++Lv) {
+      const int ne = (4 - Lv) * 256;
+      for (int e = tid; e < ne; e += kThreads) {
+        const int j = e >> 8, i = j + Lv, rr = (e >> 4) & 15, cc = e & 15;
+        float z = 0.f;
+        for (int k = j; k < i; ++k) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            z += AM[(16 * i + rr) * CH + 16 * k + q] * TS[(16 * k + q) * CH + 16 * j + cc];
+        }
+        Z[e] = z;
+      }
+      __syncthreads();
+      for (int e = tid; e < ne; e += kThreads) {
+        const int j = e >> 8, i = j + Lv, rr = (e >> 4) & 15, cc = e & 15;
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) t -= TS[(16 * i + rr) * CH + 16 * i + q] * Z[(e & ~255) + q * 16 + cc];
+        TS[(16 * i + rr) * CH + 16 * j + cc] = t;
+      }
+      __syncthreads();
+    }
+    // T -> fp16 tile (upper blocks are zero)
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int idx = tid + kThreads * q2;
+      const int i = idx >> 3, c8 = idx & 7;
+      float v8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = c8 * 8 + e;
+        v8[e] = (j >> 4) <= (i >> 4) ? TS[i * CH + j] : 0.f;
+      }
+      range_bad |= out_of_f16(v8, 8);
+      tc::sw128_store8<E>(sm + OFF_T, i, c8 * 8, v8);
     }
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     if (tid == 0) {
       tc::fence_after_sync();
-      tc::mma_tile(tmem + TM_UT, sbase + OFF_RU, 0, sbase + OFF_T, 0, 1, tc::idesc_bf16_f32(128, 64),
+      tc::mma_tile(tmem + TM_UT, sbase + OFF_RU, 0, sbase + OFF_T, 0, 1, tc::idesc_f16_f32(128, 64),
                    false);
       tc::commit(&bar);
     }
     if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
     phase ^= 1;
     tc::fence_after_sync();
-    // ---------------- U^T -> bf16 tile (over R^T, which MMA-D has consumed)
+    // ---------------- U^T -> fp16 tile (over R^T, which MMA-D has consumed)
     {
-      float ur[CH];
-      tc::tmem_ld32(tmem + lane + TM_UT, ur);
-      tc::tmem_ld32(tmem + lane + TM_UT + 32, ur + 32);
+      float ur[32];
+      tc::tmem_ld32(tmem + lane + TM_UT + chalf * 32, ur);
       tc::tmem_wait_ld();
+      range_bad |= out_of_f16(ur, 32);
 #pragma unroll
-      for (int g8 = 0; g8 < CH / 8; ++g8) tc::sw128_store8(sm + OFF_RU, tid, g8 * 8, ur + g8 * 8);
+      for (int g8 = 0; g8 < 4; ++g8)
+        tc::sw128_store8<E>(sm + OFF_RU, r128, chalf * 32 + g8 * 8, ur + g8 * 8);
     }
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     if (tid == 0) {
       tc::fence_after_sync();
-      tc::mma_tile(tmem + TM_OACC, sbase + OFF_RU, 0, sbase + OFF_P, 0, 1, tc::idesc_bf16_f32(128, 64),
+      tc::mma_tile(tmem + TM_OACC, sbase + OFF_RU, 0, sbase + OFF_P, 0, 1, tc::idesc_f16_f32(128, 64),
                    true);
       tc::mma_tile(tmem + TM_S, sbase + OFF_RU, 0, sbase + OFF_KPT, 0, 1,
-                   tc::idesc_bf16_f32(128, 128), true);
+                   tc::idesc_f16_f32(128, 128), true);
       tc::commit(&bar);
     }
     if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
     phase ^= 1;
     tc::fence_after_sync();
-    // ---------------- outputs of the chunk
+    // ---------------- outputs of the chunk, transposed through shared memory
     {
-      float orow[CH];
-      tc::tmem_ld32(tmem + lane + TM_OACC, orow);
-      tc::tmem_ld32(tmem + lane + TM_OACC + 32, orow + 32);
+      float orow[32];
+      tc::tmem_ld32(tmem + lane + TM_OACC + chalf * 32, orow);
       tc::tmem_wait_ld();
-      const int v = tid;
 #pragma unroll
-      for (int i = 0; i < CH; ++i)
-        if (i < n) out[((size_t)(seq0 + c0 + i) * Hv + h) * D + v] = __float2bfloat16_rn(orow[i]);
+      for (int e = 0; e < 32; ++e) OT[(chalf * 32 + e) * D + r128] = __float2bfloat16_rn(orow[e]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int idx = tid + kThreads * q4;
+      const int i = idx >> 4, c16 = idx & 15;
+      if (i < n)
+        *reinterpret_cast<uint4*>(out + ((size_t)(seq0 + c0 + i) * Hv + h) * D + c16 * 8) =
+            *reinterpret_cast<const uint4*>(OT + i * D + c16 * 8);
     }
   }
-
   if (failed) break;
   {
     // ---- final state -> the write block, S[v][k] at (h*D + k)*D + v
-    float srow[D];
-#pragma unroll
-    for (int c32 = 0; c32 < D / 32; ++c32) tc::tmem_ld32(tmem + lane + TM_S + c32 * 32, srow + c32 * 32);
+    float srow[64];
+    tc::tmem_ld32(tmem + lane + TM_S + chalf * 64, srow);
+    tc::tmem_ld32(tmem + lane + TM_S + chalf * 64 + 32, srow + 32);
     tc::tmem_wait_ld();
     float* S_w = reinterpret_cast<float*>(wbase + p.rec_off) + (size_t)h * D * D;
 #pragma unroll
-    for (int k = 0; k < D; ++k) S_w[(size_t)k * D + tid] = srow[k];
+    for (int k = 0; k < 64; ++k) S_w[(size_t)(chalf * 64 + k) * D + r128] = srow[k];
   }
-  __syncthreads();  // s_chain, WS and the tiles are reused by the next chain
+  if (__syncthreads_or(range_bad ? 1 : 0) && tid == 0)
+    atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
+  range_bad = false;
   }  // chains
   if (failed && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
   tc::fence_before_sync();

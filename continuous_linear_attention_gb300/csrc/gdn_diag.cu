@@ -1,6 +1,8 @@
 // Diagnostic tensor-core GEMM (see include/gdn_diag.h): exercises the shared
 // tile layout, descriptors, MMA issue/commit and TMEM load/store helpers of
 // gdn_tc.cuh on plain matrices.
+#include <type_traits>
+
 #include "gdn.h"
 #include "gdn_diag.h"
 #include "gdn_internal.cuh"
@@ -11,6 +13,7 @@ namespace {
 
 constexpr int kM = 128;
 
+template <typename E>
 __global__ void __launch_bounds__(128, 1)
 diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
                  const float* __restrict__ Cin, float* __restrict__ D, int N, int K,
@@ -31,10 +34,10 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
     for (int k0 = 0; k0 < 64; k0 += 8) {
       float v[8];
       for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(A[(size_t)tid * K + kb * 64 + k0 + j]);
-      tc::sw128_store8(a_tile + kb * a_kb, tid, k0, v);
+      tc::sw128_store8<E>(a_tile + kb * a_kb, tid, k0, v);
       for (int r = tid; r < N; r += 128) {
         for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(B[(size_t)r * K + kb * 64 + k0 + j]);
-        tc::sw128_store8(b_tile + kb * b_kb, r, k0, v);
+        tc::sw128_store8<E>(b_tile + kb * b_kb, r, k0, v);
       }
     }
   }
@@ -61,8 +64,9 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
   __syncthreads();
   if (tid == 0) {
     tc::fence_after_sync();
+    constexpr bool kF16 = std::is_same<E, __half>::value;
     tc::mma_tile(tmem, smem_u32(a_tile), a_kb, smem_u32(b_tile), b_kb, kblocks,
-                 tc::idesc_bf16_f32(kM, N), Cin != nullptr);
+                 kF16 ? tc::idesc_f16_f32(kM, N) : tc::idesc_bf16_f32(kM, N), Cin != nullptr);
     tc::commit(&bar);
     ok = mbar_wait_bounded(&bar, 0) ? 1 : 0;
   }
@@ -87,7 +91,7 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
 }  // namespace gdn
 
 extern "C" int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, int N,
-                                  int K, void* stream) {
+                                  int K, int operand_f16, void* stream) {
   if (!A || !B || !D) return GDN_ERR_NULL;
   if ((N != 64 && N != 128 && N != 192 && N != 256) || (K != 64 && K != 128))
     return GDN_ERR_DIMS;
@@ -96,10 +100,18 @@ extern "C" int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, 
   static unsigned* err = nullptr;
   if (!err && cudaMalloc((void**)&err, sizeof(unsigned)) != cudaSuccess) return GDN_ERR_CUDA;
   const size_t smem = (size_t)(K / 64) * (128 + N) * 128 + 1024;
-  if (cudaFuncSetAttribute(gdn::diag_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  gdn::diag_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
-      (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, err);
+  if (operand_f16) {
+    if (cudaFuncSetAttribute(gdn::diag_umma_kernel<__half>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    gdn::diag_umma_kernel<__half><<<1, 128, smem, (cudaStream_t)stream>>>(
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, err);
+  } else {
+    if (cudaFuncSetAttribute(gdn::diag_umma_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    gdn::diag_umma_kernel<__nv_bfloat16><<<1, 128, smem, (cudaStream_t)stream>>>(
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, err);
+  }
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -2,8 +2,9 @@
 // from the PTX ISA: shared-memory matrix descriptors, the kind::f16
 // instruction descriptor, MMA issue/commit, TMEM allocation and loads/stores.
 //
-// Operand convention used throughout: every MMA operand is a bf16 matrix in
-// shared memory, K-major, in the 128-byte swizzled canonical layout.  A tile
+// Operand convention used throughout: every MMA operand is a 16-bit float
+// matrix (fp16 or bf16, both operands of one MMA the same type) in shared
+// memory, K-major, in the 128-byte swizzled canonical layout.  A tile
 // of R rows x 64 K-elements (one "K-block", 128 bytes per row) is stored as
 // R/8 groups of 8 rows x 128 bytes (1024 bytes per group, groups contiguous);
 // inside a group, the 16-byte chunk j of row r sits at chunk position
@@ -12,6 +13,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "gdn_ptx.cuh"
@@ -26,23 +28,38 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
          (uint32_t)(k & 7) * 2u;
 }
 
-// Writes 8 consecutive K-elements (k0 % 8 == 0) of one row as one 16-byte store.
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16*) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
+  __half2 p = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Writes 8 consecutive K-elements (k0 % 8 == 0) of one row as one 16-byte
+// store, converted to the 16-bit type E (round to nearest even).
+template <typename E = __nv_bfloat16>
 __device__ __forceinline__ void sw128_store8(unsigned char* tile, int row, int k0,
                                              const float* v) {
-  __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
-  __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 p2 = __floats2bfloat162_rn(v[4], v[5]);
-  __nv_bfloat162 p3 = __floats2bfloat162_rn(v[6], v[7]);
   uint4 w;
-  w.x = *reinterpret_cast<uint32_t*>(&p0);
-  w.y = *reinterpret_cast<uint32_t*>(&p1);
-  w.z = *reinterpret_cast<uint32_t*>(&p2);
-  w.w = *reinterpret_cast<uint32_t*>(&p3);
+  w.x = pack2(v[0], v[1], (E*)nullptr);
+  w.y = pack2(v[2], v[3], (E*)nullptr);
+  w.z = pack2(v[4], v[5], (E*)nullptr);
+  w.w = pack2(v[6], v[7], (E*)nullptr);
   *reinterpret_cast<uint4*>(tile + sw128_offset(row, k0)) = w;
 }
 
-__device__ __forceinline__ void sw128_store1(unsigned char* tile, int row, int k, float v) {
+template <typename E = __nv_bfloat16>
+__device__ __forceinline__ void sw128_store1(unsigned char* tile, int row, int k, float v);
+template <>
+__device__ __forceinline__ void sw128_store1<__nv_bfloat16>(unsigned char* tile, int row, int k,
+                                                            float v) {
   *reinterpret_cast<__nv_bfloat16*>(tile + sw128_offset(row, k)) = __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ void sw128_store1<__half>(unsigned char* tile, int row, int k, float v) {
+  *reinterpret_cast<__half*>(tile + sw128_offset(row, k)) = __float2half_rn(v);
 }
 
 // Shared-memory matrix descriptor (sm_100 family): start address >> 4 in bits
@@ -60,11 +77,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1) or fp16 (both 0), both K-major
+// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K=16 step (cta_group::1).

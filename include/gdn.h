@@ -71,6 +71,8 @@ extern "C" {
 #define GDN_FLAG_DUPLICATE 0x8u   /* two active sequences name the same block: both skipped */
 #define GDN_FLAG_TIMEOUT 0x10u    /* a kernel's bounded wait gave up (its results are incomplete) */
 #define GDN_FLAG_HINT 0x20u       /* a sequence is longer than max_seqlen_hint: it was skipped */
+#define GDN_FLAG_RANGE 0x40u      /* a tensor-core operand of the chunked prefill left the fp16
+                                     range (|value| > 65000): that sequence's results are invalid */
 
 typedef struct gdn_pool gdn_pool_t;
 

@@ -9,7 +9,8 @@
  * reads the result back with tcgen05.ld:
  *     D[128][N] = (C ? C : 0) + A[128][K] * B[N][K]^T
  * A, B: bf16 row-major device arrays; C, D: fp32 row-major device arrays
- * (C may be NULL).  N in {64, 128, 192, 256}, K in {64, 128}.  Returns GDN_OK
+ * (C may be NULL).  operand_f16 != 0 converts A and B to fp16 tiles and runs
+ * the fp16 form of the MMA (the chunked kernel's operand type), else bf16.  N in {64, 128, 192, 256}, K in {64, 128}.  Returns GDN_OK
  * or GDN_ERR_NULL / GDN_ERR_DIMS / GDN_ERR_ALIGN / GDN_ERR_CUDA (nothing
  * launched on error).  Stream-ordered, no synchronisation.
  */
@@ -21,7 +22,7 @@ extern "C" {
 #endif
 
 int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, int N, int K,
-                       void* stream);
+                       int operand_f16, void* stream);
 
 #ifdef __cplusplus
 }

@@ -11,13 +11,14 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("N", [64, 128, 192, 256])
 @pytest.mark.parametrize("K", [64, 128])
 @pytest.mark.parametrize("acc", [False, True])
-def test_umma_gemm_matches_torch(N, K, acc):
+@pytest.mark.parametrize("f16", [False, True])
+def test_umma_gemm_matches_torch(N, K, acc, f16):
     g = torch.Generator(device="cuda").manual_seed(N * 1000 + K + acc)
     A = torch.randn(128, K, device="cuda", generator=g).to(torch.bfloat16)
     B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
     C = torch.randn(128, N, device="cuda", generator=g) if acc else None
     D = torch.full((128, N), float("nan"), device="cuda")
-    binding.diag_umma_gemm(A, B, C, D)
+    binding.diag_umma_gemm(A, B, C, D, operand_f16=f16)
     torch.cuda.synchronize()
     ref = A.float() @ B.float().T + (C if acc else 0)
     torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
