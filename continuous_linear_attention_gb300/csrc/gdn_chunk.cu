@@ -48,7 +48,11 @@ constexpr int kThreads = 256;
 constexpr int kLocalCh = 3 * D;  // q, k of the k-head and v of the v-head
 constexpr float kF16Max = 65000.f;
 
-// shared memory map (offsets from a 1024-byte aligned base)
+// shared memory map (offsets from a 1024-byte aligned base).  fp32 row
+// pitches are padded (132, 68 floats) so that the row-parallel float4 stores
+// of the prep and of the A matrix spread over all shared-memory banks.
+constexpr int BVP = 132;               // pitch of beta v rows (floats)
+constexpr int AP = 68;                 // pitch of A and T rows (floats)
 constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]   2 x (128 rows x 128 B)
 constexpr uint32_t OFF_QKH = 32768;    // [q^ ; k^]   2 x (128 x 128 B)
 constexpr uint32_t OFF_S0 = 65536;     // S0          2 x (128 x 128 B)
@@ -56,15 +60,15 @@ constexpr uint32_t OFF_KPT = 98304;    // k'^T        128 x 128 B
 constexpr uint32_t OFF_P = 114688;     // P           64 x 128 B
 constexpr uint32_t OFF_T = 122880;     // T           64 x 128 B
 constexpr uint32_t OFF_RU = 131072;    // R^T, then U^T   128 x 128 B
-constexpr uint32_t OFF_BV = 147456;    // beta v fp32 [64][128]
-constexpr uint32_t OFF_AM = 180224;    // A fp32 [64][64]; then the out tile bf16 [64][128]
-constexpr uint32_t OFF_TS = 196608;    // T fp32 [64][64]
-constexpr uint32_t OFF_Z = 212992;     // blocked-solve scratch fp32 [3][16][16]
-constexpr uint32_t OFF_G = 216064;     // G fp32 [64]
-constexpr uint32_t OFF_BETA = 216320;  // beta fp32 [64]
-constexpr uint32_t OFF_TOT = 216576;   // scan partials [2]
-constexpr uint32_t OFF_W = 216832;     // conv taps fp32 [4][384]
-constexpr uint32_t SMEM_BYTES = 222976 + 1024;
+constexpr uint32_t OFF_BV = 147456;    // beta v fp32 [64][BVP]
+constexpr uint32_t OFF_AM = 181248;    // A fp32 [64][AP]; then the out tile bf16 [64][128]
+constexpr uint32_t OFF_TS = 198656;    // T fp32 [64][AP]
+constexpr uint32_t OFF_Z = 216064;     // blocked-solve scratch fp32 [3][16][16]
+constexpr uint32_t OFF_G = 219136;     // G fp32 [64]
+constexpr uint32_t OFF_BETA = 219392;  // beta fp32 [64]
+constexpr uint32_t OFF_TOT = 219648;   // scan partials [2]
+constexpr uint32_t OFF_W = 219904;     // conv taps fp32 [4][384]
+constexpr uint32_t SMEM_BYTES = 226048 + 1024;
 constexpr uint32_t KB_STRIDE = 16384;  // bytes between K-blocks of a 128-row tile
 
 // tensor memory columns
@@ -203,25 +207,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     const float GC = G[CH - 1];
 
     // ---------------- prep: conv + SiLU + norms -> fp16 tiles (4 threads per token)
+    // Thread part p of token i handles the 8-channel groups p, p+4, p+8, p+12 of
+    // q, of k and of v, so the four threads of a token load adjacent 16-byte
+    // pieces of each input row.
     {
       const int i = tid >> 2;
-      const int part = tid & 3;     // 0,1: q halves, 2,3: k halves; each also 32 v channels
-      const bool isk = part >= 2;
-      const int hsel = part & 1;
+      const int part = tid & 3;
       const bool valid = i < n;
       const int pos = c0 + i;       // position inside the sequence
       const float Gi = G[i];
       const float bi = BETA[i];
-      const int lbase = (isk ? D : 0) + hsel * 64;
-      float qk[64];
-      float ss = 0.f;
+      float y[96];                  // [q groups 0..3 | k groups 0..3 | v groups 0..3] x 8
 #pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
+      for (int gi = 0; gi < 12; ++gi) {
+        const int lc0 = (gi >> 2) * D + ((gi & 3) * 4 + part) * 8;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
         if (valid) {
-          const int lc0 = lbase + g8 * 8;
           const int gc0 = gch(lc0);
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
@@ -230,69 +233,59 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
                                                 : tail_r + (size_t)(KC - 1 + pp) * C + gc0;
             float xv[8];
             load8_bf16(src, xv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += WS[j * kLocalCh + lc0 + e] * xv[e];
+            const float4 w0 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0);
+            const float4 w1 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0 + 4);
+            acc[0] += w0.x * xv[0]; acc[1] += w0.y * xv[1]; acc[2] += w0.z * xv[2]; acc[3] += w0.w * xv[3];
+            acc[4] += w1.x * xv[4]; acc[5] += w1.y * xv[5]; acc[6] += w1.z * xv[6]; acc[7] += w1.w * xv[7];
           }
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[gi * 8 + e] = valid ? silu_f32(acc[e]) : 0.f;
+      }
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        sq += y[e] * y[e];
+        sk += y[32 + e] * y[32 + e];
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+      const float qsc = valid ? rsqrtf(sq + kL2Eps) * inv_sqrt_d : 0.f;
+      const float ksc = valid ? rsqrtf(sk + kL2Eps) : 0.f;
+      const float eG = __expf(Gi);
+      const float ds = __expf(GC - Gi);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int g = m * 4 + part;          // channel group 0..15 inside the head
+        const int kb = g >> 3, k0 = (g & 7) * 8;
+        float a8[8], b8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float yv = valid ? silu_f32(acc[e]) : 0.f;
-          qk[g8 * 8 + e] = yv;
-          ss += yv * yv;
+          a8[e] = y[m * 8 + e] * qsc;          // q~
+          b8[e] = a8[e] * eG;                  // q~ e^G
         }
-      }
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      const float scale = valid ? rsqrtf(ss + kL2Eps) * (isk ? 1.f : inv_sqrt_d) : 0.f;
+        tc::sw128_store8<E>(sm + OFF_QK + kb * KB_STRIDE, i, k0, a8);
+        tc::sw128_store8<E>(sm + OFF_QKH + kb * KB_STRIDE, i, k0, b8);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) qk[e] *= scale;
-      const int trow = (isk ? CH : 0) + i;
-      const float rs = isk ? bi * __expf(Gi) : __expf(Gi);
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        float h8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) h8[e] = qk[g8 * 8 + e] * rs;
-        tc::sw128_store8<E>(sm + OFF_QK + hsel * KB_STRIDE, trow, g8 * 8, qk + g8 * 8);
-        tc::sw128_store8<E>(sm + OFF_QKH + hsel * KB_STRIDE, trow, g8 * 8, h8);
-      }
-      if (isk) {
+        for (int e = 0; e < 8; ++e) {
+          a8[e] = y[32 + m * 8 + e] * ksc;     // k~
+          b8[e] = a8[e] * (bi * eG);           // k~ beta e^G
+        }
+        tc::sw128_store8<E>(sm + OFF_QK + kb * KB_STRIDE, CH + i, k0, a8);
+        tc::sw128_store8<E>(sm + OFF_QKH + kb * KB_STRIDE, CH + i, k0, b8);
         // (k~ e^{G_C - G_i})^T : column i of the 128-row tile
-        const float ds = __expf(GC - Gi);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) tc::sw128_store1<E>(sm + OFF_KPT, hsel * 64 + e, i, qk[e] * ds);
-      }
-      // beta * v for this thread's 32 v channels
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        const int vc = part * 32 + g8 * 8;
-        if (valid) {
-          const int lc0 = 2 * D + vc;
-          const int gc0 = gch(lc0);
-#pragma unroll
-          for (int j = 0; j < KC; ++j) {
-            const int pp = pos - (KC - 1) + j;
-            const __nv_bfloat16* src = pp >= 0 ? x + (size_t)(seq0 + pp) * C + gc0
-                                                : tail_r + (size_t)(KC - 1 + pp) * C + gc0;
-            float xv[8];
-            load8_bf16(src, xv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += WS[j * kLocalCh + lc0 + e] * xv[e];
-          }
-        }
+        for (int e = 0; e < 8; ++e) tc::sw128_store1<E>(sm + OFF_KPT, g * 8 + e, i, a8[e] * ds);
+        // beta v
         float4 o0, o1;
-        o0.x = valid ? bi * silu_f32(acc[0]) : 0.f;
-        o0.y = valid ? bi * silu_f32(acc[1]) : 0.f;
-        o0.z = valid ? bi * silu_f32(acc[2]) : 0.f;
-        o0.w = valid ? bi * silu_f32(acc[3]) : 0.f;
-        o1.x = valid ? bi * silu_f32(acc[4]) : 0.f;
-        o1.y = valid ? bi * silu_f32(acc[5]) : 0.f;
-        o1.z = valid ? bi * silu_f32(acc[6]) : 0.f;
-        o1.w = valid ? bi * silu_f32(acc[7]) : 0.f;
-        *reinterpret_cast<float4*>(BV + i * D + vc) = o0;
-        *reinterpret_cast<float4*>(BV + i * D + vc + 4) = o1;
+        o0.x = bi * y[64 + m * 8 + 0]; o0.y = bi * y[64 + m * 8 + 1];
+        o0.z = bi * y[64 + m * 8 + 2]; o0.w = bi * y[64 + m * 8 + 3];
+        o1.x = bi * y[64 + m * 8 + 4]; o1.y = bi * y[64 + m * 8 + 5];
+        o1.z = bi * y[64 + m * 8 + 6]; o1.w = bi * y[64 + m * 8 + 7];
+        *reinterpret_cast<float4*>(BV + i * BVP + g * 8) = o0;
+        *reinterpret_cast<float4*>(BV + i * BVP + g * 8 + 4) = o1;
       }
     }
 
@@ -364,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
           a4.y = j + 1 < i ? bi * __expf(Gi - G[j + 1]) * xr[j4 * 4 + 1] : 0.f;
           a4.z = j + 2 < i ? bi * __expf(Gi - G[j + 2]) * xr[j4 * 4 + 2] : 0.f;
           a4.w = j + 3 < i ? bi * __expf(Gi - G[j + 3]) * xr[j4 * 4 + 3] : 0.f;
-          *reinterpret_cast<float4*>(AM + i * CH + j) = a4;
+          *reinterpret_cast<float4*>(AM + i * AP + j) = a4;
         }
       }
       float yr[32];
@@ -377,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = chalf * 32 + g8 * 8 + e;
-          v8[e] = BV[i * D + v] - yr[g8 * 8 + e];
+          v8[e] = BV[i * BVP + v] - yr[g8 * 8 + e];
         }
         range_bad |= out_of_f16(v8, 8);
         tc::sw128_store8<E>(sm + OFF_RU, v, chalf * 32 + g8 * 8, v8);
@@ -387,17 +380,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     // ---------------- T = (I + A)^{-1}: diagonal 16 x 16 blocks, column per thread
     if (tid < CH) {
       const int b = tid >> 4, m = tid & 15;
-      const float* Ab = AM + (16 * b) * CH + 16 * b;
+      const float* Ab = AM + (16 * b) * AP + 16 * b;
       float col[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
         float acc = r == m ? 1.f : 0.f;
 #pragma unroll
-        for (int j = 0; j < r; ++j) acc -= Ab[r * CH + j] * col[j];
+        for (int j = 0; j < r; ++j) acc -= Ab[r * AP + j] * col[j];
         col[r] = acc;
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) TS[(16 * b + r) * CH + 16 * b + m] = col[r];
+      for (int r = 0; r < 16; ++r) TS[(16 * b + r) * AP + 16 * b + m] = col[r];
     }
     __syncthreads();
     // off-diagonal blocks, level L = i - j: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
@@ -409,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
         for (int k = j; k < i; ++k) {
 #pragma unroll
           for (int q = 0; q < 16; ++q)
-            z += AM[(16 * i + rr) * CH + 16 * k + q] * TS[(16 * k + q) * CH + 16 * j + cc];
+            z += AM[(16 * i + rr) * AP + 16 * k + q] * TS[(16 * k + q) * AP + 16 * j + cc];
         }
         Z[e] = z;
       }
@@ -418,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
         const int j = e >> 8, i = j + Lv, rr = (e >> 4) & 15, cc = e & 15;
         float t = 0.f;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) t -= TS[(16 * i + rr) * CH + 16 * i + q] * Z[(e & ~255) + q * 16 + cc];
-        TS[(16 * i + rr) * CH + 16 * j + cc] = t;
+        for (int q = 0; q < 16; ++q) t -= TS[(16 * i + rr) * AP + 16 * i + q] * Z[(e & ~255) + q * 16 + cc];
+        TS[(16 * i + rr) * AP + 16 * j + cc] = t;
       }
       __syncthreads();
     }
@@ -432,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int j = c8 * 8 + e;
-        v8[e] = (j >> 4) <= (i >> 4) ? TS[i * CH + j] : 0.f;
+        v8[e] = (j >> 4) <= (i >> 4) ? TS[i * AP + j] : 0.f;
       }
       range_bad |= out_of_f16(v8, 8);
       tc::sw128_store8<E>(sm + OFF_T, i, c8 * 8, v8);
