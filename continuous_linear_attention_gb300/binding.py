@@ -33,6 +33,7 @@ EXPORTED = [
     "gdn_state_pool_layout",
     "gdn_state_pool_copy_block",
     "gdn_varlen_forward",
+    "gdn_varlen_forward_noalloc",
     "gdn_get_error",
     "gdn_pool_set_timing_events",
     "gdn_status_string",
@@ -75,6 +76,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_state_pool_copy_block.argtypes = [P, I, I, I, P]
     lib.gdn_varlen_forward.argtypes = [P, I, P, P, P, P, P, P, ctypes.POINTER(Weights), P,
                                        I, I, I, P]
+    lib.gdn_varlen_forward_noalloc.argtypes = [P, S] + [I] * 8 + [S, I] + [P] * 6 + [
+        ctypes.POINTER(Weights), P, I, I, I, P, P]
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
     lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, I, P]
@@ -199,3 +202,18 @@ def diag_umma_gemm(A, B, C, D, operand_f16=False, stream=None) -> None:
     _check(load().gdn_diag_umma_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K,
                                      1 if operand_f16 else 0, _stream(stream)),
            "gdn_diag_umma_gemm")
+
+
+def varlen_forward_noalloc(pool_mem, num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align,
+                           layer, x_qkv, a, b, cu_seqlens, state_block_idx, has_past, conv_w,
+                           A_log, dt_bias, out, T, N, max_seqlen_hint=0, flags_out=None,
+                           stream=None) -> None:
+    """gdn_varlen_forward_noalloc: the forward on caller-owned pool memory
+    (a CUDA uint8 tensor or a raw device pointer), allocating nothing."""
+    nbytes = pool_mem.numel() * pool_mem.element_size() if hasattr(pool_mem, "numel") else 0
+    w = Weights(_ptr(conv_w), _ptr(A_log), _ptr(dt_bias))
+    _check(load().gdn_varlen_forward_noalloc(
+        _ptr(pool_mem), nbytes, num_blocks, num_layers, Hk, Hv, dk, dv, K, act_code(act),
+        block_align, layer, _ptr(x_qkv), _ptr(a), _ptr(b), _ptr(cu_seqlens),
+        _ptr(state_block_idx), _ptr(has_past), ctypes.byref(w), _ptr(out), T, N,
+        max_seqlen_hint, _ptr(flags_out), _stream(stream)), "gdn_varlen_forward_noalloc")

@@ -158,6 +158,39 @@ int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const voi
                        const uint8_t* has_past, const gdn_weights_t* weights, void* out, int T,
                        int N, int max_seqlen_hint, void* stream);
 
+/* gdn_varlen_forward for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this entry point: it exists for engines that
+ * plan every byte of device memory ahead and forbid runtime allocation, and
+ * for code that runs under another allocator's budget, which cannot use
+ * gdn_state_pool_create (it calls cudaMalloc for the pool's work area).
+ * Same computation, data errors and output contract as gdn_varlen_forward,
+ * without a pool handle:
+ *   pool_mem, pool_bytes : caller-owned device memory of a pool with these
+ *                          dimensions, laid out as gdn_state_pool_layout_for
+ *                          describes (256-byte aligned, pool_bytes >= its
+ *                          total_bytes); the caller keeps block 0 of every
+ *                          layer zeroed (the trash block)
+ *   num_blocks .. block_align : the pool's dimensions (as for
+ *                          gdn_state_pool_create)
+ *   layer, x_qkv .. max_seqlen_hint : as for gdn_varlen_forward
+ *   flags_out            : optional device uint32 receiving the GDN_FLAG_*
+ *                          bits raised by this call (NULL: not reported)
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * The scheduler's work area is a static device array sized for pools of at
+ * most 4096 blocks (about 80 KiB, held on every GPU that loads the library
+ * until the process exits); num_blocks > 4096 returns GDN_ERR_RANGE.  Every
+ * call on a device shares that array, so calls whose work overlaps on the
+ * GPU race: order them on one stream.  The first call on each device looks
+ * up the array's device address, so make it before any stream capture on
+ * that device.  Does not synchronise. */
+int gdn_varlen_forward_noalloc(void* pool_mem, size_t pool_bytes, int num_blocks, int num_layers,
+                               int num_k_heads, int num_v_heads, int d_k, int d_v, int conv_k,
+                               int act_dtype, size_t block_align, int layer, const void* x_qkv,
+                               const void* a, const void* b, const int32_t* cu_seqlens,
+                               const int32_t* state_block_idx, const uint8_t* has_past,
+                               const gdn_weights_t* weights, void* out, int T, int N,
+                               int max_seqlen_hint, uint32_t* flags_out, void* stream);
+
 /* Read (and optionally clear) the OR of GDN_FLAG_* raised by earlier forwards
  * on one layer (layer < 0: OR over all layers).  Synchronises `stream`; not
  * for the hot path. */
