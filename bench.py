@@ -355,7 +355,7 @@ def main():
         value = tokens / (elapsed_ms / 1e3)
         alg_bytes = decode_bytes(wl)
         achieved = alg_bytes / (kern_mean_ms / 1e3) / 1e9
-        traffic = traffic_record("gdn_recurrent.cu")
+        traffic = traffic_record("gdn_decode.cu")
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,

@@ -10,17 +10,20 @@
 // Per chunk, with G_i the inclusive cumulative gate inside the chunk, beta_i
 // the write strength, q~/k~ the normalised rows and S0 the state at the chunk
 // start (S is d_v x d_k, S[v][k]):
-//   prep (CUDA cores): conv + SiLU + L2 norms + gates; fp16 tiles
-//        [q~ ; k~], [q~ e^G ; k~ beta e^G], (k~ e^{G_C - G})^T, fp32 beta v
+//   prep (CUDA cores): conv + SiLU + L2 norms + gates from the chunk's x rows,
+//        which 2-D TMA copies staged in shared memory while the previous chunk
+//        ran; fp16 tiles [q~ ; k~], (k~ e^{G_C - G})^T, beta v
 //   state hand-over: S0 -> fp16 tile; TMEM S <- e^{G_C} S0
 //   MMA  X  = [q~ ; k~] k~^T                     (QK^T and KK^T, 128 x 64)
-//   MMA  [Oacc | Y] = S0 [q~ e^G ; k~ beta e^G]^T (128 x 128)
+//   MMA  [Oq | Yk] = S0 [q~ ; k~]^T              (S0 q~_i and S0 k~_i, 128 x 128)
 //   CUDA A_ij = beta_i e^{G_i-G_j} (k~_i.k~_j) (j<i);  P_ij = (q~_i.k~_j) e^{G_i-G_j} (j<=i)
-//        R^T = (beta v)^T - Y;  T = (I + A)^{-1} (blocked forward substitution:
-//        16 x 16 diagonal blocks, then the off-diagonal blocks level by level)
+//        R^T[.,i] = beta_i v_i - beta_i e^{G_i} Yk[.,i];  T = (I + A)^{-1} (blocked
+//        forward substitution: 16 x 16 diagonal blocks, then the off-diagonal
+//        blocks level by level)
 //   MMA  U^T = R^T T^T          (the per-token updates u_i, 128 x 64)
-//   MMA  Oacc += U^T P^T        (o_i = e^{G_i} S0 q~_i + sum_{j<=i} e^{G_i-G_j}(q~_i.k~_j) u_j)
-//   MMA  S    += U^T (k~ e^{G_C-G})  (S_C = e^{G_C} S0 + sum_j e^{G_C-G_j} u_j k~_j^T)
+//   MMA  O2  = U^T P^T
+//        o_i = e^{G_i} Oq[.,i] + O2[.,i] = e^{G_i} S0 q~_i + sum_{j<=i} e^{G_i-G_j}(q~_i.k~_j) u_j
+//   MMA  S  += U^T (k~ e^{G_C-G})  (S_C = e^{G_C} S0 + sum_j e^{G_C-G_j} u_j k~_j^T)
 // MMA operands are fp16 (same tensor-core rate as bf16, 3 more mantissa bits:
 // the bf16 version of this kernel sat at ~4.5e-3 relative error on slowly
 // decaying states).  An operand outside the fp16 range raises GDN_FLAG_RANGE.
@@ -33,6 +36,8 @@
 // The conv state is only read here; the new conv states of these sequences
 // are written by tail_update_kernel, launched after this kernel, so no chain
 // can see another chain's write.
+#include <cuda.h>
+
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 #include "gdn_tc.cuh"
@@ -48,31 +53,37 @@ constexpr int kThreads = 256;
 constexpr int kLocalCh = 3 * D;  // q, k of the k-head and v of the v-head
 constexpr float kF16Max = 65000.f;
 
-// shared memory map (offsets from a 1024-byte aligned base).  fp32 row
-// pitches are padded (132, 68 floats) so that the row-parallel float4 stores
-// of the prep and of the A matrix spread over all shared-memory banks.
-constexpr int BVP = 132;               // pitch of beta v rows (floats)
+// shared memory map (offsets from a 1024-byte aligned base).  Row pitches of
+// the row-parallel buffers are padded (fp32 68, fp16 136, bf16 392 elements)
+// so that rows spread over all shared-memory banks.
 constexpr int AP = 68;                 // pitch of A and T rows (floats)
+constexpr int BVP = 136;               // pitch of beta v rows (halves)
+constexpr int XROWS = CH + KC - 1;     // 67 staged rows: 3 halo + 64 chunk rows
+constexpr uint32_t XSUB = 9216;        // one staged box: 72 rows x 128 B (64 channels), swizzled
+constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
 constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]   2 x (128 rows x 128 B)
-constexpr uint32_t OFF_QKH = 32768;    // [q^ ; k^]   2 x (128 x 128 B)
-constexpr uint32_t OFF_S0 = 65536;     // S0          2 x (128 x 128 B)
-constexpr uint32_t OFF_KPT = 98304;    // k'^T        128 x 128 B
-constexpr uint32_t OFF_P = 114688;     // P           64 x 128 B
-constexpr uint32_t OFF_T = 122880;     // T           64 x 128 B
-constexpr uint32_t OFF_RU = 131072;    // R^T, then U^T   128 x 128 B
-constexpr uint32_t OFF_BV = 147456;    // beta v fp32 [64][BVP]
-constexpr uint32_t OFF_AM = 181248;    // A fp32 [64][AP]; then the out tile bf16 [64][128]
-constexpr uint32_t OFF_TS = 198656;    // T fp32 [64][AP]
-constexpr uint32_t OFF_Z = 216064;     // blocked-solve scratch fp32 [3][16][16]
-constexpr uint32_t OFF_G = 219136;     // G fp32 [64]
-constexpr uint32_t OFF_BETA = 219392;  // beta fp32 [64]
-constexpr uint32_t OFF_TOT = 219648;   // scan partials [2]
-constexpr uint32_t OFF_W = 219904;     // conv taps fp32 [4][384]
-constexpr uint32_t SMEM_BYTES = 226048 + 1024;
+constexpr uint32_t OFF_S0 = 32768;     // S0 tile 2 x (128 x 128 B); during the solve: T fp32, Z
+constexpr uint32_t OFF_TS = OFF_S0;    // T fp32 [64][AP]
+constexpr uint32_t OFF_Z = OFF_S0 + 17408;  // blocked-solve scratch fp32 [3][16][16]
+constexpr uint32_t OFF_KPT = 65536;    // k'^T        128 x 128 B
+constexpr uint32_t OFF_P = 81920;      // P           64 x 128 B
+constexpr uint32_t OFF_T = 90112;      // T           64 x 128 B
+constexpr uint32_t OFF_RU = 98304;     // R^T, then U^T   128 x 128 B
+constexpr uint32_t OFF_BV = 114688;    // beta v fp16 [64][BVP]
+constexpr uint32_t OFF_AM = 132096;    // A fp32 [64][AP]; then the out tile bf16 [64][128]
+constexpr uint32_t OFF_XT = 150528;    // 6 staged x boxes (q0 q1 k0 k1 v0 v1), 1024-aligned
+constexpr uint32_t OFF_G = 205824;     // G fp32 [64]
+constexpr uint32_t OFF_BETA = 206080;  // beta fp32 [64]
+constexpr uint32_t OFF_EG = 206336;    // e^{G} fp32 [64]
+constexpr uint32_t OFF_F = 206592;     // beta e^{G} fp32 [64]
+constexpr uint32_t OFF_TOT = 206848;   // scan partials [2]
+constexpr uint32_t OFF_DS = 206864;    // e^{G_C - G} fp32 [64]
+constexpr uint32_t OFF_W = 207120;     // conv taps fp32 [4][384]
+constexpr uint32_t SMEM_BYTES = 213264 + 1024;
 constexpr uint32_t KB_STRIDE = 16384;  // bytes between K-blocks of a 128-row tile
 
 // tensor memory columns
-constexpr uint32_t TM_X = 0, TM_OACC = 64, TM_Y = 128, TM_UT = 192, TM_S = 256;
+constexpr uint32_t TM_X = 0, TM_OQ = 64, TM_Y = 128, TM_UT = 192, TM_S = 256, TM_O2 = 384;
 constexpr uint32_t TM_COLS = 512;
 
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
@@ -99,10 +110,12 @@ __device__ __forceinline__ bool out_of_f16(const float* v, int n) {
   return bad;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar;   // MMA completion
+  __shared__ uint64_t xbar;  // staged x rows
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
   __shared__ int s_chain;
@@ -121,18 +134,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
 
   float* G = reinterpret_cast<float*>(sm + OFF_G);
   float* BETA = reinterpret_cast<float*>(sm + OFF_BETA);
+  float* EG = reinterpret_cast<float*>(sm + OFF_EG);
+  float* F = reinterpret_cast<float*>(sm + OFF_F);
+  float* DSC = reinterpret_cast<float*>(sm + OFF_DS);
   float* WS = reinterpret_cast<float*>(sm + OFF_W);
-  float* BV = reinterpret_cast<float*>(sm + OFF_BV);
+  __half* BV = reinterpret_cast<__half*>(sm + OFF_BV);
   float* AM = reinterpret_cast<float*>(sm + OFF_AM);
   __nv_bfloat16* OT = reinterpret_cast<__nv_bfloat16*>(sm + OFF_AM);
+  unsigned char* XT = sm + OFF_XT;
   float* TS = reinterpret_cast<float*>(sm + OFF_TS);
   float* Z = reinterpret_cast<float*>(sm + OFF_Z);
   float* TOT = reinterpret_cast<float*>(sm + OFF_TOT);
   const uint32_t sbase = smem_u32(sm);
 
-  // ---- set-up: barrier, TMEM (kept for every chain this CTA runs)
+  // ---- set-up: barriers, TMEM (kept for every chain this CTA runs)
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&xbar, 1);
     fence_mbar_init();
   }
   if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
@@ -144,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
   const uint32_t lane = (uint32_t)(tid & 96) << 16;
   const int r128 = tid & 127;  // TMEM row (lane) of this thread
   const int chalf = tid >> 7;  // which half of the columns this thread handles
-  uint32_t phase = 0;
+  uint32_t phase = 0, xphase = 0;
   const float inv_sqrt_d = rsqrtf((float)D);
   bool failed = false;
   bool range_bad = false;
@@ -171,6 +189,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     return lc < D ? kh * D + lc
                   : (lc < 2 * D ? Hk * D + kh * D + (lc - D) : 2 * Hk * D + h * D + (lc - 2 * D));
   };
+  // Stage the x rows of chunk cc (packed rows seq0 + cc*64 - 3 .. + 63) of
+  // this chain's q, k and v channels into XT: six 64-channel x 67-row TMA
+  // boxes, 128-byte swizzled.  Rows outside the sequence are loaded too but
+  // never used (the first chunk's halo comes from the conv state).  Thread 0.
+  auto stage_x = [&](int cc) {
+    const int r0 = seq0 + cc * CH - (KC - 1);
+    mbar_arrive_expect_tx(&xbar, 6u * XBOX_BYTES);
+#pragma unroll
+    for (int b6 = 0; b6 < 6; ++b6) tma_load_2d(XT + b6 * XSUB, &tmx, gch(b6 * 64), r0, &xbar);
+  };
+  // gate inputs of chunk cc, token tid (threads < 64)
+  auto load_gates = [&](int cc, float& a_, float& b_) {
+    const int cc0 = cc * CH;
+    if (tid < CH && cc0 + tid < L) {
+      const size_t row = (size_t)(seq0 + cc0 + tid);
+      a_ = __bfloat162float(av[row * Hv + h]);
+      b_ = __bfloat162float(bv[row * Hv + h]);
+    }
+  };
+  if (tid == 0) stage_x(0);
+  float a_nx = 0.f, b_nx = 0.f;
+  load_gates(0, a_nx, b_nx);
   for (int lc = tid; lc < kLocalCh; lc += kThreads) {
     const int gc = gch(lc);
 #pragma unroll
@@ -184,13 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
   for (int c = 0; c < n_chunks; ++c) {
     const int c0 = c * CH;                 // chunk start inside the sequence
     const int n = min(CH, L - c0);         // valid tokens
-    // ---------------- prep: gates and their in-chunk cumulative sum
+    // ---------------- gates and their in-chunk cumulative sum
     if (tid < CH) {
       float g = 0.f, beta = 0.f;
       if (tid < n) {
-        const size_t row = (size_t)(seq0 + c0 + tid);
-        g = A_neg * softplus_f32(__bfloat162float(av[row * Hv + h]) + dtb);
-        beta = sigmoid_f32(__bfloat162float(bv[row * Hv + h]));
+        g = A_neg * softplus_f32(a_nx + dtb);
+        beta = sigmoid_f32(b_nx);
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -202,90 +241,96 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
       BETA[tid] = beta;
     }
     __syncthreads();
-    if (tid >= 32 && tid < CH) G[tid] += TOT[0];
-    __syncthreads();
+    if (tid < CH) {
+      const float Gi = G[tid] + (tid >= 32 ? TOT[0] : 0.f);
+      G[tid] = Gi;
+      const float e = __expf(Gi);
+      EG[tid] = e;
+      F[tid] = BETA[tid] * e;
+    }
+    if (!cta_wait(&xbar, xphase, &flag)) { failed = true; break; }  // also publishes G
+    xphase ^= 1;
     const float GC = G[CH - 1];
+    if (tid < CH) DSC[tid] = __expf(GC - G[tid]);
 
-    // ---------------- prep: conv + SiLU + norms -> fp16 tiles (4 threads per token)
-    // Thread part p of token i handles the 8-channel groups p, p+4, p+8, p+12 of
-    // q, of k and of v, so the four threads of a token load adjacent 16-byte
-    // pieces of each input row.
+    // ---------------- prep: conv + SiLU + norms -> fp16 tiles
+    // Thread (tq, g) computes 8-channel group g of q, of k and of v for the four
+    // tokens 4tq .. 4tq+3 with a sliding window over 7 staged rows; the 16
+    // threads of a token quad reduce the norms with shuffles.
     {
-      const int i = tid >> 2;
-      const int part = tid & 3;
-      const bool valid = i < n;
-      const int pos = c0 + i;       // position inside the sequence
-      const float Gi = G[i];
-      const float bi = BETA[i];
-      float y[96];                  // [q groups 0..3 | k groups 0..3 | v groups 0..3] x 8
+      const int tq = tid >> 4, g = tid & 15;
+      const int i0 = 4 * tq;
 #pragma unroll
-      for (int gi = 0; gi < 12; ++gi) {
-        const int lc0 = (gi >> 2) * D + ((gi & 3) * 4 + part) * 8;
-        float acc[8];
+      for (int part = 0; part < 3; ++part) {   // 0: q, 1: k, 2: v
+        const int lc0 = part * D + g * 8;
+        const int sub = lc0 >> 6, cc = lc0 & 63;
+        float w[KC][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        if (valid) {
-          const int gc0 = gch(lc0);
+        for (int j = 0; j < KC; ++j) {
+          const float4 w0 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0);
+          const float4 w1 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0 + 4);
+          w[j][0] = w0.x; w[j][1] = w0.y; w[j][2] = w0.z; w[j][3] = w0.w;
+          w[j][4] = w1.x; w[j][5] = w1.y; w[j][6] = w1.z; w[j][7] = w1.w;
+        }
+        float acc[4][8];
 #pragma unroll
-          for (int j = 0; j < KC; ++j) {
-            const int pp = pos - (KC - 1) + j;
-            const __nv_bfloat16* src = pp >= 0 ? x + (size_t)(seq0 + pp) * C + gc0
-                                                : tail_r + (size_t)(KC - 1 + pp) * C + gc0;
-            float xv[8];
-            load8_bf16(src, xv);
-            const float4 w0 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0);
-            const float4 w1 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0 + 4);
-            acc[0] += w0.x * xv[0]; acc[1] += w0.y * xv[1]; acc[2] += w0.z * xv[2]; acc[3] += w0.w * xv[3];
-            acc[4] += w1.x * xv[4]; acc[5] += w1.y * xv[5]; acc[6] += w1.z * xv[6]; acc[7] += w1.w * xv[7];
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < 4 + KC - 1; ++rr) {
+          const int r = i0 + rr;    // staged row; rows < 3 of the first chunk are the conv state
+          float xv[8];
+          if (c == 0 && r < KC - 1)
+            load8_bf16(tail_r + (size_t)r * C + gch(lc0), xv);
+          else
+            load8_bf16(reinterpret_cast<const __nv_bfloat16*>(XT + sub * XSUB + tc::sw128_offset(r, cc)), xv);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int j = rr - t;   // tap of this row for token i0 + t
+            if (j >= 0 && j < KC) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[t][e] += w[j][e] * xv[e];
+            }
           }
         }
+        float y[4][8], ss[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[gi * 8 + e] = valid ? silu_f32(acc[e]) : 0.f;
-      }
-      float sq = 0.f, sk = 0.f;
+        for (int t = 0; t < 4; ++t) {
+          const bool valid = i0 + t < n;
+          ss[t] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        sq += y[e] * y[e];
-        sk += y[32 + e] * y[32 + e];
-      }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-      const float qsc = valid ? rsqrtf(sq + kL2Eps) * inv_sqrt_d : 0.f;
-      const float ksc = valid ? rsqrtf(sk + kL2Eps) : 0.f;
-      const float eG = __expf(Gi);
-      const float ds = __expf(GC - Gi);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int g = m * 4 + part;          // channel group 0..15 inside the head
-        const int kb = g >> 3, k0 = (g & 7) * 8;
-        float a8[8], b8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          a8[e] = y[m * 8 + e] * qsc;          // q~
-          b8[e] = a8[e] * eG;                  // q~ e^G
+          for (int e = 0; e < 8; ++e) {
+            y[t][e] = valid ? silu_f32(acc[t][e]) : 0.f;
+            ss[t] += y[t][e] * y[t][e];
+          }
         }
-        tc::sw128_store8<E>(sm + OFF_QK + kb * KB_STRIDE, i, k0, a8);
-        tc::sw128_store8<E>(sm + OFF_QKH + kb * KB_STRIDE, i, k0, b8);
+        if (part < 2) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          a8[e] = y[32 + m * 8 + e] * ksc;     // k~
-          b8[e] = a8[e] * (bi * eG);           // k~ beta e^G
+          for (int t = 0; t < 4; ++t) {
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+            const bool valid = i0 + t < n;
+            const float sc = valid ? rsqrtf(ss[t] + kL2Eps) * (part == 0 ? inv_sqrt_d : 1.f) : 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[t][e] *= sc;
+            const int i = i0 + t;
+            tc::sw128_store8<E>(sm + OFF_QK + (g >> 3) * KB_STRIDE, part * CH + i, (g & 7) * 8, y[t]);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const float bi = BETA[i];
+            uint4 wv;
+            wv.x = tc::pack2(bi * y[t][0], bi * y[t][1], (__half*)nullptr);
+            wv.y = tc::pack2(bi * y[t][2], bi * y[t][3], (__half*)nullptr);
+            wv.z = tc::pack2(bi * y[t][4], bi * y[t][5], (__half*)nullptr);
+            wv.w = tc::pack2(bi * y[t][6], bi * y[t][7], (__half*)nullptr);
+            range_bad |= out_of_f16(y[t], 8);
+            *reinterpret_cast<uint4*>(BV + i * BVP + g * 8) = wv;
+          }
         }
-        tc::sw128_store8<E>(sm + OFF_QK + kb * KB_STRIDE, CH + i, k0, a8);
-        tc::sw128_store8<E>(sm + OFF_QKH + kb * KB_STRIDE, CH + i, k0, b8);
-        // (k~ e^{G_C - G_i})^T : column i of the 128-row tile
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tc::sw128_store1<E>(sm + OFF_KPT, g * 8 + e, i, a8[e] * ds);
-        // beta v
-        float4 o0, o1;
-        o0.x = bi * y[64 + m * 8 + 0]; o0.y = bi * y[64 + m * 8 + 1];
-        o0.z = bi * y[64 + m * 8 + 2]; o0.w = bi * y[64 + m * 8 + 3];
-        o1.x = bi * y[64 + m * 8 + 4]; o1.y = bi * y[64 + m * 8 + 5];
-        o1.z = bi * y[64 + m * 8 + 6]; o1.w = bi * y[64 + m * 8 + 7];
-        *reinterpret_cast<float4*>(BV + i * BVP + g * 8) = o0;
-        *reinterpret_cast<float4*>(BV + i * BVP + g * 8 + 4) = o1;
       }
     }
 
@@ -320,15 +365,36 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
       tc::fence_after_sync();
       tc::mma_tile(tmem + TM_X, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
                    tc::idesc_f16_f32(128, 64), false);
-      tc::mma_tile(tmem + TM_OACC, sbase + OFF_S0, KB_STRIDE, sbase + OFF_QKH, KB_STRIDE, 2,
+      tc::mma_tile(tmem + TM_OQ, sbase + OFF_S0, KB_STRIDE, sbase + OFF_QK, KB_STRIDE, 2,
                    tc::idesc_f16_f32(128, 128), false);
       tc::commit(&bar);
+    }
+    // the staged rows are consumed: bring in the next chunk's while this one runs
+    if (c + 1 < n_chunks) {
+      if (tid == 0) stage_x(c + 1);
+      load_gates(c + 1, a_nx, b_nx);
+    }
+    // while the tensor core runs: (k~ e^{G_C - G_i})^T, row k of the 128-row tile
+    // read as a column of the k~ tile (thread k, half of the tokens each)
+    {
+      const int k = r128;
+      const unsigned char* ksrc = sm + OFF_QK + (k >> 6) * KB_STRIDE;
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const int i0 = chalf * 32 + g8 * 8;
+        float v8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          v8[e] = __half2float(*reinterpret_cast<const __half*>(
+                      ksrc + tc::sw128_offset(CH + i0 + e, k & 63))) * DSC[i0 + e];
+        tc::sw128_store8<E>(sm + OFF_KPT, k, i0, v8);
+      }
     }
     if (!cta_wait(&bar, phase, &flag)) { failed = true; break; }
     phase ^= 1;
     tc::fence_after_sync();
 
-    // ---------------- A, P from X; R^T from Y (each thread: one row, 32 columns)
+    // ---------------- A, P from X; R^T from Yk (each thread: one row, 32 columns)
     {
       float xr[32];
       tc::tmem_ld32(tmem + lane + TM_X + chalf * 32, xr);
@@ -370,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = chalf * 32 + g8 * 8 + e;
-          v8[e] = BV[i * BVP + v] - yr[g8 * 8 + e];
+          v8[e] = __half2float(BV[i * BVP + v]) - F[i] * yr[g8 * 8 + e];
         }
         range_bad |= out_of_f16(v8, 8);
         tc::sw128_store8<E>(sm + OFF_RU, v, chalf * 32 + g8 * 8, v8);
@@ -393,26 +459,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
       for (int r = 0; r < 16; ++r) TS[(16 * b + r) * AP + 16 * b + m] = col[r];
     }
     __syncthreads();
-    // off-diagonal blocks, level L = i - j: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+    // off-diagonal blocks, level L = i - j: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj,
+    // four adjacent columns per thread
     for (int Lv = 1; Lv < 4; ++Lv) {
-      const int ne = (4 - Lv) * 256;
-      for (int e = tid; e < ne; e += kThreads) {
-        const int j = e >> 8, i = j + Lv, rr = (e >> 4) & 15, cc = e & 15;
-        float z = 0.f;
+      const int ne = (4 - Lv) * 64;
+      if (tid < ne) {
+        const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = j; k < i; ++k) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            z += AM[(16 * i + rr) * AP + 16 * k + q] * TS[(16 * k + q) * AP + 16 * j + cc];
+          for (int q = 0; q < 16; ++q) {
+            const float a = AM[(16 * i + rr) * AP + 16 * k + q];
+            const float4 t4 = *reinterpret_cast<const float4*>(TS + (16 * k + q) * AP + 16 * j + c4);
+            z.x += a * t4.x; z.y += a * t4.y; z.z += a * t4.z; z.w += a * t4.w;
+          }
         }
-        Z[e] = z;
+        *reinterpret_cast<float4*>(Z + tid * 4) = z;
       }
       __syncthreads();
-      for (int e = tid; e < ne; e += kThreads) {
-        const int j = e >> 8, i = j + Lv, rr = (e >> 4) & 15, cc = e & 15;
-        float t = 0.f;
+      if (tid < ne) {
+        const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const float* zb = Z + (tid & ~63) * 4;   // this block's Z, [16][16]
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) t -= TS[(16 * i + rr) * AP + 16 * i + q] * Z[(e & ~255) + q * 16 + cc];
-        TS[(16 * i + rr) * AP + 16 * j + cc] = t;
+        for (int q = 0; q < 16; ++q) {
+          const float a = TS[(16 * i + rr) * AP + 16 * i + q];
+          const float4 z4 = *reinterpret_cast<const float4*>(zb + q * 16 + c4);
+          t.x -= a * z4.x; t.y -= a * z4.y; t.z -= a * z4.z; t.w -= a * z4.w;
+        }
+        *reinterpret_cast<float4*>(TS + (16 * i + rr) * AP + 16 * j + c4) = t;
       }
       __syncthreads();
     }
@@ -457,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     __syncthreads();
     if (tid == 0) {
       tc::fence_after_sync();
-      tc::mma_tile(tmem + TM_OACC, sbase + OFF_RU, 0, sbase + OFF_P, 0, 1, tc::idesc_f16_f32(128, 64),
-                   true);
+      tc::mma_tile(tmem + TM_O2, sbase + OFF_RU, 0, sbase + OFF_P, 0, 1, tc::idesc_f16_f32(128, 64),
+                   false);
       tc::mma_tile(tmem + TM_S, sbase + OFF_RU, 0, sbase + OFF_KPT, 0, 1,
                    tc::idesc_f16_f32(128, 128), true);
       tc::commit(&bar);
@@ -468,11 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(FwdParams p) {
     tc::fence_after_sync();
     // ---------------- outputs of the chunk, transposed through shared memory
     {
-      float orow[32];
-      tc::tmem_ld32(tmem + lane + TM_OACC + chalf * 32, orow);
+      float oq[32], o2[32];
+      tc::tmem_ld32(tmem + lane + TM_OQ + chalf * 32, oq);
+      tc::tmem_ld32(tmem + lane + TM_O2 + chalf * 32, o2);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) OT[(chalf * 32 + e) * D + r128] = __float2bfloat16_rn(orow[e]);
+      for (int e = 0; e < 32; ++e) {
+        const int i = chalf * 32 + e;
+        OT[i * D + r128] = __float2bfloat16_rn(EG[i] * oq[e] + o2[e]);
+      }
     }
     __syncthreads();
 #pragma unroll
@@ -536,6 +615,37 @@ __global__ void __launch_bounds__(256) tail_update_kernel(FwdParams p) {
 
 bool chunk_supported(int d, int act, int K) { return d == D && act == GDN_BF16 && K == KC; }
 
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Tensor map of x [T][C] bf16 for the chunk kernel's staging boxes
+// (64 channels x 67 rows, 128-byte swizzle, zero fill outside).
+cudaError_t make_x_map(CUtensorMap* m, const void* x, int T, int C) {
+  static EncodeTiledFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)XROWS};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   if (max_pre <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -550,7 +660,10 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   }
   const long long chains = (long long)max_pre * p.Hv;
   const int grid = (int)(chains < num_sms ? chains : num_sms);
-  chunk_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p);
+  CUtensorMap tmx;
+  e = make_x_map(&tmx, p.x, p.T, p.C);
+  if (e != cudaSuccess) return e;
+  chunk_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tmx);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   tail_update_kernel<<<max_pre, 256, 0, stream>>>(p);

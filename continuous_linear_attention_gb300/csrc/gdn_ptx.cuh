@@ -72,3 +72,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// 2-D tiled TMA load (cp.async.bulk.tensor) of the box at coordinates
+// (c0 = innermost, r0) of the tensor described by *tmap into shared memory,
+// completing on `bar`.  c0 times the element size must be a multiple of 16
+// bytes; r0 may be negative or past the end (those rows read as zero).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int r0,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace gdn

@@ -24,6 +24,7 @@ class DeviceRun:
         self.wl = wl
         self.layer = layer
         self.device = device
+        self.block_align = block_align
         stride, conv_off, rec_off, total = binding.layout_for(
             wl.num_blocks, num_layers, d.Hk, d.Hv, d.dk, d.dv, d.K, d.act, block_align)
         self.mem = torch.empty(total, dtype=torch.uint8, device=device)

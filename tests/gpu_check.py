@@ -70,7 +70,8 @@ def check_against_oracle(wl, run=None, seqs=None, tol=None, expect_flags=0, ref=
               if not skip[s] and int(wl.block_idx[s]) >= 0 and cu[s + 1] > cu[s]]
     if blocks:
         raw = run.block_bytes(blocks).numpy().reshape(-1)
-        conv, rec = oracle.read_pool_states(raw, 0, range(len(blocks)), d, len(blocks), 1)
+        conv, rec = oracle.read_pool_states(raw, 0, range(len(blocks)), d, len(blocks), 1,
+                                            block_align=run.block_align)
         idx = [ref_blocks.index(b) for b in blocks]
         np.testing.assert_array_equal(conv, ref["conv_state"][idx])
         errs["rec"] = rel_l2(rec, ref["rec_state"][idx])

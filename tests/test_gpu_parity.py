@@ -284,3 +284,47 @@ def test_inputs_rewritten_after_stream_order_are_safe():
         ref.run()
         torch.cuda.synchronize()
         assert torch.equal(outs[i], ref.out)
+
+
+# ----------------------------------------------------------------------------
+# Pool lifecycle: several layers, aligned blocks, fork.
+
+def test_second_layer_of_a_multi_layer_pool_with_aligned_blocks():
+    """Layer 1 of a two-layer pool with 64 KiB block alignment: results equal the
+    oracle and layer 0 stays byte-identical."""
+    wl = synth.make_workload("layer1", synth.FULL_DIMS, [1, 70, 1], [1, 0, 1], 8, 16)
+    run = harness.DeviceRun(wl, num_layers=2, layer=1, block_align=1 << 16)
+    assert run.stride % (1 << 16) == 0
+    page0 = run.mem[:run.page].clone()
+    before = run.mem.clone()
+    run.run()
+    torch.cuda.synchronize()
+    assert torch.equal(run.mem[:run.page], page0)
+    check_against_oracle(wl, run=run)
+    from gpu_check import mask_written, written_blocks
+    wb = written_blocks(wl, [False] * wl.N)
+    assert torch.equal(mask_written(before, run, wb), mask_written(run.mem, run, wb))
+
+
+def test_fork_copies_a_block_and_both_continue_identically():
+    """A block copied on fork (gdn_state_pool_copy_block) continues exactly like
+    the original."""
+    wl = synth.make_workload("fork", synth.FULL_DIMS, [9], [1], 8, 17, block_idx=[3])
+    run = harness.DeviceRun(wl)
+    run.pool.copy_block(0, 3, 5)
+    torch.cuda.synchronize()
+    assert torch.equal(run.mem[run.block_offset(5):run.block_offset(5) + run.stride],
+                       run.mem[run.block_offset(3):run.block_offset(3) + run.stride])
+    two = dataclasses.replace(
+        wl, x=torch.cat([wl.x, wl.x]), a=torch.cat([wl.a, wl.a]), b=torch.cat([wl.b, wl.b]),
+        cu_seqlens=torch.tensor([0, 9, 18], dtype=torch.int32),
+        block_idx=torch.tensor([3, 5], dtype=torch.int32),
+        has_past=torch.tensor([1, 1], dtype=torch.uint8))
+    run.set_inputs(two)
+    run.run()
+    torch.cuda.synchronize()
+    assert torch.equal(run.out[:9], run.out[9:])
+    assert torch.equal(run.rec_view(3), run.rec_view(5))
+    assert torch.equal(run.conv_view(3), run.conv_view(5))
+    with pytest.raises(binding.GdnError):
+        run.pool.copy_block(0, 3, 0)  # the trash block is never written
