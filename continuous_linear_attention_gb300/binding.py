@@ -32,6 +32,7 @@ EXPORTED = [
     "gdn_state_pool_destroy",
     "gdn_state_pool_layout",
     "gdn_state_pool_copy_block",
+    "gdn_state_pool_reserve",
     "gdn_varlen_forward",
     "gdn_varlen_forward_noalloc",
     "gdn_get_error",
@@ -74,6 +75,7 @@ def load() -> ctypes.CDLL:
     lib.gdn_state_pool_destroy.argtypes = [P]
     lib.gdn_state_pool_layout.argtypes = [P, PS, PS, PS, ctypes.POINTER(P)]
     lib.gdn_state_pool_copy_block.argtypes = [P, I, I, I, P]
+    lib.gdn_state_pool_reserve.argtypes = [P, I]
     lib.gdn_varlen_forward.argtypes = [P, I, P, P, P, P, P, P, ctypes.POINTER(Weights), P,
                                        I, I, I, P]
     lib.gdn_varlen_forward_noalloc.argtypes = [P, S] + [I] * 8 + [S, I] + [P] * 6 + [
@@ -172,6 +174,11 @@ class Pool:
         ha = after.cuda_event if after is not None else None
         _check(load().gdn_pool_set_timing_events(self.handle, hb, ha),
                "gdn_pool_set_timing_events")
+
+    def reserve(self, max_tokens: int):
+        """gdn_state_pool_reserve: > 0 grow the prefill scratch now, 0 free it
+        and use the fused prefill kernel only, < 0 grow on demand."""
+        _check(load().gdn_state_pool_reserve(self.handle, max_tokens), "gdn_state_pool_reserve")
 
     def copy_block(self, layer, src, dst, stream=None):
         _check(load().gdn_state_pool_copy_block(self.handle, layer, src, dst, _stream(stream)),

@@ -21,11 +21,40 @@ struct gdn_pool {
   int device;
   int32_t* work;  // num_layers * WorkArea::words(num_blocks) words
   cudaEvent_t ev_before, ev_after;  // optional timing events (caller-owned)
+  // prefill scratch (fp16 q~|k~ and v of every packed row), grown on demand
+  unsigned char* scr;
+  size_t scr_tokens;
+  bool scr_grow;  // false: never allocated; the fused chunked kernel is used
 };
 
 namespace {
 
 size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+// Bytes of prefill scratch per packed row: q~|k~ of every k-head and v of
+// every v-head, fp16.
+size_t scratch_row_bytes(const gdn_pool* p) {
+  return ((size_t)2 * p->Hk * p->dk + (size_t)p->Hv * p->dv) * 2;
+}
+
+// Make the prefill scratch hold `tokens` rows (synchronous; frees the old
+// buffer first, which waits for the device).
+int grow_scratch(gdn_pool* p, size_t tokens) {
+  if (p->scr_tokens >= tokens) return GDN_OK;
+  const size_t cap = roundup(tokens, 4096);
+  if (p->scr) {
+    cudaFree(p->scr);
+    p->scr = nullptr;
+    p->scr_tokens = 0;
+  }
+  if (cudaMalloc((void**)&p->scr, cap * scratch_row_bytes(p)) != cudaSuccess) {
+    cudaGetLastError();
+    p->scr = nullptr;
+    return GDN_ERR_NOMEM;
+  }
+  p->scr_tokens = cap;
+  return GDN_OK;
+}
 
 bool is_pow2(size_t v) { return v && !(v & (v - 1)); }
 
@@ -118,6 +147,9 @@ int gdn_state_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int 
   p->dv = dv;
   p->K = K;
   p->act = act;
+  p->scr = nullptr;
+  p->scr_tokens = 0;
+  p->scr_grow = true;
   p->stride = l.stride;
   p->conv_off = l.conv_off;
   p->rec_off = l.rec_off;
@@ -165,6 +197,7 @@ int gdn_state_pool_destroy(gdn_pool_t* p) {
   cudaDeviceSynchronize();
   if (p->owns) cudaFree(p->base);
   cudaFree(p->work);
+  if (p->scr) cudaFree(p->scr);
   if (prev >= 0) cudaSetDevice(prev);
   delete p;
   return GDN_OK;
@@ -240,6 +273,20 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
   fp.work.num_blocks = p->num_blocks;
 
   cudaStream_t s = (cudaStream_t)stream;
+  // prefill scratch for the split conv/chunk kernels: grown on demand outside
+  // stream capture; without it the fused chunked kernel runs
+  if (p->scr_grow && (size_t)T > p->scr_tokens && T > 1 && max_seqlen_hint != 1 &&
+      gdn::chunk_supported(p->dk, p->act, p->K)) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
+      grow_scratch(p, (size_t)T);
+    else
+      cudaGetLastError();
+  }
+  if (p->scr && p->scr_tokens >= (size_t)T) {
+    fp.scr_qk = p->scr;
+    fp.scr_v = p->scr + p->scr_tokens * (size_t)2 * p->Hk * p->dk * 2;
+  }
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (T == 0) {
@@ -266,6 +313,28 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
       return GDN_ERR_CUDA;
   }
   if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+int gdn_state_pool_reserve(gdn_pool_t* p, int max_tokens) {
+  if (!p) return GDN_ERR_NULL;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != p->device) return GDN_ERR_DEVICE;
+  if (max_tokens > 0) {
+    p->scr_grow = true;
+    return grow_scratch(p, (size_t)max_tokens);
+  }
+  if (max_tokens == 0) {
+    if (p->scr) {
+      cudaFree(p->scr);
+      p->scr = nullptr;
+    }
+    p->scr_tokens = 0;
+    p->scr_grow = false;
+    return GDN_OK;
+  }
+  p->scr_grow = true;
   return GDN_OK;
 }
 

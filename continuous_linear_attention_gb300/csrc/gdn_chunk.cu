@@ -69,7 +69,8 @@ constexpr uint32_t OFF_KPT = 65536;    // k'^T        128 x 128 B
 constexpr uint32_t OFF_P = 81920;      // P           64 x 128 B
 constexpr uint32_t OFF_T = 90112;      // T           64 x 128 B
 constexpr uint32_t OFF_RU = 98304;     // R^T, then U^T   128 x 128 B
-constexpr uint32_t OFF_BV = 114688;    // beta v fp16 [64][BVP]
+constexpr uint32_t OFF_BV = 114688;    // fused: beta v fp16 [64][BVP]
+constexpr uint32_t OFF_V = OFF_BV;     // split: v tile, two 64 x 64 fp16 boxes, swizzled
 constexpr uint32_t OFF_AM = 132096;    // A fp32 [64][AP]; then the out tile bf16 [64][128]
 constexpr uint32_t OFF_XT = 150528;    // 6 staged x boxes (q0 q1 k0 k1 v0 v1), 1024-aligned
 constexpr uint32_t OFF_G = 205824;     // G fp32 [64]
@@ -103,6 +104,28 @@ __device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* v) {
   }
 }
 
+// Packed fp32 pairs: d = a * b + c on both lanes (one fma.rn.f32x2).
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+  return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo_f(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// 8 bf16 -> 4 packed fp32 pairs (bf16 is the high half of an fp32)
+__device__ __forceinline__ void load8_bf16_f2(const __nv_bfloat16* p, unsigned long long* v) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    v[j] = (unsigned long long)(u[j] << 16) | ((unsigned long long)(u[j] & 0xffff0000u) << 32);
+}
+
 __device__ __forceinline__ bool out_of_f16(const float* v, int n) {
   bool bad = false;
 #pragma unroll
@@ -110,8 +133,13 @@ __device__ __forceinline__ bool out_of_f16(const float* v, int n) {
   return bad;
 }
 
+// kFused: the conv prologue runs here from 2-D TMA boxes of x (tm0 = x map).
+// Otherwise prep_kernel has written q~, k~ and v to the pool's scratch and
+// this kernel loads them as TMA tiles (tm0 = q~|k~ map, tm1 = v map).
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
+chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
+             const __grid_constant__ CUtensorMap tm1) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t bar;   // MMA completion
@@ -189,15 +217,28 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     return lc < D ? kh * D + lc
                   : (lc < 2 * D ? Hk * D + kh * D + (lc - D) : 2 * Hk * D + h * D + (lc - 2 * D));
   };
-  // Stage the x rows of chunk cc (packed rows seq0 + cc*64 - 3 .. + 63) of
-  // this chain's q, k and v channels into XT: six 64-channel x 67-row TMA
-  // boxes, 128-byte swizzled.  Rows outside the sequence are loaded too but
-  // never used (the first chunk's halo comes from the conv state).  Thread 0.
-  auto stage_x = [&](int cc) {
-    const int r0 = seq0 + cc * CH - (KC - 1);
-    mbar_arrive_expect_tx(&xbar, 6u * XBOX_BYTES);
+  // Stage chunk cc's inputs, thread 0.  Fused: the x rows (packed rows
+  // seq0 + cc*64 - 3 .. + 63) of this chain's q, k and v channels into XT, six
+  // 64-channel x 67-row TMA boxes, 128-byte swizzled; rows outside the
+  // sequence are loaded too but never used.  Split: the q~ and k~ rows of the
+  // k-head straight into the swizzled [q~ ; k~] operand tile (four 64 x 64
+  // boxes) and the v rows of the v-head into the v tile (two boxes).
+  auto stage = [&](int cc) {
+    if constexpr (kFused) {
+      const int r0 = seq0 + cc * CH - (KC - 1);
+      mbar_arrive_expect_tx(&xbar, 6u * XBOX_BYTES);
 #pragma unroll
-    for (int b6 = 0; b6 < 6; ++b6) tma_load_2d(XT + b6 * XSUB, &tmx, gch(b6 * 64), r0, &xbar);
+      for (int b6 = 0; b6 < 6; ++b6) tma_load_2d(XT + b6 * XSUB, &tm0, gch(b6 * 64), r0, &xbar);
+    } else {
+      const int r0 = seq0 + cc * CH;
+      mbar_arrive_expect_tx(&xbar, 6u * 64u * 64u * 2u);
+      tma_load_2d(sm + OFF_QK, &tm0, kh * 2 * D, r0, &xbar);
+      tma_load_2d(sm + OFF_QK + KB_STRIDE, &tm0, kh * 2 * D + 64, r0, &xbar);
+      tma_load_2d(sm + OFF_QK + CH * 128, &tm0, kh * 2 * D + D, r0, &xbar);
+      tma_load_2d(sm + OFF_QK + KB_STRIDE + CH * 128, &tm0, kh * 2 * D + D + 64, r0, &xbar);
+      tma_load_2d(sm + OFF_V, &tm1, h * D, r0, &xbar);
+      tma_load_2d(sm + OFF_V + CH * 128, &tm1, h * D + 64, r0, &xbar);
+    }
   };
   // gate inputs of chunk cc, token tid (threads < 64)
   auto load_gates = [&](int cc, float& a_, float& b_) {
@@ -208,13 +249,15 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       b_ = __bfloat162float(bv[row * Hv + h]);
     }
   };
-  if (tid == 0) stage_x(0);
+  if (tid == 0) stage(0);
   float a_nx = 0.f, b_nx = 0.f;
   load_gates(0, a_nx, b_nx);
-  for (int lc = tid; lc < kLocalCh; lc += kThreads) {
-    const int gc = gch(lc);
+  if constexpr (kFused) {
+    for (int lc = tid; lc < kLocalCh; lc += kThreads) {
+      const int gc = gch(lc);
 #pragma unroll
-    for (int j = 0; j < KC; ++j) WS[j * kLocalCh + lc] = __bfloat162float(wconv[(size_t)gc * KC + j]);
+      for (int j = 0; j < KC; ++j) WS[j * kLocalCh + lc] = __bfloat162float(wconv[(size_t)gc * KC + j]);
+    }
   }
   const float A_neg = -__expf(p.A_log[h]);
   const float dtb = p.dt_bias[h];
@@ -252,48 +295,64 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     xphase ^= 1;
     const float GC = G[CH - 1];
     if (tid < CH) DSC[tid] = __expf(GC - G[tid]);
+    if (kFused && c == 0) {
+      // the first chunk's three halo rows are the conv state, not packed rows
+      // of another sequence: overwrite the staged ones (16 bytes per thread)
+      if (tid < 3 * 48) {
+        const int r = tid / 48, q8 = tid % 48;   // row, 8-channel group (6 boxes x 8)
+        const int b6 = q8 >> 3, cc = (q8 & 7) * 8;
+        *reinterpret_cast<uint4*>(XT + b6 * XSUB + tc::sw128_offset(r, cc)) =
+            *reinterpret_cast<const uint4*>(tail_r + (size_t)r * C + gch(b6 * 64 + cc));
+      }
+      __syncthreads();
+    }
 
     // ---------------- prep: conv + SiLU + norms -> fp16 tiles
     // Thread (tq, g) computes 8-channel group g of q, of k and of v for the four
     // tokens 4tq .. 4tq+3 with a sliding window over 7 staged rows; the 16
     // threads of a token quad reduce the norms with shuffles.
-    {
+    if constexpr (kFused) {
       const int tq = tid >> 4, g = tid & 15;
       const int i0 = 4 * tq;
 #pragma unroll
       for (int part = 0; part < 3; ++part) {   // 0: q, 1: k, 2: v
         const int lc0 = part * D + g * 8;
         const int sub = lc0 >> 6, cc = lc0 & 63;
-        float w[KC][8];
+        unsigned long long w2[KC][4];  // taps as packed channel pairs
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
           const float4 w0 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0);
           const float4 w1 = *reinterpret_cast<const float4*>(WS + j * kLocalCh + lc0 + 4);
-          w[j][0] = w0.x; w[j][1] = w0.y; w[j][2] = w0.z; w[j][3] = w0.w;
-          w[j][4] = w1.x; w[j][5] = w1.y; w[j][6] = w1.z; w[j][7] = w1.w;
+          w2[j][0] = pack_f2(w0.x, w0.y); w2[j][1] = pack_f2(w0.z, w0.w);
+          w2[j][2] = pack_f2(w1.x, w1.y); w2[j][3] = pack_f2(w1.z, w1.w);
         }
-        float acc[4][8];
+        unsigned long long acc2[4][4];
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+          for (int e = 0; e < 4; ++e) acc2[t][e] = 0ull;
 #pragma unroll
         for (int rr = 0; rr < 4 + KC - 1; ++rr) {
-          const int r = i0 + rr;    // staged row; rows < 3 of the first chunk are the conv state
-          float xv[8];
-          if (c == 0 && r < KC - 1)
-            load8_bf16(tail_r + (size_t)r * C + gch(lc0), xv);
-          else
-            load8_bf16(reinterpret_cast<const __nv_bfloat16*>(XT + sub * XSUB + tc::sw128_offset(r, cc)), xv);
+          const int r = i0 + rr;    // staged row
+          unsigned long long xv2[4];
+          load8_bf16_f2(reinterpret_cast<const __nv_bfloat16*>(XT + sub * XSUB + tc::sw128_offset(r, cc)), xv2);
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int j = rr - t;   // tap of this row for token i0 + t
             if (j >= 0 && j < KC) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[t][e] += w[j][e] * xv[e];
+              for (int e = 0; e < 4; ++e) acc2[t][e] = fma2(w2[j][e], xv2[e], acc2[t][e]);
             }
           }
         }
+        float acc[4][8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[t][2 * e] = lo_f(acc2[t][e]);
+            acc[t][2 * e + 1] = hi_f(acc2[t][e]);
+          }
         float y[4][8], ss[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -369,9 +428,10 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
                    tc::idesc_f16_f32(128, 128), false);
       tc::commit(&bar);
     }
-    // the staged rows are consumed: bring in the next chunk's while this one runs
-    if (c + 1 < n_chunks) {
-      if (tid == 0) stage_x(c + 1);
+    // fused: the staged rows are consumed; bring in the next chunk's while
+    // this one runs
+    if (kFused && c + 1 < n_chunks) {
+      if (tid == 0) stage(c + 1);
       load_gates(c + 1, a_nx, b_nx);
     }
     // while the tensor core runs: (k~ e^{G_C - G_i})^T, row k of the 128-row tile
@@ -385,8 +445,9 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          v8[e] = __half2float(*reinterpret_cast<const __half*>(
-                      ksrc + tc::sw128_offset(CH + i0 + e, k & 63))) * DSC[i0 + e];
+          v8[e] = i0 + e < n ? __half2float(*reinterpret_cast<const __half*>(
+                                   ksrc + tc::sw128_offset(CH + i0 + e, k & 63))) * DSC[i0 + e]
+                             : 0.f;
         tc::sw128_store8<E>(sm + OFF_KPT, k, i0, v8);
       }
     }
@@ -408,7 +469,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int j = chalf * 32 + g8 * 8 + e;
-            v8[e] = j <= i ? xr[g8 * 8 + e] * __expf(Gi - G[j]) : 0.f;
+            v8[e] = (j <= i && i < n) ? xr[g8 * 8 + e] * __expf(Gi - G[j]) : 0.f;
           }
           tc::sw128_store8<E>(sm + OFF_P, i, chalf * 32 + g8 * 8, v8);
         }
@@ -419,10 +480,11 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
         for (int j4 = 0; j4 < 8; ++j4) {
           const int j = chalf * 32 + j4 * 4;
           float4 a4;
-          a4.x = j + 0 < i ? bi * __expf(Gi - G[j + 0]) * xr[j4 * 4 + 0] : 0.f;
-          a4.y = j + 1 < i ? bi * __expf(Gi - G[j + 1]) * xr[j4 * 4 + 1] : 0.f;
-          a4.z = j + 2 < i ? bi * __expf(Gi - G[j + 2]) * xr[j4 * 4 + 2] : 0.f;
-          a4.w = j + 3 < i ? bi * __expf(Gi - G[j + 3]) * xr[j4 * 4 + 3] : 0.f;
+          const bool vi = i < n;
+          a4.x = (vi && j + 0 < i) ? bi * __expf(Gi - G[j + 0]) * xr[j4 * 4 + 0] : 0.f;
+          a4.y = (vi && j + 1 < i) ? bi * __expf(Gi - G[j + 1]) * xr[j4 * 4 + 1] : 0.f;
+          a4.z = (vi && j + 2 < i) ? bi * __expf(Gi - G[j + 2]) * xr[j4 * 4 + 2] : 0.f;
+          a4.w = (vi && j + 3 < i) ? bi * __expf(Gi - G[j + 3]) * xr[j4 * 4 + 3] : 0.f;
           *reinterpret_cast<float4*>(AM + i * AP + j) = a4;
         }
       }
@@ -436,13 +498,25 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = chalf * 32 + g8 * 8 + e;
-          v8[e] = __half2float(BV[i * BVP + v]) - F[i] * yr[g8 * 8 + e];
+          float bvv;
+          if constexpr (kFused) {
+            bvv = __half2float(BV[i * BVP + v]);
+          } else {
+            bvv = BETA[i] * __half2float(*reinterpret_cast<const __half*>(
+                                sm + OFF_V + (v >> 6) * (CH * 128) + tc::sw128_offset(i, v & 63)));
+          }
+          v8[e] = i < n ? bvv - F[i] * yr[g8 * 8 + e] : 0.f;
         }
         range_bad |= out_of_f16(v8, 8);
         tc::sw128_store8<E>(sm + OFF_RU, v, chalf * 32 + g8 * 8, v8);
       }
     }
     __syncthreads();
+    // split: the operand and v tiles are consumed; bring in the next chunk's
+    if (!kFused && c + 1 < n_chunks) {
+      if (tid == 0) stage(c + 1);
+      load_gates(c + 1, a_nx, b_nx);
+    }
     // ---------------- T = (I + A)^{-1}: diagonal 16 x 16 blocks, column per thread
     if (tid < CH) {
       const int b = tid >> 4, m = tid & 15;
@@ -624,7 +698,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 // Tensor map of x [T][C] bf16 for the chunk kernel's staging boxes
 // (64 channels x 67 rows, 128-byte swizzle, zero fill outside).
-cudaError_t make_x_map(CUtensorMap* m, const void* x, int T, int C) {
+// Tensor map of a row-major 16-bit [rows][cols] array read in boxes of
+// 64 columns x box_rows rows, 128-byte swizzled, zero fill outside.
+cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rows, int cols,
+                     int box_rows) {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -634,12 +711,12 @@ cudaError_t make_x_map(CUtensorMap* m, const void* x, int T, int C) {
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
-  const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
-  const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)XROWS};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
-                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -648,8 +725,13 @@ cudaError_t make_x_map(CUtensorMap* m, const void* x, int T, int C) {
 
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   if (max_pre <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
+  const bool fused = p.scr_qk == nullptr;
+  cudaError_t e = fused ? cudaFuncSetAttribute(chunk_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)SMEM_BYTES)
+                        : cudaFuncSetAttribute(chunk_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   static int num_sms = 0;
   if (num_sms == 0) {
@@ -660,10 +742,22 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   }
   const long long chains = (long long)max_pre * p.Hv;
   const int grid = (int)(chains < num_sms ? chains : num_sms);
-  CUtensorMap tmx;
-  e = make_x_map(&tmx, p.x, p.T, p.C);
-  if (e != cudaSuccess) return e;
-  chunk_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tmx);
+  CUtensorMap tm0, tm1;
+  if (fused) {
+    e = make_map(&tm0, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
+    if (e != cudaSuccess) return e;
+    tm1 = tm0;
+    chunk_kernel<true><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tm0, tm1);
+  } else {
+    // conv prologue first: at most T/64 + (number of prefill sequences) chunks
+    e = launch_prep(p, p.T / CH + max_pre, stream);
+    if (e != cudaSuccess) return e;
+    e = make_map(&tm0, p.scr_qk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hk * 2 * D, CH);
+    if (e != cudaSuccess) return e;
+    e = make_map(&tm1, p.scr_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
+    if (e != cudaSuccess) return e;
+    chunk_kernel<false><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tm0, tm1);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   tail_update_kernel<<<max_pre, 256, 0, stream>>>(p);

@@ -22,6 +22,7 @@ constexpr int kMaxConvK = 4;
 //                  dec[num_blocks]         active sequences of length 1
 //                  pre_tmp[num_blocks]     active sequences of length > 1, unsorted
 //                  pre[num_blocks]         the same, longest first
+//                  pre_cp[num_blocks + 1]  chunk prefix: 64-token chunks of pre[0..k)
 enum Cnt : int {
   kErr = 0,
   kNItems = 1,
@@ -29,6 +30,7 @@ enum Cnt : int {
   kNPre = 3,
   kPreTokens = 4,  // total tokens of the length>1 sequences
   kWorkHead = 5,   // dynamic work counter of persistent kernels (reset by the scheduler)
+  kPreChunks = 6,  // total 64-token chunks of the length>1 sequences
   kHeaderWords = 16,
 };
 
@@ -41,7 +43,8 @@ struct WorkArea {
   __host__ __device__ int32_t* dec() const { return base + kHeaderWords + 2 * num_blocks; }
   __host__ __device__ int32_t* pre_tmp() const { return base + kHeaderWords + 3 * num_blocks; }
   __host__ __device__ int32_t* pre() const { return base + kHeaderWords + 4 * num_blocks; }
-  static size_t words(int num_blocks) { return kHeaderWords + 5 * (size_t)num_blocks; }
+  __host__ __device__ int32_t* pre_cp() const { return base + kHeaderWords + 5 * num_blocks; }
+  static constexpr size_t words(int num_blocks) { return kHeaderWords + 6 * (size_t)num_blocks + 1; }
 };
 
 // Everything a forward kernel needs, passed by value.
@@ -62,6 +65,10 @@ struct FwdParams {
   int T, N, Hk, Hv, C, K, num_blocks;
   int max_seqlen_hint;  // 0 = unknown; else longer sequences are flagged and skipped
   WorkArea work;
+  // prefill scratch (fp16): q~|k~ [T][Hk][2][d] and v [T][Hv][d]; nullptr when
+  // the pool has none for this many tokens (the fused chunked kernel is used)
+  void* scr_qk = nullptr;
+  void* scr_v = nullptr;
 };
 
 // Launchers (each returns a cudaError_t from the launch).
@@ -78,6 +85,10 @@ cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 // update that follows it: d_k = d_v = 128, bf16 activations, K = 4.
 bool chunk_supported(int d, int act, int K);
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
+// The conv prologue of the prefill path as its own kernel, writing the
+// scratch the split chunked kernel reads (max_chunks: host bound on the
+// number of 64-token chunks of the prefill sequences).
+cudaError_t launch_prep(const FwdParams& p, int max_chunks, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.
@@ -94,7 +105,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __device__ __forceinline__ float softplus_f32(float x) {
   return x > 0.f ? x + log1pf(__expf(-x)) : log1pf(__expf(x));
 }
-__device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + __expf(-x)); }
-__device__ __forceinline__ float silu_f32(float y) { return y / (1.f + __expf(-y)); }
+// Fast reciprocal division (__fdividef): 2 ulp, and exactly 0 once the
+// denominator overflows, which is the limit of both functions there.
+__device__ __forceinline__ float sigmoid_f32(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+__device__ __forceinline__ float silu_f32(float y) { return __fdividef(y, 1.f + __expf(-y)); }
 
 }  // namespace gdn

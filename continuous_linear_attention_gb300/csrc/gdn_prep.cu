@@ -1,0 +1,171 @@
+// Conv prologue of the prefill path as its own memory-bound kernel: for every
+// token of the sequences longer than one token, the varlen causal depthwise
+// conv1d + SiLU continued from the sequence's conv state ("Continuous
+// batching for linear attention layers": a varlen causal convolution
+// continues every sequence from its own conv state), then the L2 norms of q
+// and k (q also scaled by 1/sqrt(d_k)).  Results go to a pool-owned scratch
+// in fp16, which the chunked kernel loads tile by tile with TMA:
+//   qk[row][kh][0..127]   = q~ of k-head kh,  qk[row][kh][128..255] = k~
+//   vv[row][h][0..127]    = v of v-head h (SiLU output)
+// Computing q~/k~ once per k-head here, instead of once per v-head inside the
+// chunked kernel, halves the q/k conv work, and keeps the chunked kernel's
+// instruction stream for the recurrence.
+//
+// One CTA per (64-token chunk of a prefill sequence, k-head); chunks are
+// found from the scheduler's chunk prefix over the sorted prefill list.
+// Thread (tq, g) computes channel group g (8 channels) of q, k and the two
+// v-heads for tokens 4tq .. 4tq+3 with a sliding window over 7 input rows.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int D = 128;
+constexpr int CH = 64;
+constexpr int KC = 4;
+constexpr int kThreads = 256;
+constexpr int R = 2;  // v-heads per k-head
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(u[j] << 16);
+    v[2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8_f16(const float* v) {
+  uint4 w;
+  __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+  __half2 h2 = __floats2half2_rn(v[4], v[5]), h3 = __floats2half2_rn(v[6], v[7]);
+  w.x = *reinterpret_cast<uint32_t*>(&h0);
+  w.y = *reinterpret_cast<uint32_t*>(&h1);
+  w.z = *reinterpret_cast<uint32_t*>(&h2);
+  w.w = *reinterpret_cast<uint32_t*>(&h3);
+  return w;
+}
+
+__global__ void __launch_bounds__(kThreads) prep_kernel(FwdParams p) {
+  int32_t* hdr = p.work.header();
+  const int n_chunks = hdr[kPreChunks];
+  const int gidx = blockIdx.x;
+  if (gidx >= n_chunks) return;
+  // which prefill sequence / chunk: binary search in the chunk prefix
+  const int n_pre = hdr[kNPre];
+  const int32_t* cp = p.work.pre_cp();
+  int lo = 0, hi = n_pre - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cp[mid] <= gidx) lo = mid; else hi = mid - 1;
+  }
+  const int s = p.work.pre()[lo];
+  const int c = gidx - cp[lo];
+  const int kh = blockIdx.y;
+  const int Hk = p.Hk, Hv = p.Hv, C = p.C;
+  const int seq0 = p.cu[s];
+  const int L = p.cu[s + 1] - seq0;
+  const int c0 = c * CH;
+  const int n = min(CH, L - c0);
+  const int rblk = p.has_past[s] ? p.blk[s] : 0;
+  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+  const __nv_bfloat16* tail = reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
+  const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
+  __half* qk = reinterpret_cast<__half*>(p.scr_qk);
+  __half* vv = reinterpret_cast<__half*>(p.scr_v);
+
+  const int tid = threadIdx.x;
+  const int tq = tid >> 4, g = tid & 15;
+  const int i0 = 4 * tq;
+  const float inv_sqrt_d = rsqrtf((float)D);
+  bool range_bad = false;
+#pragma unroll 1
+  for (int part = 0; part < 2 + R; ++part) {  // q, k, v of head 2kh, v of head 2kh+1
+    const int ch = part == 0 ? kh * D : (part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * R + part - 2) * D);
+    const int gc = ch + g * 8;
+    float wt[KC][8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint2 wu = *reinterpret_cast<const uint2*>(w + (size_t)(gc + e) * KC);
+      float t4[4];
+      t4[0] = __uint_as_float(wu.x << 16);
+      t4[1] = __uint_as_float(wu.x & 0xffff0000u);
+      t4[2] = __uint_as_float(wu.y << 16);
+      t4[3] = __uint_as_float(wu.y & 0xffff0000u);
+#pragma unroll
+      for (int j = 0; j < KC; ++j) wt[j][e] = t4[j];
+    }
+    float acc[4][8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < 4 + KC - 1; ++rr) {
+      const int pos = c0 + i0 + rr - (KC - 1);  // position inside the sequence
+      float xv[8];
+      if (pos < 0)
+        load8(tail + (size_t)(KC - 1 + pos) * C + gc, xv);
+      else if (pos < L)
+        load8(x + (size_t)(seq0 + pos) * C + gc, xv);
+      else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int j = rr - t;
+        if (j >= 0 && j < KC) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[t][e] += wt[j][e] * xv[e];
+        }
+      }
+    }
+    float y[4][8], ss[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      ss[t] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        y[t][e] = silu_f32(acc[t][e]);
+        ss[t] += y[t][e] * y[t][e];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = i0 + t;
+      if (part < 2) {
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+        const float sc = rsqrtf(ss[t] + kL2Eps) * (part == 0 ? inv_sqrt_d : 1.f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[t][e] *= sc;
+      }
+      if (i < n) {
+        if (part >= 2) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) range_bad |= !(fabsf(y[t][e]) <= 65000.f);
+        }
+        const size_t row = (size_t)(seq0 + c0 + i);
+        __half* dst = part < 2 ? qk + (row * Hk + kh) * (2 * D) + part * D + g * 8
+                               : vv + (row * Hv + kh * R + part - 2) * D + g * 8;
+        *reinterpret_cast<uint4*>(dst) = pack8_f16(y[t]);
+      }
+    }
+  }
+  // v enters the tensor-core operands in fp16: report values outside its range
+  if (__syncthreads_or(range_bad ? 1 : 0) && tid == 0)
+    atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_RANGE);
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const FwdParams& p, int max_chunks, cudaStream_t stream) {
+  if (max_chunks <= 0) return cudaSuccess;
+  dim3 grid(max_chunks, p.Hk);
+  prep_kernel<<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -39,7 +39,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
   if (s_bad) {
     if (tid == 0) {
       atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_SEQLENS);
-      hdr[kNItems] = hdr[kNDec] = hdr[kNPre] = hdr[kPreTokens] = 0;
+      hdr[kNItems] = hdr[kNDec] = hdr[kNPre] = hdr[kPreTokens] = hdr[kPreChunks] = 0;
       hdr[kWorkHead] = 0;
     }
     return;
@@ -96,8 +96,22 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     }
     pre[rank] = si;
   }
+  __syncthreads();
+  // 64-token chunk prefix over the sorted prefill list (for kernels that
+  // work per chunk): pre_cp[k] = chunks of pre[0..k)
+  int32_t* pre_cp = work.pre_cp();
+  for (int k = tid; k <= n_pre; k += kSchedThreads) {
+    int acc = 0;
+    for (int j = 0; j < k; ++j) {
+      const int sj = pre[j];
+      acc += (cu[sj + 1] - cu[sj] + 63) >> 6;
+    }
+    pre_cp[k] = acc;
+  }
+  __syncthreads();
   if (tid == 0) {
     if (s_flags) atomicOr((unsigned*)&hdr[kErr], s_flags);
+    hdr[kPreChunks] = pre_cp[n_pre];
     hdr[kNItems] = s_n_items;
     hdr[kNDec] = s_n_dec;
     hdr[kNPre] = n_pre;

@@ -19,7 +19,8 @@ OUT_SENTINEL = 12.5
 
 class DeviceRun:
     def __init__(self, wl: Workload, device: str = "cuda", block_align: int = 0,
-                 num_layers: int = 1, layer: int = 0, fill: bool = True):
+                 num_layers: int = 1, layer: int = 0, fill: bool = True,
+                 prefill: str = "auto"):
         d = wl.dims
         self.wl = wl
         self.layer = layer
@@ -30,6 +31,8 @@ class DeviceRun:
         self.mem = torch.empty(total, dtype=torch.uint8, device=device)
         self.pool = binding.Pool(wl.num_blocks, num_layers, d.Hk, d.Hv, d.dk, d.dv, d.K, d.act,
                                  block_align, memory=self.mem)
+        if prefill == "fused":
+            self.pool.reserve(0)  # one fused prefill kernel, no scratch
         self.stride = stride
         self.conv_off = conv_off
         self.rec_off = rec_off

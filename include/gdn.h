@@ -130,6 +130,21 @@ int gdn_state_pool_layout(const gdn_pool_t* pool, size_t* block_stride, size_t* 
  * and never shared).  dst must not be 0 (the trash block).  Stream-ordered. */
 int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, void* stream);
 
+/* Prefill scratch of the pool.  Sequences longer than one token run as two
+ * kernels when the pool has scratch for the call's T rows (fp16 q~|k~ and v
+ * of every row: (2*Hk*d_k + Hv*d_v) * 2 bytes per row, shared by the layers):
+ * a conv/normalisation kernel writes it and the chunked kernel loads it with
+ * TMA.  Without scratch they run as one fused kernel (same results within
+ * rounding).  By default the first gdn_varlen_forward with more rows than the
+ * scratch holds grows it (cudaMalloc; freeing the old buffer waits for the
+ * device), except during stream capture, where the fused kernel is used.
+ *   max_tokens > 0 : grow the scratch to at least max_tokens rows now
+ *                    (synchronous; call it before capturing a graph)
+ *   max_tokens == 0: free the scratch and never grow it (fused kernel only)
+ *   max_tokens < 0 : grow on demand again (the default)
+ * Returns GDN_ERR_NOMEM if the allocation fails (the forward still works). */
+int gdn_state_pool_reserve(gdn_pool_t* pool, int max_tokens);
+
 /* Forward of one gated-delta-net layer over a packed batch.
  *   x_qkv           : [T][C] activation dtype, the packed pre-convolution q|k|v rows
  *   a, b            : [T][Hv] activation dtype, gate and beta pre-activations
@@ -151,8 +166,10 @@ int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, voi
  * Zero-length sequences are no-ops.  Bad data in the device arrays (see
  * GDN_FLAG_*) is flagged in the layer's error word and the affected sequences
  * are skipped.  x_qkv, a, b, out and conv_w must be 16-byte aligned.
- * Never synchronises; graph-capturable.  Calls on the same layer must be
- * ordered on one stream (they share the layer's scheduler work area). */
+ * Never synchronises (except the one-time growth of the prefill scratch, see
+ * gdn_state_pool_reserve); graph-capturable.  Calls on the same pool must be
+ * ordered on one stream (they share the layer's scheduler work area and the
+ * pool's prefill scratch). */
 int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const void* a,
                        const void* b, const int32_t* cu_seqlens, const int32_t* state_block_idx,
                        const uint8_t* has_past, const gdn_weights_t* weights, void* out, int T,
@@ -177,7 +194,7 @@ int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const voi
  *                          bits raised by this call (NULL: not reported)
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  * The scheduler's work area is a static device array sized for pools of at
- * most 4096 blocks (about 80 KiB, held on every GPU that loads the library
+ * most 4096 blocks (about 96 KiB, held on every GPU that loads the library
  * until the process exits); num_blocks > 4096 returns GDN_ERR_RANGE.  Every
  * call on a device shares that array, so calls whose work overlaps on the
  * GPU race: order them on one stream.  The first call on each device looks

@@ -33,7 +33,8 @@ def mask_written(mem, run, blocks):
     return m
 
 
-def check_against_oracle(wl, run=None, seqs=None, tol=None, expect_flags=0, ref=None):
+def check_against_oracle(wl, run=None, seqs=None, tol=None, expect_flags=0, ref=None,
+                         prefill="auto"):
     """Run ``wl`` on the GPU (unless ``run`` has already been run) and compare
     with the oracle: out rows, new conv states (bit-exact: they are copies of
     inputs), recurrent states (rel-L2), untouched pool bytes and out rows of
@@ -43,7 +44,7 @@ def check_against_oracle(wl, run=None, seqs=None, tol=None, expect_flags=0, ref=
     d = wl.dims
     tol = TOL[d.act] if tol is None else tol
     if run is None:
-        run = harness.DeviceRun(wl)
+        run = harness.DeviceRun(wl, prefill=prefill)
         before = run.mem.clone()
         run.run()
         torch.cuda.synchronize()

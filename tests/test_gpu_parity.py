@@ -64,11 +64,13 @@ def test_decode_batch_full():
     check_against_oracle(synth.decode_batch())
 
 
-def test_prefill_full_dims_ragged():
-    """Full head dims, lengths spanning several 64-token chunks and ragged tails."""
+@pytest.mark.parametrize("prefill", ["auto", "fused"])
+def test_prefill_full_dims_ragged(prefill):
+    """Full head dims, lengths spanning several 64-token chunks and ragged tails;
+    both the split (conv kernel + TMA-fed chunked kernel) and the fused form."""
     wl = synth.make_workload("prefill_small", synth.FULL_DIMS, [130, 64, 257, 2, 1, 65],
                              [0, 1, 0, 1, 1, 1], 16, 7)
-    check_against_oracle(wl)
+    check_against_oracle(wl, prefill=prefill)
 
 
 def test_prefill_full_size_sampled():
@@ -98,9 +100,10 @@ def test_prefill_full_size_sampled():
     assert torch.equal(mask_written(before, run, wb), mask_written(run.mem, run, wb))
 
 
-def test_mixed_batch_full():
+@pytest.mark.parametrize("prefill", ["auto", "fused"])
+def test_mixed_batch_full(prefill):
     """64 decodes + 6 prefill continuations with past, 8192 tokens, 1024 blocks."""
-    check_against_oracle(synth.mixed_batch())
+    check_against_oracle(synth.mixed_batch(), prefill=prefill)
 
 
 def test_long_context_split_equals_single_pass():
@@ -234,10 +237,25 @@ def test_packed_equals_each_alone_gpu():
         assert torch.equal(one.conv_view(blk), run.conv_view(blk))
 
 
-def test_beta_zero_only_decays_gpu():
+@pytest.mark.parametrize("prefill", ["auto", "fused"])
+def test_beta_zero_only_decays_gpu(prefill):
     wl = synth.make_workload("beta0", synth.FULL_DIMS, [5, 1, 66], [1, 1, 1], 8, 13)
     wl = dataclasses.replace(wl, b=torch.full_like(wl.b, -1000.0))
-    check_against_oracle(wl)
+    check_against_oracle(wl, prefill=prefill)
+
+
+def test_split_and_fused_prefill_agree():
+    """The two prefill forms give the same outputs and states within rounding."""
+    wl = synth.make_workload("forms", synth.FULL_DIMS, [300, 1, 77, 2], [1, 1, 0, 0], 8, 18)
+    a = harness.DeviceRun(wl)
+    b = harness.DeviceRun(wl, prefill="fused")
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert rel_l2(a.out.float().cpu().numpy(), b.out.float().cpu().numpy()) <= 2e-3
+    for blk in [int(v) for v in wl.block_idx]:
+        assert rel_l2(a.rec_view(blk).cpu().numpy(), b.rec_view(blk).cpu().numpy()) <= 2e-3
+        assert torch.equal(a.conv_view(blk), b.conv_view(blk))
 
 
 def test_graph_capture_replays_the_same_result():
