@@ -64,7 +64,7 @@ constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
 constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]   2 x (128 rows x 128 B)
 constexpr uint32_t OFF_S0 = 32768;     // S0 tile 2 x (128 x 128 B); during the solve: T fp32, Z
 constexpr uint32_t OFF_TS = OFF_S0;    // T fp32 [64][AP]
-constexpr uint32_t OFF_Z = OFF_S0 + 17408;  // blocked-solve scratch fp32 [3][16][16]
+constexpr uint32_t OFF_Z = OFF_S0 + 17408;  // blocked-solve scratch fp32 [6][16][16]
 constexpr uint32_t OFF_KPT = 65536;    // k'^T        128 x 128 B
 constexpr uint32_t OFF_P = 81920;      // P           64 x 128 B
 constexpr uint32_t OFF_T = 90112;      // T           64 x 128 B
@@ -126,11 +126,10 @@ __device__ __forceinline__ void load8_bf16_f2(const __nv_bfloat16* p, unsigned l
     v[j] = (unsigned long long)(u[j] << 16) | ((unsigned long long)(u[j] & 0xffff0000u) << 32);
 }
 
-__device__ __forceinline__ bool out_of_f16(const float* v, int n) {
-  bool bad = false;
+// Running max of |v| (NaN propagates through the final comparison).
+__device__ __forceinline__ void track_abs(float& m, const float* v, int n) {
 #pragma unroll
-  for (int e = 0; e < n; ++e) bad |= !(fabsf(v[e]) <= kF16Max);
-  return bad;
+  for (int e = 0; e < n; ++e) m = fmaxf(m, fabsf(v[e]));
 }
 
 // kFused: the conv prologue runs here from 2-D TMA boxes of x (tm0 = x map).
@@ -193,7 +192,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
   uint32_t phase = 0, xphase = 0;
   const float inv_sqrt_d = rsqrtf((float)D);
   bool failed = false;
-  bool range_bad = false;
+  float amax = 0.f;  // largest |value| converted to an fp16 operand in this chain
 
   // ---- chains, longest sequences first, pulled from the scheduler's counter
   for (;;) {
@@ -386,7 +385,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
             wv.y = tc::pack2(bi * y[t][2], bi * y[t][3], (__half*)nullptr);
             wv.z = tc::pack2(bi * y[t][4], bi * y[t][5], (__half*)nullptr);
             wv.w = tc::pack2(bi * y[t][6], bi * y[t][7], (__half*)nullptr);
-            range_bad |= out_of_f16(y[t], 8);
+            track_abs(amax, y[t], 8);
             *reinterpret_cast<uint4*>(BV + i * BVP + g * 8) = wv;
           }
         }
@@ -406,7 +405,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
         tc::tmem_ld32(tmem + lane + TM_S + chalf * 64 + 32, srow + 32);
         tc::tmem_wait_ld();
       }
-      range_bad |= out_of_f16(srow, 64);
+      track_abs(amax, srow, 64);
 #pragma unroll
       for (int g8 = 0; g8 < 8; ++g8)
         tc::sw128_store8<E>(sm + OFF_S0 + chalf * KB_STRIDE, v, g8 * 8, srow + g8 * 8);
@@ -460,6 +459,12 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
       float xr[32];
       tc::tmem_ld32(tmem + lane + TM_X + chalf * 32, xr);
       tc::tmem_wait_ld();
+      float Gj[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(G + chalf * 32 + q4 * 4);
+        Gj[q4 * 4] = t4.x; Gj[q4 * 4 + 1] = t4.y; Gj[q4 * 4 + 2] = t4.z; Gj[q4 * 4 + 3] = t4.w;
+      }
       if (r128 < CH) {
         const int i = r128;
         const float Gi = G[i];
@@ -469,7 +474,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int j = chalf * 32 + g8 * 8 + e;
-            v8[e] = (j <= i && i < n) ? xr[g8 * 8 + e] * __expf(Gi - G[j]) : 0.f;
+            v8[e] = (j <= i && i < n) ? xr[g8 * 8 + e] * __expf(Gi - Gj[g8 * 8 + e]) : 0.f;
           }
           tc::sw128_store8<E>(sm + OFF_P, i, chalf * 32 + g8 * 8, v8);
         }
@@ -481,10 +486,10 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
           const int j = chalf * 32 + j4 * 4;
           float4 a4;
           const bool vi = i < n;
-          a4.x = (vi && j + 0 < i) ? bi * __expf(Gi - G[j + 0]) * xr[j4 * 4 + 0] : 0.f;
-          a4.y = (vi && j + 1 < i) ? bi * __expf(Gi - G[j + 1]) * xr[j4 * 4 + 1] : 0.f;
-          a4.z = (vi && j + 2 < i) ? bi * __expf(Gi - G[j + 2]) * xr[j4 * 4 + 2] : 0.f;
-          a4.w = (vi && j + 3 < i) ? bi * __expf(Gi - G[j + 3]) * xr[j4 * 4 + 3] : 0.f;
+          a4.x = (vi && j + 0 < i) ? bi * __expf(Gi - Gj[j4 * 4 + 0]) * xr[j4 * 4 + 0] : 0.f;
+          a4.y = (vi && j + 1 < i) ? bi * __expf(Gi - Gj[j4 * 4 + 1]) * xr[j4 * 4 + 1] : 0.f;
+          a4.z = (vi && j + 2 < i) ? bi * __expf(Gi - Gj[j4 * 4 + 2]) * xr[j4 * 4 + 2] : 0.f;
+          a4.w = (vi && j + 3 < i) ? bi * __expf(Gi - Gj[j4 * 4 + 3]) * xr[j4 * 4 + 3] : 0.f;
           *reinterpret_cast<float4*>(AM + i * AP + j) = a4;
         }
       }
@@ -492,22 +497,36 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
       tc::tmem_ld32(tmem + lane + TM_Y + chalf * 32, yr);
       tc::tmem_wait_ld();
       const int v = r128;
+      const unsigned char* vcol = sm + OFF_V + (v >> 6) * (CH * 128) + (v & 7) * 2;
+      const uint32_t vchunk = (uint32_t)((v & 63) >> 3);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
+        const int ib = chalf * 32 + g8 * 8;
+        const float4 f0 = *reinterpret_cast<const float4*>(F + ib);
+        const float4 f1 = *reinterpret_cast<const float4*>(F + ib + 4);
+        const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+        float bv8[8];
+        if constexpr (!kFused) {
+          const float4 b0 = *reinterpret_cast<const float4*>(BETA + ib);
+          const float4 b1 = *reinterpret_cast<const float4*>(BETA + ib + 4);
+          bv8[0] = b0.x; bv8[1] = b0.y; bv8[2] = b0.z; bv8[3] = b0.w;
+          bv8[4] = b1.x; bv8[5] = b1.y; bv8[6] = b1.z; bv8[7] = b1.w;
+        }
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int i = chalf * 32 + g8 * 8 + e;
+          const int i = ib + e;
           float bvv;
           if constexpr (kFused) {
             bvv = __half2float(BV[i * BVP + v]);
           } else {
-            bvv = BETA[i] * __half2float(*reinterpret_cast<const __half*>(
-                                sm + OFF_V + (v >> 6) * (CH * 128) + tc::sw128_offset(i, v & 63)));
+            // row i of the swizzled v box: 8-row group ib/8, row e, chunk vchunk ^ e
+            bvv = bv8[e] * __half2float(*reinterpret_cast<const __half*>(
+                               vcol + (ib >> 3) * 1024 + e * 128 + ((vchunk ^ (uint32_t)e) << 4)));
           }
-          v8[e] = i < n ? bvv - F[i] * yr[g8 * 8 + e] : 0.f;
+          v8[e] = i < n ? bvv - fv[e] * yr[g8 * 8 + e] : 0.f;
         }
-        range_bad |= out_of_f16(v8, 8);
+        track_abs(amax, v8, 8);
         tc::sw128_store8<E>(sm + OFF_RU, v, chalf * 32 + g8 * 8, v8);
       }
     }
@@ -533,33 +552,35 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
       for (int r = 0; r < 16; ++r) TS[(16 * b + r) * AP + 16 * b + m] = col[r];
     }
     __syncthreads();
-    // off-diagonal blocks, level L = i - j: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj,
-    // four adjacent columns per thread
+    // off-diagonal blocks: B_ij = T_ii A_ij for every i > j (independent), then
+    // level by level T_ij = -sum_{k=j}^{i-1} B_ik T_kj; four adjacent columns
+    // per thread.  B block (i, j) lives at Z + (i(i-1)/2 + j) * 256.
+    for (int task = tid; task < 6 * 64; task += kThreads) {
+      const int bi = task >> 6, rr = (task >> 2) & 15, c4 = (task & 3) * 4;
+      const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
+      const int j = bi - i * (i - 1) / 2;
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float t = TS[(16 * i + rr) * AP + 16 * i + q];
+        const float4 a4 = *reinterpret_cast<const float4*>(AM + (16 * i + q) * AP + 16 * j + c4);
+        z.x += t * a4.x; z.y += t * a4.y; z.z += t * a4.z; z.w += t * a4.w;
+      }
+      *reinterpret_cast<float4*>(Z + bi * 256 + rr * 16 + c4) = z;
+    }
+    __syncthreads();
     for (int Lv = 1; Lv < 4; ++Lv) {
-      const int ne = (4 - Lv) * 64;
-      if (tid < ne) {
+      if (tid < (4 - Lv) * 64) {
         const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = j; k < i; ++k) {
+          const float* Bik = Z + (i * (i - 1) / 2 + k) * 256 + rr * 16;
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            const float a = AM[(16 * i + rr) * AP + 16 * k + q];
+            const float bq = Bik[q];
             const float4 t4 = *reinterpret_cast<const float4*>(TS + (16 * k + q) * AP + 16 * j + c4);
-            z.x += a * t4.x; z.y += a * t4.y; z.z += a * t4.z; z.w += a * t4.w;
+            t.x -= bq * t4.x; t.y -= bq * t4.y; t.z -= bq * t4.z; t.w -= bq * t4.w;
           }
-        }
-        *reinterpret_cast<float4*>(Z + tid * 4) = z;
-      }
-      __syncthreads();
-      if (tid < ne) {
-        const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        const float* zb = Z + (tid & ~63) * 4;   // this block's Z, [16][16]
-        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float a = TS[(16 * i + rr) * AP + 16 * i + q];
-          const float4 z4 = *reinterpret_cast<const float4*>(zb + q * 16 + c4);
-          t.x -= a * z4.x; t.y -= a * z4.y; t.z -= a * z4.z; t.w -= a * z4.w;
         }
         *reinterpret_cast<float4*>(TS + (16 * i + rr) * AP + 16 * j + c4) = t;
       }
@@ -576,7 +597,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
         const int j = c8 * 8 + e;
         v8[e] = (j >> 4) <= (i >> 4) ? TS[i * AP + j] : 0.f;
       }
-      range_bad |= out_of_f16(v8, 8);
+      track_abs(amax, v8, 8);
       tc::sw128_store8<E>(sm + OFF_T, i, c8 * 8, v8);
     }
     tc::fence_proxy_async_smem();
@@ -596,7 +617,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
       float ur[32];
       tc::tmem_ld32(tmem + lane + TM_UT + chalf * 32, ur);
       tc::tmem_wait_ld();
-      range_bad |= out_of_f16(ur, 32);
+      track_abs(amax, ur, 32);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
         tc::sw128_store8<E>(sm + OFF_RU, r128, chalf * 32 + g8 * 8, ur + g8 * 8);
@@ -648,9 +669,9 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
 #pragma unroll
     for (int k = 0; k < 64; ++k) S_w[(size_t)(chalf * 64 + k) * D + r128] = srow[k];
   }
-  if (__syncthreads_or(range_bad ? 1 : 0) && tid == 0)
+  if (__syncthreads_or(!(amax <= kF16Max) ? 1 : 0) && tid == 0)
     atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
-  range_bad = false;
+  amax = 0.f;
   }  // chains
   if (failed && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
   tc::fence_before_sync();
@@ -660,6 +681,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
 
 // New conv states of the length > 1 sequences: the last K-1 inputs of
 // [old conv state ; x_seq], written after every chain has read the old one.
+// Grid (sequence, channel slice); each thread moves 8 channels of the K-1 rows.
 __global__ void __launch_bounds__(256) tail_update_kernel(FwdParams p) {
   const int n_pre = p.work.header()[kNPre];
   if ((int)blockIdx.x >= n_pre) return;
@@ -669,20 +691,21 @@ __global__ void __launch_bounds__(256) tail_update_kernel(FwdParams p) {
   const int wblk = p.blk[s];
   const int rblk = p.has_past[s] ? wblk : 0;
   const int C = p.C;
+  const int ch = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
+  if (ch >= C) return;
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
   const __nv_bfloat16* tail_r =
       reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
   __nv_bfloat16* tail_w = reinterpret_cast<__nv_bfloat16*>(p.layer_base + (size_t)wblk * p.stride);
-  for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
-    __nv_bfloat16 nv[KC - 1];
+  uint4 nv[KC - 1];
 #pragma unroll
-    for (int j = 0; j < KC - 1; ++j) {
-      const int pp = L - (KC - 1) + j;
-      nv[j] = pp >= 0 ? x[(size_t)(seq0 + pp) * C + ch] : tail_r[(size_t)(KC - 1 + pp) * C + ch];
-    }
-#pragma unroll
-    for (int j = 0; j < KC - 1; ++j) tail_w[(size_t)j * C + ch] = nv[j];
+  for (int j = 0; j < KC - 1; ++j) {
+    const int pp = L - (KC - 1) + j;
+    nv[j] = *reinterpret_cast<const uint4*>(pp >= 0 ? x + (size_t)(seq0 + pp) * C + ch
+                                                    : tail_r + (size_t)(KC - 1 + pp) * C + ch);
   }
+#pragma unroll
+  for (int j = 0; j < KC - 1; ++j) *reinterpret_cast<uint4*>(tail_w + (size_t)j * C + ch) = nv[j];
 }
 
 }  // namespace
@@ -750,7 +773,10 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     chunk_kernel<true><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tm0, tm1);
   } else {
     // conv prologue first: at most T/64 + (number of prefill sequences) chunks
-    e = launch_prep(p, p.T / CH + max_pre, stream);
+    CUtensorMap tmx;
+    e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
+    if (e != cudaSuccess) return e;
+    e = launch_prep(p, &tmx, p.T / CH + max_pre, stream);
     if (e != cudaSuccess) return e;
     e = make_map(&tm0, p.scr_qk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hk * 2 * D, CH);
     if (e != cudaSuccess) return e;
@@ -760,7 +786,7 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  tail_update_kernel<<<max_pre, 256, 0, stream>>>(p);
+  tail_update_kernel<<<dim3(max_pre, (p.C / 8 + 255) / 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -88,7 +88,9 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
 // The conv prologue of the prefill path as its own kernel, writing the
 // scratch the split chunked kernel reads (max_chunks: host bound on the
 // number of 64-token chunks of the prefill sequences).
-cudaError_t launch_prep(const FwdParams& p, int max_chunks, cudaStream_t stream);
+// x_map: the CUtensorMap of x (boxes of 64 channels x 67 rows, 128-byte swizzle).
+cudaError_t launch_prep(const FwdParams& p, const void* x_map, int max_chunks,
+                        cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

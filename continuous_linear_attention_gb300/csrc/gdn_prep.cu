@@ -12,10 +12,18 @@
 // instruction stream for the recurrence.
 //
 // One CTA per (64-token chunk of a prefill sequence, k-head); chunks are
-// found from the scheduler's chunk prefix over the sorted prefill list.
-// Thread (tq, g) computes channel group g (8 channels) of q, k and the two
-// v-heads for tokens 4tq .. 4tq+3 with a sliding window over 7 input rows.
+// found from the scheduler's chunk prefix over the sorted prefill list.  The
+// CTA's 67 x rows (3 halo + 64) of its 512 channels arrive as eight 2-D TMA
+// boxes (128-byte swizzled, 72 KiB) so three CTAs per SM keep ~200 KiB of
+// loads in flight; the first chunk's halo rows are then replaced by the
+// sequence's conv state.  Thread (tq, g) computes channel group g (8
+// channels) of q, k and the two v-heads for tokens 4tq .. 4tq+3 with a
+// sliding window over 7 staged rows.
+#include <cuda.h>
+
 #include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -25,6 +33,10 @@ constexpr int CH = 64;
 constexpr int KC = 4;
 constexpr int kThreads = 256;
 constexpr int R = 2;  // v-heads per k-head
+constexpr int XROWS = CH + KC - 1;
+constexpr uint32_t XSUB = 9216;  // one box: 72 rows x 128 B, 1024-aligned
+constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
+constexpr uint32_t SMEM_BYTES = 8 * XSUB + 1024;
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
   const uint4 w = *reinterpret_cast<const uint4*>(p);
@@ -47,7 +59,12 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
   return w;
 }
 
-__global__ void __launch_bounds__(kThreads) prep_kernel(FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
+                                                       const __grid_constant__ CUtensorMap tmx) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* xt = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t xbar;
+  __shared__ int ok;
   int32_t* hdr = p.work.header();
   const int n_chunks = hdr[kPreChunks];
   const int gidx = blockIdx.x;
@@ -69,13 +86,39 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(FwdParams p) {
   const int c0 = c * CH;
   const int n = min(CH, L - c0);
   const int rblk = p.has_past[s] ? p.blk[s] : 0;
-  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
   const __nv_bfloat16* tail = reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
   const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
   __half* qk = reinterpret_cast<__half*>(p.scr_qk);
   __half* vv = reinterpret_cast<__half*>(p.scr_v);
 
   const int tid = threadIdx.x;
+  // local channel block b (64 channels): 0,1 q | 2,3 k | 4..7 v of heads 2kh, 2kh+1
+  auto gch = [&](int b) {
+    return b < 2 ? kh * D + b * 64
+                 : (b < 4 ? Hk * D + kh * D + (b - 2) * 64 : 2 * Hk * D + kh * R * D + (b - 4) * 64);
+  };
+  if (tid == 0) {
+    mbar_init(&xbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&xbar, 8u * XBOX_BYTES);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) tma_load_2d(xt + b * XSUB, &tmx, gch(b), seq0 + c0 - (KC - 1), &xbar);
+    ok = mbar_wait_bounded(&xbar, 0) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!ok) {
+    if (tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+    return;
+  }
+  if (c == 0) {
+    // the halo rows of the first chunk are the conv state
+    for (int t = tid; t < (KC - 1) * 64; t += kThreads) {
+      const int r = t >> 6, q8 = t & 63, b = q8 >> 3, cc = (q8 & 7) * 8;
+      *reinterpret_cast<uint4*>(xt + b * XSUB + tc::sw128_offset(r, cc)) =
+          *reinterpret_cast<const uint4*>(tail + (size_t)r * C + gch(b) + cc);
+    }
+    __syncthreads();
+  }
   const int tq = tid >> 4, g = tid & 15;
   const int i0 = 4 * tq;
   const float inv_sqrt_d = rsqrtf((float)D);
@@ -84,6 +127,7 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(FwdParams p) {
   for (int part = 0; part < 2 + R; ++part) {  // q, k, v of head 2kh, v of head 2kh+1
     const int ch = part == 0 ? kh * D : (part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * R + part - 2) * D);
     const int gc = ch + g * 8;
+    const int lc = part * D + g * 8;  // local channel: box lc / 64, column lc % 64
     float wt[KC][8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -103,16 +147,10 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(FwdParams p) {
       for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
 #pragma unroll
     for (int rr = 0; rr < 4 + KC - 1; ++rr) {
-      const int pos = c0 + i0 + rr - (KC - 1);  // position inside the sequence
       float xv[8];
-      if (pos < 0)
-        load8(tail + (size_t)(KC - 1 + pos) * C + gc, xv);
-      else if (pos < L)
-        load8(x + (size_t)(seq0 + pos) * C + gc, xv);
-      else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xv[e] = 0.f;
-      }
+      load8(reinterpret_cast<const __nv_bfloat16*>(xt + (lc >> 6) * XSUB +
+                                                   tc::sw128_offset(i0 + rr, lc & 63)),
+            xv);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int j = rr - t;
@@ -161,10 +199,14 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(FwdParams p) {
 
 }  // namespace
 
-cudaError_t launch_prep(const FwdParams& p, int max_chunks, cudaStream_t stream) {
+cudaError_t launch_prep(const FwdParams& p, const void* x_map, int max_chunks,
+                        cudaStream_t stream) {
   if (max_chunks <= 0) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   dim3 grid(max_chunks, p.Hk);
-  prep_kernel<<<grid, kThreads, 0, stream>>>(p);
+  prep_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, *static_cast<const CUtensorMap*>(x_map));
   return cudaGetLastError();
 }
 
