@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
     lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, I, P]
     lib.gdn_diag_umma_gemm.restype = I
+    lib.gdn_diag_umma_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, I, P]
+    lib.gdn_diag_umma_gemm_ex.restype = I
     lib.gdn_status_string.argtypes = [I]
     lib.gdn_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -209,6 +211,16 @@ def diag_umma_gemm(A, B, C, D, operand_f16=False, stream=None) -> None:
     _check(load().gdn_diag_umma_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K,
                                      1 if operand_f16 else 0, _stream(stream)),
            "gdn_diag_umma_gemm")
+
+
+def diag_umma_gemm_ex(A, B, C, D, operand_f16=False, a_mn=False, b_mn=False,
+                      stream=None) -> None:
+    """gdn_diag_umma_gemm_ex: the same GEMM with A and/or B staged MN-major."""
+    N, K = B.shape
+    _check(load().gdn_diag_umma_gemm_ex(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K,
+                                        1 if operand_f16 else 0, 1 if a_mn else 0,
+                                        1 if b_mn else 0, _stream(stream)),
+           "gdn_diag_umma_gemm_ex")
 
 
 def varlen_forward_noalloc(pool_mem, num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align,

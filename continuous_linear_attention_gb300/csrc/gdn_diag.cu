@@ -13,33 +13,46 @@ namespace {
 
 constexpr int kM = 128;
 
+// Shared tiles: A at byte 0, B at byte kBOff of the 1024-aligned region.
+// K-major tiles are K/64 K-blocks of 128 (A) or N (B) rows; MN-major tiles
+// (K = 64 only) are 64-wide M/N blocks of K rows, kMnStride bytes apart.
+constexpr uint32_t kBOff = 80 * 1024;
+constexpr uint32_t kMnStride = 64 * 128;
+constexpr uint32_t kSmem = 160 * 1024 + 1024;
+
 template <typename E>
 __global__ void __launch_bounds__(128, 1)
 diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
-                 const float* __restrict__ Cin, float* __restrict__ D, int N, int K,
-                 unsigned* err) {
+                 const float* __restrict__ Cin, float* __restrict__ D, int N, int K, int a_mn,
+                 int b_mn, unsigned* err) {
   extern __shared__ unsigned char smem_raw[];
   // swizzled tiles need 1024-byte alignment: round the dynamic base up
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  // A tile: K/64 K-blocks of 128 rows (16 KiB each); B tile: K/64 K-blocks of N rows
   unsigned char* a_tile = smem;
-  unsigned char* b_tile = smem + (size_t)(K / 64) * kM * 128;
+  unsigned char* b_tile = smem + kBOff;
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int ok;
   const int tid = threadIdx.x;
-  const int kblocks = K / 64;
   const uint32_t a_kb = kM * 128, b_kb = (uint32_t)N * 128;
-  for (int kb = 0; kb < kblocks; ++kb) {
-    for (int k0 = 0; k0 < 64; k0 += 8) {
-      float v[8];
-      for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(A[(size_t)tid * K + kb * 64 + k0 + j]);
-      tc::sw128_store8<E>(a_tile + kb * a_kb, tid, k0, v);
-      for (int r = tid; r < N; r += 128) {
-        for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(B[(size_t)r * K + kb * 64 + k0 + j]);
-        tc::sw128_store8<E>(b_tile + kb * b_kb, r, k0, v);
-      }
-    }
+  // element (row r, k) of an operand with `rows` rows -> byte offset in its tile
+  auto off = [&](bool mn, uint32_t kb_stride, int r, int k) -> uint32_t {
+    return mn ? (uint32_t)(r >> 6) * kMnStride + tc::sw128_offset(k, r & 63)
+              : (uint32_t)(k >> 6) * kb_stride + tc::sw128_offset(r, k & 63);
+  };
+  for (int idx = tid; idx < kM * K; idx += 128) {
+    const int r = idx / K, k = idx % K;
+    const float v = __bfloat162float(A[idx]);
+    unsigned char* dst = a_tile + off(a_mn != 0, a_kb, r, k);
+    if (std::is_same<E, __half>::value) *reinterpret_cast<__half*>(dst) = __float2half_rn(v);
+    else *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(v);
+  }
+  for (int idx = tid; idx < N * K; idx += 128) {
+    const int r = idx / K, k = idx % K;
+    const float v = __bfloat162float(B[idx]);
+    unsigned char* dst = b_tile + off(b_mn != 0, b_kb, r, k);
+    if (std::is_same<E, __half>::value) *reinterpret_cast<__half*>(dst) = __float2half_rn(v);
+    else *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(v);
   }
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -65,8 +78,12 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
   if (tid == 0) {
     tc::fence_after_sync();
     constexpr bool kF16 = std::is_same<E, __half>::value;
-    tc::mma_tile(tmem, smem_u32(a_tile), a_kb, smem_u32(b_tile), b_kb, kblocks,
-                 kF16 ? tc::idesc_f16_f32(kM, N) : tc::idesc_bf16_f32(kM, N), Cin != nullptr);
+    const tc::Opnd a{smem_u32(a_tile), a_mn ? kMnStride : a_kb, a_mn != 0};
+    const tc::Opnd b{smem_u32(b_tile), b_mn ? kMnStride : b_kb, b_mn != 0};
+    tc::mma_op(tmem, a, b, K / 16,
+               kF16 ? tc::idesc_f16_f32(kM, N, a_mn != 0, b_mn != 0)
+                    : tc::idesc_bf16_f32(kM, N, a_mn != 0, b_mn != 0),
+               Cin != nullptr);
     tc::commit(&bar);
     ok = mbar_wait_bounded(&bar, 0) ? 1 : 0;
   }
@@ -90,28 +107,35 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
 }  // namespace
 }  // namespace gdn
 
-extern "C" int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, int N,
-                                  int K, int operand_f16, void* stream) {
+extern "C" int gdn_diag_umma_gemm_ex(const void* A, const void* B, const float* C, float* D,
+                                     int N, int K, int operand_f16, int a_mn, int b_mn,
+                                     void* stream) {
   if (!A || !B || !D) return GDN_ERR_NULL;
   if ((N != 64 && N != 128 && N != 192 && N != 256) || (K != 64 && K != 128))
     return GDN_ERR_DIMS;
+  if ((a_mn || b_mn) && K != 64) return GDN_ERR_DIMS;
   if (((uintptr_t)A & 15) || ((uintptr_t)B & 15) || ((uintptr_t)D & 15) || ((uintptr_t)C & 15))
     return GDN_ERR_ALIGN;
   static unsigned* err = nullptr;
   if (!err && cudaMalloc((void**)&err, sizeof(unsigned)) != cudaSuccess) return GDN_ERR_CUDA;
-  const size_t smem = (size_t)(K / 64) * (128 + N) * 128 + 1024;
+  const int smem = (int)gdn::kSmem;
   if (operand_f16) {
     if (cudaFuncSetAttribute(gdn::diag_umma_kernel<__half>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return GDN_ERR_CUDA;
     gdn::diag_umma_kernel<__half><<<1, 128, smem, (cudaStream_t)stream>>>(
-        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, err);
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, a_mn, b_mn, err);
   } else {
     if (cudaFuncSetAttribute(gdn::diag_umma_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return GDN_ERR_CUDA;
     gdn::diag_umma_kernel<__nv_bfloat16><<<1, 128, smem, (cudaStream_t)stream>>>(
-        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, err);
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, C, D, N, K, a_mn, b_mn, err);
   }
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, int N,
+                                  int K, int operand_f16, void* stream) {
+  return gdn_diag_umma_gemm_ex(A, B, C, D, N, K, operand_f16, 0, 0, stream);
 }

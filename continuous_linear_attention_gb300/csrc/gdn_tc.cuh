@@ -76,15 +76,50 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, 10-12 = 1) or fp16 (both 0), both K-major
-// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Descriptor of an MN-major 128-byte swizzled tile: each 128-byte row holds
+// 64 consecutive M (or N) elements of one K index, rows of 8 consecutive K
+// indices form a 1024-byte swizzle group (stride byte offset 1024), and the
+// next 64 M/N elements sit `mn_stride` bytes further (leading byte offset).
+// A 2-D TMA box of [K rows][64 columns] with 128-byte swizzle lands in exactly
+// this layout, so a token-major tile is an MN-major operand as loaded.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t smem_addr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_stride & 0x3FFFFu) >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
 }
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1) or fp16 (both 0), A / B MN-major
+// when bit 15 / 16 is set (K-major otherwise), N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
+                                                      bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn = false,
+                                                     bool b_mn = false) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// One MMA operand in shared memory.  K-major: `addr` is the first K-block
+// tile, `stride` the byte distance between K-blocks of 64.  MN-major: `addr`
+// is the first row (K index), `stride` the distance between 64-wide M/N
+// blocks.
+struct Opnd {
+  uint32_t addr, stride;
+  bool mn;
+};
+
+// Descriptor of K step s (elements 16s .. 16s+15) of an operand.
+__device__ __forceinline__ uint64_t opnd_desc(const Opnd& o, int s) {
+  return o.mn ? sw128_desc_mn(o.addr + (uint32_t)s * 2048u, o.stride)
+              : sw128_desc(o.addr + (uint32_t)(s >> 2) * o.stride + (uint32_t)(s & 3) * 32u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K=16 step (cta_group::1).
@@ -111,6 +146,15 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_smem, uint3
       mma_bf16(d_tmem, ad, bd, idesc, (accumulate || kb > 0 || ks > 0) ? 1u : 0u);
     }
   }
+}
+
+// D (M=128 rows) (+)= A * B^T over K = 16 * ksteps for operands of either
+// major-ness; idesc must carry the matching MN-major bits.
+__device__ __forceinline__ void mma_op(uint32_t d_tmem, const Opnd& a, const Opnd& b, int ksteps,
+                                       uint32_t idesc, bool accumulate) {
+#pragma unroll 4
+  for (int s = 0; s < ksteps; ++s)
+    mma_bf16(d_tmem, opnd_desc(a, s), opnd_desc(b, s), idesc, (accumulate || s > 0) ? 1u : 0u);
 }
 
 // Arrive on `bar` once every MMA issued so far by this thread has completed.

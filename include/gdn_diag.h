@@ -13,6 +13,12 @@
  * the fp16 form of the MMA (the chunked kernel's operand type), else bf16.  N in {64, 128, 192, 256}, K in {64, 128}.  Returns GDN_OK
  * or GDN_ERR_NULL / GDN_ERR_DIMS / GDN_ERR_ALIGN / GDN_ERR_CUDA (nothing
  * launched on error).  Stream-ordered, no synchronisation.
+ *
+ * gdn_diag_umma_gemm_ex is the same GEMM with a choice of operand layout:
+ * a_mn / b_mn != 0 stage A / B MN-major (each 128-byte row holds 64
+ * consecutive M / N elements of one K index, the layout a 2-D TMA box of a
+ * token-major matrix lands in) and set the matching instruction-descriptor
+ * bits.  MN-major operands need K == 64 (GDN_ERR_DIMS otherwise).
  */
 #ifndef GDN_DIAG_H_
 #define GDN_DIAG_H_
@@ -23,6 +29,8 @@ extern "C" {
 
 int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, int N, int K,
                        int operand_f16, void* stream);
+int gdn_diag_umma_gemm_ex(const void* A, const void* B, const float* C, float* D, int N, int K,
+                          int operand_f16, int a_mn, int b_mn, void* stream);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported():
     assert "gdn_varlen_forward" in names and "gdn_state_pool_create" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert sorted(binding.EXPORTED + ["gdn_diag_umma_gemm"]) == names
+    assert sorted(binding.EXPORTED + ["gdn_diag_umma_gemm", "gdn_diag_umma_gemm_ex"]) == names
 
 
 @pytest.mark.parametrize("dims", [

@@ -22,3 +22,22 @@ def test_umma_gemm_matches_torch(N, K, acc, f16):
     torch.cuda.synchronize()
     ref = A.float() @ B.float().T + (C if acc else 0)
     torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+@pytest.mark.parametrize("major", ["a_mn", "b_mn", "both"])
+@pytest.mark.parametrize("f16", [False, True])
+def test_umma_gemm_mn_major_matches_torch(N, major, f16):
+    """MN-major operands (the layout of a token-major TMA tile) give the same
+    product as K-major ones."""
+    K = 64
+    g = torch.Generator(device="cuda").manual_seed(7 * N + len(major))
+    A = torch.randn(128, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    C = torch.randn(128, N, device="cuda", generator=g)
+    D = torch.full((128, N), float("nan"), device="cuda")
+    binding.diag_umma_gemm_ex(A, B, C, D, operand_f16=f16, a_mn=major in ("a_mn", "both"),
+                              b_mn=major in ("b_mn", "both"))
+    torch.cuda.synchronize()
+    ref = A.float() @ B.float().T + C
+    torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
