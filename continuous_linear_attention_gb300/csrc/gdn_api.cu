@@ -31,10 +31,30 @@ namespace {
 
 size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
-// Bytes of prefill scratch per packed row: q~|k~ of every k-head and v of
-// every v-head, fp16.
+// Prefill scratch, one row per packed token, as consecutive token-major arrays
+// (each row a multiple of 16 bytes): q~|k~ of every k-head and v of every
+// v-head (fp16), G and beta of every v-head (fp32), -w and u of every v-head
+// (fp16) and the rows of P of every v-head (fp16, 64 each).
+enum ScrPart { kScrQK = 0, kScrV, kScrG, kScrW, kScrU, kScrP, kScrParts };
+size_t scratch_part_bytes(const gdn_pool* p, int part) {
+  switch (part) {
+    case kScrQK: return (size_t)2 * p->Hk * p->dk * 2;
+    case kScrV: return (size_t)p->Hv * p->dv * 2;
+    case kScrG: return (size_t)p->Hv * 2 * 4;
+    case kScrW: return (size_t)p->Hv * p->dk * 2;
+    case kScrU: return (size_t)p->Hv * p->dv * 2;
+    default: return (size_t)p->Hv * 64 * 2;
+  }
+}
 size_t scratch_row_bytes(const gdn_pool* p) {
-  return ((size_t)2 * p->Hk * p->dk + (size_t)p->Hv * p->dv) * 2;
+  size_t b = 0;
+  for (int i = 0; i < kScrParts; ++i) b += scratch_part_bytes(p, i);
+  return b;
+}
+void* scratch_part(const gdn_pool* p, int part) {
+  size_t off = 0;
+  for (int i = 0; i < part; ++i) off += scratch_part_bytes(p, i);
+  return p->scr + off * p->scr_tokens;
 }
 
 // Make the prefill scratch hold `tokens` rows (synchronous; frees the old
@@ -284,8 +304,12 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
       cudaGetLastError();
   }
   if (p->scr && p->scr_tokens >= (size_t)T) {
-    fp.scr_qk = p->scr;
-    fp.scr_v = p->scr + p->scr_tokens * (size_t)2 * p->Hk * p->dk * 2;
+    fp.scr_qk = scratch_part(p, kScrQK);
+    fp.scr_v = scratch_part(p, kScrV);
+    fp.scr_g = scratch_part(p, kScrG);
+    fp.scr_w = scratch_part(p, kScrW);
+    fp.scr_u = scratch_part(p, kScrU);
+    fp.scr_p = scratch_part(p, kScrP);
   }
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;

@@ -1,9 +1,12 @@
-// Chunked prefill kernel: the gated delta rule over sequences longer than one
-// token, in chunks of C = 64 tokens with the WY / UT-transform form, the dense
-// intra-chunk and state products on the 5th-generation tensor cores
-// (tcgen05.mma, bf16 operands from 128-byte-swizzled shared tiles, fp32
-// accumulators in tensor memory).  The recurrent state stays in tensor memory
-// (fp32) for the whole sequence; only the final state is written back.
+// Fused chunked prefill kernel: the gated delta rule over sequences longer
+// than one token, in chunks of C = 64 tokens with the WY / UT-transform form,
+// conv prologue included, the dense intra-chunk and state products on the
+// 5th-generation tensor cores (tcgen05.mma, fp16 operands from
+// 128-byte-swizzled shared tiles, fp32 accumulators in tensor memory).  The
+// recurrent state stays in tensor memory (fp32) for the whole sequence; only
+// the final state is written back.  This single-kernel form runs when the pool
+// has no prefill scratch (see gdn_state_pool_reserve); with scratch, the same
+// computation runs split into prep_kernel, intra_kernel and seq_kernel.
 //
 // Persistent CTAs (8 warps, one per SM) pull (sequence, v-head) chains,
 // longest sequences first.
@@ -69,8 +72,7 @@ constexpr uint32_t OFF_KPT = 65536;    // k'^T        128 x 128 B
 constexpr uint32_t OFF_P = 81920;      // P           64 x 128 B
 constexpr uint32_t OFF_T = 90112;      // T           64 x 128 B
 constexpr uint32_t OFF_RU = 98304;     // R^T, then U^T   128 x 128 B
-constexpr uint32_t OFF_BV = 114688;    // fused: beta v fp16 [64][BVP]
-constexpr uint32_t OFF_V = OFF_BV;     // split: v tile, two 64 x 64 fp16 boxes, swizzled
+constexpr uint32_t OFF_BV = 114688;    // beta v fp16 [64][BVP]
 constexpr uint32_t OFF_AM = 132096;    // A fp32 [64][AP]; then the out tile bf16 [64][128]
 constexpr uint32_t OFF_XT = 150528;    // 6 staged x boxes (q0 q1 k0 k1 v0 v1), 1024-aligned
 constexpr uint32_t OFF_G = 205824;     // G fp32 [64]
@@ -132,13 +134,9 @@ __device__ __forceinline__ void track_abs(float& m, const float* v, int n) {
   for (int e = 0; e < n; ++e) m = fmaxf(m, fabsf(v[e]));
 }
 
-// kFused: the conv prologue runs here from 2-D TMA boxes of x (tm0 = x map).
-// Otherwise prep_kernel has written q~, k~ and v to the pool's scratch and
-// this kernel loads them as TMA tiles (tm0 = q~|k~ map, tm1 = v map).
-template <bool kFused>
+// The conv prologue runs here from 2-D TMA boxes of x (tmx = x map).
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
-             const __grid_constant__ CUtensorMap tm1) {
+chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t bar;   // MMA completion
@@ -216,28 +214,15 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
     return lc < D ? kh * D + lc
                   : (lc < 2 * D ? Hk * D + kh * D + (lc - D) : 2 * Hk * D + h * D + (lc - 2 * D));
   };
-  // Stage chunk cc's inputs, thread 0.  Fused: the x rows (packed rows
+  // Stage chunk cc's inputs, thread 0: the x rows (packed rows
   // seq0 + cc*64 - 3 .. + 63) of this chain's q, k and v channels into XT, six
   // 64-channel x 67-row TMA boxes, 128-byte swizzled; rows outside the
-  // sequence are loaded too but never used.  Split: the q~ and k~ rows of the
-  // k-head straight into the swizzled [q~ ; k~] operand tile (four 64 x 64
-  // boxes) and the v rows of the v-head into the v tile (two boxes).
+  // sequence are loaded too but never used.
   auto stage = [&](int cc) {
-    if constexpr (kFused) {
-      const int r0 = seq0 + cc * CH - (KC - 1);
-      mbar_arrive_expect_tx(&xbar, 6u * XBOX_BYTES);
+    const int r0 = seq0 + cc * CH - (KC - 1);
+    mbar_arrive_expect_tx(&xbar, 6u * XBOX_BYTES);
 #pragma unroll
-      for (int b6 = 0; b6 < 6; ++b6) tma_load_2d(XT + b6 * XSUB, &tm0, gch(b6 * 64), r0, &xbar);
-    } else {
-      const int r0 = seq0 + cc * CH;
-      mbar_arrive_expect_tx(&xbar, 6u * 64u * 64u * 2u);
-      tma_load_2d(sm + OFF_QK, &tm0, kh * 2 * D, r0, &xbar);
-      tma_load_2d(sm + OFF_QK + KB_STRIDE, &tm0, kh * 2 * D + 64, r0, &xbar);
-      tma_load_2d(sm + OFF_QK + CH * 128, &tm0, kh * 2 * D + D, r0, &xbar);
-      tma_load_2d(sm + OFF_QK + KB_STRIDE + CH * 128, &tm0, kh * 2 * D + D + 64, r0, &xbar);
-      tma_load_2d(sm + OFF_V, &tm1, h * D, r0, &xbar);
-      tma_load_2d(sm + OFF_V + CH * 128, &tm1, h * D + 64, r0, &xbar);
-    }
+    for (int b6 = 0; b6 < 6; ++b6) tma_load_2d(XT + b6 * XSUB, &tmx, gch(b6 * 64), r0, &xbar);
   };
   // gate inputs of chunk cc, token tid (threads < 64)
   auto load_gates = [&](int cc, float& a_, float& b_) {
@@ -251,12 +236,10 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
   if (tid == 0) stage(0);
   float a_nx = 0.f, b_nx = 0.f;
   load_gates(0, a_nx, b_nx);
-  if constexpr (kFused) {
-    for (int lc = tid; lc < kLocalCh; lc += kThreads) {
-      const int gc = gch(lc);
+  for (int lc = tid; lc < kLocalCh; lc += kThreads) {
+    const int gc = gch(lc);
 #pragma unroll
-      for (int j = 0; j < KC; ++j) WS[j * kLocalCh + lc] = __bfloat162float(wconv[(size_t)gc * KC + j]);
-    }
+    for (int j = 0; j < KC; ++j) WS[j * kLocalCh + lc] = __bfloat162float(wconv[(size_t)gc * KC + j]);
   }
   const float A_neg = -__expf(p.A_log[h]);
   const float dtb = p.dt_bias[h];
@@ -294,7 +277,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
     xphase ^= 1;
     const float GC = G[CH - 1];
     if (tid < CH) DSC[tid] = __expf(GC - G[tid]);
-    if (kFused && c == 0) {
+    if (c == 0) {
       // the first chunk's three halo rows are the conv state, not packed rows
       // of another sequence: overwrite the staged ones (16 bytes per thread)
       if (tid < 3 * 48) {
@@ -310,7 +293,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
     // Thread (tq, g) computes 8-channel group g of q, of k and of v for the four
     // tokens 4tq .. 4tq+3 with a sliding window over 7 staged rows; the 16
     // threads of a token quad reduce the norms with shuffles.
-    if constexpr (kFused) {
+    {
       const int tq = tid >> 4, g = tid & 15;
       const int i0 = 4 * tq;
 #pragma unroll
@@ -429,7 +412,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
     }
     // fused: the staged rows are consumed; bring in the next chunk's while
     // this one runs
-    if (kFused && c + 1 < n_chunks) {
+    if (c + 1 < n_chunks) {
       if (tid == 0) stage(c + 1);
       load_gates(c + 1, a_nx, b_nx);
     }
@@ -497,33 +480,17 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
       tc::tmem_ld32(tmem + lane + TM_Y + chalf * 32, yr);
       tc::tmem_wait_ld();
       const int v = r128;
-      const unsigned char* vcol = sm + OFF_V + (v >> 6) * (CH * 128) + (v & 7) * 2;
-      const uint32_t vchunk = (uint32_t)((v & 63) >> 3);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
         const int ib = chalf * 32 + g8 * 8;
         const float4 f0 = *reinterpret_cast<const float4*>(F + ib);
         const float4 f1 = *reinterpret_cast<const float4*>(F + ib + 4);
         const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-        float bv8[8];
-        if constexpr (!kFused) {
-          const float4 b0 = *reinterpret_cast<const float4*>(BETA + ib);
-          const float4 b1 = *reinterpret_cast<const float4*>(BETA + ib + 4);
-          bv8[0] = b0.x; bv8[1] = b0.y; bv8[2] = b0.z; bv8[3] = b0.w;
-          bv8[4] = b1.x; bv8[5] = b1.y; bv8[6] = b1.z; bv8[7] = b1.w;
-        }
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = ib + e;
-          float bvv;
-          if constexpr (kFused) {
-            bvv = __half2float(BV[i * BVP + v]);
-          } else {
-            // row i of the swizzled v box: 8-row group ib/8, row e, chunk vchunk ^ e
-            bvv = bv8[e] * __half2float(*reinterpret_cast<const __half*>(
-                               vcol + (ib >> 3) * 1024 + e * 128 + ((vchunk ^ (uint32_t)e) << 4)));
-          }
+          const float bvv = __half2float(BV[i * BVP + v]);
           v8[e] = i < n ? bvv - fv[e] * yr[g8 * 8 + e] : 0.f;
         }
         track_abs(amax, v8, 8);
@@ -531,11 +498,6 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tm0,
       }
     }
     __syncthreads();
-    // split: the operand and v tiles are consumed; bring in the next chunk's
-    if (!kFused && c + 1 < n_chunks) {
-      if (tid == 0) stage(c + 1);
-      load_gates(c + 1, a_nx, b_nx);
-    }
     // ---------------- T = (I + A)^{-1}: diagonal 16 x 16 blocks, column per thread
     if (tid < CH) {
       const int b = tid >> 4, m = tid & 15;
@@ -719,21 +681,25 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Tensor map of x [T][C] bf16 for the chunk kernel's staging boxes
-// (64 channels x 67 rows, 128-byte swizzle, zero fill outside).
-// Tensor map of a row-major 16-bit [rows][cols] array read in boxes of
-// 64 columns x box_rows rows, 128-byte swizzled, zero fill outside.
-cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rows, int cols,
-                     int box_rows) {
+EncodeTiledFn encoder() {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                                      cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return nullptr;
     encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
+  return encode;
+}
+
+// Tensor map of a row-major 16-bit [rows][cols] array read in boxes of
+// 64 columns x box_rows rows, 128-byte swizzled, zero fill outside.
+cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rows, int cols,
+                     int box_rows) {
+  EncodeTiledFn encode = encoder();
+  if (!encode) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
@@ -744,18 +710,33 @@ cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of the fp32 gate scratch [rows][cols] read in boxes of 4 columns
+// (G and beta of two v-heads, 16 bytes) x 64 rows, unswizzled.
+cudaError_t make_map_gates(CUtensorMap* m, const void* base, int rows, int cols) {
+  EncodeTiledFn encode = encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {4, (cuuint32_t)CH};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   if (max_pre <= 0) return cudaSuccess;
   const bool fused = p.scr_qk == nullptr;
-  cudaError_t e = fused ? cudaFuncSetAttribute(chunk_kernel<true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)SMEM_BYTES)
-                        : cudaFuncSetAttribute(chunk_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (fused) {
+    e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+  }
   static int num_sms = 0;
   if (num_sms == 0) {
     int dev = 0;
@@ -765,24 +746,30 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   }
   const long long chains = (long long)max_pre * p.Hv;
   const int grid = (int)(chains < num_sms ? chains : num_sms);
-  CUtensorMap tm0, tm1;
   if (fused) {
-    e = make_map(&tm0, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
-    if (e != cudaSuccess) return e;
-    tm1 = tm0;
-    chunk_kernel<true><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tm0, tm1);
-  } else {
-    // conv prologue first: at most T/64 + (number of prefill sequences) chunks
     CUtensorMap tmx;
     e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
     if (e != cudaSuccess) return e;
-    e = launch_prep(p, &tmx, p.T / CH + max_pre, stream);
+    chunk_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tmx);
+  } else {
+    // split: conv prologue and gates (prep_kernel), the state-independent
+    // products of every chunk (intra_kernel), then the recurrence over the
+    // chains (seq_kernel); at most T/64 + (number of prefill sequences) chunks
+    const int max_chunks = p.T / CH + max_pre;
+    CUtensorMap tmx, tqk, tv, tw, tu, tp, tg;
+    e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
+    if (e == cudaSuccess) e = make_map(&tqk, p.scr_qk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hk * 2 * D, CH);
+    if (e == cudaSuccess) e = make_map(&tv, p.scr_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
+    if (e == cudaSuccess) e = make_map(&tw, p.scr_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
+    if (e == cudaSuccess) e = make_map(&tu, p.scr_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
+    if (e == cudaSuccess) e = make_map(&tp, p.scr_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * CH, CH);
+    if (e == cudaSuccess) e = make_map_gates(&tg, p.scr_g, p.T, p.Hv * 2);
     if (e != cudaSuccess) return e;
-    e = make_map(&tm0, p.scr_qk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hk * 2 * D, CH);
+    e = launch_prep(p, &tmx, max_chunks, stream);
+    if (e == cudaSuccess) e = launch_intra(p, &tqk, &tv, &tg, max_chunks, stream);
+    const void* maps[5] = {&tqk, &tw, &tu, &tp, &tg};
+    if (e == cudaSuccess) e = launch_seq(p, maps, grid, stream);
     if (e != cudaSuccess) return e;
-    e = make_map(&tm1, p.scr_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
-    if (e != cudaSuccess) return e;
-    chunk_kernel<false><<<grid, kThreads, SMEM_BYTES, stream>>>(p, tm0, tm1);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -65,10 +65,20 @@ struct FwdParams {
   int T, N, Hk, Hv, C, K, num_blocks;
   int max_seqlen_hint;  // 0 = unknown; else longer sequences are flagged and skipped
   WorkArea work;
-  // prefill scratch (fp16): q~|k~ [T][Hk][2][d] and v [T][Hv][d]; nullptr when
-  // the pool has none for this many tokens (the fused chunked kernel is used)
+  // prefill scratch, token-major over the packed rows; nullptr when the pool
+  // has none for this many tokens (the fused chunked kernel is used):
+  //   scr_qk [T][Hk][2][d] fp16  q~ | k~          (prep_kernel)
+  //   scr_v  [T][Hv][d]    fp16  v                (prep_kernel)
+  //   scr_g  [T][Hv][2]    fp32  G (in-chunk cumulative gate), beta (prep_kernel)
+  //   scr_w  [T][Hv][d]    fp16  -w               (intra_kernel)
+  //   scr_u  [T][Hv][d]    fp16  u = T diag(beta) v  (intra_kernel)
+  //   scr_p  [T][Hv][64]   fp16  row of P         (intra_kernel)
   void* scr_qk = nullptr;
   void* scr_v = nullptr;
+  void* scr_g = nullptr;
+  void* scr_w = nullptr;
+  void* scr_u = nullptr;
+  void* scr_p = nullptr;
 };
 
 // Launchers (each returns a cudaError_t from the launch).
@@ -91,6 +101,14 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
 // x_map: the CUtensorMap of x (boxes of 64 channels x 67 rows, 128-byte swizzle).
 cudaError_t launch_prep(const FwdParams& p, const void* x_map, int max_chunks,
                         cudaStream_t stream);
+// The state-independent products of every prefill chunk (u, -w, P), one CTA
+// per (chunk, k-head).  qk_map, v_map: q~|k~ and v scratch in 64 x 64 boxes;
+// g_map: gate scratch in boxes of 4 floats x 64 rows.
+cudaError_t launch_intra(const FwdParams& p, const void* qk_map, const void* v_map,
+                         const void* g_map, int max_chunks, cudaStream_t stream);
+// The state recurrence over the prefill chains; maps: q~|k~, -w, u, P (64 x 64
+// fp16 boxes) and gates.
+cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

@@ -11,6 +11,10 @@
 // chunked kernel, halves the q/k conv work, and keeps the chunked kernel's
 // instruction stream for the recurrence.
 //
+// The same CTA writes the gates of its chunk for both v-heads of the k-head:
+//   g[row][h] = (G, beta), G the inclusive cumulative sum of the log decay
+//   g = -e^{A_log} softplus(a + dt_bias) inside the 64-token chunk.
+//
 // One CTA per (64-token chunk of a prefill sequence, k-head); chunks are
 // found from the scheduler's chunk prefix over the sorted prefill list.  The
 // CTA's 67 x rows (3 halo + 64) of its 512 channels arrive as eight 2-D TMA
@@ -64,6 +68,7 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
   extern __shared__ unsigned char smem_raw[];
   unsigned char* xt = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t xbar;
+  __shared__ float gtot[2];
   __shared__ int ok;
   int32_t* hdr = p.work.header();
   const int n_chunks = hdr[kPreChunks];
@@ -103,9 +108,37 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
     mbar_arrive_expect_tx(&xbar, 8u * XBOX_BYTES);
 #pragma unroll
     for (int b = 0; b < 8; ++b) tma_load_2d(xt + b * XSUB, &tmx, gch(b), seq0 + c0 - (KC - 1), &xbar);
-    ok = mbar_wait_bounded(&xbar, 0) ? 1 : 0;
   }
+  // gates of the chunk's tokens for the k-head's two v-heads (threads 0..127,
+  // token tid % 64 of head 2kh + tid / 64): g = -e^{A_log} softplus(a + dt_bias),
+  // beta = sigmoid(b), and the inclusive cumulative sum G of g inside the chunk
+  float gcum = 0.f, gbeta = 0.f;
+  if (tid < R * CH) {
+    const int h = kh * R + (tid >> 6), i = tid & 63;
+    if (i < n) {
+      const size_t row = (size_t)(seq0 + c0 + i);
+      const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(p.a);
+      const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
+      gcum = -__expf(p.A_log[h]) * softplus_f32(__bfloat162float(av[row * Hv + h]) + p.dt_bias[h]);
+      gbeta = sigmoid_f32(__bfloat162float(bv[row * Hv + h]));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, gcum, o);
+      if ((tid & 31) >= o) gcum += t;
+    }
+    if ((tid & 63) == 31) gtot[tid >> 6] = gcum;
+  }
+  if (tid == 0) ok = mbar_wait_bounded(&xbar, 0) ? 1 : 0;
   __syncthreads();
+  if (tid < R * CH) {
+    const int h = kh * R + (tid >> 6), i = tid & 63;
+    if (i >= 32) gcum += gtot[tid >> 6];
+    if (i < n) {
+      float2* dst = reinterpret_cast<float2*>(p.scr_g) + (size_t)(seq0 + c0 + i) * Hv + h;
+      *dst = make_float2(gcum, gbeta);
+    }
+  }
   if (!ok) {
     if (tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
     return;

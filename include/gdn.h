@@ -130,12 +130,15 @@ int gdn_state_pool_layout(const gdn_pool_t* pool, size_t* block_stride, size_t* 
  * and never shared).  dst must not be 0 (the trash block).  Stream-ordered. */
 int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, void* stream);
 
-/* Prefill scratch of the pool.  Sequences longer than one token run as two
- * kernels when the pool has scratch for the call's T rows (fp16 q~|k~ and v
- * of every row: (2*Hk*d_k + Hv*d_v) * 2 bytes per row, shared by the layers):
- * a conv/normalisation kernel writes it and the chunked kernel loads it with
- * TMA.  Without scratch they run as one fused kernel (same results within
- * rounding).  By default the first gdn_varlen_forward with more rows than the
+/* Prefill scratch of the pool.  Sequences longer than one token run as three
+ * kernels when the pool has scratch for the call's T rows, token-major and
+ * shared by the layers: per row q~|k~ and v (fp16, (2*Hk*d_k + Hv*d_v) * 2
+ * bytes), the in-chunk cumulative gate and beta (fp32, Hv * 8 bytes) and the
+ * state-independent chunk products u, -w and the row of P (fp16,
+ * Hv * (d_v + d_k + 64) * 2 bytes).  A conv/normalisation kernel writes the
+ * first part, a chunk-parallel kernel the products, and the recurrence kernel
+ * loads them with TMA.  Without scratch they run as one fused kernel (same
+ * results within rounding).  By default the first gdn_varlen_forward with more rows than the
  * scratch holds grows it (cudaMalloc; freeing the old buffer waits for the
  * device), except during stream capture, where the fused kernel is used.
  *   max_tokens > 0 : grow the scratch to at least max_tokens rows now
