@@ -1,6 +1,6 @@
 // State-independent half of the chunked prefill, fully parallel over the
-// 64-token chunks of the prefill sequences: one CTA per (chunk, k-head) does
-// the work of both v-heads of the k-head.
+// 64-token chunks of the prefill sequences: one CTA per (chunk, v-head),
+// three CTAs per SM.
 //
 // With G_i the inclusive cumulative gate inside the chunk, beta_i the write
 // strength and q~/k~ the normalised rows (all from prep_kernel), the chunk-64
@@ -19,11 +19,10 @@
 //   U0[row][h][0..127] = u_i = (T diag(beta) V)_i   (the updates for a zero state)
 //   Wn[row][h][0..127] = -w_i = -(T diag(beta e^G) K~)_i
 //   P [row][h][0..63]  = P_ij
-// Tensor cores: X = [q~ ; k~] k~^T (one 128 x 64 x 128 MMA shared by both
-// v-heads), then per v-head [T diag(beta e^G) ; T diag(beta)] times k~ and
-// times v (128 x 128 x 64 each, k~ and v as MN-major operands straight from
-// their token-major tiles: rows 0..63 of the first product are w, rows
-// 64..127 of the second are u).  CUDA cores: the masks, the blocked forward
+// Tensor cores: X = [q~ ; k~] k~^T (128 x 64 x 128), then
+// [-T diag(beta e^G) ; T diag(beta)] times k~ and times v (128 x 128 x 64
+// each, k~ and v as MN-major operands straight from their token-major tiles:
+// rows 0..63 of the first product are -w, rows 64..127 of the second are u).  CUDA cores: the masks, the blocked forward
 // substitution of T (16 x 16 diagonal blocks, then the off-diagonal blocks
 // level by level) and the conversions.  Rows of the tiles past the end of the
 // sequence are zeroed in shared memory first, so that no value of another
@@ -42,21 +41,19 @@ constexpr int D = 128;
 constexpr int CH = 64;
 constexpr int kThreads = 256;
 constexpr int R = 2;    // v-heads per k-head
-constexpr int AP = 68;  // pitch (floats) of the fp32 A and T rows
+constexpr int AP = 68;  // pitch (floats) of the fp32 A / T rows
 constexpr float kF16Max = 65000.f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_QK = 0;       // [q~ ; k~]: 2 K-blocks x 128 rows (32 KB)
-constexpr uint32_t OFF_V = 32768;    // v of the current v-head: two 64 x 64 boxes
-constexpr uint32_t OFF_TBE = 49152;  // [T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
-constexpr uint32_t OFF_AM = 65536;   // A fp32 [64][AP]
-constexpr uint32_t OFF_TS = 82944;   // T fp32 [64][AP]
-constexpr uint32_t OFF_Z = 100352;   // B blocks fp32 [6][16][16]
-constexpr uint32_t OFF_GT = 106496;  // gates [64][4] fp32: (G, beta) of the two v-heads
-constexpr uint32_t SMEM_BYTES = 107520 + 1024;
-constexpr uint32_t KB_STRIDE = 16384;
-constexpr uint32_t BOX = 8192;
-constexpr uint32_t TM_X = 0, TM_W = 0, TM_U = 128, TM_COLS = 256;
+constexpr uint32_t BOX = 8192;         // one 64 x 64 fp16 box
+constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of the 128-row [q~ ; k~] tile
+constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]; once X is done the q~ slots hold v
+constexpr uint32_t OFF_AT = 32768;     // A, overwritten block by block by T: fp32 [64][AP]
+constexpr uint32_t OFF_TT = 50176;     // [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
+constexpr uint32_t OFF_Z = OFF_TT;     // during the solve: B blocks fp32 [6][16][16]
+constexpr uint32_t OFF_GT = 66560;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
+constexpr uint32_t SMEM_BYTES = 67584 + 1024;
+constexpr uint32_t TM_COLS = 128;      // X (64 columns), then the 128-column products
 
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
   if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity) ? 1 : 0;
@@ -73,7 +70,7 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   return w;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg) {
   extern __shared__ unsigned char smem_raw[];
@@ -83,7 +80,8 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   __shared__ int flag;
   int32_t* hdr = p.work.header();
   const int n_chunks = hdr[kPreChunks];
-  const int gidx = blockIdx.x;
+  const int h = (int)(blockIdx.x % (unsigned)p.Hv);   // heads of a chunk run next to each other
+  const int gidx = (int)(blockIdx.x / (unsigned)p.Hv);
   if (gidx >= n_chunks) return;
   // which prefill sequence / chunk: binary search in the chunk prefix
   const int n_pre = hdr[kNPre];
@@ -95,34 +93,28 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   }
   const int s = p.work.pre()[lo];
   const int c0 = (gidx - cp[lo]) * CH;
-  const int kh = blockIdx.y;
+  const int kh = h / R, r2 = h % R;
   const int Hv = p.Hv;
   const int seq0 = p.cu[s];
   const int n = min(CH, p.cu[s + 1] - seq0 - c0);
   const int row0 = seq0 + c0;
+  const size_t orow = (size_t)row0 * Hv + h;  // (packed row, head) index of row 0
   const int tid = threadIdx.x;
   const uint32_t lane = (uint32_t)(tid & 96) << 16;  // TMEM lane quarter of this warp
   const int r128 = tid & 127;                        // TMEM row of this thread
   const int hf = tid >> 7;                           // column half of this thread
   const uint32_t sbase = smem_u32(sm);
-  float* AM = reinterpret_cast<float*>(sm + OFF_AM);
-  float* TS = reinterpret_cast<float*>(sm + OFF_TS);
+  float* AT = reinterpret_cast<float*>(sm + OFF_AT);
   float* Z = reinterpret_cast<float*>(sm + OFF_Z);
   float* GT = reinterpret_cast<float*>(sm + OFF_GT);
+  const int gc = 2 * r2;  // this head's G column in GT (beta at gc + 1)
 
-  // v rows of v-head r2 into the v buffer (thread 0)
-  auto load_v = [&](int r2) {
-    mbar_arrive_expect_tx(&vbar, 2u * BOX);
-    tma_load_2d(sm + OFF_V, &tv, (kh * R + r2) * D, row0, &vbar);
-    tma_load_2d(sm + OFF_V + BOX, &tv, (kh * R + r2) * D + 64, row0, &vbar);
-  };
   if (tid == 0) {
     mbar_init(&lbar, 1);
     mbar_init(&vbar, 1);
     mbar_init(&mbar, 1);
     fence_mbar_init();
-    load_v(0);
-    mbar_arrive_expect_tx(&lbar, 4u * 8192u + 1024u);
+    mbar_arrive_expect_tx(&lbar, 4u * BOX + 1024u);
     tma_load_2d(sm + OFF_QK, &tqk, kh * 2 * D, row0, &lbar);
     tma_load_2d(sm + OFF_QK + KB_STRIDE, &tqk, kh * 2 * D + 64, row0, &lbar);
     tma_load_2d(sm + OFF_QK + CH * 128, &tqk, kh * 2 * D + D, row0, &lbar);
@@ -146,17 +138,15 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
                                   tc::sw128_offset(row, q * 8)) = make_uint4(0, 0, 0, 0);
       }
       for (int i = n + tid; i < CH; i += kThreads) {
-        GT[i * 4 + 0] = GT[(n - 1) * 4 + 0];
-        GT[i * 4 + 1] = 0.f;
-        GT[i * 4 + 2] = GT[(n - 1) * 4 + 2];
-        GT[i * 4 + 3] = 0.f;
+        GT[i * 4 + gc] = GT[(n - 1) * 4 + gc];
+        GT[i * 4 + gc + 1] = 0.f;
       }
       tc::fence_proxy_async_smem();
       __syncthreads();
     }
     if (tid == 0) {
       tc::fence_after_sync();
-      tc::mma_tile(tmem + TM_X, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
+      tc::mma_tile(tmem, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
                    tc::idesc_f16_f32(128, 64), false);
       tc::commit(&mbar);
     }
@@ -167,54 +157,56 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     tc::fence_after_sync();
     // this thread's row of X (q~_i . k~_j for rows < 64, k~_i . k~_j above), 32 columns
     float xr[32];
-    tc::tmem_ld32(tmem + lane + TM_X + hf * 32, xr);
+    tc::tmem_ld32(tmem + lane + hf * 32, xr);
     tc::tmem_wait_ld();
-    uint32_t mphase = 1, vphase = 0;
-#pragma unroll 1
-    for (int r2 = 0; r2 < R; ++r2) {
-      const int h = kh * R + r2;
-      const size_t orow = (size_t)row0 * Hv + h;  // (packed row, head) index of row 0
-      float Gj[32];
+    tc::fence_before_sync();
+    __syncthreads();
+    // X is done with the q~ rows: this head's v rows come into their slots
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&vbar, 2u * BOX);
+      tma_load_2d(sm + OFF_QK, &tv, h * D, row0, &vbar);
+      tma_load_2d(sm + OFF_QK + KB_STRIDE, &tv, h * D + 64, row0, &vbar);
+    }
+    if (r128 < CH) {
+      // P row i (tokens j of this thread's half)
+      const int i = r128;
+      const float Gi = GT[i * 4 + gc];
+      float pv[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) Gj[e] = GT[(hf * 32 + e) * 4 + 2 * r2];
-      if (r128 < CH) {
-        // P row i (tokens j of this thread's half)
-        const int i = r128;
-        const float Gi = GT[i * 4 + 2 * r2];
-        float pv[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = hf * 32 + e;
-          pv[e] = j <= i ? xr[e] * __expf(Gi - Gj[e]) : 0.f;
-          amax = fmaxf(amax, fabsf(pv[e]));
-        }
-        if (i < n) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
-                                                (orow + (size_t)i * Hv) * CH + hf * 32);
-#pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(pv + g8 * 8);
-        }
-      } else {
-        // A row i
-        const int i = r128 - CH;
-        const float Gi = GT[i * 4 + 2 * r2], bi = GT[i * 4 + 2 * r2 + 1];
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const int j = hf * 32 + j4 * 4;
-          float4 a4;
-          a4.x = j + 0 < i ? bi * __expf(Gi - Gj[j4 * 4 + 0]) * xr[j4 * 4 + 0] : 0.f;
-          a4.y = j + 1 < i ? bi * __expf(Gi - Gj[j4 * 4 + 1]) * xr[j4 * 4 + 1] : 0.f;
-          a4.z = j + 2 < i ? bi * __expf(Gi - Gj[j4 * 4 + 2]) * xr[j4 * 4 + 2] : 0.f;
-          a4.w = j + 3 < i ? bi * __expf(Gi - Gj[j4 * 4 + 3]) * xr[j4 * 4 + 3] : 0.f;
-          *reinterpret_cast<float4*>(AM + i * AP + j) = a4;
-        }
+      for (int e = 0; e < 32; ++e) {
+        const int j = hf * 32 + e;
+        pv[e] = j <= i ? xr[e] * __expf(Gi - GT[j * 4 + gc]) : 0.f;
+        amax = fmaxf(amax, fabsf(pv[e]));
       }
-      __syncthreads();
-      // T = (I + A)^{-1}: diagonal 16 x 16 blocks, one column per thread
+      if (i < n) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
+                                              (orow + (size_t)i * Hv) * CH + hf * 32);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(pv + g8 * 8);
+      }
+    } else {
+      // A row i
+      const int i = r128 - CH;
+      const float Gi = GT[i * 4 + gc], bi = GT[i * 4 + gc + 1];
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const int j = hf * 32 + j4 * 4;
+        float4 a4;
+        a4.x = j + 0 < i ? bi * __expf(Gi - GT[(j + 0) * 4 + gc]) * xr[j4 * 4 + 0] : 0.f;
+        a4.y = j + 1 < i ? bi * __expf(Gi - GT[(j + 1) * 4 + gc]) * xr[j4 * 4 + 1] : 0.f;
+        a4.z = j + 2 < i ? bi * __expf(Gi - GT[(j + 2) * 4 + gc]) * xr[j4 * 4 + 2] : 0.f;
+        a4.w = j + 3 < i ? bi * __expf(Gi - GT[(j + 3) * 4 + gc]) * xr[j4 * 4 + 3] : 0.f;
+        *reinterpret_cast<float4*>(AT + i * AP + j) = a4;
+      }
+    }
+    __syncthreads();
+    // T = (I + A)^{-1}: diagonal 16 x 16 blocks, one column per thread, written
+    // over the A blocks once every column is done
+    {
+      float col[16];
+      const int b = tid >> 4, m = tid & 15;
       if (tid < CH) {
-        const int b = tid >> 4, m = tid & 15;
-        const float* Ab = AM + (16 * b) * AP + 16 * b;
-        float col[16];
+        const float* Ab = AT + (16 * b) * AP + 16 * b;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           float acc = r == m ? 1.f : 0.f;
@@ -222,113 +214,129 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
           for (int j = 0; j < r; ++j) acc -= Ab[r * AP + j] * col[j];
           col[r] = acc;
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) TS[(16 * b + r) * AP + 16 * b + m] = col[r];
       }
       __syncthreads();
-      // off-diagonal blocks: B_ij = T_ii A_ij for every i > j, then level by
-      // level T_ij = -sum_{k=j}^{i-1} B_ik T_kj (B block (i, j) at Z + (i(i-1)/2 + j) * 256)
-      for (int task = tid; task < 6 * 64; task += kThreads) {
-        const int bi = task >> 6, rr = (task >> 2) & 15, c4 = (task & 3) * 4;
-        const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
-        const int j = bi - i * (i - 1) / 2;
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tid < CH) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float t = TS[(16 * i + rr) * AP + 16 * i + q];
-          const float4 a4 = *reinterpret_cast<const float4*>(AM + (16 * i + q) * AP + 16 * j + c4);
-          z.x += t * a4.x; z.y += t * a4.y; z.z += t * a4.z; z.w += t * a4.w;
-        }
-        *reinterpret_cast<float4*>(Z + bi * 256 + rr * 16 + c4) = z;
+        for (int r = 0; r < 16; ++r) AT[(16 * b + r) * AP + 16 * b + m] = col[r];
       }
-      __syncthreads();
-      for (int Lv = 1; Lv < 4; ++Lv) {
-        if (tid < (4 - Lv) * 64) {
-          const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-          float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int k = j; k < i; ++k) {
-            const float* Bik = Z + (i * (i - 1) / 2 + k) * 256 + rr * 16;
+    }
+    __syncthreads();
+    // off-diagonal blocks: B_ij = T_ii A_ij for every i > j, then level by
+    // level T_ij = -sum_{k=j}^{i-1} B_ik T_kj over A_ij (B block (i, j) at
+    // Z + (i(i-1)/2 + j) * 256)
+    for (int task = tid; task < 6 * 64; task += kThreads) {
+      const int bi = task >> 6, rr = (task >> 2) & 15, c4 = (task & 3) * 4;
+      const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
+      const int j = bi - i * (i - 1) / 2;
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const float bq = Bik[q];
-              const float4 t4 = *reinterpret_cast<const float4*>(TS + (16 * k + q) * AP + 16 * j + c4);
-              t.x -= bq * t4.x; t.y -= bq * t4.y; t.z -= bq * t4.z; t.w -= bq * t4.w;
-            }
+      for (int q = 0; q < 16; ++q) {
+        const float t = AT[(16 * i + rr) * AP + 16 * i + q];
+        const float4 a4 = *reinterpret_cast<const float4*>(AT + (16 * i + q) * AP + 16 * j + c4);
+        z.x += t * a4.x; z.y += t * a4.y; z.z += t * a4.z; z.w += t * a4.w;
+      }
+      *reinterpret_cast<float4*>(Z + bi * 256 + rr * 16 + c4) = z;
+    }
+    __syncthreads();
+    for (int Lv = 1; Lv < 4; ++Lv) {
+      if (tid < (4 - Lv) * 64) {
+        const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = j; k < i; ++k) {
+          const float* Bik = Z + (i * (i - 1) / 2 + k) * 256 + rr * 16;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float bq = Bik[q];
+            const float4 t4 = *reinterpret_cast<const float4*>(AT + (16 * k + q) * AP + 16 * j + c4);
+            t.x -= bq * t4.x; t.y -= bq * t4.y; t.z -= bq * t4.z; t.w -= bq * t4.w;
           }
-          *reinterpret_cast<float4*>(TS + (16 * i + rr) * AP + 16 * j + c4) = t;
         }
-        __syncthreads();
+        *reinterpret_cast<float4*>(AT + (16 * i + rr) * AP + 16 * j + c4) = t;
       }
-      // [T diag(beta e^G) ; T diag(beta)] -> the MMAs' A tile (upper blocks of T are zero)
-#pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const int idx = tid + kThreads * q2;
-        const int i = idx >> 3, c8 = idx & 7;
-        float tb[8], tbe[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = c8 * 8 + e;
-          const float t = (j >> 4) <= (i >> 4) ? TS[i * AP + j] : 0.f;
-          tb[e] = t * GT[j * 4 + 2 * r2 + 1];
-          tbe[e] = tb[e] * __expf(GT[j * 4 + 2 * r2]);
-          amax = fmaxf(amax, fabsf(tb[e]));
-        }
-        *reinterpret_cast<uint4*>(sm + OFF_TBE + tc::sw128_offset(i, c8 * 8)) = pack8(tbe);
-        *reinterpret_cast<uint4*>(sm + OFF_TBE + tc::sw128_offset(CH + i, c8 * 8)) = pack8(tb);
-      }
-      // this head's v rows have landed; rows past the sequence -> 0
-      if (!cta_wait(&vbar, vphase, &flag)) { ok = false; break; }
-      vphase ^= 1;
-      if (n < CH) {
-        const int nz = CH - n;
-        for (int t = tid; t < 2 * nz * 8; t += kThreads) {
-          const int q = t & 7, rr = (t >> 3) % nz, bx = (t >> 3) / nz;
-          *reinterpret_cast<uint4*>(sm + OFF_V + bx * BOX + tc::sw128_offset(n + rr, q * 8)) =
-              make_uint4(0, 0, 0, 0);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
       __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-        const tc::Opnd a{sbase + OFF_TBE, 0u, false};
-        // rows 0..63: w = T diag(beta e^G) k~;  rows 64..127: u = T diag(beta) v
-        tc::mma_op(tmem + TM_W, a, tc::Opnd{sbase + OFF_QK + CH * 128, KB_STRIDE, true}, CH / 16,
-                   tc::idesc_f16_f32(128, 128, false, true), false);
-        tc::mma_op(tmem + TM_U, a, tc::Opnd{sbase + OFF_V, BOX, true}, CH / 16,
-                   tc::idesc_f16_f32(128, 128, false, true), false);
-        tc::commit(&mbar);
+    }
+    // [-T diag(beta e^G) ; T diag(beta)] -> the MMAs' A tile (over the B
+    // blocks; upper blocks of T are zero)
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int idx = tid + kThreads * q2;
+      const int i = idx >> 3, c8 = idx & 7;
+      float tb[8], tbe[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = c8 * 8 + e;
+        const float t = (j >> 4) <= (i >> 4) ? AT[i * AP + j] : 0.f;
+        tb[e] = t * GT[j * 4 + gc + 1];
+        tbe[e] = -tb[e] * __expf(GT[j * 4 + gc]);
+        amax = fmaxf(amax, fabsf(tb[e]));
       }
-      if (!cta_wait(&mbar, mphase, &flag)) { ok = false; break; }
-      mphase ^= 1;
-      // the v buffer is free: the next head's rows come in behind this one's readout
-      if (r2 + 1 < R && tid == 0) load_v(r2 + 1);
+      *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(i, c8 * 8)) = pack8(tbe);
+      *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(CH + i, c8 * 8)) = pack8(tb);
+    }
+    // this head's v rows have landed; rows past the sequence -> 0
+    ok = cta_wait(&vbar, 0, &flag);
+  }
+  if (ok) {
+    if (n < CH) {
+      const int nz = CH - n;
+      for (int t = tid; t < 2 * nz * 8; t += kThreads) {
+        const int q = t & 7, rr = (t >> 3) % nz, bx = (t >> 3) / nz;
+        *reinterpret_cast<uint4*>(sm + OFF_QK + bx * KB_STRIDE + tc::sw128_offset(n + rr, q * 8)) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    // rows 0..63: -w = -T diag(beta e^G) k~   (k~ rows, MN-major)
+    if (tid == 0) {
       tc::fence_after_sync();
-      {
-        // lanes 0..63: -w row i; lanes 64..127: u row i (64 columns each)
-        const int i = r128 & 63;
-        const bool wrow = r128 < CH;
-        float vv[64];
-        const uint32_t col = (wrow ? TM_W : TM_U) + hf * 64;
-        tc::tmem_ld32(tmem + lane + col, vv);
-        tc::tmem_ld32(tmem + lane + col + 32, vv + 32);
-        tc::tmem_wait_ld();
-        const float sg = wrow ? -1.f : 1.f;
+      tc::mma_op(tmem, tc::Opnd{sbase + OFF_TT, 0u, false},
+                 tc::Opnd{sbase + OFF_QK + CH * 128, KB_STRIDE, true}, CH / 16,
+                 tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::commit(&mbar);
+    }
+    ok = cta_wait(&mbar, 1, &flag);
+  }
+  // read out rows 0..63 (-w) or 64..127 (u) of the product in TMEM, 64 columns
+  auto readout = [&](bool mine, void* base) {
+    if (!mine) return;  // warp-uniform: TMEM lane quarters
+    const int i = r128 & 63;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          vv[e] *= sg;
-          amax = fmaxf(amax, fabsf(vv[e]));
-        }
-        if (i < n) {
-          __half* base = reinterpret_cast<__half*>(wrow ? p.scr_w : p.scr_u);
-          uint4* dst = reinterpret_cast<uint4*>(base + (orow + (size_t)i * Hv) * D + hf * 64);
+    for (int hh = 0; hh < 2; ++hh) {
+      float vv[32];
+      tc::tmem_ld32(tmem + lane + hf * 64 + hh * 32, vv);
+      tc::tmem_wait_ld();
+      float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int g8 = 0; g8 < 8; ++g8) dst[g8] = pack8(vv + g8 * 8);
-        }
+      for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], fabsf(vv[e]));
+      amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+      if (i < n) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(base) +
+                                              (orow + (size_t)i * Hv) * D + hf * 64 + hh * 32);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(vv + g8 * 8);
       }
-      tc::fence_before_sync();
-      __syncthreads();  // AM, TS, the A tile and TMEM are reused by the next head
+    }
+  };
+  if (ok) {
+    tc::fence_after_sync();
+    readout(r128 < CH, p.scr_w);
+    tc::fence_before_sync();
+    __syncthreads();
+    // rows 64..127: u = T diag(beta) v   (v rows in the q~ slots, MN-major)
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_op(tmem, tc::Opnd{sbase + OFF_TT, 0u, false},
+                 tc::Opnd{sbase + OFF_QK, KB_STRIDE, true}, CH / 16,
+                 tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::commit(&mbar);
+    }
+    ok = cta_wait(&mbar, 0, &flag);
+    if (ok) {
+      tc::fence_after_sync();
+      readout(r128 >= CH, p.scr_u);
     }
   }
   if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
@@ -347,7 +355,7 @@ cudaError_t launch_intra(const FwdParams& p, const void* qk_map, const void* v_m
   cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  intra_kernel<<<dim3(max_chunks, p.Hk), kThreads, SMEM_BYTES, stream>>>(
+  intra_kernel<<<(unsigned)max_chunks * (unsigned)p.Hv, kThreads, SMEM_BYTES, stream>>>(
       p, *static_cast<const CUtensorMap*>(qk_map), *static_cast<const CUtensorMap*>(v_map),
       *static_cast<const CUtensorMap*>(g_map));
   return cudaGetLastError();
