@@ -52,7 +52,8 @@ constexpr uint32_t OFF_AT = 32768;     // A, overwritten block by block by T: fp
 constexpr uint32_t OFF_TT = 50176;     // [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
 constexpr uint32_t OFF_Z = OFF_TT;     // during the solve: B blocks fp32 [6][16][16]
 constexpr uint32_t OFF_GT = 66560;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
-constexpr uint32_t SMEM_BYTES = 67584 + 1024;
+constexpr uint32_t OFF_GH = 67584;     // this head's G [64], contiguous
+constexpr uint32_t SMEM_BYTES = 67840 + 1024;
 constexpr uint32_t TM_COLS = 128;      // X (64 columns), then the 128-column products
 
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
@@ -107,6 +108,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   float* AT = reinterpret_cast<float*>(sm + OFF_AT);
   float* Z = reinterpret_cast<float*>(sm + OFF_Z);
   float* GT = reinterpret_cast<float*>(sm + OFF_GT);
+  float* GH = reinterpret_cast<float*>(sm + OFF_GH);
   const int gc = 2 * r2;  // this head's G column in GT (beta at gc + 1)
 
   if (tid == 0) {
@@ -150,6 +152,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
                    tc::idesc_f16_f32(128, 64), false);
       tc::commit(&mbar);
     }
+    if (tid < CH) GH[tid] = GT[tid * 4 + gc];
     ok = cta_wait(&mbar, 0, &flag);
   }
   float amax = 0.f;
@@ -167,36 +170,51 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
       tma_load_2d(sm + OFF_QK, &tv, h * D, row0, &vbar);
       tma_load_2d(sm + OFF_QK + KB_STRIDE, &tv, h * D + 64, row0, &vbar);
     }
-    if (r128 < CH) {
-      // P row i (tokens j of this thread's half)
-      const int i = r128;
-      const float Gi = GT[i * 4 + gc];
-      float pv[32];
+    {
+      // row i of P (rows 0..63 of X) or of A (rows 64..127), this thread's 32
+      // columns j as two 16-blocks; blocks right of row i's block are zero
+      const bool prow = r128 < CH;
+      const int i = r128 & 63, ib = i >> 4;
+      const float Gi = GH[i];
+      const float sc = prow ? 1.f : GT[i * 4 + gc + 1];  // beta_i for A
+      float val[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = hf * 32 + e;
-        pv[e] = j <= i ? xr[e] * __expf(Gi - GT[j * 4 + gc]) : 0.f;
-        amax = fmaxf(amax, fabsf(pv[e]));
+      for (int blk = 0; blk < 2; ++blk) {
+        const int jb = 2 * hf + blk;
+        if (jb <= ib) {
+          float g16[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(GH + 16 * jb + 4 * q);
+            g16[4 * q] = t.x; g16[4 * q + 1] = t.y; g16[4 * q + 2] = t.z; g16[4 * q + 3] = t.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = 16 * jb + e;
+            const bool keep = prow ? j <= i : j < i;
+            val[blk * 16 + e] = keep ? sc * xr[blk * 16 + e] * __expf(Gi - g16[e]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) val[blk * 16 + e] = 0.f;
+        }
       }
-      if (i < n) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
-                                              (orow + (size_t)i * Hv) * CH + hf * 32);
+      if (prow) {
+        float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(pv + g8 * 8);
-      }
-    } else {
-      // A row i
-      const int i = r128 - CH;
-      const float Gi = GT[i * 4 + gc], bi = GT[i * 4 + gc + 1];
+        for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], fabsf(val[e]));
+        amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        if (i < n) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
+                                                (orow + (size_t)i * Hv) * CH + hf * 32);
 #pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
-        const int j = hf * 32 + j4 * 4;
-        float4 a4;
-        a4.x = j + 0 < i ? bi * __expf(Gi - GT[(j + 0) * 4 + gc]) * xr[j4 * 4 + 0] : 0.f;
-        a4.y = j + 1 < i ? bi * __expf(Gi - GT[(j + 1) * 4 + gc]) * xr[j4 * 4 + 1] : 0.f;
-        a4.z = j + 2 < i ? bi * __expf(Gi - GT[(j + 2) * 4 + gc]) * xr[j4 * 4 + 2] : 0.f;
-        a4.w = j + 3 < i ? bi * __expf(Gi - GT[(j + 3) * 4 + gc]) * xr[j4 * 4 + 3] : 0.f;
-        *reinterpret_cast<float4*>(AT + i * AP + j) = a4;
+          for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(val + g8 * 8);
+        }
+      } else {
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4)
+          *reinterpret_cast<float4*>(AT + i * AP + hf * 32 + j4 * 4) =
+              make_float4(val[j4 * 4], val[j4 * 4 + 1], val[j4 * 4 + 2], val[j4 * 4 + 3]);
       }
     }
     __syncthreads();

@@ -40,6 +40,11 @@ constexpr int R = 2;  // v-heads per k-head
 constexpr int XROWS = CH + KC - 1;
 constexpr uint32_t XSUB = 9216;  // one box: 72 rows x 128 B, 1024-aligned
 constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
+// the conv taps of a box's 64 channels (bf16 [64][4], 512 bytes) sit in the
+// box's padding rows, right after its 67 staged rows
+constexpr uint32_t WS_OFF = XBOX_BYTES;
+constexpr uint32_t WS_BYTES = 64 * KC * 2;
+static_assert(WS_OFF + WS_BYTES <= XSUB && WS_OFF % 16 == 0, "taps must fit the box padding");
 constexpr uint32_t SMEM_BYTES = 8 * XSUB + 1024;
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
@@ -105,9 +110,12 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
   if (tid == 0) {
     mbar_init(&xbar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&xbar, 8u * XBOX_BYTES);
+    mbar_arrive_expect_tx(&xbar, 8u * (XBOX_BYTES + WS_BYTES));
 #pragma unroll
-    for (int b = 0; b < 8; ++b) tma_load_2d(xt + b * XSUB, &tmx, gch(b), seq0 + c0 - (KC - 1), &xbar);
+    for (int b = 0; b < 8; ++b) {
+      tma_load_2d(xt + b * XSUB, &tmx, gch(b), seq0 + c0 - (KC - 1), &xbar);
+      bulk_g2s(xt + b * XSUB + WS_OFF, w + (size_t)gch(b) * KC, WS_BYTES, &xbar);
+    }
   }
   // gates of the chunk's tokens for the k-head's two v-heads (threads 0..127,
   // token tid % 64 of head 2kh + tid / 64): g = -e^{A_log} softplus(a + dt_bias),
@@ -158,13 +166,12 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
   bool range_bad = false;
 #pragma unroll 1
   for (int part = 0; part < 2 + R; ++part) {  // q, k, v of head 2kh, v of head 2kh+1
-    const int ch = part == 0 ? kh * D : (part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * R + part - 2) * D);
-    const int gc = ch + g * 8;
     const int lc = part * D + g * 8;  // local channel: box lc / 64, column lc % 64
     float wt[KC][8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const uint2 wu = *reinterpret_cast<const uint2*>(w + (size_t)(gc + e) * KC);
+      const uint2 wu = *reinterpret_cast<const uint2*>(xt + (lc >> 6) * XSUB + WS_OFF +
+                                                       ((lc + e) & 63) * KC * 2);
       float t4[4];
       t4[0] = __uint_as_float(wu.x << 16);
       t4[1] = __uint_as_float(wu.x & 0xffff0000u);

@@ -42,8 +42,10 @@ constexpr int kCompute = 256;
 constexpr int kProducer = kCompute;       // first thread of the TMA warp
 constexpr int kIssuer = kCompute + 32;    // first thread of the MMA warp
 constexpr int kThreads = kCompute + 64;
-// named barriers: 1 the compute warps; 2 and 3 compute warps -> MMA warp
+// named barriers: 1 the compute warps; 2 all compute warps -> MMA warp (S0
+// tile written); 3 the U-row warps -> MMA warp (U tile written)
 constexpr int kBarC = 1, kBarD = 2, kBarS = 3;
+constexpr int kGateD = kCompute + 32, kGateS = kCompute / 2 + 32;
 constexpr int R = 2;  // v-heads per k-head
 constexpr float kF16Max = 65000.f;
 
@@ -73,12 +75,23 @@ struct ChunkDesc {
 __device__ __forceinline__ void cbar() {  // the compute warps only
   asm volatile("bar.sync %0, %1;" ::"n"(kBarC), "n"(kCompute) : "memory");
 }
-// compute warps release the MMA warp (which waits with mma_gate)
-__device__ __forceinline__ void mma_release(int id) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(kCompute + 32) : "memory");
+// compute warps release the MMA warp, which waits with mma_gate
+template <int kId, int kCount>
+__device__ __forceinline__ void mma_release() {
+  asm volatile("bar.arrive %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
 }
-__device__ __forceinline__ void mma_gate(int id) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kCompute + 32) : "memory");
+template <int kId, int kCount>
+__device__ __forceinline__ void mma_gate() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
+}
+
+// Packed fp32 pair product (one mul.rn.f32x2 on sm_100 and later).
+__device__ __forceinline__ void mul2(float& a, float& b, float s) {
+  unsigned long long v = (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+  const unsigned long long m = (unsigned long long)__float_as_uint(s) | ((unsigned long long)__float_as_uint(s) << 32);
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(v) : "l"(m));
+  a = __uint_as_float((uint32_t)v);
+  b = __uint_as_float((uint32_t)(v >> 32));
 }
 
 __device__ __forceinline__ uint4 pack8(const float* v) {
@@ -159,11 +172,13 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     // ============================= MMA warp ==============================
     // Chunk k: gate kBarD (S0 tile ready) -> D = [-w ; e^G q~] S0^T;
     //          gate kBarS (U tile ready)  -> S += U^T k', D += [0 ; P] U.
+    // mma_s covers the state update only (the next hand-over waits for it),
+    // except on a chain's last chunk, whose outputs are written right away.
     for (int k = 0;; ++k) {
       const int b = k & 1;
       const uint32_t sb = sbase + b * ST_BYTES;
       const uint32_t dcol = TM_D + (k & 1) * 128;
-      mma_gate(kBarD);
+      mma_gate<kBarD, kGateD>();
       if (mma_stop) break;
       if (tid == kIssuer) {
         tc::fence_after_sync();
@@ -173,16 +188,21 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
         tc::commit(&mma_y);
       }
       __syncwarp();
-      mma_gate(kBarS);
+      mma_gate<kBarS, kGateS>();
       if (mma_stop) break;
       if (tid == kIssuer) {
         tc::fence_after_sync();
+        const bool last = (desc[b].flags & 2) != 0;
         const tc::Opnd ut{sbase + OFF_UT, BOX, true};
+        auto mma_o = [&]() {
+          tc::mma_op(tmem + dcol, tc::Opnd{sb + ST_ZP, 0u, false}, ut, CH / 16,
+                     tc::idesc_f16_f32(128, 128, false, true), true);
+        };
+        if (last) mma_o();
         tc::mma_op(tmem + TM_S, ut, tc::Opnd{sb + ST_K, BOX, true}, CH / 16,
                    tc::idesc_f16_f32(128, 128, true, true), true);
-        tc::mma_op(tmem + dcol, tc::Opnd{sb + ST_ZP, 0u, false}, ut, CH / 16,
-                   tc::idesc_f16_f32(128, 128, false, true), true);
         tc::commit(&mma_s);
+        if (!last) mma_o();
         tc::commit(&empty[b]);  // the stage is free once these MMAs are done
       }
       __syncwarp();
@@ -328,22 +348,18 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
               pack8(srow + g8 * 8);
         const float dc = __expf(GC);
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) srow[kk] *= dc;
+        for (int kk = 0; kk < 64; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
         tc::tmem_st32(tmem + lane + TM_S + hf * 64, srow);
         tc::tmem_st32(tmem + lane + TM_S + hf * 64 + 32, srow + 32);
         tc::tmem_wait_st();
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      mma_release(kBarD);  // D = [-w ; e^G q~] S0^T
+      mma_release<kBarD, kGateD>();  // D = [-w ; e^G q~] S0^T
       next_gate = kBarS;
       const int ob = k & 1;
       const uint32_t dcol = TM_D + ob * 128;
-      // ---- while the tensor core runs: the previous chunk's outputs, this chunk's u row
-      if (pending) {
-        flush();
-        pending = false;
-      }
+      // ---- while the tensor core runs: this chunk's u row
       uint4 ur[8];
       if (urow) {
         const unsigned char* urow_p = st + ST_U + hf * BOX + j * 128;
@@ -354,7 +370,10 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       if (!wait_c(&mma_y, ph_y)) { dead = true; break; }
       ph_y ^= 1;
       tc::fence_after_sync();
-      // ---- U = u + D[0..63] -> fp16 token-major tile (same swizzled places as u)
+      // ---- U = u + D[0..63] -> fp16 token-major tile (same swizzled places as
+      // u) on the U-row warps, which then release the state update; the
+      // output warps meanwhile write the previous chunk's outputs (its
+      // D += P U finished before this chunk's D product)
       if (urow) {
         float dv[64];
         tc::tmem_ld32(tmem + lane + dcol + hf * 64, dv);
@@ -372,10 +391,13 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
           }
           *reinterpret_cast<uint4*>(dst + ((c ^ (j & 7)) << 4)) = pack8(u8);
         }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        mma_release<kBarS, kGateS>();  // S += U^T (e^{G_C - G} k~);  D += [0 ; P] U
+      } else if (pending) {
+        flush();
       }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      mma_release(kBarS);  // S += U^T (e^{G_C - G} k~);  D += [0 ; P] U
+      pending = false;
       next_gate = kBarD;
       s_busy = true;
       pending = true;
@@ -407,7 +429,8 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     // let the MMA warp out of the gate it waits at
     if (tid == 0) mma_stop = 1;
     cbar();
-    mma_release(next_gate);
+    if (next_gate == kBarD) mma_release<kBarD, kGateD>();
+    else if (urow) mma_release<kBarS, kGateS>();
     if (dead && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
     // the state and U enter tensor-core operands in fp16
     if (!(amax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
