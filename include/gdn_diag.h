@@ -2,7 +2,7 @@
  * gdn_diag.h -- diagnostic entry point of libgdn, outside the forward path.
  *
  * gdn_diag_umma_gemm runs the tensor-core building blocks of the chunked
- * prefill kernel on plain matrices, so a test can check them against a
+ * prefill kernels on plain matrices, so a test can check them against a
  * library GEMM: one CTA stages A and B into 128-byte-swizzled K-major shared
  * tiles, optionally preloads C into tensor memory with tcgen05.st, issues
  * tcgen05.mma (kind::f16, bf16 inputs, fp32 accumulator in tensor memory) and
@@ -10,7 +10,8 @@
  *     D[128][N] = (C ? C : 0) + A[128][K] * B[N][K]^T
  * A, B: bf16 row-major device arrays; C, D: fp32 row-major device arrays
  * (C may be NULL).  operand_f16 != 0 converts A and B to fp16 tiles and runs
- * the fp16 form of the MMA (the chunked kernel's operand type), else bf16.  N in {64, 128, 192, 256}, K in {64, 128}.  Returns GDN_OK
+ * the fp16 form of the MMA (the prefill kernels' operand type), else bf16.
+ * N in {64, 128, 192, 256}, K in {64, 128}.  Returns GDN_OK
  * or GDN_ERR_NULL / GDN_ERR_DIMS / GDN_ERR_ALIGN / GDN_ERR_CUDA (nothing
  * launched on error).  Stream-ordered, no synchronisation.
  *
