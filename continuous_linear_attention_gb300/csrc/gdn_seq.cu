@@ -8,13 +8,13 @@
 //   rows 0..63  : U = u - w S0^T                 (the chunk's updates u_j)
 //   rows 64..127: O = (e^G q~) S0^T + P U        (the chunk's outputs o_i)
 // as
-//   CUDA  stage fix-ups: k~_j <- e^{G_C - G_j} k~_j, q~_i <- e^{G_i} q~_i (0 past n)
 //   CUDA  S0 -> fp16 operand tile;  TMEM S <- e^{G_C} S0
-//   MMA   D  = [-w ; e^G q~] S0^T
-//   CUDA  U  = u + D[0..63] -> fp16 token-major tile (rows past n zeroed)
-//   MMA   S += U^T (e^{G_C - G} k~)            (U and k~ as MN-major operands)
+//   MMA   D  = [-w ; q~] S0^T
+//   CUDA  U  = u + D[0..63] -> fp16 token-major tiles U and e^{G_C - G} U
+//         (rows past n zeroed);  D[64 + i] <- e^{G_i} D[64 + i] in TMEM
+//   MMA   S += (e^{G_C - G} U)^T k~            (U and k~ as MN-major operands)
 //   MMA   D += [0 ; P] U                       (rows 64..127: + P U)
-//   CUDA  o_i = D[64 + i] -> bf16              (while the next chunk's MMA runs)
+//   CUDA  o_i = D[64 + i] -> bf16              (while the next chunk's MMAs run)
 // This is the chunked gated delta rule (Gated Delta Networks, chunkwise WY
 // form) run over cu_seqlens from per-sequence initial states, as a continuous
 // batching engine does for a linear-attention layer.
@@ -42,10 +42,10 @@ constexpr int kCompute = 256;
 constexpr int kProducer = kCompute;       // first thread of the TMA warp
 constexpr int kIssuer = kCompute + 32;    // first thread of the MMA warp
 constexpr int kThreads = kCompute + 64;
-// named barriers: 1 the compute warps; 2 all compute warps -> MMA warp (S0
-// tile written); 3 the U-row warps -> MMA warp (U tile written)
+// named barriers: 1 the compute warps; 2 compute warps -> MMA warp (S0 tile
+// written); 3 compute warps -> MMA warp (U tiles written, outputs rescaled)
 constexpr int kBarC = 1, kBarD = 2, kBarS = 3;
-constexpr int kGateD = kCompute + 32, kGateS = kCompute / 2 + 32;
+constexpr int kGateD = kCompute + 32, kGateS = kCompute + 32;
 constexpr int R = 2;  // v-heads per k-head
 constexpr float kF16Max = 65000.f;
 
@@ -61,6 +61,7 @@ constexpr uint32_t ST_BYTES = 82944;
 constexpr uint32_t ST_TX = ST_BYTES - BOX;  // what the TMA brings (all but the zero tile)
 // CTA shared memory
 constexpr uint32_t OFF_S0 = 2 * ST_BYTES;    // S0 fp16, 2 K-blocks x 128 rows
+constexpr uint32_t OFF_UD = OFF_S0;          // e^{G_C - G} U, over S0 once the D product is done
 constexpr uint32_t OFF_UT = OFF_S0 + 32768;  // U fp16 [64 tokens][128]: two 64-column boxes
 constexpr uint32_t SMEM_BYTES = OFF_UT + 16384 + 1024;
 // tensor memory columns: the state, two accumulators D
@@ -75,6 +76,7 @@ struct ChunkDesc {
 __device__ __forceinline__ void cbar() {  // the compute warps only
   asm volatile("bar.sync %0, %1;" ::"n"(kBarC), "n"(kCompute) : "memory");
 }
+
 // compute warps release the MMA warp, which waits with mma_gate
 template <int kId, int kCount>
 __device__ __forceinline__ void mma_release() {
@@ -83,6 +85,15 @@ __device__ __forceinline__ void mma_release() {
 template <int kId, int kCount>
 __device__ __forceinline__ void mma_gate() {
   asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
+}
+
+// Packed fp32 pair sum (one add.rn.f32x2 on sm_100 and later): (a, b) += (x, y).
+__device__ __forceinline__ void add2(float& a, float& b, float x, float y) {
+  unsigned long long v = (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+  const unsigned long long w = (unsigned long long)__float_as_uint(x) | ((unsigned long long)__float_as_uint(y) << 32);
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(v) : "l"(w));
+  a = __uint_as_float((uint32_t)v);
+  b = __uint_as_float((uint32_t)(v >> 32));
 }
 
 // Packed fp32 pair product (one mul.rn.f32x2 on sm_100 and later).
@@ -109,23 +120,6 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
     v[2 * e] = f.x;
     v[2 * e + 1] = f.y;
-  }
-}
-
-// one 128-byte fp16 row of a tile, scaled by s in fp32 (s == 0 zeroes it);
-// the swizzle permutes 16-byte chunks inside the row only.  Chunks are
-// visited starting at `rot`, so that threads on consecutive rows hit
-// different banks.
-__device__ __forceinline__ void scale_row(unsigned char* row, float s, int rot) {
-  uint4* r = reinterpret_cast<uint4*>(row);
-#pragma unroll
-  for (int q0 = 0; q0 < 8; ++q0) {
-    const int q = (q0 + rot) & 7;
-    float v[8];
-    unpack8(r[q], v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] *= s;
-    r[q] = pack8(v);
   }
 }
 
@@ -170,8 +164,8 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
 
   if (tid >= kIssuer) {
     // ============================= MMA warp ==============================
-    // Chunk k: gate kBarD (S0 tile ready) -> D = [-w ; e^G q~] S0^T;
-    //          gate kBarS (U tile ready)  -> S += U^T k', D += [0 ; P] U.
+    // Chunk k: gate kBarD (S0 tile ready)    -> D = [-w ; q~] S0^T;
+    //          gate kBarS (U tiles ready)     -> S += (e^{G_C-G} U)^T k~, D += [0 ; P] U.
     // mma_s covers the state update only (the next hand-over waits for it),
     // except on a chain's last chunk, whose outputs are written right away.
     for (int k = 0;; ++k) {
@@ -199,8 +193,8 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
                      tc::idesc_f16_f32(128, 128, false, true), true);
         };
         if (last) mma_o();
-        tc::mma_op(tmem + TM_S, ut, tc::Opnd{sb + ST_K, BOX, true}, CH / 16,
-                   tc::idesc_f16_f32(128, 128, true, true), true);
+        tc::mma_op(tmem + TM_S, tc::Opnd{sbase + OFF_UD, BOX, true}, tc::Opnd{sb + ST_K, BOX, true},
+                   CH / 16, tc::idesc_f16_f32(128, 128, true, true), true);
         tc::commit(&mma_s);
         if (!last) mma_o();
         tc::commit(&empty[b]);  // the stage is free once these MMAs are done
@@ -281,20 +275,24 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     // (tcgen05.ld is warp-collective: the lane predicate guards the stores only)
     auto flush = [&]() {
       if (urow) return;
-      float o[64];
-      tc::tmem_ld32(tmem + lane + TM_D + p_ob * 128 + hf * 64, o);
-      tc::tmem_ld32(tmem + lane + TM_D + p_ob * 128 + hf * 64 + 32, o + 32);
-      tc::tmem_wait_ld();
-      if (j >= p_n) return;
-      uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(p_row + j) * Hv + p_h) * D + hf * 64);
 #pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        uint4 w;
-        w.x = tc::pack2(o[g8 * 8 + 0], o[g8 * 8 + 1], (__nv_bfloat16*)nullptr);
-        w.y = tc::pack2(o[g8 * 8 + 2], o[g8 * 8 + 3], (__nv_bfloat16*)nullptr);
-        w.z = tc::pack2(o[g8 * 8 + 4], o[g8 * 8 + 5], (__nv_bfloat16*)nullptr);
-        w.w = tc::pack2(o[g8 * 8 + 6], o[g8 * 8 + 7], (__nv_bfloat16*)nullptr);
-        dst[g8] = w;
+      for (int hh = 0; hh < 2; ++hh) {
+        float o[32];
+        tc::tmem_ld32(tmem + lane + TM_D + p_ob * 128 + hf * 64 + hh * 32, o);
+        tc::tmem_wait_ld();
+        if (j < p_n) {
+          uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(p_row + j) * Hv + p_h) * D + hf * 64 +
+                                                hh * 32);
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            uint4 w;
+            w.x = tc::pack2(o[g8 * 8 + 0], o[g8 * 8 + 1], (__nv_bfloat16*)nullptr);
+            w.y = tc::pack2(o[g8 * 8 + 2], o[g8 * 8 + 3], (__nv_bfloat16*)nullptr);
+            w.z = tc::pack2(o[g8 * 8 + 4], o[g8 * 8 + 5], (__nv_bfloat16*)nullptr);
+            w.w = tc::pack2(o[g8 * 8 + 6], o[g8 * 8 + 7], (__nv_bfloat16*)nullptr);
+            dst[g8] = w;
+          }
+        }
       }
     };
     for (int k = 0;; ++k) {
@@ -307,14 +305,13 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       const int r2 = d.h % R;
       const int n = d.n;
       const float GC = GT[(n - 1) * 4 + 2 * r2];
-      // ---- k~_j <- e^{G_C - G_j} k~_j and q~_i <- e^{G_i} q~_i (rows past n -> 0)
-      {
-        const int rr = tid >> 1, half = tid & 1, t = rr & 63;
-        const float gt = GT[t * 4 + 2 * r2];
-        if (rr < CH) scale_row(st + ST_K + half * BOX + t * 128, t < n ? __expf(GC - gt) : 0.f, t);
-        else scale_row(st + ST_QW + half * KB_STRIDE + (CH + t) * 128, t < n ? __expf(gt) : 0.f, t);
+      if (n < CH) {
+        // k~ rows past the sequence -> 0 (they meet zero U rows in the state update)
+        for (int t = tid; t < (CH - n) * 16; t += kCompute)
+          *reinterpret_cast<uint4*>(st + ST_K + (t & 8 ? BOX : 0) + (n + (t >> 4)) * 128 + (t & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
       // ---- the previous chunk's MMAs are done: S and its D readable
       if (s_busy) {
         if (!wait_c(&mma_s, ph_s)) { dead = true; break; }
@@ -322,35 +319,35 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
         s_busy = false;
         tc::fence_after_sync();
       }
-      // ---- state hand-over: S0 -> fp16 tile, TMEM S <- e^{G_C} S0
+      // ---- state hand-over: S0 -> fp16 tile, TMEM S <- e^{G_C} S0 (32 columns at a time)
       {
         const int v = r128;
-        float srow[64];
-        if (d.flags & 1) {
-          const float* S_r = reinterpret_cast<const float*>(p.layer_base + (size_t)d.rblk * p.stride +
-                                                            p.rec_off) + (size_t)d.h * D * D;
+        const float dc = __expf(GC);
+        const float* S_r = reinterpret_cast<const float*>(p.layer_base + (size_t)d.rblk * p.stride +
+                                                          p.rec_off) + (size_t)d.h * D * D;
 #pragma unroll
-          for (int kk = 0; kk < 64; ++kk) srow[kk] = S_r[(size_t)(hf * 64 + kk) * D + v];
-        } else {
-          tc::tmem_ld32(tmem + lane + TM_S + hf * 64, srow);
-          tc::tmem_ld32(tmem + lane + TM_S + hf * 64 + 32, srow + 32);
-          tc::tmem_wait_ld();
-        }
-        {
+        for (int hh = 0; hh < 2; ++hh) {
+          const int k0 = hf * 64 + hh * 32;
+          float srow[32];
+          if (d.flags & 1) {
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) srow[kk] = S_r[(size_t)(k0 + kk) * D + v];
+          } else {
+            tc::tmem_ld32(tmem + lane + TM_S + k0, srow);
+            tc::tmem_wait_ld();
+          }
           float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int kk = 0; kk < 64; ++kk) m4[kk & 3] = fmaxf(m4[kk & 3], fabsf(srow[kk]));
+          for (int kk = 0; kk < 32; ++kk) m4[kk & 3] = fmaxf(m4[kk & 3], fabsf(srow[kk]));
           amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8)
+            *reinterpret_cast<uint4*>(sm + OFF_S0 + hf * KB_STRIDE +
+                                      tc::sw128_offset(v, hh * 32 + g8 * 8)) = pack8(srow + g8 * 8);
+#pragma unroll
+          for (int kk = 0; kk < 32; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
+          tc::tmem_st32(tmem + lane + TM_S + k0, srow);
         }
-#pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8)
-          *reinterpret_cast<uint4*>(sm + OFF_S0 + hf * KB_STRIDE + tc::sw128_offset(v, g8 * 8)) =
-              pack8(srow + g8 * 8);
-        const float dc = __expf(GC);
-#pragma unroll
-        for (int kk = 0; kk < 64; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
-        tc::tmem_st32(tmem + lane + TM_S + hf * 64, srow);
-        tc::tmem_st32(tmem + lane + TM_S + hf * 64 + 32, srow + 32);
         tc::tmem_wait_st();
       }
       tc::fence_proxy_async_smem();
@@ -375,28 +372,55 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       // output warps meanwhile write the previous chunk's outputs (its
       // D += P U finished before this chunk's D product)
       if (urow) {
-        float dv[64];
-        tc::tmem_ld32(tmem + lane + dcol + hf * 64, dv);
-        tc::tmem_ld32(tmem + lane + dcol + hf * 64 + 32, dv + 32);
-        tc::tmem_wait_ld();
         unsigned char* dst = sm + OFF_UT + hf * BOX + j * 128;
+        unsigned char* dsd = sm + OFF_UD + hf * BOX + j * 128;
+        const float ds = j < n ? __expf(GC - GT[j * 4 + 2 * r2]) : 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float u8[8];
-          unpack8(ur[c], u8);
+        for (int hh = 0; hh < 2; ++hh) {
+          float dv[32];
+          tc::tmem_ld32(tmem + lane + dcol + hf * 64 + hh * 32, dv);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            u8[e] = j < n ? u8[e] + dv[c * 8 + e] : 0.f;
-            amax = fmaxf(amax, fabsf(u8[e]));
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c = hh * 4 + c4;
+            uint4 w = make_uint4(0, 0, 0, 0), wd = make_uint4(0, 0, 0, 0);
+            if (j < n) {
+              float u8[8];
+              unpack8(ur[c], u8);
+              float m2 = 0.f;
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                add2(u8[e], u8[e + 1], dv[c4 * 8 + e], dv[c4 * 8 + e + 1]);
+                m2 = fmaxf(m2, fmaxf(fabsf(u8[e]), fabsf(u8[e + 1])));
+              }
+              amax = fmaxf(amax, m2);
+              w = pack8(u8);
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) mul2(u8[e], u8[e + 1], ds);
+              wd = pack8(u8);
+            }
+            *reinterpret_cast<uint4*>(dst + ((c ^ (j & 7)) << 4)) = w;
+            *reinterpret_cast<uint4*>(dsd + ((c ^ (j & 7)) << 4)) = wd;
           }
-          *reinterpret_cast<uint4*>(dst + ((c ^ (j & 7)) << 4)) = pack8(u8);
         }
         tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        mma_release<kBarS, kGateS>();  // S += U^T (e^{G_C - G} k~);  D += [0 ; P] U
-      } else if (pending) {
-        flush();
+      } else {
+        if (pending) flush();
+        // o rows: D[64 + i] <- e^{G_i} D[64 + i] before P U accumulates onto them
+        const float eg = j < n ? __expf(GT[j * 4 + 2 * r2]) : 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float o[32];
+          tc::tmem_ld32(tmem + lane + dcol + hf * 64 + hh * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) mul2(o[e], o[e + 1], eg);
+          tc::tmem_st32(tmem + lane + dcol + hf * 64 + hh * 32, o);
+        }
+        tc::tmem_wait_st();
       }
+      tc::fence_before_sync();
+      mma_release<kBarS, kGateS>();  // S += (e^{G_C - G} U)^T k~;  D += [0 ; P] U
       pending = false;
       next_gate = kBarD;
       s_busy = true;
@@ -430,7 +454,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     if (tid == 0) mma_stop = 1;
     cbar();
     if (next_gate == kBarD) mma_release<kBarD, kGateD>();
-    else if (urow) mma_release<kBarS, kGateS>();
+    else mma_release<kBarS, kGateS>();
     if (dead && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
     // the state and U enter tensor-core operands in fp16
     if (!(amax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
