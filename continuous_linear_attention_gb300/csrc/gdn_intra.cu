@@ -50,7 +50,7 @@ constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of the 128-row [q~ ; k~] tile
 constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]; once X is done the q~ slots hold v
 constexpr uint32_t OFF_AT = 32768;     // A, overwritten block by block by T: fp32 [64][AP]
 constexpr uint32_t OFF_TT = 50176;     // [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
-constexpr uint32_t OFF_Z = OFF_TT;     // during the solve: B blocks fp32 [6][16][16]
+constexpr uint32_t OFF_Z = OFF_TT;     // during the solve: B blocks fp32 [6][16][20]
 constexpr uint32_t OFF_GT = 66560;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
 constexpr uint32_t OFF_GH = 67584;     // this head's G [64], contiguous
 constexpr uint32_t SMEM_BYTES = 67840 + 1024;
@@ -69,6 +69,59 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   w.z = tc::pack2(v[4], v[5], (E*)nullptr);
   w.w = tc::pack2(v[6], v[7], (E*)nullptr);
   return w;
+}
+
+// ---- 16 x 16 block products of the solve on the warp-level tensor-core path
+// (mma.sync m16n8k8, tf32 inputs, fp32 accumulation), each fp32 operand split
+// into a tf32 head and a tf32 tail with the three significant cross products
+// kept (hh + ht + th), which keeps the products at fp32-level accuracy.
+constexpr int ZP = 20;        // pitch (floats) of the B blocks of the solve
+constexpr int ZB = 16 * ZP;   // floats per B block
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// acc (this warp's fragment of a 16 x 8 block: row g col 2t, 2t+1 and row
+// g+8 col 2t, 2t+1) += X (16 x 16 at xp, pitch px) * Y[:, n0 .. n0+7] (Y at yp, pitch py)
+__device__ __forceinline__ void blk_mma3(float (&acc)[4], const float* xp, int px, const float* yp,
+                                         int py, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const int k0 = 8 * ks;
+    const float af[4] = {xp[g * px + k0 + t], xp[(g + 8) * px + k0 + t], xp[g * px + k0 + t + 4],
+                         xp[(g + 8) * px + k0 + t + 4]};
+    const float bf[2] = {yp[(k0 + t) * py + n0 + g], yp[(k0 + t + 4) * py + n0 + g]};
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ah[e] = tf32_rna(af[e]);
+      al[e] = tf32_rna(af[e] - __uint_as_float(ah[e]));
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      bh[e] = tf32_rna(bf[e]);
+      bl[e] = tf32_rna(bf[e] - __uint_as_float(bh[e]));
+    }
+    mma_tf32(acc, al, bh);
+    mma_tf32(acc, ah, bl);
+    mma_tf32(acc, ah, bh);
+  }
+}
+// store a fragment (scaled by s) into a 16 x 16 block at dp (pitch pd), columns n0 ..
+__device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float (&acc)[4], float s) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2*>(dp + g * pd + n0 + 2 * t) = make_float2(s * acc[0], s * acc[1]);
+  *reinterpret_cast<float2*>(dp + (g + 8) * pd + n0 + 2 * t) = make_float2(s * acc[2], s * acc[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -242,37 +295,28 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     __syncthreads();
     // off-diagonal blocks: B_ij = T_ii A_ij for every i > j, then level by
     // level T_ij = -sum_{k=j}^{i-1} B_ik T_kj over A_ij (B block (i, j) at
-    // Z + (i(i-1)/2 + j) * 256)
-    for (int task = tid; task < 6 * 64; task += kThreads) {
-      const int bi = task >> 6, rr = (task >> 2) & 15, c4 = (task & 3) * 4;
-      const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
-      const int j = bi - i * (i - 1) / 2;
-      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float t = AT[(16 * i + rr) * AP + 16 * i + q];
-        const float4 a4 = *reinterpret_cast<const float4*>(AT + (16 * i + q) * AP + 16 * j + c4);
-        z.x += t * a4.x; z.y += t * a4.y; z.z += t * a4.z; z.w += t * a4.w;
-      }
-      *reinterpret_cast<float4*>(Z + bi * 256 + rr * 16 + c4) = z;
-    }
-    __syncthreads();
-    for (int Lv = 1; Lv < 4; ++Lv) {
-      if (tid < (4 - Lv) * 64) {
-        const int j = tid >> 6, i = j + Lv, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = j; k < i; ++k) {
-          const float* Bik = Z + (i * (i - 1) / 2 + k) * 256 + rr * 16;
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float bq = Bik[q];
-            const float4 t4 = *reinterpret_cast<const float4*>(AT + (16 * k + q) * AP + 16 * j + c4);
-            t.x -= bq * t4.x; t.y -= bq * t4.y; t.z -= bq * t4.z; t.w -= bq * t4.w;
-          }
-        }
-        *reinterpret_cast<float4*>(AT + (16 * i + rr) * AP + 16 * j + c4) = t;
+    // Z + (i(i-1)/2 + j) * ZB); one warp per (block, 8-column half)
+    {
+      const int warp = tid >> 5;
+      for (int task = warp; task < 12; task += kThreads / 32) {
+        const int bi = task >> 1, n0 = (task & 1) * 8;
+        const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
+        const int j = bi - i * (i - 1) / 2;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        blk_mma3(acc, AT + (16 * i) * AP + 16 * i, AP, AT + (16 * i) * AP + 16 * j, AP, n0);
+        blk_store(Z + bi * ZB, ZP, n0, acc, 1.f);
       }
       __syncthreads();
+      for (int Lv = 1; Lv < 4; ++Lv) {
+        if (warp < 2 * (4 - Lv)) {
+          const int j = warp >> 1, i = j + Lv, n0 = (warp & 1) * 8;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int k = j; k < i; ++k)
+            blk_mma3(acc, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP, n0);
+          blk_store(AT + (16 * i) * AP + 16 * j, AP, n0, acc, -1.f);
+        }
+        __syncthreads();
+      }
     }
     // [-T diag(beta e^G) ; T diag(beta)] -> the MMAs' A tile (over the B
     // blocks; upper blocks of T are zero)

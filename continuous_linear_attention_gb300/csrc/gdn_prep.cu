@@ -47,14 +47,16 @@ constexpr uint32_t WS_BYTES = 64 * KC * 2;
 static_assert(WS_OFF + WS_BYTES <= XSUB && WS_OFF % 16 == 0, "taps must fit the box padding");
 constexpr uint32_t SMEM_BYTES = 8 * XSUB + 1024;
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    v[2 * j] = __uint_as_float(u[j] << 16);
-    v[2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
-  }
+// Packed fp32 pairs: d = a * b + c on both lanes (one fma.rn.f32x2).
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// bf16 pair (low, high halves of a word) -> packed fp32 pair
+__device__ __forceinline__ unsigned long long bf2_to_f2(uint32_t u) {
+  return (unsigned long long)(u << 16) | ((unsigned long long)(u & 0xffff0000u) << 32);
 }
 
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
@@ -167,39 +169,46 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
 #pragma unroll 1
   for (int part = 0; part < 2 + R; ++part) {  // q, k, v of head 2kh, v of head 2kh+1
     const int lc = part * D + g * 8;  // local channel: box lc / 64, column lc % 64
-    float wt[KC][8];
+    // taps as packed channel pairs: w2[j][p] = (w[c+2p][j], w[c+2p+1][j])
+    unsigned long long w2[KC][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint2 wu = *reinterpret_cast<const uint2*>(xt + (lc >> 6) * XSUB + WS_OFF +
-                                                       ((lc + e) & 63) * KC * 2);
-      float t4[4];
-      t4[0] = __uint_as_float(wu.x << 16);
-      t4[1] = __uint_as_float(wu.x & 0xffff0000u);
-      t4[2] = __uint_as_float(wu.y << 16);
-      t4[3] = __uint_as_float(wu.y & 0xffff0000u);
+    for (int p2 = 0; p2 < 4; ++p2) {
+      const unsigned char* wp = xt + (lc >> 6) * XSUB + WS_OFF + ((lc + 2 * p2) & 63) * KC * 2;
+      const uint2 wa = *reinterpret_cast<const uint2*>(wp);            // channel c+2p, taps 0..3
+      const uint2 wb = *reinterpret_cast<const uint2*>(wp + KC * 2);   // channel c+2p+1
+      const uint32_t a4[4] = {wa.x << 16, wa.x & 0xffff0000u, wa.y << 16, wa.y & 0xffff0000u};
+      const uint32_t b4[4] = {wb.x << 16, wb.x & 0xffff0000u, wb.y << 16, wb.y & 0xffff0000u};
 #pragma unroll
-      for (int j = 0; j < KC; ++j) wt[j][e] = t4[j];
+      for (int j = 0; j < KC; ++j) w2[j][p2] = (unsigned long long)a4[j] | ((unsigned long long)b4[j] << 32);
     }
-    float acc[4][8];
+    unsigned long long acc2[4][4];
 #pragma unroll
     for (int t = 0; t < 4; ++t)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc2[t][e] = 0ull;
 #pragma unroll
     for (int rr = 0; rr < 4 + KC - 1; ++rr) {
-      float xv[8];
-      load8(reinterpret_cast<const __nv_bfloat16*>(xt + (lc >> 6) * XSUB +
-                                                   tc::sw128_offset(i0 + rr, lc & 63)),
-            xv);
+      const uint4 xw = *reinterpret_cast<const uint4*>(xt + (lc >> 6) * XSUB +
+                                                       tc::sw128_offset(i0 + rr, lc & 63));
+      const unsigned long long xv2[4] = {bf2_to_f2(xw.x), bf2_to_f2(xw.y), bf2_to_f2(xw.z),
+                                         bf2_to_f2(xw.w)};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int j = rr - t;
         if (j >= 0 && j < KC) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[t][e] += wt[j][e] * xv[e];
+          for (int e = 0; e < 4; ++e) acc2[t][e] = fma2(w2[j][e], xv2[e], acc2[t][e]);
         }
       }
     }
+    float acc[4][8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[t][2 * e] = __uint_as_float((uint32_t)acc2[t][e]);
+        acc[t][2 * e + 1] = __uint_as_float((uint32_t)(acc2[t][e] >> 32));
+      }
     float y[4][8], ss[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
