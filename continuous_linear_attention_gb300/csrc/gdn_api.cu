@@ -34,8 +34,9 @@ size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
 // Prefill scratch, one row per packed token, as consecutive token-major arrays
 // (each row a multiple of 16 bytes): q~|k~ of every k-head and v of every
 // v-head (fp16), G and beta of every v-head (fp32), -w and u of every v-head
-// (fp16) and the rows of P of every v-head (fp16, 64 each).
-enum ScrPart { kScrQK = 0, kScrV, kScrG, kScrW, kScrU, kScrP, kScrParts };
+// (fp16), the rows of P of every v-head (fp16, 64 each) and one 8-byte record
+// per 64-token chunk (at most one chunk per row).
+enum ScrPart { kScrQK = 0, kScrV, kScrG, kScrW, kScrU, kScrP, kScrC, kScrParts };
 size_t scratch_part_bytes(const gdn_pool* p, int part) {
   switch (part) {
     case kScrQK: return (size_t)2 * p->Hk * p->dk * 2;
@@ -43,6 +44,7 @@ size_t scratch_part_bytes(const gdn_pool* p, int part) {
     case kScrG: return (size_t)p->Hv * 2 * 4;
     case kScrW: return (size_t)p->Hv * p->dk * 2;
     case kScrU: return (size_t)p->Hv * p->dv * 2;
+    case kScrC: return 16;
     default: return (size_t)p->Hv * 64 * 2;
   }
 }
@@ -310,6 +312,7 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
     fp.scr_w = scratch_part(p, kScrW);
     fp.scr_u = scratch_part(p, kScrU);
     fp.scr_p = scratch_part(p, kScrP);
+    fp.scr_c = scratch_part(p, kScrC);
   }
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;

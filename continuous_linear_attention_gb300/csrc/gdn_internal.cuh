@@ -73,12 +73,15 @@ struct FwdParams {
   //   scr_w  [T][Hv][d]    fp16  -w               (intra_kernel)
   //   scr_u  [T][Hv][d]    fp16  u = T diag(beta) v  (intra_kernel)
   //   scr_p  [T][Hv][64]   fp16  row of P         (intra_kernel)
+  //   scr_c  [chunks]      int2  (first packed row, valid tokens) of every
+  //                              prefill chunk, by chunk index (prep_kernel)
   void* scr_qk = nullptr;
   void* scr_v = nullptr;
   void* scr_g = nullptr;
   void* scr_w = nullptr;
   void* scr_u = nullptr;
   void* scr_p = nullptr;
+  void* scr_c = nullptr;
 };
 
 // Launchers (each returns a cudaError_t from the launch).

@@ -137,21 +137,12 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   const int h = (int)(blockIdx.x % (unsigned)p.Hv);   // heads of a chunk run next to each other
   const int gidx = (int)(blockIdx.x / (unsigned)p.Hv);
   if (gidx >= n_chunks) return;
-  // which prefill sequence / chunk: binary search in the chunk prefix
-  const int n_pre = hdr[kNPre];
-  const int32_t* cp = p.work.pre_cp();
-  int lo = 0, hi = n_pre - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cp[mid] <= gidx) lo = mid; else hi = mid - 1;
-  }
-  const int s = p.work.pre()[lo];
-  const int c0 = (gidx - cp[lo]) * CH;
+  // the chunk's first packed row and valid tokens, as prep_kernel recorded them
+  const int2 rec = reinterpret_cast<const int2*>(p.scr_c)[gidx];
   const int kh = h / R, r2 = h % R;
   const int Hv = p.Hv;
-  const int seq0 = p.cu[s];
-  const int n = min(CH, p.cu[s + 1] - seq0 - c0);
-  const int row0 = seq0 + c0;
+  const int n = rec.y;
+  const int row0 = rec.x;
   const size_t orow = (size_t)row0 * Hv + h;  // (packed row, head) index of row 0
   const int tid = threadIdx.x;
   const uint32_t lane = (uint32_t)(tid & 96) << 16;  // TMEM lane quarter of this warp

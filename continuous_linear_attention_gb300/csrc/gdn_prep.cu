@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
     }
     if ((tid & 63) == 31) gtot[tid >> 6] = gcum;
   }
+  if (tid == 0 && kh == 0)
+    reinterpret_cast<int2*>(p.scr_c)[gidx] = make_int2(seq0 + c0, n);  // the chunk's record
   if (tid == 0) ok = mbar_wait_bounded(&xbar, 0) ? 1 : 0;
   __syncthreads();
   if (tid < R * CH) {
