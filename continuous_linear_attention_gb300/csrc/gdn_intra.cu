@@ -1,6 +1,6 @@
 // State-independent half of the chunked prefill, fully parallel over the
 // 64-token chunks of the prefill sequences: one CTA per (chunk, v-head),
-// three CTAs per SM.
+// four CTAs per SM.
 //
 // With G_i the inclusive cumulative gate inside the chunk, beta_i the write
 // strength and q~/k~ the normalised rows (all from prep_kernel), the chunk-64
@@ -44,16 +44,19 @@ constexpr int R = 2;    // v-heads per k-head
 constexpr int AP = 68;  // pitch (floats) of the fp32 A / T rows
 constexpr float kF16Max = 65000.f;
 
-// shared memory map (offsets from a 1024-byte aligned base)
+// shared memory map (offsets from a 1024-byte aligned base).  Once X is done
+// the two q~ slots of the [q~ ; k~] tile are reused: slot 1 takes v columns
+// 64..127 at once, slot 0 holds the B blocks of the solve and then v columns
+// 0..63.  The A/T array becomes the MMAs' A tile when T is done.
 constexpr uint32_t BOX = 8192;         // one 64 x 64 fp16 box
 constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of the 128-row [q~ ; k~] tile
-constexpr uint32_t OFF_QK = 0;         // [q~ ; k~]; once X is done the q~ slots hold v
+constexpr uint32_t OFF_QK = 0;         // [q~ ; k~], 2 K-blocks x 128 rows
+constexpr uint32_t OFF_Z = 0;          // B blocks of the solve fp32 [6][16][20] (q~ slot 0)
 constexpr uint32_t OFF_AT = 32768;     // A, overwritten block by block by T: fp32 [64][AP]
-constexpr uint32_t OFF_TT = 50176;     // [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
-constexpr uint32_t OFF_Z = OFF_TT;     // during the solve: B blocks fp32 [6][16][20]
-constexpr uint32_t OFF_GT = 66560;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
-constexpr uint32_t OFF_GH = 67584;     // this head's G [64], contiguous
-constexpr uint32_t SMEM_BYTES = 67840 + 1024;
+constexpr uint32_t OFF_TT = OFF_AT;    // then [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
+constexpr uint32_t OFF_GT = 50176;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
+constexpr uint32_t OFF_GH = 51200;     // this head's G [64], contiguous
+constexpr uint32_t SMEM_BYTES = 51456 + 1024;
 constexpr uint32_t TM_COLS = 128;      // X (64 columns), then the 128-column products
 
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
@@ -124,12 +127,12 @@ __device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float
   *reinterpret_cast<float2*>(dp + (g + 8) * pd + n0 + 2 * t) = make_float2(s * acc[2], s * acc[3]);
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t lbar, vbar, mbar;
+  __shared__ uint64_t lbar, vbar0, vbar1, mbar;
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
   int32_t* hdr = p.work.header();
@@ -157,7 +160,8 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
 
   if (tid == 0) {
     mbar_init(&lbar, 1);
-    mbar_init(&vbar, 1);
+    mbar_init(&vbar0, 1);
+    mbar_init(&vbar1, 1);
     mbar_init(&mbar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&lbar, 4u * BOX + 1024u);
@@ -208,11 +212,10 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     tc::tmem_wait_ld();
     tc::fence_before_sync();
     __syncthreads();
-    // X is done with the q~ rows: this head's v rows come into their slots
+    // X is done with the q~ rows: v columns 64..127 come into q~ slot 1
     if (tid == 0) {
-      mbar_arrive_expect_tx(&vbar, 2u * BOX);
-      tma_load_2d(sm + OFF_QK, &tv, h * D, row0, &vbar);
-      tma_load_2d(sm + OFF_QK + KB_STRIDE, &tv, h * D + 64, row0, &vbar);
+      mbar_arrive_expect_tx(&vbar1, BOX);
+      tma_load_2d(sm + OFF_QK + KB_STRIDE, &tv, h * D + 64, row0, &vbar1);
     }
     {
       // row i of P (rows 0..63 of X) or of A (rows 64..127), this thread's 32
@@ -306,29 +309,48 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
             blk_mma3(acc, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP, n0);
           blk_store(AT + (16 * i) * AP + 16 * j, AP, n0, acc, -1.f);
         }
+        if (Lv == 3) tc::fence_proxy_async_smem();  // the B blocks' slot goes back to TMA
         __syncthreads();
       }
     }
-    // [-T diag(beta e^G) ; T diag(beta)] -> the MMAs' A tile (over the B
-    // blocks; upper blocks of T are zero)
+    // the B blocks are consumed: v columns 0..63 come into q~ slot 0
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&vbar0, BOX);
+      tma_load_2d(sm + OFF_QK, &tv, h * D, row0, &vbar0);
+    }
+    // [-T diag(beta e^G) ; T diag(beta)] -> the MMAs' A tile, over the A/T
+    // array once every T value is read (upper blocks of T are zero)
+    {
+      uint4 wtb[2], wtbe[2];
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
-      const int idx = tid + kThreads * q2;
-      const int i = idx >> 3, c8 = idx & 7;
-      float tb[8], tbe[8];
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int idx = tid + kThreads * q2;
+        const int i = idx >> 3, c8 = idx & 7;
+        float tb[8], tbe[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = c8 * 8 + e;
-        const float t = (j >> 4) <= (i >> 4) ? AT[i * AP + j] : 0.f;
-        tb[e] = t * GT[j * 4 + gc + 1];
-        tbe[e] = -tb[e] * __expf(GT[j * 4 + gc]);
-        amax = fmaxf(amax, fabsf(tb[e]));
+        for (int e = 0; e < 8; ++e) {
+          const int j = c8 * 8 + e;
+          const float t = (j >> 4) <= (i >> 4) ? AT[i * AP + j] : 0.f;
+          tb[e] = t * GT[j * 4 + gc + 1];
+          tbe[e] = -tb[e] * __expf(GH[j]);
+          amax = fmaxf(amax, fabsf(tb[e]));
+        }
+        wtb[q2] = pack8(tb);
+        wtbe[q2] = pack8(tbe);
       }
-      *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(i, c8 * 8)) = pack8(tbe);
-      *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(CH + i, c8 * 8)) = pack8(tb);
+      __syncthreads();
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int idx = tid + kThreads * q2;
+        const int i = idx >> 3, c8 = idx & 7;
+        *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(i, c8 * 8)) = wtbe[q2];
+        *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(CH + i, c8 * 8)) = wtb[q2];
+      }
     }
     // this head's v rows have landed; rows past the sequence -> 0
-    ok = cta_wait(&vbar, 0, &flag);
+    if (tid == 0) flag = (mbar_wait_bounded(&vbar1, 0) && mbar_wait_bounded(&vbar0, 0)) ? 1 : 0;
+    __syncthreads();
+    ok = flag != 0;
   }
   if (ok) {
     if (n < CH) {
