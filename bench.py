@@ -155,9 +155,10 @@ def prefill_flops(wl, chunk: int = 64) -> float:
     return float(d.Hv * per * toks)
 
 
-def time_secondary(harness, wl, steps, device, pk):
+def time_secondary(harness, wl, steps, device, pk, graph=False):
     """Tokens/s and the compute kernels' roofline for another workload (the
-    ~16k-token prefill, the mixed batch), timed like the main line."""
+    ~16k-token prefill, the mixed batch), timed like the main line; with
+    graph=True also the forward replayed as a CUDA graph."""
     import torch
     run = harness.DeviceRun(wl, device=device)
     stream = torch.cuda.current_stream()
@@ -179,14 +180,79 @@ def time_secondary(harness, wl, steps, device, pk):
     run.pool.set_timing_events(None, None)
     ms = start.elapsed_time(stop) / steps
     kms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(steps))
+    gms = time_graph(run, steps) if graph else None
     flags = run.pool.error_flags()
     run.close()
     fl = prefill_flops(wl)
     tf = fl / (kms / 1e3) / 1e12
-    return {"workload": wl.name, "tokens": wl.T, "ms_per_step": ms,
-            "tokens_per_s": wl.T / (ms / 1e3), "compute_kernels_ms": kms,
-            "prefill_tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
-            "algorithmic_flops": fl, "error_flags": flags}
+    res = {"workload": wl.name, "tokens": wl.T, "ms_per_step": ms,
+           "tokens_per_s": wl.T / (ms / 1e3), "compute_kernels_ms": kms,
+           "prefill_tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
+           "algorithmic_flops": fl, "error_flags": flags}
+    if gms is not None:
+        res["graph_replay_ms_per_step"] = gms
+        res["graph_replay_tokens_per_s"] = wl.T / (gms / 1e3)
+    return res
+
+
+def time_graph(run, steps, hint=0):
+    """The same forward captured once in a CUDA graph and replayed: ms per
+    replay (the prefill scratch, if any, was grown by earlier calls)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run.run(torch.cuda.current_stream(), max_seqlen_hint=hint)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / steps
+
+
+def time_long_context(harness, binding, synth, device, pk, steps=3):
+    """The long-context case: 4 sequences of 32768 tokens with no past, then
+    4096 more tokens each continued from the states the first call left; one
+    step is both calls."""
+    import torch
+    first, cont, _ = synth.long_context()
+    run = harness.DeviceRun(first, device=device)
+    dims = cont.dims
+    x2, a2, b2 = cont.x.to(device), cont.a.to(device), cont.b.to(device)
+    cu2, idx2, hp2 = (cont.cu_seqlens.to(device), cont.block_idx.to(device),
+                      cont.has_past.to(device))
+    out2 = torch.empty((cont.T, dims.Hv, dims.dv), dtype=dims.torch_act, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        run.run(stream)
+        binding.varlen_forward(run.pool, run.layer, x2, a2, b2, cu2, idx2, hp2, run.conv_w,
+                               run.A_log, run.dt_bias, out2, cont.T, cont.N, 0, stream)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flags = run.pool.error_flags()
+    run.close()
+    fl = prefill_flops(first) + prefill_flops(cont)
+    tf = fl / (ms / 1e3) / 1e12
+    tokens = first.T + cont.T
+    return {"workload": "long_4x32768_then_4x4096", "tokens": tokens, "ms_per_step": ms,
+            "tokens_per_s": tokens / (ms / 1e3), "prefill_tflops": tf,
+            "tensor_frac": tf / pk["bf16_tflops"], "algorithmic_flops": fl,
+            "error_flags": flags, "note": "both calls per step, all kernels included"}
 
 
 def max_over_ranks(values, device="cpu"):
@@ -260,7 +326,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the prefill / mixed-batch measurements")
+                    help="skip the prefill / mixed-batch / long-context measurements")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long-context measurement (4 x 32768 + 4 x 4096 tokens)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -315,6 +383,7 @@ def main():
         torch.cuda.synchronize()
     run.pool.set_timing_events(None, None)
     elapsed_ms = start.elapsed_time(stop)
+    graph_ms = time_graph(run, min(args.steps, 200), hint)
     kern_ms = [kb[i].elapsed_time(ka[i]) for i in range(args.steps)]
     flags = run.pool.error_flags()
     if flags:
@@ -377,12 +446,19 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
+            "graph_replay": {"ms_per_step": graph_ms,
+                             "tokens_per_s": wl.T * world / (graph_ms / 1e3),
+                             "note": "the decode step captured once as a CUDA graph and replayed"},
         }
         if not args.no_secondary:
+            from continuous_linear_attention_gb300 import binding
+            dev = f"cuda:{local_rank}"
             line["secondary"] = [
-                time_secondary(harness, synth.packed_prefill(), 20, f"cuda:{local_rank}", pk),
-                time_secondary(harness, synth.mixed_batch(), 20, f"cuda:{local_rank}", pk),
+                time_secondary(harness, synth.packed_prefill(), 20, dev, pk),
+                time_secondary(harness, synth.mixed_batch(), 20, dev, pk, graph=True),
             ]
+            if not args.no_long:
+                line["secondary"].append(time_long_context(harness, binding, synth, dev, pk))
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(line), flush=True)
