@@ -95,17 +95,6 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* fl
   return *flag != 0;
 }
 
-__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* v) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 f = __bfloat1622float2(h[j]);
-    v[2 * j] = f.x;
-    v[2 * j + 1] = f.y;
-  }
-}
-
 // Packed fp32 pairs: d = a * b + c on both lanes (one fma.rn.f32x2).
 __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
                                                    unsigned long long c) {
@@ -151,7 +140,6 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   int32_t* hdr = p.work.header();
   const int n_chains = hdr[kNPre] * Hv;
   if ((int)blockIdx.x >= n_chains) return;
-  const __nv_bfloat16* __restrict__ x = reinterpret_cast<const __nv_bfloat16*>(p.x);
   const __nv_bfloat16* __restrict__ wconv = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
   const __nv_bfloat16* __restrict__ av = reinterpret_cast<const __nv_bfloat16*>(p.a);
   const __nv_bfloat16* __restrict__ bv = reinterpret_cast<const __nv_bfloat16*>(p.b);

@@ -22,11 +22,13 @@
 // Tensor cores: X = [q~ ; k~] k~^T (128 x 64 x 128), then
 // [-T diag(beta e^G) ; T diag(beta)] times k~ and times v (128 x 128 x 64
 // each, k~ and v as MN-major operands straight from their token-major tiles:
-// rows 0..63 of the first product are -w, rows 64..127 of the second are u).  CUDA cores: the masks, the blocked forward
-// substitution of T (16 x 16 diagonal blocks, then the off-diagonal blocks
-// level by level) and the conversions.  Rows of the tiles past the end of the
-// sequence are zeroed in shared memory first, so that no value of another
-// sequence (or stale scratch) reaches a product.
+// rows 0..63 of the first product are -w, rows 64..127 of the second are u),
+// and the 16 x 16 block products of the solve on the warp-level path
+// (mma.sync, tf32 with a head/tail split).  CUDA cores: the masks, the
+// diagonal 16 x 16 blocks of T by column substitution, and the conversions.
+// Rows of the tiles past the end of the sequence are zeroed in shared memory
+// first, so that no value of another sequence (or stale scratch) reaches a
+// product.
 #include <cuda.h>
 
 #include "gdn_internal.cuh"
