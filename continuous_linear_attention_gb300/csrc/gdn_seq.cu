@@ -10,9 +10,11 @@
 // as
 //   CUDA  S0 -> fp16 operand tile;  TMEM S <- e^{G_C} S0
 //   MMA   D  = [-w ; q~] S0^T
-//   CUDA  U  = u + D[0..63] -> fp16 token-major tiles U and e^{G_C - G} U
-//         (rows past n zeroed);  D[64 + i] <- e^{G_i} D[64 + i] in TMEM
-//   MMA   S += (e^{G_C - G} U)^T k~            (U and k~ as MN-major operands)
+//   CUDA  k~_j <- e^{G_C - G_j} k~_j in the staged tile (rows past n zeroed),
+//         while the D product runs
+//   CUDA  U  = u + D[0..63] -> fp16 token-major tile (rows past n zeroed);
+//         D[64 + i] <- e^{G_i} D[64 + i] in TMEM
+//   MMA   S += U^T (e^{G_C - G} k~)            (U and k~ as MN-major operands)
 //   MMA   D += [0 ; P] U                       (rows 64..127: + P U)
 //   CUDA  o_i = D[64 + i] -> bf16              (while the next chunk's MMAs run)
 // This is the chunked gated delta rule (Gated Delta Networks, chunkwise WY
@@ -22,10 +24,10 @@
 // Persistent CTAs, one per SM: warp 8 is the producer (one TMA issue lane
 // that pulls chains, longest sequences first, from the scheduler's counter
 // and streams each chunk's tiles into a 2-stage ring), warp 9 issues the
-// MMAs when the compute warps release it through a named barrier, and warps
+// MMAs when the compute warps release it through named barriers, and warps
 // 0-7 run the chain.  A compute thread owns TMEM lane (tid % 128) and one half
 // of the columns; the warps on lanes 0..63 convert U, those on lanes 64..127
-// write outputs.
+// scale the k~ tile and write outputs.
 #include <cuda.h>
 
 #include "gdn_internal.cuh"
@@ -43,9 +45,10 @@ constexpr int kProducer = kCompute;       // first thread of the TMA warp
 constexpr int kIssuer = kCompute + 32;    // first thread of the MMA warp
 constexpr int kThreads = kCompute + 64;
 // named barriers: 1 the compute warps; 2 compute warps -> MMA warp (S0 tile
-// written); 3 compute warps -> MMA warp (U tiles written, outputs rescaled)
-constexpr int kBarC = 1, kBarD = 2, kBarS = 3;
-constexpr int kGateD = kCompute + 32, kGateS = kCompute + 32;
+// written); 3 compute warps -> MMA warp (k~ tile scaled, U tile written);
+// 4 output warps -> MMA warp (output rows rescaled)
+constexpr int kBarC = 1, kBarD = 2, kBarS = 3, kBarO = 4;
+constexpr int kGateD = kCompute + 32, kGateS = kCompute + 32, kGateO = kCompute / 2 + 32;
 constexpr int R = 2;  // v-heads per k-head
 constexpr float kF16Max = 65000.f;
 
@@ -61,8 +64,9 @@ constexpr uint32_t ST_BYTES = 82944;
 constexpr uint32_t ST_TX = ST_BYTES - BOX;  // what the TMA brings (all but the zero tile)
 // CTA shared memory
 constexpr uint32_t OFF_S0 = 2 * ST_BYTES;    // S0 fp16, 2 K-blocks x 128 rows
-constexpr uint32_t OFF_UD = OFF_S0;          // e^{G_C - G} U, over S0 once the D product is done
-constexpr uint32_t OFF_UT = OFF_S0 + 32768;  // U fp16 [64 tokens][128]: two 64-column boxes
+// U fp16 [64 tokens][128]: two 64-column boxes (apart from S0: D += P U may
+// still read it while the next chunk's S0 is written)
+constexpr uint32_t OFF_UT = OFF_S0 + 32768;
 constexpr uint32_t SMEM_BYTES = OFF_UT + 16384 + 1024;
 // tensor memory columns: the state, two accumulators D
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_COLS = 512;
@@ -164,10 +168,13 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
 
   if (tid >= kIssuer) {
     // ============================= MMA warp ==============================
-    // Chunk k: gate kBarD (S0 tile ready)    -> D = [-w ; q~] S0^T;
-    //          gate kBarS (U tiles ready)     -> S += (e^{G_C-G} U)^T k~, D += [0 ; P] U.
+    // Chunk k: gate kBarD (S0 tile ready)          -> D = [-w ; q~] S0^T;
+    //          gate kBarS (k~ scaled, U tile ready) -> S += U^T (e^{G_C-G} k~);
+    //          gate kBarO (output rows rescaled)    -> D += [0 ; P] U.
     // mma_s covers the state update only (the next hand-over waits for it),
     // except on a chain's last chunk, whose outputs are written right away.
+    // The compute warps only ever leave while this warp waits at kBarD or
+    // kBarS, so the stop flag is read there.
     for (int k = 0;; ++k) {
       const int b = k & 1;
       const uint32_t sb = sbase + b * ST_BYTES;
@@ -184,19 +191,21 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       __syncwarp();
       mma_gate<kBarS, kGateS>();
       if (mma_stop) break;
+      const bool last = (desc[b].flags & 2) != 0;
+      const tc::Opnd ut{sbase + OFF_UT, BOX, true};
       if (tid == kIssuer) {
         tc::fence_after_sync();
-        const bool last = (desc[b].flags & 2) != 0;
-        const tc::Opnd ut{sbase + OFF_UT, BOX, true};
-        auto mma_o = [&]() {
-          tc::mma_op(tmem + dcol, tc::Opnd{sb + ST_ZP, 0u, false}, ut, CH / 16,
-                     tc::idesc_f16_f32(128, 128, false, true), true);
-        };
-        if (last) mma_o();
-        tc::mma_op(tmem + TM_S, tc::Opnd{sbase + OFF_UD, BOX, true}, tc::Opnd{sb + ST_K, BOX, true},
-                   CH / 16, tc::idesc_f16_f32(128, 128, true, true), true);
-        tc::commit(&mma_s);
-        if (!last) mma_o();
+        tc::mma_op(tmem + TM_S, ut, tc::Opnd{sb + ST_K, BOX, true}, CH / 16,
+                   tc::idesc_f16_f32(128, 128, true, true), true);
+        if (!last) tc::commit(&mma_s);
+      }
+      __syncwarp();
+      mma_gate<kBarO, kGateO>();
+      if (tid == kIssuer) {
+        tc::fence_after_sync();
+        tc::mma_op(tmem + dcol, tc::Opnd{sb + ST_ZP, 0u, false}, ut, CH / 16,
+                   tc::idesc_f16_f32(128, 128, false, true), true);
+        if (last) tc::commit(&mma_s);
         tc::commit(&empty[b]);  // the stage is free once these MMAs are done
       }
       __syncwarp();
@@ -305,13 +314,6 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       const int r2 = d.h % R;
       const int n = d.n;
       const float GC = GT[(n - 1) * 4 + 2 * r2];
-      if (n < CH) {
-        // k~ rows past the sequence -> 0 (they meet zero U rows in the state update)
-        for (int t = tid; t < (CH - n) * 16; t += kCompute)
-          *reinterpret_cast<uint4*>(st + ST_K + (t & 8 ? BOX : 0) + (n + (t >> 4)) * 128 + (t & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
-        tc::fence_proxy_async_smem();
-      }
       // ---- the previous chunk's MMAs are done: S and its D readable
       if (s_busy) {
         if (!wait_c(&mma_s, ph_s)) { dead = true; break; }
@@ -356,13 +358,35 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       next_gate = kBarS;
       const int ob = k & 1;
       const uint32_t dcol = TM_D + ob * 128;
-      // ---- while the tensor core runs: this chunk's u row
+      // ---- while the tensor core runs: this chunk's u row (U-row warps), or
+      // k~_j <- e^{G_C - G_j} k~_j for the state update, rows past the
+      // sequence -> 0 (output warps: row j of column half hf, its 16-byte
+      // chunks in an order rotated by j, which keeps the accesses conflict-free)
       uint4 ur[8];
       if (urow) {
         const unsigned char* urow_p = st + ST_U + hf * BOX + j * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           ur[c] = *reinterpret_cast<const uint4*>(urow_p + ((c ^ (j & 7)) << 4));
+      } else {
+        unsigned char* krow = st + ST_K + hf * BOX + j * 128;
+        if (j < n) {
+          const float ds = __expf(GC - GT[j * 4 + 2 * r2]);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4* q = reinterpret_cast<uint4*>(krow + (((c + j) & 7) << 4));
+            float k8[8];
+            unpack8(*q, k8);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) mul2(k8[e], k8[e + 1], ds);
+            *q = pack8(k8);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(krow + (c << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_proxy_async_smem();
+        mma_release<kBarS, kGateS>();
       }
       if (!wait_c(&mma_y, ph_y)) { dead = true; break; }
       ph_y ^= 1;
@@ -373,8 +397,6 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       // D += P U finished before this chunk's D product)
       if (urow) {
         unsigned char* dst = sm + OFF_UT + hf * BOX + j * 128;
-        unsigned char* dsd = sm + OFF_UD + hf * BOX + j * 128;
-        const float ds = j < n ? __expf(GC - GT[j * 4 + 2 * r2]) : 0.f;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float dv[32];
@@ -383,7 +405,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const int c = hh * 4 + c4;
-            uint4 w = make_uint4(0, 0, 0, 0), wd = make_uint4(0, 0, 0, 0);
+            uint4 w = make_uint4(0, 0, 0, 0);
             if (j < n) {
               float u8[8];
               unpack8(ur[c], u8);
@@ -395,12 +417,8 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
               }
               amax = fmaxf(amax, m2);
               w = pack8(u8);
-#pragma unroll
-              for (int e = 0; e < 8; e += 2) mul2(u8[e], u8[e + 1], ds);
-              wd = pack8(u8);
             }
             *reinterpret_cast<uint4*>(dst + ((c ^ (j & 7)) << 4)) = w;
-            *reinterpret_cast<uint4*>(dsd + ((c ^ (j & 7)) << 4)) = wd;
           }
         }
         tc::fence_proxy_async_smem();
@@ -420,8 +438,8 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
         tc::tmem_wait_st();
       }
       tc::fence_before_sync();
-      mma_release<kBarS, kGateS>();  // S += (e^{G_C - G} U)^T k~;  D += [0 ; P] U
-      pending = false;
+      if (urow) mma_release<kBarS, kGateS>();  // S += U^T (e^{G_C - G} k~)
+      else mma_release<kBarO, kGateO>();       // D += [0 ; P] U
       next_gate = kBarD;
       s_busy = true;
       pending = true;
@@ -454,7 +472,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     if (tid == 0) mma_stop = 1;
     cbar();
     if (next_gate == kBarD) mma_release<kBarD, kGateD>();
-    else mma_release<kBarS, kGateS>();
+    else if (urow) mma_release<kBarS, kGateS>();  // the output warps arrived after scaling k~
     if (dead && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
     // the state and U enter tensor-core operands in fp16
     if (!(amax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
