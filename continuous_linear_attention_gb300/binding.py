@@ -215,10 +215,11 @@ def diag_umma_gemm(A, B, C, D, operand_f16=False, stream=None) -> None:
 
 def diag_umma_gemm_ex(A, B, C, D, operand_f16=False, a_mn=False, b_mn=False,
                       stream=None) -> None:
-    """gdn_diag_umma_gemm_ex: the same GEMM with A and/or B staged MN-major."""
+    """gdn_diag_umma_gemm_ex: the same GEMM with A and/or B staged MN-major
+    (a_mn=2: A in tensor memory instead)."""
     N, K = B.shape
     _check(load().gdn_diag_umma_gemm_ex(_ptr(A), _ptr(B), _ptr(C), _ptr(D), N, K,
-                                        1 if operand_f16 else 0, 1 if a_mn else 0,
+                                        1 if operand_f16 else 0, int(a_mn),
                                         1 if b_mn else 0, _stream(stream)),
            "gdn_diag_umma_gemm_ex")
 

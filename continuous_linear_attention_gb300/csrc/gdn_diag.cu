@@ -1,6 +1,6 @@
 // Diagnostic tensor-core GEMM (see include/gdn_diag.h): exercises the shared
-// tile layout, descriptors, MMA issue/commit and TMEM load/store helpers of
-// gdn_tc.cuh on plain matrices.
+// tile layout, descriptors, MMA issue/commit (A from shared or from tensor
+// memory) and TMEM load/store helpers of gdn_tc.cuh on plain matrices.
 #include <type_traits>
 
 #include "gdn.h"
@@ -19,6 +19,8 @@ constexpr int kM = 128;
 constexpr uint32_t kBOff = 80 * 1024;
 constexpr uint32_t kMnStride = 64 * 128;
 constexpr uint32_t kSmem = 160 * 1024 + 1024;
+// tensor memory: D in columns 0..N-1, an A staged in tensor memory from 256 on
+constexpr uint32_t kATmem = 256;
 
 template <typename E>
 __global__ void __launch_bounds__(128, 1)
@@ -40,7 +42,7 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
     return mn ? (uint32_t)(r >> 6) * kMnStride + tc::sw128_offset(k, r & 63)
               : (uint32_t)(k >> 6) * kb_stride + tc::sw128_offset(r, k & 63);
   };
-  for (int idx = tid; idx < kM * K; idx += 128) {
+  for (int idx = tid; a_mn != 2 && idx < kM * K; idx += 128) {
     const int r = idx / K, k = idx % K;
     const float v = __bfloat162float(A[idx]);
     unsigned char* dst = a_tile + off(a_mn != 0, a_kb, r, k);
@@ -58,7 +60,7 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
-  if (tid < 32) tc::tmem_alloc(&tmem_slot, 256);
+  if (tid < 32) tc::tmem_alloc(&tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -72,18 +74,31 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
     }
     tc::tmem_wait_st();
   }
+  if (a_mn == 2) {
+    // A row tid -> lane tid, columns kATmem.., K-elements 2c and 2c+1 in column c
+    for (int c0 = 0; c0 < K / 2; c0 += 16) {
+      uint32_t w[16];
+      for (int j = 0; j < 16; ++j) {
+        const float lo = __bfloat162float(A[(size_t)tid * K + 2 * (c0 + j)]);
+        const float hi = __bfloat162float(A[(size_t)tid * K + 2 * (c0 + j) + 1]);
+        w[j] = tc::pack2(lo, hi, (E*)nullptr);
+      }
+      tc::tmem_st16u(tmem + lane_base + kATmem + c0, w);
+    }
+    tc::tmem_wait_st();
+  }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   if (tid == 0) {
     tc::fence_after_sync();
     constexpr bool kF16 = std::is_same<E, __half>::value;
-    const tc::Opnd a{smem_u32(a_tile), a_mn ? kMnStride : a_kb, a_mn != 0};
+    const tc::Opnd a{smem_u32(a_tile), a_mn ? kMnStride : a_kb, a_mn == 1};
     const tc::Opnd b{smem_u32(b_tile), b_mn ? kMnStride : b_kb, b_mn != 0};
-    tc::mma_op(tmem, a, b, K / 16,
-               kF16 ? tc::idesc_f16_f32(kM, N, a_mn != 0, b_mn != 0)
-                    : tc::idesc_bf16_f32(kM, N, a_mn != 0, b_mn != 0),
-               Cin != nullptr);
+    const uint32_t idesc = kF16 ? tc::idesc_f16_f32(kM, N, a_mn == 1, b_mn != 0)
+                                : tc::idesc_bf16_f32(kM, N, a_mn == 1, b_mn != 0);
+    if (a_mn == 2) tc::mma_op_ts(tmem, tmem + kATmem, b, K / 16, idesc, Cin != nullptr);
+    else tc::mma_op(tmem, a, b, K / 16, idesc, Cin != nullptr);
     tc::commit(&bar);
     ok = mbar_wait_bounded(&bar, 0) ? 1 : 0;
   }
@@ -101,7 +116,7 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (tid < 32) tc::tmem_dealloc(tmem, 256);
+  if (tid < 32) tc::tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -113,7 +128,8 @@ extern "C" int gdn_diag_umma_gemm_ex(const void* A, const void* B, const float* 
   if (!A || !B || !D) return GDN_ERR_NULL;
   if ((N != 64 && N != 128 && N != 192 && N != 256) || (K != 64 && K != 128))
     return GDN_ERR_DIMS;
-  if ((a_mn || b_mn) && K != 64) return GDN_ERR_DIMS;
+  if (a_mn < 0 || a_mn > 2 || b_mn < 0 || b_mn > 1) return GDN_ERR_DIMS;
+  if ((a_mn == 1 || b_mn) && K != 64) return GDN_ERR_DIMS;
   if (((uintptr_t)A & 15) || ((uintptr_t)B & 15) || ((uintptr_t)D & 15) || ((uintptr_t)C & 15))
     return GDN_ERR_ALIGN;
   static unsigned* err = nullptr;

@@ -157,6 +157,29 @@ __device__ __forceinline__ void mma_op(uint32_t d_tmem, const Opnd& a, const Opn
     mma_bf16(d_tmem, opnd_desc(a, s), opnd_desc(b, s), idesc, (accumulate || s > 0) ? 1u : 0u);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T for one K=16 step (cta_group::1).  A sits
+// in tensor memory: row m in lane m, its 16 K-elements in 8 consecutive
+// 32-bit columns, two per column (the lower K index in the low half).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (M=128 rows) (+)= A * B^T over K = 16 * ksteps with A in tensor memory
+// from column a_tmem on (K-major by construction: the A bit of idesc is 0).
+__device__ __forceinline__ void mma_op_ts(uint32_t d_tmem, uint32_t a_tmem, const Opnd& b,
+                                          int ksteps, uint32_t idesc, bool accumulate) {
+#pragma unroll 4
+  for (int s = 0; s < ksteps; ++s)
+    mma_ts(d_tmem, a_tmem + 8u * (uint32_t)s, opnd_desc(b, s), idesc,
+           (accumulate || s > 0) ? 1u : 0u);
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile(
@@ -221,6 +244,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// 16 consecutive TMEM columns of this thread's lane, raw 32-bit words (e.g.
+// two packed 16-bit operand elements each).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
       : "memory");
 }
 

@@ -20,6 +20,10 @@
  * consecutive M / N elements of one K index, the layout a 2-D TMA box of a
  * token-major matrix lands in) and set the matching instruction-descriptor
  * bits.  MN-major operands need K == 64 (GDN_ERR_DIMS otherwise).
+ * a_mn == 2 instead places A in tensor memory (row m in lane m, two 16-bit
+ * K-elements per 32-bit column, the lower K index in the low half) and issues
+ * the MMA form that reads A from there; any K of the list above.  a_mn outside
+ * 0..2 or b_mn outside 0..1: GDN_ERR_DIMS.
  */
 #ifndef GDN_DIAG_H_
 #define GDN_DIAG_H_
