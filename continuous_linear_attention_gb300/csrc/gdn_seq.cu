@@ -9,8 +9,10 @@
 //   columns 0..63  : U^T = u^T - S0 w^T            (the chunk's updates u_j)
 //   columns 64..127: O^T = S0 (e^G q~)^T + U^T P^T (the chunk's outputs o_i)
 // as
-//   CUDA  S0 -> fp16 A operand in tensor memory;  S <- e^{G_C} S0
-//   MMA   D^T  = S0 [-w ; q~]^T;  D^T[:, j] += u_j  (u^T times an identity)
+//   CUDA  S0 -> fp16 A operand in tensor memory;  S <- e^{G_C} S0, in two
+//         passes over k (0..63, then 64..127)
+//   MMA   D^T  = S0 [-w ; q~]^T (the first pass's K-steps start while the
+//         second pass runs);  D^T[:, j] += u_j  (u^T times an identity)
 //   CUDA  k~_j <- e^{G_C - G_j} k~_j in the staged tile, rows past n zeroed
 //         (while the D product runs)
 //   CUDA  U^T = D^T[:, 0..63] -> fp16 A operand in tensor memory (columns
@@ -46,9 +48,10 @@ constexpr int kCompute = 256;
 constexpr int kProducer = kCompute;       // first thread of the TMA warp
 constexpr int kIssuer = kCompute + 32;    // first thread of the MMA warp
 constexpr int kThreads = kCompute + 64;
-// named barriers: 1 the compute warps; compute warps -> MMA warp: 2 S0
-// written, 3 k~ tile scaled and U^T written, 4 output columns rescaled
-constexpr int kBarC = 1, kBarD = 2, kBarS = 3, kBarO = 4;
+// named barriers: 1 the compute warps; compute warps -> MMA warp: 5 S0
+// columns k < 64 written, 2 all of S0 written, 3 k~ tile scaled and U^T
+// written, 4 output columns rescaled
+constexpr int kBarC = 1, kBarD = 2, kBarS = 3, kBarO = 4, kBarD1 = 5;
 constexpr int kGate = kCompute + 32;
 constexpr int R = 2;  // v-heads per k-head
 constexpr float kF16Max = 65000.f;
@@ -164,23 +167,35 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
 
   if (tid >= kIssuer) {
     // ============================= MMA warp ==============================
-    // Chunk k: gate kBarD (S0 written)       -> D^T = S0 [-w ; q~]^T, + u^T I;
+    // Chunk k: gate kBarD1 (S0, k < 64)      -> D^T  = S0[:, :64] [-w ; q~][:, :64]^T;
+    //          gate kBarD (all of S0)        -> D^T += S0[:, 64:] [-w ; q~][:, 64:]^T, + u^T I;
     //          gate kBarS (k~ scaled, U^T)   -> S += U^T (e^{G_C-G} k~);
     //          gate kBarO (outputs rescaled) -> D^T[:, 64..] += U^T P^T.
     // mma_s covers the state update only (the next hand-over waits for it),
     // except on a chain's last chunk, whose outputs are written right away.
-    // The compute warps only ever leave while this warp waits at kBarD or
+    // The compute warps only ever leave while this warp waits at kBarD1 or
     // kBarS, so the stop flag is read there.
     for (int k = 0;; ++k) {
       const int b = k % kStages;
       const uint32_t sb = sbase + b * ST_BYTES;
       const uint32_t dcol = TM_D + (k & 1) * 128;
-      mma_gate<kBarD>();
+      const tc::Opnd qw{sb + ST_QW, KB_STRIDE, false};
+      mma_gate<kBarD1>();
       if (mma_stop) break;
       if (tid == kIssuer) {
         tc::fence_after_sync();
-        tc::mma_op_ts(tmem + dcol, tmem + TM_S0, tc::Opnd{sb + ST_QW, KB_STRIDE, false}, D / 16,
-                      tc::idesc_f16_f32(128, 128), false);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          tc::mma_ts(tmem + dcol, tmem + TM_S0 + 8 * s, tc::opnd_desc(qw, s), tc::idesc_f16_f32(128, 128),
+                     s > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+      mma_gate<kBarD>();
+      if (tid == kIssuer) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int s = 4; s < 8; ++s)
+          tc::mma_ts(tmem + dcol, tmem + TM_S0 + 8 * s, tc::opnd_desc(qw, s), tc::idesc_f16_f32(128, 128), 1u);
         // + u_j on column j: u^T (MN-major; K-step s = tokens 16s..16s+15)
         // times the identity, into columns 16s..16s+15
 #pragma unroll
@@ -279,7 +294,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     bool pending = false;  // outputs of the previous chunk not written yet
     int p_row = 0, p_n = 0, p_h = 0, p_ob = 0;
     bool dead = false;
-    int next_gate = kBarD;  // the gate the MMA warp waits at
+    int next_gate = kBarD1;  // the gate the MMA warp waits at
     float amax = 0.f;
     // outputs i = 32 hf .. 32 hf + 31 of the pending chunk: column 64 + i of
     // its D^T at this thread's v (a warp writes 64 contiguous bytes per token;
@@ -318,14 +333,16 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
         tc::fence_after_sync();
       }
       // ---- state hand-over: S0 -> fp16 A operand, S <- e^{G_C} S0
-      // (this thread: row v, k = 64 hf .. 64 hf + 63, 32 at a time)
+      // (this thread: row v, k = 32 hf .. 32 hf + 31, then 64 + the same;
+      // the first K-block of the D product starts after the first pass)
+      tc::fence_proxy_async_smem();  // the zeroed u rows
       {
         const float dc = __expf(GC);
         const float* S_r = reinterpret_cast<const float*>(p.layer_base + (size_t)d.rblk * p.stride +
                                                           p.rec_off) + (size_t)d.h * D * D;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int k0 = hf * 64 + hh * 32;
+          const int k0 = hh * 64 + hf * 32;
           float srow[32];
           if (d.flags & 1) {
 #pragma unroll
@@ -346,12 +363,12 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
 #pragma unroll
           for (int kk = 0; kk < 32; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
           tc::tmem_st32(tmem + lane + TM_S + k0, srow);
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          if (hh == 0) mma_release<kBarD1>();  // D^T = S0[:, :64] [-w ; q~][:, :64]^T
         }
-        tc::tmem_wait_st();
       }
-      tc::fence_proxy_async_smem();  // the zeroed u rows
-      tc::fence_before_sync();
-      mma_release<kBarD>();  // D^T = S0 [-w ; q~]^T + u^T
+      mma_release<kBarD>();  // D^T += S0[:, 64:] [-w ; q~][:, 64:]^T + u^T
       next_gate = kBarS;
       const int ob = k & 1;
       const uint32_t dcol = TM_D + ob * 128;
@@ -421,7 +438,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
       }
       tc::fence_before_sync();
       mma_release<kBarO>();  // D^T[:, 64..] += U^T P^T
-      next_gate = kBarD;
+      next_gate = kBarD1;
       // ---- the previous chunk's outputs (its U^T P^T finished before this
       // chunk's D product)
       if (pending) flush();
@@ -454,7 +471,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     // let the MMA warp out of the gate it waits at
     if (tid == 0) mma_stop = 1;
     cbar();
-    if (next_gate == kBarD) mma_release<kBarD>();
+    if (next_gate == kBarD1) mma_release<kBarD1>();
     else mma_release<kBarS>();
     if (dead && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
     // the state and U enter tensor-core operands in fp16
