@@ -134,6 +134,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   __shared__ int flag;
   __shared__ int s_chain;
 
+  pdl_wait_then_release();
   const int tid = threadIdx.x;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
   const int R = Hv / Hk;
@@ -633,6 +634,7 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
 // [old conv state ; x_seq], written after every chain has read the old one.
 // Grid (sequence, channel slice); each thread moves 8 channels of the K-1 rows.
 __global__ void __launch_bounds__(256) tail_update_kernel(FwdParams p) {
+  pdl_wait_then_release();
   const int n_pre = p.work.header()[kNPre];
   if ((int)blockIdx.x >= n_pre) return;
   const int s = p.work.pre()[blockIdx.x];
@@ -738,7 +740,8 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     CUtensorMap tmx;
     e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
     if (e != cudaSuccess) return e;
-    chunk_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, tmx);
+    e = launch_pdl(chunk_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p, tmx);
+    if (e != cudaSuccess) return e;
   } else {
     // split: conv prologue and gates (prep_kernel), the state-independent
     // products of every chunk (intra_kernel), then the recurrence over the
@@ -761,8 +764,7 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  tail_update_kernel<<<dim3(max_pre, (p.C / 8 + 255) / 256), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(tail_update_kernel, dim3(max_pre, (p.C / 8 + 255) / 256), dim3(256), 0, stream, p);
 }
 
 }  // namespace gdn

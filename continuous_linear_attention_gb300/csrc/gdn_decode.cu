@@ -82,6 +82,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  pdl_wait_then_release();
   const int tid = threadIdx.x;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
   const int n_units = p.work.header()[kNDec] * Hk;
@@ -309,7 +310,8 @@ cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream) 
   cudaError_t e =
       cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<<<grid, kThreads, smem, stream>>>(p);
+  e = launch_pdl(decode_kernel, dim3(grid), dim3(kThreads), smem, stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -84,6 +84,25 @@ struct FwdParams {
   void* scr_c = nullptr;
 };
 
+// Launch with programmatic stream serialization: the grid may be scheduled
+// before the previous kernel on the stream completes; the kernel orders
+// itself with pdl_wait_then_release() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
 // The token-serial kernel runs over all active sequences (long_only = false)

@@ -137,6 +137,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   __shared__ uint64_t lbar, vbar0, vbar1, mbar;
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
+  pdl_wait_then_release();
   int32_t* hdr = p.work.header();
   const int n_chunks = hdr[kPreChunks];
   const int h = (int)(blockIdx.x % (unsigned)p.Hv);   // heads of a chunk run next to each other
@@ -432,10 +433,9 @@ cudaError_t launch_intra(const FwdParams& p, const void* qk_map, const void* v_m
   cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  intra_kernel<<<(unsigned)max_chunks * (unsigned)p.Hv, kThreads, SMEM_BYTES, stream>>>(
-      p, *static_cast<const CUtensorMap*>(qk_map), *static_cast<const CUtensorMap*>(v_map),
-      *static_cast<const CUtensorMap*>(g_map));
-  return cudaGetLastError();
+  return launch_pdl(intra_kernel, dim3((unsigned)max_chunks * (unsigned)p.Hv), dim3(kThreads),
+                    SMEM_BYTES, stream, p, *static_cast<const CUtensorMap*>(qk_map),
+                    *static_cast<const CUtensorMap*>(v_map), *static_cast<const CUtensorMap*>(g_map));
 }
 
 }  // namespace gdn

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
   __shared__ uint64_t xbar;
   __shared__ float gtot[2];
   __shared__ int ok;
+  pdl_wait_then_release();
   int32_t* hdr = p.work.header();
   const int n_chunks = hdr[kPreChunks];
   const int gidx = blockIdx.x;
@@ -257,8 +258,8 @@ cudaError_t launch_prep(const FwdParams& p, const void* x_map, int max_chunks,
       cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(max_chunks, p.Hk);
-  prep_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, *static_cast<const CUtensorMap*>(x_map));
-  return cudaGetLastError();
+  return launch_pdl(prep_kernel, grid, dim3(kThreads), SMEM_BYTES, stream, p,
+                    *static_cast<const CUtensorMap*>(x_map));
 }
 
 }  // namespace gdn

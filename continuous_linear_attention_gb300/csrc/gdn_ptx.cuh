@@ -64,6 +64,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Programmatic dependent launch: wait until the grid launched before this one
+// on the stream has completed and its writes are visible (returns at once for
+// a grid launched without the programmatic attribute), then allow the next
+// grid to be scheduled while this one runs (its own wait keeps it ordered).
+// Every kernel of a forward call runs this before its first global access,
+// so completion stays transitive along the call's kernels.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Bulk global -> shared copy completing on `bar` (tx bytes).  Addresses
 // 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -22,6 +22,7 @@
 // and the v channels of its v-heads, and the recurrent states of those
 // v-heads, so reading the old state and overwriting it in place is race-free.
 #include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -35,6 +36,7 @@ recurrent_kernel(FwdParams p, bool long_only) {
   constexpr int G = kHeadThreads / CV;      // row groups
   constexpr int NJ = D / G;                 // rows per thread
   static_assert(NJ * G == D, "row split");
+  pdl_wait_then_release();
   const int R = p.Hv / p.Hk;                // v-heads per k-head (1 or 2)
   const WorkArea& wk = p.work;
   const int n_items = wk.header()[long_only ? kNPre : kNItems];
@@ -208,7 +210,9 @@ cudaError_t launch_rec(const FwdParams& p, int max_items, bool long_only, cudaSt
   constexpr int G = kHeadThreads / (D / 4);
   const size_t smem = sizeof(float) * (4 * D + 2 * 2 * G * D + 2 * D + 4 + 4);
   dim3 grid(max_items, p.Hk);
-  recurrent_kernel<D, Act><<<grid, R * kHeadThreads, smem, stream>>>(p, long_only);
+  const cudaError_t e = launch_pdl(recurrent_kernel<D, Act>, grid, dim3(R * kHeadThreads), smem,
+                                   stream, p, long_only);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@
 //   ones sorted longest first (ties by sequence id), their counts and the
 //   total prefill tokens, and resets the persistent-kernel work counter.
 #include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -23,6 +24,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
   __shared__ int s_bad;
   __shared__ int s_n_items, s_n_dec, s_n_pre, s_pre_tokens;
   __shared__ unsigned s_flags;
+  pdl_wait_then_release();  // launched plainly: lets the next kernel launch early
   const int tid = threadIdx.x;
   int32_t* hdr = work.header();
   int32_t* blk_count = work.blk_count();

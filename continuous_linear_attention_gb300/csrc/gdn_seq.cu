@@ -134,6 +134,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
   __shared__ int ok_c;
   __shared__ volatile int mma_stop;
 
+  pdl_wait_then_release();
   const int tid = threadIdx.x;
   const int Hv = p.Hv;
   int32_t* hdr = p.work.header();
@@ -489,8 +490,8 @@ cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cu
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   auto m = [&](int i) { return *static_cast<const CUtensorMap*>(maps[i]); };
-  seq_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p, m(0), m(1), m(2), m(3), m(4));
-  return cudaGetLastError();
+  return launch_pdl(seq_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p, m(0), m(1), m(2),
+                    m(3), m(4));
 }
 
 }  // namespace gdn
