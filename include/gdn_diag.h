@@ -24,6 +24,19 @@
  * K-elements per 32-bit column, the lower K index in the low half) and issues
  * the MMA form that reads A from there; any K of the list above.  a_mn outside
  * 0..2 or b_mn outside 0..1: GDN_ERR_DIMS.
+ *
+ * gdn_diag_umma_issue_timing measures what one tcgen05.mma costs the thread
+ * that issues it: one CTA, one thread issues `reps` MMAs (kind::f16, M = 128,
+ * K = 16, the given N; A from shared memory, or from tensor memory when
+ * a_tmem != 0; zero operands, one fp32 accumulator) with precomputed
+ * descriptors, commits, and waits (bounded) for the commit.  It writes three
+ * unsigned 64-bit values to the device array `out`: SM clock cycles spent
+ * issuing, cycles until the commit was observed, and 1 if it was (0 on
+ * timeout).  N in {16, 32, 64, 128, 256}, a_tmem in {0, 1}, reps a multiple
+ * of 8 in [8, 4096]; `out` 8-byte aligned.  Returns GDN_OK or GDN_ERR_NULL /
+ * GDN_ERR_DIMS / GDN_ERR_ALIGN / GDN_ERR_CUDA.  Stream-ordered, no
+ * synchronisation.  (Reference for the chunked kernels' design: tcgen05,
+ * kind::f16, cta_group::1, from the PTX ISA.)
  */
 #ifndef GDN_DIAG_H_
 #define GDN_DIAG_H_
@@ -36,6 +49,7 @@ int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, i
                        int operand_f16, void* stream);
 int gdn_diag_umma_gemm_ex(const void* A, const void* B, const float* C, float* D, int N, int K,
                           int operand_f16, int a_mn, int b_mn, void* stream);
+int gdn_diag_umma_issue_timing(int N, int a_tmem, int reps, unsigned long long* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -61,3 +61,16 @@ def test_umma_gemm_a_in_tensor_memory_matches_torch(N, K, b_mn, f16):
     torch.cuda.synchronize()
     ref = A.float() @ B.float().T + C
     torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+@pytest.mark.parametrize("a_tmem", [False, True])
+def test_mma_issue_timing_completes(N, a_tmem):
+    """The issue-cost probe runs to its commit and reports a positive issue
+    time no longer than the time to completion."""
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    binding.diag_umma_issue_timing(N, a_tmem, 64, out)
+    torch.cuda.synchronize()
+    issue, total, ok = (int(v) for v in out.cpu())
+    assert ok == 1
+    assert 0 < issue <= total
