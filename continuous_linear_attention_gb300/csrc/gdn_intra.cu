@@ -213,9 +213,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     float xr[32];
     tc::tmem_ld32(tmem + lane + hf * 32, xr);
     tc::tmem_wait_ld();
-    tc::fence_before_sync();
-    __syncthreads();
-    // X is done with the q~ rows: v columns 64..127 come into q~ slot 1
+    // the X product has read the q~ rows: v columns 64..127 come into q~ slot 1
     if (tid == 0) {
       mbar_arrive_expect_tx(&vbar1, BOX);
       tma_load_2d(sm + OFF_QK + KB_STRIDE, &tv, h * D + 64, row0, &vbar1);
@@ -350,13 +348,24 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         *reinterpret_cast<uint4*>(sm + OFF_TT + tc::sw128_offset(CH + i, c8 * 8)) = wtb[q2];
       }
     }
-    // this head's v rows have landed; rows past the sequence -> 0
-    if (tid == 0) flag = (mbar_wait_bounded(&vbar1, 0) && mbar_wait_bounded(&vbar0, 0)) ? 1 : 0;
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    // rows 0..63: -w = -T diag(beta e^G) k~ (k~ rows, MN-major), then wait for
+    // it and for this head's v rows together
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_op(tmem, tc::Opnd{sbase + OFF_TT, 0u, false},
+                 tc::Opnd{sbase + OFF_QK + CH * 128, KB_STRIDE, true}, CH / 16,
+                 tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::commit(&mbar);
+      flag = (mbar_wait_bounded(&vbar1, 0) && mbar_wait_bounded(&vbar0, 0) &&
+              mbar_wait_bounded(&mbar, 1)) ? 1 : 0;
+    }
     __syncthreads();
     ok = flag != 0;
-  }
-  if (ok) {
-    if (n < CH) {
+    if (ok && n < CH) {
+      // v rows past the sequence -> 0 (made visible to the u product below)
       const int nz = CH - n;
       for (int t = tid; t < 2 * nz * 8; t += kThreads) {
         const int q = t & 7, rr = (t >> 3) % nz, bx = (t >> 3) / nz;
@@ -364,18 +373,6 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
             make_uint4(0, 0, 0, 0);
       }
     }
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    // rows 0..63: -w = -T diag(beta e^G) k~   (k~ rows, MN-major)
-    if (tid == 0) {
-      tc::fence_after_sync();
-      tc::mma_op(tmem, tc::Opnd{sbase + OFF_TT, 0u, false},
-                 tc::Opnd{sbase + OFF_QK + CH * 128, KB_STRIDE, true}, CH / 16,
-                 tc::idesc_f16_f32(128, 128, false, true), false);
-      tc::commit(&mbar);
-    }
-    ok = cta_wait(&mbar, 1, &flag);
   }
   // read out rows 0..63 (-w) or 64..127 (u) of the product in TMEM, 64 columns
   auto readout = [&](bool mine, void* base) {
@@ -401,6 +398,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   if (ok) {
     tc::fence_after_sync();
     readout(r128 < CH, p.scr_w);
+    tc::fence_proxy_async_smem();  // the zeroed v rows
     tc::fence_before_sync();
     __syncthreads();
     // rows 64..127: u = T diag(beta) v   (v rows in the q~ slots, MN-major)
