@@ -151,5 +151,12 @@ __device__ __forceinline__ float softplus_f32(float x) {
 // denominator overflows, which is the limit of both functions there.
 __device__ __forceinline__ float sigmoid_f32(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 __device__ __forceinline__ float silu_f32(float y) { return __fdividef(y, 1.f + __expf(-y)); }
+// max(|a|, |b|, |c|) in one instruction (the three-input max of sm_100 and
+// later, on absolute values); a NaN input is skipped, as fmaxf does.
+__device__ __forceinline__ float max_abs3(float a, float b, float c) {
+  float r;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 }  // namespace gdn

@@ -250,7 +250,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
       if (prow) {
         float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], fabsf(val[e]));
+        for (int e = 0; e < 32; e += 2) m4[(e >> 1) & 3] = max_abs3(m4[(e >> 1) & 3], val[e], val[e + 1]);
         amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
         if (i < n) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
@@ -385,7 +385,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
       tc::tmem_wait_ld();
       float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], fabsf(vv[e]));
+      for (int e = 0; e < 32; e += 2) m4[(e >> 1) & 3] = max_abs3(m4[(e >> 1) & 3], vv[e], vv[e + 1]);
       amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
       if (i < n) {
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(base) +

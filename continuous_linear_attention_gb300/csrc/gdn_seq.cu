@@ -356,7 +356,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
           uint32_t w16[16];
 #pragma unroll
           for (int kk = 0; kk < 32; kk += 2) {
-            m4[(kk >> 1) & 3] = fmaxf(m4[(kk >> 1) & 3], fmaxf(fabsf(srow[kk]), fabsf(srow[kk + 1])));
+            m4[(kk >> 1) & 3] = max_abs3(m4[(kk >> 1) & 3], srow[kk], srow[kk + 1]);
             w16[kk >> 1] = tc::pack2(srow[kk], srow[kk + 1], (E*)nullptr);
           }
           amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
@@ -414,7 +414,7 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
         for (int e = 0; e < 32; e += 2) {
           const float a0 = hf * 32 + e < n ? dv[e] : 0.f;
           const float a1 = hf * 32 + e + 1 < n ? dv[e + 1] : 0.f;
-          m4[(e >> 1) & 3] = fmaxf(m4[(e >> 1) & 3], fmaxf(fabsf(a0), fabsf(a1)));
+          m4[(e >> 1) & 3] = max_abs3(m4[(e >> 1) & 3], a0, a1);
           w16[e >> 1] = tc::pack2(a0, a1, (E*)nullptr);
         }
         amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
