@@ -55,3 +55,18 @@ def test_stale_nonfinite_scratch_rows_do_not_leak():
     torch.cuda.synchronize()
     check_against_oracle(small, run=run)
     run.close()
+
+
+@pytest.mark.parametrize("sign", [-1.0, 1.0])
+def test_range_flag_on_a_past_state_outside_fp16(sign):
+    """A past recurrent state of magnitude 1e5 cannot enter the recurrence's
+    fp16 D-product operand, whatever its sign: the range flag goes up."""
+    wl = synth.make_workload("big_state", synth.FULL_DIMS, [130, 70], [1, 0], 8, 25)
+    rec = wl.rec_state.clone()
+    rec[[int(b) for b in wl.ref_blocks].index(int(wl.block_idx[0]))] = sign * 1.0e5
+    wl = dataclasses.replace(wl, rec_state=rec)
+    run = harness.DeviceRun(wl)
+    run.run()
+    torch.cuda.synchronize()
+    assert run.pool.error_flags() & binding.FLAG_RANGE
+    run.close()
