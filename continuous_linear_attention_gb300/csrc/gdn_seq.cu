@@ -312,7 +312,20 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     };
     for (int k = 0;; ++k) {
       const int b = k % kStages;
-      if (!wait_c(&full[b], (k / kStages) & 1)) { dead = true; break; }
+      // ---- the chunk's tiles have landed and the previous chunk's state
+      // update is done (S readable): one wait by thread 0, one barrier
+      if (tid == 0) {
+        bool okw = mbar_wait_bounded(&full[b], (k / kStages) & 1);
+        if (okw && s_busy) okw = mbar_wait_bounded(&mma_s, ph_s);
+        ok_c = okw ? 1 : 0;
+      }
+      cbar();
+      if (!ok_c) { dead = true; break; }
+      if (s_busy) {
+        ph_s ^= 1;
+        s_busy = false;
+        tc::fence_after_sync();
+      }
       const ChunkDesc d = desc[b];
       if (d.flags & 4) break;
       unsigned char* st = sm + b * ST_BYTES;
@@ -325,13 +338,6 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
         for (int t = tid; t < (CH - n) * 16; t += kCompute)
           *reinterpret_cast<uint4*>(st + ST_U + (t & 8 ? BOX : 0) + (n + (t >> 4)) * 128 + (t & 7) * 16) =
               make_uint4(0, 0, 0, 0);
-      }
-      // ---- the previous chunk's state update is done: S readable
-      if (s_busy) {
-        if (!wait_c(&mma_s, ph_s)) { dead = true; break; }
-        ph_s ^= 1;
-        s_busy = false;
-        tc::fence_after_sync();
       }
       // ---- state hand-over: S0 -> fp16 A operand, S <- e^{G_C} S0
       // (this thread: row v, k = 32 hf .. 32 hf + 31, then 64 + the same;
