@@ -58,7 +58,9 @@ constexpr uint32_t OFF_AT = 32768;     // A, overwritten block by block by T: fp
 constexpr uint32_t OFF_TT = OFF_AT;    // then [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
 constexpr uint32_t OFF_GT = 50176;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
 constexpr uint32_t OFF_GH = 51200;     // this head's G [64], contiguous
-constexpr uint32_t SMEM_BYTES = 51456 + 1024;
+constexpr uint32_t OFF_GB = 51456;     // this head's beta [64]
+constexpr uint32_t OFF_GBE = 51712;    // this head's -beta e^G [64]
+constexpr uint32_t SMEM_BYTES = 51968 + 1024;
 constexpr uint32_t TM_COLS = 128;      // X (64 columns), then the 128-column products
 
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
@@ -159,6 +161,8 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
   float* Z = reinterpret_cast<float*>(sm + OFF_Z);
   float* GT = reinterpret_cast<float*>(sm + OFF_GT);
   float* GH = reinterpret_cast<float*>(sm + OFF_GH);
+  float* GB = reinterpret_cast<float*>(sm + OFF_GB);
+  float* GBE = reinterpret_cast<float*>(sm + OFF_GBE);
   const int gc = 2 * r2;  // this head's G column in GT (beta at gc + 1)
 
   if (tid == 0) {
@@ -203,7 +207,12 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
                    tc::idesc_f16_f32(128, 64), false);
       tc::commit(&mbar);
     }
-    if (tid < CH) GH[tid] = GT[tid * 4 + gc];
+    if (tid < CH) {
+      const float g = GT[tid * 4 + gc], bt = GT[tid * 4 + gc + 1];
+      GH[tid] = g;
+      GB[tid] = bt;
+      GBE[tid] = -bt * __expf(g);
+    }
     ok = cta_wait(&mbar, 0, &flag);
   }
   float amax = 0.f;
@@ -328,14 +337,21 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         const int idx = tid + kThreads * q2;
         const int i = idx >> 3, c8 = idx & 7;
         float tb[8], tbe[8];
+        const bool live = (c8 >> 1) <= (i >> 4);  // this 8-column group is in a block at or left of the diagonal
+        const float4 b0 = *reinterpret_cast<const float4*>(GB + c8 * 8);
+        const float4 b1 = *reinterpret_cast<const float4*>(GB + c8 * 8 + 4);
+        const float4 e0 = *reinterpret_cast<const float4*>(GBE + c8 * 8);
+        const float4 e1 = *reinterpret_cast<const float4*>(GBE + c8 * 8 + 4);
+        const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const float ej[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int j = c8 * 8 + e;
-          const float t = (j >> 4) <= (i >> 4) ? AT[i * AP + j] : 0.f;
-          tb[e] = t * GT[j * 4 + gc + 1];
-          tbe[e] = -tb[e] * __expf(GH[j]);
-          amax = fmaxf(amax, fabsf(tb[e]));
+          const float t = live ? AT[i * AP + c8 * 8 + e] : 0.f;
+          tb[e] = t * bj[e];
+          tbe[e] = t * ej[e];
         }
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) amax = max_abs3(amax, tb[e], tb[e + 1]);
         wtb[q2] = pack8(tb);
         wtbe[q2] = pack8(tbe);
       }
