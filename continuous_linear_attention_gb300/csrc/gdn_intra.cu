@@ -45,6 +45,19 @@ constexpr int kThreads = 256;
 constexpr int R = 2;    // v-heads per k-head
 constexpr int AP = 68;  // pitch (floats) of the fp32 A / T rows
 constexpr float kF16Max = 65000.f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// hardware base-2 exponential and logarithm (MUFU; lg2(0) = -inf, ex2(-inf) = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 // shared memory map (offsets from a 1024-byte aligned base).  Once X is done
 // the two q~ slots of the [q~ ; k~] tile are reused: slot 1 takes v columns
@@ -57,7 +70,7 @@ constexpr uint32_t OFF_Z = 0;          // B blocks of the solve fp32 [6][16][20]
 constexpr uint32_t OFF_AT = 32768;     // A, overwritten block by block by T: fp32 [64][AP]
 constexpr uint32_t OFF_TT = OFF_AT;    // then [-T diag(beta e^G) ; T diag(beta)] fp16, 128 rows
 constexpr uint32_t OFF_GT = 50176;     // gates [64][4] fp32: (G, beta) of the k-head's v-heads
-constexpr uint32_t OFF_GH = 51200;     // this head's G [64], contiguous
+constexpr uint32_t OFF_GH = 51200;     // this head's G [64] in log2 units (G log2 e)
 constexpr uint32_t OFF_GB = 51456;     // this head's beta [64]
 constexpr uint32_t OFF_GBE = 51712;    // this head's -beta e^G [64]
 constexpr uint32_t SMEM_BYTES = 51968 + 1024;
@@ -209,7 +222,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     }
     if (tid < CH) {
       const float g = GT[tid * 4 + gc], bt = GT[tid * 4 + gc + 1];
-      GH[tid] = g;
+      GH[tid] = g * kLog2e;
       GB[tid] = bt;
       GBE[tid] = -bt * __expf(g);
     }
@@ -232,8 +245,10 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
       // columns j as two 16-blocks; blocks right of row i's block are zero
       const bool prow = r128 < CH;
       const int i = r128 & 63, ib = i >> 4;
-      const float Gi = GH[i];
-      const float sc = prow ? 1.f : GT[i * 4 + gc + 1];  // beta_i for A
+      // e^{G_i - G_j} beta_i = 2^{(G_i + ln beta_i) log2 e - G_j log2 e}: the
+      // row's exponent offset once (beta_i for A, 1 for P; beta = 0 gives 0)
+      const float Gi2 = GH[i] + (prow ? 0.f : lg2_approx(GT[i * 4 + gc + 1]));
+      const int lim = prow ? i : i - 1;  // last kept column
       float val[32];
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
@@ -248,8 +263,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = 16 * jb + e;
-            const bool keep = prow ? j <= i : j < i;
-            val[blk * 16 + e] = keep ? sc * xr[blk * 16 + e] * __expf(Gi - g16[e]) : 0.f;
+            val[blk * 16 + e] = j <= lim ? xr[blk * 16 + e] * ex2_approx(Gi2 - g16[e]) : 0.f;
           }
         } else {
 #pragma unroll
@@ -344,11 +358,16 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         const float4 e1 = *reinterpret_cast<const float4*>(GBE + c8 * 8 + 4);
         const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
         const float ej[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0;
+        if (live) {
+          t0 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8);
+          t1 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8 + 4);
+        }
+        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float t = live ? AT[i * AP + c8 * 8 + e] : 0.f;
-          tb[e] = t * bj[e];
-          tbe[e] = t * ej[e];
+          tb[e] = tv[e] * bj[e];
+          tbe[e] = tv[e] * ej[e];
         }
 #pragma unroll
         for (int e = 0; e < 8; e += 2) amax = max_abs3(amax, tb[e], tb[e + 1]);
