@@ -115,6 +115,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ void blk_mma3(float (&acc)[4], const float* xp, int px, const float* yp,
                                          int py, int n0) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  float cr[4] = {0.f, 0.f, 0.f, 0.f};  // the cross terms, summed into acc at the end
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int k0 = 8 * ks;
@@ -132,10 +133,12 @@ __device__ __forceinline__ void blk_mma3(float (&acc)[4], const float* xp, int p
       bh[e] = tf32_rna(bf[e]);
       bl[e] = tf32_rna(bf[e] - __uint_as_float(bh[e]));
     }
-    mma_tf32(acc, al, bh);
-    mma_tf32(acc, ah, bl);
+    mma_tf32(cr, al, bh);
+    mma_tf32(cr, ah, bl);
     mma_tf32(acc, ah, bh);
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) acc[e] += cr[e];
 }
 // store a fragment (scaled by s) into a 16 x 16 block at dp (pitch pd), columns n0 ..
 __device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float (&acc)[4], float s) {
@@ -282,10 +285,12 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
           for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(val + g8 * 8);
         }
       } else {
+        // (the solve and the operand tile read only blocks at or left of the diagonal)
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4)
-          *reinterpret_cast<float4*>(AT + i * AP + hf * 32 + j4 * 4) =
-              make_float4(val[j4 * 4], val[j4 * 4 + 1], val[j4 * 4 + 2], val[j4 * 4 + 3]);
+          if (2 * hf + (j4 >> 2) <= ib)
+            *reinterpret_cast<float4*>(AT + i * AP + hf * 32 + j4 * 4) =
+                make_float4(val[j4 * 4], val[j4 * 4 + 1], val[j4 * 4 + 2], val[j4 * 4 + 3]);
       }
     }
     __syncthreads();
@@ -298,9 +303,15 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         const float* Ab = AT + (16 * b) * AP + 16 * b;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
+          float a[16];
+#pragma unroll
+          for (int q = 0; q < (r + 3) / 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(Ab + r * AP + 4 * q);
+            a[4 * q] = t.x; a[4 * q + 1] = t.y; a[4 * q + 2] = t.z; a[4 * q + 3] = t.w;
+          }
           float acc = r == m ? 1.f : 0.f;
 #pragma unroll
-          for (int j = 0; j < r; ++j) acc -= Ab[r * AP + j] * col[j];
+          for (int j = 0; j < r; ++j) acc -= a[j] * col[j];
           col[r] = acc;
         }
       }
