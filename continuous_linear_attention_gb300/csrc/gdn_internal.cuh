@@ -158,5 +158,11 @@ __device__ __forceinline__ float max_abs3(float a, float b, float c) {
   asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// The same, but a NaN input gives NaN.
+__device__ __forceinline__ float max_abs3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 }  // namespace gdn

@@ -93,8 +93,10 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
 
 // ---- 16 x 16 block products of the solve on the warp-level tensor-core path
 // (mma.sync m16n8k8, tf32 inputs, fp32 accumulation), each fp32 operand split
-// into a tf32 head and a tf32 tail with the three significant cross products
-// kept (hh + ht + th), which keeps the products at fp32-level accuracy.
+// into a tf32 head (rounded to nearest) and a tail (the exact remainder, which
+// the tensor core reads truncated to tf32: within 2^-21 of the operand), with
+// the three significant cross products kept (hh + ht + th), which keeps the
+// products at fp32-level accuracy.
 constexpr int ZP = 20;        // pitch (floats) of the B blocks of the solve
 constexpr int ZB = 16 * ZP;   // floats per B block
 
@@ -126,12 +128,12 @@ __device__ __forceinline__ void blk_mma3(float (&acc)[4], const float* xp, int p
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       ah[e] = tf32_rna(af[e]);
-      al[e] = tf32_rna(af[e] - __uint_as_float(ah[e]));
+      al[e] = __float_as_uint(af[e] - __uint_as_float(ah[e]));
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       bh[e] = tf32_rna(bf[e]);
-      bl[e] = tf32_rna(bf[e] - __uint_as_float(bh[e]));
+      bl[e] = __float_as_uint(bf[e] - __uint_as_float(bh[e]));
     }
     mma_tf32(cr, al, bh);
     mma_tf32(cr, ah, bl);

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
   const int tq = tid >> 4, g = tid & 15;
   const int i0 = 4 * tq;
   const float inv_sqrt_d = rsqrtf((float)D);
-  bool range_bad = false;
+  float vmax = 0.f;  // largest |v| written (NaN if any is NaN)
 #pragma unroll 1
   for (int part = 0; part < 2 + R; ++part) {  // q, k, v of head 2kh, v of head 2kh+1
     const int lc = part * D + g * 8;  // local channel: box lc / 64, column lc % 64
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
       if (i < n) {
         if (part >= 2) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) range_bad |= !(fabsf(y[t][e]) <= 65000.f);
+          for (int e = 0; e < 8; e += 2) vmax = max_abs3_nan(vmax, y[t][e], y[t][e + 1]);
         }
         const size_t row = (size_t)(seq0 + c0 + i);
         __half* dst = part < 2 ? qk + (row * Hk + kh) * (2 * D) + part * D + g * 8
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
     }
   }
   // v enters the tensor-core operands in fp16: report values outside its range
-  if (__syncthreads_or(range_bad ? 1 : 0) && tid == 0)
+  if (__syncthreads_or(!(vmax <= 65000.f) ? 1 : 0) && tid == 0)
     atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_RANGE);
 }
 
