@@ -112,35 +112,77 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
+// The A fragment of k-step k0 of X (16 x 16 at xp, pitch px floats; rows and
+// xp 16-byte aligned): X[g][k0+t], X[g+8][k0+t], X[g][k0+t+4], X[g+8][k0+t+4]
+// (g = lane / 4, t = lane % 4) in one ldmatrix.x4 — each 8 x 8 16-bit matrix
+// of it is an 8 x 4 block of fp32, and lane L gives the row address of row
+// L % 8 of block L / 8 — split into its tf32 head and tail.
+__device__ __forceinline__ void a_frag(const float* xp, int px, int k0, uint32_t (&ah)[4],
+                                       uint32_t (&al)[4]) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3;
+  const float* rowp = xp + ((mi & 1) * 8 + (lane & 7)) * px + k0 + (mi >> 1) * 4;
+  uint32_t r[4];
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(rowp)));
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = __uint_as_float(r[e]);
+    ah[e] = tf32_rna(a);
+    al[e] = __float_as_uint(a - __uint_as_float(ah[e]));
+  }
+}
+// The B fragment Y[k0+t][n0+g], Y[k0+t+4][n0+g] (Y at yp, pitch py), split.
+__device__ __forceinline__ void b_frag(const float* yp, int py, int k0, int n0, uint32_t (&bh)[2],
+                                       uint32_t (&bl)[2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float bf[2] = {yp[(k0 + t) * py + n0 + g], yp[(k0 + t + 4) * py + n0 + g]};
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    bh[e] = tf32_rna(bf[e]);
+    bl[e] = __float_as_uint(bf[e] - __uint_as_float(bh[e]));
+  }
+}
 // acc (this warp's fragment of a 16 x 8 block: row g col 2t, 2t+1 and row
 // g+8 col 2t, 2t+1) += X (16 x 16 at xp, pitch px) * Y[:, n0 .. n0+7] (Y at yp, pitch py)
 __device__ __forceinline__ void blk_mma3(float (&acc)[4], const float* xp, int px, const float* yp,
                                          int py, int n0) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   float cr[4] = {0.f, 0.f, 0.f, 0.f};  // the cross terms, summed into acc at the end
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
-    const int k0 = 8 * ks;
-    const float af[4] = {xp[g * px + k0 + t], xp[(g + 8) * px + k0 + t], xp[g * px + k0 + t + 4],
-                         xp[(g + 8) * px + k0 + t + 4]};
-    const float bf[2] = {yp[(k0 + t) * py + n0 + g], yp[(k0 + t + 4) * py + n0 + g]};
     uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      ah[e] = tf32_rna(af[e]);
-      al[e] = __float_as_uint(af[e] - __uint_as_float(ah[e]));
-    }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      bh[e] = tf32_rna(bf[e]);
-      bl[e] = __float_as_uint(bf[e] - __uint_as_float(bh[e]));
-    }
+    a_frag(xp, px, 8 * ks, ah, al);
+    b_frag(yp, py, 8 * ks, n0, bh, bl);
     mma_tf32(cr, al, bh);
     mma_tf32(cr, ah, bl);
     mma_tf32(acc, ah, bh);
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) acc[e] += cr[e];
+}
+// Both 8-column halves of a 16 x 16 block: acc0 / acc1 += X * Y[:, 0..7] / Y[:, 8..15],
+// the A fragments loaded and split once.
+__device__ __forceinline__ void blk_mma3_pair(float (&acc0)[4], float (&acc1)[4], const float* xp,
+                                              int px, const float* yp, int py) {
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t ah[4], al[4], bh[2], bl[2], bh1[2], bl1[2];
+    a_frag(xp, px, 8 * ks, ah, al);
+    b_frag(yp, py, 8 * ks, 0, bh, bl);
+    b_frag(yp, py, 8 * ks, 8, bh1, bl1);
+    mma_tf32(c0, al, bh);
+    mma_tf32(c1, al, bh1);
+    mma_tf32(c0, ah, bl);
+    mma_tf32(c1, ah, bl1);
+    mma_tf32(acc0, ah, bh);
+    mma_tf32(acc1, ah, bh1);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc0[e] += c0[e];
+    acc1[e] += c1[e];
+  }
 }
 // store a fragment (scaled by s) into a 16 x 16 block at dp (pitch pd), columns n0 ..
 __device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float (&acc)[4], float s) {
@@ -329,13 +371,14 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     // Z + (i(i-1)/2 + j) * ZB); one warp per (block, 8-column half)
     {
       const int warp = tid >> 5;
-      for (int task = warp; task < 12; task += kThreads / 32) {
-        const int bi = task >> 1, n0 = (task & 1) * 8;
+      if (warp < 6) {  // one warp per B block, both column halves
+        const int bi = warp;
         const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
         const int j = bi - i * (i - 1) / 2;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        blk_mma3(acc, AT + (16 * i) * AP + 16 * i, AP, AT + (16 * i) * AP + 16 * j, AP, n0);
-        blk_store(Z + bi * ZB, ZP, n0, acc, 1.f);
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        blk_mma3_pair(acc0, acc1, AT + (16 * i) * AP + 16 * i, AP, AT + (16 * i) * AP + 16 * j, AP);
+        blk_store(Z + bi * ZB, ZP, 0, acc0, 1.f);
+        blk_store(Z + bi * ZB, ZP, 8, acc1, 1.f);
       }
       __syncthreads();
       for (int Lv = 1; Lv < 4; ++Lv) {
