@@ -143,25 +143,10 @@ __device__ __forceinline__ void b_frag(const float* yp, int py, int k0, int n0, 
     bl[e] = __float_as_uint(bf[e] - __uint_as_float(bh[e]));
   }
 }
-// acc (this warp's fragment of a 16 x 8 block: row g col 2t, 2t+1 and row
-// g+8 col 2t, 2t+1) += X (16 x 16 at xp, pitch px) * Y[:, n0 .. n0+7] (Y at yp, pitch py)
-__device__ __forceinline__ void blk_mma3(float (&acc)[4], const float* xp, int px, const float* yp,
-                                         int py, int n0) {
-  float cr[4] = {0.f, 0.f, 0.f, 0.f};  // the cross terms, summed into acc at the end
-#pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    uint32_t ah[4], al[4], bh[2], bl[2];
-    a_frag(xp, px, 8 * ks, ah, al);
-    b_frag(yp, py, 8 * ks, n0, bh, bl);
-    mma_tf32(cr, al, bh);
-    mma_tf32(cr, ah, bl);
-    mma_tf32(acc, ah, bh);
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) acc[e] += cr[e];
-}
-// Both 8-column halves of a 16 x 16 block: acc0 / acc1 += X * Y[:, 0..7] / Y[:, 8..15],
-// the A fragments loaded and split once.
+// A 16 x 16 block product on one warp: acc0 / acc1 (this warp's fragments of
+// the two 16 x 8 halves: row g col 2t, 2t+1 and row g+8 col 2t, 2t+1) +=
+// X (16 x 16 at xp, pitch px) * Y[:, 0..7] / Y[:, 8..15] (Y at yp, pitch py),
+// the A fragments loaded and split once for both halves.
 __device__ __forceinline__ void blk_mma3_pair(float (&acc0)[4], float (&acc1)[4], const float* xp,
                                               int px, const float* yp, int py) {
   float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -368,7 +353,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     __syncthreads();
     // off-diagonal blocks: B_ij = T_ii A_ij for every i > j, then level by
     // level T_ij = -sum_{k=j}^{i-1} B_ik T_kj over A_ij (B block (i, j) at
-    // Z + (i(i-1)/2 + j) * ZB); one warp per (block, 8-column half)
+    // Z + (i(i-1)/2 + j) * ZB); one warp per 16 x 16 block
     {
       const int warp = tid >> 5;
       if (warp < 6) {  // one warp per B block, both column halves
@@ -382,12 +367,13 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
       }
       __syncthreads();
       for (int Lv = 1; Lv < 4; ++Lv) {
-        if (warp < 2 * (4 - Lv)) {
-          const int j = warp >> 1, i = j + Lv, n0 = (warp & 1) * 8;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (warp < 4 - Lv) {  // one warp per block of the level, both column halves
+          const int j = warp, i = j + Lv;
+          float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
           for (int k = j; k < i; ++k)
-            blk_mma3(acc, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP, n0);
-          blk_store(AT + (16 * i) * AP + 16 * j, AP, n0, acc, -1.f);
+            blk_mma3_pair(acc0, acc1, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP);
+          blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
+          blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
         }
         if (Lv == 3) tc::fence_proxy_async_smem();  // the B blocks' slot goes back to TMA
         __syncthreads();
