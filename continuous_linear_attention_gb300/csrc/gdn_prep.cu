@@ -212,23 +212,21 @@ __global__ void __launch_bounds__(kThreads, 3) prep_kernel(FwdParams p,
         acc[t][2 * e] = __uint_as_float((uint32_t)acc2[t][e]);
         acc[t][2 * e + 1] = __uint_as_float((uint32_t)(acc2[t][e] >> 32));
       }
-    float y[4][8], ss[4];
+    float y[4][8];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      ss[t] = 0.f;
+    for (int t = 0; t < 4; ++t)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        y[t][e] = silu_f32(acc[t][e]);
-        ss[t] += y[t][e] * y[t][e];
-      }
-    }
+      for (int e = 0; e < 8; ++e) y[t][e] = silu_f32(acc[t][e]);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int i = i0 + t;
-      if (part < 2) {
+      if (part < 2) {  // q and k: L2 norm over the 16 threads of the token
+        float ss = 0.f;
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
-        const float sc = rsqrtf(ss[t] + kL2Eps) * (part == 0 ? inv_sqrt_d : 1.f);
+        for (int e = 0; e < 8; ++e) ss += y[t][e] * y[t][e];
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float sc = rsqrtf(ss + kL2Eps) * (part == 0 ? inv_sqrt_d : 1.f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) y[t][e] *= sc;
       }
