@@ -352,8 +352,10 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
           const int k0 = hh * 64 + hf * 32;
           float srow[32];
           if (d.flags & 1) {
+            // a chain's first chunk: its past state, or zero (the trash block,
+            // which stays zero) without touching memory
 #pragma unroll
-            for (int kk = 0; kk < 32; ++kk) srow[kk] = S_r[(size_t)(k0 + kk) * D + v];
+            for (int kk = 0; kk < 32; ++kk) srow[kk] = d.rblk != 0 ? S_r[(size_t)(k0 + kk) * D + v] : 0.f;
           } else {
             tc::tmem_ld32(tmem + lane + TM_S + k0, srow);
             tc::tmem_wait_ld();
