@@ -353,7 +353,8 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     __syncthreads();
     // off-diagonal blocks: B_ij = T_ii A_ij for every i > j, then level by
     // level T_ij = -sum_{k=j}^{i-1} B_ik T_kj over A_ij (B block (i, j) at
-    // Z + (i(i-1)/2 + j) * ZB); one warp per 16 x 16 block
+    // Z + (i(i-1)/2 + j) * ZB); one warp per 16 x 16 block, the first level
+    // by the warps that made its B blocks
     {
       const int warp = tid >> 5;
       if (warp < 6) {  // one warp per B block, both column halves
@@ -364,9 +365,19 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         blk_mma3_pair(acc0, acc1, AT + (16 * i) * AP + 16 * i, AP, AT + (16 * i) * AP + 16 * j, AP);
         blk_store(Z + bi * ZB, ZP, 0, acc0, 1.f);
         blk_store(Z + bi * ZB, ZP, 8, acc1, 1.f);
+        if (j == i - 1) {
+          // the first level right away, from this warp's own B block:
+          // T_{i,i-1} = -B_{i,i-1} T_{i-1,i-1} over A_{i,i-1} (read only by this warp)
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+          blk_mma3_pair(acc0, acc1, Z + bi * ZB, ZP, AT + (16 * j) * AP + 16 * j, AP);
+          blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
+          blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
+        }
       }
       __syncthreads();
-      for (int Lv = 1; Lv < 4; ++Lv) {
+      for (int Lv = 2; Lv < 4; ++Lv) {
         if (warp < 4 - Lv) {  // one warp per block of the level, both column halves
           const int j = warp, i = j + Lv;
           float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
