@@ -377,18 +377,22 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         }
       }
       __syncthreads();
-      for (int Lv = 2; Lv < 4; ++Lv) {
-        if (warp < 4 - Lv) {  // one warp per block of the level, both column halves
-          const int j = warp, i = j + Lv;
-          float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int k = j; k < i; ++k)
-            blk_mma3_pair(acc0, acc1, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP);
-          blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
-          blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
-        }
-        if (Lv == 3) tc::fence_proxy_async_smem();  // the B blocks' slot goes back to TMA
-        __syncthreads();
+      // the second level on warps 0 and 1; warp 0 goes on to the third, which
+      // needs only its own second-level block and the first level
+      auto level_block = [&](int i, int j) {
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = j; k < i; ++k)
+          blk_mma3_pair(acc0, acc1, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP);
+        blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
+        blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
+      };
+      if (warp < 2) level_block(warp + 2, warp);
+      if (warp == 0) {
+        __syncwarp();
+        level_block(3, 0);
       }
+      tc::fence_proxy_async_smem();  // the B blocks' slot goes back to TMA
+      __syncthreads();
     }
     // the B blocks are consumed: v columns 0..63 come into q~ slot 0
     if (tid == 0) {
