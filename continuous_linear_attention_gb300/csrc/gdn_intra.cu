@@ -303,10 +303,8 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
         }
       }
       if (prow) {
-        float m4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) m4[(e >> 1) & 3] = max_abs3(m4[(e >> 1) & 3], val[e], val[e + 1]);
-        amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        // |P_ij| <= |q~_i| |k~_j| <= d^{-1/2} (the decays are at most 1): P
+        // needs no fp16 range check
         if (i < n) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
                                                 (orow + (size_t)i * Hv) * CH + hf * 32);
@@ -508,7 +506,7 @@ intra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk,
     }
   }
   if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
-  // P, w and u enter the next kernel's tensor-core operands in fp16
+  // w and u (and the operand tile) enter tensor-core operands in fp16
   if (!(amax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
   tc::fence_before_sync();
   __syncthreads();
