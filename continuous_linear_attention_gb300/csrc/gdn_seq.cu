@@ -298,17 +298,27 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
     int next_gate = kBarD1;  // the gate the MMA warp waits at
     float amax = 0.f;
     // outputs i = 32 hf .. 32 hf + 31 of the pending chunk: column 64 + i of
-    // its D^T at this thread's v (a warp writes 64 contiguous bytes per token;
-    // tcgen05.ld is warp-collective, the token predicate guards the stores only)
+    // its D^T at this thread's v (tcgen05.ld and the pair exchange are
+    // warp-collective, the token predicate guards the stores only)
     auto flush = [&]() {
       float o[32];
       tc::tmem_ld32(tmem + lane + TM_D + p_ob * 128 + CH + hf * 32, o);
       tc::tmem_wait_ld();
-      __nv_bfloat16* dst = out + ((size_t)(p_row + hf * 32) * Hv + p_h) * D + v;
-      const size_t step = (size_t)Hv * D;
+      // a lane pair (v, v ^ 1) writes the two v of one token with one 4-byte
+      // store: the even lane the even tokens, the odd lane the odd ones
+      const bool odd = (v & 1) != 0;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(
+          out + ((size_t)(p_row + hf * 32 + (odd ? 1 : 0)) * Hv + p_h) * D + (v & ~1));
+      const size_t step2 = (size_t)Hv * D;  // two rows, in 4-byte words
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (hf * 32 + e < p_n) dst[e * step] = __float2bfloat16_rn(o[e]);
+      for (int m = 0; m < 16; ++m) {
+        const float mine = odd ? o[2 * m + 1] : o[2 * m];
+        const float give = odd ? o[2 * m] : o[2 * m + 1];
+        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const uint32_t w = odd ? tc::pack2(got, mine, (__nv_bfloat16*)nullptr)
+                               : tc::pack2(mine, got, (__nv_bfloat16*)nullptr);
+        if (hf * 32 + 2 * m + (odd ? 1 : 0) < p_n) dst[m * step2] = w;
+      }
     };
     for (int k = 0;; ++k) {
       const int b = k % kStages;
