@@ -18,6 +18,10 @@ Value recipe (sigma is a standard deviation):
 Activation-dtype values are drawn in fp32 and rounded to bf16 (round to
 nearest even) once; every consumer sees the rounded values.
 
+Per-channel gates (the KDA variant): with ``channel_gate`` the gate input
+``a`` has one entry per key channel, [T][Hv][dk] ~ N(0, 1), and ``dt_bias``
+is [Hv][dk] ~ N(0, 0.1) (slow decay: -8 everywhere); nothing else changes.
+
 Pool contents: block 0 is the zeroed trash block; blocks of requests with a
 past hold their state; blocks written by requests without a past are filled
 with NaN (so a kernel that reads them instead of the trash block is caught).
@@ -66,11 +70,11 @@ class Workload:
     num_blocks: int
     # inputs (CPU tensors)
     x: torch.Tensor  # [T][C] act
-    a: torch.Tensor  # [T][Hv] act
+    a: torch.Tensor  # [T][Hv] act ([T][Hv][dk] with per-channel gates)
     b: torch.Tensor  # [T][Hv] act
     conv_w: torch.Tensor  # [C][K] act
     A_log: torch.Tensor  # [Hv] f32
-    dt_bias: torch.Tensor  # [Hv] f32
+    dt_bias: torch.Tensor  # [Hv] f32 ([Hv][dk] with per-channel gates)
     cu_seqlens: torch.Tensor  # [N+1] int32
     block_idx: torch.Tensor  # [N] int32
     has_past: torch.Tensor  # [N] uint8
@@ -88,6 +92,11 @@ class Workload:
     @property
     def N(self) -> int:
         return int(self.block_idx.numel())
+
+    @property
+    def channel_gate(self) -> bool:
+        """One gate per key channel (KDA) rather than one per head."""
+        return self.a.dim() == 3
 
     def seqlens(self) -> List[int]:
         cu = self.cu_seqlens.tolist()
@@ -112,7 +121,7 @@ def _act(arr: np.ndarray, act: str) -> torch.Tensor:
 
 def make_workload(name: str, dims: Dims, seqlens: List[int], has_past: List[int],
                   num_blocks: int, seed: int, block_idx: Optional[List[int]] = None,
-                  slow_decay: bool = False) -> Workload:
+                  slow_decay: bool = False, channel_gate: bool = False) -> Workload:
     """Draw one packed batch and the pool contents it runs against.
 
     ``block_idx`` defaults to a seeded random permutation of blocks
@@ -129,15 +138,16 @@ def make_workload(name: str, dims: Dims, seqlens: List[int], has_past: List[int]
         perm = rng.permutation(np.arange(1, num_blocks))
         block_idx = [int(v) for v in perm[:N]]
     x = _normal(rng, (T, C))
-    a = _normal(rng, (T, dims.Hv))
+    a = _normal(rng, (T, dims.Hv, dims.dk) if channel_gate else (T, dims.Hv))
     b = _normal(rng, (T, dims.Hv))
     conv_w = _normal(rng, (C, dims.K), 0.5)
+    gshape = (dims.Hv, dims.dk) if channel_gate else dims.Hv
     if slow_decay:
         A_log = np.log(rng.uniform(0.01, 0.1, dims.Hv))
-        dt_bias = np.full(dims.Hv, -8.0)
+        dt_bias = np.full(gshape, -8.0)
     else:
         A_log = np.log(rng.uniform(1.0, 16.0, dims.Hv))
-        dt_bias = rng.standard_normal(dims.Hv) * 0.1
+        dt_bias = rng.standard_normal(gshape) * 0.1
 
     ref = sorted({0} | {int(v) for v in block_idx if 0 <= int(v) < num_blocks})
     pos = {blk: i for i, blk in enumerate(ref)}

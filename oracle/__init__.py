@@ -8,14 +8,18 @@ the layer's arithmetic.
 
 Contents:
   * ``forward``      -- the plain token-by-token fp64 forward (C, gdn_oracle.c),
-                        on the referenced blocks of a workload;
+                        on the referenced blocks of a workload; workloads with
+                        one gate per key channel run the KDA rule;
+  * ``gdn_rule_head`` / ``kda_rule_head`` -- the two rules on one chain;
   * ``data_errors``  -- which sequences the rules for bad input skip;
   * ``pool_layout``  -- the state-pool byte layout as the boundary states it
                         (conv sub-state at 0, recurrent sub-state at the next
                         128-byte boundary, block stride rounded up);
   * ``read_pool_states`` -- decode a pool byte image with that layout;
-  * ``product_form_final_state`` / ``chunked_wy_forward`` -- two independent
-    restatements of the recurrence used only to pin the token loop (numpy).
+  * ``product_form_final_state`` / ``chunked_wy_forward`` and their KDA
+    counterparts ``kda_product_form_final_state`` / ``kda_chunked_forward``
+    -- independent restatements of the recurrences used only to pin the token
+    loops (numpy).
 
 Every function cites the passage it follows; the readings taken where the
 sources are silent are listed in the module docstring of gdn_oracle.c.
@@ -64,11 +68,16 @@ def _load():
             I = ctypes.c_int
             lib.oracle_gdn_forward.restype = I
             lib.oracle_gdn_forward.argtypes = [I] * 8 + [P] * 13 + [I]
+            lib.oracle_kda_forward.restype = I
+            lib.oracle_kda_forward.argtypes = [I] * 8 + [P] * 13 + [I]
             lib.oracle_conv_silu_seq.restype = None
             lib.oracle_conv_silu_seq.argtypes = [I, I, I, P, P, P, I, I, P]
             lib.oracle_gdn_rule_head.restype = None
             lib.oracle_gdn_rule_head.argtypes = [I, I, I, P, P, P, P, P,
                                                  ctypes.c_double, ctypes.c_double, P, P]
+            lib.oracle_kda_rule_head.restype = None
+            lib.oracle_kda_rule_head.argtypes = [I, I, I, P, P, P, P, P,
+                                                 ctypes.c_double, P, P, P]
             _lib = lib
     return _lib
 
@@ -115,6 +124,23 @@ def gdn_rule_head(q, k, v, a, b, A_log, dt_bias, S0):
     o = np.zeros((L, dv))
     _load().oracle_gdn_rule_head(L, dk, dv, _p(q), _p(k), _p(v), _p(a), _p(b),
                                  float(A_log), float(dt_bias), _p(S), _p(o))
+    return o, S
+
+
+def kda_rule_head(q, k, v, a, b, A_log, dt_bias, S0):
+    """KDA rule over one chain, token by token (Kimi Linear, the KDA
+    recurrence: the gated delta rule with one decay per key channel).
+    q,k: [L][dk] raw, v: [L][dv], a: [L][dk], b: [L], dt_bias: [dk],
+    S0: [dv][dk] -> (o [L][dv], S_L)."""
+    q, k, v, a, b, dt_bias = (_f64(t) for t in (q, k, v, a, b, dt_bias))
+    S = _f64(S0).copy()
+    L, dk = q.shape
+    dv = v.shape[1]
+    if a.shape != (L, dk) or dt_bias.shape != (dk,):
+        raise ValueError("per-channel gates: a [L][dk], dt_bias [dk]")
+    o = np.zeros((L, dv))
+    _load().oracle_kda_rule_head(L, dk, dv, _p(q), _p(k), _p(v), _p(a), _p(b),
+                                 float(A_log), _p(dt_bias), _p(S), _p(o))
     return o, S
 
 
@@ -173,7 +199,8 @@ def data_errors(cu_seqlens, block_idx, num_blocks, T):
 
 def forward(wl, nthreads: int = 0, out_init=None):
     """Run the packed forward of workload ``wl`` (see the generator module) in
-    fp64.  Returns a dict with
+    fp64, with the KDA rule when ``wl`` has one gate per key channel.
+    Returns a dict with
       out        [T][Hv][dv] fp64 (rows of skipped sequences: ``out_init`` or NaN)
       conv_state [R][K-1][C] fp64 and rec_state [R][Hv][dk][dv] fp64 (k-major,
                  like the pool), for the workload's referenced blocks after the
@@ -203,10 +230,13 @@ def forward(wl, nthreads: int = 0, out_init=None):
         out = np.full((T, d.Hv, d.dv), np.nan)
     else:
         out = _f64(out_init).reshape(T, d.Hv, d.dv).copy()
+    if wl.channel_gate and (a.shape != (T, d.Hv, d.dk) or dt_bias.shape != (d.Hv, d.dk)):
+        raise ValueError("per-channel gates: a [T][Hv][dk], dt_bias [Hv][dk]")
+    run = _load().oracle_kda_forward if wl.channel_gate else _load().oracle_gdn_forward
     if flags & ERR_SEQLENS:
         used = 0
     else:
-        used = _load().oracle_gdn_forward(
+        used = run(
             T, N, d.Hk, d.Hv, d.dk, d.dv, d.K, len(ref),
             _p(x), _p(a), _p(b), _p(cu), _p(blk_local), _p(has_past), _p(skip_arr),
             _p(w), _p(A_log), _p(dt_bias), _p(conv), _p(rec), _p(out), int(nthreads))
@@ -321,5 +351,64 @@ def chunked_wy_forward(q, k, v, g, beta, S0, chunk=64):
         M = np.where(incl, np.exp(np.where(incl, diff, 0.0)), 0.0)
         O = np.exp(G)[:, None] * (Q @ S.T) + ((Q @ Kc.T) * M) @ U
         S = np.exp(G[-1]) * S + U.T @ (np.exp(G[-1] - G)[:, None] * Kc)
+        outs.append(O)
+    return np.concatenate(outs, axis=0), S
+
+
+def kda_product_form_final_state(k, v, g, beta, S0):
+    """Closed product form of the KDA rule.  The token update is
+    S_t = S_{t-1} D_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T with
+    D_t = Diag(e^{g_t}) (one decay per key channel), so with
+    M_t = D_t (I - beta_t k_t k_t^T)
+        S_L = S_0 M_1 ... M_L + sum_t beta_t v_t k_t^T M_{t+1} ... M_L.
+    k: [L][dk] (normalised), v: [L][dv], g: [L][dk], beta: [L], S0: [dv][dk]."""
+    L, dk = k.shape
+    I = np.eye(dk)
+    Ms = [np.diag(np.exp(g[t])) @ (I - beta[t] * np.outer(k[t], k[t])) for t in range(L)]
+    suffix = [None] * (L + 1)
+    suffix[L] = I
+    for t in range(L - 1, -1, -1):
+        suffix[t] = Ms[t] @ suffix[t + 1]
+    S = S0 @ suffix[0]
+    for t in range(L):
+        S = S + beta[t] * np.outer(v[t], k[t]) @ suffix[t + 1]
+    return S
+
+
+def kda_chunked_forward(q, k, v, g, beta, S0, chunk=64):
+    """Chunked (WY / UT-transform) evaluation of the KDA rule, fp64.
+
+    With Gam_i = sum_{s<=i} g_s (a vector per token, cumulative within the
+    chunk), the state after token i of a chunk is
+        S_i = S_0 Diag(e^{Gam_i}) + sum_{j<=i} u_j (k_j o e^{Gam_i - Gam_j})^T,
+    and the update vectors solve
+        (I + A) U = diag(beta) V - diag(beta) (K o e^{Gam}) S_0^T,
+        A_ij = beta_i sum_c k_ic k_jc e^{Gam_ic - Gam_jc}   (j < i);
+    then
+        O = (Q o e^{Gam}) S_0^T + P U,  P_ij = sum_c q_ic k_jc e^{Gam_ic - Gam_jc} (j <= i),
+        S_C = S_0 Diag(e^{Gam_C}) + U^T (K o e^{Gam_C - Gam}).
+    Every pairwise factor is formed directly, so only non-positive exponents
+    appear.  q, k normalised [L][dk]; v [L][dv]; g [L][dk]; beta [L];
+    S0 [dv][dk].  Returns (O [L][dv], S_L)."""
+    L = q.shape[0]
+    S = S0.copy()
+    outs = []
+    for c0 in range(0, L, chunk):
+        Q, Kc, V = q[c0:c0 + chunk], k[c0:c0 + chunk], v[c0:c0 + chunk]
+        gc, bc = g[c0:c0 + chunk], beta[c0:c0 + chunk]
+        n = Q.shape[0]
+        Gam = np.cumsum(gc, axis=0)  # [n][dk]
+        A = np.zeros((n, n))
+        P = np.zeros((n, n))
+        for i in range(n):
+            for j in range(i + 1):
+                f = np.exp(Gam[i] - Gam[j])
+                P[i, j] = np.sum(Q[i] * Kc[j] * f)
+                if j < i:
+                    A[i, j] = bc[i] * np.sum(Kc[i] * Kc[j] * f)
+        Tm = np.linalg.inv(np.eye(n) + A)
+        U = Tm @ (bc[:, None] * V) - Tm @ (bc[:, None] * (Kc * np.exp(Gam))) @ S.T
+        O = (Q * np.exp(Gam)) @ S.T + P @ U
+        S = S * np.exp(Gam[-1])[None, :] + U.T @ (Kc * np.exp(Gam[-1] - Gam))
         outs.append(O)
     return np.concatenate(outs, axis=0), S

@@ -20,6 +20,18 @@
  *    with g_t = -exp(A_log) * softplus(a_t + dt_bias), beta_t = sigmoid(b_t),
  *    q and k L2-normalised and q scaled by 1/sqrt(d_k).
  *
+ * A second rule, Kimi Delta Attention (KDA; the decay of the families the
+ * "Continuous batching: model support tracker" page lists as Kimi Linear and
+ * GLM5-next), keeps the same per-request states and the same convolution and
+ * differs only in the gate: one decay per key channel instead of one per
+ * head (Kimi Team, "Kimi Linear: An Expressive, Efficient Hybrid Linear
+ * Attention Architecture", 2025, the KDA recurrence).  In the S[v][k]
+ * orientation used here:
+ *        S_t = S_{t-1} Diag(alpha_t) + beta_t (v_t - S_{t-1} Diag(alpha_t) k_t) k_t^T,
+ *        o_t = S_t q_t,
+ *    with alpha_t = exp(g_t), g_t[c] = -exp(A_log) * softplus(a_t[c] + dt_bias[c])
+ *    for every key channel c (a_t and dt_bias have one entry per key channel).
+ *
  * Everything is token by token in the order the definition states; there is
  * no chunking, blocking or reordering.  All arrays are fp64 and logical (no
  * pool byte layout here: the Python side converts).
@@ -144,6 +156,56 @@ void oracle_gdn_rule_head(int L, int dk, int dv, const double* q, const double* 
 }
 
 /*
+ * KDA rule for ONE (sequence, v-head) chain: the gated delta rule with one
+ * decay per key channel.  Arguments as oracle_gdn_rule_head, except
+ *   a      : [L][dk] gate pre-activations, one per key channel
+ *   dt_bias: [dk]
+ * The decay scales column c (key channel c) of S[v][k] by alpha_t[c] before
+ * the delta step; the delta step reads the decayed state.
+ */
+void oracle_kda_rule_head(int L, int dk, int dv, const double* q, const double* k, const double* v,
+                          const double* a, const double* b, double A_log, const double* dt_bias,
+                          double* S, double* o) {
+  double* qn = (double*)malloc(sizeof(double) * dk);
+  double* kn = (double*)malloc(sizeof(double) * dk);
+  double* alpha = (double*)malloc(sizeof(double) * dk);
+  double* Sk = (double*)malloc(sizeof(double) * dv);
+  for (int t = 0; t < L; ++t) {
+    const double* qt = q + (size_t)t * dk;
+    const double* kt = k + (size_t)t * dk;
+    const double* vt = v + (size_t)t * dv;
+    double sq = 0.0, sk = 0.0;
+    for (int i = 0; i < dk; ++i) { sq += qt[i] * qt[i]; sk += kt[i] * kt[i]; }
+    double qs = 1.0 / sqrt(sq + ORACLE_L2_EPS) / sqrt((double)dk);
+    double ks = 1.0 / sqrt(sk + ORACLE_L2_EPS);
+    for (int i = 0; i < dk; ++i) { qn[i] = qt[i] * qs; kn[i] = kt[i] * ks; }
+    for (int i = 0; i < dk; ++i)
+      alpha[i] = exp(-exp(A_log) * softplus_f64(a[(size_t)t * dk + i] + dt_bias[i]));
+    double beta = sigmoid_f64(b[t]);
+    /* S <- S Diag(alpha): column i (key channel i) decays by alpha_i */
+    for (int r = 0; r < dv; ++r)
+      for (int i = 0; i < dk; ++i) S[(size_t)r * dk + i] *= alpha[i];
+    /* S <- S + beta (v - S k) k^T */
+    for (int r = 0; r < dv; ++r) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)r * dk + i] * kn[i];
+      Sk[r] = acc;
+    }
+    for (int r = 0; r < dv; ++r) {
+      double u = beta * (vt[r] - Sk[r]);
+      for (int i = 0; i < dk; ++i) S[(size_t)r * dk + i] += u * kn[i];
+    }
+    /* o = S q */
+    for (int r = 0; r < dv; ++r) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)r * dk + i] * qn[i];
+      o[(size_t)t * dv + r] = acc;
+    }
+  }
+  free(qn); free(kn); free(alpha); free(Sk);
+}
+
+/*
  * Whole packed forward, on logical fp64 arrays.
  *   x        : [T][C]  with C = 2*Hk*dk + Hv*dv
  *   a, b     : [T][Hv]
@@ -158,12 +220,16 @@ void oracle_gdn_rule_head(int L, int dk, int dv, const double* q, const double* 
  *   skip     : [N] or NULL: nonzero entries are skipped like padding (data
  *              errors found by the caller's validation)
  * Returns the number of OpenMP threads used.
+ *
+ * gate_width is 1 for the gated delta rule (a [T][Hv], dt_bias [Hv]) and dk
+ * for KDA (a [T][Hv][dk], dt_bias [Hv][dk]); nothing else differs.
  */
-int oracle_gdn_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int num_blocks,
-                       const double* x, const double* a, const double* b, const int32_t* cu,
-                       const int32_t* blk, const uint8_t* has_past, const uint8_t* skip,
-                       const double* w, const double* A_log, const double* dt_bias,
-                       double* conv_st, double* rec_st, double* out, int nthreads) {
+static int packed_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int num_blocks,
+                          const double* x, const double* a, const double* b, const int32_t* cu,
+                          const int32_t* blk, const uint8_t* has_past, const uint8_t* skip,
+                          const double* w, const double* A_log, const double* dt_bias,
+                          double* conv_st, double* rec_st, double* out, int nthreads,
+                          int gate_width) {
   (void)T;
   const int C = 2 * Hk * dk + Hv * dv;
   const int W = K - 1;
@@ -198,7 +264,7 @@ int oracle_gdn_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int 
     double* qy = (double*)malloc(sizeof(double) * (size_t)L * dk);
     double* ky = (double*)malloc(sizeof(double) * (size_t)L * dk);
     double* vy = (double*)malloc(sizeof(double) * (size_t)L * dv);
-    double* at = (double*)malloc(sizeof(double) * (size_t)L);
+    double* at = (double*)malloc(sizeof(double) * (size_t)L * gate_width);
     double* bt = (double*)malloc(sizeof(double) * (size_t)L);
     double* o = (double*)malloc(sizeof(double) * (size_t)L * dv);
     double* S = (double*)malloc(sizeof(double) * rec_head);
@@ -206,11 +272,15 @@ int oracle_gdn_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int 
     oracle_conv_silu_seq(L, C, K, xs, tail, w, Hk * dk + kh * dk, dk, ky);
     oracle_conv_silu_seq(L, C, K, xs, tail, w, 2 * Hk * dk + h * dv, dv, vy);
     for (int t = 0; t < L; ++t) {
-      at[t] = a[(size_t)(cu[s] + t) * Hv + h];
+      for (int c = 0; c < gate_width; ++c)
+        at[(size_t)t * gate_width + c] = a[((size_t)(cu[s] + t) * Hv + h) * gate_width + c];
       bt[t] = b[(size_t)(cu[s] + t) * Hv + h];
     }
     memcpy(S, rec_st + (size_t)src * rec_blk + (size_t)h * rec_head, sizeof(double) * rec_head);
-    oracle_gdn_rule_head(L, dk, dv, qy, ky, vy, at, bt, A_log[h], dt_bias[h], S, o);
+    if (gate_width == 1)
+      oracle_gdn_rule_head(L, dk, dv, qy, ky, vy, at, bt, A_log[h], dt_bias[h], S, o);
+    else
+      oracle_kda_rule_head(L, dk, dv, qy, ky, vy, at, bt, A_log[h], dt_bias + (size_t)h * dk, S, o);
     for (int t = 0; t < L; ++t)
       memcpy(out + ((size_t)(cu[s] + t) * Hv + h) * dv, o + (size_t)t * dv, sizeof(double) * dv);
     Sfin[pair] = S;
@@ -242,4 +312,23 @@ int oracle_gdn_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int 
   free(tails);
   free(Sfin);
   return used;
+}
+
+int oracle_gdn_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int num_blocks,
+                       const double* x, const double* a, const double* b, const int32_t* cu,
+                       const int32_t* blk, const uint8_t* has_past, const uint8_t* skip,
+                       const double* w, const double* A_log, const double* dt_bias,
+                       double* conv_st, double* rec_st, double* out, int nthreads) {
+  return packed_forward(T, N, Hk, Hv, dk, dv, K, num_blocks, x, a, b, cu, blk, has_past, skip, w,
+                        A_log, dt_bias, conv_st, rec_st, out, nthreads, 1);
+}
+
+/* The same packed forward with the KDA rule: a [T][Hv][dk], dt_bias [Hv][dk]. */
+int oracle_kda_forward(int T, int N, int Hk, int Hv, int dk, int dv, int K, int num_blocks,
+                       const double* x, const double* a, const double* b, const int32_t* cu,
+                       const int32_t* blk, const uint8_t* has_past, const uint8_t* skip,
+                       const double* w, const double* A_log, const double* dt_bias,
+                       double* conv_st, double* rec_st, double* out, int nthreads) {
+  return packed_forward(T, N, Hk, Hv, dk, dv, K, num_blocks, x, a, b, cu, blk, has_past, skip, w,
+                        A_log, dt_bias, conv_st, rec_st, out, nthreads, dk);
 }
