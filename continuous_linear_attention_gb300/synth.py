@@ -285,3 +285,111 @@ def standard_cases():
         "mixed": mixed_batch,
         "long": long_context,
     }
+
+
+# --------------------------------------------------------------------------
+# Mamba2 mixer workloads (conv over x | B | C, then the selective scan).
+
+@dataclasses.dataclass
+class SsdDims:
+    H: int   # heads
+    P: int   # head dim
+    N: int   # state size
+    G: int   # groups sharing B and C
+    K: int   # conv width
+    act: str
+
+    @property
+    def C(self) -> int:
+        """Conv channels: x | B | C."""
+        return self.H * self.P + 2 * self.G * self.N
+
+
+@dataclasses.dataclass
+class SsdWorkload:
+    name: str
+    dims: SsdDims
+    num_blocks: int
+    xbc: torch.Tensor  # [T][C] act
+    dt: torch.Tensor  # [T][H] act
+    conv_w: torch.Tensor  # [C][K] act
+    A_log: torch.Tensor  # [H] f32
+    dt_bias: torch.Tensor  # [H] f32
+    D: torch.Tensor  # [H] f32
+    cu_seqlens: torch.Tensor  # [N+1] int32
+    block_idx: torch.Tensor  # [N] int32
+    has_past: torch.Tensor  # [N] uint8
+    ref_blocks: torch.Tensor  # [R] int64, ref_blocks[0] == 0
+    conv_state: torch.Tensor  # [R][K-1][C] act
+    ssm_state: torch.Tensor  # [R][H][P][N] f32
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def N(self) -> int:
+        return int(self.block_idx.numel())
+
+
+def make_ssd_workload(name: str, dims: SsdDims, seqlens: List[int], has_past: List[int],
+                      num_blocks: int, seed: int, block_idx: Optional[List[int]] = None,
+                      slow_decay: bool = False) -> SsdWorkload:
+    """One packed batch for a Mamba2 mixer and the pool contents it runs
+    against.  Recipe: xbc, dt ~ N(0, 1); conv weight ~ N(0, 0.5);
+    A_log = log U(1, 16); dt_bias = softplus^-1 of log-uniform [1e-3, 1e-1]
+    (the usual Mamba2 time-step range); D ~ N(1, 0.1); past conv states
+    ~ N(0, 1), past SSM states ~ N(0, 0.02); blocks written by requests with
+    no past hold NaN.  Slow decay: A_log = log U(0.01, 0.1) and dt = -4
+    (small, slowly forgetting time steps)."""
+    rng = _rng(seed)
+    N = len(seqlens)
+    T = int(sum(seqlens))
+    C = dims.C
+    if block_idx is None:
+        if N > num_blocks - 1:
+            raise ValueError("more sequences than non-trash blocks")
+        perm = rng.permutation(np.arange(1, num_blocks))
+        block_idx = [int(v) for v in perm[:N]]
+    xbc = _normal(rng, (T, C))
+    dt = _normal(rng, (T, dims.H))
+    conv_w = _normal(rng, (C, dims.K), 0.5)
+    step = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), dims.H))
+    dt_bias = step + np.log(-np.expm1(-step))  # softplus(dt_bias) = step
+    if slow_decay:
+        A_log = np.log(rng.uniform(0.01, 0.1, dims.H))
+        dt[:] = -4.0
+    else:
+        A_log = np.log(rng.uniform(1.0, 16.0, dims.H))
+    D = 1.0 + 0.1 * rng.standard_normal(dims.H)
+    ref = sorted({0} | {int(v) for v in block_idx if 0 <= int(v) < num_blocks})
+    pos = {blk: i for i, blk in enumerate(ref)}
+    R = len(ref)
+    conv_state = np.zeros((R, dims.K - 1, C), dtype=np.float32)
+    ssm_state = np.zeros((R, dims.H, dims.P, dims.N), dtype=np.float32)
+    for s in range(N):
+        blk = int(block_idx[s])
+        if blk <= 0 or blk >= num_blocks:
+            continue
+        i = pos[blk]
+        if has_past[s]:
+            conv_state[i] = _normal(rng, (dims.K - 1, C))
+            ssm_state[i] = _normal(rng, (dims.H, dims.P, dims.N), 0.02)
+        else:
+            conv_state[i] = np.nan
+            ssm_state[i] = np.nan
+    cu = np.zeros(N + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(seqlens, dtype=np.int64))
+    return SsdWorkload(
+        name=name, dims=dims, num_blocks=num_blocks,
+        xbc=_act(xbc, dims.act), dt=_act(dt, dims.act), conv_w=_act(conv_w, dims.act),
+        A_log=torch.from_numpy(A_log.astype(np.float32)),
+        dt_bias=torch.from_numpy(dt_bias.astype(np.float32)),
+        D=torch.from_numpy(D.astype(np.float32)),
+        cu_seqlens=torch.from_numpy(cu),
+        block_idx=torch.tensor(block_idx, dtype=torch.int32),
+        has_past=torch.tensor([1 if p else 0 for p in has_past], dtype=torch.uint8),
+        ref_blocks=torch.tensor(ref, dtype=torch.int64),
+        conv_state=_act(conv_state, dims.act),
+        ssm_state=torch.from_numpy(ssm_state),
+    )

@@ -16,10 +16,13 @@ Contents:
                         (conv sub-state at 0, recurrent sub-state at the next
                         128-byte boundary, block stride rounded up);
   * ``read_pool_states`` -- decode a pool byte image with that layout;
+  * ``ssd_scan_head`` / ``ssd_forward`` -- the Mamba2 mixer's selective scan
+                        (C, ssd_oracle.c) on one chain and on a packed batch;
   * ``product_form_final_state`` / ``chunked_wy_forward`` and their KDA
     counterparts ``kda_product_form_final_state`` / ``kda_chunked_forward``
     -- independent restatements of the recurrences used only to pin the token
-    loops (numpy).
+    loops (numpy); ``ssd_quadratic_form`` / ``ssd_chunked_forward`` the same
+    for the scan.
 
 Every function cites the passage it follows; the readings taken where the
 sources are silent are listed in the module docstring of gdn_oracle.c.
@@ -36,7 +39,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libgdn_oracle.so")
-_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_SRCS = [os.path.join(_HERE, "gdn_oracle.c"), os.path.join(_HERE, "ssd_oracle.c")]
 _lock = threading.Lock()
 _lib = None
 
@@ -44,13 +47,13 @@ L2_EPS = 1e-6
 
 
 def build(force: bool = False) -> str:
-    """Compile gdn_oracle.c with gcc (OpenMP if the compiler has it)."""
+    """Compile the oracle's C sources with gcc (OpenMP if the compiler has it)."""
     os.makedirs(_BUILD, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    base = ["gcc", "-O2", "-shared", "-fPIC", "-std=c11", "-o", tmp] + _SRCS + ["-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
@@ -74,6 +77,11 @@ def _load():
             lib.oracle_conv_silu_seq.argtypes = [I, I, I, P, P, P, I, I, P]
             lib.oracle_gdn_rule_head.restype = None
             lib.oracle_gdn_rule_head.argtypes = [I, I, I, P, P, P, P, P,
+                                                 ctypes.c_double, ctypes.c_double, P, P]
+            lib.oracle_ssd_forward.restype = I
+            lib.oracle_ssd_forward.argtypes = [I] * 8 + [P] * 13 + [I]
+            lib.oracle_ssd_scan_head.restype = None
+            lib.oracle_ssd_scan_head.argtypes = [I, I, I, P, P, P, P, ctypes.c_double,
                                                  ctypes.c_double, ctypes.c_double, P, P]
             lib.oracle_kda_rule_head.restype = None
             lib.oracle_kda_rule_head.argtypes = [I, I, I, P, P, P, P, P,
@@ -142,6 +150,20 @@ def kda_rule_head(q, k, v, a, b, A_log, dt_bias, S0):
     _load().oracle_kda_rule_head(L, dk, dv, _p(q), _p(k), _p(v), _p(a), _p(b),
                                  float(A_log), _p(dt_bias), _p(S), _p(o))
     return o, S
+
+
+def ssd_scan_head(x, B, C, dt, A_log, dt_bias, Dskip, h0):
+    """Mamba2 selective scan over one chain, token by token (Transformers are
+    SSMs, the SSD recurrence; see ssd_oracle.c).  x: [L][P], B, C: [L][N],
+    dt: [L] raw, h0: [P][N] -> (y [L][P], h_L)."""
+    x, B, C, dt = (_f64(t) for t in (x, B, C, dt))
+    h = _f64(h0).copy()
+    L, P = x.shape
+    N = B.shape[1]
+    y = np.zeros((L, P))
+    _load().oracle_ssd_scan_head(L, P, N, _p(x), _p(B), _p(C), _p(dt), float(A_log),
+                                 float(dt_bias), float(Dskip), _p(h), _p(y))
+    return y, h
 
 
 # ---------------------------------------------------------------------------
@@ -248,6 +270,39 @@ def forward(wl, nthreads: int = 0, out_init=None):
         "flags": flags,
         "threads": used,
     }
+
+
+def ssd_forward(wl, nthreads: int = 0, out_init=None):
+    """Packed forward of a Mamba2 mixer workload (``synth.SsdWorkload``) in
+    fp64, with the same skip rules as ``forward``.  Returns a dict with
+    ``y`` [T][H][P], ``conv_state`` [R][K-1][C], ``ssm_state`` [R][H][P][N]
+    (the referenced blocks after the call), ``skip``, ``flags``, ``threads``."""
+    d = wl.dims
+    T, Nseq = wl.T, wl.N
+    ref = [int(v) for v in wl.ref_blocks]
+    pos = {b: i for i, b in enumerate(ref)}
+    skip, flags = data_errors(wl.cu_seqlens, wl.block_idx, wl.num_blocks, T)
+    blk_local = np.array([pos.get(int(b), -1) if not skip[s] else -1
+                          for s, b in enumerate(wl.block_idx.tolist())], dtype=np.int32)
+    xbc, dt, w = _f64(wl.xbc), _f64(wl.dt), _f64(wl.conv_w)
+    A_log, dt_bias, Dskip = _f64(wl.A_log), _f64(wl.dt_bias), _f64(wl.D)
+    cu = np.ascontiguousarray(wl.cu_seqlens.numpy(), dtype=np.int32)
+    has_past = np.ascontiguousarray(wl.has_past.numpy(), dtype=np.uint8)
+    skip_arr = np.array(skip, dtype=np.uint8)
+    conv = _f64(wl.conv_state)
+    ssm = _f64(wl.ssm_state).copy()
+    if out_init is None:
+        y = np.full((T, d.H, d.P), np.nan)
+    else:
+        y = _f64(out_init).reshape(T, d.H, d.P).copy()
+    used = 0
+    if not flags & ERR_SEQLENS:
+        used = _load().oracle_ssd_forward(
+            T, Nseq, d.H, d.P, d.N, d.G, d.K, len(ref), _p(xbc), _p(dt), _p(cu), _p(blk_local),
+            _p(has_past), _p(skip_arr), _p(w), _p(A_log), _p(dt_bias), _p(Dskip), _p(conv),
+            _p(ssm), _p(y), int(nthreads))
+    return {"y": y, "conv_state": conv, "ssm_state": ssm, "skip": skip, "flags": flags,
+            "threads": used}
 
 
 # ---------------------------------------------------------------------------
@@ -412,3 +467,37 @@ def kda_chunked_forward(q, k, v, g, beta, S0, chunk=64):
         S = S * np.exp(Gam[-1])[None, :] + U.T @ (Kc * np.exp(Gam[-1] - Gam))
         outs.append(O)
     return np.concatenate(outs, axis=0), S
+
+
+def ssd_quadratic_form(x, B, C, dt, a_log_decay, Dskip, h0):
+    """The scan written as one matrix product (the "attention" side of state
+    space duality).  With per-token time steps dt_t (after softplus), decays
+    log a_t = a_log_decay[t] and the segment sums
+    Lam_ts = sum_{r=s+1..t} log a_r (s <= t):
+        y_t = sum_{s<=t} e^{Lam_ts} (C_t . B_s) dt_s x_s
+              + e^{sum_{r<=t} log a_r} h_0 C_t + D x_t,
+        h_L = e^{sum_r log a_r} h_0 + sum_s e^{Lam_Ls} dt_s x_s B_s^T.
+    x: [L][P], B, C: [L][N], dt, a_log_decay: [L], h0: [P][N]."""
+    L = x.shape[0]
+    cum = np.cumsum(a_log_decay)
+    seg = cum[:, None] - cum[None, :]  # Lam_ts for s <= t
+    causal = np.tril(np.ones((L, L), dtype=bool))
+    M = np.where(causal, np.exp(np.where(causal, seg, 0.0)), 0.0) * (C @ B.T)
+    y = M @ (dt[:, None] * x) + np.exp(cum)[:, None] * (C @ h0.T) + Dskip * x
+    h = np.exp(cum[-1]) * h0 + (np.exp(cum[-1] - cum)[:, None] * dt[:, None] * x).T @ B
+    return y, h
+
+
+def ssd_chunked_forward(x, B, C, dt, a_log_decay, Dskip, h0, chunk=64):
+    """Chunked evaluation of the scan: inside a chunk the quadratic form, and
+    between chunks only the state is passed,
+        h_end = e^{A_c} h_start + sum_s e^{A_c - A_s} dt_s x_s B_s^T
+    (A_s the within-chunk cumulative log decay).  Same arguments as
+    ``ssd_quadratic_form``."""
+    h = h0.copy()
+    ys = []
+    for c0 in range(0, x.shape[0], chunk):
+        sl = slice(c0, c0 + chunk)
+        y, h = ssd_quadratic_form(x[sl], B[sl], C[sl], dt[sl], a_log_decay[sl], Dskip, h)
+        ys.append(y)
+    return np.concatenate(ys, axis=0), h
