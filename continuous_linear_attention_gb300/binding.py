@@ -35,6 +35,7 @@ EXPORTED = [
     "gdn_state_pool_reserve",
     "gdn_varlen_forward",
     "gdn_varlen_forward_noalloc",
+    "gdn_kda_varlen_forward",
     "gdn_get_error",
     "gdn_pool_set_timing_events",
     "gdn_status_string",
@@ -78,6 +79,7 @@ def load() -> ctypes.CDLL:
     lib.gdn_state_pool_reserve.argtypes = [P, I]
     lib.gdn_varlen_forward.argtypes = [P, I, P, P, P, P, P, P, ctypes.POINTER(Weights), P,
                                        I, I, I, P]
+    lib.gdn_kda_varlen_forward.argtypes = lib.gdn_varlen_forward.argtypes
     lib.gdn_varlen_forward_noalloc.argtypes = [P, S] + [I] * 8 + [S, I] + [P] * 6 + [
         ctypes.POINTER(Weights), P, I, I, I, P, P]
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
@@ -204,6 +206,18 @@ def varlen_forward(pool: Pool, layer: int, x_qkv, a, b, cu_seqlens, state_block_
                                      _ptr(cu_seqlens), _ptr(state_block_idx), _ptr(has_past),
                                      ctypes.byref(w), _ptr(out), T, N, max_seqlen_hint,
                                      _stream(stream)), "gdn_varlen_forward")
+
+
+def kda_varlen_forward(pool: Pool, layer: int, x_qkv, a, b, cu_seqlens, state_block_idx,
+                       has_past, conv_w, A_log, dt_bias, out, T: int, N: int,
+                       max_seqlen_hint: int = 0, stream=None) -> None:
+    """gdn_kda_varlen_forward: the per-channel-decay rule (a [T][Hv][d_k],
+    dt_bias [Hv][d_k]) on device tensors (or raw device pointers)."""
+    w = Weights(_ptr(conv_w), _ptr(A_log), _ptr(dt_bias))
+    _check(load().gdn_kda_varlen_forward(pool.handle, layer, _ptr(x_qkv), _ptr(a), _ptr(b),
+                                         _ptr(cu_seqlens), _ptr(state_block_idx), _ptr(has_past),
+                                         ctypes.byref(w), _ptr(out), T, N, max_seqlen_hint,
+                                         _stream(stream)), "gdn_kda_varlen_forward")
 
 
 def diag_umma_gemm(A, B, C, D, operand_f16=False, stream=None) -> None:

@@ -131,6 +131,12 @@ cudaError_t launch_intra(const FwdParams& p, const void* qk_map, const void* v_m
 // The state recurrence over the prefill chains; maps: q~|k~, -w, u, P (64 x 64
 // fp16 boxes) and gates.
 cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cudaStream_t stream);
+// The per-channel-decay (KDA) rule: p.a is [T][Hv][d_k] and p.dt_bias
+// [Hv][d_k].  Decode kernel for the shapes decode_supported() accepts, and the
+// token-serial kernel (as launch_recurrent) for everything else.
+cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
+cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
+                                 bool long_only, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

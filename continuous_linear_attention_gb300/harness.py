@@ -5,7 +5,8 @@ memory is a torch uint8 tensor (so tests can look at every byte), every pool
 byte outside block 0 filled with a seeded pattern, the workload's referenced
 blocks written at the library's reported offsets, inputs and weights as
 device tensors and ``out`` pre-filled with a sentinel.  ``run()`` is one call
-of ``gdn_varlen_forward``.  No arithmetic of the layer happens here.
+of ``gdn_varlen_forward`` (``gdn_kda_varlen_forward`` for per-channel gates).
+No arithmetic of the layer happens here.
 """
 from __future__ import annotations
 
@@ -89,9 +90,12 @@ class DeviceRun:
 
     # -- the call ----------------------------------------------------------
     def run(self, stream=None, max_seqlen_hint: int = 0):
-        binding.varlen_forward(self.pool, self.layer, self.x, self.a, self.b, self.cu, self.idx,
-                               self.has_past, self.conv_w, self.A_log, self.dt_bias, self.out,
-                               self.wl.T, self.wl.N, max_seqlen_hint, stream)
+        """One forward call: gdn_varlen_forward, or gdn_kda_varlen_forward for a
+        workload with one gate per key channel."""
+        fwd = binding.kda_varlen_forward if self.wl.channel_gate else binding.varlen_forward
+        fwd(self.pool, self.layer, self.x, self.a, self.b, self.cu, self.idx, self.has_past,
+            self.conv_w, self.A_log, self.dt_bias, self.out, self.wl.T, self.wl.N,
+            max_seqlen_hint, stream)
 
     def set_inputs(self, wl: Workload):
         """Point the run at another batch over the same pool (a continuation)."""

@@ -178,6 +178,28 @@ int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const voi
                        const uint8_t* has_past, const gdn_weights_t* weights, void* out, int T,
                        int N, int max_seqlen_hint, void* stream);
 
+/* Forward of one layer with the per-channel-decay rule (KDA: Kimi Delta
+ * Attention, the decay of the Kimi Linear and GLM5-next families that the
+ * model support tracker lists): the gated delta rule with one decay per key
+ * channel instead of one per head,
+ *   g_t[c] = -exp(A_log[h]) * softplus(a_t[h][c] + dt_bias[h][c]),
+ *   S_t = S_{t-1} Diag(e^{g_t}) + beta_t (v_t - S_{t-1} Diag(e^{g_t}) k_t) k_t^T,
+ *   o_t = S_t q_t
+ * (Kimi Team, "Kimi Linear", the KDA recurrence, in the S[v][k] orientation).
+ * Same pool, conv, conv and recurrent states, skip rules, error flags and
+ * stream contract as gdn_varlen_forward, except:
+ *   a        : [T][Hv][d_k] activation dtype, one gate pre-activation per key
+ *              channel of every v-head
+ *   weights  : dt_bias is [Hv][d_k] fp32 (A_log stays [Hv])
+ * Length-1 sequences run on an HBM-streaming decode kernel (d = 128, bf16,
+ * Hv = 2 Hk, K = 4), everything else on a token-serial kernel; the prefill
+ * scratch is not used.  Never synchronises; graph-capturable. */
+int gdn_kda_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const void* a,
+                           const void* b, const int32_t* cu_seqlens,
+                           const int32_t* state_block_idx, const uint8_t* has_past,
+                           const gdn_weights_t* weights, void* out, int T, int N,
+                           int max_seqlen_hint, void* stream);
+
 /* gdn_varlen_forward for callers that cannot allocate device memory.  The
  * pages have no counterpart to this entry point: it exists for engines that
  * plan every byte of device memory ahead and forbid runtime allocation, and

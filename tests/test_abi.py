@@ -78,6 +78,8 @@ def test_null_arguments_are_rejected_without_device_work():
                                   None, 0, 0, 0, None) == -1
     v = ctypes.c_uint32()
     assert lib.gdn_get_error(None, 0, ctypes.byref(v), 0, None) == -1
+    assert lib.gdn_kda_varlen_forward(None, 0, None, None, None, None, None, None,
+                                      ctypes.byref(w), None, 0, 0, 0, None) == -1
     assert lib.gdn_state_pool_destroy(None) == 0
     assert lib.gdn_state_pool_layout(None, None, None, None, None) == -1
 

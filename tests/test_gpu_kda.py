@@ -1,0 +1,70 @@
+"""GPU parity of the per-channel-decay (KDA) forward against the fp64 oracle,
+through the C ABI (gdn_kda_varlen_forward): the decode kernel on the
+256-request batch, the token-serial kernel on packed prefills and other head
+sizes, and the reduction to the scalar-gate forward when every key channel
+has the same gate.
+
+These cases have not been run on a GB300 yet: the kernels were written after
+the last GPU session, so they are collected but skipped until their first
+run confirms them."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from continuous_linear_attention_gb300 import harness, synth
+
+from gpu_check import check_against_oracle, rel_l2
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skip(reason="KDA kernels not yet run on a GB300")]
+
+
+def _kda(name, dims, lens, past, blocks, seed, slow=False):
+    return synth.make_workload(name, dims, lens, past, blocks, seed, slow_decay=slow,
+                               channel_gate=True)
+
+
+def test_tiny_packed_fp32():
+    check_against_oracle(_kda("kda_tiny", synth.TINY_DIMS, [5, 1, 9], [0, 1, 0], 8, 0))
+
+
+def test_tiny_packed_fp32_slow_decay():
+    check_against_oracle(_kda("kda_tiny_slow", synth.TINY_DIMS, [5, 1, 9], [0, 1, 0], 8, 0,
+                              slow=True))
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_bf16_mixed_lengths(d):
+    dims = synth.Dims(Hk=2, Hv=4, dk=d, dv=d, K=4, act="bf16")
+    check_against_oracle(_kda("kda_mixed", dims, [70, 1, 1, 129, 3], [1, 1, 0, 0, 1], 16, 5))
+
+
+def test_decode_batch_full():
+    """256 requests x 1 token at full dims: the HBM-streaming decode kernel."""
+    wl = _kda("kda_decode", synth.FULL_DIMS, [1] * 256, [1] * 256, 512, 1)
+    check_against_oracle(wl)
+
+
+def test_mixed_batch_full_dims():
+    """Decodes and short continuations together: decode kernel + token-serial
+    kernel in one call."""
+    lens = [1] * 32 + [65, 130, 17, 200]
+    wl = _kda("kda_mixed_full", synth.FULL_DIMS, lens, [1] * len(lens), 64, 3)
+    check_against_oracle(wl)
+
+
+def test_equal_channel_gates_match_the_scalar_forward():
+    base = synth.make_workload("g", synth.FULL_DIMS, [1] * 16 + [40], [1] * 17, 32, 6)
+    d = base.dims
+    kda = dataclasses.replace(
+        base, a=base.a[:, :, None].expand(-1, -1, d.dk).contiguous(),
+        dt_bias=base.dt_bias[:, None].expand(-1, d.dk).contiguous())
+    r1, r2 = harness.DeviceRun(base), harness.DeviceRun(kda)
+    r1.run()
+    r2.run()
+    torch.cuda.synchronize()
+    err = rel_l2(r2.out.float().cpu().numpy(), r1.out.float().cpu().numpy())
+    assert err <= 1e-3, err
+    assert r1.pool.error_flags() == 0 and r2.pool.error_flags() == 0
