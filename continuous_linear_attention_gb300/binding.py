@@ -36,6 +36,9 @@ EXPORTED = [
     "gdn_varlen_forward",
     "gdn_varlen_forward_noalloc",
     "gdn_kda_varlen_forward",
+    "gdn_ssd_pool_layout_for",
+    "gdn_ssd_pool_create",
+    "gdn_ssd_varlen_forward",
     "gdn_get_error",
     "gdn_pool_set_timing_events",
     "gdn_status_string",
@@ -51,6 +54,11 @@ class GdnError(RuntimeError):
 class Weights(ctypes.Structure):
     _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
                 ("dt_bias", ctypes.c_void_p)]
+
+
+class SsdWeights(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p), ("D", ctypes.c_void_p)]
 
 
 _lib = None
@@ -80,6 +88,10 @@ def load() -> ctypes.CDLL:
     lib.gdn_varlen_forward.argtypes = [P, I, P, P, P, P, P, P, ctypes.POINTER(Weights), P,
                                        I, I, I, P]
     lib.gdn_kda_varlen_forward.argtypes = lib.gdn_varlen_forward.argtypes
+    lib.gdn_ssd_pool_layout_for.argtypes = [I] * 8 + [S, PS, PS, PS, PS]
+    lib.gdn_ssd_pool_create.argtypes = [ctypes.POINTER(P)] + [I] * 8 + [S, P, S]
+    lib.gdn_ssd_varlen_forward.argtypes = [P, I, P, P, P, P, P, ctypes.POINTER(SsdWeights), P,
+                                           I, I, I, P]
     lib.gdn_varlen_forward_noalloc.argtypes = [P, S] + [I] * 8 + [S, I] + [P] * 6 + [
         ctypes.POINTER(Weights), P, I, I, I, P, P]
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
@@ -141,6 +153,15 @@ def layout_for(num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align=0):
     return tuple(o.value for o in out)
 
 
+def ssd_layout_for(num_blocks, num_layers, H, P, N, G, K, act, block_align=0):
+    """(block_stride, conv_off, ssm_off, total_bytes) of a Mamba2 pool."""
+    out = [ctypes.c_size_t() for _ in range(4)]
+    _check(load().gdn_ssd_pool_layout_for(num_blocks, num_layers, H, P, N, G, K, act_code(act),
+                                          block_align, *[ctypes.byref(o) for o in out]),
+           "gdn_ssd_pool_layout_for")
+    return tuple(o.value for o in out)
+
+
 class Pool:
     """A state pool (gdn_state_pool_create).  With ``memory`` (a CUDA uint8
     tensor) the pool lives in that tensor, which then is a byte view of it."""
@@ -195,6 +216,39 @@ class Pool:
         _check(load().gdn_get_error(self.handle, layer, ctypes.byref(v), 1 if reset else 0,
                                     _stream(stream)), "gdn_get_error")
         return v.value
+
+
+class SsdPool(Pool):
+    """A Mamba2 state pool (gdn_ssd_pool_create); ``rec_off`` is the SSM
+    state's offset.  With ``memory`` the pool lives in that CUDA uint8 tensor."""
+
+    def __init__(self, num_blocks, num_layers, H, P, N, G, K, act, block_align=0,
+                 memory: Optional[torch.Tensor] = None):
+        self.dims = (num_blocks, num_layers, H, P, N, G, K)
+        self.act = act_code(act)
+        self.num_blocks, self.num_layers = num_blocks, num_layers
+        self.memory = memory
+        h = ctypes.c_void_p()
+        nbytes = memory.numel() * memory.element_size() if memory is not None else 0
+        _check(load().gdn_ssd_pool_create(ctypes.byref(h), num_blocks, num_layers, H, P, N, G, K,
+                                          self.act, block_align, _ptr(memory), nbytes),
+               "gdn_ssd_pool_create")
+        self.handle = h
+        s, c, r, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_void_p()
+        _check(load().gdn_state_pool_layout(h, ctypes.byref(s), ctypes.byref(c), ctypes.byref(r),
+                                            ctypes.byref(b)), "gdn_state_pool_layout")
+        self.stride, self.conv_off, self.rec_off, self.base = s.value, c.value, r.value, b.value
+
+
+def ssd_varlen_forward(pool: SsdPool, layer: int, xbc, dt, cu_seqlens, state_block_idx, has_past,
+                       conv_w, A_log, dt_bias, D, y, T: int, N: int, max_seqlen_hint: int = 0,
+                       stream=None) -> None:
+    """gdn_ssd_varlen_forward on device tensors (or raw device pointers)."""
+    w = SsdWeights(_ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(D))
+    _check(load().gdn_ssd_varlen_forward(pool.handle, layer, _ptr(xbc), _ptr(dt),
+                                         _ptr(cu_seqlens), _ptr(state_block_idx), _ptr(has_past),
+                                         ctypes.byref(w), _ptr(y), T, N, max_seqlen_hint,
+                                         _stream(stream)), "gdn_ssd_varlen_forward")
 
 
 def varlen_forward(pool: Pool, layer: int, x_qkv, a, b, cu_seqlens, state_block_idx, has_past,

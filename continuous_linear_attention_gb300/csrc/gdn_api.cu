@@ -25,6 +25,10 @@ struct gdn_pool {
   unsigned char* scr;
   size_t scr_tokens;
   bool scr_grow;  // false: never allocated; the fused chunked kernel is used
+  // 0: gated delta net pool (conv + recurrent state); 1: Mamba2 pool (conv +
+  // SSM state [H][P][N] at rec_off), with its dimensions
+  int kind;
+  int ssd_H, ssd_P, ssd_N, ssd_G;
 };
 
 namespace {
@@ -115,6 +119,35 @@ Layout layout_of(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv,
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Mamba2 pools: conv state [K-1][C] (C = H*P + 2*G*N, activation dtype) at 0,
+// SSM state [H][P][N] fp32 at the next 128-byte boundary.
+int check_ssd_dims(int num_blocks, int num_layers, int H, int P, int NS, int G, int K, int act,
+                   size_t block_align) {
+  if (num_blocks < 2 || num_layers < 1) return GDN_ERR_RANGE;
+  if (H < 1 || G < 1 || H % G != 0 || H > 4096) return GDN_ERR_DIMS;
+  if (!gdn::ssd_supported(P, NS)) return GDN_ERR_DIMS;
+  if (K < 2 || K > gdn::kMaxConvK) return GDN_ERR_DIMS;
+  if (act != GDN_F32 && act != GDN_BF16) return GDN_ERR_DIMS;
+  if (block_align != 0 && (block_align < 128 || !is_pow2(block_align))) return GDN_ERR_DIMS;
+  if ((long long)num_blocks * num_layers > (1ll << 30)) return GDN_ERR_RANGE;
+  return GDN_OK;
+}
+
+Layout ssd_layout_of(int num_blocks, int num_layers, int H, int P, int NS, int G, int K, int act,
+                     size_t block_align) {
+  const size_t C = (size_t)H * P + 2 * (size_t)G * NS;
+  const size_t act_bytes = act == GDN_F32 ? 4 : 2;
+  const size_t conv_bytes = (size_t)(K - 1) * C * act_bytes;
+  const size_t ssm_bytes = (size_t)H * P * NS * sizeof(float);
+  Layout l;
+  l.conv_off = 0;
+  l.rec_off = roundup(conv_bytes, 128);
+  size_t align = block_align > 128 ? block_align : 128;
+  l.stride = roundup(l.rec_off + ssm_bytes, align);
+  l.total = l.stride * (size_t)num_blocks * (size_t)num_layers;
+  return l;
+}
 
 }  // namespace
 
@@ -251,6 +284,7 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
                        const uint8_t* has_past, const gdn_weights_t* w, void* out, int T, int N,
                        int max_seqlen_hint, void* stream) {
   if (!p || !w) return GDN_ERR_NULL;
+  if (p->kind != 0) return GDN_ERR_DIMS;
   if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
     return GDN_ERR_RANGE;
   if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
@@ -345,6 +379,7 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
 
 int gdn_state_pool_reserve(gdn_pool_t* p, int max_tokens) {
   if (!p) return GDN_ERR_NULL;
+  if (p->kind != 0) return GDN_ERR_DIMS;
   int prev = -1;
   cudaGetDevice(&prev);
   if (prev != p->device) return GDN_ERR_DEVICE;
@@ -400,6 +435,7 @@ int gdn_kda_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const vo
                            const gdn_weights_t* w, void* out, int T, int N, int max_seqlen_hint,
                            void* stream) {
   if (!p || !w) return GDN_ERR_NULL;
+  if (p->kind != 0) return GDN_ERR_DIMS;
   if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
     return GDN_ERR_RANGE;
   if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
@@ -460,6 +496,153 @@ int gdn_kda_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const vo
                cudaSuccess) {
       return GDN_ERR_CUDA;
     }
+  }
+  if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+int gdn_ssd_pool_layout_for(int num_blocks, int num_layers, int H, int P, int NS, int G, int K,
+                            int act, size_t block_align, size_t* block_stride, size_t* conv_off,
+                            size_t* ssm_off, size_t* total_bytes) {
+  int st = check_ssd_dims(num_blocks, num_layers, H, P, NS, G, K, act, block_align);
+  if (st != GDN_OK) return st;
+  Layout l = ssd_layout_of(num_blocks, num_layers, H, P, NS, G, K, act, block_align);
+  if (block_stride) *block_stride = l.stride;
+  if (conv_off) *conv_off = l.conv_off;
+  if (ssm_off) *ssm_off = l.rec_off;
+  if (total_bytes) *total_bytes = l.total;
+  return GDN_OK;
+}
+
+int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int H, int P, int NS,
+                        int G, int K, int act, size_t block_align, void* device_mem,
+                        size_t device_bytes) {
+  if (!out) return GDN_ERR_NULL;
+  *out = nullptr;
+  int st = check_ssd_dims(num_blocks, num_layers, H, P, NS, G, K, act, block_align);
+  if (st != GDN_OK) return st;
+  Layout l = ssd_layout_of(num_blocks, num_layers, H, P, NS, G, K, act, block_align);
+  if (device_mem) {
+    if (device_bytes < l.total) return GDN_ERR_NOMEM;
+    if (((uintptr_t)device_mem & 255u) != 0) return GDN_ERR_ALIGN;
+  }
+  gdn_pool* p = new (std::nothrow) gdn_pool();
+  if (!p) return GDN_ERR_NOMEM;
+  p->kind = 1;
+  p->num_blocks = num_blocks;
+  p->num_layers = num_layers;
+  p->ssd_H = H;
+  p->ssd_P = P;
+  p->ssd_N = NS;
+  p->ssd_G = G;
+  p->K = K;
+  p->act = act;
+  p->scr = nullptr;
+  p->scr_tokens = 0;
+  p->scr_grow = false;
+  p->stride = l.stride;
+  p->conv_off = l.conv_off;
+  p->rec_off = l.rec_off;
+  p->total = l.total;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return GDN_ERR_CUDA;
+  }
+  if (device_mem) {
+    p->base = (unsigned char*)device_mem;
+    p->owns = false;
+  } else {
+    if (cudaMalloc((void**)&p->base, l.total) != cudaSuccess) {
+      cudaGetLastError();
+      delete p;
+      return GDN_ERR_NOMEM;
+    }
+    p->owns = true;
+  }
+  const size_t work_bytes = gdn::WorkArea::words(num_blocks) * num_layers * sizeof(int32_t);
+  if (cudaMalloc((void**)&p->work, work_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    if (p->owns) cudaFree(p->base);
+    delete p;
+    return GDN_ERR_NOMEM;
+  }
+  if (cudaMemset(p->base, 0, l.total) != cudaSuccess ||
+      cudaMemset(p->work, 0, work_bytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    if (p->owns) cudaFree(p->base);
+    cudaFree(p->work);
+    delete p;
+    return GDN_ERR_CUDA;
+  }
+  *out = p;
+  return GDN_OK;
+}
+
+int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void* dt,
+                           const int32_t* cu_seqlens, const int32_t* state_block_idx,
+                           const uint8_t* has_past, const gdn_ssd_weights_t* w, void* y, int T,
+                           int N, int max_seqlen_hint, void* stream) {
+  if (!p || !w) return GDN_ERR_NULL;
+  if (p->kind != 1) return GDN_ERR_DIMS;
+  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
+    return GDN_ERR_RANGE;
+  if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
+  if (!cu_seqlens || !state_block_idx || !has_past || !w->conv_w || !w->A_log || !w->dt_bias ||
+      !w->D)
+    return GDN_ERR_NULL;
+  if (T > 0 && (!xbc || !dt || !y)) return GDN_ERR_NULL;
+  const int C = p->ssd_H * p->ssd_P + 2 * p->ssd_G * p->ssd_N;
+  if ((long long)T * C > (1ll << 40)) return GDN_ERR_RANGE;
+  if (T > 0 && (!aligned16(xbc) || !aligned16(dt) || !aligned16(y))) return GDN_ERR_ALIGN;
+  if (!aligned16(w->conv_w)) return GDN_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev != p->device) return GDN_ERR_DEVICE;
+
+  gdn::SsdParams sp;
+  sp.xbc = xbc;
+  sp.dt = dt;
+  sp.cu = cu_seqlens;
+  sp.blk = state_block_idx;
+  sp.has_past = has_past;
+  sp.conv_w = w->conv_w;
+  sp.A_log = w->A_log;
+  sp.dt_bias = w->dt_bias;
+  sp.Dskip = w->D;
+  sp.y = y;
+  sp.layer_base = p->base + (size_t)layer * p->num_blocks * p->stride;
+  sp.stride = p->stride;
+  sp.ssm_off = p->rec_off;
+  sp.T = T;
+  sp.N = N;
+  sp.H = p->ssd_H;
+  sp.G = p->ssd_G;
+  sp.C = C;
+  sp.K = p->K;
+  sp.work.base = p->work + (size_t)layer * gdn::WorkArea::words(p->num_blocks);
+  sp.work.num_blocks = p->num_blocks;
+
+  // the scheduler reads only the batch description and the work area
+  gdn::FwdParams fp;
+  fp.cu = cu_seqlens;
+  fp.blk = state_block_idx;
+  fp.has_past = has_past;
+  fp.T = T;
+  fp.N = N;
+  fp.num_blocks = p->num_blocks;
+  fp.max_seqlen_hint = max_seqlen_hint;
+  fp.work = sp.work;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (T > 0) {
+    int max_items = N;
+    if (max_items > p->num_blocks - 1) max_items = p->num_blocks - 1;
+    if (max_items > T) max_items = T;
+    if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_items, s) != cudaSuccess)
+      return GDN_ERR_CUDA;
   }
   if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;

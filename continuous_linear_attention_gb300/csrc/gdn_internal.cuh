@@ -84,6 +84,25 @@ struct FwdParams {
   void* scr_c = nullptr;
 };
 
+// The Mamba2 mixer's forward (conv over x | B | C, then the selective scan).
+struct SsdParams {
+  const void* xbc;         // [T][C] act, C = H*P + 2*G*N
+  const void* dt;          // [T][H] act
+  const int32_t* cu;       // [N+1]
+  const int32_t* blk;      // [N]
+  const uint8_t* has_past; // [N]
+  const void* conv_w;      // [C][K] act
+  const float* A_log;      // [H]
+  const float* dt_bias;    // [H]
+  const float* Dskip;      // [H]
+  void* y;                 // [T][H][P] act
+  unsigned char* layer_base;
+  size_t stride;           // block stride (bytes)
+  size_t ssm_off;          // SSM sub-state [H][P][N] fp32 offset inside a block
+  int T, N, H, G, C, K;
+  WorkArea work;
+};
+
 // Launch with programmatic stream serialization: the grid may be scheduled
 // before the previous kernel on the stream completes; the kernel orders
 // itself with pdl_wait_then_release() before touching global memory.
@@ -137,6 +156,11 @@ cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cu
 cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
                                  bool long_only, cudaStream_t stream);
+// The Mamba2 scan: token-serial kernel over every active sequence, then the
+// conv-state update (head dim P in {32, 64}, state size in {32, 64, 128}).
+bool ssd_supported(int P, int NS);
+cudaError_t launch_ssd(const SsdParams& p, int P, int NS, int act, int max_items,
+                       cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

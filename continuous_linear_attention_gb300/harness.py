@@ -13,7 +13,7 @@ from __future__ import annotations
 import torch
 
 from . import binding
-from .synth import Workload
+from .synth import SsdWorkload, Workload
 
 OUT_SENTINEL = 12.5
 
@@ -106,6 +106,62 @@ class DeviceRun:
                                             wl.has_past.to(dev))
         self.out = torch.full((wl.T, wl.dims.Hv, wl.dims.dv), OUT_SENTINEL,
                               dtype=wl.dims.torch_act, device=dev)
+
+    def close(self):
+        self.pool.close()
+
+
+class SsdDeviceRun:
+    """The same staging for a Mamba2 mixer workload (``synth.SsdWorkload``):
+    a Mamba2 pool in a torch byte tensor filled with a seeded pattern outside
+    the trash block, the referenced blocks' conv and SSM states written at the
+    library's offsets, inputs on the device, ``y`` pre-filled with the
+    sentinel.  ``run()`` is one call of ``gdn_ssd_varlen_forward``."""
+
+    def __init__(self, wl: SsdWorkload, device: str = "cuda", fill_seed: int = 7):
+        d = wl.dims
+        self.wl = wl
+        self.layer = 0
+        self.block_align = 0
+        stride, conv_off, ssm_off, total = binding.ssd_layout_for(
+            wl.num_blocks, 1, d.H, d.P, d.N, d.G, d.K, d.act)
+        self.mem = torch.empty(total, dtype=torch.uint8, device=device)
+        self.pool = binding.SsdPool(wl.num_blocks, 1, d.H, d.P, d.N, d.G, d.K, d.act,
+                                    memory=self.mem)
+        self.stride, self.conv_off, self.ssm_off = stride, conv_off, ssm_off
+        act = torch.float32 if d.act == "f32" else torch.bfloat16
+        self.conv_bytes = (d.K - 1) * d.C * (4 if d.act == "f32" else 2)
+        self.ssm_bytes = d.H * d.P * d.N * 4
+        g = torch.Generator(device=device)
+        g.manual_seed(fill_seed)
+        self.mem.copy_(torch.randint(0, 256, (total,), dtype=torch.uint8, device=device,
+                                     generator=g))
+        self.mem[:stride].zero_()  # the trash block reads zeros
+        for i, blk in enumerate(wl.ref_blocks.tolist()):
+            o = int(blk) * stride
+            self.mem[o: o + self.conv_bytes].view(act).copy_(wl.conv_state[i].reshape(-1))
+            self.mem[o + ssm_off: o + ssm_off + self.ssm_bytes].view(torch.float32).copy_(
+                wl.ssm_state[i].reshape(-1))
+        self.xbc, self.dt = wl.xbc.to(device), wl.dt.to(device)
+        self.conv_w = wl.conv_w.to(device)
+        self.A_log, self.dt_bias, self.D = (wl.A_log.to(device), wl.dt_bias.to(device),
+                                            wl.D.to(device))
+        self.cu, self.idx, self.has_past = (wl.cu_seqlens.to(device), wl.block_idx.to(device),
+                                            wl.has_past.to(device))
+        self.y = torch.full((wl.T, d.H, d.P), OUT_SENTINEL, dtype=act, device=device)
+        torch.cuda.synchronize()
+
+    def block_offset(self, blk: int) -> int:
+        return blk * self.stride
+
+    def block_bytes(self, blocks) -> torch.Tensor:
+        return torch.stack([self.mem[self.block_offset(int(b)): self.block_offset(int(b)) +
+                                     self.stride] for b in blocks]).cpu()
+
+    def run(self, stream=None, max_seqlen_hint: int = 0):
+        binding.ssd_varlen_forward(self.pool, self.layer, self.xbc, self.dt, self.cu, self.idx,
+                                   self.has_past, self.conv_w, self.A_log, self.dt_bias, self.D,
+                                   self.y, self.wl.T, self.wl.N, max_seqlen_hint, stream)
 
     def close(self):
         self.pool.close()

@@ -122,7 +122,8 @@ int gdn_state_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int 
 int gdn_state_pool_destroy(gdn_pool_t* pool);
 
 /* Layout of an existing pool and its base device address (any output may be
- * NULL).  For views and byte-exact tests. */
+ * NULL; for a Mamba2 pool rec_off is the SSM state's offset).  For views and
+ * byte-exact tests. */
 int gdn_state_pool_layout(const gdn_pool_t* pool, size_t* block_stride, size_t* conv_off,
                           size_t* rec_off, void** base);
 
@@ -145,7 +146,8 @@ int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, voi
  *                    (synchronous; call it before capturing a graph)
  *   max_tokens == 0: free the scratch and never grow it (fused kernel only)
  *   max_tokens < 0 : grow on demand again (the default)
- * Returns GDN_ERR_NOMEM if the allocation fails (the forward still works). */
+ * Returns GDN_ERR_NOMEM if the allocation fails (the forward still works),
+ * GDN_ERR_DIMS for a Mamba2 pool (it has no prefill scratch). */
 int gdn_state_pool_reserve(gdn_pool_t* pool, int max_tokens);
 
 /* Forward of one gated-delta-net layer over a packed batch.
@@ -172,7 +174,8 @@ int gdn_state_pool_reserve(gdn_pool_t* pool, int max_tokens);
  * Never synchronises (except the one-time growth of the prefill scratch, see
  * gdn_state_pool_reserve); graph-capturable.  Calls on the same pool must be
  * ordered on one stream (they share the layer's scheduler work area and the
- * pool's prefill scratch). */
+ * pool's prefill scratch).  A Mamba2 pool (gdn_ssd_pool_create) is refused
+ * with GDN_ERR_DIMS. */
 int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const void* a,
                        const void* b, const int32_t* cu_seqlens, const int32_t* state_block_idx,
                        const uint8_t* has_past, const gdn_weights_t* weights, void* out, int T,
@@ -199,6 +202,57 @@ int gdn_kda_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const
                            const int32_t* state_block_idx, const uint8_t* has_past,
                            const gdn_weights_t* weights, void* out, int T, int N,
                            int max_seqlen_hint, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Mamba2 mixers (the families the model support tracker lists with a conv
+ * state and an SSM state per request; the groundwork it asks for is a varlen
+ * scan with per-sequence states next to the varlen causal convolution).  Per
+ * head h of group g = h / (H/G), per token, the SSD recurrence of
+ * "Transformers are SSMs" with a scalar A per head:
+ *   y     = SiLU(causal depthwise conv over the channels x | B | C)
+ *   dt    = softplus(dt_raw + dt_bias[h]),  a = exp(-exp(A_log[h]) * dt)
+ *   h_t   = a * h_{t-1} + dt * x_t B_t^T        (h: P x N, fp32)
+ *   out_t = h_t C_t + D[h] * x_t
+ * The pool is the same kind of paged pool (block 0 = trash, one block per
+ * request, overwritten in place; the destroy, layout, copy_block, get_error
+ * and timing entry points apply to it), with a block holding
+ *   conv state [K-1][C] activation dtype at offset 0, C = H*P + 2*G*N
+ *   SSM state  [H][P][N] fp32 at ssm_off = roundup(conv bytes, 128),
+ *              element h_h[p][n] at ((h*P)+p)*N + n
+ *   block_stride = roundup(ssm_off + SSM bytes, max(128, block_align)).
+ * Supported: head_dim P in {32, 64}, d_state N in {32, 64, 128}, H % G == 0,
+ * 2 <= conv_k <= 4, GDN_F32 or GDN_BF16. */
+typedef struct {
+  const void* conv_w;    /* [C][K] activation dtype, channels x | B | C */
+  const float* A_log;    /* [H] */
+  const float* dt_bias;  /* [H] */
+  const float* D;        /* [H] skip weight */
+} gdn_ssd_weights_t;
+
+int gdn_ssd_pool_layout_for(int num_blocks, int num_layers, int num_heads, int head_dim,
+                            int d_state, int n_groups, int conv_k, int act_dtype,
+                            size_t block_align, size_t* block_stride, size_t* conv_off,
+                            size_t* ssm_off, size_t* total_bytes);
+
+/* As gdn_state_pool_create, for a Mamba2 pool. */
+int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int num_heads,
+                        int head_dim, int d_state, int n_groups, int conv_k, int act_dtype,
+                        size_t block_align, void* device_mem, size_t device_bytes);
+
+/* Forward of one Mamba2 mixer's conv + scan over a packed batch.
+ *   xbc : [T][C] activation dtype, the packed pre-convolution x | B | C rows
+ *   dt  : [T][H] activation dtype, time-step pre-activations
+ *   y   : [T][H][P] activation dtype (the scan output, before the gate and
+ *         norm that follow it in the mixer)
+ * cu_seqlens, state_block_idx, has_past, T, N, max_seqlen_hint, the skip
+ * rules, error flags and stream contract: as gdn_varlen_forward.  The pool
+ * must come from gdn_ssd_pool_create (GDN_ERR_DIMS otherwise).  Runs as a
+ * token-serial kernel (one CTA per sequence and head, state in registers)
+ * followed by the conv-state update.  Never synchronises; graph-capturable. */
+int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const void* dt,
+                           const int32_t* cu_seqlens, const int32_t* state_block_idx,
+                           const uint8_t* has_past, const gdn_ssd_weights_t* weights, void* y,
+                           int T, int N, int max_seqlen_hint, void* stream);
 
 /* gdn_varlen_forward for callers that cannot allocate device memory.  The
  * pages have no counterpart to this entry point: it exists for engines that

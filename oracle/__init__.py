@@ -355,6 +355,43 @@ def read_pool_states(pool_bytes: np.ndarray, layer, blocks, dims, num_blocks, nu
     return np.stack(convs), np.stack(recs)
 
 
+def ssd_pool_layout(num_blocks, num_layers, H, P, N, G, K, act_bytes, block_align=0):
+    """Byte layout of a Mamba2 state pool: the same per-request block as the
+    gated delta net's, with the mixer's two declared states each on a 128-byte
+    boundary ("Continuous batching for linear attention layers", the commit
+    that makes the layers declare their states): conv state [K-1][C]
+    (C = H*P + 2*G*N, activation dtype) at 0, SSM state [H][P][N] fp32 at the
+    next 128-byte boundary, stride rounded up to max(128, block_align)."""
+    C = H * P + 2 * G * N
+    conv_bytes = (K - 1) * C * act_bytes
+    ssm_off = _roundup(conv_bytes, 128)
+    ssm_bytes = H * P * N * 4
+    stride = _roundup(ssm_off + ssm_bytes, max(128, block_align))
+    return {"stride": stride, "conv_off": 0, "conv_bytes": conv_bytes, "ssm_off": ssm_off,
+            "ssm_bytes": ssm_bytes, "total": stride * num_blocks * num_layers}
+
+
+def read_ssd_pool_states(pool_bytes: np.ndarray, layer, blocks, dims, num_blocks, num_layers,
+                         block_align=0):
+    """Decode the conv and SSM sub-states of ``blocks`` from a Mamba2 pool byte
+    image.  Returns fp64 (conv [B][K-1][C], ssm [B][H][P][N])."""
+    act_bytes = 4 if dims.act == "f32" else 2
+    lay = ssd_pool_layout(num_blocks, num_layers, dims.H, dims.P, dims.N, dims.G, dims.K,
+                          act_bytes, block_align)
+    convs, ssms = [], []
+    for blk in blocks:
+        base = (layer * num_blocks + int(blk)) * lay["stride"]
+        cb = pool_bytes[base: base + lay["conv_bytes"]]
+        if act_bytes == 4:
+            conv = cb.view(np.float32).astype(np.float64)
+        else:
+            conv = (cb.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        sb = pool_bytes[base + lay["ssm_off"]: base + lay["ssm_off"] + lay["ssm_bytes"]]
+        convs.append(conv.reshape(dims.K - 1, dims.C))
+        ssms.append(sb.view(np.float32).astype(np.float64).reshape(dims.H, dims.P, dims.N))
+    return np.stack(convs), np.stack(ssms)
+
+
 # ---------------------------------------------------------------------------
 # Independent restatements used only as pins (numpy, fp64).
 

@@ -87,3 +87,47 @@ def check_against_oracle(wl, run=None, seqs=None, tol=None, expect_flags=0, ref=
             "bytes outside the written sub-states changed"
     assert errs["out"] <= tol and errs["rec"] <= tol, errs
     return errs
+
+
+def check_ssd_against_oracle(wl, tol=None, expect_flags=0):
+    """Run a Mamba2 workload through gdn_ssd_varlen_forward and compare with
+    the oracle: y rows (rel-L2), new conv states (bit-exact), SSM states
+    (rel-L2), y rows of skipped sequences and every pool byte outside the
+    written sub-states (byte-equal)."""
+    d = wl.dims
+    tol = TOL[d.act] if tol is None else tol
+    run = harness.SsdDeviceRun(wl)
+    before = run.mem.clone()
+    run.run()
+    torch.cuda.synchronize()
+    flags = run.pool.error_flags()
+    assert flags == expect_flags, f"error flags {flags:#x} != {expect_flags:#x}"
+    ref = oracle.ssd_forward(wl)
+    skip = ref["skip"]
+    cu = wl.cu_seqlens.tolist()
+    y = run.y.float().cpu().numpy().astype(np.float64)
+    active = [s for s in range(wl.N)
+              if not skip[s] and int(wl.block_idx[s]) >= 0 and cu[s + 1] > cu[s]]
+    rows = [r for s in active for r in range(cu[s], cu[s + 1])]
+    errs = {"y": rel_l2(y[rows], ref["y"][rows]) if rows else 0.0, "ssm": 0.0}
+    blocks = [int(wl.block_idx[s]) for s in active]
+    ref_blocks = [int(v) for v in wl.ref_blocks]
+    if blocks:
+        raw = run.block_bytes(blocks).numpy().reshape(-1)
+        conv, ssm = oracle.read_ssd_pool_states(raw, 0, range(len(blocks)), d, len(blocks), 1)
+        idx = [ref_blocks.index(b) for b in blocks]
+        np.testing.assert_array_equal(conv, ref["conv_state"][idx])
+        errs["ssm"] = rel_l2(ssm, ref["ssm_state"][idx])
+    for s in range(wl.N):
+        if s not in active:
+            assert (y[cu[s]:cu[s + 1]] == harness.OUT_SENTINEL).all(), f"seq {s} y written"
+    masked_before, masked_after = before.clone(), run.mem.clone()
+    for blk in blocks:
+        o = run.block_offset(blk)
+        for m in (masked_before, masked_after):
+            m[o: o + run.conv_bytes] = 0
+            m[o + run.ssm_off: o + run.ssm_off + run.ssm_bytes] = 0
+    assert torch.equal(masked_before, masked_after), "bytes outside the written sub-states changed"
+    run.close()
+    assert errs["y"] <= tol and errs["ssm"] <= tol, errs
+    return errs

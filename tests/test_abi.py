@@ -27,6 +27,7 @@ def test_every_declared_symbol_is_exported():
         assert hasattr(lib, n), n
     assert sorted(binding.EXPORTED + ["gdn_diag_umma_gemm", "gdn_diag_umma_gemm_ex",
                                       "gdn_diag_umma_issue_timing"]) == names
+    assert "gdn_kda_varlen_forward" in names and "gdn_ssd_varlen_forward" in names
 
 
 @pytest.mark.parametrize("dims", [
@@ -93,3 +94,39 @@ def test_mma_timing_arguments_are_checked_on_the_host():
         assert lib.gdn_diag_umma_issue_timing(N, a_tmem, reps, out, None) == -2
     misaligned = ctypes.c_void_p(ctypes.addressof(buf) + 4)
     assert lib.gdn_diag_umma_issue_timing(128, 0, 64, misaligned, None) == -4
+
+
+@pytest.mark.parametrize("dims", [
+    (512, 1, 128, 64, 128, 8, 4, "bf16", 0),
+    (8, 1, 4, 32, 32, 2, 4, "f32", 0),
+    (16, 3, 8, 64, 64, 1, 3, "bf16", 4096),
+    (4, 2, 2, 32, 128, 2, 2, "f32", 1 << 16),
+])
+def test_ssd_layout_matches_the_stated_layout(dims):
+    nb, nl, H, P, N, G, K, act, align = dims
+    stride, conv_off, ssm_off, total = binding.ssd_layout_for(nb, nl, H, P, N, G, K, act, align)
+    spec = oracle.ssd_pool_layout(nb, nl, H, P, N, G, K, 4 if act == "f32" else 2, align)
+    assert (stride, conv_off, ssm_off, total) == (spec["stride"], spec["conv_off"],
+                                                  spec["ssm_off"], spec["total"])
+    assert ssm_off % 128 == 0 and stride % 128 == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(P=16), dict(P=128), dict(N=16), dict(N=256), dict(G=3), dict(H=6, G=4), dict(K=1),
+    dict(K=5), dict(align=100),
+])
+def test_ssd_layout_rejects_unsupported_dims(bad):
+    args = dict(nb=8, nl=1, H=4, P=32, N=32, G=2, K=4, act="f32", align=0)
+    args.update(bad)
+    with pytest.raises(binding.GdnError) as e:
+        binding.ssd_layout_for(args["nb"], args["nl"], args["H"], args["P"], args["N"], args["G"],
+                               args["K"], args["act"], args["align"])
+    assert e.value.status == -2
+
+
+def test_ssd_null_arguments_are_rejected_without_device_work():
+    lib = binding.load()
+    assert lib.gdn_ssd_pool_create(None, 8, 1, 4, 32, 32, 2, 4, 0, 0, None, 0) == -1
+    w = binding.SsdWeights(None, None, None, None)
+    assert lib.gdn_ssd_varlen_forward(None, 0, None, None, None, None, None, ctypes.byref(w),
+                                      None, 0, 0, 0, None) == -1

@@ -1,0 +1,50 @@
+"""GPU parity of the Mamba2 mixer forward (gdn_ssd_varlen_forward) against the
+fp64 oracle, through the C ABI: packed batches of decodes and prefills with
+and without a past, head dims 32 and 64, state sizes 32 to 128, fp32 and bf16
+activations, padding and bad block indices.
+
+These cases have not been run on a GB300 yet: the kernels were written after
+the last GPU session, so they are collected but skipped until their first
+run confirms them."""
+import pytest
+
+from continuous_linear_attention_gb300 import synth
+
+from gpu_check import check_ssd_against_oracle
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skip(reason="Mamba2 kernels not yet run on a GB300")]
+
+TINY = synth.SsdDims(H=4, P=32, N=32, G=2, K=4, act="f32")
+
+
+def test_tiny_packed_fp32():
+    check_ssd_against_oracle(synth.make_ssd_workload("ssd_tiny", TINY, [5, 1, 9], [0, 1, 0], 8,
+                                                     0))
+
+
+def test_tiny_packed_fp32_slow_decay():
+    check_ssd_against_oracle(synth.make_ssd_workload("ssd_tiny_slow", TINY, [5, 1, 70],
+                                                     [0, 1, 1], 8, 0, slow_decay=True))
+
+
+@pytest.mark.parametrize("P,N", [(32, 64), (64, 32), (64, 128)])
+def test_bf16_mixed_lengths(P, N):
+    dims = synth.SsdDims(H=8, P=P, N=N, G=2, K=4, act="bf16")
+    wl = synth.make_ssd_workload("ssd_mixed", dims, [70, 1, 1, 129, 3], [1, 1, 0, 0, 1], 16, 5)
+    check_ssd_against_oracle(wl)
+
+
+def test_decode_batch_large_heads():
+    """128 heads of 64, state 128, 8 groups (the size class of the hybrid
+    families' Mamba2 mixers): 64 decodes with a past."""
+    dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
+    wl = synth.make_ssd_workload("ssd_decode", dims, [1] * 64, [1] * 64, 128, 1)
+    check_ssd_against_oracle(wl)
+
+
+def test_padding_and_bad_blocks_are_skipped():
+    dims = synth.SsdDims(H=4, P=32, N=32, G=1, K=3, act="f32")
+    wl = synth.make_ssd_workload("ssd_pad", dims, [3, 2, 0, 4], [1, 1, 0, 1], 6, 4,
+                                 block_idx=[2, -1, 3, 4])
+    check_ssd_against_oracle(wl)
