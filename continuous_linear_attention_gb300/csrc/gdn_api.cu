@@ -641,8 +641,18 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
     int max_items = N;
     if (max_items > p->num_blocks - 1) max_items = p->num_blocks - 1;
     if (max_items > T) max_items = T;
-    if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_items, s) != cudaSuccess)
+    if (gdn::ssd_decode_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->ssd_G, p->K, p->act)) {
+      // length-1 sequences: HBM-streaming decode kernel; longer ones (at most
+      // T/2 of them): token-serial kernel and conv-state update
+      if (gdn::launch_ssd_decode(sp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+      int max_long = max_items < T / 2 ? max_items : T / 2;
+      if (max_seqlen_hint == 1) max_long = 0;
+      if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_long, true, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    } else if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_items, false, s) !=
+               cudaSuccess) {
       return GDN_ERR_CUDA;
+    }
   }
   if (p->ev_after && cudaEventRecord(p->ev_after, s) != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;

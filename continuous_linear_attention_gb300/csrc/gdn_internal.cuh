@@ -156,11 +156,16 @@ cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cu
 cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
                                  bool long_only, cudaStream_t stream);
-// The Mamba2 scan: token-serial kernel over every active sequence, then the
-// conv-state update (head dim P in {32, 64}, state size in {32, 64, 128}).
+// The Mamba2 scan: token-serial kernel over every active sequence (or, with
+// long_only, those longer than one token), then their conv-state update (head
+// dim P in {32, 64}, state size in {32, 64, 128}); and the persistent decode
+// kernel for length-1 sequences at P = 64, N = 128, K = 4, bf16, H/G a
+// multiple of 8 up to 16.
 bool ssd_supported(int P, int NS);
 cudaError_t launch_ssd(const SsdParams& p, int P, int NS, int act, int max_items,
-                       cudaStream_t stream);
+                       bool long_only, cudaStream_t stream);
+bool ssd_decode_supported(int H, int P, int NS, int G, int K, int act);
+cudaError_t launch_ssd_decode(const SsdParams& p, int max_dec, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

@@ -246,9 +246,11 @@ int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int nu
  *         norm that follow it in the mixer)
  * cu_seqlens, state_block_idx, has_past, T, N, max_seqlen_hint, the skip
  * rules, error flags and stream contract: as gdn_varlen_forward.  The pool
- * must come from gdn_ssd_pool_create (GDN_ERR_DIMS otherwise).  Runs as a
- * token-serial kernel (one CTA per sequence and head, state in registers)
- * followed by the conv-state update.  Never synchronises; graph-capturable. */
+ * must come from gdn_ssd_pool_create (GDN_ERR_DIMS otherwise).  Length-1
+ * sequences run on an HBM-streaming decode kernel when P = 64, N = 128,
+ * K = 4, bf16 and H/G is 8 or 16; everything else on a token-serial kernel
+ * (one CTA per sequence and head, state in registers) followed by the
+ * conv-state update.  Never synchronises; graph-capturable. */
 int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const void* dt,
                            const int32_t* cu_seqlens, const int32_t* state_block_idx,
                            const uint8_t* has_past, const gdn_ssd_weights_t* weights, void* y,

@@ -37,9 +37,19 @@ def test_bf16_mixed_lengths(P, N):
 
 def test_decode_batch_large_heads():
     """128 heads of 64, state 128, 8 groups (the size class of the hybrid
-    families' Mamba2 mixers): 64 decodes with a past."""
+    families' Mamba2 mixers): 64 decodes with a past, on the decode kernel."""
     dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
     wl = synth.make_ssd_workload("ssd_decode", dims, [1] * 64, [1] * 64, 128, 1)
+    check_ssd_against_oracle(wl)
+
+
+def test_decode_kernel_with_longer_sequences():
+    """Decode kernel (H/G = 8) for the length-1 sequences and the token-serial
+    kernel for the others, in one call."""
+    dims = synth.SsdDims(H=16, P=64, N=128, G=2, K=4, act="bf16")
+    lens = [1] * 24 + [65, 130, 3]
+    wl = synth.make_ssd_workload("ssd_mixed_dec", dims, lens, [1] * 20 + [0] * 4 + [1, 0, 1], 40,
+                                 2)
     check_ssd_against_oracle(wl)
 
 
