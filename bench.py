@@ -56,12 +56,26 @@ def peaks():
 def decode_bytes(wl) -> int:
     """Algorithmic HBM bytes of one decode forward: per request the recurrent
     state read + write, the conv state read + write, x, a, b and out; the conv
-    weight, A_log and dt_bias once."""
+    weight, A_log and dt_bias once.  With one gate per key channel (KDA) a has
+    d_k entries per v-head and dt_bias is [Hv][d_k]."""
     d = wl.dims
     act = 4 if d.act == "f32" else 2
+    gate = d.dk if wl.channel_gate else 1
     per_req = (2 * d.Hv * d.dk * d.dv * 4 + 2 * (d.K - 1) * d.C * act + d.C * act
-               + 2 * d.Hv * act + d.Hv * d.dv * act)
-    weights = d.C * d.K * act + 2 * d.Hv * 4
+               + d.Hv * gate * act + d.Hv * act + d.Hv * d.dv * act)
+    weights = d.C * d.K * act + d.Hv * 4 + d.Hv * gate * 4
+    return wl.N * per_req + weights
+
+
+def ssd_decode_bytes(wl) -> int:
+    """Algorithmic HBM bytes of one Mamba2 decode forward: per request the SSM
+    state read + write (H x P x N fp32), the conv state read + write, the xbc
+    row, dt and y; the conv weight, A_log, dt_bias and D once."""
+    d = wl.dims
+    act = 4 if d.act == "f32" else 2
+    per_req = (2 * d.H * d.P * d.N * 4 + 2 * (d.K - 1) * d.C * act + d.C * act + d.H * act
+               + d.H * d.P * act)
+    weights = d.C * d.K * act + 3 * d.H * 4
     return wl.N * per_req + weights
 
 
@@ -193,6 +207,41 @@ def time_secondary(harness, wl, steps, device, pk, graph=False):
         res["graph_replay_ms_per_step"] = gms
         res["graph_replay_tokens_per_s"] = wl.T / (gms / 1e3)
     return res
+
+
+def time_variant_decode(harness, wl, steps, device, pk, nbytes):
+    """One-token-per-request batch of another layer family (the per-channel
+    decay rule, the Mamba2 scan): tokens/s and the HBM roofline of its decode
+    kernel, timed like the main line."""
+    import torch
+    ssd = hasattr(wl, "ssm_state")
+    run = (harness.SsdDeviceRun if ssd else harness.DeviceRun)(wl, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        run.run(stream, max_seqlen_hint=1)
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in kb + ka:
+        e.record(stream)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        run.pool.set_timing_events(kb[i], ka[i])
+        run.run(stream, max_seqlen_hint=1)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    run.pool.set_timing_events(None, None)
+    ms = start.elapsed_time(stop) / steps
+    kms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(steps))
+    flags = run.pool.error_flags()
+    run.close()
+    gbs = nbytes / (kms / 1e3) / 1e9
+    return {"workload": wl.name, "tokens": wl.T, "ms_per_step": ms,
+            "tokens_per_s": wl.T / (ms / 1e3), "compute_kernels_ms": kms,
+            "achieved_gbs": gbs, "hbm_frac": gbs / pk["hbm_gbs"],
+            "algorithmic_bytes": nbytes, "error_flags": flags}
 
 
 def time_graph(run, steps, hint=0):
@@ -343,6 +392,9 @@ def main():
                     help="skip the prefill / mixed-batch / long-context measurements")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the long-context measurement (4 x 32768 + 4 x 4096 tokens)")
+    ap.add_argument("--variants", action="store_true",
+                    help="also time the decode batches of the per-channel-decay rule and of "
+                         "the Mamba2 scan")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -473,6 +525,18 @@ def main():
             ]
             if not args.no_long:
                 line["secondary"].append(time_long_context(harness, binding, synth, dev, pk))
+        if args.variants:
+            dev = f"cuda:{local_rank}"
+            kda = synth.make_workload("kda_decode_256req", synth.FULL_DIMS, [1] * 256, [1] * 256,
+                                      512, 1, channel_gate=True)
+            ssd = synth.make_ssd_workload("mamba2_decode_256req_h128_p64_n128_g8",
+                                          synth.SsdDims(H=128, P=64, N=128, G=8, K=4,
+                                                        act="bf16"),
+                                          [1] * 256, [1] * 256, 512, 1)
+            line["variants"] = [
+                time_variant_decode(harness, kda, 200, dev, pk, decode_bytes(kda)),
+                time_variant_decode(harness, ssd, 200, dev, pk, ssd_decode_bytes(ssd)),
+            ]
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(line), flush=True)

@@ -49,3 +49,28 @@ def test_committed_traffic_record_names_a_kernel_source():
     for name, entry in rec.items():
         assert os.path.exists(os.path.join(bench.ROOT, "continuous_linear_attention_gb300", "csrc", name))
         assert entry["dram_bytes_per_launch"] > 0 and len(entry["source_sha256_16"]) == 16
+
+
+def test_decode_bytes_at_full_dims():
+    """State 2 x 32 x 128 x 128 x 4, conv state 2 x 3 x 8192 x 2, x 8192 x 2,
+    a and b 2 x 32 x 2, out 32 x 128 x 2 per request; weights 8192 x 4 x 2 +
+    2 x 32 x 4 once: 4,317,312 per request + 65,792."""
+    wl = synth.make_workload("d", synth.FULL_DIMS, [1] * 4, [1] * 4, 8, 4)
+    assert bench.decode_bytes(wl) == 4 * 4_317_312 + 65_792
+
+
+def test_decode_bytes_with_channel_gates():
+    """The gate input grows to 32 x 128 bf16 per request and dt_bias to
+    32 x 128 fp32 once."""
+    wl = synth.make_workload("d", synth.FULL_DIMS, [1] * 4, [1] * 4, 8, 4, channel_gate=True)
+    assert bench.decode_bytes(wl) == 4 * (4_317_312 + 32 * 127 * 2) + 65_792 + 32 * 127 * 4
+
+
+def test_mamba2_decode_bytes():
+    """H = 128, P = 64, N = 128, G = 8, K = 4, bf16 (C = 10240): state
+    2 x 4 MiB, conv state 2 x 3 x 10240 x 2, xbc 10240 x 2, dt 128 x 2,
+    y 128 x 64 x 2 per request; weights 10240 x 4 x 2 + 3 x 128 x 4."""
+    dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
+    wl = synth.make_ssd_workload("m", dims, [1] * 2, [1] * 2, 4, 0)
+    per = 2 * 4_194_304 + 2 * 3 * 10240 * 2 + 10240 * 2 + 256 + 16384
+    assert bench.ssd_decode_bytes(wl) == 2 * per + 10240 * 8 + 1536
