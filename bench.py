@@ -329,13 +329,11 @@ def max_over_ranks(values, device="cpu"):
     return [float(v) for v in t.tolist()]
 
 
-def cpu_baseline(wl, budget_s: float = 12.0):
+def cpu_baseline(wl, budget_s: float = 12.0, one_thread_s: float = 0.0):
     """The fp64 oracle as it stands, on the host cores, on a bounded sample of
-    the workload (its first requests), scaled to tokens/s."""
+    the workload (its first requests), scaled to tokens/s.  With one_thread_s
+    > 0 the same sample is also timed on one thread for about that long."""
     import dataclasses
-
-    import numpy as np
-    import torch
 
     import oracle
     cu = wl.cu_seqlens.tolist()
@@ -344,17 +342,25 @@ def cpu_baseline(wl, budget_s: float = 12.0):
     sub = dataclasses.replace(wl, x=wl.x[:T], a=wl.a[:T], b=wl.b[:T],
                               cu_seqlens=wl.cu_seqlens[:n + 1].clone(),
                               block_idx=wl.block_idx[:n], has_past=wl.has_past[:n])
-    reps, t0, threads = 0, time.perf_counter(), 1
-    while True:
-        res = oracle.forward(sub)
-        threads = res["threads"]
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
-            break
-    return {"value": reps * T / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {wl.N} requests ({T} tokens), {reps} passes, "
-                      f"{el:.1f} s wall, fp64 token-by-token"}
+
+    def timed(budget, nthreads):
+        reps, t0, threads = 0, time.perf_counter(), 1
+        while True:
+            res = oracle.forward(sub, nthreads=nthreads)
+            threads = res["threads"]
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget or reps >= 50:
+                return reps, el, threads
+
+    reps, el, threads = timed(budget_s, 0)
+    out = {"value": reps * T / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"first {n} of {wl.N} requests ({T} tokens), {reps} passes, "
+                     f"{el:.1f} s wall, fp64 token-by-token"}
+    if one_thread_s > 0:
+        r1, e1, _ = timed(one_thread_s, 1)
+        out["value_1_thread"] = r1 * T / e1
+    return out
 
 
 def run_reference(args, rank, world):
@@ -538,7 +544,7 @@ def main():
                 time_variant_decode(harness, ssd, 200, dev, pk, ssd_decode_bytes(ssd)),
             ]
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(wl)
+            line["cpu_baseline"] = cpu_baseline(wl, one_thread_s=4.0)
         print(json.dumps(line), flush=True)
     run.close()
     if world > 1:

@@ -74,3 +74,12 @@ def test_mamba2_decode_bytes():
     wl = synth.make_ssd_workload("m", dims, [1] * 2, [1] * 2, 4, 0)
     per = 2 * 4_194_304 + 2 * 3 * 10240 * 2 + 10240 * 2 + 256 + 16384
     assert bench.ssd_decode_bytes(wl) == 2 * per + 10240 * 8 + 1536
+
+
+def test_cpu_baseline_reports_cores_and_one_thread_rate():
+    """The oracle leg runs on the host alone (no GPU): a bounded sample, the
+    threads it used, and the one-thread rate."""
+    wl = synth.make_workload("d", synth.TINY_DIMS, [1] * 8, [1] * 8, 16, 2)
+    cb = bench.cpu_baseline(wl, budget_s=0.2, one_thread_s=0.1)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["cores"] >= 1
+    assert cb["value"] > 0 and cb["value_1_thread"] > 0
