@@ -68,3 +68,33 @@ def test_equal_channel_gates_match_the_scalar_forward():
     err = rel_l2(r2.out.float().cpu().numpy(), r1.out.float().cpu().numpy())
     assert err <= 1e-3, err
     assert r1.pool.error_flags() == 0 and r2.pool.error_flags() == 0
+
+
+def test_decode_hint_and_graph_replay():
+    """A pure decode batch with max_seqlen_hint = 1 (decode kernel only),
+    captured once in a CUDA graph and replayed from the same pool contents:
+    the replay gives the eager result bit for bit."""
+    wl = _kda("kda_graph", synth.FULL_DIMS, [1] * 16, [1] * 16, 32, 7)
+    eager = harness.DeviceRun(wl)
+    pool0 = eager.mem.clone()
+    eager.run(max_seqlen_hint=1)
+    torch.cuda.synchronize()
+    check_against_oracle(wl, run=eager)
+    g = torch.cuda.CUDAGraph()
+    eager.mem.copy_(pool0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        eager.run(torch.cuda.current_stream(), max_seqlen_hint=1)
+    eager.mem.copy_(pool0)
+    out_eager = eager.out.clone()
+    eager.out.fill_(harness.OUT_SENTINEL)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.out, out_eager)
+
+
+@pytest.mark.parametrize("blocks,flag", [([3, 9, 5], 0x2), ([3, 0, 5], 0x4), ([3, 5, 5], 0x8)])
+def test_bad_block_indices_are_flagged_and_skipped(blocks, flag):
+    wl = synth.make_workload("kda_bad", synth.TINY_DIMS, [4, 1, 3], [1, 1, 0], 8, 2,
+                             block_idx=blocks, channel_gate=True)
+    check_against_oracle(wl, expect_flags=flag)

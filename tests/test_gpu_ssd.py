@@ -58,3 +58,36 @@ def test_padding_and_bad_blocks_are_skipped():
     wl = synth.make_ssd_workload("ssd_pad", dims, [3, 2, 0, 4], [1, 1, 0, 1], 6, 4,
                                  block_idx=[2, -1, 3, 4])
     check_ssd_against_oracle(wl)
+
+
+def test_graph_replay_matches_eager():
+    """Decodes and one prefill, captured once in a CUDA graph and replayed
+    from the same pool contents: bit-identical to the eager call."""
+    import torch
+
+    from continuous_linear_attention_gb300 import harness
+    dims = synth.SsdDims(H=16, P=64, N=128, G=2, K=4, act="bf16")
+    wl = synth.make_ssd_workload("ssd_graph", dims, [1] * 8 + [40], [1] * 9, 16, 3)
+    run = harness.SsdDeviceRun(wl)
+    pool0 = run.mem.clone()
+    run.run()
+    torch.cuda.synchronize()
+    y_eager = run.y.clone()
+    g = torch.cuda.CUDAGraph()
+    run.mem.copy_(pool0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        run.run(torch.cuda.current_stream())
+    run.mem.copy_(pool0)
+    run.y.fill_(harness.OUT_SENTINEL)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(run.y, y_eager)
+    assert run.pool.error_flags() == 0
+    run.close()
+
+
+@pytest.mark.parametrize("blocks,flag", [([3, 9, 5], 0x2), ([3, 0, 5], 0x4), ([3, 5, 5], 0x8)])
+def test_bad_block_indices_are_flagged_and_skipped(blocks, flag):
+    wl = synth.make_ssd_workload("ssd_bad", TINY, [4, 1, 3], [1, 1, 0], 8, 2, block_idx=blocks)
+    check_ssd_against_oracle(wl, expect_flags=flag)
