@@ -4,9 +4,8 @@ through the C ABI (gdn_kda_varlen_forward): the decode kernel on the
 sizes, and the reduction to the scalar-gate forward when every key channel
 has the same gate.
 
-These cases have not been run on a GB300 yet: the kernels were written after
-the last GPU session, so they are collected but skipped until their first
-run confirms them."""
+The kernels behind these cases have not run on a GB300 yet, so the cases are
+collected but skipped until a first run confirms them."""
 import dataclasses
 
 import numpy as np

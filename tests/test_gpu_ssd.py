@@ -3,9 +3,8 @@ fp64 oracle, through the C ABI: packed batches of decodes and prefills with
 and without a past, head dims 32 and 64, state sizes 32 to 128, fp32 and bf16
 activations, padding and bad block indices.
 
-These cases have not been run on a GB300 yet: the kernels were written after
-the last GPU session, so they are collected but skipped until their first
-run confirms them."""
+The kernels behind these cases have not run on a GB300 yet, so the cases are
+collected but skipped until a first run confirms them."""
 import pytest
 
 from continuous_linear_attention_gb300 import synth
