@@ -193,7 +193,8 @@ def time_secondary(harness, wl, steps, device, pk, graph=False):
     torch.cuda.synchronize()
     run.pool.set_timing_events(None, None)
     ms = start.elapsed_time(stop) / steps
-    kms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(steps))
+    kall = [kb[i].elapsed_time(ka[i]) for i in range(steps)]
+    kms = statistics.mean(kall)
     gms = time_graph(run, steps) if graph else None
     flags = run.pool.error_flags()
     run.close()
@@ -201,6 +202,7 @@ def time_secondary(harness, wl, steps, device, pk, graph=False):
     tf = fl / (kms / 1e3) / 1e12
     res = {"workload": wl.name, "tokens": wl.T, "ms_per_step": ms,
            "tokens_per_s": wl.T / (ms / 1e3), "compute_kernels_ms": kms,
+           "compute_kernels_ms_median": statistics.median(kall),
            "prefill_tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
            "algorithmic_flops": fl, "error_flags": flags}
     if gms is not None:
@@ -513,7 +515,8 @@ def main():
                          "traffic": traffic, "peak_source": pk["source"],
                          "kernel": "decode_kernel (the only compute kernel of a decode batch)",
                          "algorithmic_bytes_per_launch": alg_bytes,
-                         "kernel_ms_mean": kern_mean_ms},
+                         "kernel_ms_mean": kern_mean_ms,
+                         "kernel_ms_median": statistics.median(kern_ms)},
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
