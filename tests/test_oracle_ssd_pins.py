@@ -185,3 +185,25 @@ def test_skipped_sequences_and_new_conv_tails():
         r = refb.index(int(wl.block_idx[s]))
         old = wl.conv_state[r].numpy()
         np.testing.assert_array_equal(res["conv_state"][r], np.concatenate([old, xbc[lo:hi]])[-3:])
+
+
+def test_pool_image_round_trip_through_the_stated_layout():
+    """States packed into a byte image at the stated offsets (bf16 conv state,
+    fp32 SSM state) decode back exactly: the decoder the GPU checks use reads
+    the layout the boundary states."""
+    dims = synth.SsdDims(H=4, P=32, N=32, G=2, K=4, act="bf16")
+    nb, align = 5, 4096
+    lay = oracle.ssd_pool_layout(nb, 1, dims.H, dims.P, dims.N, dims.G, dims.K, 2, align)
+    img = np.zeros(lay["total"], dtype=np.uint8)
+    rng = _rng(9)
+    conv = torch.from_numpy(rng.standard_normal((nb, dims.K - 1, dims.C)).astype(np.float32))
+    conv = conv.to(torch.bfloat16)
+    ssm = rng.standard_normal((nb, dims.H, dims.P, dims.N)).astype(np.float32)
+    for b in range(nb):
+        o = b * lay["stride"]
+        img[o:o + lay["conv_bytes"]] = conv[b].reshape(-1).view(torch.uint8).numpy()
+        img[o + lay["ssm_off"]:o + lay["ssm_off"] + lay["ssm_bytes"]] = ssm[b].reshape(-1).view(np.uint8)
+    c2, s2 = oracle.read_ssd_pool_states(img, 0, [3, 1], dims, nb, 1, block_align=align)
+    np.testing.assert_array_equal(c2, conv.float().numpy()[[3, 1]].astype(np.float64))
+    np.testing.assert_array_equal(s2, ssm[[3, 1]].astype(np.float64))
+    assert lay["ssm_off"] % 128 == 0 and lay["stride"] % align == 0
