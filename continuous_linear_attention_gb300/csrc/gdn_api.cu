@@ -120,6 +120,26 @@ Layout layout_of(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv,
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Mamba2 pools: the chunked scan's fp16 conv output, one row of C per packed
+// token (synchronous; frees the old buffer first, which waits for the device).
+int ssd_grow_scratch(gdn_pool* p, size_t tokens) {
+  if (p->scr_tokens >= tokens) return GDN_OK;
+  const size_t cap = roundup(tokens, 4096);
+  const size_t C = (size_t)p->ssd_H * p->ssd_P + 2 * (size_t)p->ssd_G * p->ssd_N;
+  if (p->scr) {
+    cudaFree(p->scr);
+    p->scr = nullptr;
+    p->scr_tokens = 0;
+  }
+  if (cudaMalloc((void**)&p->scr, cap * C * 2) != cudaSuccess) {
+    cudaGetLastError();
+    p->scr = nullptr;
+    return GDN_ERR_NOMEM;
+  }
+  p->scr_tokens = cap;
+  return GDN_OK;
+}
+
 // Mamba2 pools: conv state [K-1][C] (C = H*P + 2*G*N, activation dtype) at 0,
 // SSM state [H][P][N] fp32 at the next 128-byte boundary.
 int check_ssd_dims(int num_blocks, int num_layers, int H, int P, int NS, int G, int K, int act,
@@ -379,7 +399,27 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
 
 int gdn_state_pool_reserve(gdn_pool_t* p, int max_tokens) {
   if (!p) return GDN_ERR_NULL;
-  if (p->kind != 0) return GDN_ERR_DIMS;
+  if (p->kind != 0) {
+    // Mamba2 pool: the chunked scan's fp16 conv scratch
+    int prev_dev = -1;
+    cudaGetDevice(&prev_dev);
+    if (prev_dev != p->device) return GDN_ERR_DEVICE;
+    if (max_tokens > 0) {
+      p->scr_grow = true;
+      return ssd_grow_scratch(p, (size_t)max_tokens);
+    }
+    if (max_tokens == 0) {
+      if (p->scr) {
+        cudaFree(p->scr);
+        p->scr = nullptr;
+      }
+      p->scr_tokens = 0;
+      p->scr_grow = false;
+      return GDN_OK;
+    }
+    p->scr_grow = true;
+    return GDN_OK;
+  }
   int prev = -1;
   cudaGetDevice(&prev);
   if (prev != p->device) return GDN_ERR_DEVICE;
@@ -539,7 +579,7 @@ int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int H,
   p->act = act;
   p->scr = nullptr;
   p->scr_tokens = 0;
-  p->scr_grow = false;
+  p->scr_grow = true;  // the chunked scan's fp16 conv scratch, grown on demand
   p->stride = l.stride;
   p->conv_off = l.conv_off;
   p->rec_off = l.rec_off;
@@ -635,6 +675,15 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
   fp.work = sp.work;
 
   cudaStream_t s = (cudaStream_t)stream;
+  // fp16 conv scratch of the chunked scan: grown on demand outside stream capture
+  if (p->scr_grow && (size_t)T > p->scr_tokens && T > 1 && max_seqlen_hint != 1 &&
+      gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act)) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
+      ssd_grow_scratch(p, (size_t)T);
+    else
+      cudaGetLastError();
+  }
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (T > 0) {
@@ -643,12 +692,19 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
     if (max_items > T) max_items = T;
     if (gdn::ssd_decode_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->ssd_G, p->K, p->act)) {
       // length-1 sequences: HBM-streaming decode kernel; longer ones (at most
-      // T/2 of them): token-serial kernel and conv-state update
+      // T/2 of them): the chunked scan when the scratch holds T rows, else the
+      // token-serial kernel, then their conv-state update
       if (gdn::launch_ssd_decode(sp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
       int max_long = max_items < T / 2 ? max_items : T / 2;
       if (max_seqlen_hint == 1) max_long = 0;
-      if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_long, true, s) != cudaSuccess)
+      const bool chunked = max_long > 0 && p->scr && p->scr_tokens >= (size_t)T &&
+                           gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act);
+      if (chunked) {
+        if (gdn::launch_ssd_chunk(sp, p->scr, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;
+      } else if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_long, true, s) !=
+                 cudaSuccess) {
         return GDN_ERR_CUDA;
+      }
     } else if (gdn::launch_ssd(sp, p->ssd_P, p->ssd_N, p->act, max_items, false, s) !=
                cudaSuccess) {
       return GDN_ERR_CUDA;

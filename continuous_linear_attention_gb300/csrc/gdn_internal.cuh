@@ -166,6 +166,11 @@ cudaError_t launch_ssd(const SsdParams& p, int P, int NS, int act, int max_items
                        bool long_only, cudaStream_t stream);
 bool ssd_decode_supported(int H, int P, int NS, int G, int K, int act);
 cudaError_t launch_ssd_decode(const SsdParams& p, int max_dec, cudaStream_t stream);
+// The chunked tensor-core scan of the prefill sequences (P = 64, N = 128, bf16,
+// H even): conv into the fp16 scratch xs [T][C], the chunk kernel, the
+// conv-state update.
+bool ssd_chunk_supported(int H, int P, int NS, int K, int act);
+cudaError_t launch_ssd_chunk(const SsdParams& p, void* xs, int max_pre, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

@@ -23,9 +23,23 @@
 //    write it from registers to HBM.  A unit is (request, group): it owns the
 //    x channels of the group's heads and the group's B and C channels, so it
 //    writes its part of the conv state in place.  Longer sequences then run on
-//    the token-serial kernel.
+//    the token-serial kernel, or, at that shape and when the pool's scratch
+//    holds the call's rows, on the chunked scan below.
+//  - ssd_prep_kernel + ssd_chunk_kernel: the chunked scan of the prefill
+//    sequences on the tensor cores (chunks of 128 tokens, one CTA per
+//    (sequence, pair of heads of one group), the pair's two 64 x 128 states
+//    stacked as one 128-lane fp32 accumulator in tensor memory).  The chunk
+//    form of the SSD recurrence needs no triangular solve: with dt_h and the
+//    in-chunk cumulative log decay cum_h,
+//      CB  = C B^T,  M_h[t][s] = CB[t][s] e^{cum_h[t] - cum_h[s]} dt_h[s] (s <= t)
+//      y_h = M_h X_h + e^{cum_h[t]} (C h_h^T)[t] + D_h x_h
+//      h_h <- e^{cum_h[end]} h_h + (X_h e^{cum_h[end] - cum_h} dt_h)^T B
+//    (state space duality, "Transformers are SSMs").
+#include <cuda.h>
+
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -426,6 +440,368 @@ cudaError_t launch_by_state(const SsdParams& p, int NS, int max_items, bool long
   return launch_rec_t<P, 128, Act>(p, max_items, long_only, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Chunked scan (prefill).  Per chunk (r0 = first row, n valid tokens), heads
+// h0 = 2 hp and h0 + 1 of group g:
+//   TMA   X = xs[r0.., h0*64 .. h0*64+127] (2 boxes), B and C of the group
+//   CUDA  dt_h, cum_h (inclusive scan over the chunk); rows t >= n of X, B, C
+//         zeroed (another sequence's rows or stale scratch)
+//   CUDA  hand-over: h (TMEM, lane = (head, p), column = n) -> h16 (fp16
+//         K-major B operand), h <- e^{cum_h[n-1]} h
+//   CUDA  X'[s][(head,p)] = X dt_h[s] e^{cum_h[n-1] - cum_h[s]}
+//   MMA   CB = C B^T, YI = C h16^T, h += X'^T B (X' and B MN-major)
+//   CUDA  M_h from CB; MMA Y[:, 64 head ..] = M_h X_h, one head at a time
+//   CUDA  y = Y + e^{cum_h[t]} YI + D_h x  -> bf16
+// fp16 operands, fp32 accumulators and state; |h| is range-checked against
+// the fp16 limit (GDN_FLAG_RANGE).
+
+using E = __half;
+constexpr int SP = 64;     // head dim
+constexpr int SN = 128;    // state size
+constexpr int SQ = 128;    // chunk
+constexpr int kCThreads = 256;
+constexpr uint32_t CBOX = 16384;  // one [128 rows][64 cols] fp16 box, 128-byte swizzled
+constexpr uint32_t OFF_X = 0;          // X pair: 2 boxes (head 0, head 1)
+constexpr uint32_t OFF_B = 2 * CBOX;    // B: 2 boxes (n 0..63, 64..127)
+constexpr uint32_t OFF_C = 4 * CBOX;    // C: 2 boxes
+constexpr uint32_t OFF_XP = 6 * CBOX;   // X' (same layout as X)
+constexpr uint32_t OFF_H16 = 8 * CBOX;  // h16: [128 rows (head,p)][128 n], 2 K-blocks
+constexpr uint32_t OFF_M = 10 * CBOX;   // M_h: [128 t][128 s], 2 K-blocks
+constexpr uint32_t TILE_BYTES = 12 * CBOX;               // 196608
+constexpr uint32_t CSMEM_BYTES = TILE_BYTES + 1024;      // + alignment slack
+constexpr uint32_t TM_CB = 0, TM_YI = 128, TM_Y = 256, TM_H = 384, TM_COLS = 512;
+constexpr float kCF16Max = 65000.f;
+
+__device__ __forceinline__ bool ssd_cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
+  if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity) ? 1 : 0;
+  __syncthreads();
+  return *flag != 0;
+}
+
+__global__ void __launch_bounds__(kCThreads, 1)
+ssd_chunk_kernel(SsdParams p, const __grid_constant__ CUtensorMap txs) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t full, mma_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int okf;
+  __shared__ float cum[2][SQ], dts[2][SQ];
+  pdl_wait_then_release();
+  const int tid = threadIdx.x;
+  const int H = p.H, G = p.G;
+  const int hpg = H / G;
+  const int pairs = H / 2;
+  const int n_pre = p.work.header()[kNPre];
+  if ((int)blockIdx.x >= n_pre * pairs) return;
+  const int s = p.work.pre()[blockIdx.x / pairs];
+  const int hp = blockIdx.x % pairs;
+  const int h0 = 2 * hp;
+  const int g = h0 / hpg;
+  const int seq0 = p.cu[s];
+  const int L = p.cu[s + 1] - seq0;
+  const int wblk = p.blk[s];
+  const int rblk = p.has_past[s] ? wblk : 0;
+  const uint32_t sbase = smem_u32(sm);
+
+  if (tid == 0) {
+    mbar_init(&full, 1);
+    mbar_init(&mma_bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane = (uint32_t)(tid & 96) << 16;  // TMEM lane quarter of this warp
+  const int row = tid & 127;                          // TMEM lane: token t or (head, p)
+  const int hf = tid >> 7;                            // column half
+  const int rhead = row >> 6, rp = row & 63;          // (head, p) of a state row
+  uint32_t ph_full = 0, ph_mma = 0;
+  bool dead = false;
+  float amax = 0.f;
+  const float* S_r = reinterpret_cast<const float*>(p.layer_base + (size_t)rblk * p.stride +
+                                                    p.ssm_off);
+  float* S_w = reinterpret_cast<float*>(p.layer_base + (size_t)wblk * p.stride + p.ssm_off);
+  __nv_bfloat16* __restrict__ yout = reinterpret_cast<__nv_bfloat16*>(p.y);
+  const __nv_bfloat16* __restrict__ dtr = reinterpret_cast<const __nv_bfloat16*>(p.dt);
+  const int nc = (L + SQ - 1) / SQ;
+
+  // ---- initial state into TMEM (row = (head, p), columns n of this half)
+  {
+    float hv[32];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int n0 = hf * 64 + q * 32;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        hv[e] = rblk != 0 ? S_r[((size_t)(h0 + rhead) * SP + rp) * SN + n0 + e] : 0.f;
+      tc::tmem_st32(tmem + lane + TM_H + n0, hv);
+    }
+    tc::tmem_wait_st();
+  }
+
+  for (int c = 0; c < nc; ++c) {
+    const int r0 = seq0 + c * SQ;
+    const int n = min(SQ, L - c * SQ);
+    // ---- tiles of this chunk
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&full, 6 * CBOX);
+      tma_load_2d(sm + OFF_X, &txs, h0 * SP, r0, &full);
+      tma_load_2d(sm + OFF_X + CBOX, &txs, h0 * SP + SP, r0, &full);
+      tma_load_2d(sm + OFF_B, &txs, H * SP + g * SN, r0, &full);
+      tma_load_2d(sm + OFF_B + CBOX, &txs, H * SP + g * SN + 64, r0, &full);
+      tma_load_2d(sm + OFF_C, &txs, H * SP + G * SN + g * SN, r0, &full);
+      tma_load_2d(sm + OFF_C + CBOX, &txs, H * SP + G * SN + g * SN + 64, r0, &full);
+    }
+    // ---- time steps and in-chunk cumulative log decays of the two heads
+    {
+      const int hh = tid >> 7, t = tid & 127;
+      const int h = h0 + hh;
+      float d = 0.f;
+      if (t < n) d = softplus_f32(__bfloat162float(dtr[(size_t)(r0 + t) * H + h]) + p.dt_bias[h]);
+      dts[hh][t] = d;
+      cum[hh][t] = -__expf(p.A_log[h]) * d;
+    }
+    __syncthreads();
+    // inclusive scan over t (Hillis-Steele, 7 steps) per head
+    for (int off = 1; off < SQ; off <<= 1) {
+      const int hh = tid >> 7, t = tid & 127;
+      const float add = t >= off ? cum[hh][t - off] : 0.f;
+      __syncthreads();
+      cum[hh][t] += add;
+      __syncthreads();
+    }
+    if (!ssd_cta_wait(&full, ph_full, &okf)) { dead = true; break; }
+    ph_full ^= 1;
+    // ---- rows t >= n of X, B, C -> 0 (another sequence's rows or stale data)
+    if (n < SQ) {
+      for (int i = tid; i < (SQ - n) * 8 * 6; i += kCThreads) {
+        const int box = i / ((SQ - n) * 8);
+        const int rem = i % ((SQ - n) * 8);
+        const int r = n + rem / 8, ch = rem % 8;
+        *reinterpret_cast<uint4*>(sm + box * CBOX + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    // ---- hand-over: h16 <- h (fp16, K-major rows (head,p)), h <- e^{cum[n-1]} h
+    {
+      const float dc = __expf(cum[rhead][n - 1]);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n0 = hf * 64 + q * 32;
+        float hv[32];
+        tc::tmem_ld32(tmem + lane + TM_H + n0, hv);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          amax = fmaxf(amax, max_abs3(max_abs3(hv[e], hv[e + 1], hv[e + 2]),
+                                      max_abs3(hv[e + 3], hv[e + 4], hv[e + 5]),
+                                      max_abs3(hv[e + 6], hv[e + 7], 0.f)));
+          tc::sw128_store8<E>(sm + OFF_H16 + hf * CBOX, row, q * 32 + e, hv + e);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) hv[e] *= dc;
+        tc::tmem_st32(tmem + lane + TM_H + n0, hv);
+      }
+      tc::tmem_wait_st();
+    }
+    // ---- X'[s][(head,p)] = X dt e^{cum[n-1] - cum[s]}: thread = token s, one box
+    {
+      const int sidx = tid & 127, hh = tid >> 7;
+      const float f = sidx < n ? dts[hh][sidx] * __expf(cum[hh][n - 1] - cum[hh][sidx]) : 0.f;
+      const unsigned char* xr = sm + OFF_X + hh * CBOX;
+      unsigned char* xw = sm + OFF_XP + hh * CBOX;
+#pragma unroll
+      for (int k0 = 0; k0 < 64; k0 += 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(xr + tc::sw128_offset(sidx, k0));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        float v8[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
+          v8[2 * e] = fl.x * f;
+          v8[2 * e + 1] = fl.y * f;
+        }
+        tc::sw128_store8<E>(xw, sidx, k0, v8);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- CB, YI, state update
+    if (tid == 0) {
+      tc::fence_after_sync();
+      const uint32_t idesc = tc::idesc_f16_f32(128, 128);
+      tc::mma_tile(tmem + TM_CB, sbase + OFF_C, CBOX, sbase + OFF_B, CBOX, 2, idesc, false);
+      tc::mma_tile(tmem + TM_YI, sbase + OFF_C, CBOX, sbase + OFF_H16, CBOX, 2, idesc, false);
+      tc::mma_op(tmem + TM_H, tc::Opnd{sbase + OFF_XP, CBOX, true}, tc::Opnd{sbase + OFF_B, CBOX, true},
+                 SQ / 16, tc::idesc_f16_f32(128, 128, true, true), true);
+      tc::commit(&mma_bar);
+    }
+    if (!ssd_cta_wait(&mma_bar, ph_mma, &okf)) { dead = true; break; }
+    ph_mma ^= 1;
+    tc::fence_after_sync();
+    // ---- per head: M_h from CB, then Y[:, 64 head ..] = M_h X_h
+    for (int hh = 0; hh < 2; ++hh) {
+      {
+        const int t = row;  // token row of CB
+        const float ct = cum[hh][t];
+        float cb[32];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int s0 = hf * 64 + q * 32;
+          tc::tmem_ld32(tmem + lane + TM_CB + s0, cb);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int sidx = s0 + e;
+            cb[e] = (sidx <= t && t < n) ? cb[e] * __expf(ct - cum[hh][sidx]) * dts[hh][sidx] : 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            tc::sw128_store8<E>(sm + OFF_M + hf * CBOX, t, q * 32 + e, cb + e);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        tc::mma_op(tmem + TM_Y + hh * 64, tc::Opnd{sbase + OFF_M, CBOX, false},
+                   tc::Opnd{sbase + OFF_X + hh * CBOX, CBOX, true}, SQ / 16,
+                   tc::idesc_f16_f32(128, 64, false, true), false);
+        tc::commit(&mma_bar);
+      }
+      if (!ssd_cta_wait(&mma_bar, ph_mma, &okf)) { dead = true; break; }
+      ph_mma ^= 1;
+      tc::fence_after_sync();
+    }
+    if (dead) break;
+    // ---- outputs: thread = token t (lane), head = column half
+    {
+      const int t = row, hh = hf;
+      const int h = h0 + hh;
+      float yv[32], yi[32];
+      const float et = __expf(cum[hh][t]);
+      const float Dh = p.Dskip[h];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        tc::tmem_ld32(tmem + lane + TM_Y + hh * 64 + q * 32, yv);
+        tc::tmem_ld32(tmem + lane + TM_YI + hh * 64 + q * 32, yi);
+        tc::tmem_wait_ld();
+        if (t < n) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float o2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int pp = q * 32 + e + u;
+              const __half xh = *reinterpret_cast<const __half*>(
+                  sm + OFF_X + hh * CBOX + tc::sw128_offset(t, pp));
+              o2[u] = yv[e + u] + et * yi[e + u] + Dh * __half2float(xh);
+            }
+            w[e / 2] = tc::pack2(o2[0], o2[1], (__nv_bfloat16*)nullptr);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(yout + ((size_t)(r0 + t) * H + h) * SP + q * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();  // generic accesses of the tiles before the next TMA writes
+    tc::fence_before_sync();
+    __syncthreads();  // every read of this chunk's tiles is done before the next loads
+  }
+
+  if (!dead) {
+    // ---- final state (row = (head, p), this half's columns)
+    float hv[32];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int n0 = hf * 64 + q * 32;
+      tc::tmem_ld32(tmem + lane + TM_H + n0, hv);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) S_w[((size_t)(h0 + rhead) * SP + rp) * SN + n0 + e] = hv[e];
+    }
+  } else if (tid == 0) {
+    atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+  }
+  if (!(amax <= kCF16Max)) atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_RANGE);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+}
+
+// Conv + SiLU of every prefill token into the fp16 scratch xs [T][C]: one
+// thread per (sequence, channel), the K-1 window in registers.
+__global__ void __launch_bounds__(256) ssd_prep_kernel(SsdParams p, __half* xs) {
+  pdl_wait_then_release();
+  const int n_pre = p.work.header()[kNPre];
+  if ((int)blockIdx.x >= n_pre) return;
+  const int s = p.work.pre()[blockIdx.x];
+  const int ch = blockIdx.y * blockDim.x + threadIdx.x;
+  const int C = p.C, K = p.K;
+  if (ch >= C) return;
+  const int seq0 = p.cu[s];
+  const int L = p.cu[s + 1] - seq0;
+  const int rblk = p.has_past[s] ? p.blk[s] : 0;
+  const __nv_bfloat16* tail = reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
+  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.xbc);
+  const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
+  float win[kMaxConvK - 1], wc[kMaxConvK];
+#pragma unroll
+  for (int j = 0; j < kMaxConvK - 1; ++j)
+    win[j] = j < K - 1 ? __bfloat162float(tail[(size_t)j * C + ch]) : 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxConvK; ++j) wc[j] = j < K ? __bfloat162float(w[(size_t)ch * K + j]) : 0.f;
+  for (int t = 0; t < L; ++t) {
+    const float xv = __bfloat162float(x[(size_t)(seq0 + t) * C + ch]);
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxConvK; ++j) {
+      if (j < K - 1) acc += wc[j] * win[j];
+      else if (j == K - 1) acc += wc[j] * xv;
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxConvK - 1; ++j) {
+      if (j < K - 2) win[j] = win[j + 1];
+      else if (j == K - 2) win[j] = xv;
+    }
+    xs[(size_t)(seq0 + t) * C + ch] = __float2half_rn(silu_f32(acc));
+  }
+}
+
+
+typedef CUresult (*SsdEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Tensor map of the fp16 scratch [rows][cols] in boxes of 64 columns x 128
+// rows, 128-byte swizzled, zero fill outside.
+cudaError_t ssd_scratch_map(CUtensorMap* m, const void* base, int rows, int cols) {
+  static SsdEncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<SsdEncodeFn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 }  // namespace
 
 bool ssd_decode_supported(int H, int P, int NS, int G, int K, int act) {
@@ -465,6 +841,30 @@ cudaError_t launch_ssd(const SsdParams& p, int P, int NS, int act, int max_items
                    : launch_by_state<64, float>(p, NS, max_items, long_only, stream);
   return P == 32 ? launch_by_state<32, __nv_bfloat16>(p, NS, max_items, long_only, stream)
                  : launch_by_state<64, __nv_bfloat16>(p, NS, max_items, long_only, stream);
+}
+
+bool ssd_chunk_supported(int H, int P, int NS, int K, int act) {
+  return P == SP && NS == SN && act == GDN_BF16 && H % 2 == 0 && K <= kMaxConvK;
+}
+
+cudaError_t launch_ssd_chunk(const SsdParams& p, void* xs, int max_pre, cudaStream_t stream) {
+  if (max_pre <= 0) return cudaSuccess;
+  CUtensorMap m;
+  cudaError_t e = ssd_scratch_map(&m, xs, p.T, p.C);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(ssd_prep_kernel, dim3(max_pre, (p.C + 255) / 256), dim3(256), 0, stream, p,
+                 static_cast<__half*>(xs));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ssd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)CSMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(ssd_chunk_kernel, dim3(max_pre * (p.H / 2)), dim3(kCThreads), CSMEM_BYTES,
+                 stream, p, m);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(ssd_tail_kernel<__nv_bfloat16>, dim3(max_pre, (p.C + 255) / 256), dim3(256), 0,
+                 stream, p, true);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace gdn

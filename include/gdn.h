@@ -146,8 +146,9 @@ int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, voi
  *                    (synchronous; call it before capturing a graph)
  *   max_tokens == 0: free the scratch and never grow it (fused kernel only)
  *   max_tokens < 0 : grow on demand again (the default)
- * Returns GDN_ERR_NOMEM if the allocation fails (the forward still works),
- * GDN_ERR_DIMS for a Mamba2 pool (it has no prefill scratch). */
+ * Returns GDN_ERR_NOMEM if the allocation fails (the forward still works).
+ * For a Mamba2 pool the scratch is the chunked scan's fp16 conv output
+ * (C * 2 bytes per row), with the same three modes. */
 int gdn_state_pool_reserve(gdn_pool_t* pool, int max_tokens);
 
 /* Forward of one gated-delta-net layer over a packed batch.
@@ -248,9 +249,13 @@ int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int nu
  * rules, error flags and stream contract: as gdn_varlen_forward.  The pool
  * must come from gdn_ssd_pool_create (GDN_ERR_DIMS otherwise).  Length-1
  * sequences run on an HBM-streaming decode kernel when P = 64, N = 128,
- * K = 4, bf16 and H/G is 8 or 16; everything else on a token-serial kernel
- * (one CTA per sequence and head, state in registers) followed by the
- * conv-state update.  Never synchronises; graph-capturable. */
+ * K = 4, bf16 and H/G is 8 or 16; at that shape the longer ones run as a
+ * chunked tensor-core scan (128-token chunks) when the pool's scratch holds
+ * the call's T rows (grown on demand like the prefill scratch, see
+ * gdn_state_pool_reserve); everything else on a token-serial kernel (one CTA
+ * per sequence and head, state in registers).  The conv states of the longer
+ * sequences are written by a last kernel.  Never synchronises except for the
+ * one-time scratch growth; graph-capturable once the scratch is reserved. */
 int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const void* dt,
                            const int32_t* cu_seqlens, const int32_t* state_block_idx,
                            const uint8_t* has_past, const gdn_ssd_weights_t* weights, void* y,

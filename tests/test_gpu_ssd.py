@@ -90,3 +90,36 @@ def test_graph_replay_matches_eager():
 def test_bad_block_indices_are_flagged_and_skipped(blocks, flag):
     wl = synth.make_ssd_workload("ssd_bad", TINY, [4, 1, 3], [1, 1, 0], 8, 2, block_idx=blocks)
     check_ssd_against_oracle(wl, expect_flags=flag)
+
+
+FULL = synth.SsdDims(H=16, P=64, N=128, G=2, K=4, act="bf16")
+
+
+@pytest.mark.parametrize("lens,past", [
+    ([128], [0]),                     # exactly one chunk
+    ([129, 1, 40], [1, 1, 0]),        # a second chunk of one token, a decode, a short prefill
+    ([300, 257], [0, 1]),             # three chunks with a partial last one, with a past
+])
+def test_chunked_scan_matches_the_oracle(lens, past):
+    """At P = 64, N = 128, bf16 the prefills run as the chunked tensor-core
+    scan (the scratch grows on the first call)."""
+    wl = synth.make_ssd_workload("ssd_chunked", FULL, lens, past, 16, 11)
+    check_ssd_against_oracle(wl)
+
+
+def test_chunked_and_token_serial_scans_agree():
+    import torch
+
+    from continuous_linear_attention_gb300 import harness
+    wl = synth.make_ssd_workload("ssd_both", FULL, [200, 1, 70], [1, 1, 0], 8, 12)
+    a = harness.SsdDeviceRun(wl)
+    b = harness.SsdDeviceRun(wl)
+    b.pool.reserve(0)  # no scratch: token-serial kernel for the prefills
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    err = (a.y.float() - b.y.float()).norm() / b.y.float().norm()
+    assert float(err) <= 5e-3
+    assert a.pool.error_flags() == 0 and b.pool.error_flags() == 0
+    a.close()
+    b.close()
