@@ -246,6 +246,55 @@ def time_variant_decode(harness, wl, steps, device, pk, nbytes):
             "algorithmic_bytes": nbytes, "error_flags": flags}
 
 
+def ssd_prefill_cost(wl, chunk: int = 128):
+    """Algorithmic HBM bytes and flops of a Mamba2 prefill forward (sequences
+    longer than one token): per token the xbc row read, dt and the y row
+    written; per token and head the chunk form's products (C B^T shared by a
+    group's heads, the masked M X, C h^T and the state step X'^T B)."""
+    d = wl.dims
+    act = 4 if d.act == "f32" else 2
+    toks = sum(L for L in _seqlens(wl) if L > 1)
+    nbytes = toks * (d.C * act + d.H * act + d.H * d.P * act)
+    per_tok_head = (2 * chunk * d.P + 2 * d.N * d.P + 2 * d.P * d.N
+                    + 2 * chunk * d.N / (d.H // d.G))
+    return nbytes, toks * d.H * per_tok_head
+
+
+def _seqlens(wl):
+    cu = wl.cu_seqlens.tolist()
+    return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+
+
+def time_variant_prefill(harness, wl, steps, device, pk):
+    """A Mamba2 prefill batch: tokens/s and both roofline fractions of its
+    compute kernels (the scan is HBM-bound at these sizes)."""
+    import torch
+    run = harness.SsdDeviceRun(wl, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        run.run(stream)
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in kb + ka:
+        e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        run.pool.set_timing_events(kb[i], ka[i])
+        run.run(stream)
+    torch.cuda.synchronize()
+    run.pool.set_timing_events(None, None)
+    kms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(steps))
+    flags = run.pool.error_flags()
+    run.close()
+    nbytes, flops = ssd_prefill_cost(wl)
+    gbs = nbytes / (kms / 1e3) / 1e9
+    tf = flops / (kms / 1e3) / 1e12
+    return {"workload": wl.name, "tokens": wl.T, "compute_kernels_ms": kms,
+            "tokens_per_s": wl.T / (kms / 1e3), "achieved_gbs": gbs,
+            "hbm_frac": gbs / pk["hbm_gbs"], "tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "error_flags": flags}
+
+
 def time_graph(run, steps, hint=0):
     """The same forward captured once in a CUDA graph and replayed: ms per
     replay (the prefill scratch, if any, was grown by earlier calls)."""
@@ -542,9 +591,14 @@ def main():
                                           synth.SsdDims(H=128, P=64, N=128, G=8, K=4,
                                                         act="bf16"),
                                           [1] * 256, [1] * 256, 512, 1)
+            ssd_dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
+            lens = synth.prefill_lengths()
+            ssd_pre = synth.make_ssd_workload("mamba2_prefill_8seq_16k_h128_p64_n128_g8",
+                                              ssd_dims, lens, [0] * len(lens), 64, 2)
             line["variants"] = [
                 time_variant_decode(harness, kda, 200, dev, pk, decode_bytes(kda)),
                 time_variant_decode(harness, ssd, 200, dev, pk, ssd_decode_bytes(ssd)),
+                time_variant_prefill(harness, ssd_pre, 10, dev, pk),
             ]
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, one_thread_s=4.0)

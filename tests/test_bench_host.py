@@ -83,3 +83,14 @@ def test_cpu_baseline_reports_cores_and_one_thread_rate():
     cb = bench.cpu_baseline(wl, budget_s=0.2, one_thread_s=0.1)
     assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["cores"] >= 1
     assert cb["value"] > 0 and cb["value_1_thread"] > 0
+
+
+def test_mamba2_prefill_cost():
+    """Two sequences of 130 and 1 tokens (only the 130-token one counts):
+    bytes 130 x (10240 + 128 + 8192) x 2; flops per token and head
+    2*128*64 + 2*128*64 + 2*64*128 + 2*128*128/16 = 51,200."""
+    dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
+    wl = synth.make_ssd_workload("m", dims, [130, 1], [0, 1], 4, 0)
+    nbytes, flops = bench.ssd_prefill_cost(wl)
+    assert nbytes == 130 * (10240 + 128 + 8192) * 2
+    assert flops == 130 * 128 * 51_200
