@@ -257,3 +257,28 @@ def test_gate_shapes_are_checked():
     bad = dataclasses.replace(wl, dt_bias=wl.dt_bias[:, :1].contiguous())
     with pytest.raises(ValueError):
         oracle.forward(bad)
+
+
+@pytest.mark.parametrize("sub,split", [(16, 8), (16, 16), (32, 8)])
+def test_referenced_intra_blocks_equal_the_pairwise_ones(sub, split):
+    """The operand-rescaling form of A and P (references between sub-chunks
+    and between the halves of a sub-chunk) equals the pairwise definition, on
+    gates strong enough that one whole-chunk factorisation overflows."""
+    n, dk = 64, 16
+    d = _inputs(n, dk, 4, 41)
+    g = d["g"] * 8.0  # about -30 per token and channel: e^{-Gam} overflows fp64 by the end
+    Gam = np.cumsum(g, axis=0)
+    A, P = oracle.kda_intra_blocks(d["qn"], d["kn"], Gam, d["beta"], sub=sub, split=split)
+    Aref = np.zeros((n, n))
+    Pref = np.zeros((n, n))
+    for i in range(n):
+        for j in range(i + 1):
+            f = np.exp(Gam[i] - Gam[j])
+            Pref[i, j] = np.sum(d["qn"][i] * d["kn"][j] * f)
+            if j < i:
+                Aref[i, j] = d["beta"][i] * np.sum(d["kn"][i] * d["kn"][j] * f)
+    np.testing.assert_allclose(A, Aref, rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(P, Pref, rtol=1e-12, atol=1e-300)
+    with np.errstate(over="ignore", invalid="ignore"):
+        whole = (d["kn"] * np.exp(Gam)) @ (d["kn"] * np.exp(-Gam)).T
+    assert not np.isfinite(whole).all()
