@@ -100,8 +100,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_diag_umma_gemm.restype = I
     lib.gdn_diag_umma_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, I, P]
     lib.gdn_diag_umma_gemm_ex.restype = I
-    lib.gdn_diag_umma_issue_timing.argtypes = [I, I, I, P, P]
-    lib.gdn_diag_umma_issue_timing.restype = I
+    lib.gdn_diag_wait_timeout.argtypes = [P, P]
+    lib.gdn_diag_wait_timeout.restype = I
     lib.gdn_status_string.argtypes = [I]
     lib.gdn_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -294,12 +294,10 @@ def diag_umma_gemm_ex(A, B, C, D, operand_f16=False, a_mn=False, b_mn=False,
            "gdn_diag_umma_gemm_ex")
 
 
-def diag_umma_issue_timing(N, a_tmem, reps, out, stream=None) -> None:
-    """gdn_diag_umma_issue_timing: issue / completion cycles of `reps`
-    tcgen05.mma (M=128, K=16, N) into `out` (3 x uint64 device tensor)."""
-    _check(load().gdn_diag_umma_issue_timing(int(N), 1 if a_tmem else 0, int(reps), _ptr(out),
-                                             _stream(stream)),
-           "gdn_diag_umma_issue_timing")
+def diag_wait_timeout(flags, stream=None) -> None:
+    """gdn_diag_wait_timeout: a bounded wait that runs out and ORs
+    GDN_FLAG_TIMEOUT into ``flags`` (a 1-element int32/uint32 CUDA tensor)."""
+    _check(load().gdn_diag_wait_timeout(_ptr(flags), _stream(stream)), "gdn_diag_wait_timeout")
 
 
 def varlen_forward_noalloc(pool_mem, num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align,

@@ -1,6 +1,8 @@
-// Diagnostic tensor-core GEMM (see include/gdn_diag.h): exercises the shared
-// tile layout, descriptors, MMA issue/commit (A from shared or from tensor
-// memory) and TMEM load/store helpers of gdn_tc.cuh on plain matrices.
+// Diagnostic entry points (see include/gdn_diag.h): a tensor-core GEMM that
+// exercises the shared tile layout, descriptors, MMA issue/commit (A from
+// shared or from tensor memory) and TMEM load/store helpers of gdn_tc.cuh on
+// plain matrices, and a wait that must run out, which checks the bounded-wait
+// path that reports GDN_FLAG_TIMEOUT.
 #include <type_traits>
 
 #include "gdn.h"
@@ -119,86 +121,27 @@ diag_umma_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __res
   if (tid < 32) tc::tmem_dealloc(tmem, 512);
 }
 
-// Issue cost of tcgen05.mma: one thread issues `reps` MMAs (M = 128, K = 16,
-// the given N; A from shared or tensor memory; all into one accumulator,
-// operands zero) back to back with precomputed descriptors, then commits.
-// out[0] = clock cycles spent issuing, out[1] = cycles until the commit is
-// observed, out[2] = 1 if it was.
-__global__ void __launch_bounds__(128, 1)
-diag_mma_timing_kernel(unsigned long long* out, int N, int a_tmem, int reps) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+// The bounded wait every kernel of the library uses, run where it must give
+// up: thread 0 waits on an mbarrier that nothing arrives on, with no bulk copy
+// and no MMA in flight, and raises GDN_FLAG_TIMEOUT in *flags when the wait
+// returns unfinished, exactly as the forward kernels report a timeout.
+__global__ void __launch_bounds__(32, 1) diag_wait_timeout_kernel(unsigned* flags) {
   __shared__ uint64_t bar;
-  __shared__ uint32_t tmem_slot;
-  const int tid = threadIdx.x;
-  // A: 128 x 64 K-major (16 KiB) at 0; B: up to 256 x 64 K-major at 16 KiB
-  for (int i = tid; i < (48 * 1024) / 16; i += 128)
-    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0)) atomicOr(flags, GDN_FLAG_TIMEOUT);
   }
-  if (tid < 32) tc::tmem_alloc(&tmem_slot, 512);
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_slot;
-  {
-    // a tensor-memory A of zeros in columns kATmem .. kATmem + 15
-    uint32_t z[16];
-    for (int j = 0; j < 16; ++j) z[j] = 0u;
-    tc::tmem_st16u(tmem + ((uint32_t)(tid & ~31) << 16) + kATmem, z);
-    tc::tmem_wait_st();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (tid == 0) {
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t idesc = tc::idesc_f16_f32(kM, N);
-    uint64_t ad[4], bd[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      ad[s] = tc::opnd_desc(tc::Opnd{sb, 16384u, false}, s);
-      bd[s] = tc::opnd_desc(tc::Opnd{sb + 16384u, 32768u, false}, s);
-    }
-    const unsigned long long t0 = clock64();
-    for (int r = 0; r < reps; r += 8) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (a_tmem) tc::mma_ts(tmem, tmem + kATmem + 8 * (u & 1), bd[u & 3], idesc, 1u);
-        else tc::mma_bf16(tmem, ad[u & 3], bd[u & 3], idesc, 1u);
-      }
-    }
-    const unsigned long long t1 = clock64();
-    tc::commit(&bar);
-    const bool ok = mbar_wait_bounded(&bar, 0);
-    const unsigned long long t2 = clock64();
-    out[0] = t1 - t0;
-    out[1] = t2 - t0;
-    out[2] = ok ? 1ull : 0ull;
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (tid < 32) tc::tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
 }  // namespace gdn
 
-extern "C" int gdn_diag_umma_issue_timing(int N, int a_tmem, int reps, unsigned long long* out,
-                                          void* stream) {
-  if (!out) return GDN_ERR_NULL;
-  if ((N != 16 && N != 32 && N != 64 && N != 128 && N != 256) || (a_tmem != 0 && a_tmem != 1) ||
-      reps < 8 || reps > 4096 || reps % 8 != 0)
-    return GDN_ERR_DIMS;
-  if ((uintptr_t)out & 7) return GDN_ERR_ALIGN;
-  const int smem = 49 * 1024;
-  if (cudaFuncSetAttribute(gdn::diag_mma_timing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  gdn::diag_mma_timing_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(out, N, a_tmem, reps);
+extern "C" int gdn_diag_wait_timeout(uint32_t* flags, void* stream) {
+  if (!flags) return GDN_ERR_NULL;
+  if ((uintptr_t)flags & 3) return GDN_ERR_ALIGN;
+  gdn::diag_wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<unsigned*>(flags));
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -1,5 +1,5 @@
 /*
- * gdn_diag.h -- diagnostic entry point of libgdn, outside the forward path.
+ * gdn_diag.h -- diagnostic entry points of libgdn, outside the forward path.
  *
  * gdn_diag_umma_gemm runs the tensor-core building blocks of the chunked
  * prefill kernels on plain matrices, so a test can check them against a
@@ -23,23 +23,23 @@
  * a_mn == 2 instead places A in tensor memory (row m in lane m, two 16-bit
  * K-elements per 32-bit column, the lower K index in the low half) and issues
  * the MMA form that reads A from there; any K of the list above.  a_mn outside
- * 0..2 or b_mn outside 0..1: GDN_ERR_DIMS.
+ * 0..2 or b_mn outside 0..1: GDN_ERR_DIMS.  (Reference for the chunked
+ * kernels' design: tcgen05, kind::f16, cta_group::1, from the PTX ISA.)
  *
- * gdn_diag_umma_issue_timing measures what one tcgen05.mma costs the thread
- * that issues it: one CTA, one thread issues `reps` MMAs (kind::f16, M = 128,
- * K = 16, the given N; A from shared memory, or from tensor memory when
- * a_tmem != 0; zero operands, one fp32 accumulator) with precomputed
- * descriptors, commits, and waits (bounded) for the commit.  It writes three
- * unsigned 64-bit values to the device array `out`: SM clock cycles spent
- * issuing, cycles until the commit was observed, and 1 if it was (0 on
- * timeout).  N in {16, 32, 64, 128, 256}, a_tmem in {0, 1}, reps a multiple
- * of 8 in [8, 4096]; `out` 8-byte aligned.  Returns GDN_OK or GDN_ERR_NULL /
- * GDN_ERR_DIMS / GDN_ERR_ALIGN / GDN_ERR_CUDA.  Stream-ordered, no
- * synchronisation.  (Reference for the chunked kernels' design: tcgen05,
- * kind::f16, cta_group::1, from the PTX ISA.)
+ * gdn_diag_wait_timeout checks the time-out path of the library's bounded
+ * waits without faulting or hanging anything: one thread waits on an mbarrier
+ * that nothing arrives on (no bulk copy, no MMA in flight) with the same
+ * bounded wait the forward kernels use (about 2 s), and when that wait gives
+ * up it ORs GDN_FLAG_TIMEOUT into the device word *flags, as the forward
+ * kernels do into a layer's error word.  flags: device uint32, 4-byte
+ * aligned.  Returns GDN_OK or GDN_ERR_NULL / GDN_ERR_ALIGN / GDN_ERR_CUDA.
+ * Stream-ordered; the kernel ends by itself after the limit and leaves the
+ * context usable.
  */
 #ifndef GDN_DIAG_H_
 #define GDN_DIAG_H_
+
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -49,7 +49,7 @@ int gdn_diag_umma_gemm(const void* A, const void* B, const float* C, float* D, i
                        int operand_f16, void* stream);
 int gdn_diag_umma_gemm_ex(const void* A, const void* B, const float* C, float* D, int N, int K,
                           int operand_f16, int a_mn, int b_mn, void* stream);
-int gdn_diag_umma_issue_timing(int N, int a_tmem, int reps, unsigned long long* out, void* stream);
+int gdn_diag_wait_timeout(uint32_t* flags, void* stream);
 
 #ifdef __cplusplus
 }

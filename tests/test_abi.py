@@ -26,7 +26,7 @@ def test_every_declared_symbol_is_exported():
     for n in names:
         assert hasattr(lib, n), n
     assert sorted(binding.EXPORTED + ["gdn_diag_umma_gemm", "gdn_diag_umma_gemm_ex",
-                                      "gdn_diag_umma_issue_timing"]) == names
+                                      "gdn_diag_wait_timeout"]) == names
     assert "gdn_kda_varlen_forward" in names and "gdn_ssd_varlen_forward" in names
 
 
@@ -85,15 +85,12 @@ def test_null_arguments_are_rejected_without_device_work():
     assert lib.gdn_state_pool_layout(None, None, None, None, None) == -1
 
 
-def test_mma_timing_arguments_are_checked_on_the_host():
+def test_wait_timeout_arguments_are_checked_on_the_host():
     lib = binding.load()
-    buf = (ctypes.c_ulonglong * 3)()
-    out = ctypes.cast(buf, ctypes.c_void_p)
-    assert lib.gdn_diag_umma_issue_timing(128, 0, 64, None, None) == -1
-    for N, a_tmem, reps in [(96, 0, 64), (128, 2, 64), (128, 0, 12), (128, 0, 0), (128, 0, 8192)]:
-        assert lib.gdn_diag_umma_issue_timing(N, a_tmem, reps, out, None) == -2
-    misaligned = ctypes.c_void_p(ctypes.addressof(buf) + 4)
-    assert lib.gdn_diag_umma_issue_timing(128, 0, 64, misaligned, None) == -4
+    buf = (ctypes.c_uint32 * 2)()
+    assert lib.gdn_diag_wait_timeout(None, None) == -1
+    misaligned = ctypes.c_void_p(ctypes.addressof(buf) + 2)
+    assert lib.gdn_diag_wait_timeout(misaligned, None) == -4
 
 
 @pytest.mark.parametrize("dims", [

@@ -18,6 +18,7 @@ import pytest
 import torch
 import torch.nn.functional as F
 
+import kernel_forms
 import oracle
 from continuous_linear_attention_gb300 import synth
 
@@ -268,7 +269,7 @@ def test_referenced_intra_blocks_equal_the_pairwise_ones(sub, split):
     d = _inputs(n, dk, 4, 41)
     g = d["g"] * 8.0  # about -30 per token and channel: e^{-Gam} overflows fp64 by the end
     Gam = np.cumsum(g, axis=0)
-    A, P = oracle.kda_intra_blocks(d["qn"], d["kn"], Gam, d["beta"], sub=sub, split=split)
+    A, P = kernel_forms.kda_intra_blocks(d["qn"], d["kn"], Gam, d["beta"], sub=sub, split=split)
     Aref = np.zeros((n, n))
     Pref = np.zeros((n, n))
     for i in range(n):

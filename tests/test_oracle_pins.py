@@ -308,3 +308,60 @@ def test_pool_layout_formula():
     lay = oracle.pool_layout(4, 2, 1, 1, 8, 8, 4, 2, block_align=4096)
     assert lay["conv_bytes"] == 144 and lay["rec_off"] == 256 and lay["stride"] == 4096
     assert lay["total"] == 4096 * 8
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_read_pool_states_round_trips_a_hand_built_image(act):
+    """The pool decoder reads back a byte image written element by element in
+    the stated layout ("Continuous batching for linear attention layers": one
+    block per request, each declared state on a 128-byte boundary): conv state
+    [K-1][C] at offset 0, oldest row first; recurrent state at the next
+    128-byte boundary with S_h[v][k] at ((h*d_k + k)*d_v + v)*4; block b of
+    layer l at (l*num_blocks + b)*stride.  The offsets below are worked out
+    by hand for Hk = 1, Hv = 2, d = 8, K = 3 (C = 2*8 + 2*8 = 32 channels):
+    bf16 conv 2*32*2 = 128 bytes -> rec at 128, rec 2*8*8*4 = 512 bytes,
+    block 640 -> stride 1024 with a 1024-byte alignment; f32 conv 256 bytes ->
+    rec at 256, block 768 -> stride 1024.  Every value encodes its own indices
+    (exact in bf16 and fp32), so a transposed state, a swapped row order or a
+    wrong block or layer offset reads a different number."""
+    import struct
+    dims = synth.Dims(Hk=1, Hv=2, dk=8, dv=8, K=3, act=act)
+    nb, nl, align = 3, 2, 1024
+    stride, rec_off = 1024, (128 if act == "bf16" else 256)
+    img = bytearray(stride * nb * nl)
+
+    def conv_val(l, b, r, c):
+        return float(l * 128 + b * 64 + r * 32 + c - 200)
+
+    def rec_val(l, b, h, v, k):
+        return l * 10000.0 + b * 1000.0 + h * 100.0 + v * 10.0 + k + 0.25
+
+    for l in range(nl):
+        for b in range(nb):
+            base = (l * nb + b) * stride
+            for r in range(2):
+                for c in range(32):
+                    val = conv_val(l, b, r, c)
+                    if act == "bf16":
+                        raw = struct.unpack("<I", struct.pack("<f", val))[0] >> 16
+                        struct.pack_into("<H", img, base + (r * 32 + c) * 2, raw)
+                    else:
+                        struct.pack_into("<f", img, base + (r * 32 + c) * 4, val)
+            for h in range(2):
+                for k in range(8):
+                    for v in range(8):
+                        off = base + rec_off + ((h * 8 + k) * 8 + v) * 4
+                        struct.pack_into("<f", img, off, rec_val(l, b, h, v, k))
+    pool = np.frombuffer(bytes(img), dtype=np.uint8)
+    for layer in range(nl):
+        conv, rec = oracle.read_pool_states(pool, layer, [2, 0, 1], dims, nb, nl,
+                                            block_align=align)
+        for i, b in enumerate([2, 0, 1]):
+            for r in range(2):
+                for c in range(32):
+                    assert conv[i, r, c] == conv_val(layer, b, r, c)
+            for h in range(2):
+                for k in range(8):
+                    for v in range(8):
+                        # rec is returned as [h][k][v] = S_h[v][k]
+                        assert rec[i, h, k, v] == rec_val(layer, b, h, v, k)
