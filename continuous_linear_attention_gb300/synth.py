@@ -200,10 +200,11 @@ def tiny_packed(seed: int = 0, slow_decay: bool = False) -> Workload:
 
 
 def decode_batch(seed: int = 1, n_req: int = 256, num_blocks: int = 512,
-                 dims: Dims = FULL_DIMS) -> Workload:
+                 dims: Dims = FULL_DIMS, slow_decay: bool = False) -> Workload:
     """256 requests with one new token each, all with a past, mapped to a
     random permutation of blocks 1..511 of a 512-block pool."""
-    return make_workload(f"decode_{n_req}req", dims, [1] * n_req, [1] * n_req, num_blocks, seed)
+    return make_workload(f"decode_{n_req}req", dims, [1] * n_req, [1] * n_req, num_blocks, seed,
+                         slow_decay=slow_decay)
 
 
 def prefill_lengths(seed: int = 2, n: int = 8, lo: int = 512, hi: int = 4096,
@@ -216,10 +217,12 @@ def prefill_lengths(seed: int = 2, n: int = 8, lo: int = 512, hi: int = 4096,
             return [int(v) for v in lens]
 
 
-def packed_prefill(seed: int = 2, num_blocks: int = 64, dims: Dims = FULL_DIMS) -> Workload:
+def packed_prefill(seed: int = 2, num_blocks: int = 64, dims: Dims = FULL_DIMS,
+                   slow_decay: bool = False) -> Workload:
     """8 sequences, lengths U[512, 4096] totalling ~16k tokens, no past."""
     lens = prefill_lengths(seed)
-    return make_workload("prefill_8seq_16k", dims, lens, [0] * len(lens), num_blocks, seed)
+    return make_workload("prefill_8seq_16k", dims, lens, [0] * len(lens), num_blocks, seed,
+                         slow_decay=slow_decay)
 
 
 def mixed_lengths(seed: int = 3, n_dec: int = 64, n_pre: int = 6, lo: int = 256, hi: int = 2048,
@@ -240,11 +243,13 @@ def mixed_lengths(seed: int = 3, n_dec: int = 64, n_pre: int = 6, lo: int = 256,
     return [lens[i] for i in order]
 
 
-def mixed_batch(seed: int = 3, num_blocks: int = 1024, dims: Dims = FULL_DIMS) -> Workload:
+def mixed_batch(seed: int = 3, num_blocks: int = 1024, dims: Dims = FULL_DIMS,
+                slow_decay: bool = False) -> Workload:
     """64 decode requests + 6 chunked-prefill continuations, all with past,
     8192 tokens, 1024-block pool with random block assignment."""
     lens = mixed_lengths(seed)
-    return make_workload("mixed_64dec_6pre_8k", dims, lens, [1] * len(lens), num_blocks, seed)
+    return make_workload("mixed_64dec_6pre_8k", dims, lens, [1] * len(lens), num_blocks, seed,
+                         slow_decay=slow_decay)
 
 
 def long_context(seed: int = 4, n: int = 4, first: int = 32768, cont: int = 4096,
@@ -274,6 +279,33 @@ def long_context(seed: int = 4, n: int = 4, first: int = 32768, cont: int = 4096
             cu_seqlens=cu, has_past=torch.full((n,), past, dtype=torch.uint8))
 
     return part(0, first, 0, "long_first_32k"), part(first, total, 1, "long_cont_4k"), whole
+
+
+def row_split(wl: Workload, cuts: List[int]):
+    """Split every sequence of ``wl`` at its own cut (tokens of the first
+    part; 0 < cut < length) into two consecutive calls on the same blocks: the
+    first with the workload's own has_past, the second continuing from the
+    states the first leaves (has_past = 1).  Only the batch description and
+    x/a/b change; weights, blocks and the pool contents are the workload's."""
+    cu = wl.cu_seqlens.tolist()
+    parts = []
+    for first in (True, False):
+        rows, lens = [], []
+        for s in range(wl.N):
+            lo, hi = cu[s], cu[s + 1]
+            mid = lo + cuts[s]
+            r = range(lo, mid) if first else range(mid, hi)
+            rows.extend(r)
+            lens.append(len(r))
+        idx = torch.tensor(rows, dtype=torch.int64)
+        ncu = np.zeros(wl.N + 1, dtype=np.int32)
+        ncu[1:] = np.cumsum(lens)
+        hp = wl.has_past.clone() if first else torch.ones(wl.N, dtype=torch.uint8)
+        parts.append(dataclasses.replace(
+            wl, name=wl.name + ("_first" if first else "_cont"), x=wl.x[idx].contiguous(),
+            a=wl.a[idx].contiguous(), b=wl.b[idx].contiguous(),
+            cu_seqlens=torch.from_numpy(ncu), has_past=hp))
+    return parts[0], parts[1]
 
 
 def standard_cases():

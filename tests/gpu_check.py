@@ -1,5 +1,8 @@
 """Helpers of the GPU parity tests: run a workload through the C ABI and
 compare every output with the fp64 oracle."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -9,6 +12,16 @@ from continuous_linear_attention_gb300 import harness
 # Tolerances (relative L2 over a whole tensor): fp32 activations everywhere
 # 1e-5; bf16 activations with fp32 states 5e-3.
 TOL = {"f32": 1e-5, "bf16": 5e-3}
+
+
+def log_errs(errs):
+    """Append the measured errors of the running test to the file named by
+    GDN_PARITY_LOG (one JSON object per line), when that variable is set."""
+    path = os.environ.get("GDN_PARITY_LOG")
+    if path:
+        name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": name, **{k: float(v) for k, v in errs.items()}}) + "\n")
 
 
 def rel_l2(got, ref):
@@ -85,6 +98,7 @@ def check_against_oracle(wl, run=None, seqs=None, tol=None, expect_flags=0, ref=
         wb = written_blocks(wl, skip)
         assert torch.equal(mask_written(before, run, wb), mask_written(after, run, wb)), \
             "bytes outside the written sub-states changed"
+    log_errs(errs)
     assert errs["out"] <= tol and errs["rec"] <= tol, errs
     return errs
 
@@ -129,5 +143,6 @@ def check_ssd_against_oracle(wl, tol=None, expect_flags=0):
             m[o + run.ssm_off: o + run.ssm_off + run.ssm_bytes] = 0
     assert torch.equal(masked_before, masked_after), "bytes outside the written sub-states changed"
     run.close()
+    log_errs(errs)
     assert errs["y"] <= tol and errs["ssm"] <= tol, errs
     return errs
