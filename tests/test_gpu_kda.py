@@ -2,10 +2,7 @@
 through the C ABI (gdn_kda_varlen_forward): the decode kernel on the
 256-request batch, the token-serial kernel on packed prefills and other head
 sizes, and the reduction to the scalar-gate forward when every key channel
-has the same gate.
-
-The kernels behind these cases have not run on a GB300 yet, so the cases are
-collected but skipped until a first run confirms them."""
+has the same gate."""
 import dataclasses
 
 import numpy as np
@@ -14,10 +11,10 @@ import torch
 
 from continuous_linear_attention_gb300 import harness, synth
 
-from gpu_check import check_against_oracle, rel_l2
+import oracle
+from gpu_check import TOL, check_against_oracle, rel_l2
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="KDA kernels not yet run on a GB300")]
+pytestmark = pytest.mark.gpu
 
 
 def _kda(name, dims, lens, past, blocks, seed, slow=False):
@@ -64,9 +61,14 @@ def test_equal_channel_gates_match_the_scalar_forward():
     r1.run()
     r2.run()
     torch.cuda.synchronize()
-    err = rel_l2(r2.out.float().cpu().numpy(), r1.out.float().cpu().numpy())
-    assert err <= 1e-3, err
     assert r1.pool.error_flags() == 0 and r2.pool.error_flags() == 0
+    # the KDA kernels with equal channel gates against the scalar rule's oracle
+    check_against_oracle(base, run=r2, ref=oracle.forward(base))
+    # and against the scalar forward on the GPU: both sides round their outputs
+    # to bf16 on their own (about 1.6e-3 rms apart) and the scalar side's
+    # prefill runs on fp16 tensor-core operands, so the bf16 bar applies
+    err = rel_l2(r2.out.float().cpu().numpy(), r1.out.float().cpu().numpy())
+    assert err <= TOL["bf16"], err
 
 
 def test_decode_hint_and_graph_replay():

@@ -1,18 +1,14 @@
 """GPU parity of the Mamba2 mixer forward (gdn_ssd_varlen_forward) against the
 fp64 oracle, through the C ABI: packed batches of decodes and prefills with
 and without a past, head dims 32 and 64, state sizes 32 to 128, fp32 and bf16
-activations, padding and bad block indices.
-
-The kernels behind these cases have not run on a GB300 yet, so the cases are
-collected but skipped until a first run confirms them."""
+activations, padding and bad block indices."""
 import pytest
 
 from continuous_linear_attention_gb300 import synth
 
 from gpu_check import check_ssd_against_oracle
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="Mamba2 kernels not yet run on a GB300")]
+pytestmark = pytest.mark.gpu
 
 TINY = synth.SsdDims(H=4, P=32, N=32, G=2, K=4, act="f32")
 
