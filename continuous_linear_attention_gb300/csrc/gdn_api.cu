@@ -36,15 +36,14 @@ namespace {
 size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
 // Prefill scratch, one row per packed token, as consecutive token-major arrays
-// (each row a multiple of 16 bytes): q~|k~ of every k-head and v of every
-// v-head (fp16), G and beta of every v-head (fp32), -w and u of every v-head
-// (fp16), the rows of P of every v-head (fp16, 64 each) and one 8-byte record
-// per 64-token chunk (at most one chunk per row).
-enum ScrPart { kScrQK = 0, kScrV, kScrG, kScrW, kScrU, kScrP, kScrC, kScrParts };
+// (each row a multiple of 16 bytes): q~|k~ of every k-head (fp16), G and beta
+// of every v-head (fp32), -w and u of every v-head (fp16), the rows of P of
+// every v-head (fp16, 64 each) and one record per 64-token chunk (at most one
+// chunk per row).
+enum ScrPart { kScrQK = 0, kScrG, kScrW, kScrU, kScrP, kScrC, kScrParts };
 size_t scratch_part_bytes(const gdn_pool* p, int part) {
   switch (part) {
     case kScrQK: return (size_t)2 * p->Hk * p->dk * 2;
-    case kScrV: return (size_t)p->Hv * p->dv * 2;
     case kScrG: return (size_t)p->Hv * 2 * 4;
     case kScrW: return (size_t)p->Hv * p->dk * 2;
     case kScrU: return (size_t)p->Hv * p->dv * 2;
@@ -361,7 +360,6 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
   }
   if (p->scr && p->scr_tokens >= (size_t)T) {
     fp.scr_qk = scratch_part(p, kScrQK);
-    fp.scr_v = scratch_part(p, kScrV);
     fp.scr_g = scratch_part(p, kScrG);
     fp.scr_w = scratch_part(p, kScrW);
     fp.scr_u = scratch_part(p, kScrU);

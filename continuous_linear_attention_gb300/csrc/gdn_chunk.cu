@@ -743,21 +743,19 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     e = launch_pdl(chunk_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p, tmx);
     if (e != cudaSuccess) return e;
   } else {
-    // split: conv prologue and gates (prep_kernel), the state-independent
-    // products of every chunk (intra_kernel), then the recurrence over the
-    // chains (seq_kernel); at most T/64 + (number of prefill sequences) chunks
+    // split: conv, gates and the state-independent products of every chunk
+    // (cintra_kernel), then the recurrence over the chains (seq_kernel); at
+    // most T/64 + (number of prefill sequences) chunks
     const int max_chunks = p.T / CH + max_pre;
-    CUtensorMap tmx, tqk, tv, tw, tu, tp, tg;
+    CUtensorMap tmx, tqk, tw, tu, tp, tg;
     e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
     if (e == cudaSuccess) e = make_map(&tqk, p.scr_qk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hk * 2 * D, CH);
-    if (e == cudaSuccess) e = make_map(&tv, p.scr_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
     if (e == cudaSuccess) e = make_map(&tw, p.scr_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
     if (e == cudaSuccess) e = make_map(&tu, p.scr_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
     if (e == cudaSuccess) e = make_map(&tp, p.scr_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * CH, CH);
     if (e == cudaSuccess) e = make_map_gates(&tg, p.scr_g, p.T, p.Hv * 2);
     if (e != cudaSuccess) return e;
-    e = launch_prep(p, &tmx, max_chunks, stream);
-    if (e == cudaSuccess) e = launch_intra(p, &tqk, &tv, &tg, max_chunks, stream);
+    e = launch_cintra(p, &tmx, max_chunks, stream);
     const void* maps[5] = {&tqk, &tw, &tu, &tp, &tg};
     if (e == cudaSuccess) e = launch_seq(p, maps, grid, stream);
     if (e != cudaSuccess) return e;

@@ -1,0 +1,743 @@
+// Conv prologue and state-independent chunk products of the prefill path in
+// one kernel, fully parallel over the 64-token chunks of the prefill
+// sequences: one CTA per (chunk, k-head), both v-heads of the k-head at once,
+// two CTAs per SM.
+//
+// Per chunk (rows past the sequence end count as zero tokens), following
+// "Continuous batching for linear attention layers" (a varlen causal
+// convolution continues every sequence from its own conv state; the chunked
+// kernels take the per-sequence states through cu_seqlens) and the chunk-64 WY
+// form of the gated delta rule (Gated Delta Networks, chunkwise form):
+//   conv + SiLU over the k-head's q | k channels and its two v-heads' v
+//     channels, continued from the conv state on the first chunk; L2 norms of
+//     q and k (q also scaled by 1/sqrt(d_k)): q~, k~, v
+//   gates of both v-heads: g = -e^{A_log} softplus(a + dt_bias), beta =
+//     sigmoid(b), G the inclusive cumulative sum of g inside the chunk
+//   X = [q~ ; k~] k~^T                               (tcgen05, once for both heads)
+//   per head:  A_ij = beta_i e^{G_i - G_j} (k~_i . k~_j)  (j < i)
+//              P_ij = e^{G_i - G_j} (q~_i . k~_j)          (j <= i)
+//              T = (I + A)^{-1}     (16 x 16 diagonal blocks by column
+//                                    substitution, off-diagonal blocks on
+//                                    mma.sync with a tf32 head/tail split)
+//   [-w_0 ; -w_1] = [-T_0 diag(beta_0 e^{G_0}) ; -T_1 diag(beta_1 e^{G_1})] k~
+//   u_h = T_h diag(beta_h) v_h                       (tcgen05)
+// and writes, token-major next to each other in the pool's prefill scratch
+// (rows i < n of the chunk only): q~ | k~ of the k-head, (G, beta), -w, u and
+// the row of P of each v-head.  The recurrence kernel reads them as TMA
+// tiles.  The chunk's first row, valid tokens and sequence come from the
+// scheduler's chunk records.
+//
+// The x rows reach shared memory as 2-D TMA boxes of 64 channels x 67 rows
+// (3 halo rows + 64), the conv taps of a box in its padding, in two passes
+// through one 36 KiB staging area: q | k first (whose conv writes the
+// [q~ ; k~] operand tile, so the X product starts while the v boxes load),
+// then the two v-heads (whose conv writes the token-major v tiles the u
+// products read as MN-major operands).  v never goes to HBM.
+#include <cuda.h>
+
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+using E = __half;
+constexpr int D = 128;
+constexpr int CH = 64;
+constexpr int KC = 4;
+constexpr int kThreads = 256;
+constexpr int R = 2;  // v-heads per k-head
+constexpr int XROWS = CH + KC - 1;
+constexpr uint32_t XSUB = 9216;  // one staged box: 72 rows x 128 B, 1024-aligned
+constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
+constexpr uint32_t WS_OFF = XBOX_BYTES;  // the box's 64 channels' taps, bf16 [64][4]
+constexpr uint32_t WS_BYTES = 64 * KC * 2;
+static_assert(WS_OFF + WS_BYTES <= XSUB && WS_OFF % 16 == 0, "taps must fit the box padding");
+constexpr int AP = 68;  // pitch (floats) of the fp32 A / T rows
+constexpr int ZP = 20;  // pitch (floats) of the B blocks of the solve
+constexpr int ZB = 16 * ZP;
+constexpr uint32_t BOX = 8192;         // 64 rows x 128 B
+constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of the 128-row [q~ ; k~] tile
+constexpr float kF16Max = 65000.f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared memory (offsets from a 1024-byte aligned base):
+//   S   staging of 4 x boxes (pass 1: q, q, k, k; pass 2: v0, v0, v1, v1);
+//       then A / T of both heads fp32 [2][64][AP]; then the MMA A tiles
+//       A_w = [-T_0 diag(beta_0 e^G_0) ; -T_1 ...] and A_u = [T_0 diag(beta_0) ;
+//       T_1 ...], fp16 128 rows x 64 K each
+//   QK  [q~ ; k~] fp16, 2 K-blocks x 128 rows (K-major for X, the k~ rows read
+//       MN-major by the w product); once X is done the q~ rows of K-block h
+//       hold head h's B blocks of the solve
+//   V   v0 | v1 fp16 token-major: 4 blocks of 64 channels x 64 tokens
+//       (MN-major B operands of the u products)
+//   gates: G log2 e, beta, -beta e^G of both heads [2][64]
+//   WT  the conv taps of each pass transposed to [box][tap][64 channels], so
+//       that a thread's 8 channels of one tap are one 16-byte load
+constexpr uint32_t OFF_S = 0;
+constexpr uint32_t OFF_AW = OFF_S;
+constexpr uint32_t OFF_AU = OFF_S + 16384;
+constexpr uint32_t OFF_QK = 4 * XSUB;
+constexpr uint32_t OFF_V = OFF_QK + 2 * KB_STRIDE;
+constexpr uint32_t OFF_GH = OFF_V + 4 * BOX;
+constexpr uint32_t OFF_GB = OFF_GH + 512;
+constexpr uint32_t OFF_GBE = OFF_GB + 512;
+constexpr uint32_t OFF_WT = OFF_GBE + 512;  // taps of each pass, bf16 [2 passes][4 boxes][4 taps][64 ch]
+constexpr uint32_t SMEM_BYTES = OFF_WT + 2 * 4 * KC * 64 * 2 + 1024;
+static_assert(2 * CH * AP * 4 <= 4 * XSUB, "A / T of both heads fit the staging area");
+static_assert(6 * ZB * 4 <= BOX, "B blocks of one head fit the q~ rows of a K-block");
+static_assert(OFF_QK % 1024 == 0 && OFF_V % 1024 == 0, "operand tiles on 1024-byte boundaries");
+static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
+constexpr uint32_t TM_COLS = 256;  // X (64 columns), then [-w] (0..127) and u (128..255)
+
+// hardware base-2 exponential and logarithm (MUFU; lg2(0) = -inf, ex2(-inf) = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Packed fp32 pairs: d = a * b + c on both lanes (one fma.rn.f32x2).
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mul2p(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ unsigned long long pack2f(float lo, float hi) {
+  return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+// SiLU of a packed fp32 pair: y sigmoid(y) = y (1/2 + tanh(y/2) / 2), one MUFU
+// operation per value (tanh.approx: absolute error about 2^-11 on tanh, so
+// about |y| 2^-12 on the result, the size of the fp16 rounding that follows)
+__device__ __forceinline__ unsigned long long silu2(unsigned long long y2) {
+  const unsigned long long half2 = pack2f(0.5f, 0.5f);
+  const unsigned long long h2 = mul2p(y2, half2);
+  const unsigned long long t2 = pack2f(tanh_approx(__uint_as_float((uint32_t)h2)),
+                                       tanh_approx(__uint_as_float((uint32_t)(h2 >> 32))));
+  return mul2p(y2, fma2(t2, half2, half2));
+}
+// bf16 pair (low, high halves of a word) -> packed fp32 pair
+__device__ __forceinline__ unsigned long long bf2_to_f2(uint32_t u) {
+  return (unsigned long long)(u << 16) | ((unsigned long long)(u & 0xffff0000u) << 32);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 w;
+  w.x = tc::pack2(v[0], v[1], (E*)nullptr);
+  w.y = tc::pack2(v[2], v[3], (E*)nullptr);
+  w.z = tc::pack2(v[4], v[5], (E*)nullptr);
+  w.w = tc::pack2(v[6], v[7], (E*)nullptr);
+  return w;
+}
+
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
+  if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity) ? 1 : 0;
+  __syncthreads();
+  return *flag != 0;
+}
+
+// ---- 16 x 16 block products of the solve on the warp-level tensor-core path
+// (mma.sync m16n8k8, tf32 inputs, fp32 accumulation), each fp32 operand split
+// into a tf32 head (rounded to nearest) and a tail (the exact remainder, which
+// the tensor core reads truncated to tf32: within 2^-21 of the operand), with
+// the three significant cross products kept (hh + ht + th): fp32-level
+// accuracy.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// A fragment of k-step k0 of a 16 x 16 block X (at xp, pitch px floats, rows
+// 16-byte aligned) by one ldmatrix.x4 (each 8 x 8 16-bit matrix is an 8 x 4
+// block of fp32), split into its tf32 head and tail.
+__device__ __forceinline__ void a_frag(const float* xp, int px, int k0, uint32_t (&ah)[4],
+                                       uint32_t (&al)[4]) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3;
+  const float* rowp = xp + ((mi & 1) * 8 + (lane & 7)) * px + k0 + (mi >> 1) * 4;
+  uint32_t r[4];
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(rowp)));
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = __uint_as_float(r[e]);
+    ah[e] = tf32_rna(a);
+    al[e] = __float_as_uint(a - __uint_as_float(ah[e]));
+  }
+}
+// B fragment Y[k0+t][n0+g], Y[k0+t+4][n0+g] (Y at yp, pitch py), split.
+__device__ __forceinline__ void b_frag(const float* yp, int py, int k0, int n0, uint32_t (&bh)[2],
+                                       uint32_t (&bl)[2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float bf[2] = {yp[(k0 + t) * py + n0 + g], yp[(k0 + t + 4) * py + n0 + g]};
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    bh[e] = tf32_rna(bf[e]);
+    bl[e] = __float_as_uint(bf[e] - __uint_as_float(bh[e]));
+  }
+}
+// acc0 / acc1 (this warp's fragments of the two 16 x 8 halves of a 16 x 16
+// block) += X (16 x 16 at xp) * Y[:, 0..7] / Y[:, 8..15] (Y at yp).
+__device__ __forceinline__ void blk_mma3_pair(float (&acc0)[4], float (&acc1)[4], const float* xp,
+                                              int px, const float* yp, int py) {
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t ah[4], al[4], bh[2], bl[2], bh1[2], bl1[2];
+    a_frag(xp, px, 8 * ks, ah, al);
+    b_frag(yp, py, 8 * ks, 0, bh, bl);
+    b_frag(yp, py, 8 * ks, 8, bh1, bl1);
+    mma_tf32(c0, al, bh);
+    mma_tf32(c1, al, bh1);
+    mma_tf32(c0, ah, bl);
+    mma_tf32(c1, ah, bl1);
+    mma_tf32(acc0, ah, bh);
+    mma_tf32(acc1, ah, bh1);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc0[e] += c0[e];
+    acc1[e] += c1[e];
+  }
+}
+// store a fragment (scaled by s) into a 16 x 16 block at dp (pitch pd), columns n0 ..
+__device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float (&acc)[4],
+                                          float s) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2*>(dp + g * pd + n0 + 2 * t) = make_float2(s * acc[0], s * acc[1]);
+  *reinterpret_cast<float2*>(dp + (g + 8) * pd + n0 + 2 * t) =
+      make_float2(s * acc[2], s * acc[3]);
+}
+// Off-diagonal block (i, j) of T from the B blocks (B_ik = T_ii A_ik at
+// Z + (i(i-1)/2 + k) ZB) and the blocks of T below the diagonal already done:
+// T_ij = -sum_{k=j}^{i-1} B_ik T_kj, stored over A_ij.  One warp.
+__device__ __forceinline__ void level_block(float* AT, const float* Z, int i, int j) {
+  float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k = j; k < i; ++k)
+    blk_mma3_pair(acc0, acc1, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP);
+  blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
+  blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t xbar1, xbar2, mbar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int flag;
+  __shared__ float gtot[R];
+  pdl_wait_then_release();
+  int32_t* hdr = p.work.header();
+  const int n_chunks = hdr[kPreChunks];
+  const int gidx = blockIdx.x;
+  // the chunk's record (scheduler): first packed row, valid tokens, chunk
+  // index inside its sequence, sequence
+  const int4 rec = reinterpret_cast<const int4*>(p.scr_c)[gidx];
+  if (gidx >= n_chunks) return;
+  const int kh = blockIdx.y;
+  const int Hk = p.Hk, Hv = p.Hv, C = p.C;
+  const int row0 = rec.x, n = rec.y, c = rec.z, s = rec.w;
+  const int rblk = (c == 0 && p.has_past[s]) ? p.blk[s] : 0;  // the conv state is read on chunk 0 only
+  const __nv_bfloat16* tail =
+      reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
+  const __nv_bfloat16* wconv = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
+  const int tid = threadIdx.x;
+  const uint32_t sbase = smem_u32(sm);
+  float* GH = reinterpret_cast<float*>(sm + OFF_GH);
+  float* GB = reinterpret_cast<float*>(sm + OFF_GB);
+  float* GBE = reinterpret_cast<float*>(sm + OFF_GBE);
+
+  // global channel of staged box b of pass ps: q | q | k | k, then v of head
+  // 2kh (two boxes) and of head 2kh+1 (two boxes)
+  auto gch = [&](int ps, int b) {
+    return ps == 0 ? (b < 2 ? kh * D + b * 64 : Hk * D + kh * D + (b - 2) * 64)
+                   : 2 * Hk * D + kh * R * D + b * 64;
+  };
+  auto issue_x = [&](int ps, uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, 4u * (XBOX_BYTES + WS_BYTES));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      tma_load_2d(sm + OFF_S + b * XSUB, &tmx, gch(ps, b), row0 - (KC - 1), bar);
+      bulk_g2s(sm + OFF_S + b * XSUB + WS_OFF, wconv + (size_t)gch(ps, b) * KC, WS_BYTES, bar);
+    }
+  };
+  if (tid == 0) {
+    mbar_init(&xbar1, 1);
+    mbar_init(&xbar2, 1);
+    mbar_init(&mbar, 1);
+    fence_mbar_init();
+    issue_x(0, &xbar1);
+  }
+  if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
+
+  // ---- gates of the chunk's tokens for both v-heads (threads 0..127, token
+  // tid % 64 of head 2kh + tid / 64): g, beta and the inclusive cumulative sum
+  // G of g inside the chunk; tokens past the end take g = 0 and beta = 0
+  float gcum = 0.f, gbeta = 0.f;
+  if (tid < R * CH) {
+    const int h = kh * R + (tid >> 6), i = tid & 63;
+    if (i < n) {
+      const size_t row = (size_t)(row0 + i);
+      const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(p.a);
+      const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
+      gcum = -__expf(p.A_log[h]) *
+             softplus_f32(__bfloat162float(av[row * Hv + h]) + p.dt_bias[h]);
+      gbeta = sigmoid_f32(__bfloat162float(bv[row * Hv + h]));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, gcum, o);
+      if ((tid & 31) >= o) gcum += t;
+    }
+    if ((tid & 63) == 31) gtot[tid >> 6] = gcum;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  if (tid < R * CH) {
+    const int hl = tid >> 6, i = tid & 63;
+    if (i >= 32) gcum += gtot[hl];
+    GH[hl * CH + i] = gcum * kLog2e;
+    GB[hl * CH + i] = gbeta;
+    GBE[hl * CH + i] = -gbeta * __expf(gcum);
+    if (i < n) {
+      float2* dst = reinterpret_cast<float2*>(p.scr_g) + (size_t)(row0 + i) * Hv + kh * R + hl;
+      *dst = make_float2(gcum, gbeta);
+    }
+  }
+
+  const int tq = tid >> 4, g = tid & 15;
+  const int i0 = 4 * tq;
+  const float inv_sqrt_d = rsqrtf((float)D);
+  float vmax = 0.f;   // largest |v| (NaN if any is NaN)
+  float amax = 0.f;   // largest |value| entering an fp16 operand or the u / w scratch
+  __half* qk_out = reinterpret_cast<__half*>(p.scr_qk);
+
+  // conv + SiLU of part (0 q, 1 k, 2 v of head 2kh, 3 v of head 2kh+1) for
+  // tokens i0 .. i0+3, channels g*8 .. g*8+7 of the part, from the staged
+  // boxes of the current pass (the part's channels are boxes (part & 1) * 2
+  // and (part & 1) * 2 + 1); q and k L2-normalised over the 16 threads of a
+  // token.  Rows past the sequence end are written as zeros.  conv_load reads
+  // the 7 staged rows and the taps, conv_finish does the arithmetic and the
+  // stores, so that the staging area can be released in between.
+  struct ConvIn {
+    uint4 xw[4 + KC - 1];
+    uint4 wt[KC];
+  };
+  auto conv_load = [&](int part, ConvIn& in) {
+    const int lc = (part & 1) * D + g * 8;  // pass-local channel: box lc / 64, column lc % 64
+    const unsigned char* box = sm + OFF_S + (lc >> 6) * XSUB;
+    const unsigned char* wt = sm + OFF_WT + (part >> 1) * (4 * KC * 128) + (lc >> 6) * (KC * 128) +
+                              (lc & 63) * 2;
+#pragma unroll
+    for (int j = 0; j < KC; ++j) in.wt[j] = *reinterpret_cast<const uint4*>(wt + j * 128);
+#pragma unroll
+    for (int rr = 0; rr < 4 + KC - 1; ++rr)
+      in.xw[rr] = *reinterpret_cast<const uint4*>(box + tc::sw128_offset(i0 + rr, lc & 63));
+  };
+  auto conv_finish = [&](int part, const ConvIn& in) {
+    unsigned long long acc2[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc2[t][e] = 0ull;
+#pragma unroll
+    for (int rr = 0; rr < 4 + KC - 1; ++rr) {
+      const uint4 xw = in.xw[rr];
+      const unsigned long long xv2[4] = {bf2_to_f2(xw.x), bf2_to_f2(xw.y), bf2_to_f2(xw.z),
+                                         bf2_to_f2(xw.w)};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int j = rr - t;
+        if (j >= 0 && j < KC) {
+          const uint32_t wj[4] = {in.wt[j].x, in.wt[j].y, in.wt[j].z, in.wt[j].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc2[t][e] = fma2(bf2_to_f2(wj[e]), xv2[e], acc2[t][e]);
+        }
+      }
+    }
+    float y[4][8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const unsigned long long s2 = silu2(acc2[t][e]);
+        y[t][2 * e] = __uint_as_float((uint32_t)s2);
+        y[t][2 * e + 1] = __uint_as_float((uint32_t)(s2 >> 32));
+      }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = i0 + t;
+      if (part < 2) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss += y[t][e] * y[t][e];
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float sc = rsqrtf(ss + kL2Eps) * (part == 0 ? inv_sqrt_d : 1.f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[t][e] *= sc;
+      } else if (i < n) {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) vmax = max_abs3_nan(vmax, y[t][e], y[t][e + 1]);
+      }
+      const uint4 wv = i < n ? pack8(y[t]) : make_uint4(0, 0, 0, 0);
+      if (part < 2) {
+        // [q~ ; k~] tile: row i (q~) or 64 + i (k~), K-block g / 8
+        *reinterpret_cast<uint4*>(sm + OFF_QK + (g >> 3) * KB_STRIDE +
+                                  tc::sw128_offset(part * CH + i, (g & 7) * 8)) = wv;
+        if (i < n)
+          *reinterpret_cast<uint4*>(qk_out + ((size_t)(row0 + i) * Hk + kh) * (2 * D) + part * D +
+                                    g * 8) = wv;
+      } else {
+        // v tile of head part - 2: token row i, channel block g / 8
+        *reinterpret_cast<uint4*>(sm + OFF_V + (2 * (part - 2) + (g >> 3)) * BOX +
+                                  tc::sw128_offset(i, (g & 7) * 8)) = wv;
+      }
+    }
+  };
+  // after a pass's boxes land: the halo rows of a sequence's first chunk are
+  // its conv state (rows 0..2 of the 4 boxes), and the taps (bf16 [64][4] in
+  // each box's padding) are transposed to [tap][64 channels] (thread = one
+  // channel of one box)
+  auto pass_setup = [&](int ps) {
+    if (c == 0) {
+      for (int t = tid; t < (KC - 1) * 4 * 8; t += kThreads) {
+        const int r = t >> 5, b = (t >> 3) & 3, cc = (t & 7) * 8;
+        *reinterpret_cast<uint4*>(sm + OFF_S + b * XSUB + tc::sw128_offset(r, cc)) =
+            *reinterpret_cast<const uint4*>(tail + (size_t)r * C + gch(ps, b) + cc);
+      }
+    }
+    {
+      const int b = tid >> 6, ch = tid & 63;
+      const uint2 w4 = *reinterpret_cast<const uint2*>(sm + OFF_S + b * XSUB + WS_OFF + ch * KC * 2);
+      __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(sm + OFF_WT + ps * (4 * KC * 128) +
+                                                           b * (KC * 128)) + ch;
+      const uint32_t u[2] = {w4.x, w4.y};
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {
+        const uint16_t hb = (uint16_t)(u[j >> 1] >> (16 * (j & 1)));
+        wt[j * 64] = __ushort_as_bfloat16(hb);
+      }
+    }
+    __syncthreads();
+  };
+
+  bool ok = cta_wait(&xbar1, 0, &flag);
+  if (ok) {
+    pass_setup(0);
+    {
+      ConvIn in;
+      conv_load(0, in);
+      conv_finish(0, in);
+      conv_load(1, in);
+      // every read of the staged q | k boxes is done and the halo writes are
+      // visible to the async proxy: the v boxes come in while k is finished
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) issue_x(1, &xbar2);
+      conv_finish(1, in);
+    }
+    // the [q~ ; k~] operand tile is complete: X product
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_tile(tmem, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
+                   tc::idesc_f16_f32(128, 64), false);
+      tc::commit(&mbar);
+    }
+    ok = cta_wait(&xbar2, 0, &flag);
+  }
+  if (ok) {
+    pass_setup(1);
+    {
+      ConvIn in;
+      conv_load(2, in);
+      conv_finish(2, in);
+      conv_load(3, in);
+      conv_finish(3, in);
+    }
+    tc::fence_proxy_async_smem();  // the v tiles, read by the u products
+    ok = cta_wait(&mbar, 0, &flag);  // X done; every read of the staging area done
+  }
+  float* AT = reinterpret_cast<float*>(sm + OFF_S);  // [2][64][AP]
+  const uint32_t lane = (uint32_t)(tid & 96) << 16;  // TMEM lane quarter of this warp
+  const int r128 = tid & 127;                        // TMEM row of this thread
+  const int hf = tid >> 7;                           // column half of this thread
+  if (ok) {
+    tc::fence_after_sync();
+    // this thread's row of X (q~_i . k~_j for rows < 64, k~_i . k~_j above),
+    // 32 columns j = 32 hf .. 32 hf + 31; both heads' rows of P or A from it
+    float xr[32];
+    tc::tmem_ld32(tmem + lane + hf * 32, xr);
+    tc::tmem_wait_ld();
+    const bool prow = r128 < CH;
+    const int i = r128 & 63, ib = i >> 4;
+    const int lim = prow ? i : i - 1;  // last kept column
+#pragma unroll
+    for (int hl = 0; hl < R; ++hl) {
+      // e^{G_i - G_j} beta_i = 2^{(G_i + lg beta_i) - G_j} in log2 units (beta = 0 gives 0)
+      const float* gh = GH + hl * CH;
+      const float Gi2 = gh[i] + (prow ? 0.f : lg2_approx(GB[hl * CH + i]));
+      float val[32];
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const int jb = 2 * hf + blk;
+        if (jb <= ib) {
+          float g16[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(gh + 16 * jb + 4 * q);
+            g16[4 * q] = t.x; g16[4 * q + 1] = t.y; g16[4 * q + 2] = t.z; g16[4 * q + 3] = t.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = 16 * jb + e;
+            val[blk * 16 + e] = j <= lim ? xr[blk * 16 + e] * ex2_approx(Gi2 - g16[e]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) val[blk * 16 + e] = 0.f;
+        }
+      }
+      if (prow) {
+        // |P_ij| <= |q~_i| |k~_j| <= d^{-1/2}: no fp16 range check needed
+        if (i < n) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
+                                                ((size_t)(row0 + i) * Hv + kh * R + hl) * CH +
+                                                hf * 32);
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(val + g8 * 8);
+        }
+      } else {
+        // (the solve and the operand tiles read only blocks at or left of the diagonal)
+        float* Ar = AT + (hl * CH + i) * AP + hf * 32;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4)
+          if (2 * hf + (j4 >> 2) <= ib)
+            *reinterpret_cast<float4*>(Ar + j4 * 4) =
+                make_float4(val[j4 * 4], val[j4 * 4 + 1], val[j4 * 4 + 2], val[j4 * 4 + 3]);
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- T_h = (I + A_h)^{-1}: diagonal 16 x 16 blocks, one column per
+    // thread (threads 0..127: head, block, column), written over the A blocks
+    {
+      float col[16];
+      const int hl = tid >> 6, b = (tid >> 4) & 3, m = tid & 15;
+      float* Ab = AT + (hl * CH + 16 * b) * AP + 16 * b;
+      if (tid < R * CH) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float a[16];
+#pragma unroll
+          for (int q = 0; q < (r + 3) / 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(Ab + r * AP + 4 * q);
+            a[4 * q] = t.x; a[4 * q + 1] = t.y; a[4 * q + 2] = t.z; a[4 * q + 3] = t.w;
+          }
+          float acc = r == m ? 1.f : 0.f;
+#pragma unroll
+          for (int j = 0; j < r; ++j) acc -= a[j] * col[j];
+          col[r] = acc;
+        }
+      }
+      __syncthreads();
+      if (tid < R * CH) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Ab[r * AP + m] = col[r];
+      }
+    }
+    __syncthreads();
+    // ---- off-diagonal blocks of both heads: B_ij = T_ii A_ij for i > j (the
+    // six B blocks of a head on its four warps), the first level
+    // T_{i,i-1} = -B_{i,i-1} T_{i-1,i-1} right away by the warp that made
+    // B_{i,i-1}; then T_20, T_31 and T_30 (= -sum B_3k T_k0)
+    {
+      const int warp = tid >> 5;
+      const int hl = warp >> 2, wl = warp & 3;
+      float* ATh = AT + hl * CH * AP;
+      float* Z = reinterpret_cast<float*>(sm + OFF_QK + hl * KB_STRIDE);
+#pragma unroll 1
+      for (int bi = wl; bi < 6; bi += 4) {
+        const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
+        const int j = bi - i * (i - 1) / 2;
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        blk_mma3_pair(acc0, acc1, ATh + (16 * i) * AP + 16 * i, AP, ATh + (16 * i) * AP + 16 * j, AP);
+        blk_store(Z + bi * ZB, ZP, 0, acc0, 1.f);
+        blk_store(Z + bi * ZB, ZP, 8, acc1, 1.f);
+        if (j == i - 1) {
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+          blk_mma3_pair(acc0, acc1, Z + bi * ZB, ZP, ATh + (16 * j) * AP + 16 * j, AP);
+          blk_store(ATh + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
+          blk_store(ATh + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
+        }
+      }
+      __syncthreads();
+      if (wl < 2) level_block(ATh, Z, wl + 2, wl);
+      if (wl == 0) {
+        __syncwarp();
+        level_block(ATh, Z, 3, 0);
+      }
+    }
+    __syncthreads();
+    // ---- the MMAs' A tiles over the A / T array once every T value is read:
+    // row 64 hl + i of A_w = -T_hl[i][:] beta_j e^{G_j}, of A_u = T_hl[i][:] beta_j
+    {
+      uint4 wtb[R][2], wtbe[R][2];
+#pragma unroll
+      for (int hl = 0; hl < R; ++hl)
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int idx = tid + kThreads * q2;
+          const int i = idx >> 3, c8 = idx & 7;
+          const bool live = (c8 >> 1) <= (i >> 4);  // an 8-column group at or left of the diagonal
+          const float4 b0 = *reinterpret_cast<const float4*>(GB + hl * CH + c8 * 8);
+          const float4 b1 = *reinterpret_cast<const float4*>(GB + hl * CH + c8 * 8 + 4);
+          const float4 e0 = *reinterpret_cast<const float4*>(GBE + hl * CH + c8 * 8);
+          const float4 e1 = *reinterpret_cast<const float4*>(GBE + hl * CH + c8 * 8 + 4);
+          const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          const float ej[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+          float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0;
+          if (live) {
+            t0 = *reinterpret_cast<const float4*>(AT + (hl * CH + i) * AP + c8 * 8);
+            t1 = *reinterpret_cast<const float4*>(AT + (hl * CH + i) * AP + c8 * 8 + 4);
+          }
+          const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+          float tb[8], tbe[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            tb[e] = tv[e] * bj[e];
+            tbe[e] = tv[e] * ej[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) amax = max_abs3(amax, tb[e], tb[e + 1]);
+          wtb[hl][q2] = pack8(tb);
+          wtbe[hl][q2] = pack8(tbe);
+        }
+      __syncthreads();
+#pragma unroll
+      for (int hl = 0; hl < R; ++hl)
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int idx = tid + kThreads * q2;
+          const int i = idx >> 3, c8 = idx & 7;
+          *reinterpret_cast<uint4*>(sm + OFF_AW + tc::sw128_offset(hl * CH + i, c8 * 8)) =
+              wtbe[hl][q2];
+          *reinterpret_cast<uint4*>(sm + OFF_AU + tc::sw128_offset(hl * CH + i, c8 * 8)) =
+              wtb[hl][q2];
+        }
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    // [-w_0 ; -w_1] = A_w k~ into columns 0..127 (k~ rows of the [q~ ; k~]
+    // tile as an MN-major operand); A_u v_0 into columns 128..255 (rows
+    // 0..63 are u_0)
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_op(tmem, tc::Opnd{sbase + OFF_AW, 0u, false},
+                 tc::Opnd{sbase + OFF_QK + CH * 128, KB_STRIDE, true}, CH / 16,
+                 tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::mma_op(tmem + 128, tc::Opnd{sbase + OFF_AU, 0u, false},
+                 tc::Opnd{sbase + OFF_V, BOX, true}, CH / 16,
+                 tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::commit(&mbar);
+    }
+    ok = cta_wait(&mbar, 1, &flag);
+  }
+  // read out 64 columns (col0 .. col0 + 63) of this thread's TMEM row into
+  // the scratch rows of (token r128 % 64, v-head 2kh + head)
+  auto readout = [&](uint32_t col0, void* base, int head) {
+    const int i = r128 & 63;
+    __half* dstrow = reinterpret_cast<__half*>(base) +
+                     ((size_t)(row0 + i) * Hv + kh * R + head) * D + hf * 64;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float vv[32];
+      tc::tmem_ld32(tmem + lane + col0 + hf * 64 + hh * 32, vv);
+      tc::tmem_wait_ld();
+      float m4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 32; e += 2)
+        m4[(e >> 1) & 3] = max_abs3(m4[(e >> 1) & 3], vv[e], vv[e + 1]);
+      amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+      if (i < n) {
+        uint4* dst = reinterpret_cast<uint4*>(dstrow + hh * 32);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(vv + g8 * 8);
+      }
+    }
+  };
+  if (ok) {
+    tc::fence_after_sync();
+    readout(0, p.scr_w, r128 >> 6);            // -w of both heads
+    if (r128 < CH) readout(128, p.scr_u, 0);   // u_0 (warp-uniform: lane quarters 0, 1)
+    tc::fence_before_sync();
+    __syncthreads();
+    // A_u v_1 into columns 0..127 (rows 64..127 are u_1)
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_op(tmem, tc::Opnd{sbase + OFF_AU, 0u, false},
+                 tc::Opnd{sbase + OFF_V + 2 * BOX, BOX, true}, CH / 16,
+                 tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::commit(&mbar);
+    }
+    ok = cta_wait(&mbar, 0, &flag);
+    if (ok) {
+      tc::fence_after_sync();
+      if (r128 >= CH) readout(0, p.scr_u, 1);  // u_1 (lane quarters 2, 3)
+    }
+  }
+  if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+  // v, w, u and the operand tiles enter tensor-core operands in fp16
+  if (!(amax <= kF16Max) || !(vmax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks,
+                          cudaStream_t stream) {
+  if (max_chunks <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(cintra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(cintra_kernel, dim3(max_chunks, p.Hk), dim3(kThreads), SMEM_BYTES, stream, p,
+                    *static_cast<const CUtensorMap*>(x_map));
+}
+
+}  // namespace gdn

@@ -67,16 +67,16 @@ struct FwdParams {
   WorkArea work;
   // prefill scratch, token-major over the packed rows; nullptr when the pool
   // has none for this many tokens (the fused chunked kernel is used):
-  //   scr_qk [T][Hk][2][d] fp16  q~ | k~          (prep_kernel)
-  //   scr_v  [T][Hv][d]    fp16  v                (prep_kernel)
-  //   scr_g  [T][Hv][2]    fp32  G (in-chunk cumulative gate), beta (prep_kernel)
-  //   scr_w  [T][Hv][d]    fp16  -w               (intra_kernel)
-  //   scr_u  [T][Hv][d]    fp16  u = T diag(beta) v  (intra_kernel)
-  //   scr_p  [T][Hv][64]   fp16  row of P         (intra_kernel)
-  //   scr_c  [chunks]      int2  (first packed row, valid tokens) of every
-  //                              prefill chunk, by chunk index (prep_kernel)
+  //   scr_qk [T][Hk][2][d] fp16  q~ | k~
+  //   scr_g  [T][Hv][2]    fp32  G (in-chunk cumulative gate), beta
+  //   scr_w  [T][Hv][d]    fp16  -w
+  //   scr_u  [T][Hv][d]    fp16  u = T diag(beta) v
+  //   scr_p  [T][Hv][64]   fp16  row of P
+  //   scr_c  [chunks]      int4  (first packed row, valid tokens, chunk index
+  //                              inside its sequence, sequence) of every
+  //                              prefill chunk, by chunk index (scheduler)
+  // (the rest written by cintra_kernel, read by seq_kernel)
   void* scr_qk = nullptr;
-  void* scr_v = nullptr;
   void* scr_g = nullptr;
   void* scr_w = nullptr;
   void* scr_u = nullptr;
@@ -136,17 +136,13 @@ cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 // update that follows it: d_k = d_v = 128, bf16 activations, K = 4.
 bool chunk_supported(int d, int act, int K);
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
-// The conv prologue of the prefill path as its own kernel, writing the
-// scratch the split chunked kernel reads (max_chunks: host bound on the
-// number of 64-token chunks of the prefill sequences).
-// x_map: the CUtensorMap of x (boxes of 64 channels x 67 rows, 128-byte swizzle).
-cudaError_t launch_prep(const FwdParams& p, const void* x_map, int max_chunks,
-                        cudaStream_t stream);
-// The state-independent products of every prefill chunk (u, -w, P), one CTA
-// per (chunk, k-head).  qk_map, v_map: q~|k~ and v scratch in 64 x 64 boxes;
-// g_map: gate scratch in boxes of 4 floats x 64 rows.
-cudaError_t launch_intra(const FwdParams& p, const void* qk_map, const void* v_map,
-                         const void* g_map, int max_chunks, cudaStream_t stream);
+// Conv, gates and the state-independent products of every prefill chunk, one
+// CTA per (64-token chunk, k-head), writing the scratch the recurrence kernel
+// reads (max_chunks: host bound on the number of 64-token chunks of the
+// prefill sequences).  x_map: the CUtensorMap of x (boxes of 64 channels x 67
+// rows, 128-byte swizzle).
+cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks,
+                          cudaStream_t stream);
 // The state recurrence over the prefill chains; maps: q~|k~, -w, u, P (64 x 64
 // fp16 boxes) and gates.
 cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cudaStream_t stream);

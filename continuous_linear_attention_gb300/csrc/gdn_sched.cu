@@ -9,7 +9,9 @@
 // and writes:
 //   items[] all active sequences, dec[] the length-1 ones, pre[] the longer
 //   ones sorted longest first (ties by sequence id), their counts and the
-//   total prefill tokens, and resets the persistent-kernel work counter.
+//   total prefill tokens, the 64-token chunk prefix over the sorted prefill
+//   list and (with prefill scratch) one record per chunk, and resets the
+//   persistent-kernel work counter.
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -20,7 +22,7 @@ constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
 schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk, int N, int T,
-                int num_blocks, int hint, WorkArea work) {
+                int num_blocks, int hint, WorkArea work, int4* __restrict__ chunk_rec) {
   __shared__ int s_bad;
   __shared__ int s_n_items, s_n_dec, s_n_pre, s_pre_tokens;
   __shared__ unsigned s_flags;
@@ -111,6 +113,24 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     pre_cp[k] = acc;
   }
   __syncthreads();
+  // one record per 64-token prefill chunk, by chunk index (when the caller
+  // has room for them): (first packed row, valid tokens, chunk index inside
+  // its sequence, sequence)
+  if (chunk_rec) {
+    const int total = pre_cp[n_pre];
+    for (int g = tid; g < total; g += kSchedThreads) {
+      int lo = 0, hi = n_pre - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre_cp[mid] <= g) lo = mid; else hi = mid - 1;
+      }
+      const int s = pre[lo];
+      const int c = g - pre_cp[lo];
+      const int seq0 = cu[s];
+      const int L = cu[s + 1] - seq0;
+      chunk_rec[g] = make_int4(seq0 + 64 * c, min(64, L - 64 * c), c, s);
+    }
+  }
   if (tid == 0) {
     if (s_flags) atomicOr((unsigned*)&hdr[kErr], s_flags);
     hdr[kPreChunks] = pre_cp[n_pre];
@@ -126,7 +146,8 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
 
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream) {
   schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p.cu, p.blk, p.N, p.T, p.num_blocks,
-                                                   p.max_seqlen_hint, p.work);
+                                                   p.max_seqlen_hint, p.work,
+                                                   static_cast<int4*>(p.scr_c));
   return cudaGetLastError();
 }
 
