@@ -41,8 +41,11 @@ EXPORTED = [
     "gdn_ssd_varlen_forward",
     "gdn_get_error",
     "gdn_pool_set_timing_events",
+    "gdn_pool_last_prefill_path",
     "gdn_status_string",
 ]
+
+PREFILL_NONE, PREFILL_SPLIT, PREFILL_FUSED, PREFILL_SERIAL = 0, 1, 2, 3
 
 
 class GdnError(RuntimeError):
@@ -96,6 +99,7 @@ def load() -> ctypes.CDLL:
         ctypes.POINTER(Weights), P, I, I, I, P, P]
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
+    lib.gdn_pool_last_prefill_path.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
     lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, I, P]
     lib.gdn_diag_umma_gemm.restype = I
     lib.gdn_diag_umma_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, I, P]
@@ -206,6 +210,13 @@ class Pool:
         """gdn_state_pool_reserve: > 0 grow the prefill scratch now, 0 free it
         and use the fused prefill kernel only, < 0 grow on demand."""
         _check(load().gdn_state_pool_reserve(self.handle, max_tokens), "gdn_state_pool_reserve")
+
+    def last_prefill_path(self) -> int:
+        """gdn_pool_last_prefill_path: PREFILL_NONE / SPLIT / FUSED / SERIAL."""
+        v = ctypes.c_int()
+        _check(load().gdn_pool_last_prefill_path(self.handle, ctypes.byref(v)),
+               "gdn_pool_last_prefill_path")
+        return v.value
 
     def copy_block(self, layer, src, dst, stream=None):
         _check(load().gdn_state_pool_copy_block(self.handle, layer, src, dst, _stream(stream)),

@@ -21,10 +21,13 @@ struct gdn_pool {
   int device;
   int32_t* work;  // num_layers * WorkArea::words(num_blocks) words
   cudaEvent_t ev_before, ev_after;  // optional timing events (caller-owned)
-  // prefill scratch (fp16 q~|k~ and v of every packed row), grown on demand
+  // prefill scratch: chunk-major tiles of the split prefill path (gated delta
+  // net pools, capacity in 64-token chunks) or the fp16 conv output of the
+  // chunked scan (Mamba2 pools, capacity in tokens); allocated stream-ordered
   unsigned char* scr;
-  size_t scr_tokens;
+  size_t scr_units;
   bool scr_grow;  // false: never allocated; the fused chunked kernel is used
+  int last_path;  // GDN_PREFILL_* of the last forward
   // 0: gated delta net pool (conv + recurrent state); 1: Mamba2 pool (conv +
   // SSM state [H][P][N] at rec_off), with its dimensions
   int kind;
@@ -35,50 +38,83 @@ namespace {
 
 size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
-// Prefill scratch, one row per packed token, as consecutive token-major arrays
-// (each row a multiple of 16 bytes): q~|k~ of every k-head (fp16), G and beta
-// of every v-head (fp32), -w and u of every v-head (fp16), the rows of P of
-// every v-head (fp16, 64 each) and one record per 64-token chunk (at most one
-// chunk per row).
+// Prefill scratch of a gated delta net pool, chunk-major: for every 64-token
+// chunk of the call's prefill sequences (by the scheduler's chunk index) the
+// tiles the recurrence kernel loads, each in the 128-byte-swizzled shared
+// memory layout of its MMA operand, so both kernels move them with plain bulk
+// copies:
+//   QK [chunk][Hk]  the [q~ ; k~] tile: 2 K-blocks x (64 q~ rows, 64 k~ rows) fp16
+//   G  [chunk][Hk]  (G, beta) of the k-head's two v-heads per token, fp32 [64][4]
+//   W  [chunk][Hv]  -w: 2 boxes of 64 channels x 64 tokens fp16
+//   U  [chunk][Hv]  u:  2 boxes of 64 channels x 64 tokens fp16
+//   P  [chunk][Hv]  P:  64 x 64 fp16
+//   C  [chunk]      record (first packed row, valid tokens, chunk index, sequence)
 enum ScrPart { kScrQK = 0, kScrG, kScrW, kScrU, kScrP, kScrC, kScrParts };
 size_t scratch_part_bytes(const gdn_pool* p, int part) {
   switch (part) {
-    case kScrQK: return (size_t)2 * p->Hk * p->dk * 2;
-    case kScrG: return (size_t)p->Hv * 2 * 4;
-    case kScrW: return (size_t)p->Hv * p->dk * 2;
-    case kScrU: return (size_t)p->Hv * p->dv * 2;
+    case kScrQK: return (size_t)p->Hk * 64 * 2 * p->dk * 2;
+    case kScrG: return (size_t)p->Hk * 64 * 4 * 4;
+    case kScrW: return (size_t)p->Hv * 64 * p->dk * 2;
+    case kScrU: return (size_t)p->Hv * 64 * p->dv * 2;
     case kScrC: return 16;
-    default: return (size_t)p->Hv * 64 * 2;
+    default: return (size_t)p->Hv * 64 * 64 * 2;
   }
 }
-size_t scratch_row_bytes(const gdn_pool* p) {
+// Bytes of one scratch unit: a 64-token chunk (gated delta net pools) or one
+// token row of C fp16 channels (Mamba2 pools).
+size_t scratch_unit_bytes(const gdn_pool* p) {
+  if (p->kind != 0) return ((size_t)p->ssd_H * p->ssd_P + 2 * (size_t)p->ssd_G * p->ssd_N) * 2;
   size_t b = 0;
   for (int i = 0; i < kScrParts; ++i) b += scratch_part_bytes(p, i);
   return b;
 }
+// Units a call with T tokens and N sequences can need: at most T/64 + (number
+// of prefill sequences) chunks, and at most one prefill sequence per
+// non-trash block and per two tokens.
+size_t scratch_units_for(const gdn_pool* p, long long T, long long N) {
+  if (p->kind != 0) return (size_t)T;
+  long long seqs = N < T / 2 ? N : T / 2;
+  if (seqs > p->num_blocks - 1) seqs = p->num_blocks - 1;
+  return (size_t)(T / 64 + seqs + 1);
+}
 void* scratch_part(const gdn_pool* p, int part) {
   size_t off = 0;
   for (int i = 0; i < part; ++i) off += scratch_part_bytes(p, i);
-  return p->scr + off * p->scr_tokens;
+  return p->scr + off * p->scr_units;
 }
 
-// Make the prefill scratch hold `tokens` rows (synchronous; frees the old
-// buffer first, which waits for the device).
-int grow_scratch(gdn_pool* p, size_t tokens) {
-  if (p->scr_tokens >= tokens) return GDN_OK;
-  const size_t cap = roundup(tokens, 4096);
-  if (p->scr) {
-    cudaFree(p->scr);
-    p->scr = nullptr;
-    p->scr_tokens = 0;
-  }
-  if (cudaMalloc((void**)&p->scr, cap * scratch_row_bytes(p)) != cudaSuccess) {
+// Make the scratch hold `units` units, stream-ordered on `s` (the old buffer
+// is freed on the stream after every earlier use of it; nothing waits for the
+// device).  With `sync`, waits for `s` afterwards.
+int scratch_grow(gdn_pool* p, size_t units, cudaStream_t s, bool sync) {
+  if (p->scr_units >= units) return GDN_OK;
+  const size_t cap = roundup(units, p->kind == 0 ? 64 : 4096);
+  void* np = nullptr;
+  if (cudaMallocAsync(&np, cap * scratch_unit_bytes(p), s) != cudaSuccess || !np) {
     cudaGetLastError();
-    p->scr = nullptr;
     return GDN_ERR_NOMEM;
   }
-  p->scr_tokens = cap;
+  if (p->scr) cudaFreeAsync(p->scr, s);
+  p->scr = (unsigned char*)np;
+  p->scr_units = cap;
+  if (sync && cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;
+}
+void scratch_release(gdn_pool* p) {
+  if (p->scr) {
+    cudaFreeAsync(p->scr, 0);
+    cudaStreamSynchronize(0);
+  }
+  p->scr = nullptr;
+  p->scr_units = 0;
+}
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return true;  // unknown: do not allocate
+  }
+  return cs != cudaStreamCaptureStatusNone;
 }
 
 bool is_pow2(size_t v) { return v && !(v & (v - 1)); }
@@ -118,26 +154,6 @@ Layout layout_of(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv,
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-// Mamba2 pools: the chunked scan's fp16 conv output, one row of C per packed
-// token (synchronous; frees the old buffer first, which waits for the device).
-int ssd_grow_scratch(gdn_pool* p, size_t tokens) {
-  if (p->scr_tokens >= tokens) return GDN_OK;
-  const size_t cap = roundup(tokens, 4096);
-  const size_t C = (size_t)p->ssd_H * p->ssd_P + 2 * (size_t)p->ssd_G * p->ssd_N;
-  if (p->scr) {
-    cudaFree(p->scr);
-    p->scr = nullptr;
-    p->scr_tokens = 0;
-  }
-  if (cudaMalloc((void**)&p->scr, cap * C * 2) != cudaSuccess) {
-    cudaGetLastError();
-    p->scr = nullptr;
-    return GDN_ERR_NOMEM;
-  }
-  p->scr_tokens = cap;
-  return GDN_OK;
-}
 
 // Mamba2 pools: conv state [K-1][C] (C = H*P + 2*G*N, activation dtype) at 0,
 // SSM state [H][P][N] fp32 at the next 128-byte boundary.
@@ -222,8 +238,9 @@ int gdn_state_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int 
   p->K = K;
   p->act = act;
   p->scr = nullptr;
-  p->scr_tokens = 0;
+  p->scr_units = 0;
   p->scr_grow = true;
+  p->last_path = GDN_PREFILL_NONE;
   p->stride = l.stride;
   p->conv_off = l.conv_off;
   p->rec_off = l.rec_off;
@@ -271,7 +288,7 @@ int gdn_state_pool_destroy(gdn_pool_t* p) {
   cudaDeviceSynchronize();
   if (p->owns) cudaFree(p->base);
   cudaFree(p->work);
-  if (p->scr) cudaFree(p->scr);
+  scratch_release(p);
   if (prev >= 0) cudaSetDevice(prev);
   delete p;
   return GDN_OK;
@@ -348,17 +365,15 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
   fp.work.num_blocks = p->num_blocks;
 
   cudaStream_t s = (cudaStream_t)stream;
-  // prefill scratch for the split conv/chunk kernels: grown on demand outside
-  // stream capture; without it the fused chunked kernel runs
-  if (p->scr_grow && (size_t)T > p->scr_tokens && T > 1 && max_seqlen_hint != 1 &&
-      gdn::chunk_supported(p->dk, p->act, p->K)) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
-      grow_scratch(p, (size_t)T);
-    else
-      cudaGetLastError();
-  }
-  if (p->scr && p->scr_tokens >= (size_t)T) {
+  // prefill scratch of the split path: grown on demand, stream-ordered,
+  // outside stream capture; without enough of it the fused chunked kernel runs
+  const bool chunked = gdn::decode_supported(p->dk, p->act, p->Hk, p->Hv, p->K) &&
+                       gdn::chunk_supported(p->dk, p->act, p->K);
+  const bool may_prefill = T > 1 && max_seqlen_hint != 1;
+  const size_t need = scratch_units_for(p, T, N);
+  if (chunked && may_prefill && p->scr_grow && need > p->scr_units && !capturing(s))
+    scratch_grow(p, need, s, false);
+  if (chunked && may_prefill && p->scr && p->scr_units >= need) {
     fp.scr_qk = scratch_part(p, kScrQK);
     fp.scr_g = scratch_part(p, kScrG);
     fp.scr_w = scratch_part(p, kScrW);
@@ -366,6 +381,10 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
     fp.scr_p = scratch_part(p, kScrP);
     fp.scr_c = scratch_part(p, kScrC);
   }
+  p->last_path = !may_prefill ? GDN_PREFILL_NONE
+                 : !chunked   ? GDN_PREFILL_SERIAL
+                 : fp.scr_qk  ? GDN_PREFILL_SPLIT
+                              : GDN_PREFILL_FUSED;
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (T == 0) {
@@ -397,44 +416,25 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
 
 int gdn_state_pool_reserve(gdn_pool_t* p, int max_tokens) {
   if (!p) return GDN_ERR_NULL;
-  if (p->kind != 0) {
-    // Mamba2 pool: the chunked scan's fp16 conv scratch
-    int prev_dev = -1;
-    cudaGetDevice(&prev_dev);
-    if (prev_dev != p->device) return GDN_ERR_DEVICE;
-    if (max_tokens > 0) {
-      p->scr_grow = true;
-      return ssd_grow_scratch(p, (size_t)max_tokens);
-    }
-    if (max_tokens == 0) {
-      if (p->scr) {
-        cudaFree(p->scr);
-        p->scr = nullptr;
-      }
-      p->scr_tokens = 0;
-      p->scr_grow = false;
-      return GDN_OK;
-    }
-    p->scr_grow = true;
-    return GDN_OK;
-  }
   int prev = -1;
   cudaGetDevice(&prev);
   if (prev != p->device) return GDN_ERR_DEVICE;
   if (max_tokens > 0) {
     p->scr_grow = true;
-    return grow_scratch(p, (size_t)max_tokens);
+    return scratch_grow(p, scratch_units_for(p, max_tokens, max_tokens), 0, true);
   }
   if (max_tokens == 0) {
-    if (p->scr) {
-      cudaFree(p->scr);
-      p->scr = nullptr;
-    }
-    p->scr_tokens = 0;
+    scratch_release(p);
     p->scr_grow = false;
     return GDN_OK;
   }
   p->scr_grow = true;
+  return GDN_OK;
+}
+
+int gdn_pool_last_prefill_path(const gdn_pool_t* p, int* path) {
+  if (!p || !path) return GDN_ERR_NULL;
+  *path = p->last_path;
   return GDN_OK;
 }
 
@@ -576,8 +576,9 @@ int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int H,
   p->K = K;
   p->act = act;
   p->scr = nullptr;
-  p->scr_tokens = 0;
+  p->scr_units = 0;
   p->scr_grow = true;  // the chunked scan's fp16 conv scratch, grown on demand
+  p->last_path = GDN_PREFILL_NONE;
   p->stride = l.stride;
   p->conv_off = l.conv_off;
   p->rec_off = l.rec_off;
@@ -673,15 +674,11 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
   fp.work = sp.work;
 
   cudaStream_t s = (cudaStream_t)stream;
-  // fp16 conv scratch of the chunked scan: grown on demand outside stream capture
-  if (p->scr_grow && (size_t)T > p->scr_tokens && T > 1 && max_seqlen_hint != 1 &&
-      gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act)) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
-      ssd_grow_scratch(p, (size_t)T);
-    else
-      cudaGetLastError();
-  }
+  // fp16 conv scratch of the chunked scan: grown on demand, stream-ordered,
+  // outside stream capture
+  if (p->scr_grow && (size_t)T > p->scr_units && T > 1 && max_seqlen_hint != 1 &&
+      gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act) && !capturing(s))
+    scratch_grow(p, (size_t)T, s, false);
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (T > 0) {
@@ -695,7 +692,7 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
       if (gdn::launch_ssd_decode(sp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
       int max_long = max_items < T / 2 ? max_items : T / 2;
       if (max_seqlen_hint == 1) max_long = 0;
-      const bool chunked = max_long > 0 && p->scr && p->scr_tokens >= (size_t)T &&
+      const bool chunked = max_long > 0 && p->scr && p->scr_units >= (size_t)T &&
                            gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act);
       if (chunked) {
         if (gdn::launch_ssd_chunk(sp, p->scr, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;

@@ -5,8 +5,8 @@
 // 128-byte-swizzled shared tiles, fp32 accumulators in tensor memory).  The
 // recurrent state stays in tensor memory (fp32) for the whole sequence; only
 // the final state is written back.  This single-kernel form runs when the pool
-// has no prefill scratch (see gdn_state_pool_reserve); with scratch, the same
-// computation runs split into prep_kernel, intra_kernel and seq_kernel.
+// has not enough prefill scratch (see gdn_state_pool_reserve); with scratch,
+// the same computation runs split into cintra_kernel and seq_kernel.
 //
 // Persistent CTAs (8 warps, one per SM) pull (sequence, v-head) chains,
 // longest sequences first.
@@ -700,22 +700,6 @@ cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tensor map of the fp32 gate scratch [rows][cols] read in boxes of 4 columns
-// (G and beta of two v-heads, 16 bytes) x 64 rows, unswizzled.
-cudaError_t make_map_gates(CUtensorMap* m, const void* base, int rows, int cols) {
-  EncodeTiledFn encode = encoder();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-  const cuuint32_t box[2] = {4, (cuuint32_t)CH};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 }  // namespace
 
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
@@ -747,17 +731,11 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     // (cintra_kernel), then the recurrence over the chains (seq_kernel); at
     // most T/64 + (number of prefill sequences) chunks
     const int max_chunks = p.T / CH + max_pre;
-    CUtensorMap tmx, tqk, tw, tu, tp, tg;
+    CUtensorMap tmx;
     e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
-    if (e == cudaSuccess) e = make_map(&tqk, p.scr_qk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hk * 2 * D, CH);
-    if (e == cudaSuccess) e = make_map(&tw, p.scr_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
-    if (e == cudaSuccess) e = make_map(&tu, p.scr_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * D, CH);
-    if (e == cudaSuccess) e = make_map(&tp, p.scr_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.T, p.Hv * CH, CH);
-    if (e == cudaSuccess) e = make_map_gates(&tg, p.scr_g, p.T, p.Hv * 2);
     if (e != cudaSuccess) return e;
     e = launch_cintra(p, &tmx, max_chunks, stream);
-    const void* maps[5] = {&tqk, &tw, &tu, &tp, &tg};
-    if (e == cudaSuccess) e = launch_seq(p, maps, grid, stream);
+    if (e == cudaSuccess) e = launch_seq(p, grid, stream);
     if (e != cudaSuccess) return e;
   }
   e = cudaGetLastError();

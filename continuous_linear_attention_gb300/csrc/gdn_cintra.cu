@@ -21,11 +21,14 @@
 //                                    mma.sync with a tf32 head/tail split)
 //   [-w_0 ; -w_1] = [-T_0 diag(beta_0 e^{G_0}) ; -T_1 diag(beta_1 e^{G_1})] k~
 //   u_h = T_h diag(beta_h) v_h                       (tcgen05)
-// and writes, token-major next to each other in the pool's prefill scratch
-// (rows i < n of the chunk only): q~ | k~ of the k-head, (G, beta), -w, u and
-// the row of P of each v-head.  The recurrence kernel reads them as TMA
-// tiles.  The chunk's first row, valid tokens and sequence come from the
-// scheduler's chunk records.
+// and writes to the pool's prefill scratch, chunk-major (by the scheduler's
+// chunk index), the tiles the recurrence kernel loads: the [q~ ; k~] tile of
+// the k-head, (G, beta) of its two v-heads, and -w, u and P of each v-head.
+// Every tile is built in shared memory in the 128-byte-swizzled layout of the
+// MMA operand it becomes and leaves with one bulk copy, so no thread stores
+// scattered rows.  Rows past the sequence end are zero in every tile.  The
+// chunk's first row, valid tokens and sequence come from the scheduler's chunk
+// records.
 //
 // The x rows reach shared memory as 2-D TMA boxes of 64 channels x 67 rows
 // (3 halo rows + 64), the conv taps of a box in its padding, in two passes
@@ -327,10 +330,9 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     GH[hl * CH + i] = gcum * kLog2e;
     GB[hl * CH + i] = gbeta;
     GBE[hl * CH + i] = -gbeta * __expf(gcum);
-    if (i < n) {
-      float2* dst = reinterpret_cast<float2*>(p.scr_g) + (size_t)(row0 + i) * Hv + kh * R + hl;
-      *dst = make_float2(gcum, gbeta);
-    }
+    // the chunk's gate tile of the k-head: [64 tokens][(G, beta) of both heads]
+    reinterpret_cast<float2*>(p.scr_g)[((size_t)gidx * Hk + kh) * (CH * R) + i * R + hl] =
+        make_float2(gcum, gbeta);
   }
 
   const int tq = tid >> 4, g = tid & 15;
@@ -338,7 +340,6 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   const float inv_sqrt_d = rsqrtf((float)D);
   float vmax = 0.f;   // largest |v| (NaN if any is NaN)
   float amax = 0.f;   // largest |value| entering an fp16 operand or the u / w scratch
-  __half* qk_out = reinterpret_cast<__half*>(p.scr_qk);
 
   // conv + SiLU of part (0 q, 1 k, 2 v of head 2kh, 3 v of head 2kh+1) for
   // tokens i0 .. i0+3, channels g*8 .. g*8+7 of the part, from the staged
@@ -413,9 +414,6 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
         // [q~ ; k~] tile: row i (q~) or 64 + i (k~), K-block g / 8
         *reinterpret_cast<uint4*>(sm + OFF_QK + (g >> 3) * KB_STRIDE +
                                   tc::sw128_offset(part * CH + i, (g & 7) * 8)) = wv;
-        if (i < n)
-          *reinterpret_cast<uint4*>(qk_out + ((size_t)(row0 + i) * Hk + kh) * (2 * D) + part * D +
-                                    g * 8) = wv;
       } else {
         // v tile of head part - 2: token row i, channel block g / 8
         *reinterpret_cast<uint4*>(sm + OFF_V + (2 * (part - 2) + (g >> 3)) * BOX +
@@ -474,6 +472,10 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       tc::mma_tile(tmem, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
                    tc::idesc_f16_f32(128, 64), false);
       tc::commit(&mbar);
+      // the [q~ ; k~] tile to the scratch, as the recurrence kernel loads it
+      bulk_s2g(static_cast<unsigned char*>(p.scr_qk) + ((size_t)gidx * Hk + kh) * (2 * KB_STRIDE),
+               sm + OFF_QK, 2 * KB_STRIDE);
+      bulk_commit();
     }
     ok = cta_wait(&xbar2, 0, &flag);
   }
@@ -487,6 +489,8 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       conv_finish(3, in);
     }
     tc::fence_proxy_async_smem();  // the v tiles, read by the u products
+    // the q~ rows take the P tiles next: the [q~ ; k~] store has read them
+    if (tid == 0) bulk_wait_read_all();
     ok = cta_wait(&mbar, 0, &flag);  // X done; every read of the staging area done
   }
   float* AT = reinterpret_cast<float*>(sm + OFF_S);  // [2][64][AP]
@@ -530,14 +534,14 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
         }
       }
       if (prow) {
-        // |P_ij| <= |q~_i| |k~_j| <= d^{-1/2}: no fp16 range check needed
-        if (i < n) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.scr_p) +
-                                                ((size_t)(row0 + i) * Hv + kh * R + hl) * CH +
-                                                hf * 32);
+        // |P_ij| <= |q~_i| |k~_j| <= d^{-1/2}: no fp16 range check needed.
+        // Head hl's P tile [64 i][64 j] (K-major B operand of the output
+        // product) in the q~ rows of K-block hl
+        unsigned char* pt = sm + OFF_QK + hl * KB_STRIDE;
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(val + g8 * 8);
-        }
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(pt + tc::sw128_offset(i, (hf * 4 + g8) * 8)) =
+              pack8(val + g8 * 8);
       } else {
         // (the solve and the operand tiles read only blocks at or left of the diagonal)
         float* Ar = AT + (hl * CH + i) * AP + hf * 32;
@@ -548,8 +552,16 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
                 make_float4(val[j4 * 4], val[j4 * 4 + 1], val[j4 * 4 + 2], val[j4 * 4 + 3]);
       }
     }
+    tc::fence_proxy_async_smem();  // the P tiles
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int hl = 0; hl < R; ++hl)
+        bulk_s2g(static_cast<unsigned char*>(p.scr_p) + ((size_t)gidx * Hv + kh * R + hl) * BOX,
+                 sm + OFF_QK + hl * KB_STRIDE, BOX);
+      bulk_commit();
+    }
     // ---- T_h = (I + A_h)^{-1}: diagonal 16 x 16 blocks, one column per
     // thread (threads 0..127: head, block, column), written over the A blocks
     {
@@ -577,6 +589,8 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
         for (int r = 0; r < 16; ++r) Ab[r * AP + m] = col[r];
       }
     }
+    // the q~ rows take the B blocks next: the P stores have read them
+    if (tid == 0) bulk_wait_read_all();
     __syncthreads();
     // ---- off-diagonal blocks of both heads: B_ij = T_ii A_ij for i > j (the
     // six B blocks of a head on its four warps), the first level
@@ -677,12 +691,12 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     }
     ok = cta_wait(&mbar, 1, &flag);
   }
-  // read out 64 columns (col0 .. col0 + 63) of this thread's TMEM row into
-  // the scratch rows of (token r128 % 64, v-head 2kh + head)
-  auto readout = [&](uint32_t col0, void* base, int head) {
+  // read out 64 columns (col0 .. col0 + 63) of this thread's TMEM row (token
+  // r128 % 64) into row r128 % 64 of box hf of a staged 2-box tile (boxes of
+  // 64 channels x 64 tokens, the layout the recurrence kernel loads)
+  auto readout = [&](uint32_t col0, unsigned char* tile) {
     const int i = r128 & 63;
-    __half* dstrow = reinterpret_cast<__half*>(base) +
-                     ((size_t)(row0 + i) * Hv + kh * R + head) * D + hf * 64;
+    unsigned char* box = tile + hf * BOX;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       float vv[32];
@@ -693,31 +707,46 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       for (int e = 0; e < 32; e += 2)
         m4[(e >> 1) & 3] = max_abs3(m4[(e >> 1) & 3], vv[e], vv[e + 1]);
       amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-      if (i < n) {
-        uint4* dst = reinterpret_cast<uint4*>(dstrow + hh * 32);
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) dst[g8] = pack8(vv + g8 * 8);
-      }
+      for (int g8 = 0; g8 < 4; ++g8)
+        *reinterpret_cast<uint4*>(box + tc::sw128_offset(i, hh * 32 + g8 * 8)) = pack8(vv + g8 * 8);
     }
   };
+  unsigned char* const Wg = static_cast<unsigned char*>(p.scr_w);
+  unsigned char* const Ug = static_cast<unsigned char*>(p.scr_u);
+  const size_t tile0 = ((size_t)gidx * Hv + kh * R) * (2 * BOX);  // head 2kh's tile
   if (ok) {
     tc::fence_after_sync();
-    readout(0, p.scr_w, r128 >> 6);            // -w of both heads
-    if (r128 < CH) readout(128, p.scr_u, 0);   // u_0 (warp-uniform: lane quarters 0, 1)
+    // -w of head r128 / 64 into the [q~ ; k~] area (free: the w product is
+    // done); u_0 (lanes 0..63, warp-uniform) into the A_w tile (free too)
+    readout(0, sm + OFF_QK + (r128 >> 6) * (2 * BOX));
+    if (r128 < CH) readout(128, sm + OFF_AW);
+    tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
-    // A_u v_1 into columns 0..127 (rows 64..127 are u_1)
     if (tid == 0) {
+      // A_u v_1 into columns 0..127 (rows 64..127 are u_1), and the -w and
+      // u_0 tiles to the scratch
       tc::fence_after_sync();
       tc::mma_op(tmem, tc::Opnd{sbase + OFF_AU, 0u, false},
                  tc::Opnd{sbase + OFF_V + 2 * BOX, BOX, true}, CH / 16,
                  tc::idesc_f16_f32(128, 128, false, true), false);
       tc::commit(&mbar);
+      bulk_s2g(Wg + tile0, sm + OFF_QK, 4 * BOX);
+      bulk_s2g(Ug + tile0, sm + OFF_AW, 2 * BOX);
+      bulk_commit();
     }
     ok = cta_wait(&mbar, 0, &flag);
     if (ok) {
+      // u_1 (lanes 64..127) into the v_0 tile (free: the u_0 product is done)
       tc::fence_after_sync();
-      if (r128 >= CH) readout(0, p.scr_u, 1);  // u_1 (lane quarters 2, 3)
+      if (r128 >= CH) readout(0, sm + OFF_V);
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        bulk_s2g(Ug + tile0 + 2 * BOX, sm + OFF_V, 2 * BOX);
+        bulk_commit();
+      }
     }
   }
   if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
@@ -726,6 +755,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   tc::fence_before_sync();
   __syncthreads();
   if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+  if (tid == 0) bulk_wait_all();  // the tiles have reached the scratch before the CTA ends
 }
 
 }  // namespace

@@ -65,17 +65,18 @@ struct FwdParams {
   int T, N, Hk, Hv, C, K, num_blocks;
   int max_seqlen_hint;  // 0 = unknown; else longer sequences are flagged and skipped
   WorkArea work;
-  // prefill scratch, token-major over the packed rows; nullptr when the pool
-  // has none for this many tokens (the fused chunked kernel is used):
-  //   scr_qk [T][Hk][2][d] fp16  q~ | k~
-  //   scr_g  [T][Hv][2]    fp32  G (in-chunk cumulative gate), beta
-  //   scr_w  [T][Hv][d]    fp16  -w
-  //   scr_u  [T][Hv][d]    fp16  u = T diag(beta) v
-  //   scr_p  [T][Hv][64]   fp16  row of P
-  //   scr_c  [chunks]      int4  (first packed row, valid tokens, chunk index
-  //                              inside its sequence, sequence) of every
-  //                              prefill chunk, by chunk index (scheduler)
-  // (the rest written by cintra_kernel, read by seq_kernel)
+  // prefill scratch, chunk-major over the scheduler's 64-token prefill chunks
+  // (chunk index g); nullptr when the pool has not enough of it (the fused
+  // chunked kernel is used).  Every tile is in the 128-byte-swizzled shared
+  // memory layout of the MMA operand it becomes:
+  //   scr_qk [g][Hk] 32 KiB  [q~ ; k~]: 2 K-blocks of (64 q~ rows, 64 k~ rows)
+  //   scr_g  [g][Hk]  1 KiB  fp32 [64 tokens][(G, beta) of the two v-heads]
+  //   scr_w  [g][Hv] 16 KiB  -w: 2 boxes of 64 channels x 64 tokens
+  //   scr_u  [g][Hv] 16 KiB  u = T diag(beta) v, same layout
+  //   scr_p  [g][Hv]  8 KiB  P [64 i][64 j]
+  //   scr_c  [g]     int4    (first packed row, valid tokens, chunk index
+  //                          inside its sequence, sequence) (scheduler)
+  // (the tiles written by cintra_kernel, read by seq_kernel)
   void* scr_qk = nullptr;
   void* scr_g = nullptr;
   void* scr_w = nullptr;
@@ -143,9 +144,9 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
 // rows, 128-byte swizzle).
 cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks,
                           cudaStream_t stream);
-// The state recurrence over the prefill chains; maps: q~|k~, -w, u, P (64 x 64
-// fp16 boxes) and gates.
-cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cudaStream_t stream);
+// The state recurrence over the prefill chains, reading the chunk-major tiles
+// cintra_kernel leaves in the prefill scratch.
+cudaError_t launch_seq(const FwdParams& p, int grid, cudaStream_t stream);
 // The per-channel-decay (KDA) rule: p.a is [T][Hv][d_k] and p.dt_bias
 // [Hv][d_k].  Decode kernel for the shapes decode_supported() accepts, and the
 // token-serial kernel (as launch_recurrent) for everything else.

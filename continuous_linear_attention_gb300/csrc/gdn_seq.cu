@@ -1,7 +1,7 @@
 // State half of the chunked prefill: the recurrence across the 64-token
 // chunks of each (sequence, v-head) chain, with every state-independent
-// product precomputed (q~, k~, gates by prep_kernel; u, -w, P by
-// intra_kernel).  Per chunk, with S0 the state at the chunk start (S[v][k],
+// product precomputed by cintra_kernel (q~, k~, gates, u, -w, P).  Per
+// chunk, with S0 the state at the chunk start (S[v][k],
 // fp32 in tensor memory for the whole chain), G_C the cumulative gate of the
 // chunk's last valid token and n its valid tokens, everything runs in the
 // transposed orientation: tensor-memory lane = v, columns = k or tokens.  One
@@ -27,9 +27,10 @@
 // memory, and every compute warp owns one lane quarter and one column half of
 // each step, so the CUDA-core work spreads over all four SM sub-partitions.
 //
-// Persistent CTAs, one per SM: warp 8 is the producer (one TMA issue lane
-// that pulls chains, longest sequences first, from the scheduler's counter
-// and streams each chunk's tiles into a 3-stage ring), warp 9 issues the
+// Persistent CTAs, one per SM: warp 8 is the producer (one lane that pulls
+// chains, longest sequences first, from the scheduler's counter and
+// bulk-copies each chunk's tiles, chunk-major in the prefill scratch, into a
+// 3-stage ring), warp 9 issues the
 // MMAs when the compute warps release it through named barriers, and warps
 // 0-7 run the chain: thread t owns lane v = t % 128 and column half t / 128.
 #include <cuda.h>
@@ -45,7 +46,7 @@ using E = __half;
 constexpr int D = 128;
 constexpr int CH = 64;
 constexpr int kCompute = 256;
-constexpr int kProducer = kCompute;       // first thread of the TMA warp
+constexpr int kProducer = kCompute;       // first thread of the bulk-copy warp
 constexpr int kIssuer = kCompute + 32;    // first thread of the MMA warp
 constexpr int kThreads = kCompute + 64;
 // named barriers: 1 the compute warps; compute warps -> MMA warp: 5 S0
@@ -122,9 +123,7 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_constant__ CUtensorMap tw,
-           const __grid_constant__ CUtensorMap tu, const __grid_constant__ CUtensorMap tp,
-           const __grid_constant__ CUtensorMap tg) {
+seq_kernel(FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t full[kStages], empty[kStages], mma_y, mma_s;
@@ -260,19 +259,27 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
                          : "memory");
             break;
           }
-          const int kh = h / R, r0 = seq0 + c * CH;
+          // the chunk's tiles, as the chunk-parallel kernel left them
+          // (chunk-major, each in its operand layout): -w and q~ interleaved
+          // by K-block into [-w ; q~], k~, u, P and the gate tile
+          const int kh = h / R;
+          const size_t gi = (size_t)(p.work.pre_cp()[chain / Hv] + c);
+          const unsigned char* qk = static_cast<const unsigned char*>(p.scr_qk) + (gi * p.Hk + kh) * (2 * KB_STRIDE);
+          const unsigned char* wt = static_cast<const unsigned char*>(p.scr_w) + (gi * Hv + h) * (2 * BOX);
+          const unsigned char* ut = static_cast<const unsigned char*>(p.scr_u) + (gi * Hv + h) * (2 * BOX);
+          const unsigned char* pt = static_cast<const unsigned char*>(p.scr_p) + (gi * Hv + h) * BOX;
+          const unsigned char* gt = static_cast<const unsigned char*>(p.scr_g) + (gi * p.Hk + kh) * 1024;
           unsigned char* st = sm + b * ST_BYTES;
           mbar_arrive_expect_tx(&full[b], ST_BYTES);
-          tma_load_2d(st + ST_QW, &tw, h * D, r0, &full[b]);
-          tma_load_2d(st + ST_QW + KB_STRIDE, &tw, h * D + 64, r0, &full[b]);
-          tma_load_2d(st + ST_QW + CH * 128, &tqk, kh * 2 * D, r0, &full[b]);
-          tma_load_2d(st + ST_QW + KB_STRIDE + CH * 128, &tqk, kh * 2 * D + 64, r0, &full[b]);
-          tma_load_2d(st + ST_K, &tqk, kh * 2 * D + D, r0, &full[b]);
-          tma_load_2d(st + ST_K + BOX, &tqk, kh * 2 * D + D + 64, r0, &full[b]);
-          tma_load_2d(st + ST_U, &tu, h * D, r0, &full[b]);
-          tma_load_2d(st + ST_U + BOX, &tu, h * D + 64, r0, &full[b]);
-          tma_load_2d(st + ST_P, &tp, h * CH, r0, &full[b]);
-          tma_load_2d(st + ST_G, &tg, 4 * kh, r0, &full[b]);
+          bulk_g2s(st + ST_QW, wt, BOX, &full[b]);
+          bulk_g2s(st + ST_QW + KB_STRIDE, wt + BOX, BOX, &full[b]);
+          bulk_g2s(st + ST_QW + BOX, qk, BOX, &full[b]);
+          bulk_g2s(st + ST_QW + KB_STRIDE + BOX, qk + KB_STRIDE, BOX, &full[b]);
+          bulk_g2s(st + ST_K, qk + BOX, BOX, &full[b]);
+          bulk_g2s(st + ST_K + BOX, qk + KB_STRIDE + BOX, BOX, &full[b]);
+          bulk_g2s(st + ST_U, ut, 2 * BOX, &full[b]);
+          bulk_g2s(st + ST_P, pt, BOX, &full[b]);
+          bulk_g2s(st + ST_G, gt, 1024, &full[b]);
         }
         if (dead || end) break;
       }
@@ -503,13 +510,11 @@ seq_kernel(FwdParams p, const __grid_constant__ CUtensorMap tqk, const __grid_co
 
 }  // namespace
 
-cudaError_t launch_seq(const FwdParams& p, const void* const* maps, int grid, cudaStream_t stream) {
+cudaError_t launch_seq(const FwdParams& p, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  auto m = [&](int i) { return *static_cast<const CUtensorMap*>(maps[i]); };
-  return launch_pdl(seq_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p, m(0), m(1), m(2),
-                    m(3), m(4));
+  return launch_pdl(seq_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p);
 }
 
 }  // namespace gdn

@@ -131,24 +131,29 @@ int gdn_state_pool_layout(const gdn_pool_t* pool, size_t* block_stride, size_t* 
  * and never shared).  dst must not be 0 (the trash block).  Stream-ordered. */
 int gdn_state_pool_copy_block(gdn_pool_t* pool, int layer, int src, int dst, void* stream);
 
-/* Prefill scratch of the pool.  Sequences longer than one token run as three
- * kernels when the pool has scratch for the call's T rows, token-major and
- * shared by the layers: per row q~|k~ and v (fp16, (2*Hk*d_k + Hv*d_v) * 2
- * bytes), the in-chunk cumulative gate and beta (fp32, Hv * 8 bytes) and the
- * state-independent chunk products u, -w and the row of P (fp16,
- * Hv * (d_v + d_k + 64) * 2 bytes).  A conv/normalisation kernel writes the
- * first part, a chunk-parallel kernel the products, and the recurrence kernel
- * loads them with TMA.  Without scratch they run as one fused kernel (same
- * results within rounding).  By default the first gdn_varlen_forward with more rows than the
- * scratch holds grows it (cudaMalloc; freeing the old buffer waits for the
- * device), except during stream capture, where the fused kernel is used.
- *   max_tokens > 0 : grow the scratch to at least max_tokens rows now
- *                    (synchronous; call it before capturing a graph)
+/* Prefill scratch of the pool.  Sequences longer than one token run as two
+ * kernels when the pool has scratch for the call: a chunk-parallel kernel
+ * (conv, norms, gates and the state-independent products of every 64-token
+ * chunk) writes per-chunk tiles, and the recurrence kernel loads them.  The
+ * scratch is chunk-major (its capacity is counted in 64-token chunks; a call
+ * with T tokens and N sequences needs at most T/64 + min(N, T/2,
+ * num_blocks - 1) + 1 of them) and shared by the layers; at the full shape
+ * (d_k = d_v = 128, Hk = 16, Hv = 32) a chunk takes about 1.8 MB.  Without
+ * enough scratch the same computation runs as one fused kernel (same results
+ * within rounding; gdn_pool_last_prefill_path tells which one ran).  By
+ * default a gdn_varlen_forward that needs more scratch than the pool holds
+ * grows it first, stream-ordered on the call's stream (cudaMallocAsync /
+ * cudaFreeAsync: no device synchronisation), except during stream capture,
+ * where it never allocates and takes the fused kernel if the scratch is too
+ * small.
+ *   max_tokens > 0 : grow the scratch now to cover any call of up to
+ *                    max_tokens tokens (synchronous; call it before capturing
+ *                    a graph)
  *   max_tokens == 0: free the scratch and never grow it (fused kernel only)
  *   max_tokens < 0 : grow on demand again (the default)
  * Returns GDN_ERR_NOMEM if the allocation fails (the forward still works).
  * For a Mamba2 pool the scratch is the chunked scan's fp16 conv output
- * (C * 2 bytes per row), with the same three modes. */
+ * (C * 2 bytes per token), with the same three modes. */
 int gdn_state_pool_reserve(gdn_pool_t* pool, int max_tokens);
 
 /* Forward of one gated-delta-net layer over a packed batch.
@@ -172,7 +177,7 @@ int gdn_state_pool_reserve(gdn_pool_t* pool, int max_tokens);
  * Zero-length sequences are no-ops.  Bad data in the device arrays (see
  * GDN_FLAG_*) is flagged in the layer's error word and the affected sequences
  * are skipped.  x_qkv, a, b, out and conv_w must be 16-byte aligned.
- * Never synchronises (except the one-time growth of the prefill scratch, see
+ * Never synchronises (the prefill scratch grows stream-ordered, see
  * gdn_state_pool_reserve); graph-capturable.  Calls on the same pool must be
  * ordered on one stream (they share the layer's scheduler work area and the
  * pool's prefill scratch).  A Mamba2 pool (gdn_ssd_pool_create) is refused
@@ -254,8 +259,9 @@ int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int nu
  * the call's T rows (grown on demand like the prefill scratch, see
  * gdn_state_pool_reserve); everything else on a token-serial kernel (one CTA
  * per sequence and head, state in registers).  The conv states of the longer
- * sequences are written by a last kernel.  Never synchronises except for the
- * one-time scratch growth; graph-capturable once the scratch is reserved. */
+ * sequences are written by a last kernel.  Never synchronises (the scratch
+ * grows stream-ordered); graph-capturable, and takes the chunked scan under
+ * capture once the scratch is reserved. */
 int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const void* dt,
                            const int32_t* cu_seqlens, const int32_t* state_block_idx,
                            const uint8_t* has_past, const gdn_ssd_weights_t* weights, void* y,
@@ -298,6 +304,23 @@ int gdn_varlen_forward_noalloc(void* pool_mem, size_t pool_bytes, int num_blocks
  * on one layer (layer < 0: OR over all layers).  Synchronises `stream`; not
  * for the hot path. */
 int gdn_get_error(gdn_pool_t* pool, int layer, uint32_t* flags, int reset, void* stream);
+
+/* Which path the sequences longer than one token took in the last
+ * gdn_varlen_forward (or gdn_varlen_forward enqueued into a captured graph)
+ * on this pool, decided on the host when the call was made:
+ *   GDN_PREFILL_NONE   no such sequence could be in the call (T < 2 or a
+ *                      max_seqlen_hint of 1)
+ *   GDN_PREFILL_SPLIT  the chunk-parallel kernel and the recurrence kernel on
+ *                      the pool's scratch
+ *   GDN_PREFILL_FUSED  the single fused chunked kernel (not enough scratch)
+ *   GDN_PREFILL_SERIAL the token-serial kernel (shapes the chunked kernels do
+ *                      not cover)
+ * Does not synchronise. */
+#define GDN_PREFILL_NONE 0
+#define GDN_PREFILL_SPLIT 1
+#define GDN_PREFILL_FUSED 2
+#define GDN_PREFILL_SERIAL 3
+int gdn_pool_last_prefill_path(const gdn_pool_t* pool, int* path);
 
 /* Profiling aid: while set, every later gdn_varlen_forward on this pool
  * records cudaEvent_t `before` on its stream right after the scheduler kernel

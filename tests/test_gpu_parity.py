@@ -346,3 +346,40 @@ def test_fork_copies_a_block_and_both_continue_identically():
     assert torch.equal(run.conv_view(3), run.conv_view(5))
     with pytest.raises(binding.GdnError):
         run.pool.copy_block(0, 3, 0)  # the trash block is never written
+
+
+def test_captured_prefill_after_reserve_takes_the_split_path():
+    """A prefill captured in a CUDA graph after gdn_state_pool_reserve runs the
+    split kernels (the query says so) and replays to the eager result; on a
+    pool with no scratch, capture never allocates and reports the fused
+    kernel; an eager call grows the scratch stream-ordered and takes the split
+    path."""
+    wl = synth.make_workload("cap", synth.FULL_DIMS, [300, 1, 129, 70], [1, 1, 0, 1], 16, 22)
+    eager = harness.DeviceRun(wl)
+    eager.run()
+    torch.cuda.synchronize()
+    assert eager.pool.last_prefill_path() == binding.PREFILL_SPLIT
+    for reserve, path in [(wl.T, binding.PREFILL_SPLIT), (None, binding.PREFILL_FUSED)]:
+        run = harness.DeviceRun(wl)
+        snapshot = run.mem.clone()
+        if reserve is not None:
+            run.pool.reserve(reserve)
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run.run(stream=s)
+        assert run.pool.last_prefill_path() == path
+        run.mem.copy_(snapshot)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert run.pool.error_flags() == 0
+        if path == binding.PREFILL_SPLIT:
+            assert torch.equal(run.out, eager.out)
+            assert torch.equal(run.mem, eager.mem)
+        else:
+            assert rel_l2(run.out.float().cpu().numpy(), eager.out.float().cpu().numpy()) <= 2e-3
+    decode = synth.make_workload("dec_only", synth.FULL_DIMS, [1, 1], [1, 1], 8, 23)
+    d = harness.DeviceRun(decode)
+    d.run(max_seqlen_hint=1)
+    assert d.pool.last_prefill_path() == binding.PREFILL_NONE
