@@ -76,8 +76,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   V   v0 | v1 fp16 token-major: 4 blocks of 64 channels x 64 tokens
 //       (MN-major B operands of the u products)
 //   gates: G log2 e, beta, -beta e^G of both heads [2][64]
-//   WT  the conv taps of each pass transposed to [box][tap][64 channels], so
-//       that a thread's 8 channels of one tap are one 16-byte load
+//   WT  the conv taps of each pass, halved (see silu_half2) and converted to
+//       fp32, as [box][tap][64 channels] with the 16-byte groups of 4 channels
+//       ordered 0, 2, 4, ..., 14, 1, 3, ..., 15, so that a thread's 8
+//       channels of one tap are two conflict-free 16-byte loads
 constexpr uint32_t OFF_S = 0;
 constexpr uint32_t OFF_AW = OFF_S;
 constexpr uint32_t OFF_AU = OFF_S + 16384;
@@ -86,8 +88,9 @@ constexpr uint32_t OFF_V = OFF_QK + 2 * KB_STRIDE;
 constexpr uint32_t OFF_GH = OFF_V + 4 * BOX;
 constexpr uint32_t OFF_GB = OFF_GH + 512;
 constexpr uint32_t OFF_GBE = OFF_GB + 512;
-constexpr uint32_t OFF_WT = OFF_GBE + 512;  // taps of each pass, bf16 [2 passes][4 boxes][4 taps][64 ch]
-constexpr uint32_t SMEM_BYTES = OFF_WT + 2 * 4 * KC * 64 * 2 + 1024;
+constexpr uint32_t WT_TAP = 64 * 4;        // one tap of a box's 64 channels, fp32
+constexpr uint32_t OFF_WT = OFF_GBE + 512;  // taps of each pass, fp32 [2 passes][4 boxes][4 taps][64 ch]
+constexpr uint32_t SMEM_BYTES = OFF_WT + 2 * 4 * KC * WT_TAP + 1024;
 static_assert(2 * CH * AP * 4 <= 4 * XSUB, "A / T of both heads fit the staging area");
 static_assert(6 * ZB * 4 <= BOX, "B blocks of one head fit the q~ rows of a K-block");
 static_assert(OFF_QK % 1024 == 0 && OFF_V % 1024 == 0, "operand tiles on 1024-byte boundaries");
@@ -126,15 +129,14 @@ __device__ __forceinline__ float tanh_approx(float x) {
 __device__ __forceinline__ unsigned long long pack2f(float lo, float hi) {
   return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
 }
-// SiLU of a packed fp32 pair: y sigmoid(y) = y (1/2 + tanh(y/2) / 2), one MUFU
+// SiLU of a packed fp32 pair given h = y / 2 (the conv taps are halved, which
+// is exact): y sigmoid(y) = y (1 + tanh(y/2)) / 2 = h + h tanh(h), one MUFU
 // operation per value (tanh.approx: absolute error about 2^-11 on tanh, so
 // about |y| 2^-12 on the result, the size of the fp16 rounding that follows)
-__device__ __forceinline__ unsigned long long silu2(unsigned long long y2) {
-  const unsigned long long half2 = pack2f(0.5f, 0.5f);
-  const unsigned long long h2 = mul2p(y2, half2);
+__device__ __forceinline__ unsigned long long silu_half2(unsigned long long h2) {
   const unsigned long long t2 = pack2f(tanh_approx(__uint_as_float((uint32_t)h2)),
                                        tanh_approx(__uint_as_float((uint32_t)(h2 >> 32))));
-  return mul2p(y2, fma2(t2, half2, half2));
+  return fma2(h2, t2, h2);
 }
 // bf16 pair (low, high halves of a word) -> packed fp32 pair
 __device__ __forceinline__ unsigned long long bf2_to_f2(uint32_t u) {
@@ -350,15 +352,20 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   // stores, so that the staging area can be released in between.
   struct ConvIn {
     uint4 xw[4 + KC - 1];
-    uint4 wt[KC];
+    uint4 wt[KC][2];  // halved taps of channels c..c+3 and c+4..c+7, fp32
   };
   auto conv_load = [&](int part, ConvIn& in) {
     const int lc = (part & 1) * D + g * 8;  // pass-local channel: box lc / 64, column lc % 64
     const unsigned char* box = sm + OFF_S + (lc >> 6) * XSUB;
-    const unsigned char* wt = sm + OFF_WT + (part >> 1) * (4 * KC * 128) + (lc >> 6) * (KC * 128) +
-                              (lc & 63) * 2;
+    // channel group m = (lc % 64) / 8 has its two 4-channel halves at 16-byte
+    // positions m and 8 + m of each tap
+    const unsigned char* wt = sm + OFF_WT + ((part >> 1) * 4 + (lc >> 6)) * (KC * WT_TAP) +
+                              ((lc & 63) >> 3) * 16;
 #pragma unroll
-    for (int j = 0; j < KC; ++j) in.wt[j] = *reinterpret_cast<const uint4*>(wt + j * 128);
+    for (int j = 0; j < KC; ++j) {
+      in.wt[j][0] = *reinterpret_cast<const uint4*>(wt + j * WT_TAP);
+      in.wt[j][1] = *reinterpret_cast<const uint4*>(wt + j * WT_TAP + 128);
+    }
 #pragma unroll
     for (int rr = 0; rr < 4 + KC - 1; ++rr)
       in.xw[rr] = *reinterpret_cast<const uint4*>(box + tc::sw128_offset(i0 + rr, lc & 63));
@@ -378,9 +385,13 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       for (int t = 0; t < 4; ++t) {
         const int j = rr - t;
         if (j >= 0 && j < KC) {
-          const uint32_t wj[4] = {in.wt[j].x, in.wt[j].y, in.wt[j].z, in.wt[j].w};
+          const unsigned long long wj[4] = {
+              (unsigned long long)in.wt[j][0].x | ((unsigned long long)in.wt[j][0].y << 32),
+              (unsigned long long)in.wt[j][0].z | ((unsigned long long)in.wt[j][0].w << 32),
+              (unsigned long long)in.wt[j][1].x | ((unsigned long long)in.wt[j][1].y << 32),
+              (unsigned long long)in.wt[j][1].z | ((unsigned long long)in.wt[j][1].w << 32)};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc2[t][e] = fma2(bf2_to_f2(wj[e]), xv2[e], acc2[t][e]);
+          for (int e = 0; e < 4; ++e) acc2[t][e] = fma2(wj[e], xv2[e], acc2[t][e]);
         }
       }
     }
@@ -389,7 +400,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     for (int t = 0; t < 4; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const unsigned long long s2 = silu2(acc2[t][e]);
+        const unsigned long long s2 = silu_half2(acc2[t][e]);
         y[t][2 * e] = __uint_as_float((uint32_t)s2);
         y[t][2 * e + 1] = __uint_as_float((uint32_t)(s2 >> 32));
       }
@@ -397,14 +408,23 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     for (int t = 0; t < 4; ++t) {
       const int i = i0 + t;
       if (part < 2) {
-        float ss = 0.f;
+        unsigned long long ss2 = 0ull;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss += y[t][e] * y[t][e];
+        for (int e = 0; e < 8; e += 2) {
+          const unsigned long long y2 = pack2f(y[t][e], y[t][e + 1]);
+          ss2 = fma2(y2, y2, ss2);
+        }
+        float ss = __uint_as_float((uint32_t)ss2) + __uint_as_float((uint32_t)(ss2 >> 32));
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const float sc = rsqrtf(ss + kL2Eps) * (part == 0 ? inv_sqrt_d : 1.f);
+        const unsigned long long sc2 = pack2f(sc, sc);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[t][e] *= sc;
+        for (int e = 0; e < 8; e += 2) {
+          const unsigned long long r2 = mul2p(pack2f(y[t][e], y[t][e + 1]), sc2);
+          y[t][e] = __uint_as_float((uint32_t)r2);
+          y[t][e + 1] = __uint_as_float((uint32_t)(r2 >> 32));
+        }
       } else if (i < n) {
 #pragma unroll
         for (int e = 0; e < 8; e += 2) vmax = max_abs3_nan(vmax, y[t][e], y[t][e + 1]);
@@ -434,15 +454,19 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       }
     }
     {
+      // thread = channel ch of box b: its 4 taps, halved, to the fp32 tap
+      // rows; 4-channel group q = ch / 4 sits at 16-byte position
+      // q / 2 + 8 (q % 2)
       const int b = tid >> 6, ch = tid & 63;
       const uint2 w4 = *reinterpret_cast<const uint2*>(sm + OFF_S + b * XSUB + WS_OFF + ch * KC * 2);
-      __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(sm + OFF_WT + ps * (4 * KC * 128) +
-                                                           b * (KC * 128)) + ch;
+      const int q = ch >> 2;
+      float* wt = reinterpret_cast<float*>(sm + OFF_WT + (ps * 4 + b) * (KC * WT_TAP) +
+                                           ((q >> 1) + 8 * (q & 1)) * 16) + (ch & 3);
       const uint32_t u[2] = {w4.x, w4.y};
 #pragma unroll
       for (int j = 0; j < KC; ++j) {
-        const uint16_t hb = (uint16_t)(u[j >> 1] >> (16 * (j & 1)));
-        wt[j * 64] = __ushort_as_bfloat16(hb);
+        const uint32_t bits = (j & 1) ? (u[j >> 1] & 0xffff0000u) : (u[j >> 1] << 16);
+        wt[j * (WT_TAP / 4)] = 0.5f * __uint_as_float(bits);
       }
     }
     __syncthreads();
@@ -517,16 +541,27 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       for (int blk = 0; blk < 2; ++blk) {
         const int jb = 2 * hf + blk;
         if (jb <= ib) {
-          float g16[16];
+          // val_j = X_ij 2^{Gi2 - G_j log2 e}, two columns per packed step
+          const unsigned long long gi2 = pack2f(Gi2, Gi2);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float4 t = *reinterpret_cast<const float4*>(gh + 16 * jb + 4 * q);
-            g16[4 * q] = t.x; g16[4 * q + 1] = t.y; g16[4 * q + 2] = t.z; g16[4 * q + 3] = t.w;
-          }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = 16 * jb + e;
-            val[blk * 16 + e] = j <= lim ? xr[blk * 16 + e] * ex2_approx(Gi2 - g16[e]) : 0.f;
+            for (int hh = 0; hh < 2; ++hh) {
+              const unsigned long long d2 =
+                  fma2(pack2f(hh ? t.z : t.x, hh ? t.w : t.y), pack2f(-1.f, -1.f), gi2);
+              const unsigned long long e2 = pack2f(ex2_approx(__uint_as_float((uint32_t)d2)),
+                                                   ex2_approx(__uint_as_float((uint32_t)(d2 >> 32))));
+              const int e = blk * 16 + 4 * q + 2 * hh;
+              const unsigned long long v2 = mul2p(pack2f(xr[e], xr[e + 1]), e2);
+              val[e] = __uint_as_float((uint32_t)v2);
+              val[e + 1] = __uint_as_float((uint32_t)(v2 >> 32));
+            }
+          }
+          if (jb == ib) {  // the diagonal block: columns past the row's last kept one
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (16 * jb + e > lim) val[blk * 16 + e] = 0.f;
           }
         } else {
 #pragma unroll
