@@ -29,7 +29,9 @@
 //   MMA  S  += U^T (k~ e^{G_C-G})  (S_C = e^{G_C} S0 + sum_j e^{G_C-G_j} u_j k~_j^T)
 // MMA operands are fp16 (same tensor-core rate as bf16, 3 more mantissa bits:
 // the bf16 version of this kernel sat at ~4.5e-3 relative error on slowly
-// decaying states).  An operand outside the fp16 range raises GDN_FLAG_RANGE.
+// decaying states).  A chain with an operand outside the fp16 range leaves its
+// block's state untouched and is rerun by the token-serial kernel (redo mode)
+// in the same call.
 // Every exponent is of a non-positive number.  Tokens past the end of a
 // partial chunk get zero q/k/v, beta = 0 and g = 0, which leaves everything
 // unchanged.  This is the chunked form of the gated delta rule (Gated Delta
@@ -610,8 +612,12 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     }
   }
   if (failed) break;
-  {
-    // ---- final state -> the write block, S[v][k] at (h*D + k)*D + v
+  // an fp16 operand of this chain out of range: the block keeps the old state
+  // and the chain is rerun token-serially; else the final state -> the write
+  // block, S[v][k] at (h*D + k)*D + v
+  if (__syncthreads_or(!(amax <= kF16Max) ? 1 : 0)) {
+    if (tid == 0) mark_redo(p.work, chain / Hv, h);
+  } else {
     float srow[64];
     tc::tmem_ld32(tmem + lane + TM_S + chalf * 64, srow);
     tc::tmem_ld32(tmem + lane + TM_S + chalf * 64 + 32, srow + 32);
@@ -620,8 +626,6 @@ chunk_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
 #pragma unroll
     for (int k = 0; k < 64; ++k) S_w[(size_t)(chalf * 64 + k) * D + r128] = srow[k];
   }
-  if (__syncthreads_or(!(amax <= kF16Max) ? 1 : 0) && tid == 0)
-    atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
   amax = 0.f;
   }  // chains
   if (failed && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
@@ -739,6 +743,10 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // chains whose fp16 operands left their range, token-serially, before the
+  // conv states change
+  e = launch_redo(p, D, GDN_BF16, max_pre, stream);
   if (e != cudaSuccess) return e;
   return launch_pdl(tail_update_kernel, dim3(max_pre, (p.C / 8 + 255) / 256), dim3(256), 0, stream, p);
 }

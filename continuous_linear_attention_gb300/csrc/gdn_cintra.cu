@@ -267,8 +267,12 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   if (gidx >= n_chunks) return;
   const int kh = blockIdx.y;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
-  const int row0 = rec.x, n = rec.y, c = rec.z, s = rec.w;
-  const int rblk = (c == 0 && p.has_past[s]) ? p.blk[s] : 0;  // the conv state is read on chunk 0 only
+  const int row0 = rec.x, n = rec.y, c = rec.z, kpre = rec.w;
+  int rblk = 0;  // the conv state is read on chunk 0 only
+  if (c == 0) {
+    const int s = p.work.pre()[kpre];
+    rblk = p.has_past[s] ? p.blk[s] : 0;
+  }
   const __nv_bfloat16* tail =
       reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
   const __nv_bfloat16* wconv = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
@@ -785,8 +789,13 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     }
   }
   if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
-  // v, w, u and the operand tiles enter tensor-core operands in fp16
-  if (!(amax <= kF16Max) || !(vmax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
+  // v, w, u and the operand tiles enter tensor-core operands in fp16: a value
+  // out of its range sends both v-heads of this sequence to the token-serial
+  // redo
+  if (__syncthreads_or(!(amax <= kF16Max) || !(vmax <= kF16Max)) && tid == 0) {
+    mark_redo(p.work, kpre, kh * R);
+    mark_redo(p.work, kpre, kh * R + 1);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);

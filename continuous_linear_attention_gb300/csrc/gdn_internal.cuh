@@ -23,6 +23,9 @@ constexpr int kMaxConvK = 4;
 //                  pre_tmp[num_blocks]     active sequences of length > 1, unsorted
 //                  pre[num_blocks]         the same, longest first
 //                  pre_cp[num_blocks + 1]  chunk prefix: 64-token chunks of pre[0..k)
+//                  redo[2 * num_blocks]    per entry k of pre[], a 64-bit mask of the
+//                                          v-heads whose chunked prefill met an fp16
+//                                          operand out of range (rerun token-serially)
 enum Cnt : int {
   kErr = 0,
   kNItems = 1,
@@ -44,7 +47,8 @@ struct WorkArea {
   __host__ __device__ int32_t* pre_tmp() const { return base + kHeaderWords + 3 * num_blocks; }
   __host__ __device__ int32_t* pre() const { return base + kHeaderWords + 4 * num_blocks; }
   __host__ __device__ int32_t* pre_cp() const { return base + kHeaderWords + 5 * num_blocks; }
-  static constexpr size_t words(int num_blocks) { return kHeaderWords + 6 * (size_t)num_blocks + 1; }
+  __host__ __device__ int32_t* redo() const { return base + kHeaderWords + 6 * num_blocks + 1; }
+  static constexpr size_t words(int num_blocks) { return kHeaderWords + 8 * (size_t)num_blocks + 1; }
 };
 
 // Everything a forward kernel needs, passed by value.
@@ -75,7 +79,8 @@ struct FwdParams {
   //   scr_u  [g][Hv] 16 KiB  u = T diag(beta) v, same layout
   //   scr_p  [g][Hv]  8 KiB  P [64 i][64 j]
   //   scr_c  [g]     int4    (first packed row, valid tokens, chunk index
-  //                          inside its sequence, sequence) (scheduler)
+  //                          inside its sequence, index of the sequence in
+  //                          the prefill list) (scheduler)
   // (the tiles written by cintra_kernel, read by seq_kernel)
   void* scr_qk = nullptr;
   void* scr_g = nullptr;
@@ -129,6 +134,18 @@ cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
 // or only over those longer than one token (long_only = true).
 cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, bool long_only,
                              cudaStream_t stream);
+// The token-serial kernel in redo mode: for every prefill-list entry whose
+// redo mask (WorkArea::redo) has bits set, recompute exactly those v-heads
+// from the states still in the block, writing their outputs and recurrent
+// states (not the conv state, which the conv-state update writes after it).
+cudaError_t launch_redo(const FwdParams& p, int d, int act, int max_pre, cudaStream_t stream);
+// Mark v-head h of prefill-list entry k for the redo.
+__device__ __forceinline__ void mark_redo(const WorkArea& w, int k, int h) {
+  atomicOr(reinterpret_cast<unsigned*>(w.redo()) + 2 * k + (h >> 5), 1u << (h & 31));
+}
+__device__ __forceinline__ bool redo_marked(const WorkArea& w, int k, int h) {
+  return (reinterpret_cast<const unsigned*>(w.redo())[2 * k + (h >> 5)] >> (h & 31)) & 1u;
+}
 // The persistent decode kernel (length-1 sequences): d_k = d_v = 128, bf16
 // activations, Hv = 2 Hk, K = 4.
 bool decode_supported(int d, int act, int Hk, int Hv, int K);

@@ -27,7 +27,8 @@ constexpr int kNoAllocMaxBlocks = 4096;
 constexpr size_t kNoAllocWords = gdn::WorkArea::words(kNoAllocMaxBlocks);
 
 // The scheduler's work area for this entry point (error word, counters,
-// block-use counts, work lists and the prefill chunk prefix), ~96 KiB per device.
+// block-use counts, work lists, the prefill chunk prefix and the redo masks), ~128 KiB per
+// device.
 static __device__ __align__(256) int32_t g_noalloc_work[kNoAllocWords];
 
 constexpr int kMaxDevices = 64;

@@ -29,9 +29,14 @@ namespace {
 
 constexpr int kHeadThreads = 256;  // threads per v-head
 
+// mode: kAll every active sequence, kLong those longer than one token, kRedo
+// the v-heads of the prefill list marked for a redo (outputs and recurrent
+// states of those heads only; the conv state is left to the conv-state update)
+enum Mode : int { kAll = 0, kLong = 1, kRedo = 2 };
+
 template <int D, typename Act>
 __global__ void __launch_bounds__(2 * kHeadThreads)
-recurrent_kernel(FwdParams p, bool long_only) {
+recurrent_kernel(FwdParams p, int mode) {
   constexpr int CV = D / 4;                 // float4 columns per state row
   constexpr int G = kHeadThreads / CV;      // row groups
   constexpr int NJ = D / G;                 // rows per thread
@@ -39,10 +44,19 @@ recurrent_kernel(FwdParams p, bool long_only) {
   pdl_wait_then_release();
   const int R = p.Hv / p.Hk;                // v-heads per k-head (1 or 2)
   const WorkArea& wk = p.work;
+  const bool long_only = mode != kAll;
   const int n_items = wk.header()[long_only ? kNPre : kNItems];
   if ((int)blockIdx.x >= n_items) return;
-  const int s = (long_only ? wk.pre() : wk.items())[blockIdx.x];
   const int kh = blockIdx.y;
+  // redo: the marked v-heads of this k-head group (bits kh*R .. kh*R+R-1)
+  uint32_t marks = (1u << R) - 1u;
+  if (mode == kRedo) {
+    const int h0 = kh * R;
+    marks = (reinterpret_cast<const uint32_t*>(wk.redo())[2 * blockIdx.x + (h0 >> 5)] >> (h0 & 31)) &
+            ((1u << R) - 1u);
+    if (!marks) return;
+  }
+  const int s = (long_only ? wk.pre() : wk.items())[blockIdx.x];
   const int t0 = p.cu[s];
   const int L = p.cu[s + 1] - t0;
   const int wblk = p.blk[s];
@@ -94,6 +108,7 @@ recurrent_kernel(FwdParams p, bool long_only) {
   const int j_head = tid / kHeadThreads;
   const int li = tid % kHeadThreads;
   const int h = kh * R + j_head;
+  const bool mine = (marks >> j_head) & 1u;  // this thread's v-head is written
   const int cv = li % CV;
   const int rg = li / CV;
   const float* S_r = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * D * D;
@@ -177,7 +192,7 @@ recurrent_kernel(FwdParams p, bool long_only) {
       const float u = beta * (vv - decay * sk);
       const float kq = red[2] * qs * ks;
       uo[j_head * D + li] = u;
-      out[(row * Hv + h) * D + li] = from_f32<Act>(decay * sq + kq * u);
+      if (mine) out[(row * Hv + h) * D + li] = from_f32<Act>(decay * sq + kq * u);
     }
     __syncthreads();
     // 5. S <- e^g S + u k^T
@@ -192,9 +207,12 @@ recurrent_kernel(FwdParams p, bool long_only) {
   }
 
   // ---- write back: recurrent state, then the conv window as the new conv state
+  if (mine) {
 #pragma unroll
-  for (int i = 0; i < NJ; ++i)
-    *reinterpret_cast<float4*>(S_w + (size_t)(rg + G * i) * D + 4 * cv) = S[i];
+    for (int i = 0; i < NJ; ++i)
+      *reinterpret_cast<float4*>(S_w + (size_t)(rg + G * i) * D + 4 * cv) = S[i];
+  }
+  if (mode == kRedo) return;
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     if (gch[c] < 0) continue;
@@ -205,13 +223,13 @@ recurrent_kernel(FwdParams p, bool long_only) {
 }
 
 template <int D, typename Act>
-cudaError_t launch_rec(const FwdParams& p, int max_items, bool long_only, cudaStream_t stream) {
+cudaError_t launch_rec(const FwdParams& p, int max_items, int mode, cudaStream_t stream) {
   const int R = p.Hv / p.Hk;
   constexpr int G = kHeadThreads / (D / 4);
   const size_t smem = sizeof(float) * (4 * D + 2 * 2 * G * D + 2 * D + 4 + 4);
   dim3 grid(max_items, p.Hk);
   const cudaError_t e = launch_pdl(recurrent_kernel<D, Act>, grid, dim3(R * kHeadThreads), smem,
-                                   stream, p, long_only);
+                                   stream, p, mode);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -221,14 +239,21 @@ cudaError_t launch_rec(const FwdParams& p, int max_items, bool long_only, cudaSt
 cudaError_t launch_recurrent(const FwdParams& p, int d, int act, int max_items, bool long_only,
                              cudaStream_t stream) {
   if (max_items <= 0) return cudaSuccess;
+  const int mode = long_only ? kLong : kAll;
   if (act == GDN_F32) {
-    if (d == 32) return launch_rec<32, float>(p, max_items, long_only, stream);
-    if (d == 64) return launch_rec<64, float>(p, max_items, long_only, stream);
-    return launch_rec<128, float>(p, max_items, long_only, stream);
+    if (d == 32) return launch_rec<32, float>(p, max_items, mode, stream);
+    if (d == 64) return launch_rec<64, float>(p, max_items, mode, stream);
+    return launch_rec<128, float>(p, max_items, mode, stream);
   }
-  if (d == 32) return launch_rec<32, __nv_bfloat16>(p, max_items, long_only, stream);
-  if (d == 64) return launch_rec<64, __nv_bfloat16>(p, max_items, long_only, stream);
-  return launch_rec<128, __nv_bfloat16>(p, max_items, long_only, stream);
+  if (d == 32) return launch_rec<32, __nv_bfloat16>(p, max_items, mode, stream);
+  if (d == 64) return launch_rec<64, __nv_bfloat16>(p, max_items, mode, stream);
+  return launch_rec<128, __nv_bfloat16>(p, max_items, mode, stream);
+}
+
+cudaError_t launch_redo(const FwdParams& p, int d, int act, int max_pre, cudaStream_t stream) {
+  if (max_pre <= 0) return cudaSuccess;
+  if (d != 128 || act != GDN_BF16) return cudaErrorInvalidValue;  // the chunked kernels' shape
+  return launch_rec<128, __nv_bfloat16>(p, max_pre, kRedo, stream);
 }
 
 }  // namespace gdn

@@ -113,9 +113,12 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     pre_cp[k] = acc;
   }
   __syncthreads();
+  // clear the redo masks of the prefill list
+  int32_t* redo = work.redo();
+  for (int i = tid; i < 2 * n_pre; i += kSchedThreads) redo[i] = 0;
   // one record per 64-token prefill chunk, by chunk index (when the caller
   // has room for them): (first packed row, valid tokens, chunk index inside
-  // its sequence, sequence)
+  // its sequence, index of the sequence in the prefill list)
   if (chunk_rec) {
     const int total = pre_cp[n_pre];
     for (int g = tid; g < total; g += kSchedThreads) {
@@ -128,7 +131,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
       const int c = g - pre_cp[lo];
       const int seq0 = cu[s];
       const int L = cu[s + 1] - seq0;
-      chunk_rec[g] = make_int4(seq0 + 64 * c, min(64, L - 64 * c), c, s);
+      chunk_rec[g] = make_int4(seq0 + 64 * c, min(64, L - 64 * c), c, lo);
     }
   }
   if (tid == 0) {

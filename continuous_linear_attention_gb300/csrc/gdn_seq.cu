@@ -78,10 +78,22 @@ struct ChunkDesc {
   int seq0, c0, n;    // sequence start row, chunk start, valid tokens
   int h, rblk, wblk;  // v-head, block read, block written
   int flags;          // 1 first chunk of the chain, 2 last, 4 end of work
+  int kpre;           // index of the sequence in the prefill list
 };
 
 __device__ __forceinline__ void cbar() {  // the compute warps only
   asm volatile("bar.sync %0, %1;" ::"n"(kBarC), "n"(kCompute) : "memory");
+}
+// the same barrier, returning whether any compute thread passed true
+__device__ __forceinline__ bool cbar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kBarC), "n"(kCompute)
+      : "memory");
+  return r != 0;
 }
 
 // compute warps release the MMA warp, which waits with mma_gate
@@ -235,8 +247,11 @@ seq_kernel(FwdParams p) {
         const bool end = chain >= n_chains;
         int s = 0, h = 0, seq0 = 0, L = 0, nc = 1;
         if (!end) {
-          s = p.work.pre()[chain / Hv];
           h = chain % Hv;
+          // a chain whose chunk products left the fp16 range goes to the
+          // token-serial redo instead
+          if (redo_marked(p.work, chain / Hv, h)) continue;
+          s = p.work.pre()[chain / Hv];
           seq0 = p.cu[s];
           L = p.cu[s + 1] - seq0;
           nc = (L + CH - 1) / CH;
@@ -253,6 +268,7 @@ seq_kernel(FwdParams p) {
           d.wblk = end ? 0 : p.blk[s];
           d.rblk = (!end && p.has_past[s]) ? d.wblk : 0;
           d.flags = end ? 4 : ((c == 0 ? 1 : 0) | (c == nc - 1 ? 2 : 0));
+          d.kpre = chain / Hv;
           desc[b] = d;
           if (end) {
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&full[b]))
@@ -482,15 +498,25 @@ seq_kernel(FwdParams p) {
         tc::fence_after_sync();
         flush();
         pending = false;
-        float* S_w = reinterpret_cast<float*>(p.layer_base + (size_t)d.wblk * p.stride + p.rec_off) +
-                     (size_t)d.h * D * D;
+        // the state and U entered tensor-core operands in fp16: if any value
+        // of this chain left that range, its block keeps the old state and the
+        // chain is rerun token-serially (outputs included); else the final
+        // state goes to the block
+        const bool bad = cbar_or(!(amax <= kF16Max));
+        amax = 0.f;
+        if (bad) {
+          if (tid == 0) mark_redo(p.work, d.kpre, d.h);
+        } else {
+          float* S_w = reinterpret_cast<float*>(p.layer_base + (size_t)d.wblk * p.stride +
+                                                p.rec_off) + (size_t)d.h * D * D;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float srow[32];
-          tc::tmem_ld32(tmem + lane + TM_S + hf * 64 + half * 32, srow);
-          tc::tmem_wait_ld();
+          for (int half = 0; half < 2; ++half) {
+            float srow[32];
+            tc::tmem_ld32(tmem + lane + TM_S + hf * 64 + half * 32, srow);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int kk = 0; kk < 32; ++kk) S_w[(size_t)(hf * 64 + half * 32 + kk) * D + v] = srow[kk];
+            for (int kk = 0; kk < 32; ++kk) S_w[(size_t)(hf * 64 + half * 32 + kk) * D + v] = srow[kk];
+          }
         }
       }
     }
@@ -500,8 +526,6 @@ seq_kernel(FwdParams p) {
     if (next_gate == kBarD1) mma_release<kBarD1>();
     else mma_release<kBarS>();
     if (dead && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
-    // the state and U enter tensor-core operands in fp16
-    if (!(amax <= kF16Max)) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_RANGE);
   }
   tc::fence_before_sync();
   __syncthreads();

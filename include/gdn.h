@@ -71,8 +71,12 @@ extern "C" {
 #define GDN_FLAG_DUPLICATE 0x8u   /* two active sequences name the same block: both skipped */
 #define GDN_FLAG_TIMEOUT 0x10u    /* a kernel's bounded wait gave up (its results are incomplete) */
 #define GDN_FLAG_HINT 0x20u       /* a sequence is longer than max_seqlen_hint: it was skipped */
-#define GDN_FLAG_RANGE 0x40u      /* a tensor-core operand of the chunked prefill left the fp16
-                                     range (|value| > 65000): that sequence's results are invalid */
+#define GDN_FLAG_RANGE 0x40u      /* Mamba2 pools only: an SSM state entering the chunked scan's
+                                     fp16 operand left the fp16 range (|value| > 65000); that
+                                     sequence's results are invalid.  (The gated delta net
+                                     forwards never raise it: a (sequence, v-head) whose chunked-
+                                     prefill operands leave the fp16 range is recomputed by the
+                                     token-serial kernel within the same call.) */
 
 typedef struct gdn_pool gdn_pool_t;
 
@@ -286,7 +290,7 @@ int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const v
  *                          bits raised by this call (NULL: not reported)
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  * The scheduler's work area is a static device array sized for pools of at
- * most 4096 blocks (about 96 KiB, held on every GPU that loads the library
+ * most 4096 blocks (about 128 KiB, held on every GPU that loads the library
  * until the process exits); num_blocks > 4096 returns GDN_ERR_RANGE.  Every
  * call on a device shares that array, so calls whose work overlaps on the
  * GPU race: order them on one stream.  The first call on each device looks
