@@ -169,14 +169,14 @@ def prefill_flops(wl, chunk: int = 64) -> float:
     return float(d.Hv * per * toks)
 
 
-def time_secondary(harness, wl, steps, device, pk, graph=False):
+def time_secondary(harness, wl, steps, device, pk, graph=False, warmup=3):
     """Tokens/s and the compute kernels' roofline for another workload (the
     ~16k-token prefill, the mixed batch), timed like the main line; with
     graph=True also the forward replayed as a CUDA graph."""
     import torch
     run = harness.DeviceRun(wl, device=device)
     stream = torch.cuda.current_stream()
-    for _ in range(3):
+    for _ in range(warmup):
         run.run(stream)
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ka = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -452,6 +452,9 @@ def main():
     ap.add_argument("--variants", action="store_true",
                     help="also time the decode batches of the per-channel-decay rule and of "
                          "the Mamba2 scan")
+    ap.add_argument("--profile", choices=["prefill", "mixed"], default=None,
+                    help="profiler aid: run only the ~16k-token prefill or the mixed batch, "
+                         "--warmup + --steps forwards, and print their timing line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -472,6 +475,13 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from continuous_linear_attention_gb300 import harness, synth
+
+    if args.profile:
+        wl = synth.packed_prefill() if args.profile == "prefill" else synth.mixed_batch()
+        res = time_secondary(harness, wl, args.steps, f"cuda:{local_rank}", peaks(),
+                             warmup=args.warmup)
+        print(json.dumps({"profile": args.profile, **res}), flush=True)
+        return
 
     wl = synth.decode_batch(seed=1 + rank, n_req=args.requests,
                             num_blocks=max(512, 2 * args.requests))
