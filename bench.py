@@ -295,6 +295,49 @@ def time_variant_prefill(harness, wl, steps, device, pk):
             "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "error_flags": flags}
 
 
+def time_projections(binding, synth, T, steps, device, pk):
+    """The layer's dense neighbours on T tokens (d_model 2048, full head dims):
+    gdn_in_proj (hidden -> x_qkv | z | b | a) and gdn_out_proj (gated norm +
+    output projection), each timed with CUDA events; dense-contraction flops
+    over their time against the bf16 peak."""
+    import torch
+    d = synth.FULL_DIMS
+    lw = synth.layer_weights(d)
+    h = synth.hidden_states(T).to(device)
+    ws = [t.to(device) for t in (lw.w_qkv, lw.w_z, lw.w_b, lw.w_a, lw.w_out)]
+    nw = lw.norm_w.to(device)
+    outs = [torch.empty(T, n, dtype=torch.bfloat16, device=device)
+            for n in (d.C, d.Hv * d.dv, d.Hv, d.Hv)]
+    o = torch.randn(T, d.Hv, d.dv, device=device).to(torch.bfloat16)
+    o_norm = torch.empty_like(o)
+    y = torch.empty(T, lw.d_model, dtype=torch.bfloat16, device=device)
+
+    def run_in():
+        binding.in_proj(h, *ws[:4], *outs, d.C, d.Hv, d.dv)
+
+    def run_out():
+        binding.out_proj(o, outs[1].view(T, d.Hv, d.dv), nw, lw.eps, ws[4], o_norm, y)
+
+    res = {"workload": f"layer_projections_{T}tok_dmodel{lw.d_model}", "tokens": T}
+    n_in = d.C + d.Hv * d.dv + 2 * d.Hv
+    for name, fn, fl in (("in_proj", run_in, 2.0 * T * lw.d_model * n_in),
+                         ("out_proj", run_out, 2.0 * T * d.Hv * d.dv * lw.d_model)):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        tf = fl / (ms / 1e3) / 1e12
+        res[name] = {"ms": ms, "tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
+                     "algorithmic_flops": fl}
+    return res
+
+
 def time_graph(run, steps, hint=0):
     """The same forward captured once in a CUDA graph and replayed: ms per
     replay (the prefill scratch, if any, was grown by earlier calls)."""
@@ -452,9 +495,10 @@ def main():
     ap.add_argument("--variants", action="store_true",
                     help="also time the decode batches of the per-channel-decay rule and of "
                          "the Mamba2 scan")
-    ap.add_argument("--profile", choices=["prefill", "mixed"], default=None,
-                    help="profiler aid: run only the ~16k-token prefill or the mixed batch, "
-                         "--warmup + --steps forwards, and print their timing line")
+    ap.add_argument("--profile", choices=["prefill", "mixed", "proj"], default=None,
+                    help="profiler aid: run only the ~16k-token prefill, the mixed batch or "
+                         "the layer's projections on 15843 tokens, --warmup + --steps times, "
+                         "and print their timing line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -476,6 +520,11 @@ def main():
     __graft_entry__.build()
     from continuous_linear_attention_gb300 import harness, synth
 
+    if args.profile == "proj":
+        from continuous_linear_attention_gb300 import binding
+        res = time_projections(binding, synth, 15843, args.steps, f"cuda:{local_rank}", peaks())
+        print(json.dumps({"profile": args.profile, **res}), flush=True)
+        return
     if args.profile:
         wl = synth.packed_prefill() if args.profile == "prefill" else synth.mixed_batch()
         res = time_secondary(harness, wl, args.steps, f"cuda:{local_rank}", peaks(),
@@ -593,6 +642,7 @@ def main():
             ]
             if not args.no_long:
                 line["secondary"].append(time_long_context(harness, binding, synth, dev, pk))
+            line["secondary"].append(time_projections(binding, synth, 15843, 20, dev, pk))
         if args.variants:
             dev = f"cuda:{local_rank}"
             kda = synth.make_workload("kda_decode_256req", synth.FULL_DIMS, [1] * 256, [1] * 256,

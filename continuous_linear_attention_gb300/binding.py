@@ -42,6 +42,8 @@ EXPORTED = [
     "gdn_get_error",
     "gdn_pool_set_timing_events",
     "gdn_pool_last_prefill_path",
+    "gdn_in_proj",
+    "gdn_out_proj",
     "gdn_status_string",
 ]
 
@@ -100,6 +102,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
     lib.gdn_pool_last_prefill_path.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_in_proj.argtypes = [P, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.gdn_out_proj.argtypes = [P, P, P, ctypes.c_float, P, I, I, I, I, P, P, P, P]
     lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, I, P]
     lib.gdn_diag_umma_gemm.restype = I
     lib.gdn_diag_umma_gemm_ex.argtypes = [P, P, P, P, I, I, I, I, I, P]
@@ -309,6 +313,24 @@ def diag_wait_timeout(flags, stream=None) -> None:
     """gdn_diag_wait_timeout: a bounded wait that runs out and ORs
     GDN_FLAG_TIMEOUT into ``flags`` (a 1-element int32/uint32 CUDA tensor)."""
     _check(load().gdn_diag_wait_timeout(_ptr(flags), _stream(stream)), "gdn_diag_wait_timeout")
+
+
+def in_proj(hidden, w_qkv, w_z, w_b, w_a, x_qkv, z, b, a, C, Hv, dv, flags=None,
+            stream=None) -> None:
+    """gdn_in_proj: x_qkv | z | b | a = hidden W^T (device tensors)."""
+    T, d_model = hidden.shape
+    _check(load().gdn_in_proj(_ptr(hidden), T, d_model, _ptr(w_qkv), _ptr(w_z), _ptr(w_b),
+                              _ptr(w_a), C, Hv, dv, _ptr(x_qkv), _ptr(z), _ptr(b), _ptr(a),
+                              _ptr(flags), _stream(stream)), "gdn_in_proj")
+
+
+def out_proj(o, z, norm_w, eps, w_out, o_norm, y, flags=None, stream=None) -> None:
+    """gdn_out_proj: o_norm = gated RMS norm of o, y = o_norm W_out^T."""
+    T, Hv, dv = o.shape
+    d_model = w_out.shape[0]
+    _check(load().gdn_out_proj(_ptr(o), _ptr(z), _ptr(norm_w), float(eps), _ptr(w_out), T, Hv,
+                               dv, d_model, _ptr(o_norm), _ptr(y), _ptr(flags), _stream(stream)),
+           "gdn_out_proj")
 
 
 def varlen_forward_noalloc(pool_mem, num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align,

@@ -186,6 +186,15 @@ cudaError_t launch_ssd_decode(const SsdParams& p, int max_dec, cudaStream_t stre
 bool ssd_chunk_supported(int H, int P, int NS, int K, int act);
 cudaError_t launch_ssd_chunk(const SsdParams& p, void* xs, int max_pre, cudaStream_t stream);
 
+// The dense neighbours (gdn_proj.cu): C_g = A B_g^T for up to four groups
+// sharing A (bf16, row-major, K contiguous; fp32 accumulation; bf16 out), and
+// the gated RMS norm of the output (d_v = 128).
+cudaError_t launch_gemm(const void* A, int M, int K, int lda, int n_groups, const void* const* B,
+                        const int* N, const int* ldb, void* const* C, const int* ldc,
+                        unsigned* flags, cudaStream_t stream);
+cudaError_t launch_gated_norm(const void* o, const void* z, const float* w, void* on, int rows,
+                              float eps, cudaStream_t stream);
+
 // ---------------------------------------------------------------------------
 // Device helpers.
 

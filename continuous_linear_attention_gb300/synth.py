@@ -425,3 +425,40 @@ def make_ssd_workload(name: str, dims: SsdDims, seqlens: List[int], has_past: Li
         conv_state=_act(conv_state, dims.act),
         ssm_state=torch.from_numpy(ssm_state),
     )
+
+
+# --------------------------------------------------------------------------
+# The dense neighbours of the forward (input projection, gated norm, output
+# projection), with random-init weights of a hybrid model's gated-delta-net
+# layer: d_model = 2048 with the full head dims (16 k-heads, 32 v-heads,
+# d = 128) is the size class of the Qwen3-Next gated-delta-net layers.
+
+@dataclasses.dataclass
+class LayerWeights:
+    d_model: int
+    w_qkv: torch.Tensor   # [C][d_model] bf16, rows q | k | v
+    w_z: torch.Tensor     # [Hv*dv][d_model] bf16
+    w_b: torch.Tensor     # [Hv][d_model] bf16
+    w_a: torch.Tensor     # [Hv][d_model] bf16
+    w_out: torch.Tensor   # [d_model][Hv*dv] bf16
+    norm_w: torch.Tensor  # [dv] f32
+    eps: float = 1e-6
+
+
+def layer_weights(dims: Dims, d_model: int = 2048, seed: int = 31) -> LayerWeights:
+    """Projection weights ~ N(0, 1/fan_in) (so every output is ~N(0, 1) for
+    unit inputs), norm weight ~ 1 + N(0, 0.1); bf16 except the norm weight."""
+    rng = _rng(seed)
+    C, HV = dims.C, dims.Hv * dims.dv
+
+    def w(n_out, n_in):
+        return _act(_normal(rng, (n_out, n_in), 1.0 / np.sqrt(n_in)), BF16)
+
+    return LayerWeights(d_model=d_model, w_qkv=w(C, d_model), w_z=w(HV, d_model),
+                        w_b=w(dims.Hv, d_model), w_a=w(dims.Hv, d_model), w_out=w(d_model, HV),
+                        norm_w=torch.from_numpy(1.0 + _normal(rng, (dims.dv,), 0.1)))
+
+
+def hidden_states(T: int, d_model: int = 2048, seed: int = 32) -> torch.Tensor:
+    """Layer inputs [T][d_model] ~ N(0, 1), bf16."""
+    return _act(_normal(_rng(seed), (T, d_model)), BF16)

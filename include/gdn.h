@@ -304,6 +304,38 @@ int gdn_varlen_forward_noalloc(void* pool_mem, size_t pool_bytes, int num_blocks
                                const gdn_weights_t* weights, void* out, int T, int N,
                                int max_seqlen_hint, uint32_t* flags_out, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The dense neighbours of the forward in a hybrid model's gated-delta-net
+ * layer (the pages name the layer; its projections are the plainest reading
+ * of what surrounds the varlen forward): the input projection that produces
+ * the forward's inputs and the output gate z, and the gated RMS norm and
+ * output projection behind it.  Both run on the tensor cores (bf16 operands,
+ * fp32 accumulation, bf16 results), allocate nothing and do not synchronise.
+ * Weights are row-major [out features][in features] (the layout of a linear
+ * layer's weight); every pointer 16-byte aligned; flags: optional device
+ * uint32 that receives GDN_FLAG_TIMEOUT if a bounded wait gave up.
+ *
+ * gdn_in_proj: for every token t,
+ *   x_qkv[t] = W_qkv hidden[t]   ([C][d_model], q | k | v channels)
+ *   z[t]     = W_z hidden[t]     ([Hv*d_v][d_model], the output gate)
+ *   b[t]     = W_b hidden[t],  a[t] = W_a hidden[t]   ([Hv][d_model] each)
+ * hidden [T][d_model], outputs [T][C], [T][Hv*d_v], [T][Hv], [T][Hv].
+ * d_model, C, Hv and Hv*d_v must be multiples of 8 (GDN_ERR_DIMS). */
+int gdn_in_proj(const void* hidden, int T, int d_model, const void* w_qkv, const void* w_z,
+                const void* w_b, const void* w_a, int C, int Hv, int d_v, void* x_qkv, void* z,
+                void* b, void* a, uint32_t* flags, void* stream);
+
+/* gdn_out_proj: per token t and v-head h, the gated RMS norm of the layer's
+ * output
+ *   o_norm[t][h] = o[t][h] / sqrt(mean_v(o[t][h][v]^2) + eps) * norm_w * silu(z[t][h])
+ * (norm_w [d_v] fp32, shared by the heads), written to the caller's o_norm
+ * [T][Hv][d_v] bf16, then y[t] = W_out o_norm[t] with W_out [d_model][Hv*d_v]
+ * and y [T][d_model].  o, z as the forward's out and gdn_in_proj's z.  d_v
+ * must be 128, Hv and d_model multiples of 8. */
+int gdn_out_proj(const void* o, const void* z, const float* norm_w, float eps, const void* w_out,
+                 int T, int Hv, int d_v, int d_model, void* o_norm, void* y, uint32_t* flags,
+                 void* stream);
+
 /* Read (and optionally clear) the OR of GDN_FLAG_* raised by earlier forwards
  * on one layer (layer < 0: OR over all layers).  Synchronises `stream`; not
  * for the hot path. */

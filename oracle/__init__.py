@@ -18,6 +18,9 @@ Contents:
   * ``read_pool_states`` -- decode a pool byte image with that layout;
   * ``ssd_scan_head`` / ``ssd_forward`` -- the Mamba2 mixer's selective scan
                         (C, ssd_oracle.c) on one chain and on a packed batch;
+  * ``in_proj`` / ``gated_rmsnorm`` / ``out_proj`` -- the dense neighbours
+                        of the forward in the layer (the projections around it
+                        and the gated output norm), fp64;
   * ``product_form_final_state`` / ``chunked_wy_forward`` and their KDA
     counterparts ``kda_product_form_final_state`` / ``kda_chunked_forward``
     -- independent restatements of the recurrences used only to pin the token
@@ -538,3 +541,35 @@ def ssd_chunked_forward(x, B, C, dt, a_log_decay, Dskip, h0, chunk=64):
         y, h = ssd_quadratic_form(x[sl], B[sl], C[sl], dt[sl], a_log_decay[sl], Dskip, h)
         ys.append(y)
     return np.concatenate(ys, axis=0), h
+
+
+# ---------------------------------------------------------------------------
+# The dense neighbours of the forward in a hybrid model's gated-delta-net layer
+# (the pages name the layer; its projections are the plainest reading of what
+# surrounds the varlen forward).  A matmul is the library primitive here.
+
+def in_proj(hidden, w_qkv, w_z, w_b, w_a):
+    """Input projection, token by token: x_qkv = W_qkv h, z = W_z h, b = W_b h,
+    a = W_a h (weights [out][in]).  fp64.  Returns (x_qkv, z, b, a) as
+    [T][C], [T][Hv*d_v], [T][Hv], [T][Hv]."""
+    h = _f64(hidden)
+    return tuple(h @ _f64(w).T for w in (w_qkv, w_z, w_b, w_a))
+
+
+def gated_rmsnorm(o, z, norm_w, eps):
+    """Gated RMS norm of the layer's output, per token and v-head over its d_v
+    channels: o / sqrt(mean(o^2) + eps) * norm_w * silu(z), silu(z) =
+    z / (1 + e^{-z}).  o, z: [T][Hv][d_v]; norm_w: [d_v].  fp64."""
+    o = _f64(o)
+    z = _f64(z)
+    rs = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    with np.errstate(over="ignore"):
+        silu = z / (1.0 + np.exp(-z))
+    return o * rs * _f64(norm_w) * silu
+
+
+def out_proj(o_norm, w_out):
+    """Output projection, token by token: y = W_out o_norm (o_norm flattened over
+    its heads; W_out [d_model][Hv*d_v]).  fp64."""
+    o = _f64(o_norm)
+    return o.reshape(o.shape[0], -1) @ _f64(w_out).T
