@@ -184,6 +184,64 @@ Layout ssd_layout_of(int num_blocks, int num_layers, int H, int P, int NS, int G
   return l;
 }
 
+// Host checks and kernel parameters shared by the gated-delta-net forwards
+// (scalar gate, or one gate per key channel with `channel_gate`): returns
+// GDN_OK with *fp filled, or the status of the first failed check (nothing
+// launched).  *fp_empty is set when there is nothing to do (N == 0, T == 0).
+int prepare_forward(gdn_pool* p, int layer, const void* x_qkv, const void* a, const void* b,
+                    const int32_t* cu_seqlens, const int32_t* state_block_idx,
+                    const uint8_t* has_past, const gdn_weights_t* w, void* out, int T, int N,
+                    int max_seqlen_hint, bool channel_gate, gdn::FwdParams* fp, bool* fp_empty) {
+  *fp_empty = false;
+  if (!p || !w) return GDN_ERR_NULL;
+  if (p->kind != 0) return GDN_ERR_DIMS;
+  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
+    return GDN_ERR_RANGE;
+  if (N == 0) {
+    *fp_empty = true;
+    return T == 0 ? GDN_OK : GDN_ERR_RANGE;
+  }
+  if (!cu_seqlens || !state_block_idx || !has_past || !w->conv_w || !w->A_log || !w->dt_bias)
+    return GDN_ERR_NULL;
+  if (T > 0 && (!x_qkv || !a || !b || !out)) return GDN_ERR_NULL;
+  const int C = 2 * p->Hk * p->dk + p->Hv * p->dv;
+  const size_t act_bytes = p->act == GDN_F32 ? 4 : 2;
+  if ((long long)T * C > (1ll << 40)) return GDN_ERR_RANGE;
+  if (T > 0 && (!aligned16(x_qkv) || !aligned16(a) || !aligned16(b) || !aligned16(out)))
+    return GDN_ERR_ALIGN;
+  if (!aligned16(w->conv_w) || ((size_t)C * act_bytes) % 16 != 0 ||
+      ((size_t)p->dv * act_bytes) % 16 != 0 ||
+      (channel_gate && ((size_t)p->dk * act_bytes) % 16 != 0))
+    return GDN_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev != p->device) return GDN_ERR_DEVICE;
+  fp->x = x_qkv;
+  fp->a = a;  // [T][Hv], or [T][Hv][d_k] with one gate per key channel
+  fp->b = b;
+  fp->cu = cu_seqlens;
+  fp->blk = state_block_idx;
+  fp->has_past = has_past;
+  fp->conv_w = w->conv_w;
+  fp->A_log = w->A_log;
+  fp->dt_bias = w->dt_bias;  // [Hv], or [Hv][d_k] with one gate per key channel
+  fp->out = out;
+  fp->layer_base = p->base + (size_t)layer * p->num_blocks * p->stride;
+  fp->stride = p->stride;
+  fp->rec_off = p->rec_off;
+  fp->T = T;
+  fp->N = N;
+  fp->Hk = p->Hk;
+  fp->Hv = p->Hv;
+  fp->C = C;
+  fp->K = p->K;
+  fp->num_blocks = p->num_blocks;
+  fp->max_seqlen_hint = max_seqlen_hint;
+  fp->work.base = p->work + (size_t)layer * gdn::WorkArea::words(p->num_blocks);
+  fp->work.num_blocks = p->num_blocks;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -319,51 +377,11 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
                        const int32_t* cu_seqlens, const int32_t* state_block_idx,
                        const uint8_t* has_past, const gdn_weights_t* w, void* out, int T, int N,
                        int max_seqlen_hint, void* stream) {
-  if (!p || !w) return GDN_ERR_NULL;
-  if (p->kind != 0) return GDN_ERR_DIMS;
-  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
-    return GDN_ERR_RANGE;
-  if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
-  if (!cu_seqlens || !state_block_idx || !has_past || !w->conv_w || !w->A_log || !w->dt_bias)
-    return GDN_ERR_NULL;
-  if (T > 0 && (!x_qkv || !a || !b || !out)) return GDN_ERR_NULL;
-  const int C = 2 * p->Hk * p->dk + p->Hv * p->dv;
-  const size_t act_bytes = p->act == GDN_F32 ? 4 : 2;
-  if ((long long)T * C > (1ll << 40)) return GDN_ERR_RANGE;
-  if (T > 0 && (!aligned16(x_qkv) || !aligned16(a) || !aligned16(b) || !aligned16(out)))
-    return GDN_ERR_ALIGN;
-  if (!aligned16(w->conv_w) || ((size_t)C * act_bytes) % 16 != 0 ||
-      ((size_t)p->dv * act_bytes) % 16 != 0)
-    return GDN_ERR_ALIGN;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-  if (dev != p->device) return GDN_ERR_DEVICE;
-
   gdn::FwdParams fp;
-  fp.x = x_qkv;
-  fp.a = a;
-  fp.b = b;
-  fp.cu = cu_seqlens;
-  fp.blk = state_block_idx;
-  fp.has_past = has_past;
-  fp.conv_w = w->conv_w;
-  fp.A_log = w->A_log;
-  fp.dt_bias = w->dt_bias;
-  fp.out = out;
-  fp.layer_base = p->base + (size_t)layer * p->num_blocks * p->stride;
-  fp.stride = p->stride;
-  fp.rec_off = p->rec_off;
-  fp.T = T;
-  fp.N = N;
-  fp.Hk = p->Hk;
-  fp.Hv = p->Hv;
-  fp.C = C;
-  fp.K = p->K;
-  fp.num_blocks = p->num_blocks;
-  fp.max_seqlen_hint = max_seqlen_hint;
-  fp.work.base = p->work + (size_t)layer * gdn::WorkArea::words(p->num_blocks);
-  fp.work.num_blocks = p->num_blocks;
-
+  bool empty = false;
+  const int st = prepare_forward(p, layer, x_qkv, a, b, cu_seqlens, state_block_idx, has_past, w,
+                                 out, T, N, max_seqlen_hint, false, &fp, &empty);
+  if (st != GDN_OK || empty) return st;
   cudaStream_t s = (cudaStream_t)stream;
   // prefill scratch of the split path: grown on demand, stream-ordered,
   // outside stream capture; without enough of it the fused chunked kernel runs
@@ -472,51 +490,11 @@ int gdn_kda_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const vo
                            const int32_t* state_block_idx, const uint8_t* has_past,
                            const gdn_weights_t* w, void* out, int T, int N, int max_seqlen_hint,
                            void* stream) {
-  if (!p || !w) return GDN_ERR_NULL;
-  if (p->kind != 0) return GDN_ERR_DIMS;
-  if (layer < 0 || layer >= p->num_layers || T < 0 || N < 0 || max_seqlen_hint < 0)
-    return GDN_ERR_RANGE;
-  if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_RANGE;
-  if (!cu_seqlens || !state_block_idx || !has_past || !w->conv_w || !w->A_log || !w->dt_bias)
-    return GDN_ERR_NULL;
-  if (T > 0 && (!x_qkv || !a || !b || !out)) return GDN_ERR_NULL;
-  const int C = 2 * p->Hk * p->dk + p->Hv * p->dv;
-  const size_t act_bytes = p->act == GDN_F32 ? 4 : 2;
-  if ((long long)T * C > (1ll << 40)) return GDN_ERR_RANGE;
-  if (T > 0 && (!aligned16(x_qkv) || !aligned16(a) || !aligned16(b) || !aligned16(out)))
-    return GDN_ERR_ALIGN;
-  if (!aligned16(w->conv_w) || ((size_t)C * act_bytes) % 16 != 0 ||
-      ((size_t)p->dv * act_bytes) % 16 != 0 || ((size_t)p->dk * act_bytes) % 16 != 0)
-    return GDN_ERR_ALIGN;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-  if (dev != p->device) return GDN_ERR_DEVICE;
-
   gdn::FwdParams fp;
-  fp.x = x_qkv;
-  fp.a = a;  // [T][Hv][d_k]
-  fp.b = b;
-  fp.cu = cu_seqlens;
-  fp.blk = state_block_idx;
-  fp.has_past = has_past;
-  fp.conv_w = w->conv_w;
-  fp.A_log = w->A_log;
-  fp.dt_bias = w->dt_bias;  // [Hv][d_k]
-  fp.out = out;
-  fp.layer_base = p->base + (size_t)layer * p->num_blocks * p->stride;
-  fp.stride = p->stride;
-  fp.rec_off = p->rec_off;
-  fp.T = T;
-  fp.N = N;
-  fp.Hk = p->Hk;
-  fp.Hv = p->Hv;
-  fp.C = C;
-  fp.K = p->K;
-  fp.num_blocks = p->num_blocks;
-  fp.max_seqlen_hint = max_seqlen_hint;
-  fp.work.base = p->work + (size_t)layer * gdn::WorkArea::words(p->num_blocks);
-  fp.work.num_blocks = p->num_blocks;
-
+  bool empty = false;
+  const int st = prepare_forward(p, layer, x_qkv, a, b, cu_seqlens, state_block_idx, has_past, w,
+                                 out, T, N, max_seqlen_hint, true, &fp, &empty);
+  if (st != GDN_OK || empty) return st;
   cudaStream_t s = (cudaStream_t)stream;
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;

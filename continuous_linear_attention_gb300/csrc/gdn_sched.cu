@@ -19,6 +19,9 @@ namespace gdn {
 namespace {
 
 constexpr int kSchedThreads = 1024;
+// pools of up to this many blocks keep their block-use counts in shared
+// memory (fast atomics, no global round trips); larger ones in the work area
+constexpr int kSmemCounts = 8192;
 
 __global__ void __launch_bounds__(kSchedThreads)
 schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk, int N, int T,
@@ -26,10 +29,11 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
   __shared__ int s_bad;
   __shared__ int s_n_items, s_n_dec, s_n_pre, s_pre_tokens;
   __shared__ unsigned s_flags;
+  __shared__ int32_t s_counts[kSmemCounts];
   pdl_wait_then_release();  // launched plainly: lets the next kernel launch early
   const int tid = threadIdx.x;
   int32_t* hdr = work.header();
-  int32_t* blk_count = work.blk_count();
+  int32_t* blk_count = num_blocks <= kSmemCounts ? s_counts : work.blk_count();
   if (tid == 0) {
     s_bad = (cu[0] != 0 || cu[N] != T) ? 1 : 0;
     s_n_items = s_n_dec = s_n_pre = s_pre_tokens = 0;
