@@ -169,6 +169,18 @@ def prefill_flops(wl, chunk: int = 64) -> float:
     return float(d.Hv * per * toks)
 
 
+def prefill_cost(wl):
+    """Algorithmic HBM bytes (x, gate inputs and out rows of the sequences
+    longer than one token; the per-channel rule's gate input a has d_k values
+    per v-head) and the chunked form's flops."""
+    d = wl.dims
+    act = 4 if d.act == "f32" else 2
+    toks = sum(L for L in wl.seqlens() if L > 1)
+    gate = d.Hv * (d.dk if wl.channel_gate else 1)
+    nbytes = toks * (d.C + gate + d.Hv + d.Hv * d.dv) * act
+    return nbytes, prefill_flops(wl)
+
+
 def time_secondary(harness, wl, steps, device, pk, graph=False, warmup=3):
     """Tokens/s and the compute kernels' roofline for another workload (the
     ~16k-token prefill, the mixed batch), timed like the main line; with
@@ -265,11 +277,30 @@ def _seqlens(wl):
     return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
 
 
+def ssd_prefill_workload(synth):
+    """The Mamba2 prefill batch: the ~16k-token prefill's 8 lengths, no past,
+    H = 128, P = 64, N = 128, G = 8, K = 4, bf16."""
+    dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
+    lens = synth.prefill_lengths()
+    return synth.make_ssd_workload("mamba2_prefill_8seq_16k_h128_p64_n128_g8", dims, lens,
+                                   [0] * len(lens), 64, 2)
+
+
+def kda_prefill_workload(synth):
+    """The ~16k-token prefill's lengths and head dims under the per-channel
+    decay rule, no past."""
+    lens = synth.prefill_lengths()
+    return synth.make_workload("kda_prefill_8seq_16k", synth.FULL_DIMS, lens, [0] * len(lens),
+                               64, 2, channel_gate=True)
+
+
 def time_variant_prefill(harness, wl, steps, device, pk):
-    """A Mamba2 prefill batch: tokens/s and both roofline fractions of its
-    compute kernels (the scan is HBM-bound at these sizes)."""
+    """A prefill batch of another layer family (the Mamba2 scan, the
+    per-channel decay rule): tokens/s and both roofline fractions of its
+    compute kernels."""
     import torch
-    run = harness.SsdDeviceRun(wl, device=device)
+    ssd = hasattr(wl, "ssm_state")
+    run = (harness.SsdDeviceRun if ssd else harness.DeviceRun)(wl, device=device)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         run.run(stream)
@@ -286,7 +317,7 @@ def time_variant_prefill(harness, wl, steps, device, pk):
     kms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(steps))
     flags = run.pool.error_flags()
     run.close()
-    nbytes, flops = ssd_prefill_cost(wl)
+    nbytes, flops = ssd_prefill_cost(wl) if ssd else prefill_cost(wl)
     gbs = nbytes / (kms / 1e3) / 1e9
     tf = flops / (kms / 1e3) / 1e12
     return {"workload": wl.name, "tokens": wl.T, "compute_kernels_ms": kms,
@@ -495,10 +526,11 @@ def main():
     ap.add_argument("--variants", action="store_true",
                     help="also time the decode batches of the per-channel-decay rule and of "
                          "the Mamba2 scan")
-    ap.add_argument("--profile", choices=["prefill", "mixed", "proj"], default=None,
-                    help="profiler aid: run only the ~16k-token prefill, the mixed batch or "
-                         "the layer's projections on 15843 tokens, --warmup + --steps times, "
-                         "and print their timing line")
+    ap.add_argument("--profile", choices=["prefill", "mixed", "proj", "ssd_prefill"],
+                    default=None,
+                    help="profiler aid: run only the ~16k-token prefill, the mixed batch, "
+                         "the layer's projections on 15843 tokens or the Mamba2 prefill of the "
+                         "same lengths, --warmup + --steps times, and print their timing line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -523,6 +555,11 @@ def main():
     if args.profile == "proj":
         from continuous_linear_attention_gb300 import binding
         res = time_projections(binding, synth, 15843, args.steps, f"cuda:{local_rank}", peaks())
+        print(json.dumps({"profile": args.profile, **res}), flush=True)
+        return
+    if args.profile == "ssd_prefill":
+        res = time_variant_prefill(harness, ssd_prefill_workload(synth), args.steps,
+                                   f"cuda:{local_rank}", peaks())
         print(json.dumps({"profile": args.profile, **res}), flush=True)
         return
     if args.profile:
@@ -651,14 +688,12 @@ def main():
                                           synth.SsdDims(H=128, P=64, N=128, G=8, K=4,
                                                         act="bf16"),
                                           [1] * 256, [1] * 256, 512, 1)
-            ssd_dims = synth.SsdDims(H=128, P=64, N=128, G=8, K=4, act="bf16")
-            lens = synth.prefill_lengths()
-            ssd_pre = synth.make_ssd_workload("mamba2_prefill_8seq_16k_h128_p64_n128_g8",
-                                              ssd_dims, lens, [0] * len(lens), 64, 2)
+            ssd_pre = ssd_prefill_workload(synth)
             line["variants"] = [
                 time_variant_decode(harness, kda, 200, dev, pk, decode_bytes(kda)),
                 time_variant_decode(harness, ssd, 200, dev, pk, ssd_decode_bytes(ssd)),
                 time_variant_prefill(harness, ssd_pre, 10, dev, pk),
+                time_variant_prefill(harness, kda_prefill_workload(synth), 5, dev, pk),
             ]
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, one_thread_s=4.0)

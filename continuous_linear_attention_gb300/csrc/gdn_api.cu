@@ -25,7 +25,7 @@ struct gdn_pool {
   // net pools, capacity in 64-token chunks) or the fp16 conv output of the
   // chunked scan (Mamba2 pools, capacity in tokens); allocated stream-ordered
   unsigned char* scr;
-  size_t scr_units;
+  size_t scr_bytes;
   bool scr_grow;  // false: never allocated; the fused chunked kernel is used
   int last_path;  // GDN_PREFILL_* of the last forward
   // 0: gated delta net pool (conv + recurrent state); 1: Mamba2 pool (conv +
@@ -45,11 +45,18 @@ size_t roundup(size_t v, size_t m) { return (v + m - 1) / m * m; }
 // copies:
 //   QK [chunk][Hk]  the [q~ ; k~] tile: 2 K-blocks x (64 q~ rows, 64 k~ rows) fp16
 //   G  [chunk][Hk]  (G, beta) of the k-head's two v-heads per token, fp32 [64][4]
+//                   (per-channel decay: e^{Gamma_C} of both v-heads, fp32 [2][128])
 //   W  [chunk][Hv]  -w: 2 boxes of 64 channels x 64 tokens fp16
 //   U  [chunk][Hv]  u:  2 boxes of 64 channels x 64 tokens fp16
 //   P  [chunk][Hv]  P:  64 x 64 fp16
 //   C  [chunk]      record (first packed row, valid tokens, chunk index, sequence)
-enum ScrPart { kScrQK = 0, kScrG, kScrW, kScrU, kScrP, kScrC, kScrParts };
+// and, for the per-channel-decay forward only,
+//   V  [chunk][Hv]  v:  2 boxes of 64 channels x 64 tokens fp16 (conv output)
+//   QH [chunk][Hv]  [q^ ; k^]: the decayed q~ and k~ of the v-head, QK's layout
+// The buffer is laid out part-major for the capacity of the layout a call
+// uses (the scalar forward's six parts, or all eight).
+enum ScrPart { kScrQK = 0, kScrG, kScrW, kScrU, kScrP, kScrC, kScrV, kScrQH, kScrParts };
+constexpr int kScrScalarParts = kScrV;
 size_t scratch_part_bytes(const gdn_pool* p, int part) {
   switch (part) {
     case kScrQK: return (size_t)p->Hk * 64 * 2 * p->dk * 2;
@@ -57,16 +64,22 @@ size_t scratch_part_bytes(const gdn_pool* p, int part) {
     case kScrW: return (size_t)p->Hv * 64 * p->dk * 2;
     case kScrU: return (size_t)p->Hv * 64 * p->dv * 2;
     case kScrC: return 16;
+    case kScrV: return (size_t)p->Hv * 64 * p->dv * 2;
+    case kScrQH: return (size_t)p->Hv * 64 * 2 * p->dk * 2;
     default: return (size_t)p->Hv * 64 * 64 * 2;
   }
 }
-// Bytes of one scratch unit: a 64-token chunk (gated delta net pools) or one
-// token row of C fp16 channels (Mamba2 pools).
-size_t scratch_unit_bytes(const gdn_pool* p) {
+// Bytes of one scratch unit: a 64-token chunk of the first `parts` parts
+// (gated delta net pools) or one token row of C fp16 channels (Mamba2 pools).
+size_t scratch_unit_bytes(const gdn_pool* p, int parts = kScrScalarParts) {
   if (p->kind != 0) return ((size_t)p->ssd_H * p->ssd_P + 2 * (size_t)p->ssd_G * p->ssd_N) * 2;
   size_t b = 0;
-  for (int i = 0; i < kScrParts; ++i) b += scratch_part_bytes(p, i);
+  for (int i = 0; i < parts; ++i) b += scratch_part_bytes(p, i);
   return b;
+}
+// Units the current buffer holds in the layout of the first `parts` parts.
+size_t scratch_cap(const gdn_pool* p, int parts = kScrScalarParts) {
+  return p->scr ? p->scr_bytes / scratch_unit_bytes(p, parts) : 0;
 }
 // Units a call with T tokens and N sequences can need: at most T/64 + (number
 // of prefill sequences) chunks, and at most one prefill sequence per
@@ -77,26 +90,28 @@ size_t scratch_units_for(const gdn_pool* p, long long T, long long N) {
   if (seqs > p->num_blocks - 1) seqs = p->num_blocks - 1;
   return (size_t)(T / 64 + seqs + 1);
 }
-void* scratch_part(const gdn_pool* p, int part) {
+void* scratch_part(const gdn_pool* p, int part, int parts = kScrScalarParts) {
   size_t off = 0;
   for (int i = 0; i < part; ++i) off += scratch_part_bytes(p, i);
-  return p->scr + off * p->scr_units;
+  return p->scr + off * scratch_cap(p, parts);
 }
 
-// Make the scratch hold `units` units, stream-ordered on `s` (the old buffer
-// is freed on the stream after every earlier use of it; nothing waits for the
-// device).  With `sync`, waits for `s` afterwards.
-int scratch_grow(gdn_pool* p, size_t units, cudaStream_t s, bool sync) {
-  if (p->scr_units >= units) return GDN_OK;
-  const size_t cap = roundup(units, p->kind == 0 ? 64 : 4096);
+// Make the scratch hold `units` units of the first `parts` parts' layout,
+// stream-ordered on `s` (the old buffer is freed on the stream after every
+// earlier use of it; nothing waits for the device).  With `sync`, waits for
+// `s` afterwards.
+int scratch_grow(gdn_pool* p, size_t units, cudaStream_t s, bool sync,
+                 int parts = kScrScalarParts) {
+  if (scratch_cap(p, parts) >= units) return GDN_OK;
+  const size_t bytes = roundup(units, p->kind == 0 ? 64 : 4096) * scratch_unit_bytes(p, parts);
   void* np = nullptr;
-  if (cudaMallocAsync(&np, cap * scratch_unit_bytes(p), s) != cudaSuccess || !np) {
+  if (cudaMallocAsync(&np, bytes, s) != cudaSuccess || !np) {
     cudaGetLastError();
     return GDN_ERR_NOMEM;
   }
   if (p->scr) cudaFreeAsync(p->scr, s);
   p->scr = (unsigned char*)np;
-  p->scr_units = cap;
+  p->scr_bytes = bytes;
   if (sync && cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;
 }
@@ -106,7 +121,7 @@ void scratch_release(gdn_pool* p) {
     cudaStreamSynchronize(0);
   }
   p->scr = nullptr;
-  p->scr_units = 0;
+  p->scr_bytes = 0;
 }
 bool capturing(cudaStream_t s) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -296,7 +311,7 @@ int gdn_state_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int 
   p->K = K;
   p->act = act;
   p->scr = nullptr;
-  p->scr_units = 0;
+  p->scr_bytes = 0;
   p->scr_grow = true;
   p->last_path = GDN_PREFILL_NONE;
   p->stride = l.stride;
@@ -389,9 +404,9 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
                        gdn::chunk_supported(p->dk, p->act, p->K);
   const bool may_prefill = T > 1 && max_seqlen_hint != 1;
   const size_t need = scratch_units_for(p, T, N);
-  if (chunked && may_prefill && p->scr_grow && need > p->scr_units && !capturing(s))
+  if (chunked && may_prefill && p->scr_grow && need > scratch_cap(p) && !capturing(s))
     scratch_grow(p, need, s, false);
-  if (chunked && may_prefill && p->scr && p->scr_units >= need) {
+  if (chunked && may_prefill && scratch_cap(p) >= need) {
     fp.scr_qk = scratch_part(p, kScrQK);
     fp.scr_g = scratch_part(p, kScrG);
     fp.scr_w = scratch_part(p, kScrW);
@@ -496,6 +511,28 @@ int gdn_kda_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const vo
                                  out, T, N, max_seqlen_hint, true, &fp, &empty);
   if (st != GDN_OK || empty) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  // the split prefill (conv pass, chunk products, recurrence) needs the
+  // scratch in its eight-part layout: grown on demand, stream-ordered,
+  // outside stream capture; without it the token-serial kernel runs
+  const bool chunked = gdn::decode_supported(p->dk, p->act, p->Hk, p->Hv, p->K) &&
+                       gdn::chunk_supported(p->dk, p->act, p->K);
+  const bool may_prefill = T > 1 && max_seqlen_hint != 1;
+  const size_t need = scratch_units_for(p, T, N);
+  if (chunked && may_prefill && p->scr_grow && need > scratch_cap(p, kScrParts) && !capturing(s))
+    scratch_grow(p, need, s, false, kScrParts);
+  if (chunked && may_prefill && scratch_cap(p, kScrParts) >= need) {
+    fp.scr_qk = scratch_part(p, kScrQK, kScrParts);
+    fp.scr_g = scratch_part(p, kScrG, kScrParts);
+    fp.scr_w = scratch_part(p, kScrW, kScrParts);
+    fp.scr_u = scratch_part(p, kScrU, kScrParts);
+    fp.scr_p = scratch_part(p, kScrP, kScrParts);
+    fp.scr_c = scratch_part(p, kScrC, kScrParts);
+    fp.scr_v = scratch_part(p, kScrV, kScrParts);
+    fp.scr_qh = scratch_part(p, kScrQH, kScrParts);
+  }
+  p->last_path = !may_prefill ? GDN_PREFILL_NONE
+                 : fp.scr_qk  ? GDN_PREFILL_SPLIT
+                              : GDN_PREFILL_SERIAL;
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (p->ev_before && cudaEventRecord(p->ev_before, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (T > 0) {
@@ -506,8 +543,11 @@ int gdn_kda_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const vo
       if (gdn::launch_kda_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
       int max_long = max_items < T / 2 ? max_items : T / 2;
       if (max_seqlen_hint == 1) max_long = 0;
-      if (gdn::launch_kda_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess)
+      if (fp.scr_qk) {
+        if (gdn::launch_kda_chunk(fp, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;
+      } else if (gdn::launch_kda_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess) {
         return GDN_ERR_CUDA;
+      }
     } else if (gdn::launch_kda_recurrent(fp, p->dk, p->act, max_items, false, s) !=
                cudaSuccess) {
       return GDN_ERR_CUDA;
@@ -554,7 +594,7 @@ int gdn_ssd_pool_create(gdn_pool_t** out, int num_blocks, int num_layers, int H,
   p->K = K;
   p->act = act;
   p->scr = nullptr;
-  p->scr_units = 0;
+  p->scr_bytes = 0;
   p->scr_grow = true;  // the chunked scan's fp16 conv scratch, grown on demand
   p->last_path = GDN_PREFILL_NONE;
   p->stride = l.stride;
@@ -654,7 +694,7 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
   cudaStream_t s = (cudaStream_t)stream;
   // fp16 conv scratch of the chunked scan: grown on demand, stream-ordered,
   // outside stream capture
-  if (p->scr_grow && (size_t)T > p->scr_units && T > 1 && max_seqlen_hint != 1 &&
+  if (p->scr_grow && (size_t)T > scratch_cap(p) && T > 1 && max_seqlen_hint != 1 &&
       gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act) && !capturing(s))
     scratch_grow(p, (size_t)T, s, false);
   if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
@@ -670,7 +710,7 @@ int gdn_ssd_varlen_forward(gdn_pool_t* p, int layer, const void* xbc, const void
       if (gdn::launch_ssd_decode(sp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
       int max_long = max_items < T / 2 ? max_items : T / 2;
       if (max_seqlen_hint == 1) max_long = 0;
-      const bool chunked = max_long > 0 && p->scr && p->scr_units >= (size_t)T &&
+      const bool chunked = max_long > 0 && scratch_cap(p) >= (size_t)T &&
                            gdn::ssd_chunk_supported(p->ssd_H, p->ssd_P, p->ssd_N, p->K, p->act);
       if (chunked) {
         if (gdn::launch_ssd_chunk(sp, p->scr, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;

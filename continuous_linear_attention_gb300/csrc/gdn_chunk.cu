@@ -738,8 +738,8 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     CUtensorMap tmx;
     e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
     if (e != cudaSuccess) return e;
-    e = launch_cintra(p, &tmx, max_chunks, stream);
-    if (e == cudaSuccess) e = launch_seq(p, grid, stream);
+    e = launch_cintra(p, &tmx, max_chunks, false, stream);
+    if (e == cudaSuccess) e = launch_seq(p, grid, false, stream);
     if (e != cudaSuccess) return e;
   }
   e = cudaGetLastError();
@@ -747,6 +747,36 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   // chains whose fp16 operands left their range, token-serially, before the
   // conv states change
   e = launch_redo(p, D, GDN_BF16, max_pre, stream);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tail_update_kernel, dim3(max_pre, (p.C / 8 + 255) / 256), dim3(256), 0, stream, p);
+}
+
+cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
+  if (max_pre <= 0) return cudaSuccess;
+  if (!p.scr_qk || !p.scr_v || !p.scr_qh) return cudaErrorInvalidValue;
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (num_sms <= 0) num_sms = 1;
+  }
+  const long long chains = (long long)max_pre * p.Hv;
+  const int grid = (int)(chains < num_sms ? chains : num_sms);
+  // at most T/64 + (number of prefill sequences) chunks: the conv pass, the
+  // per-channel-decay chunk products, the recurrence
+  const int max_chunks = p.T / CH + max_pre;
+  CUtensorMap tmx;
+  cudaError_t e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
+  if (e != cudaSuccess) return e;
+  e = launch_cintra(p, &tmx, max_chunks, true, stream);
+  if (e == cudaSuccess) e = launch_kintra(p, max_chunks, stream);
+  if (e == cudaSuccess) e = launch_seq(p, grid, true, stream);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // chains whose fp16 operands left their range, token-serially, before the
+  // conv states change
+  e = launch_kda_redo(p, max_pre, stream);
   if (e != cudaSuccess) return e;
   return launch_pdl(tail_update_kernel, dim3(max_pre, (p.C / 8 + 255) / 256), dim3(256), 0, stream, p);
 }

@@ -36,10 +36,15 @@
 // [q~ ; k~] operand tile, so the X product starts while the v boxes load),
 // then the two v-heads (whose conv writes the token-major v tiles the u
 // products read as MN-major operands).  v never goes to HBM.
+//
+// The conv-only instance serves the per-channel-decay rule: it stops after
+// the conv and writes the [q~ ; k~] tile and the two v tiles to the scratch
+// for kintra_kernel (no gates, no products).
 #include <cuda.h>
 
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
+#include "gdn_solve.cuh"
 #include "gdn_tc.cuh"
 
 namespace gdn {
@@ -57,9 +62,7 @@ constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
 constexpr uint32_t WS_OFF = XBOX_BYTES;  // the box's 64 channels' taps, bf16 [64][4]
 constexpr uint32_t WS_BYTES = 64 * KC * 2;
 static_assert(WS_OFF + WS_BYTES <= XSUB && WS_OFF % 16 == 0, "taps must fit the box padding");
-constexpr int AP = 68;  // pitch (floats) of the fp32 A / T rows
-constexpr int ZP = 20;  // pitch (floats) of the B blocks of the solve
-constexpr int ZB = 16 * ZP;
+constexpr int AP = solve::AP;  // pitch (floats) of the fp32 A / T rows
 constexpr uint32_t BOX = 8192;         // 64 rows x 128 B
 constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of the 128-row [q~ ; k~] tile
 constexpr float kF16Max = 65000.f;
@@ -92,7 +95,7 @@ constexpr uint32_t WT_TAP = 64 * 4;        // one tap of a box's 64 channels, fp
 constexpr uint32_t OFF_WT = OFF_GBE + 512;  // taps of each pass, fp32 [2 passes][4 boxes][4 taps][64 ch]
 constexpr uint32_t SMEM_BYTES = OFF_WT + 2 * 4 * KC * WT_TAP + 1024;
 static_assert(2 * CH * AP * 4 <= 4 * XSUB, "A / T of both heads fit the staging area");
-static_assert(6 * ZB * 4 <= BOX, "B blocks of one head fit the q~ rows of a K-block");
+static_assert(solve::kZFloats * 4 <= BOX, "B blocks of one head fit the q~ rows of a K-block");
 static_assert(OFF_QK % 1024 == 0 && OFF_V % 1024 == 0, "operand tiles on 1024-byte boundaries");
 static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t TM_COLS = 256;  // X (64 columns), then [-w] (0..127) and u (128..255)
@@ -158,97 +161,7 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* fl
   return *flag != 0;
 }
 
-// ---- 16 x 16 block products of the solve on the warp-level tensor-core path
-// (mma.sync m16n8k8, tf32 inputs, fp32 accumulation), each fp32 operand split
-// into a tf32 head (rounded to nearest) and a tail (the exact remainder, which
-// the tensor core reads truncated to tf32: within 2^-21 of the operand), with
-// the three significant cross products kept (hh + ht + th): fp32-level
-// accuracy.
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-// A fragment of k-step k0 of a 16 x 16 block X (at xp, pitch px floats, rows
-// 16-byte aligned) by one ldmatrix.x4 (each 8 x 8 16-bit matrix is an 8 x 4
-// block of fp32), split into its tf32 head and tail.
-__device__ __forceinline__ void a_frag(const float* xp, int px, int k0, uint32_t (&ah)[4],
-                                       uint32_t (&al)[4]) {
-  const int lane = threadIdx.x & 31, mi = lane >> 3;
-  const float* rowp = xp + ((mi & 1) * 8 + (lane & 7)) * px + k0 + (mi >> 1) * 4;
-  uint32_t r[4];
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(rowp)));
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float a = __uint_as_float(r[e]);
-    ah[e] = tf32_rna(a);
-    al[e] = __float_as_uint(a - __uint_as_float(ah[e]));
-  }
-}
-// B fragment Y[k0+t][n0+g], Y[k0+t+4][n0+g] (Y at yp, pitch py), split.
-__device__ __forceinline__ void b_frag(const float* yp, int py, int k0, int n0, uint32_t (&bh)[2],
-                                       uint32_t (&bl)[2]) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float bf[2] = {yp[(k0 + t) * py + n0 + g], yp[(k0 + t + 4) * py + n0 + g]};
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    bh[e] = tf32_rna(bf[e]);
-    bl[e] = __float_as_uint(bf[e] - __uint_as_float(bh[e]));
-  }
-}
-// acc0 / acc1 (this warp's fragments of the two 16 x 8 halves of a 16 x 16
-// block) += X (16 x 16 at xp) * Y[:, 0..7] / Y[:, 8..15] (Y at yp).
-__device__ __forceinline__ void blk_mma3_pair(float (&acc0)[4], float (&acc1)[4], const float* xp,
-                                              int px, const float* yp, int py) {
-  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    uint32_t ah[4], al[4], bh[2], bl[2], bh1[2], bl1[2];
-    a_frag(xp, px, 8 * ks, ah, al);
-    b_frag(yp, py, 8 * ks, 0, bh, bl);
-    b_frag(yp, py, 8 * ks, 8, bh1, bl1);
-    mma_tf32(c0, al, bh);
-    mma_tf32(c1, al, bh1);
-    mma_tf32(c0, ah, bl);
-    mma_tf32(c1, ah, bl1);
-    mma_tf32(acc0, ah, bh);
-    mma_tf32(acc1, ah, bh1);
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    acc0[e] += c0[e];
-    acc1[e] += c1[e];
-  }
-}
-// store a fragment (scaled by s) into a 16 x 16 block at dp (pitch pd), columns n0 ..
-__device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float (&acc)[4],
-                                          float s) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  *reinterpret_cast<float2*>(dp + g * pd + n0 + 2 * t) = make_float2(s * acc[0], s * acc[1]);
-  *reinterpret_cast<float2*>(dp + (g + 8) * pd + n0 + 2 * t) =
-      make_float2(s * acc[2], s * acc[3]);
-}
-// Off-diagonal block (i, j) of T from the B blocks (B_ik = T_ii A_ik at
-// Z + (i(i-1)/2 + k) ZB) and the blocks of T below the diagonal already done:
-// T_ij = -sum_{k=j}^{i-1} B_ik T_kj, stored over A_ij.  One warp.
-__device__ __forceinline__ void level_block(float* AT, const float* Z, int i, int j) {
-  float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int k = j; k < i; ++k)
-    blk_mma3_pair(acc0, acc1, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP);
-  blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
-  blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
-}
-
+template <bool kConvOnly>
 __global__ void __launch_bounds__(kThreads, 2)
 cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   extern __shared__ unsigned char smem_raw[];
@@ -309,7 +222,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   // tid % 64 of head 2kh + tid / 64): g, beta and the inclusive cumulative sum
   // G of g inside the chunk; tokens past the end take g = 0 and beta = 0
   float gcum = 0.f, gbeta = 0.f;
-  if (tid < R * CH) {
+  if (!kConvOnly && tid < R * CH) {
     const int h = kh * R + (tid >> 6), i = tid & 63;
     if (i < n) {
       const size_t row = (size_t)(row0 + i);
@@ -330,7 +243,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  if (tid < R * CH) {
+  if (!kConvOnly && tid < R * CH) {
     const int hl = tid >> 6, i = tid & 63;
     if (i >= 32) gcum += gtot[hl];
     GH[hl * CH + i] = gcum * kLog2e;
@@ -496,10 +409,12 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     tc::fence_before_sync();
     __syncthreads();
     if (tid == 0) {
-      tc::fence_after_sync();
-      tc::mma_tile(tmem, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
-                   tc::idesc_f16_f32(128, 64), false);
-      tc::commit(&mbar);
+      if constexpr (!kConvOnly) {
+        tc::fence_after_sync();
+        tc::mma_tile(tmem, sbase + OFF_QK, KB_STRIDE, sbase + OFF_QK + CH * 128, KB_STRIDE, 2,
+                     tc::idesc_f16_f32(128, 64), false);
+        tc::commit(&mbar);
+      }
       // the [q~ ; k~] tile to the scratch, as the recurrence kernel loads it
       bulk_s2g(static_cast<unsigned char*>(p.scr_qk) + ((size_t)gidx * Hk + kh) * (2 * KB_STRIDE),
                sm + OFF_QK, 2 * KB_STRIDE);
@@ -516,11 +431,22 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       conv_load(3, in);
       conv_finish(3, in);
     }
-    tc::fence_proxy_async_smem();  // the v tiles, read by the u products
-    // the q~ rows take the P tiles next: the [q~ ; k~] store has read them
-    if (tid == 0) bulk_wait_read_all();
-    ok = cta_wait(&mbar, 0, &flag);  // X done; every read of the staging area done
+    tc::fence_proxy_async_smem();  // the v tiles, read by the u products (or stored)
+    if constexpr (kConvOnly) {
+      // the conv-only pass ends here: the two v-heads' v tiles to the scratch
+      __syncthreads();
+      if (tid == 0) {
+        bulk_s2g(static_cast<unsigned char*>(p.scr_v) + ((size_t)gidx * Hv + kh * R) * (2 * BOX),
+                 sm + OFF_V, 4 * BOX);
+        bulk_commit();
+      }
+    } else {
+      // the q~ rows take the P tiles next: the [q~ ; k~] store has read them
+      if (tid == 0) bulk_wait_read_all();
+      ok = cta_wait(&mbar, 0, &flag);  // X done; every read of the staging area done
+    }
   }
+  if constexpr (!kConvOnly) {
   float* AT = reinterpret_cast<float*>(sm + OFF_S);  // [2][64][AP]
   const uint32_t lane = (uint32_t)(tid & 96) << 16;  // TMEM lane quarter of this warp
   const int r128 = tid & 127;                        // TMEM row of this thread
@@ -607,26 +533,9 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       float col[16];
       const int hl = tid >> 6, b = (tid >> 4) & 3, m = tid & 15;
       float* Ab = AT + (hl * CH + 16 * b) * AP + 16 * b;
-      if (tid < R * CH) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float a[16];
-#pragma unroll
-          for (int q = 0; q < (r + 3) / 4; ++q) {
-            const float4 t = *reinterpret_cast<const float4*>(Ab + r * AP + 4 * q);
-            a[4 * q] = t.x; a[4 * q + 1] = t.y; a[4 * q + 2] = t.z; a[4 * q + 3] = t.w;
-          }
-          float acc = r == m ? 1.f : 0.f;
-#pragma unroll
-          for (int j = 0; j < r; ++j) acc -= a[j] * col[j];
-          col[r] = acc;
-        }
-      }
+      if (tid < R * CH) solve::diag_col(Ab, m, col);
       __syncthreads();
-      if (tid < R * CH) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Ab[r * AP + m] = col[r];
-      }
+      if (tid < R * CH) solve::diag_col_store(Ab, m, col);
     }
     // the q~ rows take the B blocks next: the P stores have read them
     if (tid == 0) bulk_wait_read_all();
@@ -640,29 +549,9 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       const int hl = warp >> 2, wl = warp & 3;
       float* ATh = AT + hl * CH * AP;
       float* Z = reinterpret_cast<float*>(sm + OFF_QK + hl * KB_STRIDE);
-#pragma unroll 1
-      for (int bi = wl; bi < 6; bi += 4) {
-        const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
-        const int j = bi - i * (i - 1) / 2;
-        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-        blk_mma3_pair(acc0, acc1, ATh + (16 * i) * AP + 16 * i, AP, ATh + (16 * i) * AP + 16 * j, AP);
-        blk_store(Z + bi * ZB, ZP, 0, acc0, 1.f);
-        blk_store(Z + bi * ZB, ZP, 8, acc1, 1.f);
-        if (j == i - 1) {
-          __syncwarp();
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
-          blk_mma3_pair(acc0, acc1, Z + bi * ZB, ZP, ATh + (16 * j) * AP + 16 * j, AP);
-          blk_store(ATh + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
-          blk_store(ATh + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
-        }
-      }
+      solve::offdiag_first(ATh, Z, wl);
       __syncthreads();
-      if (wl < 2) level_block(ATh, Z, wl + 2, wl);
-      if (wl == 0) {
-        __syncwarp();
-        level_block(ATh, Z, 3, 0);
-      }
+      solve::offdiag_rest(ATh, Z, wl);
     }
     __syncthreads();
     // ---- the MMAs' A tiles over the A / T array once every T value is read:
@@ -788,6 +677,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       }
     }
   }
+  }  // !kConvOnly
   if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
   // v, w, u and the operand tiles enter tensor-core operands in fp16: a value
   // out of its range sends both v-heads of this sequence to the token-serial
@@ -804,13 +694,14 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
 
 }  // namespace
 
-cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks,
+cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks, bool conv_only,
                           cudaStream_t stream) {
   if (max_chunks <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(cintra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = conv_only ? cintra_kernel<true> : cintra_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return launch_pdl(cintra_kernel, dim3(max_chunks, p.Hk), dim3(kThreads), SMEM_BYTES, stream, p,
+  return launch_pdl(kern, dim3(max_chunks, p.Hk), dim3(kThreads), SMEM_BYTES, stream, p,
                     *static_cast<const CUtensorMap*>(x_map));
 }
 

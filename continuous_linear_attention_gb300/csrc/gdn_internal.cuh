@@ -88,6 +88,14 @@ struct FwdParams {
   void* scr_u = nullptr;
   void* scr_p = nullptr;
   void* scr_c = nullptr;
+  // the per-channel-decay rule's split prefill: its gate tile scr_g holds
+  // e^{Gamma_C}, the chunk's decay of every key channel, fp32 [2 v-heads][128],
+  // and it adds
+  //   scr_v  [g][Hv] 16 KiB  v: 2 boxes of 64 channels x 64 tokens (conv output)
+  //   scr_qh [g][Hv] 32 KiB  [q~ e^{Gamma_i} ; k~ e^{Gamma_C - Gamma_j}] in
+  //                          the [q~ ; k~] layout, per v-head
+  void* scr_v = nullptr;
+  void* scr_qh = nullptr;
 };
 
 // The Mamba2 mixer's forward (conv over x | B | C, then the selective scan).
@@ -159,17 +167,29 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
 // reads (max_chunks: host bound on the number of 64-token chunks of the
 // prefill sequences).  x_map: the CUtensorMap of x (boxes of 64 channels x 67
 // rows, 128-byte swizzle).
-cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks,
+// With conv_only, only the conv: the [q~ ; k~] tiles to scr_qk and the v
+// tiles to scr_v (the per-channel-decay rule's first pass).
+cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks, bool conv_only,
                           cudaStream_t stream);
 // The state recurrence over the prefill chains, reading the chunk-major tiles
-// cintra_kernel leaves in the prefill scratch.
-cudaError_t launch_seq(const FwdParams& p, int grid, cudaStream_t stream);
+// cintra_kernel (kda: kintra_kernel) leaves in the prefill scratch.
+cudaError_t launch_seq(const FwdParams& p, int grid, bool kda, cudaStream_t stream);
+// The per-channel-decay rule's state-independent chunk products, one CTA per
+// (64-token chunk, v-head), from the conv-only pass's tiles: gates, the
+// decayed q / k tiles, A and P, the solve, u and -w.
+cudaError_t launch_kintra(const FwdParams& p, int max_chunks, cudaStream_t stream);
 // The per-channel-decay (KDA) rule: p.a is [T][Hv][d_k] and p.dt_bias
 // [Hv][d_k].  Decode kernel for the shapes decode_supported() accepts, and the
 // token-serial kernel (as launch_recurrent) for everything else.
 cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
                                  bool long_only, cudaStream_t stream);
+// The KDA token-serial kernel in redo mode (as launch_redo; d = 128, bf16).
+cudaError_t launch_kda_redo(const FwdParams& p, int max_pre, cudaStream_t stream);
+// The KDA split prefill (d = 128, bf16, Hv = 2 Hk, K = 4, scratch present):
+// conv-only pass, kintra, the recurrence, the redo of out-of-range chains and
+// the conv-state update.
+cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
 // The Mamba2 scan: token-serial kernel over every active sequence (or, with
 // long_only, those longer than one token), then their conv-state update (head
 // dim P in {32, 64}, state size in {32, 64, 128}); and the persistent decode

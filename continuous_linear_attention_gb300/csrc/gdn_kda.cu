@@ -300,9 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(FwdParams p) {
 
 constexpr int kHeadThreads = 256;  // threads per v-head
 
+// mode: kAll every active sequence, kLong those longer than one token, kRedo
+// the v-heads of the prefill list that the chunked prefill marked for a redo
+// (outputs and recurrent states of those heads only; the conv state is left
+// to the conv-state update)
+enum Mode : int { kAll = 0, kLong = 1, kRedo = 2 };
+
 template <int DD, typename Act>
 __global__ void __launch_bounds__(2 * kHeadThreads)
-kda_recurrent_kernel(FwdParams p, bool long_only) {
+kda_recurrent_kernel(FwdParams p, int mode) {
   constexpr int CV = DD / 4;
   constexpr int G = kHeadThreads / CV;
   constexpr int NJ = DD / G;
@@ -310,10 +316,19 @@ kda_recurrent_kernel(FwdParams p, bool long_only) {
   pdl_wait_then_release();
   const int RR = p.Hv / p.Hk;
   const WorkArea& wk = p.work;
+  const bool long_only = mode != kAll;
   const int n_items = wk.header()[long_only ? kNPre : kNItems];
   if ((int)blockIdx.x >= n_items) return;
-  const int s = (long_only ? wk.pre() : wk.items())[blockIdx.x];
   const int kh = blockIdx.y;
+  // redo: the marked v-heads of this k-head group (bits kh*RR .. kh*RR+RR-1)
+  uint32_t marks = (1u << RR) - 1u;
+  if (mode == kRedo) {
+    const int h0 = kh * RR;
+    marks = (reinterpret_cast<const uint32_t*>(wk.redo())[2 * blockIdx.x + (h0 >> 5)] >>
+             (h0 & 31)) & ((1u << RR) - 1u);
+    if (!marks) return;
+  }
+  const int s = (long_only ? wk.pre() : wk.items())[blockIdx.x];
   const int t0 = p.cu[s];
   const int L = p.cu[s + 1] - t0;
   const int wblk = p.blk[s];
@@ -364,6 +379,7 @@ kda_recurrent_kernel(FwdParams p, bool long_only) {
   const int j_head = tid / kHeadThreads;
   const int li = tid % kHeadThreads;
   const int h = kh * RR + j_head;
+  const bool mine = (marks >> j_head) & 1u;  // this thread's v-head is written
   const int cv = li % CV;
   const int rg = li / CV;
   const float* S_r = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * DD * DD;
@@ -446,7 +462,7 @@ kda_recurrent_kernel(FwdParams p, bool long_only) {
       const float u = beta * (vv - sk);
       const float kq = red[2] * qs * ks;
       uo[j_head * DD + li] = u;
-      out[(row * Hv + h) * DD + li] = from_f32<Act>(sq + kq * u);
+      if (mine) out[(row * Hv + h) * DD + li] = from_f32<Act>(sq + kq * u);
     }
     __syncthreads();
     // 5. S <- S Diag(alpha) + u k^T
@@ -464,9 +480,12 @@ kda_recurrent_kernel(FwdParams p, bool long_only) {
     __syncthreads();
   }
 
+  if (mine) {
 #pragma unroll
-  for (int i = 0; i < NJ; ++i)
-    *reinterpret_cast<float4*>(S_w + (size_t)(rg + G * i) * DD + 4 * cv) = S[i];
+    for (int i = 0; i < NJ; ++i)
+      *reinterpret_cast<float4*>(S_w + (size_t)(rg + G * i) * DD + 4 * cv) = S[i];
+  }
+  if (mode == kRedo) return;
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     if (gch[c] < 0) continue;
@@ -477,14 +496,13 @@ kda_recurrent_kernel(FwdParams p, bool long_only) {
 }
 
 template <int DD, typename Act>
-cudaError_t launch_kda_rec(const FwdParams& p, int max_items, bool long_only,
-                           cudaStream_t stream) {
+cudaError_t launch_kda_rec(const FwdParams& p, int max_items, int mode, cudaStream_t stream) {
   const int RR = p.Hv / p.Hk;
   constexpr int G = kHeadThreads / (DD / 4);
   const size_t smem = sizeof(float) * (4 * DD + 2 * 2 * G * DD + 2 * DD + 2 * DD + 4 + 4);
   dim3 grid(max_items, p.Hk);
   const cudaError_t e = launch_pdl(kda_recurrent_kernel<DD, Act>, grid, dim3(RR * kHeadThreads),
-                                   smem, stream, p, long_only);
+                                   smem, stream, p, mode);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -496,14 +514,20 @@ int g_kda_num_sms = 0;
 cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
                                  bool long_only, cudaStream_t stream) {
   if (max_items <= 0) return cudaSuccess;
+  const int mode = long_only ? kLong : kAll;
   if (act == GDN_F32) {
-    if (d == 32) return launch_kda_rec<32, float>(p, max_items, long_only, stream);
-    if (d == 64) return launch_kda_rec<64, float>(p, max_items, long_only, stream);
-    return launch_kda_rec<128, float>(p, max_items, long_only, stream);
+    if (d == 32) return launch_kda_rec<32, float>(p, max_items, mode, stream);
+    if (d == 64) return launch_kda_rec<64, float>(p, max_items, mode, stream);
+    return launch_kda_rec<128, float>(p, max_items, mode, stream);
   }
-  if (d == 32) return launch_kda_rec<32, __nv_bfloat16>(p, max_items, long_only, stream);
-  if (d == 64) return launch_kda_rec<64, __nv_bfloat16>(p, max_items, long_only, stream);
-  return launch_kda_rec<128, __nv_bfloat16>(p, max_items, long_only, stream);
+  if (d == 32) return launch_kda_rec<32, __nv_bfloat16>(p, max_items, mode, stream);
+  if (d == 64) return launch_kda_rec<64, __nv_bfloat16>(p, max_items, mode, stream);
+  return launch_kda_rec<128, __nv_bfloat16>(p, max_items, mode, stream);
+}
+
+cudaError_t launch_kda_redo(const FwdParams& p, int max_pre, cudaStream_t stream) {
+  if (max_pre <= 0) return cudaSuccess;
+  return launch_kda_rec<128, __nv_bfloat16>(p, max_pre, kRedo, stream);
 }
 
 cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {

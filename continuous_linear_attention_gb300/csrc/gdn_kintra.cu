@@ -1,0 +1,480 @@
+// State-independent chunk products of the per-channel-decay (KDA) rule's
+// prefill, one CTA per (64-token chunk, v-head), between the conv-only pass of
+// cintra_kernel (which leaves the chunk's [q~ ; k~] tile and v tiles in the
+// prefill scratch) and the recurrence kernel's KDA instance.
+//
+// The rule (Kimi Linear's delta rule with a decay per key channel, applied to
+// the key columns of S[v][k]) in chunk form, with alpha_s[c] = e^{g_s[c]},
+// Gamma_i[c] = sum_{s <= i} g_s[c] inside the chunk and Gamma_C that of the
+// chunk's last token:
+//   A_ij = beta_i sum_c k~_i[c] k~_j[c] e^{Gamma_i[c] - Gamma_j[c]}   (j < i)
+//   P_ij =        sum_c q~_i[c] k~_j[c] e^{Gamma_i[c] - Gamma_j[c]}   (j <= i)
+//   T = (I + A)^{-1},  u = T diag(beta) v,  w = T diag(beta) (k~ e^{Gamma})
+//   q^_i = q~_i e^{Gamma_i},  k^_j = k~_j e^{Gamma_C - Gamma_j}
+// and the recurrence kernel then forms U = u - w S0^T, O = q^ S0^T + P U and
+// S = S0 Diag(e^{Gamma_C}) + U^T k^.  Every decay factor above is a product
+// of alphas over a token range (all <= 1), so this kernel takes no pairwise
+// exponentials: it forms the per-channel products by running products over
+// the tokens, one thread per channel pair:
+//   q^ and -k~ e^{Gamma} forward from the chunk start, k^ backward from its
+//   end, e^{Gamma_C} at the end;
+//   for the three 16-token sub-chunks I = 1..3, with r the last token before
+//   I: L_I = [q~ ; k~]_I e^{Gamma_i - Gamma_r} forward from r and R_I =
+//   k~_{j <= r} e^{Gamma_r - Gamma_j} backward from r, so that the
+//   off-diagonal 16 x 16 blocks of A and P are plain products L_I R_I^T
+//   (mma.sync, fp16 operands <= 1, fp32 accumulation);
+//   the four diagonal 16 x 16 blocks by running products per pair column j
+//   (fp32, CUDA cores).
+// Then the shared blocked solve for T, T diag(beta) as an fp16 operand, and u
+// and -w on tcgen05 (fp32 in tensor memory).  Every tile leaves in the layout
+// the recurrence kernel loads, by bulk copy: [q^ ; k^] (per v-head), P, u, -w,
+// and e^{Gamma_C} into the k-head's gate tile.  A value of T diag(beta), u or
+// w outside the fp16 range sends the (sequence, v-head) chain to the
+// token-serial redo.
+#include <cuda.h>
+
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+#include "gdn_solve.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int D = 128;
+constexpr int CH = 64;
+constexpr int R = 2;  // v-heads per k-head
+constexpr int kThreads = 256;
+constexpr uint32_t BOX = 8192;         // 64 rows x 128 B
+constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of a 128-row [q ; k] tile
+constexpr int AP = solve::AP;
+constexpr int LRP = 136;  // pitch (halves) of the L / R rows: conflict-free ldmatrix
+constexpr float kF16Max = 65000.f;
+
+// Shared memory (offsets from a 1024-byte aligned base):
+//   QK  [q~ ; k~] of the k-head (loaded); then the u and -w staging tiles
+//   V   v of the v-head: 2 boxes of 64 channels x 64 tokens (loaded)
+//   QH  [q^ ; k^] (built, stored)
+//   NK  -k~ e^{Gamma}: 2 token-major boxes (MN-major B operand of -w)
+//   AL  alpha fp32 [64 tokens][128 channels]
+//   LR  L_1..L_3 (32 rows each: 16 q rows, 16 k rows), then R_1..R_3 (16,
+//       32, 48 rows), fp16 [192][LRP]; after the products: the T diag(beta)
+//       operand (128 rows x 64 tokens, rows 64.. zero) and the solve's B blocks
+//   PT  P fp16 [64 i][64 j] (K-major B operand of the output product)
+//   AT  A, then T, fp32 [64][AP]
+//   GB  beta fp32 [64]
+constexpr uint32_t OFF_QK = 0;
+constexpr uint32_t OFF_V = 32768;
+constexpr uint32_t OFF_QH = 49152;
+constexpr uint32_t OFF_NK = 81920;
+constexpr uint32_t OFF_AL = 98304;
+constexpr uint32_t OFF_LR = 131072;
+constexpr uint32_t OFF_AU = OFF_LR;
+constexpr uint32_t OFF_Z = OFF_LR + 16384;
+constexpr uint32_t OFF_PT = 184320;
+constexpr uint32_t OFF_AT = OFF_PT + BOX;
+constexpr uint32_t OFF_GB = OFF_AT + CH * AP * 4;
+constexpr uint32_t SMEM_BYTES = OFF_GB + CH * 4 + 1024;
+constexpr int kLRows = 96;  // rows of L_1..L_3
+static_assert(OFF_LR + 192 * LRP * 2 <= OFF_PT, "L / R rows");
+static_assert(OFF_Z + solve::kZFloats * 4 <= OFF_PT, "solve blocks");
+static_assert(OFF_PT % 1024 == 0 && OFF_AU % 1024 == 0, "operand tiles on 1024-byte boundaries");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
+constexpr uint32_t TM_COLS = 256;  // u (0..127), -w (128..255)
+
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
+  if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity) ? 1 : 0;
+  __syncthreads();
+  return *flag != 0;
+}
+
+// channel pair (c, c + 1) of row r of a 128-row [q ; k] tile / of a
+// token-major 2-box tile
+__device__ __forceinline__ uint32_t qk_off(int r, int c) {
+  return (uint32_t)(c >> 6) * KB_STRIDE + tc::sw128_offset(r, c & 63);
+}
+__device__ __forceinline__ uint32_t box_off(int r, int c) {
+  return (uint32_t)(c >> 6) * BOX + tc::sw128_offset(r, c & 63);
+}
+__device__ __forceinline__ float2 ld_h2(const unsigned char* p) {
+  return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+__device__ __forceinline__ void st_h2(unsigned char* p, float a, float b) {
+  *reinterpret_cast<__half2*>(p) = __floats2half2_rn(a, b);
+}
+// 8 fp16 (16 bytes) -> fp32
+__device__ __forceinline__ void ld_h8(const unsigned char* p, float* v) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 w;
+  w.x = tc::pack2(v[0], v[1], (__half*)nullptr);
+  w.y = tc::pack2(v[2], v[3], (__half*)nullptr);
+  w.z = tc::pack2(v[4], v[5], (__half*)nullptr);
+  w.w = tc::pack2(v[6], v[7], (__half*)nullptr);
+  return w;
+}
+
+// Warp-level fp16 products (mma.sync m16n8k16, fp32 accumulation) with
+// ldmatrix fragment loads.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4],
+                                        const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t ldbar, mbar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int flag;
+  pdl_wait_then_release();
+  int32_t* hdr = p.work.header();
+  const int gidx = blockIdx.x;
+  if (gidx >= hdr[kPreChunks]) return;
+  // the chunk's record (scheduler): first packed row, valid tokens, chunk
+  // index inside its sequence, sequence
+  const int4 rec = reinterpret_cast<const int4*>(p.scr_c)[gidx];
+  const int h = blockIdx.y, kh = h / R, hl = h % R;
+  const int row0 = rec.x, n = rec.y, kpre = rec.w;
+  // a chain the conv pass already sent to the redo needs no tiles
+  if (redo_marked(p.work, kpre, h)) return;
+  const int Hk = p.Hk, Hv = p.Hv;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t sbase = smem_u32(sm);
+  float* AL = reinterpret_cast<float*>(sm + OFF_AL);
+  float* AT = reinterpret_cast<float*>(sm + OFF_AT);
+  float* GB = reinterpret_cast<float*>(sm + OFF_GB);
+
+  if (tid == 0) {
+    mbar_init(&ldbar, 1);
+    mbar_init(&mbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&ldbar, 2 * KB_STRIDE + 2 * BOX);
+    bulk_g2s(sm + OFF_QK,
+             static_cast<const unsigned char*>(p.scr_qk) + ((size_t)gidx * Hk + kh) * (2 * KB_STRIDE),
+             2 * KB_STRIDE, &ldbar);
+    bulk_g2s(sm + OFF_V, static_cast<const unsigned char*>(p.scr_v) + ((size_t)gidx * Hv + h) * (2 * BOX),
+             2 * BOX, &ldbar);
+  }
+  if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
+
+  // ---- gates: alpha_i[c] = e^{-e^{A_log} softplus(a_i[c] + dt_bias[c])}
+  // (thread: channel tid % 128, tokens 32 (tid / 128) ..; 1 past the end),
+  // beta_i = sigmoid(b_i) (0 past the end); the P tile starts zero
+  {
+    const int c = tid & 127, th = tid >> 7;
+    const float ea = __expf(p.A_log[h]);
+    const float db = p.dt_bias[(size_t)h * D + c];
+    const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(p.a);
+#pragma unroll 8
+    for (int t = 0; t < 32; ++t) {
+      const int i = 32 * th + t;
+      float al = 1.f;
+      if (i < n) {
+        const float x = __bfloat162float(av[((size_t)(row0 + i) * Hv + h) * D + c]) + db;
+        al = __expf(-ea * softplus_f32(x));
+      }
+      AL[i * D + c] = al;
+    }
+    if (tid < CH) {
+      const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
+      GB[tid] = tid < n ? sigmoid_f32(__bfloat162float(bv[(size_t)(row0 + tid) * Hv + h])) : 0.f;
+    }
+    reinterpret_cast<uint4*>(sm + OFF_PT)[tid] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + OFF_PT)[tid + kThreads] = make_uint4(0, 0, 0, 0);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  float amax = 0.f;  // largest |value| entering an fp16 operand or the u / w scratch
+  bool ok = cta_wait(&ldbar, 0, &flag);
+
+  if (ok) {
+    // ---- running products over the tokens, thread group gr = tid / 64 and
+    // channel pair c = 2 (tid % 64)
+    const int gr = tid >> 6, c = 2 * (tid & 63);
+    const unsigned char* QK = sm + OFF_QK;
+    const float2* AL2 = reinterpret_cast<const float2*>(AL) + (c >> 1);  // row i at AL2[i * 64]
+    if (gr == 0) {
+      // q^_i = q~_i e^{Gamma_i}, -k~_i e^{Gamma_i}; e^{Gamma_C} to the gate tile
+      float2 f = make_float2(1.f, 1.f);
+      for (int i = 0; i < CH; ++i) {
+        const float2 a = AL2[i * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+        const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
+        st_h2(sm + OFF_QH + qk_off(i, c), q.x * f.x, q.y * f.y);
+        st_h2(sm + OFF_NK + box_off(i, c), -k.x * f.x, -k.y * f.y);
+      }
+      reinterpret_cast<float2*>(p.scr_g)[(((size_t)gidx * Hk + kh) * R + hl) * (D / 2) + (c >> 1)] = f;
+    } else if (gr == 1) {
+      // k^_j = k~_j e^{Gamma_C - Gamma_j}, backward from the chunk end
+      float2 f = make_float2(1.f, 1.f);
+      for (int j = CH - 1; j >= 0; --j) {
+        const float2 k = ld_h2(QK + qk_off(CH + j, c));
+        st_h2(sm + OFF_QH + qk_off(CH + j, c), k.x * f.x, k.y * f.y);
+        const float2 a = AL2[j * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+      }
+    } else if (gr == 2) {
+      // L_I rows: [q~ ; k~]_i e^{Gamma_i - Gamma_r}, r = 16 I - 1
+      for (int I = 1; I < 4; ++I) {
+        float2 f = make_float2(1.f, 1.f);
+        unsigned char* lr = sm + OFF_LR + (size_t)((I - 1) * 32) * (LRP * 2) + c * 2;
+        for (int t = 0; t < 16; ++t) {
+          const int i = 16 * I + t;
+          const float2 a = AL2[i * 64];
+          f.x *= a.x;
+          f.y *= a.y;
+          const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
+          st_h2(lr + t * (LRP * 2), q.x * f.x, q.y * f.y);
+          st_h2(lr + (16 + t) * (LRP * 2), k.x * f.x, k.y * f.y);
+        }
+      }
+    } else {
+      // R_I rows j = 0 .. r: k~_j e^{Gamma_r - Gamma_j}, backward from r
+      for (int I = 1; I < 4; ++I) {
+        const int r = 16 * I - 1;
+        const int rb = kLRows + 8 * I * (I - 1);  // first row of R_I (96, 112, 144)
+        float2 f = make_float2(1.f, 1.f);
+        for (int j = r; j >= 0; --j) {
+          const float2 k = ld_h2(QK + qk_off(CH + j, c));
+          st_h2(sm + OFF_LR + (size_t)(rb + j) * (LRP * 2) + c * 2, k.x * f.x, k.y * f.y);
+          const float2 a = AL2[j * 64];
+          f.x *= a.x;
+          f.y *= a.y;
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();  // [q^ ; k^] (bulk store) and -k~ e^{Gamma} (MMA operand)
+    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(static_cast<unsigned char*>(p.scr_qh) + ((size_t)gidx * Hv + h) * (2 * KB_STRIDE),
+               sm + OFF_QH, 2 * KB_STRIDE);
+      bulk_commit();
+    }
+
+    // ---- off-diagonal blocks (I, J), I > J: [P ; A / beta] = [L_I^q ; L_I^k]
+    // R_I[16 J ..]^T, one warp per block
+    if (warp < 6) {
+      const int I = warp < 1 ? 1 : (warp < 3 ? 2 : 3);
+      const int J = warp - I * (I - 1) / 2;
+      const int lane = tid & 31;
+      const uint32_t lbase = sbase + OFF_LR + (uint32_t)((I - 1) * 32) * (LRP * 2);
+      const uint32_t rbase = sbase + OFF_LR + (uint32_t)(kLRows + 8 * I * (I - 1) + 16 * J) * (LRP * 2);
+      float acc[2][2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[2][4], b[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          ldsm_x4(lbase + (uint32_t)(mt * 16 + (lane & 15)) * (LRP * 2) + (ks * 16 + (lane >> 4) * 8) * 2,
+                  a[mt]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          ldsm_x2(rbase + (uint32_t)(nt * 8 + (lane & 7)) * (LRP * 2) + (ks * 16 + ((lane >> 3) & 1) * 8) * 2,
+                  b[nt]);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_f16(acc[mt][nt], a[mt], b[nt]);
+      }
+      const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = 16 * I + g + 8 * hh, j = 16 * J + nt * 8 + 2 * t4;
+          st_h2(sm + OFF_PT + tc::sw128_offset(i, j), acc[0][nt][2 * hh], acc[0][nt][2 * hh + 1]);
+          const float bi = GB[i];
+          *reinterpret_cast<float2*>(AT + i * AP + j) =
+              make_float2(bi * acc[1][nt][2 * hh], bi * acc[1][nt][2 * hh + 1]);
+        }
+    }
+    // ---- diagonal blocks: thread (block I, column j = 16 I + jl, channel
+    // quarter cq) walks the block's rows i with the running decay product
+    // f[c] = e^{Gamma_i[c] - Gamma_j[c]} over its 32 channels; the four
+    // quarters' partial sums meet by shuffles
+    {
+      const int I = tid >> 6, jl = (tid >> 2) & 15, cq = tid & 3;
+      const int j = 16 * I + jl, c0 = 32 * cq;
+      float kj[32], f[32];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) ld_h8(QK + qk_off(CH + j, c0 + 8 * m), kj + 8 * m);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] = 1.f;
+#pragma unroll 1
+      for (int tt = 0; tt < 16; ++tt) {
+        const int i = 16 * I + tt;
+        if (tt > jl) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(AL + i * D + c0 + e);
+            f[e] *= a.x;
+            f[e + 1] *= a.y;
+            f[e + 2] *= a.z;
+            f[e + 3] *= a.w;
+          }
+        }
+        float sp = 0.f, sa = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float q8[8], k8[8];
+          ld_h8(QK + qk_off(i, c0 + 8 * m), q8);
+          ld_h8(QK + qk_off(CH + i, c0 + 8 * m), k8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float kf = kj[8 * m + e] * f[8 * m + e];
+            sp = fmaf(q8[e], kf, sp);
+            sa = fmaf(k8[e], kf, sa);
+          }
+        }
+        sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+        sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+        sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+        sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+        if (cq == 0 && tt >= jl) {
+          *reinterpret_cast<__half*>(sm + OFF_PT + tc::sw128_offset(i, j)) = __float2half_rn(sp);
+          if (tt > jl) AT[i * AP + j] = GB[i] * sa;
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();  // the P tile
+    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(static_cast<unsigned char*>(p.scr_p) + ((size_t)gidx * Hv + h) * BOX, sm + OFF_PT, BOX);
+      bulk_commit();
+    }
+    // ---- T = (I + A)^{-1}: diagonal blocks (threads 0..63), then the
+    // off-diagonal blocks (warps 0..3)
+    {
+      float col[16];
+      const int b = (tid >> 4) & 3, m = tid & 15;
+      float* Ab = AT + (16 * b) * AP + 16 * b;
+      if (tid < CH) solve::diag_col(Ab, m, col);
+      __syncthreads();
+      if (tid < CH) solve::diag_col_store(Ab, m, col);
+    }
+    __syncthreads();
+    float* Z = reinterpret_cast<float*>(sm + OFF_Z);
+    if (warp < 4) solve::offdiag_first(AT, Z, warp);
+    __syncthreads();
+    if (warp < 4) solve::offdiag_rest(AT, Z, warp);
+    __syncthreads();
+    // ---- T diag(beta) as the fp16 A operand (rows 64..127 zero): row i,
+    // 8-column group c8 (only the groups at or left of the diagonal block
+    // are T's; the rest are zero)
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int idx = tid + kThreads * q2;
+      const int i = idx >> 3, c8 = idx & 7;
+      float tb[8];
+      if ((c8 >> 1) <= (i >> 4)) {
+        const float4 t0 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8);
+        const float4 t1 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8 + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(GB + c8 * 8);
+        const float4 b1 = *reinterpret_cast<const float4*>(GB + c8 * 8 + 4);
+        tb[0] = t0.x * b0.x; tb[1] = t0.y * b0.y; tb[2] = t0.z * b0.z; tb[3] = t0.w * b0.w;
+        tb[4] = t1.x * b1.x; tb[5] = t1.y * b1.y; tb[6] = t1.z * b1.z; tb[7] = t1.w * b1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tb[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) amax = max_abs3(amax, tb[e], tb[e + 1]);
+      *reinterpret_cast<uint4*>(sm + OFF_AU + tc::sw128_offset(i, c8 * 8)) = pack8(tb);
+      *reinterpret_cast<uint4*>(sm + OFF_AU + tc::sw128_offset(CH + i, c8 * 8)) = make_uint4(0, 0, 0, 0);
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    // u = T diag(beta) v into columns 0..127, -w = T diag(beta) (-k~ e^{Gamma})
+    // into 128..255 (v and -k~ e^{Gamma} as MN-major operands; rows 0..63)
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_op(tmem, tc::Opnd{sbase + OFF_AU, 0u, false}, tc::Opnd{sbase + OFF_V, BOX, true},
+                 CH / 16, tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::mma_op(tmem + 128, tc::Opnd{sbase + OFF_AU, 0u, false}, tc::Opnd{sbase + OFF_NK, BOX, true},
+                 CH / 16, tc::idesc_f16_f32(128, 128, false, true), false);
+      tc::commit(&mbar);
+    }
+    ok = cta_wait(&mbar, 0, &flag);
+  }
+  if (ok) {
+    tc::fence_after_sync();
+    // rows 0..63 (warps 0, 1, 4, 5): u and -w of token r128 into the staging
+    // tiles over the [q~ ; k~] area (free: every read of it is done)
+    const uint32_t lane = (uint32_t)(tid & 96) << 16;
+    const int r128 = tid & 127, hf = tid >> 7;
+    if (r128 < CH) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        unsigned char* box = sm + OFF_QK + part * (2 * BOX) + hf * BOX;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float vv[32];
+          tc::tmem_ld32(tmem + lane + part * 128 + hf * 64 + hh * 32, vv);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) amax = max_abs3(amax, vv[e], vv[e + 1]);
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8)
+            *reinterpret_cast<uint4*>(box + tc::sw128_offset(r128, hh * 32 + g8 * 8)) =
+                pack8(vv + g8 * 8);
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      const size_t tile = ((size_t)gidx * Hv + h) * (2 * BOX);
+      bulk_s2g(static_cast<unsigned char*>(p.scr_u) + tile, sm + OFF_QK, 2 * BOX);
+      bulk_s2g(static_cast<unsigned char*>(p.scr_w) + tile, sm + OFF_QK + 2 * BOX, 2 * BOX);
+      bulk_commit();
+    }
+  }
+  if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+  // T diag(beta), u and w enter tensor-core operands or the scratch in fp16:
+  // a value out of its range sends this chain to the token-serial redo
+  if (__syncthreads_or(!(amax <= kF16Max)) && tid == 0) mark_redo(p.work, kpre, h);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+  if (tid == 0) bulk_wait_all();  // the tiles have reached the scratch before the CTA ends
+}
+
+}  // namespace
+
+cudaError_t launch_kintra(const FwdParams& p, int max_chunks, cudaStream_t stream) {
+  if (max_chunks <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kintra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kintra_kernel, dim3(max_chunks, p.Hv), dim3(kThreads), SMEM_BYTES, stream, p);
+}
+
+}  // namespace gdn

@@ -53,15 +53,18 @@ struct GemmParams {
 };
 
 // tile t -> (group, m-tile, n-tile): groups in order, inside a group the
-// m-tiles of one n-tile next to each other (consecutive CTAs share a B tile)
+// n-tiles of one m-tile next to each other.  The CTAs working at one time
+// then share a few 128-row bands of A, read from DRAM once, and walk all of
+// B_g, which stays in L2 (the layer's weight matrices are 17-34 MB, its A
+// operands 65-130 MB); the other order re-reads A once per n-tile.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& g, int& mt, int& nt) {
   g = 0;
   while (g < p.n_groups - 1 && t >= p.tiles_m * p.g[g].tiles_n) {
     t -= p.tiles_m * p.g[g].tiles_n;
     ++g;
   }
-  nt = t / p.tiles_m;
-  mt = t % p.tiles_m;
+  mt = t / p.g[g].tiles_n;
+  nt = t % p.g[g].tiles_n;
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)

@@ -27,6 +27,13 @@
 // memory, and every compute warp owns one lane quarter and one column half of
 // each step, so the CUDA-core work spreads over all four SM sub-partitions.
 //
+// The per-channel-decay (KDA) instance runs the same steps on that rule's
+// tiles: q^_i = q~_i e^{Gamma_i} and k^_j = k~_j e^{Gamma_C - Gamma_j} (per
+// key channel, from kintra_kernel, one tile per v-head) take the places of
+// q~ and e^{G_C - G_j} k~_j with the output scales 1, -w = -T diag(beta)
+// (k~ e^{Gamma}), and the hand-over scales state column k by its own
+// e^{Gamma_C[k]}: S <- S0 Diag(e^{Gamma_C}).
+//
 // Persistent CTAs, one per SM: warp 8 is the producer (one lane that pulls
 // chains, longest sequences first, from the scheduler's counter and
 // bulk-copies each chunk's tiles, chunk-major in the prefill scratch, into a
@@ -134,6 +141,7 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v) {
   }
 }
 
+template <bool kKda>
 __global__ void __launch_bounds__(kThreads, 1)
 seq_kernel(FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -280,7 +288,11 @@ seq_kernel(FwdParams p) {
           // by K-block into [-w ; q~], k~, u, P and the gate tile
           const int kh = h / R;
           const size_t gi = (size_t)(p.work.pre_cp()[chain / Hv] + c);
-          const unsigned char* qk = static_cast<const unsigned char*>(p.scr_qk) + (gi * p.Hk + kh) * (2 * KB_STRIDE);
+          // scalar gate: the k-head's [q~ ; k~]; per-channel decay: the
+          // v-head's decayed [q^ ; k^]
+          const unsigned char* qk =
+              kKda ? static_cast<const unsigned char*>(p.scr_qh) + (gi * Hv + h) * (2 * KB_STRIDE)
+                   : static_cast<const unsigned char*>(p.scr_qk) + (gi * p.Hk + kh) * (2 * KB_STRIDE);
           const unsigned char* wt = static_cast<const unsigned char*>(p.scr_w) + (gi * Hv + h) * (2 * BOX);
           const unsigned char* ut = static_cast<const unsigned char*>(p.scr_u) + (gi * Hv + h) * (2 * BOX);
           const unsigned char* pt = static_cast<const unsigned char*>(p.scr_p) + (gi * Hv + h) * BOX;
@@ -365,7 +377,10 @@ seq_kernel(FwdParams p) {
       const float* GT = reinterpret_cast<const float*>(st + ST_G);
       const int r2 = d.h % R;
       const int n = d.n;
-      const float GC = GT[(n - 1) * 4 + 2 * r2];
+      // scalar gate: G_C of the chunk; per-channel decay: e^{Gamma_C[k]} of
+      // every key channel k, fp32 [2 v-heads][128]
+      const float GC = kKda ? 0.f : GT[(n - 1) * 4 + 2 * r2];
+      const float* DK = GT + r2 * D;
       if (n < CH) {
         // u rows past the sequence -> 0: the identity product reads every row
         for (int t = tid; t < (CH - n) * 16; t += kCompute)
@@ -402,8 +417,17 @@ seq_kernel(FwdParams p) {
           }
           amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
           tc::tmem_st16u(tmem + lane + TM_S0 + k0 / 2, w16);
+          if constexpr (kKda) {
 #pragma unroll
-          for (int kk = 0; kk < 32; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
+            for (int kk = 0; kk < 32; kk += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(DK + k0 + kk);
+              mul2v(srow[kk], srow[kk + 1], f.x, f.y);
+              mul2v(srow[kk + 2], srow[kk + 3], f.z, f.w);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 32; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
+          }
           tc::tmem_st32(tmem + lane + TM_S + k0, srow);
           tc::tmem_wait_st();
           tc::fence_before_sync();
@@ -422,7 +446,15 @@ seq_kernel(FwdParams p) {
         const int j = tid & 63;
         unsigned char* krow = st + ST_K + ((tid >> 6) & 1) * BOX + j * 128;
         const int c0 = 4 * (tid >> 7);
-        if (j < n) {
+        if (kKda) {
+          // the per-channel decays are in the tile already; rows past n are
+          // zero there too, zeroed again like the scalar tile's
+          if (j >= n) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(krow + (((c0 + c + j) & 7) << 4)) = make_uint4(0, 0, 0, 0);
+          }
+        } else if (j < n) {
           const float ds = __expf(GC - GT[j * 4 + 2 * r2]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -438,7 +470,7 @@ seq_kernel(FwdParams p) {
           for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(krow + (((c0 + c + j) & 7) << 4)) = make_uint4(0, 0, 0, 0);
         }
-        if (tid < CH) EF[tid] = tid < n ? __expf(GT[tid * 4 + 2 * r2]) : 0.f;
+        if (tid < CH) EF[tid] = tid < n ? (kKda ? 1.f : __expf(GT[tid * 4 + 2 * r2])) : 0.f;
         tc::fence_proxy_async_smem();
       }
       if (!wait_c(&mma_y, ph_y)) { dead = true; break; }
@@ -534,11 +566,12 @@ seq_kernel(FwdParams p) {
 
 }  // namespace
 
-cudaError_t launch_seq(const FwdParams& p, int grid, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+cudaError_t launch_seq(const FwdParams& p, int grid, bool kda, cudaStream_t stream) {
+  auto kern = kda ? seq_kernel<true> : seq_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return launch_pdl(seq_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p);
 }
 
 }  // namespace gdn

@@ -735,45 +735,119 @@ ssd_chunk_kernel(SsdParams p, const __grid_constant__ CUtensorMap txs) {
   if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
 }
 
-// Conv + SiLU of every prefill token into the fp16 scratch xs [T][C]: one
-// thread per (sequence, channel), the K-1 window in registers.
-__global__ void __launch_bounds__(256) ssd_prep_kernel(SsdParams p, __half* xs) {
-  pdl_wait_then_release();
-  const int n_pre = p.work.header()[kNPre];
-  if ((int)blockIdx.x >= n_pre) return;
-  const int s = p.work.pre()[blockIdx.x];
-  const int ch = blockIdx.y * blockDim.x + threadIdx.x;
-  const int C = p.C, K = p.K;
-  if (ch >= C) return;
-  const int seq0 = p.cu[s];
-  const int L = p.cu[s + 1] - seq0;
-  const int rblk = p.has_past[s] ? p.blk[s] : 0;
-  const __nv_bfloat16* tail = reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
-  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.xbc);
-  const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
-  float win[kMaxConvK - 1], wc[kMaxConvK];
+// Conv + SiLU of every prefill token into the fp16 scratch xs [T][C], token-
+// parallel: one CTA per (64-token prefill chunk of the scheduler's chunk
+// prefix, every kPrepSlices-th slice of 256 channels); thread (v, q) takes 8
+// channels (one 16-byte vector) of the chunk's tokens 8q .. 8q+7, its K-1
+// window read from the sequence's earlier rows or, before its first token,
+// from the conv state (block 0, all zeros, for a sequence without a past).
+// The chunk lookup (a chain of dependent loads) is paid once per CTA, not
+// once per slice; two CTAs per SM, so that one loads while the other
+// computes.
+//
+// SiLU as h + h tanh(h) with h = y/2 (the taps are halved, which is exact):
+// y sigmoid(y) = y (1 + tanh(y/2)) / 2, one MUFU operation per value;
+// tanh.approx has an absolute error of about 2^-11, so the result is off by
+// about |y| 2^-12, the size of the fp16 rounding that follows.
+constexpr int kPrepTok = 8;     // tokens per thread
+constexpr int kPrepCh = 256;    // channels per slice
+constexpr int kPrepCtaY = 5;    // CTAs per chunk (each takes every 5th slice)
+__device__ __forceinline__ float tanh_approx_f32(float x) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
-  for (int j = 0; j < kMaxConvK - 1; ++j)
-    win[j] = j < K - 1 ? __bfloat162float(tail[(size_t)j * C + ch]) : 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxConvK; ++j) wc[j] = j < K ? __bfloat162float(w[(size_t)ch * K + j]) : 0.f;
-  for (int t = 0; t < L; ++t) {
-    const float xv = __bfloat162float(x[(size_t)(seq0 + t) * C + ch]);
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxConvK; ++j) {
-      if (j < K - 1) acc += wc[j] * win[j];
-      else if (j == K - 1) acc += wc[j] * xv;
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxConvK - 1; ++j) {
-      if (j < K - 2) win[j] = win[j + 1];
-      else if (j == K - 2) win[j] = xv;
-    }
-    xs[(size_t)(seq0 + t) * C + ch] = __float2half_rn(silu_f32(acc));
+  for (int e = 0; e < 4; ++e) {
+    const float2 t = __bfloat1622float2(h2[e]);
+    f[2 * e] = t.x;
+    f[2 * e + 1] = t.y;
   }
 }
 
+template <int KW>
+__global__ void __launch_bounds__(256, 2) ssd_prep_kernel(SsdParams p, __half* __restrict__ xs) {
+  static_assert(KW >= 2 && KW <= kMaxConvK, "conv width");
+  pdl_wait_then_release();
+  const int32_t* hdr = p.work.header();
+  const int g = blockIdx.x;
+  if (g >= hdr[kPreChunks]) return;
+  const int n_pre = hdr[kNPre];
+  const int32_t* pre_cp = p.work.pre_cp();
+  int lo = 0, hi = n_pre - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre_cp[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  const int s = p.work.pre()[lo];
+  const int c = g - pre_cp[lo];
+  const int C = p.C;
+  const int seq0 = p.cu[s];
+  const int L = p.cu[s + 1] - seq0;
+  const int t0 = 64 * c + kPrepTok * (threadIdx.x >> 5);  // first token, sequence-local
+  const int t1 = min(t0 + kPrepTok, L);
+  if (t0 >= t1) return;
+  const int rblk = p.has_past[s] ? p.blk[s] : 0;
+  const __nv_bfloat16* __restrict__ tail =
+      reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
+  const __nv_bfloat16* __restrict__ x = reinterpret_cast<const __nv_bfloat16*>(p.xbc);
+  const __nv_bfloat16* __restrict__ w = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
+  constexpr int kW = KW - 1;  // window rows
+  for (int ch0 = blockIdx.y * kPrepCh + (threadIdx.x & 31) * 8; ch0 < C;
+       ch0 += kPrepCtaY * kPrepCh) {
+    // rows: the window (oldest first), then the thread's tokens
+    uint4 rows[kW + kPrepTok];
+#pragma unroll
+    for (int j = 0; j < kW; ++j) {
+      const int pos = t0 - kW + j;  // sequence-local row
+      rows[j] = pos >= 0 ? *reinterpret_cast<const uint4*>(x + (size_t)(seq0 + pos) * C + ch0)
+                         : *reinterpret_cast<const uint4*>(tail + (size_t)(kW + pos) * C + ch0);
+    }
+#pragma unroll
+    for (int i = 0; i < kPrepTok; ++i)
+      rows[kW + i] = t0 + i < t1
+                         ? *reinterpret_cast<const uint4*>(x + (size_t)(seq0 + t0 + i) * C + ch0)
+                         : make_uint4(0, 0, 0, 0);
+    // the 8 channels' taps, [channel][tap] contiguous: KW 16-byte vectors
+    uint4 wraw[KW];
+#pragma unroll
+    for (int j = 0; j < KW; ++j) wraw[j] = reinterpret_cast<const uint4*>(w + (size_t)ch0 * KW)[j];
+    const __nv_bfloat16* wv = reinterpret_cast<const __nv_bfloat16*>(wraw);
+    // wh[m][e] = half the tap of channel e on the input m rows before the
+    // current one (tap KW-1 is on the current token)
+    float wh[KW][8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int m = 0; m < KW; ++m) wh[m][e] = 0.5f * __bfloat162float(wv[e * KW + (KW - 1 - m)]);
+#pragma unroll
+    for (int i = 0; i < kPrepTok; ++i) {
+      float h[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = 0.f;
+#pragma unroll
+      for (int m = 0; m < KW; ++m) {
+        float f[8];
+        bf16x8_to_f32(rows[kW + i - m], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = fmaf(wh[m][e], f[e], h[e]);
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const float a0 = fmaf(h[e], tanh_approx_f32(h[e]), h[e]);
+        const float a1 = fmaf(h[e + 1], tanh_approx_f32(h[e + 1]), h[e + 1]);
+        const __half2 hv = __floats2half2_rn(a0, a1);
+        o[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      if (t0 + i < t1)
+        *reinterpret_cast<uint4*>(xs + (size_t)(seq0 + t0 + i) * C + ch0) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
 
 typedef CUresult (*SsdEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -852,8 +926,15 @@ cudaError_t launch_ssd_chunk(const SsdParams& p, void* xs, int max_pre, cudaStre
   CUtensorMap m;
   cudaError_t e = ssd_scratch_map(&m, xs, p.T, p.C);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(ssd_prep_kernel, dim3(max_pre, (p.C + 255) / 256), dim3(256), 0, stream, p,
-                 static_cast<__half*>(xs));
+  // at most T/64 + (prefill sequences) 64-token chunks
+  const dim3 pgrid(p.T / 64 + max_pre, kPrepCtaY);
+  __half* xh = static_cast<__half*>(xs);
+  switch (p.K) {
+    case 2: e = launch_pdl(ssd_prep_kernel<2>, pgrid, dim3(256), 0, stream, p, xh); break;
+    case 3: e = launch_pdl(ssd_prep_kernel<3>, pgrid, dim3(256), 0, stream, p, xh); break;
+    case 4: e = launch_pdl(ssd_prep_kernel<4>, pgrid, dim3(256), 0, stream, p, xh); break;
+    default: return cudaErrorInvalidValue;
+  }
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(ssd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)CSMEM_BYTES);

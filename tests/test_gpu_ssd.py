@@ -119,3 +119,15 @@ def test_chunked_and_token_serial_scans_agree():
     assert a.pool.error_flags() == 0 and b.pool.error_flags() == 0
     a.close()
     b.close()
+
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_chunked_scan_conv_widths_and_short_sequences(K):
+    """The chunked scan's token-parallel conv at every conv width: sequences
+    of two and three tokens whose window reaches into the past conv state,
+    lengths on and next to the conv's 64-token chunks, with and without past."""
+    dims = synth.SsdDims(H=16, P=64, N=128, G=2, K=K, act="bf16")
+    lens = [2, 3, 63, 64, 65, 191, 1, 130]
+    past = [1, 1, 1, 0, 1, 1, 1, 0]
+    wl = synth.make_ssd_workload("ssd_conv_widths", dims, lens, past, 16, 13 + K)
+    check_ssd_against_oracle(wl)
