@@ -526,11 +526,13 @@ def main():
     ap.add_argument("--variants", action="store_true",
                     help="also time the decode batches of the per-channel-decay rule and of "
                          "the Mamba2 scan")
-    ap.add_argument("--profile", choices=["prefill", "mixed", "proj", "ssd_prefill"],
+    ap.add_argument("--profile",
+                    choices=["prefill", "mixed", "proj", "ssd_prefill", "kda_prefill"],
                     default=None,
                     help="profiler aid: run only the ~16k-token prefill, the mixed batch, "
-                         "the layer's projections on 15843 tokens or the Mamba2 prefill of the "
-                         "same lengths, --warmup + --steps times, and print their timing line")
+                         "the layer's projections on 15843 tokens, or the Mamba2 or "
+                         "per-channel-decay prefill of the same lengths, --warmup + --steps "
+                         "times, and print their timing line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -557,9 +559,9 @@ def main():
         res = time_projections(binding, synth, 15843, args.steps, f"cuda:{local_rank}", peaks())
         print(json.dumps({"profile": args.profile, **res}), flush=True)
         return
-    if args.profile == "ssd_prefill":
-        res = time_variant_prefill(harness, ssd_prefill_workload(synth), args.steps,
-                                   f"cuda:{local_rank}", peaks())
+    if args.profile in ("ssd_prefill", "kda_prefill"):
+        wl = (ssd_prefill_workload if args.profile == "ssd_prefill" else kda_prefill_workload)(synth)
+        res = time_variant_prefill(harness, wl, args.steps, f"cuda:{local_rank}", peaks())
         print(json.dumps({"profile": args.profile, **res}), flush=True)
         return
     if args.profile:

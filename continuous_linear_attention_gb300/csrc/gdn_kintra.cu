@@ -23,8 +23,10 @@
 //   k~_{j <= r} e^{Gamma_r - Gamma_j} backward from r, so that the
 //   off-diagonal 16 x 16 blocks of A and P are plain products L_I R_I^T
 //   (mma.sync, fp16 operands <= 1, fp32 accumulation);
-//   the four diagonal 16 x 16 blocks by running products per pair column j
-//   (fp32, CUDA cores).
+//   inside each diagonal 16 x 16 block, with m its eighth token, the
+//   lower-left 8 x 8 quadrant the same way (L'_I = [q~ ; k~]_i e^{Gamma_i -
+//   Gamma_m}, R'_I = k~_j e^{Gamma_m - Gamma_j}), and the two diagonal 8 x 8
+//   blocks by running products per pair column j (fp32, CUDA cores).
 // Then the shared blocked solve for T, T diag(beta) as an fp16 operand, and u
 // and -w on tcgen05 (fp32 in tensor memory).  Every tile leaves in the layout
 // the recurrence kernel loads, by bulk copy: [q^ ; k^] (per v-head), P, u, -w,
@@ -44,7 +46,7 @@ namespace {
 constexpr int D = 128;
 constexpr int CH = 64;
 constexpr int R = 2;  // v-heads per k-head
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr uint32_t BOX = 8192;         // 64 rows x 128 B
 constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of a 128-row [q ; k] tile
 constexpr int AP = solve::AP;
@@ -52,25 +54,29 @@ constexpr int LRP = 136;  // pitch (halves) of the L / R rows: conflict-free ldm
 constexpr float kF16Max = 65000.f;
 
 // Shared memory (offsets from a 1024-byte aligned base):
-//   QK  [q~ ; k~] of the k-head (loaded); then the u and -w staging tiles
+//   QK  [q~ ; k~] of the k-head (loaded); turned into [q^ ; k^] in place
+//       once the products have read it, and stored
 //   V   v of the v-head: 2 boxes of 64 channels x 64 tokens (loaded)
-//   QH  [q^ ; k^] (built, stored)
+//   LM  the mid-block operands of the four 16-token blocks I: 24 rows each,
+//       L'_I (8 q rows, 8 k rows) and R'_I (8 k rows), fp16 [96][LRP]
 //   NK  -k~ e^{Gamma}: 2 token-major boxes (MN-major B operand of -w)
 //   AL  alpha fp32 [64 tokens][128 channels]
 //   LR  L_1..L_3 (32 rows each: 16 q rows, 16 k rows), then R_1..R_3 (16,
-//       32, 48 rows), fp16 [192][LRP]; after the products: the T diag(beta)
-//       operand (128 rows x 64 tokens, rows 64.. zero) and the solve's B blocks
+//       32, 48 rows), fp16 [192][LRP]; after the products: the solve's B
+//       blocks, then the T diag(beta) operand (128 rows x 64 tokens, rows
+//       64.. zero) and the u and -w staging tiles
 //   PT  P fp16 [64 i][64 j] (K-major B operand of the output product)
 //   AT  A, then T, fp32 [64][AP]
 //   GB  beta fp32 [64]
 constexpr uint32_t OFF_QK = 0;
 constexpr uint32_t OFF_V = 32768;
-constexpr uint32_t OFF_QH = 49152;
+constexpr uint32_t OFF_LM = 49152;
 constexpr uint32_t OFF_NK = 81920;
 constexpr uint32_t OFF_AL = 98304;
 constexpr uint32_t OFF_LR = 131072;
+constexpr uint32_t OFF_Z = OFF_LR;
 constexpr uint32_t OFF_AU = OFF_LR;
-constexpr uint32_t OFF_Z = OFF_LR + 16384;
+constexpr uint32_t OFF_UW = OFF_LR + 16384;  // u, then -w: 2 boxes each
 constexpr uint32_t OFF_PT = 184320;
 constexpr uint32_t OFF_AT = OFF_PT + BOX;
 constexpr uint32_t OFF_GB = OFF_AT + CH * AP * 4;
@@ -78,6 +84,8 @@ constexpr uint32_t SMEM_BYTES = OFF_GB + CH * 4 + 1024;
 constexpr int kLRows = 96;  // rows of L_1..L_3
 static_assert(OFF_LR + 192 * LRP * 2 <= OFF_PT, "L / R rows");
 static_assert(OFF_Z + solve::kZFloats * 4 <= OFF_PT, "solve blocks");
+static_assert(OFF_LM + 96 * LRP * 2 <= OFF_NK, "mid-block rows");
+static_assert(OFF_UW + 4 * BOX <= OFF_PT && OFF_UW % 1024 == 0, "u / -w staging");
 static_assert(OFF_PT % 1024 == 0 && OFF_AU % 1024 == 0, "operand tiles on 1024-byte boundaries");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 constexpr uint32_t TM_COLS = 256;  // u (0..127), -w (128..255)
@@ -101,17 +109,6 @@ __device__ __forceinline__ float2 ld_h2(const unsigned char* p) {
 }
 __device__ __forceinline__ void st_h2(unsigned char* p, float a, float b) {
   *reinterpret_cast<__half2*>(p) = __floats2half2_rn(a, b);
-}
-// 8 fp16 (16 bytes) -> fp32
-__device__ __forceinline__ void ld_h8(const unsigned char* p, float* v) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
-    v[2 * e] = f.x;
-    v[2 * e + 1] = f.y;
-  }
 }
 __device__ __forceinline__ uint4 pack8(const float* v) {
   uint4 w;
@@ -141,6 +138,41 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4],
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Packed fp32 pairs (one fma.rn.f32x2 / mul.rn.f32x2 on sm_100 and later).
+__device__ __forceinline__ unsigned long long f2p(float lo, float hi) {
+  return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// 4 fp16 (8 bytes) -> 2 packed fp32 pairs
+__device__ __forceinline__ void ld_h4p(const unsigned char* p, unsigned long long* v) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  v[0] = f2p(a.x, a.y);
+  v[1] = f2p(b.x, b.y);
+}
+
+// named barrier 1 over warps 0..3 (the solve)
+__device__ __forceinline__ void solve_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// softplus(x) = max(x, 0) + ln(1 + e^{-|x|}) with the fast exponential and
+// logarithm: an absolute error of a few 1e-7 (the fast logarithm near 1, the
+// rounding of 1 + e^{-|x|}), which moves e^{-e^{A_log} softplus} by a
+// relative e^{A_log} times that (1e-5 at e^{A_log} = 16).
+__device__ __forceinline__ float softplus_fast(float x) {
+  return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
@@ -181,29 +213,34 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
 
   // ---- gates: alpha_i[c] = e^{-e^{A_log} softplus(a_i[c] + dt_bias[c])}
-  // (thread: channel tid % 128, tokens 32 (tid / 128) ..; 1 past the end),
-  // beta_i = sigmoid(b_i) (0 past the end); the P tile starts zero
+  // (thread: channel pair 2 (tid % 64), tokens 8 (tid / 64) .. + 7, all loads
+  // first; 1 past the end), beta_i = sigmoid(b_i) (0 past the end); the P
+  // tile starts zero
   {
-    const int c = tid & 127, th = tid >> 7;
+    const int c = 2 * (tid & 63), i0 = 8 * (tid >> 6);
     const float ea = __expf(p.A_log[h]);
-    const float db = p.dt_bias[(size_t)h * D + c];
-    const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(p.a);
-#pragma unroll 8
-    for (int t = 0; t < 32; ++t) {
-      const int i = 32 * th + t;
-      float al = 1.f;
-      if (i < n) {
-        const float x = __bfloat162float(av[((size_t)(row0 + i) * Hv + h) * D + c]) + db;
-        al = __expf(-ea * softplus_f32(x));
+    // (dt_bias carries no alignment promise beyond its element type)
+    const float2 db = make_float2(p.dt_bias[(size_t)h * D + c], p.dt_bias[(size_t)h * D + c + 1]);
+    const __nv_bfloat162* av = reinterpret_cast<const __nv_bfloat162*>(p.a);
+    __nv_bfloat162 araw[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (i0 + t < n) araw[t] = av[(((size_t)(row0 + i0 + t) * Hv + h) * D + c) >> 1];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      float2 al = make_float2(1.f, 1.f);
+      if (i0 + t < n) {
+        const float2 x = __bfloat1622float2(araw[t]);
+        al.x = __expf(-ea * softplus_fast(x.x + db.x));
+        al.y = __expf(-ea * softplus_fast(x.y + db.y));
       }
-      AL[i * D + c] = al;
+      *reinterpret_cast<float2*>(AL + (i0 + t) * D + c) = al;
     }
     if (tid < CH) {
       const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
       GB[tid] = tid < n ? sigmoid_f32(__bfloat162float(bv[(size_t)(row0 + tid) * Hv + h])) : 0.f;
     }
     reinterpret_cast<uint4*>(sm + OFF_PT)[tid] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(sm + OFF_PT)[tid + kThreads] = make_uint4(0, 0, 0, 0);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -214,69 +251,124 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
 
   if (ok) {
     // ---- running products over the tokens, thread group gr = tid / 64 and
-    // channel pair c = 2 (tid % 64)
+    // channel pair c = 2 (tid % 64); the chains (token steps):
+    //   0 R_3 (48);  1 R_2, L'_0, L'_1 (48);  2 L_1, L_2, L_3 (48);
+    //   3 R_1, R'_0..R'_3 (48);  4 L'_2, L'_3, -k~ e^{Gamma} rows 0..31 (48);
+    //   5 -k~ e^{Gamma} rows 32..63 (32);  6 e^{Gamma_C} (64 products)
     const int gr = tid >> 6, c = 2 * (tid & 63);
     const unsigned char* QK = sm + OFF_QK;
     const float2* AL2 = reinterpret_cast<const float2*>(AL) + (c >> 1);  // row i at AL2[i * 64]
-    if (gr == 0) {
-      // q^_i = q~_i e^{Gamma_i}, -k~_i e^{Gamma_i}; e^{Gamma_C} to the gate tile
+    // L_I rows: [q~ ; k~]_i e^{Gamma_i - Gamma_r}, r = 16 I - 1, forward from r
+    auto l_rows = [&](int I) {
       float2 f = make_float2(1.f, 1.f);
-      for (int i = 0; i < CH; ++i) {
+      unsigned char* lr = sm + OFF_LR + (size_t)((I - 1) * 32) * (LRP * 2) + c * 2;
+#pragma unroll 8
+      for (int t = 0; t < 16; ++t) {
+        const int i = 16 * I + t;
         const float2 a = AL2[i * 64];
         f.x *= a.x;
         f.y *= a.y;
         const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
-        st_h2(sm + OFF_QH + qk_off(i, c), q.x * f.x, q.y * f.y);
-        st_h2(sm + OFF_NK + box_off(i, c), -k.x * f.x, -k.y * f.y);
+        st_h2(lr + t * (LRP * 2), q.x * f.x, q.y * f.y);
+        st_h2(lr + (16 + t) * (LRP * 2), k.x * f.x, k.y * f.y);
       }
-      reinterpret_cast<float2*>(p.scr_g)[(((size_t)gidx * Hk + kh) * R + hl) * (D / 2) + (c >> 1)] = f;
-    } else if (gr == 1) {
-      // k^_j = k~_j e^{Gamma_C - Gamma_j}, backward from the chunk end
+    };
+    // R_I rows j = 0 .. r: k~_j e^{Gamma_r - Gamma_j}, backward from r
+    auto r_rows = [&](int I) {
+      const int r = 16 * I - 1;
+      const int rb = kLRows + 8 * I * (I - 1);  // first row of R_I (96, 112, 144)
       float2 f = make_float2(1.f, 1.f);
-      for (int j = CH - 1; j >= 0; --j) {
+#pragma unroll 8
+      for (int j = r; j >= 0; --j) {
         const float2 k = ld_h2(QK + qk_off(CH + j, c));
-        st_h2(sm + OFF_QH + qk_off(CH + j, c), k.x * f.x, k.y * f.y);
+        st_h2(sm + OFF_LR + (size_t)(rb + j) * (LRP * 2) + c * 2, k.x * f.x, k.y * f.y);
         const float2 a = AL2[j * 64];
         f.x *= a.x;
         f.y *= a.y;
       }
+    };
+    // L'_I rows (LM rows 24 I + t and 24 I + 8 + t): [q~ ; k~]_i e^{Gamma_i -
+    // Gamma_m}, i = 16 I + 8 + t, m = 16 I + 7, forward from m
+    auto lm_rows = [&](int I) {
+      float2 f = make_float2(1.f, 1.f);
+      unsigned char* lr = sm + OFF_LM + (size_t)(24 * I) * (LRP * 2) + c * 2;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int i = 16 * I + 8 + t;
+        const float2 a = AL2[i * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+        const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
+        st_h2(lr + t * (LRP * 2), q.x * f.x, q.y * f.y);
+        st_h2(lr + (8 + t) * (LRP * 2), k.x * f.x, k.y * f.y);
+      }
+    };
+    // R'_I rows (LM rows 24 I + 16 + t): k~_j e^{Gamma_m - Gamma_j}, j = 16 I +
+    // t, backward from m
+    auto rm_rows = [&](int I) {
+      float2 f = make_float2(1.f, 1.f);
+      unsigned char* lr = sm + OFF_LM + (size_t)(24 * I + 16) * (LRP * 2) + c * 2;
+#pragma unroll
+      for (int t = 7; t >= 0; --t) {
+        const int j = 16 * I + t;
+        const float2 k = ld_h2(QK + qk_off(CH + j, c));
+        st_h2(lr + t * (LRP * 2), k.x * f.x, k.y * f.y);
+        const float2 a = AL2[j * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+      }
+    };
+    // -k~_i e^{Gamma_i} for rows i0 .. i0 + 31, from the product f over the
+    // rows before i0
+    auto nk_rows = [&](int i0, float2 f) {
+#pragma unroll 8
+      for (int i = i0; i < i0 + 32; ++i) {
+        const float2 a = AL2[i * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+        const float2 k = ld_h2(QK + qk_off(CH + i, c));
+        st_h2(sm + OFF_NK + box_off(i, c), -k.x * f.x, -k.y * f.y);
+      }
+    };
+    if (gr == 0) {
+      r_rows(3);
+    } else if (gr == 1) {
+      r_rows(2);
+      lm_rows(0);
+      lm_rows(1);
     } else if (gr == 2) {
-      // L_I rows: [q~ ; k~]_i e^{Gamma_i - Gamma_r}, r = 16 I - 1
-      for (int I = 1; I < 4; ++I) {
-        float2 f = make_float2(1.f, 1.f);
-        unsigned char* lr = sm + OFF_LR + (size_t)((I - 1) * 32) * (LRP * 2) + c * 2;
-        for (int t = 0; t < 16; ++t) {
-          const int i = 16 * I + t;
-          const float2 a = AL2[i * 64];
-          f.x *= a.x;
-          f.y *= a.y;
-          const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
-          st_h2(lr + t * (LRP * 2), q.x * f.x, q.y * f.y);
-          st_h2(lr + (16 + t) * (LRP * 2), k.x * f.x, k.y * f.y);
-        }
+      l_rows(1);
+      l_rows(2);
+      l_rows(3);
+    } else if (gr == 3) {
+      r_rows(1);
+      for (int I = 0; I < 4; ++I) rm_rows(I);
+    } else if (gr == 4) {
+      lm_rows(2);
+      lm_rows(3);
+      nk_rows(0, make_float2(1.f, 1.f));
+    } else if (gr == 5) {
+      float2 f = make_float2(1.f, 1.f);
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const float2 a = AL2[i * 64];
+        f.x *= a.x;
+        f.y *= a.y;
       }
-    } else {
-      // R_I rows j = 0 .. r: k~_j e^{Gamma_r - Gamma_j}, backward from r
-      for (int I = 1; I < 4; ++I) {
-        const int r = 16 * I - 1;
-        const int rb = kLRows + 8 * I * (I - 1);  // first row of R_I (96, 112, 144)
-        float2 f = make_float2(1.f, 1.f);
-        for (int j = r; j >= 0; --j) {
-          const float2 k = ld_h2(QK + qk_off(CH + j, c));
-          st_h2(sm + OFF_LR + (size_t)(rb + j) * (LRP * 2) + c * 2, k.x * f.x, k.y * f.y);
-          const float2 a = AL2[j * 64];
-          f.x *= a.x;
-          f.y *= a.y;
-        }
+      nk_rows(32, f);
+    } else if (gr == 6) {
+      // e^{Gamma_C} of every key channel to the gate tile
+      float2 f = make_float2(1.f, 1.f);
+#pragma unroll 8
+      for (int i = 0; i < CH; ++i) {
+        const float2 a = AL2[i * 64];
+        f.x *= a.x;
+        f.y *= a.y;
       }
+      reinterpret_cast<float2*>(p.scr_g)[(((size_t)gidx * Hk + kh) * R + hl) * (D / 2) + (c >> 1)] = f;
     }
-    tc::fence_proxy_async_smem();  // [q^ ; k^] (bulk store) and -k~ e^{Gamma} (MMA operand)
+    tc::fence_proxy_async_smem();  // -k~ e^{Gamma} (MMA operand)
     __syncthreads();
-    if (tid == 0) {
-      bulk_s2g(static_cast<unsigned char*>(p.scr_qh) + ((size_t)gidx * Hv + h) * (2 * KB_STRIDE),
-               sm + OFF_QH, 2 * KB_STRIDE);
-      bulk_commit();
-    }
 
     // ---- off-diagonal blocks (I, J), I > J: [P ; A / beta] = [L_I^q ; L_I^k]
     // R_I[16 J ..]^T, one warp per block
@@ -315,48 +407,72 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
               make_float2(bi * acc[1][nt][2 * hh], bi * acc[1][nt][2 * hh + 1]);
         }
     }
-    // ---- diagonal blocks: thread (block I, column j = 16 I + jl, channel
-    // quarter cq) walks the block's rows i with the running decay product
-    // f[c] = e^{Gamma_i[c] - Gamma_j[c]} over its 32 channels; the four
-    // quarters' partial sums meet by shuffles
+    // ---- lower-left 8 x 8 quadrants of the diagonal 16-token blocks:
+    // [P ; A / beta] = [L'_I^q ; L'_I^k] R'_I^T, warps 6..9 (block I = warp - 6)
+    if (warp >= 6 && warp < 10) {
+      const int I = warp - 6;
+      const int lane = tid & 31;
+      const uint32_t lbase = sbase + OFF_LM + (uint32_t)(24 * I) * (LRP * 2);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4], b[2];
+        ldsm_x4(lbase + (uint32_t)(lane & 15) * (LRP * 2) + (ks * 16 + (lane >> 4) * 8) * 2, a);
+        ldsm_x2(lbase + (uint32_t)(16 + (lane & 7)) * (LRP * 2) + (ks * 16 + ((lane >> 3) & 1) * 8) * 2,
+                b);
+        mma_f16(acc, a, b);
+      }
+      const int g = lane >> 2, t4 = lane & 3;
+      const int i = 16 * I + 8 + g, j = 16 * I + 2 * t4;
+      st_h2(sm + OFF_PT + tc::sw128_offset(i, j), acc[0], acc[1]);
+      const float bi = GB[i];
+      *reinterpret_cast<float2*>(AT + i * AP + j) = make_float2(bi * acc[2], bi * acc[3]);
+    }
+    // ---- diagonal 8 x 8 blocks: thread (block B, column j = 8 B + jl,
+    // channel group cq) walks the block's rows i with the running decay
+    // product f[c] = e^{Gamma_i[c] - Gamma_j[c]} over its 16 channels 32 s +
+    // 4 cq + e (s, e < 4: the eight groups of a row read disjoint banks); the
+    // groups' partial sums meet by shuffles.  A warp's four columns start at
+    // its first one's row.
     {
-      const int I = tid >> 6, jl = (tid >> 2) & 15, cq = tid & 3;
-      const int j = 16 * I + jl, c0 = 32 * cq;
-      float kj[32], f[32];
+      const int B = tid >> 6, jl = (tid >> 3) & 7, cq = tid & 7;
+      const int j = 8 * B + jl;
+      unsigned long long kj[8], f[8];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) ld_h8(QK + qk_off(CH + j, c0 + 8 * m), kj + 8 * m);
+      for (int s4 = 0; s4 < 4; ++s4) ld_h4p(QK + qk_off(CH + j, 32 * s4 + 4 * cq), kj + 2 * s4);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) f[e] = 1.f;
+      for (int e = 0; e < 8; ++e) f[e] = f2p(1.f, 1.f);
 #pragma unroll 1
-      for (int tt = 0; tt < 16; ++tt) {
-        const int i = 16 * I + tt;
+      for (int tt = jl & 4; tt < 8; ++tt) {
+        const int i = 8 * B + tt;
         if (tt > jl) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(AL + i * D + c0 + e);
-            f[e] *= a.x;
-            f[e + 1] *= a.y;
-            f[e + 2] *= a.z;
-            f[e + 3] *= a.w;
+          for (int s4 = 0; s4 < 4; ++s4) {
+            const float4 a = *reinterpret_cast<const float4*>(AL + i * D + 32 * s4 + 4 * cq);
+            f[2 * s4] = mul2(f[2 * s4], f2p(a.x, a.y));
+            f[2 * s4 + 1] = mul2(f[2 * s4 + 1], f2p(a.z, a.w));
           }
         }
-        float sp = 0.f, sa = 0.f;
+        unsigned long long sp2 = 0ull, sa2 = 0ull;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float q8[8], k8[8];
-          ld_h8(QK + qk_off(i, c0 + 8 * m), q8);
-          ld_h8(QK + qk_off(CH + i, c0 + 8 * m), k8);
+        for (int s4 = 0; s4 < 4; ++s4) {
+          unsigned long long q2[2], k2[2];
+          ld_h4p(QK + qk_off(i, 32 * s4 + 4 * cq), q2);
+          ld_h4p(QK + qk_off(CH + i, 32 * s4 + 4 * cq), k2);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float kf = kj[8 * m + e] * f[8 * m + e];
-            sp = fmaf(q8[e], kf, sp);
-            sa = fmaf(k8[e], kf, sa);
+          for (int e = 0; e < 2; ++e) {
+            const unsigned long long kf = mul2(kj[2 * s4 + e], f[2 * s4 + e]);
+            sp2 = fma2(q2[e], kf, sp2);
+            sa2 = fma2(k2[e], kf, sa2);
           }
         }
-        sp += __shfl_xor_sync(0xffffffffu, sp, 1);
-        sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-        sp += __shfl_xor_sync(0xffffffffu, sp, 2);
-        sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+        float sp = __uint_as_float((uint32_t)sp2) + __uint_as_float((uint32_t)(sp2 >> 32));
+        float sa = __uint_as_float((uint32_t)sa2) + __uint_as_float((uint32_t)(sa2 >> 32));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          sp += __shfl_xor_sync(0xffffffffu, sp, o);
+          sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        }
         if (cq == 0 && tt >= jl) {
           *reinterpret_cast<__half*>(sm + OFF_PT + tc::sw128_offset(i, j)) = __float2half_rn(sp);
           if (tt > jl) AT[i * AP + j] = GB[i] * sa;
@@ -369,29 +485,61 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       bulk_s2g(static_cast<unsigned char*>(p.scr_p) + ((size_t)gidx * Hv + h) * BOX, sm + OFF_PT, BOX);
       bulk_commit();
     }
-    // ---- T = (I + A)^{-1}: diagonal blocks (threads 0..63), then the
-    // off-diagonal blocks (warps 0..3)
-    {
+    // ---- T = (I + A)^{-1} on warps 0..3 (diagonal blocks by threads 0..63,
+    // then the off-diagonal blocks; named barrier 1 over those 128 threads),
+    // while warps 4..7 turn the [q~ ; k~] tile into [q^ ; k^] in place (every
+    // product has read it): q^_i = q~_i e^{Gamma_i} forward from the chunk
+    // start (threads 128..191), k^_j = k~_j e^{Gamma_C - Gamma_j} backward
+    // from its end (threads 192..255)
+    if (warp < 4) {
       float col[16];
       const int b = (tid >> 4) & 3, m = tid & 15;
       float* Ab = AT + (16 * b) * AP + 16 * b;
       if (tid < CH) solve::diag_col(Ab, m, col);
-      __syncthreads();
+      solve_bar();
       if (tid < CH) solve::diag_col_store(Ab, m, col);
+      solve_bar();
+      float* Z = reinterpret_cast<float*>(sm + OFF_Z);
+      solve::offdiag_first(AT, Z, warp);
+      solve_bar();
+      solve::offdiag_rest(AT, Z, warp);
+    } else if (warp < 6) {
+      float2 f = make_float2(1.f, 1.f);
+      unsigned char* QKw = sm + OFF_QK;
+#pragma unroll 8
+      for (int i = 0; i < CH; ++i) {
+        const float2 a = AL2[i * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+        const uint32_t o = qk_off(i, c);
+        const float2 q = ld_h2(QKw + o);
+        st_h2(QKw + o, q.x * f.x, q.y * f.y);
+      }
+    } else if (warp < 8) {
+      float2 f = make_float2(1.f, 1.f);
+      unsigned char* QKw = sm + OFF_QK;
+#pragma unroll 8
+      for (int j = CH - 1; j >= 0; --j) {
+        const uint32_t o = qk_off(CH + j, c);
+        const float2 k = ld_h2(QKw + o);
+        st_h2(QKw + o, k.x * f.x, k.y * f.y);
+        const float2 a = AL2[j * 64];
+        f.x *= a.x;
+        f.y *= a.y;
+      }
     }
+    tc::fence_proxy_async_smem();  // [q^ ; k^] (bulk store)
     __syncthreads();
-    float* Z = reinterpret_cast<float*>(sm + OFF_Z);
-    if (warp < 4) solve::offdiag_first(AT, Z, warp);
-    __syncthreads();
-    if (warp < 4) solve::offdiag_rest(AT, Z, warp);
-    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(static_cast<unsigned char*>(p.scr_qh) + ((size_t)gidx * Hv + h) * (2 * KB_STRIDE),
+               sm + OFF_QK, 2 * KB_STRIDE);
+      bulk_commit();
+    }
     // ---- T diag(beta) as the fp16 A operand (rows 64..127 zero): row i,
     // 8-column group c8 (only the groups at or left of the diagonal block
     // are T's; the rest are zero)
-#pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
-      const int idx = tid + kThreads * q2;
-      const int i = idx >> 3, c8 = idx & 7;
+    {
+      const int i = tid >> 3, c8 = tid & 7;
       float tb[8];
       if ((c8 >> 1) <= (i >> 4)) {
         const float4 t0 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8);
@@ -426,34 +574,31 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   }
   if (ok) {
     tc::fence_after_sync();
-    // rows 0..63 (warps 0, 1, 4, 5): u and -w of token r128 into the staging
-    // tiles over the [q~ ; k~] area (free: every read of it is done)
+    // rows 0..63: u and -w of token r128 into the staging tiles
+    // (thread: TMEM lane r128, column quarter cq4 of each 128-column part)
     const uint32_t lane = (uint32_t)(tid & 96) << 16;
-    const int r128 = tid & 127, hf = tid >> 7;
+    const int r128 = tid & 127, cq4 = tid >> 7;
     if (r128 < CH) {
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        unsigned char* box = sm + OFF_QK + part * (2 * BOX) + hf * BOX;
+        unsigned char* box = sm + OFF_UW + part * (2 * BOX) + (cq4 >> 1) * BOX;
+        float vv[32];
+        tc::tmem_ld32(tmem + lane + part * 128 + cq4 * 32, vv);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float vv[32];
-          tc::tmem_ld32(tmem + lane + part * 128 + hf * 64 + hh * 32, vv);
-          tc::tmem_wait_ld();
+        for (int e = 0; e < 32; e += 2) amax = max_abs3(amax, vv[e], vv[e + 1]);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) amax = max_abs3(amax, vv[e], vv[e + 1]);
-#pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8)
-            *reinterpret_cast<uint4*>(box + tc::sw128_offset(r128, hh * 32 + g8 * 8)) =
-                pack8(vv + g8 * 8);
-        }
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(box + tc::sw128_offset(r128, (cq4 & 1) * 32 + g8 * 8)) =
+              pack8(vv + g8 * 8);
       }
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
       const size_t tile = ((size_t)gidx * Hv + h) * (2 * BOX);
-      bulk_s2g(static_cast<unsigned char*>(p.scr_u) + tile, sm + OFF_QK, 2 * BOX);
-      bulk_s2g(static_cast<unsigned char*>(p.scr_w) + tile, sm + OFF_QK + 2 * BOX, 2 * BOX);
+      bulk_s2g(static_cast<unsigned char*>(p.scr_u) + tile, sm + OFF_UW, 2 * BOX);
+      bulk_s2g(static_cast<unsigned char*>(p.scr_w) + tile, sm + OFF_UW + 2 * BOX, 2 * BOX);
       bulk_commit();
     }
   }
