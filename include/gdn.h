@@ -205,8 +205,17 @@ int gdn_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const voi
  *              channel of every v-head
  *   weights  : dt_bias is [Hv][d_k] fp32 (A_log stays [Hv])
  * Length-1 sequences run on an HBM-streaming decode kernel (d = 128, bf16,
- * Hv = 2 Hk, K = 4), everything else on a token-serial kernel; the prefill
- * scratch is not used.  Never synchronises; graph-capturable. */
+ * Hv = 2 Hk, K = 4).  At that shape longer sequences run on a split chunked
+ * prefill (conv pass, per-(chunk, v-head) decay products on the tensor
+ * cores, the recurrence with the state in tensor memory; chains whose fp16
+ * operands leave their range are recomputed token-serially in the same call)
+ * when the pool's prefill scratch holds the call in this forward's layout,
+ * which needs about 1.9 times the scalar rule's bytes per chunk: the forward
+ * grows the scratch stream-ordered as gdn_varlen_forward does, never under
+ * stream capture, and gdn_state_pool_reserve sizes it for the scalar rule
+ * only.  Otherwise, and at every other shape, a token-serial kernel runs;
+ * gdn_pool_last_prefill_path reports which.  Never synchronises;
+ * graph-capturable. */
 int gdn_kda_varlen_forward(gdn_pool_t* pool, int layer, const void* x_qkv, const void* a,
                            const void* b, const int32_t* cu_seqlens,
                            const int32_t* state_block_idx, const uint8_t* has_past,
