@@ -22,6 +22,13 @@
 //   g = -exp(A_log) softplus(a + dt_bias),  beta = sigmoid(b)
 //   p = S k, r = S q,  u = beta (v - e^g p),  o = e^g r + (k.q) u,
 //   S <- e^g S + u k^T.
+// The per-channel-decay (KDA) instance takes one decay per key channel,
+// alpha[c] = e^{-exp(A_log) softplus(a[c] + dt_bias[c])}, and with S' = S
+// Diag(alpha): p = S' k, r = S' q, u = beta (v - p), o = r + (k.q) u,
+// S <- S' + u k^T; the state is stored k-major (row c = key channel c), so
+// the decay scales whole rows, folded into the k and q of the reductions and
+// into the row update.  Its unit's gate rows (2 v-heads x d_k bf16) arrive
+// with the conv inputs.
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -41,13 +48,34 @@ constexpr int R = 2;                   // v-heads per k-head
 constexpr int kUnitCh = (2 + R) * D;   // conv channels of a unit (512)
 constexpr int kMaxHv = 64;
 
-// Conv inputs of one unit, bf16, channel order q | k | v of the unit.
+// Conv inputs of one unit, bf16, channel order q | k | v of the unit, and the
+// gate pre-activations: the token's row of a (scalar gate) or the unit's two
+// v-heads' rows of a (per-channel decay), and the token's row of b.
+template <bool kKda> struct GateIn;
+template <> struct GateIn<false> {
+  __nv_bfloat16 a[kMaxHv];
+};
+template <> struct GateIn<true> {
+  __nv_bfloat16 a[R][D];
+};
+template <bool kKda>
 struct ConvIn {
   __nv_bfloat16 x[kUnitCh];
   __nv_bfloat16 tail[KC - 1][kUnitCh];
   __nv_bfloat16 w[kUnitCh][KC];
-  __nv_bfloat16 a[kMaxHv];
+  GateIn<kKda> g;
   __nv_bfloat16 b[kMaxHv];
+};
+
+// Gates of the unit's two v-heads: (e^g, beta), or the key-channel decays
+// and beta.
+template <bool kKda> struct Gates;
+template <> struct Gates<false> {
+  float gate[R][2];
+};
+template <> struct Gates<true> {
+  float alpha[R][D];
+  float beta[R];
 };
 
 struct Meta {
@@ -56,14 +84,15 @@ struct Meta {
   int pad0, pad1;
 };
 
+template <bool kKda>
 struct DecodeSmem {
   float buf[kStages][D * D];  // state ring
-  ConvIn cin[2];              // conv inputs, double-buffered by unit
+  ConvIn<kKda> cin[2];        // conv inputs, double-buffered by unit
   float part[2][kG][D];       // partial S k and S q
   float y[kUnitCh];           // conv + SiLU outputs of the unit
   float u[D];
   float red[4];
-  float gate[R][2];           // e^g, beta
+  Gates<kKda> gt;
   Meta meta[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -79,9 +108,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+static_assert(R * D == kConsumers, "one key-channel decay per compute thread");
+static_assert(sizeof(DecodeSmem<false>) <= 227 * 1024 && sizeof(DecodeSmem<true>) <= 227 * 1024,
+              "shared memory of one CTA");
+static_assert(sizeof(ConvIn<false>) % 16 == 0 && sizeof(ConvIn<true>) % 16 == 0 &&
+                  offsetof(ConvIn<true>, g) % 16 == 0 && offsetof(ConvIn<false>, g) % 16 == 0 &&
+                  offsetof(ConvIn<false>, b) % 16 == 0 && offsetof(ConvIn<true>, b) % 16 == 0,
+              "bulk-copy destinations on 16-byte boundaries");
+
+template <bool kKda>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  DecodeSmem<kKda>& sm = *reinterpret_cast<DecodeSmem<kKda>*>(smem_raw);
   pdl_wait_then_release();
   const int tid = threadIdx.x;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
@@ -124,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
       const unsigned char* rbase = p.layer_base + (size_t)rblk * p.stride;
       const float* src = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * D * D;
       uint32_t bytes = kHeadBytes;
-      ConvIn* ci = nullptr;
+      ConvIn<kKda>* ci = nullptr;
       if (jh == 0) {
         const int cb = k & 1;
         if (k >= 2 && !mbar_wait_bounded(&sm.cempty[cb], ((k >> 1) - 1) & 1)) {
@@ -132,7 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
           return;
         }
         ci = &sm.cin[cb];
-        bytes += (uint32_t)(KC * kUnitCh * 2 + kUnitCh * KC * 2 + 2 * Hv * 2);
+        bytes += (uint32_t)(KC * kUnitCh * 2 + kUnitCh * KC * 2 + (kKda ? R * D * 2 : Hv * 2) +
+                            Hv * 2);
       }
       mbar_arrive_expect_tx(&sm.full[st], bytes);
 #pragma unroll
@@ -155,8 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
         bulk_g2s(ci->w[0], w + (size_t)cq * KC, D * KC * 2, &sm.full[st]);
         bulk_g2s(ci->w[D], w + (size_t)ck * KC, D * KC * 2, &sm.full[st]);
         bulk_g2s(ci->w[2 * D], w + (size_t)cv * KC, R * D * KC * 2, &sm.full[st]);
-        bulk_g2s(ci->a, reinterpret_cast<const __nv_bfloat16*>(p.a) + (size_t)row * Hv, Hv * 2,
-                 &sm.full[st]);
+        if constexpr (kKda) {
+          // a is [T][Hv][D]: the unit's two v-heads are adjacent rows
+          bulk_g2s(ci->g.a[0],
+                   reinterpret_cast<const __nv_bfloat16*>(p.a) + ((size_t)row * Hv + kh * R) * D,
+                   R * D * 2, &sm.full[st]);
+        } else {
+          bulk_g2s(ci->g.a, reinterpret_cast<const __nv_bfloat16*>(p.a) + (size_t)row * Hv,
+                   Hv * 2, &sm.full[st]);
+        }
         bulk_g2s(ci->b, reinterpret_cast<const __nv_bfloat16*>(p.b) + (size_t)row * Hv, Hv * 2,
                  &sm.full[st]);
       }
@@ -194,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
 
     if (jh == 0) {
       // ---- conv + SiLU of the unit's channels; new conv state; gates
-      const ConvIn& ci = sm.cin[k & 1];
+      const ConvIn<kKda>& ci = sm.cin[k & 1];
       __nv_bfloat16* tail_w = reinterpret_cast<__nv_bfloat16*>(wbase);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -213,12 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
         for (int j = 0; j < KC - 2; ++j) tail_w[(size_t)j * C + ch] = ci.tail[j + 1][lc];
         tail_w[(size_t)(KC - 2) * C + ch] = ci.x[lc];
       }
-      if (tid < R) {
+      if constexpr (kKda) {
+        // one key-channel decay per thread: R v-heads x D channels = kConsumers
+        const int jg = tid / D, c = tid % D;
+        const int hh = kh * R + jg;
+        const float araw = __bfloat162float(ci.g.a[jg][c]) + p.dt_bias[(size_t)hh * D + c];
+        sm.gt.alpha[jg][c] = __expf(-__expf(p.A_log[hh]) * softplus_f32(araw));
+        if (tid < R) sm.gt.beta[tid] = sigmoid_f32(__bfloat162float(ci.b[kh * R + tid]));
+      } else if (tid < R) {
         const int hh = kh * R + tid;
-        const float araw = __bfloat162float(ci.a[hh]) + p.dt_bias[hh];
+        const float araw = __bfloat162float(ci.g.a[hh]) + p.dt_bias[hh];
         const float g = -__expf(p.A_log[hh]) * softplus_f32(araw);
-        sm.gate[tid][0] = __expf(g);
-        sm.gate[tid][1] = sigmoid_f32(__bfloat162float(ci.b[hh]));
+        sm.gt.gate[tid][0] = __expf(g);
+        sm.gt.gate[tid][1] = sigmoid_f32(__bfloat162float(ci.b[hh]));
       }
       consumer_sync();
       if (lane == 0) mbar_arrive(&sm.cempty[k & 1]);
@@ -236,11 +289,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
     }
     const float qs = rsqrtf(sm.red[0] + kL2Eps) * inv_sqrt_d;
     const float ks = rsqrtf(sm.red[1] + kL2Eps);
-    const float decay = sm.gate[jh][0];
-    const float beta = sm.gate[jh][1];
+    // scalar gate: e^g scales the whole state (decay); per-channel decay:
+    // alpha[r] scales state row r (decay stays 1)
+    float decay = 1.f, beta;
+    const float* alpha = nullptr;
+    if constexpr (kKda) {
+      beta = sm.gt.beta[jh];
+      alpha = sm.gt.alpha[jh];
+    } else {
+      decay = sm.gt.gate[jh][0];
+      beta = sm.gt.gate[jh][1];
+    }
     const float* buf = sm.buf[st];
 
-    // ---- pass 1: state rows into registers, partial S k and S q
+    // ---- pass 1: state rows into registers, partial S k and S q (S' k and
+    // S' q with the per-channel decay)
     float4 S[kRows];
     float kr[kRows];
     float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
@@ -249,8 +312,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
       const int r = rg + kG * i;
       S[i] = *reinterpret_cast<const float4*>(buf + r * D + 4 * cv);
       kr[i] = sm.y[D + r] * ks;
-      const float qr = sm.y[r] * qs;
-      pk.x += S[i].x * kr[i]; pk.y += S[i].y * kr[i]; pk.z += S[i].z * kr[i]; pk.w += S[i].w * kr[i];
+      float ka = kr[i], qr = sm.y[r] * qs;
+      if constexpr (kKda) {
+        ka *= alpha[r];
+        qr *= alpha[r];
+      }
+      pk.x += S[i].x * ka; pk.y += S[i].y * ka; pk.z += S[i].z * ka; pk.w += S[i].w * ka;
       pq.x += S[i].x * qr; pq.y += S[i].y * qr; pq.z += S[i].z * qr; pq.w += S[i].w * qr;
     }
     __syncwarp();
@@ -272,19 +339,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
           __float2bfloat16_rn(decay * sq + sm.red[2] * qs * ks * u);
     }
     consumer_sync();
-    // ---- pass 2: S <- e^g S + u k^T from registers, straight to the write block
+    // ---- pass 2: S <- e^g S + u k^T (S Diag(alpha) + u k^T) from registers,
+    // straight to the write block
     float* S_w = reinterpret_cast<float*>(wbase + p.rec_off) + (size_t)h * D * D;
     const float4 u4 = *reinterpret_cast<const float4*>(&sm.u[4 * cv]);
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       const int r = rg + kG * i;
+      const float dr = kKda ? alpha[r] : decay;
       float4 s4 = S[i];
-      s4.x = decay * s4.x + u4.x * kr[i];
-      s4.y = decay * s4.y + u4.y * kr[i];
-      s4.z = decay * s4.z + u4.z * kr[i];
-      s4.w = decay * s4.w + u4.w * kr[i];
+      s4.x = dr * s4.x + u4.x * kr[i];
+      s4.y = dr * s4.y + u4.y * kr[i];
+      s4.z = dr * s4.z + u4.z * kr[i];
+      s4.w = dr * s4.w + u4.w * kr[i];
       *reinterpret_cast<float4*>(S_w + (size_t)r * D + 4 * cv) = s4;
     }
+    // (per-channel decay: the next unit's gate pass rewrites alpha only after
+    // its own full-barrier wait and a consumer barrier, which every thread
+    // reaches after this loop)
   }
 }
 
@@ -296,7 +368,10 @@ bool decode_supported(int d, int act, int Hk, int Hv, int K) {
   return d == D && act == GDN_BF16 && Hv == R * Hk && K == KC && Hv % 8 == 0 && Hv <= kMaxHv;
 }
 
-cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {
+namespace {
+
+template <bool kKda>
+cudaError_t launch_decode_t(const FwdParams& p, int max_dec, cudaStream_t stream) {
   if (max_dec <= 0) return cudaSuccess;
   if (g_num_sms == 0) {
     int dev = 0;
@@ -306,13 +381,22 @@ cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream) 
   }
   const long long max_units = (long long)max_dec * p.Hk;
   const int grid = (int)(max_units < g_num_sms ? max_units : g_num_sms);
-  const size_t smem = sizeof(DecodeSmem);
-  cudaError_t e =
-      cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(DecodeSmem<kKda>);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kKda>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_kernel, dim3(grid), dim3(kThreads), smem, stream, p);
+  e = launch_pdl(decode_kernel<kKda>, dim3(grid), dim3(kThreads), smem, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {
+  return launch_decode_t<false>(p, max_dec, stream);
+}
+cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {
+  return launch_decode_t<true>(p, max_dec, stream);
 }
 
 }  // namespace gdn

@@ -18,6 +18,13 @@
 // The conv window of each channel lives in registers, so after the last token
 // it IS the new conv state (the last K-1 inputs of [old state ; x]).
 //
+// The per-channel-decay (KDA) instance takes one decay per key channel,
+// alpha[c] = e^{-exp(A_log[h]) softplus(a_t[h][c] + dt_bias[h][c])}, and with
+// S' = S Diag(alpha): p = S' k, r = S' q, u = beta (v - p), o = r + (k.q) u,
+// S <- S' + u k^T (Kimi Linear's delta rule with per-channel decay); with
+// the state stored k-major the decay scales whole rows, folded into the k and
+// q of the reductions and into the row update.
+//
 // Ownership: this CTA is the only one touching the q/k channels of its k-head
 // and the v channels of its v-heads, and the recurrent states of those
 // v-heads, so reading the old state and overwriting it in place is race-free.
@@ -34,7 +41,7 @@ constexpr int kHeadThreads = 256;  // threads per v-head
 // states of those heads only; the conv state is left to the conv-state update)
 enum Mode : int { kAll = 0, kLong = 1, kRedo = 2 };
 
-template <int D, typename Act>
+template <int D, typename Act, bool kKda>
 __global__ void __launch_bounds__(2 * kHeadThreads)
 recurrent_kernel(FwdParams p, int mode) {
   constexpr int CV = D / 4;                 // float4 columns per state row
@@ -77,8 +84,9 @@ recurrent_kernel(FwdParams p, int mode) {
   float* y = smem;                      // [NCH] conv + SiLU output of the token
   float* part = y + 4 * D;              // [R][2][G][D] partial S k, S q
   float* uo = part + 2 * 2 * G * D;     // [R][D] u
-  float* red = uo + 2 * D;              // [4] sum q^2, sum k^2, q.k
-  float* gb = red + 4;                  // [R][2] e^g, beta
+  float* al = uo + 2 * D;               // [R][D] key-channel decays (per-channel decay only)
+  float* red = kKda ? al + 2 * D : al;  // [4] sum q^2, sum k^2, q.k
+  float* gb = red + 4;                  // [R][2] e^g (scalar gate only), beta
 
   const int tid = threadIdx.x;
   const int nt = blockDim.x;
@@ -141,7 +149,15 @@ recurrent_kernel(FwdParams p, int mode) {
       }
       y[tid + c * nt] = silu_f32(acc);
     }
-    if (tid < R) {
+    if constexpr (kKda) {
+      if (tid < R * D) {
+        const int jg = tid / D, c = tid % D;
+        const int hh = kh * R + jg;
+        const float araw = to_f32(av[(row * Hv + hh) * D + c]) + p.dt_bias[(size_t)hh * D + c];
+        al[jg * D + c] = __expf(-__expf(p.A_log[hh]) * softplus_f32(araw));
+      }
+      if (tid < R) gb[2 * tid + 1] = sigmoid_f32(to_f32(bv[row * Hv + kh * R + tid]));
+    } else if (tid < R) {
       const int hh = kh * R + tid;
       const float araw = to_f32(av[row * Hv + hh]) + p.dt_bias[hh];
       const float g = -__expf(p.A_log[hh]) * softplus_f32(araw);
@@ -164,17 +180,24 @@ recurrent_kernel(FwdParams p, int mode) {
     __syncthreads();
     const float qs = rsqrtf(red[0] + kL2Eps) * inv_sqrt_d;
     const float ks = rsqrtf(red[1] + kL2Eps);
-    const float decay = gb[2 * j_head];
+    // scalar gate: e^g scales the whole state; per-channel decay: alpha[r]
+    // scales state row r (decay stays 1)
+    const float decay = kKda ? 1.f : gb[2 * j_head];
     const float beta = gb[2 * j_head + 1];
-    // 3. partial S k and S q over this thread's rows
+    const float* alh = al + j_head * D;
+    // 3. partial S k and S q (S' k and S' q) over this thread's rows
     float kr[NJ];
     float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
     for (int i = 0; i < NJ; ++i) {
       const int r = rg + G * i;
       kr[i] = y[D + r] * ks;
-      const float qr = y[r] * qs;
-      pk.x += S[i].x * kr[i]; pk.y += S[i].y * kr[i]; pk.z += S[i].z * kr[i]; pk.w += S[i].w * kr[i];
+      float ka = kr[i], qr = y[r] * qs;
+      if constexpr (kKda) {
+        ka *= alh[r];
+        qr *= alh[r];
+      }
+      pk.x += S[i].x * ka; pk.y += S[i].y * ka; pk.z += S[i].z * ka; pk.w += S[i].w * ka;
       pq.x += S[i].x * qr; pq.y += S[i].y * qr; pq.z += S[i].z * qr; pq.w += S[i].w * qr;
     }
     float* myp = part + (size_t)j_head * 2 * G * D;
@@ -195,15 +218,19 @@ recurrent_kernel(FwdParams p, int mode) {
       if (mine) out[(row * Hv + h) * D + li] = from_f32<Act>(decay * sq + kq * u);
     }
     __syncthreads();
-    // 5. S <- e^g S + u k^T
+    // 5. S <- e^g S + u k^T  (S Diag(alpha) + u k^T)
     const float4 u4 = *reinterpret_cast<const float4*>(uo + j_head * D + 4 * cv);
 #pragma unroll
     for (int i = 0; i < NJ; ++i) {
-      S[i].x = decay * S[i].x + u4.x * kr[i];
-      S[i].y = decay * S[i].y + u4.y * kr[i];
-      S[i].z = decay * S[i].z + u4.z * kr[i];
-      S[i].w = decay * S[i].w + u4.w * kr[i];
+      const float dr = kKda ? alh[rg + G * i] : decay;
+      S[i].x = dr * S[i].x + u4.x * kr[i];
+      S[i].y = dr * S[i].y + u4.y * kr[i];
+      S[i].z = dr * S[i].z + u4.z * kr[i];
+      S[i].w = dr * S[i].w + u4.w * kr[i];
     }
+    // per-channel decay: the next token's gate pass overwrites al[], which
+    // step 5 just read
+    if constexpr (kKda) __syncthreads();
   }
 
   // ---- write back: recurrent state, then the conv window as the new conv state
@@ -222,14 +249,14 @@ recurrent_kernel(FwdParams p, int mode) {
   }
 }
 
-template <int D, typename Act>
+template <int D, typename Act, bool kKda = false>
 cudaError_t launch_rec(const FwdParams& p, int max_items, int mode, cudaStream_t stream) {
   const int R = p.Hv / p.Hk;
   constexpr int G = kHeadThreads / (D / 4);
-  const size_t smem = sizeof(float) * (4 * D + 2 * 2 * G * D + 2 * D + 4 + 4);
+  const size_t smem = sizeof(float) * (4 * D + 2 * 2 * G * D + 2 * D + (kKda ? 2 * D : 0) + 4 + 4);
   dim3 grid(max_items, p.Hk);
-  const cudaError_t e = launch_pdl(recurrent_kernel<D, Act>, grid, dim3(R * kHeadThreads), smem,
-                                   stream, p, mode);
+  const cudaError_t e = launch_pdl(recurrent_kernel<D, Act, kKda>, grid, dim3(R * kHeadThreads),
+                                   smem, stream, p, mode);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -254,6 +281,25 @@ cudaError_t launch_redo(const FwdParams& p, int d, int act, int max_pre, cudaStr
   if (max_pre <= 0) return cudaSuccess;
   if (d != 128 || act != GDN_BF16) return cudaErrorInvalidValue;  // the chunked kernels' shape
   return launch_rec<128, __nv_bfloat16>(p, max_pre, kRedo, stream);
+}
+
+cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
+                                 bool long_only, cudaStream_t stream) {
+  if (max_items <= 0) return cudaSuccess;
+  const int mode = long_only ? kLong : kAll;
+  if (act == GDN_F32) {
+    if (d == 32) return launch_rec<32, float, true>(p, max_items, mode, stream);
+    if (d == 64) return launch_rec<64, float, true>(p, max_items, mode, stream);
+    return launch_rec<128, float, true>(p, max_items, mode, stream);
+  }
+  if (d == 32) return launch_rec<32, __nv_bfloat16, true>(p, max_items, mode, stream);
+  if (d == 64) return launch_rec<64, __nv_bfloat16, true>(p, max_items, mode, stream);
+  return launch_rec<128, __nv_bfloat16, true>(p, max_items, mode, stream);
+}
+
+cudaError_t launch_kda_redo(const FwdParams& p, int max_pre, cudaStream_t stream) {
+  if (max_pre <= 0) return cudaSuccess;
+  return launch_rec<128, __nv_bfloat16, true>(p, max_pre, kRedo, stream);
 }
 
 }  // namespace gdn
