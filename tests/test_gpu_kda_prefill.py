@@ -98,3 +98,71 @@ def test_inputs_outside_fp16_are_recomputed():
     wl = dataclasses.replace(wl, x=x.to(torch.bfloat16))
     check_against_oracle(wl, run=_run_split(wl))
 
+
+
+def test_captured_prefill_replays_the_eager_result():
+    """A per-channel-decay prefill captured in a CUDA graph on a pool whose
+    scratch an eager call has grown runs the split kernels (no allocation, no
+    host sync inside the capture) and replays to the eager result bit for bit;
+    on a pool without prefill scratch the capture takes the token-serial
+    kernel."""
+    wl = _kda("kda_cap", [300, 1, 129, 70], [1, 1, 0, 1], 16, 49, True)
+    eager = _run_split(wl)
+    run = harness.DeviceRun(wl)
+    snapshot = run.mem.clone()
+    run.run()  # eager: grows the scratch to this call's size
+    torch.cuda.synchronize()
+    run.mem.copy_(snapshot)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run.run(stream=s)
+    assert run.pool.last_prefill_path() == binding.PREFILL_SPLIT
+    run.mem.copy_(snapshot)
+    run.out.fill_(harness.OUT_SENTINEL)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert run.pool.error_flags() == 0
+    assert torch.equal(run.out, eager.out)
+    assert torch.equal(run.mem, eager.mem)
+    # a pool without prefill scratch: the capture runs the token-serial kernel
+    small = harness.DeviceRun(wl, prefill="fused")
+    snap2 = small.mem.clone()
+    s2 = torch.cuda.Stream()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s2):
+        small.run(stream=s2)
+    assert small.pool.last_prefill_path() == binding.PREFILL_SERIAL
+    small.mem.copy_(snap2)
+    torch.cuda.synchronize()
+    g2.replay()
+    torch.cuda.synchronize()
+    assert small.pool.error_flags() == 0
+    err = rel_l2(small.out.float().cpu().numpy(), eager.out.float().cpu().numpy())
+    assert err <= TOL["bf16"], err
+    run.close()
+    small.close()
+    eager.close()
+
+
+def test_scalar_and_per_channel_forwards_share_a_pool():
+    """Scalar-gate and per-channel-decay prefills alternate on one pool (and
+    so on one prefill scratch, laid out differently by each); each matches its
+    own oracle."""
+    kda = _kda("kda_share", [200, 90, 1], [0, 1, 1], 8, 50)
+    run = _run_split(kda)
+    check_against_oracle(kda, run=run)
+    scal = synth.make_workload("scalar_share", synth.FULL_DIMS, [150, 64, 1], [0, 0, 1], 8, 51)
+    # the same pool: the scalar forward on its own inputs and states
+    blocks = [int(b) for b in scal.ref_blocks]
+    run.upload_states(blocks, scal.conv_state, scal.rec_state)
+    run.wl = scal
+    run.set_inputs(scal)
+    run.conv_w, run.A_log, run.dt_bias = (scal.conv_w.to(run.device), scal.A_log.to(run.device),
+                                          scal.dt_bias.to(run.device))
+    run.run()
+    torch.cuda.synchronize()
+    assert run.pool.last_prefill_path() == binding.PREFILL_SPLIT
+    check_against_oracle(scal, run=run)
+    run.close()
