@@ -450,27 +450,42 @@ cudaError_t launch_by_state(const SsdParams& p, int NS, int max_items, bool long
 //         K-major B operand), h <- e^{cum_h[n-1]} h
 //   CUDA  X'[s][(head,p)] = X dt_h[s] e^{cum_h[n-1] - cum_h[s]}
 //   MMA   CB = C B^T, YI = C h16^T, h += X'^T B (X' and B MN-major)
-//   CUDA  M_h from CB; MMA Y[:, 64 head ..] = M_h X_h, one head at a time
+//   CUDA  M_0 and M_1 from one read of CB; MMA Y[:, 64 head ..] = M_h X_h for both
 //   CUDA  y = Y + e^{cum_h[t]} YI + D_h x  -> bf16
 // fp16 operands, fp32 accumulators and state; |h| is range-checked against
-// the fp16 limit (GDN_FLAG_RANGE).
+// the fp16 limit (GDN_FLAG_RANGE).  16 warps, one chunk ahead: X and M_0
+// swap regions every chunk, so the next chunk's X is loaded as soon as this
+// chunk's M products are done (while its outputs are made), the next B and C
+// once the state update has read these, and the next chunk's dt / cum are
+// scanned while the tensor core runs.
 
 using E = __half;
 constexpr int SP = 64;     // head dim
 constexpr int SN = 128;    // state size
 constexpr int SQ = 128;    // chunk
-constexpr int kCThreads = 256;
+constexpr int kCThreads = 512;
 constexpr uint32_t CBOX = 16384;  // one [128 rows][64 cols] fp16 box, 128-byte swizzled
 constexpr uint32_t OFF_X = 0;          // X pair: 2 boxes (head 0, head 1)
 constexpr uint32_t OFF_B = 2 * CBOX;    // B: 2 boxes (n 0..63, 64..127)
 constexpr uint32_t OFF_C = 4 * CBOX;    // C: 2 boxes
 constexpr uint32_t OFF_XP = 6 * CBOX;   // X' (same layout as X)
 constexpr uint32_t OFF_H16 = 8 * CBOX;  // h16: [128 rows (head,p)][128 n], 2 K-blocks
-constexpr uint32_t OFF_M = 10 * CBOX;   // M_h: [128 t][128 s], 2 K-blocks
+constexpr uint32_t OFF_M = 10 * CBOX;   // M_0: [128 t][128 s], 2 K-blocks (M_1 over X')
+// X and M_0 alternate between the two regions OFF_X and OFF_M by chunk
+// parity, so the next chunk's X can land while this chunk's outputs are made
 constexpr uint32_t TILE_BYTES = 12 * CBOX;               // 196608
 constexpr uint32_t CSMEM_BYTES = TILE_BYTES + 1024;      // + alignment slack
+// (with the kernel's ~4 KiB of static shared memory)
+static_assert(CSMEM_BYTES + 8192 <= 227 * 1024, "shared memory of one CTA");
 constexpr uint32_t TM_CB = 0, TM_YI = 128, TM_Y = 256, TM_H = 384, TM_COLS = 512;
 constexpr float kCF16Max = 65000.f;
+
+// 2^x on the MFU (ex2.approx: relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ssd_ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 __device__ __forceinline__ bool ssd_cta_wait(uint64_t* bar, uint32_t parity, int* flag) {
   if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity) ? 1 : 0;
@@ -482,10 +497,14 @@ __global__ void __launch_bounds__(kCThreads, 1)
 ssd_chunk_kernel(SsdParams p, const __grid_constant__ CUtensorMap txs) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t full, mma_bar;
+  __shared__ uint64_t full_x[2], full_bc, mma_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int okf;
-  __shared__ float cum[2][SQ], dts[2][SQ];
+  // [chunk parity][head][token]: dt and the in-chunk cumulative log decay, in
+  // log2 units (so every decay factor is one ex2)
+  __shared__ __align__(16) float cum[2][2][SQ];
+  __shared__ __align__(16) float dts[2][2][SQ];
+  __shared__ float wsum[2][SQ / 32];
   pdl_wait_then_release();
   const int tid = threadIdx.x;
   const int H = p.H, G = p.G;
@@ -502,22 +521,46 @@ ssd_chunk_kernel(SsdParams p, const __grid_constant__ CUtensorMap txs) {
   const int wblk = p.blk[s];
   const int rblk = p.has_past[s] ? wblk : 0;
   const uint32_t sbase = smem_u32(sm);
+  const int nc = (L + SQ - 1) / SQ;
 
+  // loads: X of chunk cc into region xb (OFF_X or OFF_M); B and C of chunk cc
+  auto issue_x = [&](int cc, int xb) {
+    unsigned char* xt = sm + (xb ? OFF_M : OFF_X);
+    mbar_arrive_expect_tx(&full_x[xb], 2 * CBOX);
+    tma_load_2d(xt, &txs, h0 * SP, seq0 + cc * SQ, &full_x[xb]);
+    tma_load_2d(xt + CBOX, &txs, h0 * SP + SP, seq0 + cc * SQ, &full_x[xb]);
+  };
+  auto issue_bc = [&](int cc) {
+    const int r = seq0 + cc * SQ;
+    mbar_arrive_expect_tx(&full_bc, 4 * CBOX);
+    tma_load_2d(sm + OFF_B, &txs, H * SP + g * SN, r, &full_bc);
+    tma_load_2d(sm + OFF_B + CBOX, &txs, H * SP + g * SN + 64, r, &full_bc);
+    tma_load_2d(sm + OFF_C, &txs, H * SP + G * SN + g * SN, r, &full_bc);
+    tma_load_2d(sm + OFF_C + CBOX, &txs, H * SP + G * SN + g * SN + 64, r, &full_bc);
+  };
+  bool x_pending[2] = {false, false}, bc_pending = false;  // (thread 0's record)
   if (tid == 0) {
-    mbar_init(&full, 1);
+    mbar_init(&full_x[0], 1);
+    mbar_init(&full_x[1], 1);
+    mbar_init(&full_bc, 1);
     mbar_init(&mma_bar, 1);
     fence_mbar_init();
+    issue_x(0, 0);
+    issue_bc(0);
+    x_pending[0] = bc_pending = true;
   }
   if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane = (uint32_t)(tid & 96) << 16;  // TMEM lane quarter of this warp
+  // thread = (TMEM lane row = tid % 128 of this warp's lane quarter, column
+  // quarter cg = tid / 128): 32 columns of every 128-column accumulator
+  const uint32_t lane = (uint32_t)(tid & 96) << 16;
   const int row = tid & 127;                          // TMEM lane: token t or (head, p)
-  const int hf = tid >> 7;                            // column half
+  const int cg = tid >> 7;                            // column quarter
   const int rhead = row >> 6, rp = row & 63;          // (head, p) of a state row
-  uint32_t ph_full = 0, ph_mma = 0;
+  uint32_t ph_x[2] = {0, 0}, ph_bc = 0, ph_mma = 0;
   bool dead = false;
   float amax = 0.f;
   const float* S_r = reinterpret_cast<const float*>(p.layer_base + (size_t)rblk * p.stride +
@@ -525,94 +568,111 @@ ssd_chunk_kernel(SsdParams p, const __grid_constant__ CUtensorMap txs) {
   float* S_w = reinterpret_cast<float*>(p.layer_base + (size_t)wblk * p.stride + p.ssm_off);
   __nv_bfloat16* __restrict__ yout = reinterpret_cast<__nv_bfloat16*>(p.y);
   const __nv_bfloat16* __restrict__ dtr = reinterpret_cast<const __nv_bfloat16*>(p.dt);
-  const int nc = (L + SQ - 1) / SQ;
 
-  // ---- initial state into TMEM (row = (head, p), columns n of this half)
+  // time steps and in-chunk cumulative log decays of the two heads for chunk
+  // cc into parity buffer cb (threads 0..255: head tid / 128, token tid %
+  // 128; an inclusive scan by warp shuffles, then the warp prefix); every
+  // thread calls it (one barrier inside)
+  auto gates = [&](int cc, int cb) {
+    const int n = min(SQ, L - cc * SQ);
+    const int hh = tid >> 7, t = tid & 127, ln = tid & 31;
+    float v = 0.f;
+    if (tid < 2 * SQ) {
+      const int h = h0 + hh;
+      float d = 0.f;
+      if (t < n)
+        d = softplus_f32(__bfloat162float(dtr[(size_t)(seq0 + cc * SQ + t) * H + h]) + p.dt_bias[h]);
+      dts[cb][hh][t] = d;
+      v = -__expf(p.A_log[h]) * d * 1.4426950408889634f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (ln >= o) v += u;
+      }
+      if (ln == 31) wsum[hh][t >> 5] = v;
+    }
+    __syncthreads();
+    if (tid < 2 * SQ) {
+      float add = 0.f;
+      for (int w = 0; w < (t >> 5); ++w) add += wsum[hh][w];
+      cum[cb][hh][t] = v + add;
+    }
+  };
+
+  // ---- initial state into TMEM (row = (head, p), columns n of this quarter;
+  // 128 contiguous bytes of the state row, 16-byte loads)
   {
     float hv[32];
+    const int n0 = cg * 32;
+    const float4* src = reinterpret_cast<const float4*>(S_r + ((size_t)(h0 + rhead) * SP + rp) * SN + n0);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int n0 = hf * 64 + q * 32;
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        hv[e] = rblk != 0 ? S_r[((size_t)(h0 + rhead) * SP + rp) * SN + n0 + e] : 0.f;
-      tc::tmem_st32(tmem + lane + TM_H + n0, hv);
+    for (int e = 0; e < 8; ++e) {
+      const float4 v = rblk != 0 ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+      hv[4 * e] = v.x; hv[4 * e + 1] = v.y; hv[4 * e + 2] = v.z; hv[4 * e + 3] = v.w;
     }
+    tc::tmem_st32(tmem + lane + TM_H + n0, hv);
     tc::tmem_wait_st();
   }
+  gates(0, 0);
 
   for (int c = 0; c < nc; ++c) {
     const int r0 = seq0 + c * SQ;
     const int n = min(SQ, L - c * SQ);
-    // ---- tiles of this chunk
+    const int xb = c & 1;
+    const uint32_t OX = xb ? OFF_M : OFF_X;  // this chunk's X; its M_0 goes to the other
+    const uint32_t OM = xb ? OFF_X : OFF_M;
+    // ---- this chunk's tiles (issued one chunk ahead)
     if (tid == 0) {
-      mbar_arrive_expect_tx(&full, 6 * CBOX);
-      tma_load_2d(sm + OFF_X, &txs, h0 * SP, r0, &full);
-      tma_load_2d(sm + OFF_X + CBOX, &txs, h0 * SP + SP, r0, &full);
-      tma_load_2d(sm + OFF_B, &txs, H * SP + g * SN, r0, &full);
-      tma_load_2d(sm + OFF_B + CBOX, &txs, H * SP + g * SN + 64, r0, &full);
-      tma_load_2d(sm + OFF_C, &txs, H * SP + G * SN + g * SN, r0, &full);
-      tma_load_2d(sm + OFF_C + CBOX, &txs, H * SP + G * SN + g * SN + 64, r0, &full);
-    }
-    // ---- time steps and in-chunk cumulative log decays of the two heads
-    {
-      const int hh = tid >> 7, t = tid & 127;
-      const int h = h0 + hh;
-      float d = 0.f;
-      if (t < n) d = softplus_f32(__bfloat162float(dtr[(size_t)(r0 + t) * H + h]) + p.dt_bias[h]);
-      dts[hh][t] = d;
-      cum[hh][t] = -__expf(p.A_log[h]) * d;
+      const bool bc_ok = mbar_wait_bounded(&full_bc, ph_bc);
+      const bool x_ok = bc_ok && mbar_wait_bounded(&full_x[xb], ph_x[xb]);
+      if (bc_ok) bc_pending = false;
+      if (x_ok) x_pending[xb] = false;
+      okf = x_ok ? 1 : 0;
     }
     __syncthreads();
-    // inclusive scan over t (Hillis-Steele, 7 steps) per head
-    for (int off = 1; off < SQ; off <<= 1) {
-      const int hh = tid >> 7, t = tid & 127;
-      const float add = t >= off ? cum[hh][t - off] : 0.f;
-      __syncthreads();
-      cum[hh][t] += add;
-      __syncthreads();
-    }
-    if (!ssd_cta_wait(&full, ph_full, &okf)) { dead = true; break; }
-    ph_full ^= 1;
+    if (!okf) { dead = true; break; }
+    ph_bc ^= 1;
+    ph_x[xb] ^= 1;
+    const float* CU = cum[xb][0];
+    const float* DT = dts[xb][0];
     // ---- rows t >= n of X, B, C -> 0 (another sequence's rows or stale data)
     if (n < SQ) {
       for (int i = tid; i < (SQ - n) * 8 * 6; i += kCThreads) {
         const int box = i / ((SQ - n) * 8);
         const int rem = i % ((SQ - n) * 8);
         const int r = n + rem / 8, ch = rem % 8;
-        *reinterpret_cast<uint4*>(sm + box * CBOX + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        const uint32_t base = box < 2 ? OX + box * CBOX : OFF_B + (box - 2) * CBOX;
+        *reinterpret_cast<uint4*>(sm + base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
       }
     }
     // ---- hand-over: h16 <- h (fp16, K-major rows (head,p)), h <- e^{cum[n-1]} h
     {
-      const float dc = __expf(cum[rhead][n - 1]);
+      const float dc = ssd_ex2(CU[rhead * SQ + n - 1]);
+      const int n0 = cg * 32;
+      float hv[32];
+      tc::tmem_ld32(tmem + lane + TM_H + n0, hv);
+      tc::tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int n0 = hf * 64 + q * 32;
-        float hv[32];
-        tc::tmem_ld32(tmem + lane + TM_H + n0, hv);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          amax = fmaxf(amax, max_abs3(max_abs3(hv[e], hv[e + 1], hv[e + 2]),
-                                      max_abs3(hv[e + 3], hv[e + 4], hv[e + 5]),
-                                      max_abs3(hv[e + 6], hv[e + 7], 0.f)));
-          tc::sw128_store8<E>(sm + OFF_H16 + hf * CBOX, row, q * 32 + e, hv + e);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) hv[e] *= dc;
-        tc::tmem_st32(tmem + lane + TM_H + n0, hv);
+      for (int e = 0; e < 32; e += 8) {
+        amax = fmaxf(amax, max_abs3(max_abs3(hv[e], hv[e + 1], hv[e + 2]),
+                                    max_abs3(hv[e + 3], hv[e + 4], hv[e + 5]),
+                                    max_abs3(hv[e + 6], hv[e + 7], 0.f)));
+        tc::sw128_store8<E>(sm + OFF_H16 + (cg >> 1) * CBOX, row, (cg & 1) * 32 + e, hv + e);
       }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) hv[e] *= dc;
+      tc::tmem_st32(tmem + lane + TM_H + n0, hv);
       tc::tmem_wait_st();
     }
-    // ---- X'[s][(head,p)] = X dt e^{cum[n-1] - cum[s]}: thread = token s, one box
+    // ---- X'[s][(head,p)] = X dt e^{cum[n-1] - cum[s]}: thread = token s, one
+    // box, one half of its 64 columns
     {
-      const int sidx = tid & 127, hh = tid >> 7;
-      const float f = sidx < n ? dts[hh][sidx] * __expf(cum[hh][n - 1] - cum[hh][sidx]) : 0.f;
-      const unsigned char* xr = sm + OFF_X + hh * CBOX;
+      const int sidx = tid & 127, hh = (tid >> 7) & 1, half = tid >> 8;
+      const float f = sidx < n ? DT[hh * SQ + sidx] * ssd_ex2(CU[hh * SQ + n - 1] - CU[hh * SQ + sidx]) : 0.f;
+      const unsigned char* xr = sm + OX + hh * CBOX;
       unsigned char* xw = sm + OFF_XP + hh * CBOX;
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 8) {
+      for (int k0 = 32 * half; k0 < 32 * half + 32; k0 += 8) {
         const uint4 w = *reinterpret_cast<const uint4*>(xr + tc::sw128_offset(sidx, k0));
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
         float v8[8];
@@ -638,96 +698,144 @@ ssd_chunk_kernel(SsdParams p, const __grid_constant__ CUtensorMap txs) {
                  SQ / 16, tc::idesc_f16_f32(128, 128, true, true), true);
       tc::commit(&mma_bar);
     }
+    // while they run: the next chunk's gates into the other parity buffer
+    if (c + 1 < nc) gates(c + 1, xb ^ 1);
     if (!ssd_cta_wait(&mma_bar, ph_mma, &okf)) { dead = true; break; }
     ph_mma ^= 1;
     tc::fence_after_sync();
-    // ---- per head: M_h from CB, then Y[:, 64 head ..] = M_h X_h
-    for (int hh = 0; hh < 2; ++hh) {
-      {
-        const int t = row;  // token row of CB
-        const float ct = cum[hh][t];
-        float cb[32];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int s0 = hf * 64 + q * 32;
-          tc::tmem_ld32(tmem + lane + TM_CB + s0, cb);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int sidx = s0 + e;
-            cb[e] = (sidx <= t && t < n) ? cb[e] * __expf(ct - cum[hh][sidx]) * dts[hh][sidx] : 0.f;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; e += 8)
-            tc::sw128_store8<E>(sm + OFF_M + hf * CBOX, t, q * 32 + e, cb + e);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-        tc::mma_op(tmem + TM_Y + hh * 64, tc::Opnd{sbase + OFF_M, CBOX, false},
-                   tc::Opnd{sbase + OFF_X + hh * CBOX, CBOX, true}, SQ / 16,
-                   tc::idesc_f16_f32(128, 64, false, true), false);
-        tc::commit(&mma_bar);
-      }
-      if (!ssd_cta_wait(&mma_bar, ph_mma, &okf)) { dead = true; break; }
-      ph_mma ^= 1;
-      tc::fence_after_sync();
+    // B and C are read: the next chunk's come in now
+    if (tid == 0 && c + 1 < nc) {
+      issue_bc(c + 1);
+      bc_pending = true;
     }
-    if (dead) break;
-    // ---- outputs: thread = token t (lane), head = column half
+    // ---- M_h from CB for both heads (thread: token row t, columns s of this
+    // quarter; M_0 to the region X does not use this chunk, M_1 over X', which
+    // the state update has read), then Y[:, 64 head ..] = M_h X_h for both
     {
-      const int t = row, hh = hf;
+      // a warp's 32 rows t = 32 (warp % 4) + lane against its 32 columns s =
+      // 32 cg ..: above the diagonal (cg > warp % 4) the block is zero, below
+      // it (cg < warp % 4) every entry is kept (warp-uniform cases)
+      const int t = row;
+      const int s0 = cg * 32;
+      const int rq = (tid >> 5) & 3;
+      float cb[32];
+      tc::tmem_ld32(tmem + lane + TM_CB + s0, cb);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float m[32];
+        if (cg > rq || t >= n) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) m[e] = 0.f;
+        } else {
+          const float ct = CU[hh * SQ + t];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 cu4 = *reinterpret_cast<const float4*>(CU + hh * SQ + s0 + e);
+            const float4 dt4 = *reinterpret_cast<const float4*>(DT + hh * SQ + s0 + e);
+            m[e] = cb[e] * ssd_ex2(ct - cu4.x) * dt4.x;
+            m[e + 1] = cb[e + 1] * ssd_ex2(ct - cu4.y) * dt4.y;
+            m[e + 2] = cb[e + 2] * ssd_ex2(ct - cu4.z) * dt4.z;
+            m[e + 3] = cb[e + 3] * ssd_ex2(ct - cu4.w) * dt4.w;
+          }
+          if (cg == rq) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (s0 + e > t) m[e] = 0.f;
+          }
+        }
+        unsigned char* mt = sm + (hh ? OFF_XP : OM) + (cg >> 1) * CBOX;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) tc::sw128_store8<E>(mt, t, (cg & 1) * 32 + e, m + e);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        tc::mma_op(tmem + TM_Y + hh * 64, tc::Opnd{sbase + (hh ? OFF_XP : OM), CBOX, false},
+                   tc::Opnd{sbase + OX + hh * CBOX, CBOX, true}, SQ / 16,
+                   tc::idesc_f16_f32(128, 64, false, true), false);
+      tc::commit(&mma_bar);
+    }
+    if (!ssd_cta_wait(&mma_bar, ph_mma, &okf)) { dead = true; break; }
+    ph_mma ^= 1;
+    tc::fence_after_sync();
+    // M_0 is read: the next chunk's X comes into its region now
+    if (tid == 0 && c + 1 < nc) {
+      issue_x(c + 1, xb ^ 1);
+      x_pending[xb ^ 1] = true;
+    }
+    // ---- outputs: thread = token t (lane), head cg / 2, columns 32 (cg % 2) ..
+    // of y = Y + e^{cum[t]} YI + D x, staged as the chunk's bf16 output rows
+    // (token t: the pair's 2 x 64 values, 256 bytes, its 16-byte chunks
+    // XOR-rotated by t % 16) over X', which the Y products have read; then
+    // written out a whole row per 16 threads
+    {
+      const int t = row, hh = cg >> 1, q = cg & 1;
       const int h = h0 + hh;
       float yv[32], yi[32];
-      const float et = __expf(cum[hh][t]);
+      const float et = ssd_ex2(CU[hh * SQ + t]);
       const float Dh = p.Dskip[h];
+      tc::tmem_ld32(tmem + lane + TM_Y + hh * 64 + q * 32, yv);
+      tc::tmem_ld32(tmem + lane + TM_YI + hh * 64 + q * 32, yi);
+      tc::tmem_wait_ld();
+      uint32_t w[16];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        tc::tmem_ld32(tmem + lane + TM_Y + hh * 64 + q * 32, yv);
-        tc::tmem_ld32(tmem + lane + TM_YI + hh * 64 + q * 32, yi);
-        tc::tmem_wait_ld();
-        if (t < n) {
-          uint32_t w[16];
+      for (int e = 0; e < 32; e += 8) {
+        // 8 x values of this row: one 16-byte load
+        const uint4 xw = *reinterpret_cast<const uint4*>(
+            sm + OX + hh * CBOX + tc::sw128_offset(t, q * 32 + e));
+        const uint32_t xu[4] = {xw.x, xw.y, xw.z, xw.w};
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float o2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int pp = q * 32 + e + u;
-              const __half xh = *reinterpret_cast<const __half*>(
-                  sm + OFF_X + hh * CBOX + tc::sw128_offset(t, pp));
-              o2[u] = yv[e + u] + et * yi[e + u] + Dh * __half2float(xh);
-            }
-            w[e / 2] = tc::pack2(o2[0], o2[1], (__nv_bfloat16*)nullptr);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(yout + ((size_t)(r0 + t) * H + h) * SP + q * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        for (int u = 0; u < 4; ++u) {
+          const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xu[u]));
+          const float o0 = yv[e + 2 * u] + et * yi[e + 2 * u] + Dh * xf.x;
+          const float o1 = yv[e + 2 * u + 1] + et * yi[e + 2 * u + 1] + Dh * xf.y;
+          w[(e >> 1) + u] = tc::pack2(o0, o1, (__nv_bfloat16*)nullptr);
         }
+      }
+      unsigned char* orow = sm + OFF_XP + t * 256;
+      const int c0 = hh * 8 + q * 4;  // the row's first 16-byte chunk of these 32 values
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        *reinterpret_cast<uint4*>(orow + (((c0 + v4) ^ (t & 15)) << 4)) =
+            make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < SQ * 16 / kCThreads; ++k) {
+      const int i = tid + k * kCThreads;
+      const int t = i >> 4, ch = i & 15;
+      if (t < n) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sm + OFF_XP + t * 256 + ((ch ^ (t & 15)) << 4));
+        reinterpret_cast<uint4*>(yout + ((size_t)(r0 + t) * H + h0) * SP)[ch] = v;
       }
     }
     tc::fence_proxy_async_smem();  // generic accesses of the tiles before the next TMA writes
     tc::fence_before_sync();
-    __syncthreads();  // every read of this chunk's tiles is done before the next loads
+    __syncthreads();  // every read of this chunk's X is done (its region takes M_0 next)
   }
 
   if (!dead) {
-    // ---- final state (row = (head, p), this half's columns)
+    // ---- final state (row = (head, p), this quarter's columns)
     float hv[32];
+    const int n0 = cg * 32;
+    tc::tmem_ld32(tmem + lane + TM_H + n0, hv);
+    tc::tmem_wait_ld();
+    float4* dst = reinterpret_cast<float4*>(S_w + ((size_t)(h0 + rhead) * SP + rp) * SN + n0);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int n0 = hf * 64 + q * 32;
-      tc::tmem_ld32(tmem + lane + TM_H + n0, hv);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) S_w[((size_t)(h0 + rhead) * SP + rp) * SN + n0 + e] = hv[e];
-    }
+    for (int e = 0; e < 8; ++e)
+      dst[e] = make_float4(hv[4 * e], hv[4 * e + 1], hv[4 * e + 2], hv[4 * e + 3]);
   } else if (tid == 0) {
     atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+    // the loads still in flight land before the CTA's shared memory goes
+    if (bc_pending) mbar_wait_bounded(&full_bc, ph_bc);
+    for (int b = 0; b < 2; ++b)
+      if (x_pending[b]) mbar_wait_bounded(&full_x[b], ph_x[b]);
   }
   if (!(amax <= kCF16Max)) atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_RANGE);
   tc::fence_before_sync();
