@@ -184,14 +184,17 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   pdl_wait_then_release();
   int32_t* hdr = p.work.header();
   const int gidx = blockIdx.x;
-  if (gidx >= hdr[kPreChunks]) return;
   // the chunk's record (scheduler): first packed row, valid tokens, chunk
-  // index inside its sequence, sequence
+  // index inside its sequence, sequence; loaded together with the chunk
+  // count (the scratch holds a record slot for every launched chunk).  A
+  // chain the conv pass already sent to the redo still gets its tiles: the
+  // recurrence skips it, so they are never read (and no load waits on the
+  // redo masks here)
+  const int n_chunks = hdr[kPreChunks];
   const int4 rec = reinterpret_cast<const int4*>(p.scr_c)[gidx];
+  if (gidx >= n_chunks) return;
   const int h = blockIdx.y, kh = h / R, hl = h % R;
   const int row0 = rec.x, n = rec.y, kpre = rec.w;
-  // a chain the conv pass already sent to the redo needs no tiles
-  if (redo_marked(p.work, kpre, h)) return;
   const int Hk = p.Hk, Hv = p.Hv;
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t sbase = smem_u32(sm);
