@@ -131,3 +131,16 @@ def test_chunked_scan_conv_widths_and_short_sequences(K):
     past = [1, 1, 1, 0, 1, 1, 1, 0]
     wl = synth.make_ssd_workload("ssd_conv_widths", dims, lens, past, 16, 13 + K)
     check_ssd_against_oracle(wl)
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_chunked_scan_multi_chunk_chains(slow):
+    """Chains of two to eight 128-token chunks (the X tile and the first
+    head's masked matrix swap shared-memory regions every chunk and the next
+    chunk's tiles load one chunk ahead), lengths on and next to two and three
+    chunks, with and without a past; with slow decay the state carried from
+    chunk to chunk dominates the outputs."""
+    lens = [256, 257, 383, 384, 385, 1000, 2, 1]
+    past = [1, 0, 1, 1, 0, 1, 1, 1]
+    wl = synth.make_ssd_workload("ssd_multi_chunk", FULL, lens, past, 16, 17, slow_decay=slow)
+    check_ssd_against_oracle(wl)
