@@ -41,7 +41,7 @@ EXPORTED = [
     "gdn_ssd_varlen_forward",
     "gdn_get_error",
     "gdn_pool_set_timing_events",
-    "gdn_pool_last_prefill_path",
+    "gdn_prefill_scratch_bytes", "gdn_pool_last_prefill_path",
     "gdn_in_proj",
     "gdn_out_proj",
     "gdn_status_string",
@@ -102,6 +102,7 @@ def load() -> ctypes.CDLL:
     lib.gdn_get_error.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint32), I, P]
     lib.gdn_pool_set_timing_events.argtypes = [P, P, P]
     lib.gdn_pool_last_prefill_path.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_prefill_scratch_bytes.argtypes = [I] * 6 + [PS]
     lib.gdn_in_proj.argtypes = [P, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P]
     lib.gdn_out_proj.argtypes = [P, P, P, ctypes.c_float, P, I, I, I, I, P, P, P, P]
     lib.gdn_diag_umma_gemm.argtypes = [P, P, P, P, I, I, I, P]
@@ -331,6 +332,15 @@ def out_proj(o, z, norm_w, eps, w_out, o_norm, y, flags=None, stream=None) -> No
     _check(load().gdn_out_proj(_ptr(o), _ptr(z), _ptr(norm_w), float(eps), _ptr(w_out), T, Hv,
                                dv, d_model, _ptr(o_norm), _ptr(y), _ptr(flags), _stream(stream)),
            "gdn_out_proj")
+
+
+def prefill_scratch_bytes(num_blocks, Hk, Hv, dk, dv, max_tokens) -> int:
+    """gdn_prefill_scratch_bytes: bytes of prefill scratch the split prefill
+    needs for calls of at most max_tokens tokens."""
+    out = ctypes.c_size_t(0)
+    _check(load().gdn_prefill_scratch_bytes(num_blocks, Hk, Hv, dk, dv, max_tokens,
+                                            ctypes.byref(out)), "gdn_prefill_scratch_bytes")
+    return int(out.value)
 
 
 def varlen_forward_noalloc(pool_mem, num_blocks, num_layers, Hk, Hv, dk, dv, K, act, block_align,

@@ -69,6 +69,17 @@ size_t scratch_part_bytes(const gdn_pool* p, int part) {
     default: return (size_t)p->Hv * 64 * 64 * 2;
   }
 }
+// Part sizes of a gated delta net scratch unit from the head dimensions alone
+// (for callers without a pool object).
+size_t part_bytes_of(int Hk, int Hv, int dk, int dv, int part) {
+  gdn_pool q{};
+  q.Hk = Hk;
+  q.Hv = Hv;
+  q.dk = dk;
+  q.dv = dv;
+  return scratch_part_bytes(&q, part);
+}
+
 // Bytes of one scratch unit: a 64-token chunk of the first `parts` parts
 // (gated delta net pools) or one token row of C fp16 channels (Mamba2 pools).
 size_t scratch_unit_bytes(const gdn_pool* p, int parts = kScrScalarParts) {
@@ -84,11 +95,14 @@ size_t scratch_cap(const gdn_pool* p, int parts = kScrScalarParts) {
 // Units a call with T tokens and N sequences can need: at most T/64 + (number
 // of prefill sequences) chunks, and at most one prefill sequence per
 // non-trash block and per two tokens.
+size_t chunk_units_for(long long T, long long N, int num_blocks) {
+  long long seqs = N < T / 2 ? N : T / 2;
+  if (seqs > num_blocks - 1) seqs = num_blocks - 1;
+  return (size_t)(T / 64 + seqs + 1);
+}
 size_t scratch_units_for(const gdn_pool* p, long long T, long long N) {
   if (p->kind != 0) return (size_t)T;
-  long long seqs = N < T / 2 ? N : T / 2;
-  if (seqs > p->num_blocks - 1) seqs = p->num_blocks - 1;
-  return (size_t)(T / 64 + seqs + 1);
+  return chunk_units_for(T, N, p->num_blocks);
 }
 void* scratch_part(const gdn_pool* p, int part, int parts = kScrScalarParts) {
   size_t off = 0;
@@ -133,6 +147,36 @@ bool capturing(cudaStream_t s) {
 }
 
 bool is_pow2(size_t v) { return v && !(v & (v - 1)); }
+
+}  // namespace
+
+namespace gdn {
+size_t prefill_scratch_unit_bytes(int Hk, int Hv, int dk, int dv) {
+  size_t b = 0;
+  for (int i = 0; i < kScrScalarParts; ++i) b += part_bytes_of(Hk, Hv, dk, dv, i);
+  return b;
+}
+size_t prefill_scratch_units(long long T, long long N, int num_blocks) {
+  return chunk_units_for(T, N, num_blocks);
+}
+void prefill_scratch_parts(unsigned char* base, size_t cap_units, int Hk, int Hv, int dk, int dv,
+                           FwdParams* fp) {
+  void* part[kScrScalarParts];
+  size_t off = 0;
+  for (int i = 0; i < kScrScalarParts; ++i) {
+    part[i] = base + off * cap_units;
+    off += part_bytes_of(Hk, Hv, dk, dv, i);
+  }
+  fp->scr_qk = part[kScrQK];
+  fp->scr_g = part[kScrG];
+  fp->scr_w = part[kScrW];
+  fp->scr_u = part[kScrU];
+  fp->scr_p = part[kScrP];
+  fp->scr_c = part[kScrC];
+}
+}  // namespace gdn
+
+namespace {
 
 int check_dims(int num_blocks, int num_layers, int Hk, int Hv, int dk, int dv, int K, int act,
                size_t block_align) {
@@ -462,6 +506,17 @@ int gdn_state_pool_reserve(gdn_pool_t* p, int max_tokens) {
     return GDN_OK;
   }
   p->scr_grow = true;
+  return GDN_OK;
+}
+
+int gdn_prefill_scratch_bytes(int num_blocks, int num_k_heads, int num_v_heads, int d_k, int d_v,
+                              int max_tokens, size_t* bytes) {
+  if (!bytes) return GDN_ERR_NULL;
+  if (num_blocks < 2 || max_tokens < 0) return GDN_ERR_RANGE;
+  if (num_k_heads < 1 || num_v_heads < 1 || d_k < 1 || d_v < 1) return GDN_ERR_DIMS;
+  // any N: at most one prefill sequence per two tokens
+  *bytes = gdn::prefill_scratch_units(max_tokens, max_tokens, num_blocks) *
+           gdn::prefill_scratch_unit_bytes(num_k_heads, num_v_heads, d_k, d_v);
   return GDN_OK;
 }
 

@@ -206,6 +206,15 @@ cudaError_t launch_ssd_decode(const SsdParams& p, int max_dec, cudaStream_t stre
 bool ssd_chunk_supported(int H, int P, int NS, int K, int act);
 cudaError_t launch_ssd_chunk(const SsdParams& p, void* xs, int max_pre, cudaStream_t stream);
 
+// The scalar-gate split prefill's scratch (host side, gdn_api.cu): bytes per
+// 64-token chunk, the chunks a call with T tokens and N sequences can need on
+// a pool of num_blocks blocks, and the part pointers of a buffer of cap_units
+// chunks laid out part-major.
+size_t prefill_scratch_unit_bytes(int Hk, int Hv, int dk, int dv);
+size_t prefill_scratch_units(long long T, long long N, int num_blocks);
+void prefill_scratch_parts(unsigned char* base, size_t cap_units, int Hk, int Hv, int dk, int dv,
+                           FwdParams* fp);
+
 // The dense neighbours (gdn_proj.cu): C_g = A B_g^T for up to four groups
 // sharing A (bf16, row-major, K contiguous; fp32 accumulation; bf16 out), and
 // the gated RMS norm of the output (d_v = 128).

@@ -125,6 +125,17 @@ extern "C" int gdn_varlen_forward_noalloc(void* pool_mem, size_t pool_bytes, int
     fp.max_seqlen_hint = max_seqlen_hint;
     fp.work.base = work;
     fp.work.num_blocks = num_blocks;
+    // memory past the pool's layout (from the next 256-byte boundary) serves
+    // as the split prefill's scratch when it holds this call's chunks;
+    // otherwise prefills run on the fused kernel
+    if (T > 1 && max_seqlen_hint != 1 && gdn::chunk_supported(d_k, act_dtype, conv_k)) {
+      const size_t units = gdn::prefill_scratch_units(T, N, num_blocks);
+      const size_t need = units * gdn::prefill_scratch_unit_bytes(num_k_heads, num_v_heads, d_k, d_v);
+      const size_t start = (total + 255) / 256 * 256;
+      if (pool_bytes >= start && pool_bytes - start >= need)
+        gdn::prefill_scratch_parts(static_cast<unsigned char*>(pool_mem) + start, units,
+                                   num_k_heads, num_v_heads, d_k, d_v, &fp);
+    }
     if (gdn::launch_schedule(fp, s) != cudaSuccess) return GDN_ERR_CUDA;
     if (T > 0) {
       int max_items = N;

@@ -280,6 +280,13 @@ int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const v
                            const uint8_t* has_past, const gdn_ssd_weights_t* weights, void* y,
                            int T, int N, int max_seqlen_hint, void* stream);
 
+/* Bytes of prefill scratch the split prefill needs for calls of at most
+ * max_tokens tokens (any number of sequences) on a pool of these dimensions
+ * (for callers that provide it themselves, see gdn_varlen_forward_noalloc).
+ * Returns GDN_ERR_NULL, GDN_ERR_RANGE or GDN_ERR_DIMS on bad arguments. */
+int gdn_prefill_scratch_bytes(int num_blocks, int num_k_heads, int num_v_heads, int d_k, int d_v,
+                              int max_tokens, size_t* bytes);
+
 /* gdn_varlen_forward for callers that cannot allocate device memory.  The
  * pages have no counterpart to this entry point: it exists for engines that
  * plan every byte of device memory ahead and forbid runtime allocation, and
@@ -291,7 +298,12 @@ int gdn_ssd_varlen_forward(gdn_pool_t* pool, int layer, const void* xbc, const v
  *                          dimensions, laid out as gdn_state_pool_layout_for
  *                          describes (256-byte aligned, pool_bytes >= its
  *                          total_bytes); the caller keeps block 0 of every
- *                          layer zeroed (the trash block)
+ *                          layer zeroed (the trash block).  Bytes past
+ *                          total_bytes, from the next 256-byte boundary, are
+ *                          the call's prefill scratch when there are at least
+ *                          gdn_prefill_scratch_bytes(..., T, ...) of them:
+ *                          prefills then run on the split kernels as in
+ *                          gdn_varlen_forward, else on the fused kernel
  *   num_blocks .. block_align : the pool's dimensions (as for
  *                          gdn_state_pool_create)
  *   layer, x_qkv .. max_seqlen_hint : as for gdn_varlen_forward

@@ -127,3 +127,13 @@ def test_ssd_null_arguments_are_rejected_without_device_work():
     w = binding.SsdWeights(None, None, None, None)
     assert lib.gdn_ssd_varlen_forward(None, 0, None, None, None, None, None, ctypes.byref(w),
                                       None, 0, 0, 0, None) == -1
+
+
+def test_prefill_scratch_bytes_grows_with_the_call():
+    """The scratch size query: one slot per 64-token chunk plus one per
+    possible prefill sequence, and argument checks."""
+    small = binding.prefill_scratch_bytes(64, 16, 32, 128, 128, 64)
+    large = binding.prefill_scratch_bytes(64, 16, 32, 128, 128, 16384)
+    assert 0 < small < large
+    with pytest.raises(binding.GdnError):
+        binding.prefill_scratch_bytes(1, 16, 32, 128, 128, 64)

@@ -91,3 +91,32 @@ def test_noalloc_reports_flags_and_rejects_oversized_pools():
             run.cu, run.idx, run.has_past, run.conv_w, run.A_log, run.dt_bias, out, wl.T, wl.N,
             0, flags)
     assert e.value.status == -3
+
+
+def test_noalloc_with_scratch_after_the_pool_runs_the_split_prefill():
+    """Pool memory with gdn_prefill_scratch_bytes more bytes after the pool's
+    layout: the allocation-free call runs the split prefill kernels in them,
+    exactly as the pool entry point does (bit-identical outputs and states)."""
+    wl = synth.make_workload("noalloc_split", synth.FULL_DIMS, [1, 300, 1, 129, 64, 3],
+                             [1, 1, 0, 0, 1, 1], 16, 35)
+    d = wl.dims
+    ref = harness.DeviceRun(wl)
+    snapshot = ref.mem.clone()
+    ref.run()
+    torch.cuda.synchronize()
+    assert ref.pool.last_prefill_path() == binding.PREFILL_SPLIT
+    extra = binding.prefill_scratch_bytes(wl.num_blocks, d.Hk, d.Hv, d.dk, d.dv, wl.T)
+    assert extra > 0
+    total = snapshot.numel()
+    mem = torch.zeros((total + 255) // 256 * 256 + extra, dtype=torch.uint8, device="cuda")
+    mem[:total].copy_(snapshot)
+    dev = {k: getattr(wl, k).cuda() for k in ("x", "a", "b", "cu_seqlens", "block_idx",
+                                              "has_past")}
+    out = torch.full_like(ref.out, harness.OUT_SENTINEL)
+    flags = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _noalloc_call(mem, wl, ref, dev["x"], dev["a"], dev["b"], dev["cu_seqlens"],
+                  dev["block_idx"], dev["has_past"], out, flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    assert torch.equal(out, ref.out)
+    assert torch.equal(mem[:total], ref.mem)
