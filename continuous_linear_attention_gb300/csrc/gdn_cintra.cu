@@ -689,7 +689,10 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   tc::fence_before_sync();
   __syncthreads();
   if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
-  if (tid == 0) bulk_wait_all();  // the tiles have reached the scratch before the CTA ends
+  // the shared-memory sources of the tile stores are read before the CTA ends;
+  // the stores themselves complete with the grid (the recurrence kernel, launched
+  // after it, waits for that)
+  if (tid == 0) bulk_wait_read_all();
 }
 
 }  // namespace

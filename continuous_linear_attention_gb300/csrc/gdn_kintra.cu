@@ -612,7 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   tc::fence_before_sync();
   __syncthreads();
   if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
-  if (tid == 0) bulk_wait_all();  // the tiles have reached the scratch before the CTA ends
+  // the shared-memory sources of the tile stores are read before the CTA ends;
+  // the stores themselves complete with the grid (the recurrence kernel, launched
+  // after it, waits for that)
+  if (tid == 0) bulk_wait_read_all();
 }
 
 }  // namespace
