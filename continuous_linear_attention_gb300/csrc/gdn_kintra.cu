@@ -14,15 +14,15 @@
 // and the recurrence kernel then forms U = u - w S0^T, O = q^ S0^T + P U and
 // S = S0 Diag(e^{Gamma_C}) + U^T k^.  Every decay factor above is a product
 // of alphas over a token range (all <= 1), so this kernel takes no pairwise
-// exponentials: it forms the per-channel products by running products over
-// the tokens, one thread per channel pair:
-//   q^ and -k~ e^{Gamma} forward from the chunk start, k^ backward from its
-//   end, e^{Gamma_C} at the end;
+// exponentials and no ratios of products: each thread (channel pair, 8-token
+// block) forms the running products inside its block, forward and backward,
+// and every factor is one of them times the totals E8 of whole blocks:
+//   q^ and -k~ e^{Gamma} from the chunk start, k^ to its end, e^{Gamma_C};
 //   for the three 16-token sub-chunks I = 1..3, with r the last token before
-//   I: L_I = [q~ ; k~]_I e^{Gamma_i - Gamma_r} forward from r and R_I =
-//   k~_{j <= r} e^{Gamma_r - Gamma_j} backward from r, so that the
-//   off-diagonal 16 x 16 blocks of A and P are plain products L_I R_I^T
-//   (mma.sync, fp16 operands <= 1, fp32 accumulation);
+//   I: L_I = [q~ ; k~]_I e^{Gamma_i - Gamma_r} and R_I = k~_{j <= r}
+//   e^{Gamma_r - Gamma_j}, so that the off-diagonal 16 x 16 blocks of A and P
+//   are plain products L_I R_I^T (mma.sync, fp16 operands <= 1, fp32
+//   accumulation);
 //   inside each diagonal 16 x 16 block, with m its eighth token, the
 //   lower-left 8 x 8 quadrant the same way (L'_I = [q~ ; k~]_i e^{Gamma_i -
 //   Gamma_m}, R'_I = k~_j e^{Gamma_m - Gamma_j}), and the two diagonal 8 x 8
@@ -68,6 +68,7 @@ constexpr float kF16Max = 65000.f;
 //   PT  P fp16 [64 i][64 j] (K-major B operand of the output product)
 //   AT  A, then T, fp32 [64][AP]
 //   GB  beta fp32 [64]
+//   E8  alpha products over each 8-token block, fp32 [8 blocks][128 channels]
 constexpr uint32_t OFF_QK = 0;
 constexpr uint32_t OFF_V = 32768;
 constexpr uint32_t OFF_LM = 49152;
@@ -80,7 +81,8 @@ constexpr uint32_t OFF_UW = OFF_LR + 16384;  // u, then -w: 2 boxes each
 constexpr uint32_t OFF_PT = 184320;
 constexpr uint32_t OFF_AT = OFF_PT + BOX;
 constexpr uint32_t OFF_GB = OFF_AT + CH * AP * 4;
-constexpr uint32_t SMEM_BYTES = OFF_GB + CH * 4 + 1024;
+constexpr uint32_t OFF_E8 = OFF_GB + CH * 4;
+constexpr uint32_t SMEM_BYTES = OFF_E8 + 8 * D * 4 + 1024;
 constexpr int kLRows = 96;  // rows of L_1..L_3
 static_assert(OFF_LR + 192 * LRP * 2 <= OFF_PT, "L / R rows");
 static_assert(OFF_Z + solve::kZFloats * 4 <= OFF_PT, "solve blocks");
@@ -216,9 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
 
   // ---- gates: alpha_i[c] = e^{-e^{A_log} softplus(a_i[c] + dt_bias[c])}
-  // (thread: channel pair 2 (tid % 64), tokens 8 (tid / 64) .. + 7, all loads
-  // first; 1 past the end), beta_i = sigmoid(b_i) (0 past the end); the P
-  // tile starts zero
+  // (thread: channel pair 2 (tid % 64), tokens of the 8-token block tid / 64,
+  // all loads first; 1 past the end), beta_i = sigmoid(b_i) (0 past the end);
+  // the P tile starts zero.  The thread keeps the products inside its block
+  // (b8[t] = alpha_{8b} .. alpha_{8b+t}, s8[t] = alpha_{8b+t+1} .. alpha_{8b+7})
+  // and publishes the block's total b8[7] in the E8 table
+  float2 b8[8], s8[8];
   {
     const int c = 2 * (tid & 63), i0 = 8 * (tid >> 6);
     const float ea = __expf(p.A_log[h]);
@@ -229,16 +234,25 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
 #pragma unroll
     for (int t = 0; t < 8; ++t)
       if (i0 + t < n) araw[t] = av[(((size_t)(row0 + i0 + t) * Hv + h) * D + c) >> 1];
+    float2 al[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      float2 al = make_float2(1.f, 1.f);
+      al[t] = make_float2(1.f, 1.f);
       if (i0 + t < n) {
         const float2 x = __bfloat1622float2(araw[t]);
-        al.x = __expf(-ea * softplus_fast(x.x + db.x));
-        al.y = __expf(-ea * softplus_fast(x.y + db.y));
+        al[t].x = __expf(-ea * softplus_fast(x.x + db.x));
+        al[t].y = __expf(-ea * softplus_fast(x.y + db.y));
       }
-      *reinterpret_cast<float2*>(AL + (i0 + t) * D + c) = al;
+      *reinterpret_cast<float2*>(AL + (i0 + t) * D + c) = al[t];
     }
+    b8[0] = al[0];
+#pragma unroll
+    for (int t = 1; t < 8; ++t) b8[t] = make_float2(b8[t - 1].x * al[t].x, b8[t - 1].y * al[t].y);
+    s8[7] = make_float2(1.f, 1.f);
+#pragma unroll
+    for (int t = 6; t >= 0; --t)
+      s8[t] = make_float2(s8[t + 1].x * al[t + 1].x, s8[t + 1].y * al[t + 1].y);
+    reinterpret_cast<float2*>(sm + OFF_E8)[tid] = b8[7];  // E8[block][pair]
     if (tid < CH) {
       const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
       GB[tid] = tid < n ? sigmoid_f32(__bfloat162float(bv[(size_t)(row0 + tid) * Hv + h])) : 0.f;
@@ -253,122 +267,67 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   bool ok = cta_wait(&ldbar, 0, &flag);
 
   if (ok) {
-    // ---- running products over the tokens, thread group gr = tid / 64 and
-    // channel pair c = 2 (tid % 64); the chains (token steps):
-    //   0 R_3 (48);  1 R_2, L'_0, L'_1 (48);  2 L_1, L_2, L_3 (48);
-    //   3 R_1, R'_0..R'_3 (48);  4 L'_2, L'_3, -k~ e^{Gamma} rows 0..31 (48);
-    //   5 -k~ e^{Gamma} rows 32..63 (32);  6 e^{Gamma_C} (64 products)
-    const int gr = tid >> 6, c = 2 * (tid & 63);
+    // ---- decay products of every operand row, thread group gr = tid / 64
+    // (the 8-token block b = gr, rows i = 8 b + t) and channel pair c = 2 (tid
+    // % 64).  Each factor is the thread's in-block product times totals E8 of
+    // whole blocks, all multiplications (no ratio of products, which could
+    // meet 0 / 0 where the decay underflows):
+    //   L_J (16-block J = b / 2 >= 1, from its first token): b8[t], times E8
+    //     of block b - 1 in the second half;
+    //   L'_J (b odd, from token 16 J + 8): b8[t];   R'_J (b even, to token
+    //     16 J + 7): s8[t];
+    //   R_I (I = J + 1 .. 3, to token 16 I - 1): s8[t] E8_{b+1} .. E8_{2I-1};
+    //   -k~ e^{Gamma} (from the chunk start): b8[t] E8_0 .. E8_{b-1};
+    //   e^{Gamma_C}: E8_0 .. E8_7.
+    const int gr = tid >> 6, c = 2 * (tid & 63), J = gr >> 1;
     const unsigned char* QK = sm + OFF_QK;
+    const float2* E8 = reinterpret_cast<const float2*>(sm + OFF_E8) + (c >> 1);  // block b at E8[64 b]
     const float2* AL2 = reinterpret_cast<const float2*>(AL) + (c >> 1);  // row i at AL2[i * 64]
-    // L_I rows: [q~ ; k~]_i e^{Gamma_i - Gamma_r}, r = 16 I - 1, forward from r
-    auto l_rows = [&](int I) {
-      float2 f = make_float2(1.f, 1.f);
-      unsigned char* lr = sm + OFF_LR + (size_t)((I - 1) * 32) * (LRP * 2) + c * 2;
-#pragma unroll 8
-      for (int t = 0; t < 16; ++t) {
-        const int i = 16 * I + t;
-        const float2 a = AL2[i * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-        const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
-        st_h2(lr + t * (LRP * 2), q.x * f.x, q.y * f.y);
-        st_h2(lr + (16 + t) * (LRP * 2), k.x * f.x, k.y * f.y);
-      }
-    };
-    // R_I rows j = 0 .. r: k~_j e^{Gamma_r - Gamma_j}, backward from r
-    auto r_rows = [&](int I) {
-      const int r = 16 * I - 1;
-      const int rb = kLRows + 8 * I * (I - 1);  // first row of R_I (96, 112, 144)
-      float2 f = make_float2(1.f, 1.f);
-#pragma unroll 8
-      for (int j = r; j >= 0; --j) {
-        const float2 k = ld_h2(QK + qk_off(CH + j, c));
-        st_h2(sm + OFF_LR + (size_t)(rb + j) * (LRP * 2) + c * 2, k.x * f.x, k.y * f.y);
-        const float2 a = AL2[j * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-      }
-    };
-    // L'_I rows (LM rows 24 I + t and 24 I + 8 + t): [q~ ; k~]_i e^{Gamma_i -
-    // Gamma_m}, i = 16 I + 8 + t, m = 16 I + 7, forward from m
-    auto lm_rows = [&](int I) {
-      float2 f = make_float2(1.f, 1.f);
-      unsigned char* lr = sm + OFF_LM + (size_t)(24 * I) * (LRP * 2) + c * 2;
+    float2 pb = make_float2(1.f, 1.f);   // E8_0 .. E8_{b-1}
+    float2 fl = make_float2(1.f, 1.f);   // E8_{b-1} in a second half, else 1
+    float2 mr[4];                        // mr[I] = E8_{b+1} .. E8_{2I-1}
+    {
+      float2 m = make_float2(1.f, 1.f);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int i = 16 * I + 8 + t;
-        const float2 a = AL2[i * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-        const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
-        st_h2(lr + t * (LRP * 2), q.x * f.x, q.y * f.y);
-        st_h2(lr + (8 + t) * (LRP * 2), k.x * f.x, k.y * f.y);
+      for (int bb = 0; bb < 8; ++bb) {
+        const float2 e = E8[64 * bb];
+        if (bb < gr) pb = make_float2(pb.x * e.x, pb.y * e.y);
+        if (bb == gr - 1 && (gr & 1)) fl = e;
+        if (bb > gr) m = make_float2(m.x * e.x, m.y * e.y);
+        if (bb & 1) mr[(bb + 1) >> 1 & 3] = m;
       }
-    };
-    // R'_I rows (LM rows 24 I + 16 + t): k~_j e^{Gamma_m - Gamma_j}, j = 16 I +
-    // t, backward from m
-    auto rm_rows = [&](int I) {
-      float2 f = make_float2(1.f, 1.f);
-      unsigned char* lr = sm + OFF_LM + (size_t)(24 * I + 16) * (LRP * 2) + c * 2;
+      if (gr == 7) {
+        // e^{Gamma_C} of every key channel to the gate tile
+        const float2 e = E8[64 * 7];
+        reinterpret_cast<float2*>(p.scr_g)[(((size_t)gidx * Hk + kh) * R + hl) * (D / 2) + (c >> 1)] =
+            make_float2(pb.x * e.x, pb.y * e.y);
+      }
+    }
 #pragma unroll
-      for (int t = 7; t >= 0; --t) {
-        const int j = 16 * I + t;
-        const float2 k = ld_h2(QK + qk_off(CH + j, c));
-        st_h2(lr + t * (LRP * 2), k.x * f.x, k.y * f.y);
-        const float2 a = AL2[j * 64];
-        f.x *= a.x;
-        f.y *= a.y;
+    for (int t = 0; t < 8; ++t) {
+      const int i = 8 * gr + t;
+      const float2 q = ld_h2(QK + qk_off(i, c)), k = ld_h2(QK + qk_off(CH + i, c));
+      if (J >= 1) {  // L_J rows (gr & 1) * 8 + t: q and k
+        const float fx = b8[t].x * fl.x, fy = b8[t].y * fl.y;
+        unsigned char* lr = sm + OFF_LR + (size_t)((J - 1) * 32 + (gr & 1) * 8 + t) * (LRP * 2) + c * 2;
+        st_h2(lr, q.x * fx, q.y * fy);
+        st_h2(lr + 16 * (LRP * 2), k.x * fx, k.y * fy);
       }
-    };
-    // -k~_i e^{Gamma_i} for rows i0 .. i0 + 31, from the product f over the
-    // rows before i0
-    auto nk_rows = [&](int i0, float2 f) {
-#pragma unroll 8
-      for (int i = i0; i < i0 + 32; ++i) {
-        const float2 a = AL2[i * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-        const float2 k = ld_h2(QK + qk_off(CH + i, c));
-        st_h2(sm + OFF_NK + box_off(i, c), -k.x * f.x, -k.y * f.y);
+      if (gr & 1) {  // L'_J rows t (q) and 8 + t (k)
+        unsigned char* lm = sm + OFF_LM + (size_t)(24 * J + t) * (LRP * 2) + c * 2;
+        st_h2(lm, q.x * b8[t].x, q.y * b8[t].y);
+        st_h2(lm + 8 * (LRP * 2), k.x * b8[t].x, k.y * b8[t].y);
+      } else {  // R'_J row t
+        st_h2(sm + OFF_LM + (size_t)(24 * J + 16 + t) * (LRP * 2) + c * 2, k.x * s8[t].x, k.y * s8[t].y);
       }
-    };
-    if (gr == 0) {
-      r_rows(3);
-    } else if (gr == 1) {
-      r_rows(2);
-      lm_rows(0);
-      lm_rows(1);
-    } else if (gr == 2) {
-      l_rows(1);
-      l_rows(2);
-      l_rows(3);
-    } else if (gr == 3) {
-      r_rows(1);
-      for (int I = 0; I < 4; ++I) rm_rows(I);
-    } else if (gr == 4) {
-      lm_rows(2);
-      lm_rows(3);
-      nk_rows(0, make_float2(1.f, 1.f));
-    } else if (gr == 5) {
-      float2 f = make_float2(1.f, 1.f);
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const float2 a = AL2[i * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-      }
-      nk_rows(32, f);
-    } else if (gr == 6) {
-      // e^{Gamma_C} of every key channel to the gate tile
-      float2 f = make_float2(1.f, 1.f);
-#pragma unroll 8
-      for (int i = 0; i < CH; ++i) {
-        const float2 a = AL2[i * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-      }
-      reinterpret_cast<float2*>(p.scr_g)[(((size_t)gidx * Hk + kh) * R + hl) * (D / 2) + (c >> 1)] = f;
+#pragma unroll
+      for (int I = 1; I < 4; ++I)
+        if (I > J) {  // R_I row i
+          const float fx = s8[t].x * mr[I].x, fy = s8[t].y * mr[I].y;
+          st_h2(sm + OFF_LR + (size_t)(kLRows + 8 * I * (I - 1) + i) * (LRP * 2) + c * 2, k.x * fx,
+                k.y * fy);
+        }
+      st_h2(sm + OFF_NK + box_off(i, c), -k.x * (b8[t].x * pb.x), -k.y * (b8[t].y * pb.y));
     }
     tc::fence_proxy_async_smem();  // -k~ e^{Gamma} (MMA operand)
     __syncthreads();
@@ -490,10 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     }
     // ---- T = (I + A)^{-1} on warps 0..3 (diagonal blocks by threads 0..63,
     // then the off-diagonal blocks; named barrier 1 over those 128 threads),
-    // while warps 4..7 turn the [q~ ; k~] tile into [q^ ; k^] in place (every
-    // product has read it): q^_i = q~_i e^{Gamma_i} forward from the chunk
-    // start (threads 128..191), k^_j = k~_j e^{Gamma_C - Gamma_j} backward
-    // from its end (threads 192..255)
+    // while warps 4..15 turn the [q~ ; k~] tile into [q^ ; k^] in place (every
+    // product has read it), one 8-token block of q or k per 64 threads and
+    // task (16 tasks over 6 groups): q^_i = q~_i e^{Gamma_i} forward through
+    // the block from E8_0 .. E8_{b-1}, k^_j = k~_j e^{Gamma_C - Gamma_j}
+    // backward through it from E8_{b+1} .. E8_7
     if (warp < 4) {
       float col[16];
       const int b = (tid >> 4) & 3, m = tid & 15;
@@ -506,29 +466,43 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       solve::offdiag_first(AT, Z, warp);
       solve_bar();
       solve::offdiag_rest(AT, Z, warp);
-    } else if (warp < 6) {
-      float2 f = make_float2(1.f, 1.f);
+    } else {
       unsigned char* QKw = sm + OFF_QK;
-#pragma unroll 8
-      for (int i = 0; i < CH; ++i) {
-        const float2 a = AL2[i * 64];
-        f.x *= a.x;
-        f.y *= a.y;
-        const uint32_t o = qk_off(i, c);
-        const float2 q = ld_h2(QKw + o);
-        st_h2(QKw + o, q.x * f.x, q.y * f.y);
-      }
-    } else if (warp < 8) {
-      float2 f = make_float2(1.f, 1.f);
-      unsigned char* QKw = sm + OFF_QK;
-#pragma unroll 8
-      for (int j = CH - 1; j >= 0; --j) {
-        const uint32_t o = qk_off(CH + j, c);
-        const float2 k = ld_h2(QKw + o);
-        st_h2(QKw + o, k.x * f.x, k.y * f.y);
-        const float2 a = AL2[j * 64];
-        f.x *= a.x;
-        f.y *= a.y;
+#pragma unroll 1
+      for (int task = (tid - 128) >> 6; task < 16; task += 6) {
+        const int b = task & 7;
+        const bool is_q = task < 8;
+        float2 f = make_float2(1.f, 1.f);
+#pragma unroll
+        for (int bb = 0; bb < 8; ++bb)
+          if (is_q ? bb < b : bb > b) {
+            const float2 e = E8[64 * bb];
+            f.x *= e.x;
+            f.y *= e.y;
+          }
+        if (is_q) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int i = 8 * b + t;
+            const float2 a = AL2[i * 64];
+            f.x *= a.x;
+            f.y *= a.y;
+            const uint32_t o = qk_off(i, c);
+            const float2 q = ld_h2(QKw + o);
+            st_h2(QKw + o, q.x * f.x, q.y * f.y);
+          }
+        } else {
+#pragma unroll
+          for (int t = 7; t >= 0; --t) {
+            const int j = 8 * b + t;
+            const uint32_t o = qk_off(CH + j, c);
+            const float2 k = ld_h2(QKw + o);
+            st_h2(QKw + o, k.x * f.x, k.y * f.y);
+            const float2 a = AL2[j * 64];
+            f.x *= a.x;
+            f.y *= a.y;
+          }
+        }
       }
     }
     tc::fence_proxy_async_smem();  // [q^ ; k^] (bulk store)
