@@ -35,6 +35,8 @@
 // token-serial redo.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 #include "gdn_solve.cuh"
@@ -333,10 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     __syncthreads();
 
     // ---- off-diagonal blocks (I, J), I > J: [P ; A / beta] = [L_I^q ; L_I^k]
-    // R_I[16 J ..]^T, one warp per block
-    if (warp < 6) {
-      const int I = warp < 1 ? 1 : (warp < 3 ? 2 : 3);
-      const int J = warp - I * (I - 1) / 2;
+    // R_I[16 J ..]^T, one block on each odd warp 1..11 (the odd warps have the
+    // shorter share of the diagonal pass below)
+    if ((warp & 1) && warp < 12) {
+      const int ob = warp >> 1;
+      const int I = ob < 1 ? 1 : (ob < 3 ? 2 : 3);
+      const int J = ob - I * (I - 1) / 2;
       const int lane = tid & 31;
       const uint32_t lbase = sbase + OFF_LR + (uint32_t)((I - 1) * 32) * (LRP * 2);
       const uint32_t rbase = sbase + OFF_LR + (uint32_t)(kLRows + 8 * I * (I - 1) + 16 * J) * (LRP * 2);
@@ -370,9 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
         }
     }
     // ---- lower-left 8 x 8 quadrants of the diagonal 16-token blocks:
-    // [P ; A / beta] = [L'_I^q ; L'_I^k] R'_I^T, warps 6..9 (block I = warp - 6)
-    if (warp >= 6 && warp < 10) {
-      const int I = warp - 6;
+    // [P ; A / beta] = [L'_I^q ; L'_I^k] R'_I^T, blocks I = 0, 1 on warp 13
+    // and I = 2, 3 on warp 15
+#pragma unroll 1
+    for (int I = warp - 13; I < warp - 11 && warp >= 13 && (warp & 1); ++I) {
       const int lane = tid & 31;
       const uint32_t lbase = sbase + OFF_LM + (uint32_t)(24 * I) * (LRP * 2);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -390,56 +395,84 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       const float bi = GB[i];
       *reinterpret_cast<float2*>(AT + i * AP + j) = make_float2(bi * acc[2], bi * acc[3]);
     }
-    // ---- diagonal 8 x 8 blocks: thread (block B, column j = 8 B + jl,
-    // channel group cq) walks the block's rows i with the running decay
-    // product f[c] = e^{Gamma_i[c] - Gamma_j[c]} over its 16 channels 32 s +
-    // 4 cq + e (s, e < 4: the eight groups of a row read disjoint banks); the
-    // groups' partial sums meet by shuffles.  A warp's four columns start at
-    // its first one's row.
+    // ---- diagonal 8 x 8 blocks: warp (block B, column quad cg) covers the
+    // columns j = 8 B + 4 cg + jj (jj < 4) and the rows from its first
+    // column's on; lane l holds the channels 4 l .. 4 l + 3 and, per column,
+    // the running decay product f = e^{Gamma_i - Gamma_j} on them.  A row's
+    // eight sums (P and A / beta of the four columns) meet over the 32 lanes
+    // in a butterfly (three halving levels, two plain ones); every row's
+    // results wait in registers and are stored at the end.
     {
-      const int B = tid >> 6, jl = (tid >> 3) & 7, cq = tid & 7;
-      const int j = 8 * B + jl;
-      unsigned long long kj[8], f[8];
+      const int B = warp >> 1, cg = warp & 1, lane = tid & 31;
+      const int cl = 4 * lane;
+      auto walk = [&](auto rows) {
+        constexpr int NR = decltype(rows)::value, T0 = 8 - NR;  // T0 = 4 cg
+        unsigned long long kj[4][2], f[4][2];
 #pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) ld_h4p(QK + qk_off(CH + j, 32 * s4 + 4 * cq), kj + 2 * s4);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = f2p(1.f, 1.f);
-#pragma unroll 1
-      for (int tt = jl & 4; tt < 8; ++tt) {
-        const int i = 8 * B + tt;
-        if (tt > jl) {
-#pragma unroll
-          for (int s4 = 0; s4 < 4; ++s4) {
-            const float4 a = *reinterpret_cast<const float4*>(AL + i * D + 32 * s4 + 4 * cq);
-            f[2 * s4] = mul2(f[2 * s4], f2p(a.x, a.y));
-            f[2 * s4 + 1] = mul2(f[2 * s4 + 1], f2p(a.z, a.w));
-          }
+        for (int jj = 0; jj < 4; ++jj) {
+          ld_h4p(QK + qk_off(CH + 8 * B + T0 + jj, cl), kj[jj]);
+          f[jj][0] = f[jj][1] = f2p(1.f, 1.f);
         }
-        unsigned long long sp2 = 0ull, sa2 = 0ull;
+        float res[NR];
 #pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
+        for (int r = 0; r < NR; ++r) {
+          const int tt = T0 + r, i = 8 * B + tt;
+          const float4 a = *reinterpret_cast<const float4*>(AL + i * D + cl);
+          const unsigned long long a01 = f2p(a.x, a.y), a23 = f2p(a.z, a.w);
           unsigned long long q2[2], k2[2];
-          ld_h4p(QK + qk_off(i, 32 * s4 + 4 * cq), q2);
-          ld_h4p(QK + qk_off(CH + i, 32 * s4 + 4 * cq), k2);
+          ld_h4p(QK + qk_off(i, cl), q2);
+          ld_h4p(QK + qk_off(CH + i, cl), k2);
+          float w[8];  // P of columns 0..3, then A / beta
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const unsigned long long kf = mul2(kj[2 * s4 + e], f[2 * s4 + e]);
-            sp2 = fma2(q2[e], kf, sp2);
-            sa2 = fma2(k2[e], kf, sa2);
+          for (int jj = 0; jj < 4; ++jj) {
+            if (tt > T0 + jj) {
+              f[jj][0] = mul2(f[jj][0], a01);
+              f[jj][1] = mul2(f[jj][1], a23);
+            }
+            const unsigned long long kf0 = mul2(kj[jj][0], f[jj][0]), kf1 = mul2(kj[jj][1], f[jj][1]);
+            const unsigned long long sp2 = fma2(q2[1], kf1, mul2(q2[0], kf0));
+            const unsigned long long sa2 = fma2(k2[1], kf1, mul2(k2[0], kf0));
+            w[jj] = __uint_as_float((uint32_t)sp2) + __uint_as_float((uint32_t)(sp2 >> 32));
+            w[4 + jj] = __uint_as_float((uint32_t)sa2) + __uint_as_float((uint32_t)(sa2 >> 32));
+          }
+          // lanes xor 16, 8, 4 each keep half of the values (the upper half
+          // where the bit is set); lane l ends with w[(l >> 2) & 7] summed
+          // over the eight lanes that share l & 3, then xor 2, 1 finish it
+          float w4[4], w2[2];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const bool hi = lane & 16;
+            w4[k] = (hi ? w[4 + k] : w[k]) + __shfl_xor_sync(0xffffffffu, hi ? w[k] : w[4 + k], 16);
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const bool hi = lane & 8;
+            w2[k] = (hi ? w4[2 + k] : w4[k]) + __shfl_xor_sync(0xffffffffu, hi ? w4[k] : w4[2 + k], 8);
+          }
+          const bool hi = lane & 4;
+          float x = (hi ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, hi ? w2[0] : w2[1], 4);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          res[r] = x;
+        }
+        if ((lane & 3) == 0) {
+          const int idx = (lane >> 2) & 7, jj = idx & 3;
+          const int j = 8 * B + T0 + jj;
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            const int tt = T0 + r, i = 8 * B + tt;
+            if (idx < 4) {
+              if (tt >= T0 + jj) *reinterpret_cast<__half*>(sm + OFF_PT + tc::sw128_offset(i, j)) = __float2half_rn(res[r]);
+            } else if (tt > T0 + jj) {
+              AT[i * AP + j] = GB[i] * res[r];
+            }
           }
         }
-        float sp = __uint_as_float((uint32_t)sp2) + __uint_as_float((uint32_t)(sp2 >> 32));
-        float sa = __uint_as_float((uint32_t)sa2) + __uint_as_float((uint32_t)(sa2 >> 32));
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-          sp += __shfl_xor_sync(0xffffffffu, sp, o);
-          sa += __shfl_xor_sync(0xffffffffu, sa, o);
-        }
-        if (cq == 0 && tt >= jl) {
-          *reinterpret_cast<__half*>(sm + OFF_PT + tc::sw128_offset(i, j)) = __float2half_rn(sp);
-          if (tt > jl) AT[i * AP + j] = GB[i] * sa;
-        }
-      }
+      };
+      if (cg)
+        walk(std::integral_constant<int, 4>{});
+      else
+        walk(std::integral_constant<int, 8>{});
     }
     tc::fence_proxy_async_smem();  // the P tile
     __syncthreads();
