@@ -770,7 +770,7 @@ cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t strea
   cudaError_t e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
   if (e != cudaSuccess) return e;
   e = launch_cintra(p, &tmx, max_chunks, true, stream);
-  if (e == cudaSuccess) e = launch_kintra(p, max_chunks, stream);
+  if (e == cudaSuccess) e = launch_kintra(p, max_chunks, num_sms, stream);
   if (e == cudaSuccess) e = launch_seq(p, grid, true, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -174,10 +174,10 @@ cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks,
 // The state recurrence over the prefill chains, reading the chunk-major tiles
 // cintra_kernel (kda: kintra_kernel) leaves in the prefill scratch.
 cudaError_t launch_seq(const FwdParams& p, int grid, bool kda, cudaStream_t stream);
-// The per-channel-decay rule's state-independent chunk products, one CTA per
-// (64-token chunk, v-head), from the conv-only pass's tiles: gates, the
-// decayed q / k tiles, A and P, the solve, u and -w.
-cudaError_t launch_kintra(const FwdParams& p, int max_chunks, cudaStream_t stream);
+// The per-channel-decay rule's state-independent chunk products of every (64-token chunk,
+// v-head), from the conv-only pass's tiles: gates, the decayed q / k tiles, A
+// and P, the solve, u and -w; a persistent grid of up to num_sms CTAs.
+cudaError_t launch_kintra(const FwdParams& p, int max_chunks, int num_sms, cudaStream_t stream);
 // The per-channel-decay (KDA) rule: p.a is [T][Hv][d_k] and p.dt_bias
 // [Hv][d_k].  Decode kernel for the shapes decode_supported() accepts, and the
 // token-serial kernel (as launch_recurrent) for everything else.

@@ -1,5 +1,7 @@
 // State-independent chunk products of the per-channel-decay (KDA) rule's
-// prefill, one CTA per (64-token chunk, v-head), between the conv-only pass of
+// prefill, per (64-token chunk, v-head) on a persistent grid (one CTA per SM
+// walking its items, the next item's inputs loaded during the current one),
+// between the conv-only pass of
 // cintra_kernel (which leaves the chunk's [q~ ; k~] tile and v tiles in the
 // prefill scratch) and the recurrence kernel's KDA instance.
 //
@@ -179,69 +181,134 @@ __device__ __forceinline__ float softplus_fast(float x) {
   return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
 }
 
+// The gate inputs of one item, copied asynchronously (cp.async: nothing
+// held in registers while in flight) into the mid-block rows' space, which is
+// free from the solve until the next item's products: the a tile [64
+// tokens][128 channels] bf16 (16-byte copies, rows past the chunk's end
+// skipped), dt_bias [128] and A_log of the head, and per token the aligned
+// word of b that holds the head's value (Hv is even).  The copies are waited
+// for by every thread before a barrier.
+constexpr uint32_t OFF_GS = OFF_LM;
+constexpr uint32_t OFF_GSD = OFF_GS + CH * D * 2;
+constexpr uint32_t OFF_GSL = OFF_GSD + D * 4;
+constexpr uint32_t OFF_GSB = OFF_GSL + 16;
+static_assert(OFF_GSB + CH * 4 <= OFF_LM + 96 * LRP * 2, "gate staging");
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void stage_gates(const FwdParams& p, int4 rec, int h, int tid,
+                                            uint32_t sbase) {
+  const int Hv = p.Hv, row0 = rec.x, n = rec.y;
+  const unsigned char* av = static_cast<const unsigned char*>(p.a);
+  // all on warps 4..15 (warps 0..3 run the solve and thread 0 drives the
+  // bulk copies: they issue none and never wait for these): 16-byte pieces
+  // q = tid - 128 + 384 e
+  const int u0 = tid - 2 * CH;
+  if (u0 < 0) return;
+#pragma unroll
+  for (int e = 0; e < 3; ++e) {
+    const int q = u0 + e * (kThreads - 2 * CH), r = q >> 4, ch = q & 15;
+    if (q < CH * 16 && r < n)
+      cp_async16(sbase + OFF_GS + r * (D * 2) + ch * 16,
+                 av + ((size_t)(row0 + r) * Hv + h) * (D * 2) + ch * 16);
+  }
+  if (u0 < D) cp_async4(sbase + OFF_GSD + 4 * u0, p.dt_bias + (size_t)h * D + u0);
+  if (u0 == D) cp_async4(sbase + OFF_GSL, p.A_log + h);
+  const int tb = tid - 3 * CH - 1;
+  if (tb >= 0 && tb < n && tb < CH)
+    cp_async4(sbase + OFF_GSB + 4 * tb,
+              reinterpret_cast<const __nv_bfloat16*>(p.b) + (size_t)(row0 + tb) * Hv + (h & ~1));
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Persistent: CTA blockIdx.x takes the items (chunk, v-head) blockIdx.x,
+// + gridDim.x, ... (item = chunk * Hv + v-head, so that the two v-heads of a
+// k-head run side by side and share its [q~ ; k~] tile in L2).  The next
+// item's record and gate inputs are read during the current one's solve and
+// its tiles are loaded during the current one's last products, so an item
+// starts with its inputs on chip.
 __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t ldbar, mbar;
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
+  __shared__ int4 s_next;
   pdl_wait_then_release();
   int32_t* hdr = p.work.header();
-  const int gidx = blockIdx.x;
-  // the chunk's record (scheduler): first packed row, valid tokens, chunk
-  // index inside its sequence, sequence; loaded together with the chunk
-  // count (the scratch holds a record slot for every launched chunk).  A
+  const int Hk = p.Hk, Hv = p.Hv;
+  // items: every chunk of the scheduler's records (first packed row, valid
+  // tokens, chunk index inside its sequence, sequence) times the v-heads.  A
   // chain the conv pass already sent to the redo still gets its tiles: the
   // recurrence skips it, so they are never read (and no load waits on the
   // redo masks here)
-  const int n_chunks = hdr[kPreChunks];
-  const int4 rec = reinterpret_cast<const int4*>(p.scr_c)[gidx];
-  if (gidx >= n_chunks) return;
-  const int h = blockIdx.y, kh = h / R, hl = h % R;
-  const int row0 = rec.x, n = rec.y, kpre = rec.w;
-  const int Hk = p.Hk, Hv = p.Hv;
+  const int n_items = hdr[kPreChunks] * Hv;
+  int item = blockIdx.x;
+  if (item >= n_items) return;
+  const int4* recs = reinterpret_cast<const int4*>(p.scr_c);
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t sbase = smem_u32(sm);
   float* AL = reinterpret_cast<float*>(sm + OFF_AL);
   float* AT = reinterpret_cast<float*>(sm + OFF_AT);
   float* GB = reinterpret_cast<float*>(sm + OFF_GB);
+  // the tiles of an item: [q~ ; k~] of its k-head (expecting the v tile too)
+  // and v of its v-head, on the load barrier's next phase
+  auto issue_qk = [&](int it) {
+    const int g = it / Hv, hh = it % Hv;
+    mbar_arrive_expect_tx(&ldbar, 2 * KB_STRIDE + 2 * BOX);
+    bulk_g2s(sm + OFF_QK,
+             static_cast<const unsigned char*>(p.scr_qk) + ((size_t)g * Hk + hh / R) * (2 * KB_STRIDE),
+             2 * KB_STRIDE, &ldbar);
+  };
+  auto issue_v = [&](int it) {
+    bulk_g2s(sm + OFF_V, static_cast<const unsigned char*>(p.scr_v) + (size_t)it * (2 * BOX), 2 * BOX,
+             &ldbar);
+  };
 
   if (tid == 0) {
     mbar_init(&ldbar, 1);
     mbar_init(&mbar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&ldbar, 2 * KB_STRIDE + 2 * BOX);
-    bulk_g2s(sm + OFF_QK,
-             static_cast<const unsigned char*>(p.scr_qk) + ((size_t)gidx * Hk + kh) * (2 * KB_STRIDE),
-             2 * KB_STRIDE, &ldbar);
-    bulk_g2s(sm + OFF_V, static_cast<const unsigned char*>(p.scr_v) + ((size_t)gidx * Hv + h) * (2 * BOX),
-             2 * BOX, &ldbar);
+    issue_qk(item);
+    issue_v(item);
   }
   if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
+  int4 rec = recs[item / Hv];
+  stage_gates(p, rec, item % Hv, tid, sbase);
+  if (tid >= 2 * CH) cp_async_wait_all();
+  __syncthreads();
+  bool ok = true;
+  uint32_t it_par = 0;   // parity of this item's load and product barriers
+  int pending = 1;       // 1 + parity of a load phase in flight (thread 0's view), or 0
+
+  for (;;) {
+  const int gidx = item / Hv, h = item % Hv, kh = h / R, hl = h % R;
+  const int n = rec.y, kpre = rec.w;
+  const int next = item + (int)gridDim.x;
+  if (tid == 0 && next < n_items) s_next = recs[next / Hv];
 
   // ---- gates: alpha_i[c] = e^{-e^{A_log} softplus(a_i[c] + dt_bias[c])}
-  // (thread: channel pair 2 (tid % 64), tokens of the 8-token block tid / 64,
-  // all loads first; 1 past the end), beta_i = sigmoid(b_i) (0 past the end);
-  // the P tile starts zero.  The thread keeps the products inside its block
-  // (b8[t] = alpha_{8b} .. alpha_{8b+t}, s8[t] = alpha_{8b+t+1} .. alpha_{8b+7})
-  // and publishes the block's total b8[7] in the E8 table
+  // (thread: channel pair 2 (tid % 64), tokens of the 8-token block tid / 64;
+  // 1 past the end), beta_i = sigmoid(b_i) (0 past the end).  The thread
+  // keeps the products inside its block (b8[t] = alpha_{8b} .. alpha_{8b+t},
+  // s8[t] = alpha_{8b+t+1} .. alpha_{8b+7}) and publishes the block's total
+  // b8[7] in the E8 table
   float2 b8[8], s8[8];
   {
     const int c = 2 * (tid & 63), i0 = 8 * (tid >> 6);
-    const float ea = __expf(p.A_log[h]);
-    // (dt_bias carries no alignment promise beyond its element type)
-    const float2 db = make_float2(p.dt_bias[(size_t)h * D + c], p.dt_bias[(size_t)h * D + c + 1]);
-    const __nv_bfloat162* av = reinterpret_cast<const __nv_bfloat162*>(p.a);
-    __nv_bfloat162 araw[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-      if (i0 + t < n) araw[t] = av[(((size_t)(row0 + i0 + t) * Hv + h) * D + c) >> 1];
+    const float ea = __expf(*reinterpret_cast<const float*>(sm + OFF_GSL));
+    const float2 db = *reinterpret_cast<const float2*>(sm + OFF_GSD + c * 4);
     float2 al[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       al[t] = make_float2(1.f, 1.f);
       if (i0 + t < n) {
-        const float2 x = __bfloat1622float2(araw[t]);
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(sm + OFF_GS + (i0 + t) * (D * 2) + c * 2);
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
         al[t].x = __expf(-ea * softplus_fast(x.x + db.x));
         al[t].y = __expf(-ea * softplus_fast(x.y + db.y));
       }
@@ -256,19 +323,24 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       s8[t] = make_float2(s8[t + 1].x * al[t + 1].x, s8[t + 1].y * al[t + 1].y);
     reinterpret_cast<float2*>(sm + OFF_E8)[tid] = b8[7];  // E8[block][pair]
     if (tid < CH) {
-      const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
-      GB[tid] = tid < n ? sigmoid_f32(__bfloat162float(bv[(size_t)(row0 + tid) * Hv + h])) : 0.f;
+      const __nv_bfloat16* bw = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_GSB + 4 * tid);
+      GB[tid] = tid < n ? sigmoid_f32(__bfloat162float(bw[h & 1])) : 0.f;
     }
-    reinterpret_cast<uint4*>(sm + OFF_PT)[tid] = make_uint4(0, 0, 0, 0);
   }
+  // the previous item's tile stores have read their sources (the P tile, the
+  // u / -w staging) before they are written again
+  if (tid == 0) bulk_wait_read_all();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
   float amax = 0.f;  // largest |value| entering an fp16 operand or the u / w scratch
-  bool ok = cta_wait(&ldbar, 0, &flag);
+  ok = cta_wait(&ldbar, it_par, &flag);
+  if (!ok) break;
+  pending = 0;
 
-  if (ok) {
+  {
+    reinterpret_cast<uint4*>(sm + OFF_PT)[tid] = make_uint4(0, 0, 0, 0);  // P starts zero
     // ---- decay products of every operand row, thread group gr = tid / 64
     // (the 8-token block b = gr, rows i = 8 b + t) and channel pair c = 2 (tid
     // % 64).  Each factor is the thread's in-block product times totals E8 of
@@ -480,6 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       bulk_s2g(static_cast<unsigned char*>(p.scr_p) + ((size_t)gidx * Hv + h) * BOX, sm + OFF_PT, BOX);
       bulk_commit();
     }
+    // the next item's record (thread 0 read it at this item's start) and gate
+    // inputs (the mid-block rows are read), in flight during the rest of this
+    // item
+    if (next < n_items) {
+      rec = s_next;
+      stage_gates(p, rec, next % Hv, tid, sbase);
+    }
     // ---- T = (I + A)^{-1} on warps 0..3 (diagonal blocks by threads 0..63,
     // then the off-diagonal blocks; named barrier 1 over those 128 threads),
     // while warps 4..15 turn the [q~ ; k~] tile into [q^ ; k^] in place (every
@@ -580,7 +659,15 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
                  CH / 16, tc::idesc_f16_f32(128, 128, false, true), false);
       tc::commit(&mbar);
     }
-    ok = cta_wait(&mbar, 0, &flag);
+    ok = cta_wait(&mbar, it_par, &flag);
+    // the products have read v, and the [q^ ; k^] store its space: the next
+    // item's tiles
+    if (ok && tid == 0 && next < n_items) {
+      bulk_wait_read_all();
+      issue_qk(next);
+      issue_v(next);
+      pending = 1 + (int)(it_par ^ 1u);
+    }
   }
   if (ok) {
     tc::fence_after_sync();
@@ -612,13 +699,26 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       bulk_commit();
     }
   }
-  if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+  if (!ok) break;
   // T diag(beta), u and w enter tensor-core operands or the scratch in fp16:
   // a value out of its range sends this chain to the token-serial redo
+  tc::fence_before_sync();
+  if (tid >= 2 * CH) cp_async_wait_all();  // the next item's gate inputs, visible after the barrier
   if (__syncthreads_or(!(amax <= kF16Max)) && tid == 0) mark_redo(p.work, kpre, h);
+  if (next >= n_items) break;
+  item = next;
+  it_par ^= 1u;
+  }  // items
+
+  if (!ok && tid == 0) {
+    atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+    // tiles still in flight for an item this CTA will not take land before
+    // it ends (a bounded wait)
+    if (pending) (void)mbar_wait_bounded(&ldbar, (uint32_t)(pending - 1));
+  }
   tc::fence_before_sync();
   __syncthreads();
-  if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+  if (tid < 32) tc::tmem_dealloc(tmem_slot, TM_COLS);
   // the shared-memory sources of the tile stores are read before the CTA ends;
   // the stores themselves complete with the grid (the recurrence kernel, launched
   // after it, waits for that)
@@ -627,12 +727,14 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
 
 }  // namespace
 
-cudaError_t launch_kintra(const FwdParams& p, int max_chunks, cudaStream_t stream) {
+cudaError_t launch_kintra(const FwdParams& p, int max_chunks, int num_sms, cudaStream_t stream) {
   if (max_chunks <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kintra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kintra_kernel, dim3(max_chunks, p.Hv), dim3(kThreads), SMEM_BYTES, stream, p);
+  const long long items = (long long)max_chunks * p.Hv;
+  const int grid = (int)(items < num_sms ? items : num_sms);
+  return launch_pdl(kintra_kernel, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p);
 }
 
 }  // namespace gdn
