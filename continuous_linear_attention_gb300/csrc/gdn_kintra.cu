@@ -1,9 +1,9 @@
 // State-independent chunk products of the per-channel-decay (KDA) rule's
 // prefill, per (64-token chunk, v-head) on a persistent grid (one CTA per SM
 // walking its items, the next item's inputs loaded during the current one),
-// between the conv-only pass of
-// cintra_kernel (which leaves the chunk's [q~ ; k~] tile and v tiles in the
-// prefill scratch) and the recurrence kernel's KDA instance.
+// between the conv-only pass of cintra_kernel (which leaves the chunk's
+// [q~ ; k~] tile and v tiles in the prefill scratch) and the recurrence
+// kernel's KDA instance.
 //
 // The rule (Kimi Linear's delta rule with a decay per key channel, applied to
 // the key columns of S[v][k]) in chunk form, with alpha_s[c] = e^{g_s[c]},
