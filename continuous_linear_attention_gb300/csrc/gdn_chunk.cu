@@ -738,7 +738,7 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
     CUtensorMap tmx;
     e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
     if (e != cudaSuccess) return e;
-    e = launch_cintra(p, &tmx, max_chunks, false, stream);
+    e = launch_cintra(p, &tmx, max_chunks, false, num_sms, stream);
     if (e == cudaSuccess) e = launch_seq(p, grid, false, stream);
     if (e != cudaSuccess) return e;
   }
@@ -769,7 +769,7 @@ cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t strea
   CUtensorMap tmx;
   cudaError_t e = make_map(&tmx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.T, p.C, XROWS);
   if (e != cudaSuccess) return e;
-  e = launch_cintra(p, &tmx, max_chunks, true, stream);
+  e = launch_cintra(p, &tmx, max_chunks, true, num_sms, stream);
   if (e == cudaSuccess) e = launch_kintra(p, max_chunks, num_sms, stream);
   if (e == cudaSuccess) e = launch_seq(p, grid, true, stream);
   if (e == cudaSuccess) e = cudaGetLastError();

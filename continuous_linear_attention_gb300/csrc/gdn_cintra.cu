@@ -83,6 +83,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 //       fp32, as [box][tap][64 channels] with the 16-byte groups of 4 channels
 //       ordered 0, 2, 4, ..., 14, 1, 3, ..., 15, so that a thread's 8
 //       channels of one tap are two conflict-free 16-byte loads
+//   GIN the next item's gate inputs, staged by cp.async
 constexpr uint32_t OFF_S = 0;
 constexpr uint32_t OFF_AW = OFF_S;
 constexpr uint32_t OFF_AU = OFF_S + 16384;
@@ -93,7 +94,11 @@ constexpr uint32_t OFF_GB = OFF_GH + 512;
 constexpr uint32_t OFF_GBE = OFF_GB + 512;
 constexpr uint32_t WT_TAP = 64 * 4;        // one tap of a box's 64 channels, fp32
 constexpr uint32_t OFF_WT = OFF_GBE + 512;  // taps of each pass, fp32 [2 passes][4 boxes][4 taps][64 ch]
-constexpr uint32_t SMEM_BYTES = OFF_WT + 2 * 4 * KC * WT_TAP + 1024;
+// gate inputs of the next item (cp.async): per token the aligned word of a
+// and of b holding both v-heads' values, then A_log and dt_bias of both
+constexpr uint32_t OFF_GIN = OFF_WT + 2 * 4 * KC * WT_TAP;
+constexpr uint32_t GIN_BYTES = 2 * CH * 4 + 16;
+constexpr uint32_t SMEM_BYTES = OFF_GIN + GIN_BYTES + 1024;
 static_assert(2 * CH * AP * 4 <= 4 * XSUB, "A / T of both heads fit the staging area");
 static_assert(solve::kZFloats * 4 <= BOX, "B blocks of one head fit the q~ rows of a K-block");
 static_assert(OFF_QK % 1024 == 0 && OFF_V % 1024 == 0, "operand tiles on 1024-byte boundaries");
@@ -161,33 +166,54 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* fl
   return *flag != 0;
 }
 
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(g) : "memory");
+}
+// The gate inputs of an item (record rec, k-head kh) into the GIN words, by
+// cp.async on warps 4..7 (thread 0 drives the bulk copies and issues none):
+// per token the aligned 4-byte word of a and of b that holds the values of
+// v-heads 2kh and 2kh + 1 (low and high half; Hv is even), A_log and dt_bias
+// of both heads.
+__device__ __forceinline__ void stage_gates(const FwdParams& p, int4 rec, int kh, int tid,
+                                            uint32_t gin) {
+  const int u = tid - 2 * CH, row0 = rec.x, n = rec.y, Hv = p.Hv;
+  if (u < 0) return;
+  const int i = u & 63;
+  if (i < n) {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(u < CH ? p.a : p.b);
+    cp_async4(gin + 4 * u, src + (size_t)(row0 + i) * Hv + kh * R);
+  }
+  if (u < R) {
+    cp_async4(gin + 2 * CH * 4 + 4 * u, p.A_log + kh * R + u);
+    cp_async4(gin + 2 * CH * 4 + 8 + 4 * u, p.dt_bias + kh * R + u);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Persistent: CTA blockIdx.x takes the items (chunk, k-head) blockIdx.x,
+// + gridDim.x, ... (item = chunk * Hk + k-head; two CTAs per SM).  The next
+// item's record and gate inputs are read during the current one, and its
+// first x boxes load during the current one's last readout.
 template <bool kConvOnly>
 __global__ void __launch_bounds__(kThreads, 2)
 cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t xbar1, xbar2, mbar;
+  __shared__ uint64_t xbar1, xbar2, mbar, rbar;
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
+  __shared__ int s_ni;  // the CTA's next item (a dynamic counter hands them out)
   __shared__ float gtot[R];
+  __shared__ int4 s_nx[2];  // the record of the item of each parity (by bulk copy on rbar)
   pdl_wait_then_release();
   int32_t* hdr = p.work.header();
-  const int n_chunks = hdr[kPreChunks];
-  const int gidx = blockIdx.x;
-  // the chunk's record (scheduler): first packed row, valid tokens, chunk
-  // index inside its sequence, sequence
-  const int4 rec = reinterpret_cast<const int4*>(p.scr_c)[gidx];
-  if (gidx >= n_chunks) return;
-  const int kh = blockIdx.y;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
-  const int row0 = rec.x, n = rec.y, c = rec.z, kpre = rec.w;
-  int rblk = 0;  // the conv state is read on chunk 0 only
-  if (c == 0) {
-    const int s = p.work.pre()[kpre];
-    rblk = p.has_past[s] ? p.blk[s] : 0;
-  }
-  const __nv_bfloat16* tail =
-      reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
+  // items: the scheduler's chunk records (first packed row, valid tokens,
+  // chunk index inside its sequence, sequence) times the k-heads
+  const int n_items = hdr[kPreChunks] * Hk;
+  int item = blockIdx.x;
+  if (item >= n_items) return;
+  const int4* recs = reinterpret_cast<const int4*>(p.scr_c);
   const __nv_bfloat16* wconv = reinterpret_cast<const __nv_bfloat16*>(p.conv_w);
   const int tid = threadIdx.x;
   const uint32_t sbase = smem_u32(sm);
@@ -195,42 +221,74 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   float* GB = reinterpret_cast<float*>(sm + OFF_GB);
   float* GBE = reinterpret_cast<float*>(sm + OFF_GBE);
 
-  // global channel of staged box b of pass ps: q | q | k | k, then v of head
-  // 2kh (two boxes) and of head 2kh+1 (two boxes)
-  auto gch = [&](int ps, int b) {
-    return ps == 0 ? (b < 2 ? kh * D + b * 64 : Hk * D + kh * D + (b - 2) * 64)
-                   : 2 * Hk * D + kh * R * D + b * 64;
+  // global channel of staged box b of pass ps for k-head kh_: q | q | k | k,
+  // then v of head 2kh_ (two boxes) and of head 2kh_+1 (two boxes)
+  auto gch = [&](int kh_, int ps, int b) {
+    return ps == 0 ? (b < 2 ? kh_ * D + b * 64 : Hk * D + kh_ * D + (b - 2) * 64)
+                   : 2 * Hk * D + kh_ * R * D + b * 64;
   };
-  auto issue_x = [&](int ps, uint64_t* bar) {
+  auto issue_x = [&](int row0_, int kh_, int ps, uint64_t* bar) {
     mbar_arrive_expect_tx(bar, 4u * (XBOX_BYTES + WS_BYTES));
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      tma_load_2d(sm + OFF_S + b * XSUB, &tmx, gch(ps, b), row0 - (KC - 1), bar);
-      bulk_g2s(sm + OFF_S + b * XSUB + WS_OFF, wconv + (size_t)gch(ps, b) * KC, WS_BYTES, bar);
+      tma_load_2d(sm + OFF_S + b * XSUB, &tmx, gch(kh_, ps, b), row0_ - (KC - 1), bar);
+      bulk_g2s(sm + OFF_S + b * XSUB + WS_OFF, wconv + (size_t)gch(kh_, ps, b) * KC, WS_BYTES, bar);
     }
   };
+  int4 rec = recs[item / Hk];
+  // (thread 0) 1 + parity of an x-box or record phase in flight, or 0
+  int xpend1 = 0, xpend2 = 0, rpend = 0;
   if (tid == 0) {
     mbar_init(&xbar1, 1);
     mbar_init(&xbar2, 1);
     mbar_init(&mbar, 1);
+    mbar_init(&rbar, 1);
     fence_mbar_init();
-    issue_x(0, &xbar1);
+    s_ni = (int)gridDim.x + atomicAdd(&hdr[kItemHeadC], 1);
+    issue_x(rec.x, item % Hk, 0, &xbar1);
+    xpend1 = 1;
   }
   if (tid < 32) tc::tmem_alloc(&tmem_slot, TM_COLS);
+  if (!kConvOnly) {
+    stage_gates(p, rec, item % Hk, tid, sbase + OFF_GIN);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+  __syncthreads();
+  bool ok = true;
+  uint32_t par = 0;  // parity of this item's x-box barriers and first product barrier
+
+  for (;;) {
+  const int gidx = item / Hk, kh = item % Hk;
+  const int row0 = rec.x, n = rec.y, c = rec.z, kpre = rec.w;
+  const int next = s_ni;
+  int nn = 0;  // (thread 0) counter value of the item after next
+  if (tid == 0 && next < n_items) nn = atomicAdd(&hdr[kItemHeadC], 1);
+  if (tid == 0 && next < n_items) {
+    mbar_arrive_expect_tx(&rbar, 16);
+    bulk_g2s(&s_nx[par ^ 1u], recs + next / Hk, 16, &rbar);
+    rpend = 1 + (int)par;
+  }
+  int rblk = 0;  // the conv state is read on chunk 0 only
+  if (c == 0) {
+    const int s = p.work.pre()[kpre];
+    rblk = p.has_past[s] ? p.blk[s] : 0;
+  }
+  const __nv_bfloat16* tail =
+      reinterpret_cast<const __nv_bfloat16*>(p.layer_base + (size_t)rblk * p.stride);
 
   // ---- gates of the chunk's tokens for both v-heads (threads 0..127, token
-  // tid % 64 of head 2kh + tid / 64): g, beta and the inclusive cumulative sum
-  // G of g inside the chunk; tokens past the end take g = 0 and beta = 0
+  // tid % 64 of head 2kh + tid / 64, from the staged inputs): g, beta and the
+  // inclusive cumulative sum G of g inside the chunk; tokens past the end
+  // take g = 0 and beta = 0
   float gcum = 0.f, gbeta = 0.f;
   if (!kConvOnly && tid < R * CH) {
-    const int h = kh * R + (tid >> 6), i = tid & 63;
+    const int hl = tid >> 6, i = tid & 63;
     if (i < n) {
-      const size_t row = (size_t)(row0 + i);
-      const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(p.a);
-      const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(p.b);
-      gcum = -__expf(p.A_log[h]) *
-             softplus_f32(__bfloat162float(av[row * Hv + h]) + p.dt_bias[h]);
-      gbeta = sigmoid_f32(__bfloat162float(bv[row * Hv + h]));
+      const uint32_t* gw = reinterpret_cast<const uint32_t*>(sm + OFF_GIN);
+      const float* gs = reinterpret_cast<const float*>(sm + OFF_GIN + 2 * CH * 4);
+      const uint32_t aw = gw[i] >> (16 * hl), bw = gw[CH + i] >> (16 * hl);
+      gcum = -__expf(gs[hl]) * softplus_f32(__uint_as_float(aw << 16) + gs[2 + hl]);
+      gbeta = sigmoid_f32(__uint_as_float(bw << 16));
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -239,6 +297,9 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     }
     if ((tid & 63) == 31) gtot[tid >> 6] = gcum;
   }
+  // (kConvOnly) the previous item's [q~ ; k~] store has read its source
+  // before the conv writes it again
+  if (kConvOnly && tid == 0) bulk_wait_read_but_last();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -367,7 +428,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       for (int t = tid; t < (KC - 1) * 4 * 8; t += kThreads) {
         const int r = t >> 5, b = (t >> 3) & 3, cc = (t & 7) * 8;
         *reinterpret_cast<uint4*>(sm + OFF_S + b * XSUB + tc::sw128_offset(r, cc)) =
-            *reinterpret_cast<const uint4*>(tail + (size_t)r * C + gch(ps, b) + cc);
+            *reinterpret_cast<const uint4*>(tail + (size_t)r * C + gch(kh, ps, b) + cc);
       }
     }
     {
@@ -389,7 +450,8 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     __syncthreads();
   };
 
-  bool ok = cta_wait(&xbar1, 0, &flag);
+  ok = cta_wait(&xbar1, par, &flag);
+  if (ok && tid == 0) xpend1 = 0;
   if (ok) {
     pass_setup(0);
     {
@@ -401,7 +463,10 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       // visible to the async proxy: the v boxes come in while k is finished
       tc::fence_proxy_async_smem();
       __syncthreads();
-      if (tid == 0) issue_x(1, &xbar2);
+      if (tid == 0) {
+        issue_x(row0, kh, 1, &xbar2);
+        xpend2 = 1 + (int)par;
+      }
       conv_finish(1, in);
     }
     // the [q~ ; k~] operand tile is complete: X product
@@ -420,9 +485,13 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
                sm + OFF_QK, 2 * KB_STRIDE);
       bulk_commit();
     }
-    ok = cta_wait(&xbar2, 0, &flag);
+    ok = cta_wait(&xbar2, par, &flag);
+    if (ok && tid == 0) xpend2 = 0;
   }
   if (ok) {
+    // the previous item's last tile store (its u_1 or v tiles) has read the
+    // v area before the conv writes it
+    if (tid == 0) bulk_wait_read_but_last();
     pass_setup(1);
     {
       ConvIn in;
@@ -434,16 +503,35 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     tc::fence_proxy_async_smem();  // the v tiles, read by the u products (or stored)
     if constexpr (kConvOnly) {
       // the conv-only pass ends here: the two v-heads' v tiles to the scratch
-      __syncthreads();
-      if (tid == 0) {
+      // (and the next item's record has landed)
+      if (next < n_items) {
+        ok = cta_wait(&rbar, par, &flag);
+        if (ok && tid == 0) rpend = 0;
+      } else {
+        __syncthreads();
+      }
+      if (ok && tid == 0) {
         bulk_s2g(static_cast<unsigned char*>(p.scr_v) + ((size_t)gidx * Hv + kh * R) * (2 * BOX),
                  sm + OFF_V, 4 * BOX);
         bulk_commit();
+        // every read of the staged v boxes is done: the next item's q | k boxes
+        if (next < n_items) {
+          issue_x(s_nx[par ^ 1u].x, next % Hk, 0, &xbar1);
+          xpend1 = 1 + (int)(par ^ 1u);
+        }
       }
     } else {
       // the q~ rows take the P tiles next: the [q~ ; k~] store has read them
       if (tid == 0) bulk_wait_read_all();
-      ok = cta_wait(&mbar, 0, &flag);  // X done; every read of the staging area done
+      ok = cta_wait(&mbar, par, &flag);  // X done; every read of the staging area done
+      // the next item's record has landed (its bulk copy on rbar, issued at
+      // this item's start): stage its gate inputs (this item's were read
+      // before the first barrier)
+      if (ok && next < n_items) {
+        ok = cta_wait(&rbar, par, &flag);
+        if (ok && tid == 0) rpend = 0;
+        if (ok) stage_gates(p, s_nx[par ^ 1u], next % Hk, tid, sbase + OFF_GIN);
+      }
     }
   }
   if constexpr (!kConvOnly) {
@@ -617,7 +705,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
                  tc::idesc_f16_f32(128, 128, false, true), false);
       tc::commit(&mbar);
     }
-    ok = cta_wait(&mbar, 1, &flag);
+    ok = cta_wait(&mbar, par ^ 1u, &flag);
   }
   // read out 64 columns (col0 .. col0 + 63) of this thread's TMEM row (token
   // r128 % 64) into row r128 % 64 of box hf of a staged 2-box tile (boxes of
@@ -664,7 +752,14 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       bulk_s2g(Ug + tile0, sm + OFF_AW, 2 * BOX);
       bulk_commit();
     }
-    ok = cta_wait(&mbar, 0, &flag);
+    ok = cta_wait(&mbar, par, &flag);
+    // the products are done and the -w / u_0 stores have read the staging
+    // area: the next item's q | k boxes load during this readout
+    if (ok && tid == 0 && next < n_items) {
+      bulk_wait_read_all();
+      issue_x(s_nx[par ^ 1u].x, next % Hk, 0, &xbar1);
+      xpend1 = 1 + (int)(par ^ 1u);
+    }
     if (ok) {
       // u_1 (lanes 64..127) into the v_0 tile (free: the u_0 product is done)
       tc::fence_after_sync();
@@ -678,17 +773,33 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     }
   }
   }  // !kConvOnly
-  if (!ok && tid == 0) atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+  if (!ok) break;
   // v, w, u and the operand tiles enter tensor-core operands in fp16: a value
   // out of its range sends both v-heads of this sequence to the token-serial
-  // redo
+  // redo.  (The next item's staged gate inputs are visible after this barrier.)
+  tc::fence_before_sync();
+  if (!kConvOnly) asm volatile("cp.async.wait_all;" ::: "memory");
+  if (tid == 0 && next < n_items) s_ni = (int)gridDim.x + nn;  // read after the barrier
   if (__syncthreads_or(!(amax <= kF16Max) || !(vmax <= kF16Max)) && tid == 0) {
     mark_redo(p.work, kpre, kh * R);
     mark_redo(p.work, kpre, kh * R + 1);
   }
+  if (next >= n_items) break;
+  item = next;
+  rec = s_nx[par ^ 1u];
+  par ^= 1u;
+  }  // items
+
+  if (!ok && tid == 0) {
+    atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+    // copies still in flight land before the CTA ends (bounded waits)
+    if (xpend1) (void)mbar_wait_bounded(&xbar1, (uint32_t)(xpend1 - 1));
+    if (xpend2) (void)mbar_wait_bounded(&xbar2, (uint32_t)(xpend2 - 1));
+    if (rpend) (void)mbar_wait_bounded(&rbar, (uint32_t)(rpend - 1));
+  }
   tc::fence_before_sync();
   __syncthreads();
-  if (tid < 32) tc::tmem_dealloc(tmem, TM_COLS);
+  if (tid < 32) tc::tmem_dealloc(tmem_slot, TM_COLS);
   // the shared-memory sources of the tile stores are read before the CTA ends;
   // the stores themselves complete with the grid (the recurrence kernel, launched
   // after it, waits for that)
@@ -698,13 +809,16 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
 }  // namespace
 
 cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks, bool conv_only,
-                          cudaStream_t stream) {
+                          int num_sms, cudaStream_t stream) {
   if (max_chunks <= 0) return cudaSuccess;
   auto kern = conv_only ? cintra_kernel<true> : cintra_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(max_chunks, p.Hk), dim3(kThreads), SMEM_BYTES, stream, p,
+  // a persistent grid of two CTAs per SM
+  const long long items = (long long)max_chunks * p.Hk;
+  const int grid = (int)(items < 2LL * num_sms ? items : 2LL * num_sms);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, p,
                     *static_cast<const CUtensorMap*>(x_map));
 }
 

@@ -34,6 +34,8 @@ enum Cnt : int {
   kPreTokens = 4,  // total tokens of the length>1 sequences
   kWorkHead = 5,   // dynamic work counter of persistent kernels (reset by the scheduler)
   kPreChunks = 6,  // total 64-token chunks of the length>1 sequences
+  kItemHeadC = 7,  // item counters of the persistent chunk-parallel kernels
+  kItemHeadK = 8,  // (cintra_kernel, kintra_kernel; reset by the scheduler)
   kHeaderWords = 16,
 };
 
@@ -162,15 +164,15 @@ cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
 // update that follows it: d_k = d_v = 128, bf16 activations, K = 4.
 bool chunk_supported(int d, int act, int K);
 cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
-// Conv, gates and the state-independent products of every prefill chunk, one
-// CTA per (64-token chunk, k-head), writing the scratch the recurrence kernel
-// reads (max_chunks: host bound on the number of 64-token chunks of the
-// prefill sequences).  x_map: the CUtensorMap of x (boxes of 64 channels x 67
-// rows, 128-byte swizzle).
+// Conv, gates and the state-independent products of every prefill (64-token
+// chunk, k-head), on a persistent grid of up to 2 num_sms CTAs, writing the
+// scratch the recurrence kernel reads (max_chunks: host bound on the number
+// of 64-token chunks of the prefill sequences).  x_map: the CUtensorMap of x
+// (boxes of 64 channels x 67 rows, 128-byte swizzle).
 // With conv_only, only the conv: the [q~ ; k~] tiles to scr_qk and the v
 // tiles to scr_v (the per-channel-decay rule's first pass).
 cudaError_t launch_cintra(const FwdParams& p, const void* x_map, int max_chunks, bool conv_only,
-                          cudaStream_t stream);
+                          int num_sms, cudaStream_t stream);
 // The state recurrence over the prefill chains, reading the chunk-major tiles
 // cintra_kernel (kda: kintra_kernel) leaves in the prefill scratch.
 cudaError_t launch_seq(const FwdParams& p, int grid, bool kda, cudaStream_t stream);

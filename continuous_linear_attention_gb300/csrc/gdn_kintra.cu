@@ -234,10 +234,11 @@ __device__ __forceinline__ void stage_gates(const FwdParams& p, int4 rec, int h,
 __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t ldbar, mbar;
+  __shared__ uint64_t ldbar, mbar, rbar;
   __shared__ uint32_t tmem_slot;
   __shared__ int flag;
-  __shared__ int4 s_next;
+  __shared__ int s_ni;  // the CTA's next item (a dynamic counter hands them out)
+  __shared__ int4 s_next;  // the next item's record (by bulk copy on rbar)
   pdl_wait_then_release();
   int32_t* hdr = p.work.header();
   const int Hk = p.Hk, Hv = p.Hv;
@@ -272,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   if (tid == 0) {
     mbar_init(&ldbar, 1);
     mbar_init(&mbar, 1);
+    mbar_init(&rbar, 1);
     fence_mbar_init();
+    s_ni = (int)gridDim.x + atomicAdd(&hdr[kItemHeadK], 1);
     issue_qk(item);
     issue_v(item);
   }
@@ -284,12 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   bool ok = true;
   uint32_t it_par = 0;   // parity of this item's load and product barriers
   int pending = 1;       // 1 + parity of a load phase in flight (thread 0's view), or 0
+  int rpend = 0;         // the same for the record barrier
 
   for (;;) {
   const int gidx = item / Hv, h = item % Hv, kh = h / R, hl = h % R;
   const int n = rec.y, kpre = rec.w;
-  const int next = item + (int)gridDim.x;
-  if (tid == 0 && next < n_items) s_next = recs[next / Hv];
+  const int next = s_ni;
+  int nn = 0;  // (thread 0) counter value of the item after next
+  if (tid == 0 && next < n_items) nn = atomicAdd(&hdr[kItemHeadK], 1);
+  if (tid == 0 && next < n_items) {
+    mbar_arrive_expect_tx(&rbar, 16);
+    bulk_g2s(&s_next, recs + next / Hv, 16, &rbar);
+    rpend = 1 + (int)it_par;
+  }
+  bool rok = true;
 
   // ---- gates: alpha_i[c] = e^{-e^{A_log} softplus(a_i[c] + dt_bias[c])}
   // (thread: channel pair 2 (tid % 64), tokens of the 8-token block tid / 64;
@@ -556,8 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     // inputs (the mid-block rows are read), in flight during the rest of this
     // item
     if (next < n_items) {
-      rec = s_next;
-      stage_gates(p, rec, next % Hv, tid, sbase);
+      rok = cta_wait(&rbar, it_par, &flag);
+      if (rok && tid == 0) rpend = 0;
+      if (rok) {
+        rec = s_next;
+        stage_gates(p, rec, next % Hv, tid, sbase);
+      }
     }
     // ---- T = (I + A)^{-1} on warps 0..3 (diagonal blocks by threads 0..63,
     // then the off-diagonal blocks; named barrier 1 over those 128 threads),
@@ -659,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
                  CH / 16, tc::idesc_f16_f32(128, 128, false, true), false);
       tc::commit(&mbar);
     }
-    ok = cta_wait(&mbar, it_par, &flag);
+    ok = cta_wait(&mbar, it_par, &flag) && rok;
     // the products have read v, and the [q^ ; k^] store its space: the next
     // item's tiles
     if (ok && tid == 0 && next < n_items) {
@@ -704,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   // a value out of its range sends this chain to the token-serial redo
   tc::fence_before_sync();
   if (tid >= 2 * CH) cp_async_wait_all();  // the next item's gate inputs, visible after the barrier
+  if (tid == 0 && next < n_items) s_ni = (int)gridDim.x + nn;  // read after the barrier
   if (__syncthreads_or(!(amax <= kF16Max)) && tid == 0) mark_redo(p.work, kpre, h);
   if (next >= n_items) break;
   item = next;
@@ -715,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     // tiles still in flight for an item this CTA will not take land before
     // it ends (a bounded wait)
     if (pending) (void)mbar_wait_bounded(&ldbar, (uint32_t)(pending - 1));
+    if (rpend) (void)mbar_wait_bounded(&rbar, (uint32_t)(rpend - 1));
   }
   tc::fence_before_sync();
   __syncthreads();

@@ -11,7 +11,7 @@
 //   ones sorted longest first (ties by sequence id), their counts and the
 //   total prefill tokens, the 64-token chunk prefix over the sorted prefill
 //   list and (with prefill scratch) one record per chunk, and resets the
-//   persistent-kernel work counter.
+//   persistent kernels' work and item counters.
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -48,7 +48,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     if (tid == 0) {
       atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_SEQLENS);
       hdr[kNItems] = hdr[kNDec] = hdr[kNPre] = hdr[kPreTokens] = hdr[kPreChunks] = 0;
-      hdr[kWorkHead] = 0;
+      hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = 0;
     }
     return;
   }
@@ -145,7 +145,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     hdr[kNDec] = s_n_dec;
     hdr[kNPre] = n_pre;
     hdr[kPreTokens] = s_pre_tokens;
-    hdr[kWorkHead] = 0;
+    hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = 0;
   }
 }
 
