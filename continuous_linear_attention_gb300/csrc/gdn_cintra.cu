@@ -628,18 +628,14 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
     // the q~ rows take the B blocks next: the P stores have read them
     if (tid == 0) bulk_wait_read_all();
     __syncthreads();
-    // ---- off-diagonal blocks of both heads: B_ij = T_ii A_ij for i > j (the
-    // six B blocks of a head on its four warps), the first level
-    // T_{i,i-1} = -B_{i,i-1} T_{i-1,i-1} right away by the warp that made
-    // B_{i,i-1}; then T_20, T_31 and T_30 (= -sum B_3k T_k0)
+    // ---- off-diagonal blocks of both heads, a head's six product chains on
+    // its four warps (the block barriers are the CTA's)
     {
       const int warp = tid >> 5;
       const int hl = warp >> 2, wl = warp & 3;
       float* ATh = AT + hl * CH * AP;
       float* Z = reinterpret_cast<float*>(sm + OFF_QK + hl * KB_STRIDE);
-      solve::offdiag_first(ATh, Z, wl);
-      __syncthreads();
-      solve::offdiag_rest(ATh, Z, wl);
+      solve::offdiag_chains<4>(ATh, Z, wl, [] { __syncthreads(); });
     }
     __syncthreads();
     // ---- the MMAs' A tiles over the A / T array once every T value is read:

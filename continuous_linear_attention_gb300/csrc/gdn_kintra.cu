@@ -170,8 +170,8 @@ __device__ __forceinline__ void ld_h4p(const unsigned char* p, unsigned long lon
   v[1] = f2p(b.x, b.y);
 }
 
-// named barrier 1 over warps 0..3 (the solve)
-__device__ __forceinline__ void solve_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barrier 1 over warps 0..5 (the solve)
+__device__ __forceinline__ void solve_bar() { asm volatile("bar.sync 1, 192;" ::: "memory"); }
 
 // softplus(x) = max(x, 0) + ln(1 + e^{-|x|}) with the fast exponential and
 // logarithm: an absolute error of a few 1e-7 (the fast logarithm near 1, the
@@ -574,14 +574,15 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
         stage_gates(p, rec, next % Hv, tid, sbase);
       }
     }
-    // ---- T = (I + A)^{-1} on warps 0..3 (diagonal blocks by threads 0..63,
-    // then the off-diagonal blocks; named barrier 1 over those 128 threads),
-    // while warps 4..15 turn the [q~ ; k~] tile into [q^ ; k^] in place (every
-    // product has read it), one 8-token block of q or k per 64 threads and
-    // task (16 tasks over 6 groups): q^_i = q~_i e^{Gamma_i} forward through
-    // the block from E8_0 .. E8_{b-1}, k^_j = k~_j e^{Gamma_C - Gamma_j}
-    // backward through it from E8_{b+1} .. E8_7
-    if (warp < 4) {
+    // ---- T = (I + A)^{-1} on warps 0..5 (diagonal blocks by threads 0..63,
+    // then the off-diagonal blocks in four product steps, one chain per warp;
+    // named barrier 1 over those 192 threads), while warps 6..15 turn the
+    // [q~ ; k~] tile into [q^ ; k^] in place (every product has read it), one
+    // 8-token block of q or k per 64 threads and task (16 tasks over 5
+    // groups; a task's loads all issue before its stores): q^_i = q~_i
+    // e^{Gamma_i} forward through the block from E8_0 .. E8_{b-1}, k^_j = k~_j
+    // e^{Gamma_C - Gamma_j} backward through it from E8_{b+1} .. E8_7
+    if (warp < 6) {
       float col[16];
       const int b = (tid >> 4) & 3, m = tid & 15;
       float* Ab = AT + (16 * b) * AP + 16 * b;
@@ -590,13 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       if (tid < CH) solve::diag_col_store(Ab, m, col);
       solve_bar();
       float* Z = reinterpret_cast<float*>(sm + OFF_Z);
-      solve::offdiag_first(AT, Z, warp);
-      solve_bar();
-      solve::offdiag_rest(AT, Z, warp);
+      solve::offdiag_chains<6>(AT, Z, warp, solve_bar);
     } else {
       unsigned char* QKw = sm + OFF_QK;
 #pragma unroll 1
-      for (int task = (tid - 128) >> 6; task < 16; task += 6) {
+      for (int task = (tid - 192) >> 6; task < 16; task += 5) {
         const int b = task & 7;
         const bool is_q = task < 8;
         float2 f = make_float2(1.f, 1.f);
@@ -607,27 +606,28 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
             f.x *= e.x;
             f.y *= e.y;
           }
+        float2 al[8], v[8];
+        uint32_t o[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int i = 8 * b + t;
+          al[t] = AL2[i * 64];
+          o[t] = qk_off(is_q ? i : CH + i, c);
+          v[t] = ld_h2(QKw + o[t]);
+        }
         if (is_q) {
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
-            const int i = 8 * b + t;
-            const float2 a = AL2[i * 64];
-            f.x *= a.x;
-            f.y *= a.y;
-            const uint32_t o = qk_off(i, c);
-            const float2 q = ld_h2(QKw + o);
-            st_h2(QKw + o, q.x * f.x, q.y * f.y);
+            f.x *= al[t].x;
+            f.y *= al[t].y;
+            st_h2(QKw + o[t], v[t].x * f.x, v[t].y * f.y);
           }
         } else {
 #pragma unroll
           for (int t = 7; t >= 0; --t) {
-            const int j = 8 * b + t;
-            const uint32_t o = qk_off(CH + j, c);
-            const float2 k = ld_h2(QKw + o);
-            st_h2(QKw + o, k.x * f.x, k.y * f.y);
-            const float2 a = AL2[j * 64];
-            f.x *= a.x;
-            f.y *= a.y;
+            st_h2(QKw + o[t], v[t].x * f.x, v[t].y * f.y);
+            f.x *= al[t].x;
+            f.y *= al[t].y;
           }
         }
       }

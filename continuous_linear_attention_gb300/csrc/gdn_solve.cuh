@@ -4,9 +4,9 @@
 // (decayed k_i . k_j), j < i), overwritten by T in place, in 16 x 16 blocks:
 //   diagonal blocks T_ii = (I + A_ii)^{-1} by column substitution, one thread
 //   per column (64 threads per matrix);
-//   B_ij = T_ii A_ij for the six blocks below the diagonal, and the first
-//   level T_{i,i-1} = -B_{i,i-1} T_{i-1,i-1} right away (four warps);
-//   then T_20, T_31 and T_30 = -sum_k B_3k T_k0 (two warps, then one).
+//   the six blocks below the diagonal as six chains of block products that
+//   start from B_ij = T_ii A_ij, in four dependent product steps with two
+//   barriers (offdiag_chains).
 // The block products run on the warp-level tensor-core path (mma.sync
 // m16n8k8, tf32 inputs, fp32 accumulation) with every fp32 operand split into
 // a tf32 head (rounded to nearest) and a tail (the exact remainder, which the
@@ -98,18 +98,6 @@ __device__ __forceinline__ void blk_store(float* dp, int pd, int n0, const float
   *reinterpret_cast<float2*>(dp + (g + 8) * pd + n0 + 2 * t) =
       make_float2(s * acc[2], s * acc[3]);
 }
-// Off-diagonal block (i, j) of T from the B blocks (B_ik = T_ii A_ik at
-// Z + (i(i-1)/2 + k) ZB) and the blocks of T below the diagonal already done:
-// T_ij = -sum_{k=j}^{i-1} B_ik T_kj, stored over A_ij.  One warp.
-__device__ __forceinline__ void level_block(float* AT, const float* Z, int i, int j) {
-  float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int k = j; k < i; ++k)
-    blk_mma3_pair(acc0, acc1, Z + (i * (i - 1) / 2 + k) * ZB, ZP, AT + (16 * k) * AP + 16 * j, AP);
-  blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
-  blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
-}
-
-
 // Column m of the inverse of the unit lower-triangular diagonal block at Ab
 // (pitch AP; only the entries below its diagonal are read).
 __device__ __forceinline__ void diag_col(const float* Ab, int m, float (&col)[16]) {
@@ -131,34 +119,63 @@ __device__ __forceinline__ void diag_col_store(float* Ab, int m, const float (&c
 #pragma unroll
   for (int r = 0; r < 16; ++r) Ab[r * AP + m] = col[r];
 }
-// The six B blocks and the first level, by warp wl (0..3) of the four warps
-// of one matrix (A at AT with its diagonal blocks already inverted; Z holds
-// kZFloats floats).
-__device__ __forceinline__ void offdiag_first(float* AT, float* Z, int wl) {
+// The off-diagonal blocks in four dependent product steps instead of eight:
+// six chains c = (i, j), (1,0) (2,1) (3,2) (2,0) (3,1) (3,0), each first
+// B_ij = T_ii A_ij (kept in Z block c for the other chains), then for the
+// first three T_ij = -B_ij T_jj and for the others the partial sum
+// P_ij = B_ij T_jj in registers; after a barrier T_20 = -(P_20 + B_21 T_10),
+// T_31 = -(P_31 + B_32 T_21) and P_30 += B_31 T_10; after another
+// T_30 = -(P_30 + B_32 T_20).  Chain c runs on warp c % NW of the NW warps
+// (wl = this warp's index among them) and bar() is their barrier; A's
+// diagonal blocks must already be inverted.
+template <int NW, typename Bar>
+__device__ __forceinline__ void offdiag_chains(float* AT, float* Z, int wl, Bar bar) {
+  auto blk = [&](int i, int j) { return AT + (16 * i) * AP + 16 * j; };
+  float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's P (chains 3..5)
 #pragma unroll 1
-  for (int bi = wl; bi < 6; bi += 4) {
-    const int i = bi < 1 ? 1 : (bi < 3 ? 2 : 3);
-    const int j = bi - i * (i - 1) / 2;
-    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    blk_mma3_pair(acc0, acc1, AT + (16 * i) * AP + 16 * i, AP, AT + (16 * i) * AP + 16 * j, AP);
-    blk_store(Z + bi * ZB, ZP, 0, acc0, 1.f);
-    blk_store(Z + bi * ZB, ZP, 8, acc1, 1.f);
-    if (j == i - 1) {
-      __syncwarp();
+  for (int c = wl; c < 6; c += NW) {
+    const int i = c == 0 ? 1 : (c == 1 || c == 3 ? 2 : 3);
+    const int j = c == 0 || c == 3 || c == 5 ? 0 : (c == 1 || c == 4 ? 1 : 2);
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    blk_mma3_pair(a0, a1, blk(i, i), AP, blk(i, j), AP);  // B_ij
+    blk_store(Z + c * ZB, ZP, 0, a0, 1.f);
+    blk_store(Z + c * ZB, ZP, 8, a1, 1.f);
+    __syncwarp();
+    float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+    blk_mma3_pair(b0, b1, Z + c * ZB, ZP, blk(j, j), AP);  // B_ij T_jj
+    if (c < 3) {
+      blk_store(blk(i, j), AP, 0, b0, -1.f);
+      blk_store(blk(i, j), AP, 8, b1, -1.f);
+    } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
-      blk_mma3_pair(acc0, acc1, Z + bi * ZB, ZP, AT + (16 * j) * AP + 16 * j, AP);
-      blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, acc0, -1.f);
-      blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, acc1, -1.f);
+      for (int e = 0; e < 4; ++e) {
+        p0[e] = b0[e];
+        p1[e] = b1[e];
+      }
     }
   }
-}
-// The remaining levels (after a barrier over the four warps' first level).
-__device__ __forceinline__ void offdiag_rest(float* AT, const float* Z, int wl) {
-  if (wl < 2) level_block(AT, Z, wl + 2, wl);
-  if (wl == 0) {
-    __syncwarp();
-    level_block(AT, Z, 3, 0);
+  bar();
+  // chains 3, 4, 5: one more product each (Z blocks: 1 = B_21, 2 = B_32, 4 = B_31)
+#pragma unroll 1
+  for (int c = wl; c < 6; c += NW) {
+    if (c < 3) continue;
+    if (c == 3) {
+      blk_mma3_pair(p0, p1, Z + 1 * ZB, ZP, blk(1, 0), AP);
+      blk_store(blk(2, 0), AP, 0, p0, -1.f);
+      blk_store(blk(2, 0), AP, 8, p1, -1.f);
+    } else if (c == 4) {
+      blk_mma3_pair(p0, p1, Z + 2 * ZB, ZP, blk(2, 1), AP);
+      blk_store(blk(3, 1), AP, 0, p0, -1.f);
+      blk_store(blk(3, 1), AP, 8, p1, -1.f);
+    } else {
+      blk_mma3_pair(p0, p1, Z + 4 * ZB, ZP, blk(1, 0), AP);
+    }
+  }
+  bar();
+  if (5 % NW == wl) {
+    blk_mma3_pair(p0, p1, Z + 2 * ZB, ZP, blk(2, 0), AP);
+    blk_store(blk(3, 0), AP, 0, p0, -1.f);
+    blk_store(blk(3, 0), AP, 8, p1, -1.f);
   }
 }
 
