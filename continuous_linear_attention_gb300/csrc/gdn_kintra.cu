@@ -31,8 +31,9 @@
 //   blocks by running products per pair column j (fp32, CUDA cores).
 // Then the shared blocked solve for T, T diag(beta) as an fp16 operand, and u
 // and -w on tcgen05 (fp32 in tensor memory).  Every tile leaves in the layout
-// the recurrence kernel loads, by bulk copy: [q^ ; k^] (per v-head), P, u, -w,
-// and e^{Gamma_C} into the k-head's gate tile.  A value of T diag(beta), u or
+// the recurrence kernel loads: [q^ ; k^] (per v-head) by plain stores as its
+// rows are formed, P, u and -w by bulk copy, and e^{Gamma_C} into the
+// k-head's gate tile.  A value of T diag(beta), u or
 // w outside the fp16 range sends the (sequence, v-head) chain to the
 // token-serial redo.
 #include <cuda.h>
@@ -58,8 +59,8 @@ constexpr int LRP = 136;  // pitch (halves) of the L / R rows: conflict-free ldm
 constexpr float kF16Max = 65000.f;
 
 // Shared memory (offsets from a 1024-byte aligned base):
-//   QK  [q~ ; k~] of the k-head (loaded); turned into [q^ ; k^] in place
-//       once the products have read it, and stored
+//   QK  [q~ ; k~] of the k-head (loaded; the next item's lands here once the
+//       A / P blocks have read it)
 //   V   v of the v-head: 2 boxes of 64 channels x 64 tokens (loaded)
 //   LM  the mid-block operands of the four 16-token blocks I: 24 rows each,
 //       L'_I (8 q rows, 8 k rows) and R'_I (8 k rows), fp16 [96][LRP]
@@ -362,17 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     //   L'_J (b odd, from token 16 J + 8): b8[t];   R'_J (b even, to token
     //     16 J + 7): s8[t];
     //   R_I (I = J + 1 .. 3, to token 16 I - 1): s8[t] E8_{b+1} .. E8_{2I-1};
-    //   -k~ e^{Gamma} (from the chunk start): b8[t] E8_0 .. E8_{b-1};
+    //   -k~ e^{Gamma} and q^ (from the chunk start): b8[t] E8_0 .. E8_{b-1};
+    //   k^ (to the chunk end): s8[t] E8_{b+1} .. E8_7;
     //   e^{Gamma_C}: E8_0 .. E8_7.
+    // [q^ ; k^] goes straight to its scratch tile (the [q ; k] tile's layout)
+    // by plain stores, so that the [q~ ; k~] space is free once the A / P
+    // blocks have read it.
     const int gr = tid >> 6, c = 2 * (tid & 63), J = gr >> 1;
     const unsigned char* QK = sm + OFF_QK;
+    unsigned char* qh = static_cast<unsigned char*>(p.scr_qh) + ((size_t)gidx * Hv + h) * (2 * KB_STRIDE);
     const float2* E8 = reinterpret_cast<const float2*>(sm + OFF_E8) + (c >> 1);  // block b at E8[64 b]
-    const float2* AL2 = reinterpret_cast<const float2*>(AL) + (c >> 1);  // row i at AL2[i * 64]
     float2 pb = make_float2(1.f, 1.f);   // E8_0 .. E8_{b-1}
     float2 fl = make_float2(1.f, 1.f);   // E8_{b-1} in a second half, else 1
     float2 mr[4];                        // mr[I] = E8_{b+1} .. E8_{2I-1}
+    float2 m = make_float2(1.f, 1.f);    // at the end E8_{b+1} .. E8_7
     {
-      float2 m = make_float2(1.f, 1.f);
 #pragma unroll
       for (int bb = 0; bb < 8; ++bb) {
         const float2 e = E8[64 * bb];
@@ -412,7 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
           st_h2(sm + OFF_LR + (size_t)(kLRows + 8 * I * (I - 1) + i) * (LRP * 2) + c * 2, k.x * fx,
                 k.y * fy);
         }
-      st_h2(sm + OFF_NK + box_off(i, c), -k.x * (b8[t].x * pb.x), -k.y * (b8[t].y * pb.y));
+      const float fqx = b8[t].x * pb.x, fqy = b8[t].y * pb.y;
+      st_h2(sm + OFF_NK + box_off(i, c), -k.x * fqx, -k.y * fqy);
+      st_h2(qh + qk_off(i, c), q.x * fqx, q.y * fqy);
+      st_h2(qh + qk_off(CH + i, c), k.x * (s8[t].x * m.x), k.y * (s8[t].y * m.y));
     }
     tc::fence_proxy_async_smem();  // -k~ e^{Gamma} (MMA operand)
     __syncthreads();
@@ -562,6 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     if (tid == 0) {
       bulk_s2g(static_cast<unsigned char*>(p.scr_p) + ((size_t)gidx * Hv + h) * BOX, sm + OFF_PT, BOX);
       bulk_commit();
+      // nothing reads the [q~ ; k~] tile any more: the next item's
+      if (next < n_items) {
+        issue_qk(next);
+        pending = 1 + (int)(it_par ^ 1u);
+      }
     }
     // the next item's record (thread 0 read it at this item's start) and gate
     // inputs (the mid-block rows are read), in flight during the rest of this
@@ -576,12 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     }
     // ---- T = (I + A)^{-1} on warps 0..5 (diagonal blocks by threads 0..63,
     // then the off-diagonal blocks in four product steps, one chain per warp;
-    // named barrier 1 over those 192 threads), while warps 6..15 turn the
-    // [q~ ; k~] tile into [q^ ; k^] in place (every product has read it), one
-    // 8-token block of q or k per 64 threads and task (16 tasks over 5
-    // groups; a task's loads all issue before its stores): q^_i = q~_i
-    // e^{Gamma_i} forward through the block from E8_0 .. E8_{b-1}, k^_j = k~_j
-    // e^{Gamma_C - Gamma_j} backward through it from E8_{b+1} .. E8_7
+    // named barrier 1 over those 192 threads)
     if (warp < 6) {
       float col[16];
       const int b = (tid >> 4) & 3, m = tid & 15;
@@ -592,53 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       solve_bar();
       float* Z = reinterpret_cast<float*>(sm + OFF_Z);
       solve::offdiag_chains<6>(AT, Z, warp, solve_bar);
-    } else {
-      unsigned char* QKw = sm + OFF_QK;
-#pragma unroll 1
-      for (int task = (tid - 192) >> 6; task < 16; task += 5) {
-        const int b = task & 7;
-        const bool is_q = task < 8;
-        float2 f = make_float2(1.f, 1.f);
-#pragma unroll
-        for (int bb = 0; bb < 8; ++bb)
-          if (is_q ? bb < b : bb > b) {
-            const float2 e = E8[64 * bb];
-            f.x *= e.x;
-            f.y *= e.y;
-          }
-        float2 al[8], v[8];
-        uint32_t o[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int i = 8 * b + t;
-          al[t] = AL2[i * 64];
-          o[t] = qk_off(is_q ? i : CH + i, c);
-          v[t] = ld_h2(QKw + o[t]);
-        }
-        if (is_q) {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            f.x *= al[t].x;
-            f.y *= al[t].y;
-            st_h2(QKw + o[t], v[t].x * f.x, v[t].y * f.y);
-          }
-        } else {
-#pragma unroll
-          for (int t = 7; t >= 0; --t) {
-            st_h2(QKw + o[t], v[t].x * f.x, v[t].y * f.y);
-            f.x *= al[t].x;
-            f.y *= al[t].y;
-          }
-        }
-      }
     }
-    tc::fence_proxy_async_smem();  // [q^ ; k^] (bulk store)
     __syncthreads();
-    if (tid == 0) {
-      bulk_s2g(static_cast<unsigned char*>(p.scr_qh) + ((size_t)gidx * Hv + h) * (2 * KB_STRIDE),
-               sm + OFF_QK, 2 * KB_STRIDE);
-      bulk_commit();
-    }
     // ---- T diag(beta) as the fp16 A operand (rows 64..127 zero): row i,
     // 8-column group c8 (only the groups at or left of the diagonal block
     // are T's; the rest are zero)
@@ -675,14 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
       tc::commit(&mbar);
     }
     ok = cta_wait(&mbar, it_par, &flag) && rok;
-    // the products have read v, and the [q^ ; k^] store its space: the next
-    // item's tiles
-    if (ok && tid == 0 && next < n_items) {
-      bulk_wait_read_all();
-      issue_qk(next);
-      issue_v(next);
-      pending = 1 + (int)(it_par ^ 1u);
-    }
+    // the products have read v: the next item's v tile
+    if (ok && tid == 0 && next < n_items) issue_v(next);
   }
   if (ok) {
     tc::fence_after_sync();
