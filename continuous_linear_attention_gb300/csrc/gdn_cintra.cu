@@ -1,7 +1,7 @@
 // Conv prologue and state-independent chunk products of the prefill path in
 // one kernel, fully parallel over the 64-token chunks of the prefill
-// sequences: one CTA per (chunk, k-head), both v-heads of the k-head at once,
-// two CTAs per SM.
+// sequences: an item per (chunk, k-head), both v-heads of the k-head at once,
+// on a persistent grid of two CTAs per SM.
 //
 // Per chunk (rows past the sequence end count as zero tokens), following
 // "Continuous batching for linear attention layers" (a varlen causal
@@ -17,8 +17,9 @@
 //   per head:  A_ij = beta_i e^{G_i - G_j} (k~_i . k~_j)  (j < i)
 //              P_ij = e^{G_i - G_j} (q~_i . k~_j)          (j <= i)
 //              T = (I + A)^{-1}     (16 x 16 diagonal blocks by column
-//                                    substitution, off-diagonal blocks on
-//                                    mma.sync with a tf32 head/tail split)
+//                                    substitution, off-diagonal blocks as
+//                                    product chains on mma.sync with a tf32
+//                                    head/tail split)
 //   [-w_0 ; -w_1] = [-T_0 diag(beta_0 e^{G_0}) ; -T_1 diag(beta_1 e^{G_1})] k~
 //   u_h = T_h diag(beta_h) v_h                       (tcgen05)
 // and writes to the pool's prefill scratch, chunk-major (by the scheduler's
