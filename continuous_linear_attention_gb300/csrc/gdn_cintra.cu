@@ -636,7 +636,8 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       const int hl = warp >> 2, wl = warp & 3;
       float* ATh = AT + hl * CH * AP;
       float* Z = reinterpret_cast<float*>(sm + OFF_QK + hl * KB_STRIDE);
-      solve::offdiag_chains<4>(ATh, Z, wl, [] { __syncthreads(); });
+      solve::offdiag_chains<4>(ATh, Z, wl, [] { __syncthreads(); },
+                               [](int, int, const float(&)[4], const float(&)[4]) {});
     }
     __syncthreads();
     // ---- the MMAs' A tiles over the A / T array once every T value is read:

@@ -67,9 +67,9 @@ constexpr float kF16Max = 65000.f;
 //   NK  -k~ e^{Gamma}: 2 token-major boxes (MN-major B operand of -w)
 //   AL  alpha fp32 [64 tokens][128 channels]
 //   LR  L_1..L_3 (32 rows each: 16 q rows, 16 k rows), then R_1..R_3 (16,
-//       32, 48 rows), fp16 [192][LRP]; after the products: the solve's B
-//       blocks, then the T diag(beta) operand (128 rows x 64 tokens, rows
-//       64.. zero) and the u and -w staging tiles
+//       32, 48 rows), fp16 [192][LRP]; after the products: the T diag(beta)
+//       operand (128 rows x 64 tokens, rows 64.. zero), written by the solve,
+//       and at 16 KiB the solve's B blocks, then the u and -w staging tiles
 //   PT  P fp16 [64 i][64 j] (K-major B operand of the output product)
 //   AT  A, then T, fp32 [64][AP]
 //   GB  beta fp32 [64]
@@ -80,9 +80,9 @@ constexpr uint32_t OFF_LM = 49152;
 constexpr uint32_t OFF_NK = 81920;
 constexpr uint32_t OFF_AL = 98304;
 constexpr uint32_t OFF_LR = 131072;
-constexpr uint32_t OFF_Z = OFF_LR;
-constexpr uint32_t OFF_AU = OFF_LR;
 constexpr uint32_t OFF_UW = OFF_LR + 16384;  // u, then -w: 2 boxes each
+constexpr uint32_t OFF_Z = OFF_UW;  // the solve's B blocks (the staging is free then)
+constexpr uint32_t OFF_AU = OFF_LR;
 constexpr uint32_t OFF_PT = 184320;
 constexpr uint32_t OFF_AT = OFF_PT + BOX;
 constexpr uint32_t OFF_GB = OFF_AT + CH * AP * 4;
@@ -590,41 +590,62 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
     // ---- T = (I + A)^{-1} on warps 0..5 (diagonal blocks by threads 0..63,
     // then the off-diagonal blocks in four product steps, one chain per warp;
     // named barrier 1 over those 192 threads)
+    // Every block of T goes to AT (fp32, for the solve's later steps) and,
+    // scaled by beta_j, to the fp16 A operand T diag(beta) of the u / -w
+    // products; the helper warps 6..15 zero that operand's blocks above the
+    // diagonal and its rows 64..127.
+    unsigned char* AU = sm + OFF_AU;
     if (warp < 6) {
       float col[16];
       const int b = (tid >> 4) & 3, m = tid & 15;
       float* Ab = AT + (16 * b) * AP + 16 * b;
       if (tid < CH) solve::diag_col(Ab, m, col);
       solve_bar();
-      if (tid < CH) solve::diag_col_store(Ab, m, col);
+      if (tid < CH) {
+        solve::diag_col_store(Ab, m, col);
+        const float bm = GB[16 * b + m];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const float t = col[r] * bm;
+          amax = fmaxf(amax, fabsf(t));
+          *reinterpret_cast<__half*>(AU + tc::sw128_offset(16 * b + r, 16 * b + m)) = __float2half_rn(t);
+        }
+      }
       solve_bar();
       float* Z = reinterpret_cast<float*>(sm + OFF_Z);
-      solve::offdiag_chains<6>(AT, Z, warp, solve_bar);
-    }
-    __syncthreads();
-    // ---- T diag(beta) as the fp16 A operand (rows 64..127 zero): row i,
-    // 8-column group c8 (only the groups at or left of the diagonal block
-    // are T's; the rest are zero)
-    {
-      const int i = tid >> 3, c8 = tid & 7;
-      float tb[8];
-      if ((c8 >> 1) <= (i >> 4)) {
-        const float4 t0 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8);
-        const float4 t1 = *reinterpret_cast<const float4*>(AT + i * AP + c8 * 8 + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(GB + c8 * 8);
-        const float4 b1 = *reinterpret_cast<const float4*>(GB + c8 * 8 + 4);
-        tb[0] = t0.x * b0.x; tb[1] = t0.y * b0.y; tb[2] = t0.z * b0.z; tb[3] = t0.w * b0.w;
-        tb[4] = t1.x * b1.x; tb[5] = t1.y * b1.y; tb[6] = t1.z * b1.z; tb[7] = t1.w * b1.w;
-      } else {
+      const int lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+      solve::offdiag_chains<6>(AT, Z, warp, solve_bar,
+                               [&](int i, int j, const float(&t0)[4], const float(&t1)[4]) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) tb[e] = 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+          const float(&t)[4] = hh ? t1 : t0;
+          const int col = 16 * j + 8 * hh + 2 * t4;
+          const float b0 = GB[col], b1 = GB[col + 1];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float v0 = t[2 * rr] * b0, v1 = t[2 * rr + 1] * b1;
+            amax = max_abs3(amax, v0, v1);
+            *reinterpret_cast<__half2*>(AU + tc::sw128_offset(16 * i + g + 8 * rr, col)) =
+                __floats2half2_rn(v0, v1);
+          }
+        }
+      });
+    } else {
+      // zero rows 64..127 (64 x 128 B) and the six blocks above the diagonal
+      // (16 rows x 32 B each) of the operand
+      for (int q = tid - 192; q < 512 + 6 * 32; q += 320) {
+        if (q < 512) {
+          *reinterpret_cast<uint4*>(AU + (CH + (q >> 3)) * 128 + (q & 7) * 16) = make_uint4(0, 0, 0, 0);
+        } else {
+          const int z = q - 512, blkz = z >> 5, r = (z >> 1) & 15, hh = z & 1;
+          const int bi = blkz < 3 ? 0 : (blkz < 5 ? 1 : 2);
+          const int bj = blkz < 3 ? blkz + 1 : (blkz < 5 ? blkz - 1 : 3);
+          *reinterpret_cast<uint4*>(AU + tc::sw128_offset(16 * bi + r, 16 * bj + 8 * hh)) =
+              make_uint4(0, 0, 0, 0);
+        }
       }
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) amax = max_abs3(amax, tb[e], tb[e + 1]);
-      *reinterpret_cast<uint4*>(sm + OFF_AU + tc::sw128_offset(i, c8 * 8)) = pack8(tb);
-      *reinterpret_cast<uint4*>(sm + OFF_AU + tc::sw128_offset(CH + i, c8 * 8)) = make_uint4(0, 0, 0, 0);
     }
-    tc::fence_proxy_async_smem();
+    tc::fence_proxy_async_smem();  // T diag(beta) (MMA operand)
     tc::fence_before_sync();
     __syncthreads();
     // u = T diag(beta) v into columns 0..127, -w = T diag(beta) (-k~ e^{Gamma})

@@ -127,9 +127,21 @@ __device__ __forceinline__ void diag_col_store(float* Ab, int m, const float (&c
 // T_31 = -(P_31 + B_32 T_21) and P_30 += B_31 T_10; after another
 // T_30 = -(P_30 + B_32 T_20).  Chain c runs on warp c % NW of the NW warps
 // (wl = this warp's index among them) and bar() is their barrier; A's
-// diagonal blocks must already be inverted.
-template <int NW, typename Bar>
-__device__ __forceinline__ void offdiag_chains(float* AT, float* Z, int wl, Bar bar) {
+// diagonal blocks must already be inverted.  on_t(i, j, t0, t1) sees each
+// block T_ij as this warp's fragments of its two 16 x 8 halves (blk_store's
+// layout, signs applied).
+template <int NW, typename Bar, typename OnT>
+__device__ __forceinline__ void offdiag_chains(float* AT, float* Z, int wl, Bar bar, OnT on_t) {
+  auto put = [&](int i, int j, float (&a0)[4], float (&a1)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a0[e] = -a0[e];
+      a1[e] = -a1[e];
+    }
+    blk_store(AT + (16 * i) * AP + 16 * j, AP, 0, a0, 1.f);
+    blk_store(AT + (16 * i) * AP + 16 * j, AP, 8, a1, 1.f);
+    on_t(i, j, a0, a1);
+  };
   auto blk = [&](int i, int j) { return AT + (16 * i) * AP + 16 * j; };
   float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's P (chains 3..5)
 #pragma unroll 1
@@ -144,8 +156,7 @@ __device__ __forceinline__ void offdiag_chains(float* AT, float* Z, int wl, Bar 
     float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
     blk_mma3_pair(b0, b1, Z + c * ZB, ZP, blk(j, j), AP);  // B_ij T_jj
     if (c < 3) {
-      blk_store(blk(i, j), AP, 0, b0, -1.f);
-      blk_store(blk(i, j), AP, 8, b1, -1.f);
+      put(i, j, b0, b1);
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -161,12 +172,10 @@ __device__ __forceinline__ void offdiag_chains(float* AT, float* Z, int wl, Bar 
     if (c < 3) continue;
     if (c == 3) {
       blk_mma3_pair(p0, p1, Z + 1 * ZB, ZP, blk(1, 0), AP);
-      blk_store(blk(2, 0), AP, 0, p0, -1.f);
-      blk_store(blk(2, 0), AP, 8, p1, -1.f);
+      put(2, 0, p0, p1);
     } else if (c == 4) {
       blk_mma3_pair(p0, p1, Z + 2 * ZB, ZP, blk(2, 1), AP);
-      blk_store(blk(3, 1), AP, 0, p0, -1.f);
-      blk_store(blk(3, 1), AP, 8, p1, -1.f);
+      put(3, 1, p0, p1);
     } else {
       blk_mma3_pair(p0, p1, Z + 4 * ZB, ZP, blk(1, 0), AP);
     }
@@ -174,8 +183,7 @@ __device__ __forceinline__ void offdiag_chains(float* AT, float* Z, int wl, Bar 
   bar();
   if (5 % NW == wl) {
     blk_mma3_pair(p0, p1, Z + 2 * ZB, ZP, blk(2, 0), AP);
-    blk_store(blk(3, 0), AP, 0, p0, -1.f);
-    blk_store(blk(3, 0), AP, 8, p1, -1.f);
+    put(3, 0, p0, p1);
   }
 }
 
