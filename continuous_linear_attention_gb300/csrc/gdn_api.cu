@@ -473,13 +473,18 @@ int gdn_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const void* 
   if (max_items > p->num_blocks - 1) max_items = p->num_blocks - 1;
   if (max_items > T) max_items = T;
   if (gdn::decode_supported(p->dk, p->act, p->Hk, p->Hv, p->K)) {
-    // length-1 sequences: persistent HBM-streaming decode kernel; longer ones
-    // (at most T/2 of them): token-serial kernel
-    if (gdn::launch_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+    // length-1 sequences: persistent HBM-streaming decode kernel, right
+    // after the scheduler, or with prefills behind their recurrence (on the
+    // SMs its last chains leave idle); longer ones (at most T/2 of them):
+    // the chunked prefill, else the token-serial kernel
     int max_long = max_items < T / 2 ? max_items : T / 2;
     if (max_seqlen_hint == 1) max_long = 0;  // longer sequences are flagged, never listed
-    if (gdn::chunk_supported(p->dk, p->act, p->K)) {
-      if (gdn::launch_chunk(fp, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;
+    const bool chunk = gdn::chunk_supported(p->dk, p->act, p->K);
+    const bool dec_late = chunk && max_long > 0;
+    if (!dec_late && gdn::launch_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (chunk) {
+      if (gdn::launch_chunk(fp, max_long, s, dec_late ? max_items : 0) != cudaSuccess)
+        return GDN_ERR_CUDA;
     } else if (gdn::launch_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess) {
       return GDN_ERR_CUDA;
     }
@@ -595,11 +600,14 @@ int gdn_kda_varlen_forward(gdn_pool_t* p, int layer, const void* x_qkv, const vo
     if (max_items > p->num_blocks - 1) max_items = p->num_blocks - 1;
     if (max_items > T) max_items = T;
     if (gdn::decode_supported(p->dk, p->act, p->Hk, p->Hv, p->K)) {
-      if (gdn::launch_kda_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
       int max_long = max_items < T / 2 ? max_items : T / 2;
       if (max_seqlen_hint == 1) max_long = 0;
+      // decodes behind the split prefill's recurrence when there is one
+      const bool dec_late = fp.scr_qk && max_long > 0;
+      if (!dec_late && gdn::launch_kda_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
       if (fp.scr_qk) {
-        if (gdn::launch_kda_chunk(fp, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;
+        if (gdn::launch_kda_chunk(fp, max_long, s, dec_late ? max_items : 0) != cudaSuccess)
+          return GDN_ERR_CUDA;
       } else if (gdn::launch_kda_recurrent(fp, p->dk, p->act, max_long, true, s) != cudaSuccess) {
         return GDN_ERR_CUDA;
       }

@@ -706,7 +706,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
 
 }  // namespace
 
-cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
+cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream, int max_dec) {
   if (max_pre <= 0) return cudaSuccess;
   const bool fused = p.scr_qk == nullptr;
   cudaError_t e = cudaSuccess;
@@ -744,6 +744,8 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // the batch's decodes, on the SMs the recurrence's last chains leave idle
+  if (max_dec > 0 && (e = launch_decode(p, max_dec, stream, true)) != cudaSuccess) return e;
   // chains whose fp16 operands left their range, token-serially, before the
   // conv states change
   e = launch_redo(p, D, GDN_BF16, max_pre, stream);
@@ -751,7 +753,7 @@ cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
   return launch_pdl(tail_update_kernel, dim3(max_pre, (p.C / 8 + 255) / 256), dim3(256), 0, stream, p);
 }
 
-cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t stream) {
+cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t stream, int max_dec) {
   if (max_pre <= 0) return cudaSuccess;
   if (!p.scr_qk || !p.scr_v || !p.scr_qh) return cudaErrorInvalidValue;
   static int num_sms = 0;
@@ -774,6 +776,8 @@ cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t strea
   if (e == cudaSuccess) e = launch_seq(p, grid, true, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // the batch's decodes, on the SMs the recurrence's last chains leave idle
+  if (max_dec > 0 && (e = launch_kda_decode(p, max_dec, stream, true)) != cudaSuccess) return e;
   // chains whose fp16 operands left their range, token-serially, before the
   // conv states change
   e = launch_kda_redo(p, max_pre, stream);

@@ -7,7 +7,9 @@
 //  - Work units are (request, k-head group).  A unit owns the q/k conv
 //    channels of its k-head and the v channels and states of its v-heads, so
 //    reading the old conv/recurrent state and overwriting it in place needs no
-//    cross-CTA ordering.  Units are dealt round-robin over the CTAs.
+//    cross-CTA ordering.  A CTA's first unit is its index, the next ones come
+//    from a counter the scheduler resets, so that CTAs which start late (see
+//    below) take fewer.
 //  - One producer warp streams, kStages heads ahead, each v-head's state
 //    (64 KiB) into a ring of shared-memory buffers with bulk (TMA) copies, and
 //    with the first head of a unit also that unit's conv inputs (its x row,
@@ -16,6 +18,11 @@
 //  - Eight compute warps read a state buffer once into registers (releasing
 //    it to the producer at once), reduce S k and S q across warps, and write
 //    the new state straight from registers to HBM with 16-byte stores.
+//  - In a batch that also has prefills it is launched after the prefill's
+//    recurrence (p.decode_late): its CTAs start on the SMs the recurrence's
+//    last chains leave idle, without waiting for it (no data is shared: other
+//    requests, other blocks), and wait for it only before they end, so that
+//    the kernels after them still see everything before them complete.
 //
 // Per token (v-head h, k-head h / (Hv/Hk)), as in the gated delta rule:
 //   y = SiLU(conv over [conv state ; x]),  q, k L2-normalised, q /= sqrt(d_k)
@@ -81,7 +88,8 @@ template <> struct Gates<true> {
 struct Meta {
   int row;   // packed row of the token
   int wblk;  // block written
-  int pad0, pad1;
+  int unit;  // the unit, or -1: no more units
+  int pad;
 };
 
 template <bool kKda>
@@ -98,6 +106,7 @@ struct DecodeSmem {
   uint64_t empty[kStages];
   uint64_t cempty[2];
   int ok;
+  volatile int issued;  // stages the producer has issued (for the drain on a timeout)
 };
 
 __device__ __forceinline__ void consumer_sync() {
@@ -120,14 +129,19 @@ template <bool kKda>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecodeSmem<kKda>& sm = *reinterpret_cast<DecodeSmem<kKda>*>(smem_raw);
-  pdl_wait_then_release();
+  const bool late = p.decode_late != 0;
+  if (late)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  else
+    pdl_wait_then_release();
   const int tid = threadIdx.x;
   const int Hk = p.Hk, Hv = p.Hv, C = p.C;
-  const int n_units = p.work.header()[kNDec] * Hk;
-  const int my_units = n_units > (int)blockIdx.x
-                           ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int n_stages = my_units * R;
-  if (n_stages == 0) return;
+  int32_t* hdr = p.work.header();
+  const int n_units = hdr[kNDec] * Hk;
+  if ((int)blockIdx.x >= n_units) {
+    if (late && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -143,14 +157,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
     // ======================= producer warp =======================
     if (tid != kConsumers) return;
     const int* dec = p.work.dec();
-    for (int n = 0; n < n_stages; ++n) {
+    // this CTA's units: its index, then from the counter (one fetched ahead)
+    int unit = blockIdx.x;
+    int nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
+    sm.issued = 0;
+    for (int n = 0;; ++n) {
       const int st = n % kStages;
       if (n >= kStages && !mbar_wait_bounded(&sm.empty[st], ((n / kStages) - 1) & 1)) {
-        atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+        atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
         return;
       }
       const int k = n / R, jh = n % R;
-      const int unit = blockIdx.x + k * gridDim.x;
+      if (jh == 0 && k > 0) {
+        unit = nxt;
+        if (unit < n_units) nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
+      }
+      if (unit >= n_units) {
+        // no more units: an empty stage tells the compute warps
+        sm.meta[st].unit = -1;
+        mbar_arrive(&sm.full[st]);
+        return;
+      }
       const int s = dec[unit / Hk];
       const int kh = unit % Hk;
       const int h = kh * R + jh;
@@ -159,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
       const int rblk = p.has_past[s] ? wblk : 0;
       sm.meta[st].row = row;
       sm.meta[st].wblk = wblk;
+      sm.meta[st].unit = unit;
       const unsigned char* rbase = p.layer_base + (size_t)rblk * p.stride;
       const float* src = reinterpret_cast<const float*>(rbase + p.rec_off) + (size_t)h * D * D;
       uint32_t bytes = kHeadBytes;
@@ -206,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
         bulk_g2s(ci->b, reinterpret_cast<const __nv_bfloat16*>(p.b) + (size_t)row * Hv, Hv * 2,
                  &sm.full[st]);
       }
+      sm.issued = n + 1;
     }
-    return;
   }
 
   // ======================= compute warps =======================
@@ -217,23 +245,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
   const int rg = tid / kCV;
   const int warp = tid >> 5, lane = tid & 31;
 
-  for (int n = 0; n < n_stages; ++n) {
+  for (int n = 0;; ++n) {
     const int st = n % kStages;
     const int k = n / R, jh = n % R;
-    const int unit = blockIdx.x + k * gridDim.x;
-    const int kh = unit % Hk;
-    const int h = kh * R + jh;
 
     if (tid == 0) sm.ok = mbar_wait_bounded(&sm.full[st], (n / kStages) & 1) ? 1 : 0;
     consumer_sync();
     if (!sm.ok) {
       if (tid == 0) {
-        atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
-        for (int m = n + 1; m < n_stages && m < n + kStages; ++m)
+        atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+        // the copies already issued land before the CTA ends
+        for (int m = n + 1; m < sm.issued && m < n + kStages; ++m)
           mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1);
+        if (late) asm volatile("griddepcontrol.wait;" ::: "memory");
       }
       return;
     }
+    const int unit = sm.meta[st].unit;
+    if (unit < 0) break;
+    const int kh = unit % Hk;
+    const int h = kh * R + jh;
     const int row = sm.meta[st].row;
     const int wblk = sm.meta[st].wblk;
     unsigned char* wbase = p.layer_base + (size_t)wblk * p.stride;
@@ -358,6 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
     // its own full-barrier wait and a consumer barrier, which every thread
     // reaches after this loop)
   }
+  // launched early behind the prefill's recurrence: it has completed before
+  // this CTA ends
+  if (late && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 int g_num_sms = 0;
@@ -371,7 +405,9 @@ bool decode_supported(int d, int act, int Hk, int Hv, int K) {
 namespace {
 
 template <bool kKda>
-cudaError_t launch_decode_t(const FwdParams& p, int max_dec, cudaStream_t stream) {
+cudaError_t launch_decode_t(const FwdParams& pin, int max_dec, bool late, cudaStream_t stream) {
+  FwdParams p = pin;
+  p.decode_late = late ? 1 : 0;
   if (max_dec <= 0) return cudaSuccess;
   if (g_num_sms == 0) {
     int dev = 0;
@@ -392,11 +428,11 @@ cudaError_t launch_decode_t(const FwdParams& p, int max_dec, cudaStream_t stream
 
 }  // namespace
 
-cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {
-  return launch_decode_t<false>(p, max_dec, stream);
+cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream, bool late) {
+  return launch_decode_t<false>(p, max_dec, late, stream);
 }
-cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream) {
-  return launch_decode_t<true>(p, max_dec, stream);
+cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream, bool late) {
+  return launch_decode_t<true>(p, max_dec, late, stream);
 }
 
 }  // namespace gdn

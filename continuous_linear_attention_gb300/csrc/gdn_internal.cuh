@@ -36,6 +36,7 @@ enum Cnt : int {
   kPreChunks = 6,  // total 64-token chunks of the length>1 sequences
   kItemHeadC = 7,  // item counters of the persistent chunk-parallel kernels
   kItemHeadK = 8,  // (cintra_kernel, kintra_kernel; reset by the scheduler)
+  kDecHead = 9,    // unit counter of the decode kernel (reset by the scheduler)
   kHeaderWords = 16,
 };
 
@@ -70,6 +71,7 @@ struct FwdParams {
   size_t rec_off;       // recurrent sub-state offset inside a block (bytes)
   int T, N, Hk, Hv, C, K, num_blocks;
   int max_seqlen_hint;  // 0 = unknown; else longer sequences are flagged and skipped
+  int decode_late;      // (decode kernel) launched behind the prefill's recurrence
   WorkArea work;
   // prefill scratch, chunk-major over the scheduler's 64-token prefill chunks
   // (chunk index g); nullptr when the pool has not enough of it (the fused
@@ -157,13 +159,17 @@ __device__ __forceinline__ bool redo_marked(const WorkArea& w, int k, int h) {
   return (reinterpret_cast<const unsigned*>(w.redo())[2 * k + (h >> 5)] >> (h & 31)) & 1u;
 }
 // The persistent decode kernel (length-1 sequences): d_k = d_v = 128, bf16
-// activations, Hv = 2 Hk, K = 4.
+// activations, Hv = 2 Hk, K = 4.  late: launched right behind the prefill's
+// recurrence, whose idle SMs it takes without waiting for it (it waits only
+// before its CTAs end); otherwise right behind the scheduler.
 bool decode_supported(int d, int act, int Hk, int Hv, int K);
-cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
+cudaError_t launch_decode(const FwdParams& p, int max_dec, cudaStream_t stream, bool late = false);
 // The tcgen05 chunked prefill kernel (length > 1 sequences) and the conv-state
-// update that follows it: d_k = d_v = 128, bf16 activations, K = 4.
+// update that follows it: d_k = d_v = 128, bf16 activations, K = 4.  With
+// max_dec > 0 the decode kernel runs late, between the recurrence and the
+// redo.
 bool chunk_supported(int d, int act, int K);
-cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
+cudaError_t launch_chunk(const FwdParams& p, int max_pre, cudaStream_t stream, int max_dec = 0);
 // Conv, gates and the state-independent products of every prefill (64-token
 // chunk, k-head), on a persistent grid of up to 2 num_sms CTAs, writing the
 // scratch the recurrence kernel reads (max_chunks: host bound on the number
@@ -183,15 +189,18 @@ cudaError_t launch_kintra(const FwdParams& p, int max_chunks, int num_sms, cudaS
 // The per-channel-decay (KDA) rule: p.a is [T][Hv][d_k] and p.dt_bias
 // [Hv][d_k].  Decode kernel for the shapes decode_supported() accepts, and the
 // token-serial kernel (as launch_recurrent) for everything else.
-cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream);
+cudaError_t launch_kda_decode(const FwdParams& p, int max_dec, cudaStream_t stream,
+                              bool late = false);
 cudaError_t launch_kda_recurrent(const FwdParams& p, int d, int act, int max_items,
                                  bool long_only, cudaStream_t stream);
 // The KDA token-serial kernel in redo mode (as launch_redo; d = 128, bf16).
 cudaError_t launch_kda_redo(const FwdParams& p, int max_pre, cudaStream_t stream);
 // The KDA split prefill (d = 128, bf16, Hv = 2 Hk, K = 4, scratch present):
 // conv-only pass, kintra, the recurrence, the redo of out-of-range chains and
-// the conv-state update.
-cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t stream);
+// the conv-state update; with max_dec > 0 the KDA decode kernel runs late,
+// between the recurrence and the redo.
+cudaError_t launch_kda_chunk(const FwdParams& p, int max_pre, cudaStream_t stream,
+                             int max_dec = 0);
 // The Mamba2 scan: token-serial kernel over every active sequence (or, with
 // long_only, those longer than one token), then their conv-state update (head
 // dim P in {32, 64}, state size in {32, 64, 128}); and the persistent decode

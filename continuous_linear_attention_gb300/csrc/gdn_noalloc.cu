@@ -142,11 +142,15 @@ extern "C" int gdn_varlen_forward_noalloc(void* pool_mem, size_t pool_bytes, int
       if (max_items > num_blocks - 1) max_items = num_blocks - 1;
       if (max_items > T) max_items = T;
       if (gdn::decode_supported(d_k, act_dtype, num_k_heads, num_v_heads, conv_k)) {
-        if (gdn::launch_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
         int max_long = max_items < T / 2 ? max_items : T / 2;
         if (max_seqlen_hint == 1) max_long = 0;
-        if (gdn::chunk_supported(d_k, act_dtype, conv_k)) {
-          if (gdn::launch_chunk(fp, max_long, s) != cudaSuccess) return GDN_ERR_CUDA;
+        // decodes behind the prefill's recurrence when there is one
+        const bool chunk = gdn::chunk_supported(d_k, act_dtype, conv_k);
+        const bool dec_late = chunk && max_long > 0;
+        if (!dec_late && gdn::launch_decode(fp, max_items, s) != cudaSuccess) return GDN_ERR_CUDA;
+        if (chunk) {
+          if (gdn::launch_chunk(fp, max_long, s, dec_late ? max_items : 0) != cudaSuccess)
+            return GDN_ERR_CUDA;
         } else if (gdn::launch_recurrent(fp, d_k, act_dtype, max_long, true, s) != cudaSuccess) {
           return GDN_ERR_CUDA;
         }

@@ -48,7 +48,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     if (tid == 0) {
       atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_SEQLENS);
       hdr[kNItems] = hdr[kNDec] = hdr[kNPre] = hdr[kPreTokens] = hdr[kPreChunks] = 0;
-      hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = 0;
+      hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = hdr[kDecHead] = 0;
     }
     return;
   }
@@ -145,7 +145,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     hdr[kNDec] = s_n_dec;
     hdr[kNPre] = n_pre;
     hdr[kPreTokens] = s_pre_tokens;
-    hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = 0;
+    hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = hdr[kDecHead] = 0;
   }
 }
 
