@@ -22,7 +22,8 @@
 //    head also the unit's conv inputs) and eight compute warps update it and
 //    write it from registers to HBM.  A unit is (request, group): it owns the
 //    x channels of the group's heads and the group's B and C channels, so it
-//    writes its part of the conv state in place.  Longer sequences then run on
+//    writes its part of the conv state in place.  A CTA's first unit is its
+//    index, the next ones come from a counter.  Longer sequences then run on
 //    the token-serial kernel, or, at that shape and when the pool's scratch
 //    holds the call's rows, on the chunked scan below.
 //  - ssd_prep_kernel + ssd_chunk_kernel: the chunked scan of the prefill
@@ -227,10 +228,12 @@ struct SsdDecodeSmem {
   float av[kMaxHpg];
   int row[kDStages];
   int wblk[kDStages];
+  int unit[kDStages];  // the stage's unit, or -1: no more units
   uint64_t full[kDStages];
   uint64_t empty[kDStages];
   uint64_t cempty[2];
   int ok;
+  volatile int issued;  // stages the producer has issued (for the drain on a timeout)
 };
 
 static_assert(sizeof(SsdDecodeSmem) <= 227 * 1024, "shared memory of one CTA");
@@ -255,11 +258,9 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
   const int tid = threadIdx.x;
   const int H = p.H, G = p.G, C = p.C;
   const int hpg = H / G;
-  const int n_units = p.work.header()[kNDec] * G;
-  const int my_units = n_units > (int)blockIdx.x
-                           ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int n_stages = my_units * hpg;
-  if (n_stages == 0) return;
+  int32_t* hdr = p.work.header();
+  const int n_units = hdr[kNDec] * G;
+  if ((int)blockIdx.x >= n_units) return;
 
   if (tid == 0) {
     for (int i = 0; i < kDStages; ++i) {
@@ -276,14 +277,28 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
     if (tid != kDConsumers) return;
     const int* dec = p.work.dec();
     const uint32_t unit_ch = (uint32_t)(hpg * DP + 2 * DN);
-    for (int n = 0; n < n_stages; ++n) {
+    // this CTA's units (request, group): its index, then from a counter the
+    // scheduler resets (one fetched ahead), so that no CTA ends far behind
+    int unit = blockIdx.x;
+    int nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
+    sm.issued = 0;
+    for (int n = 0;; ++n) {
       const int st = n % kDStages;
       if (n >= kDStages && !mbar_wait_bounded(&sm.empty[st], ((n / kDStages) - 1) & 1)) {
-        atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
+        atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
         return;
       }
       const int k = n / hpg, j = n % hpg;
-      const int unit = blockIdx.x + k * gridDim.x;
+      if (j == 0 && k > 0) {
+        unit = nxt;
+        if (unit < n_units) nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
+      }
+      if (unit >= n_units) {
+        // no more units: an empty stage tells the compute warps
+        sm.unit[st] = -1;
+        ssd_mbar_arrive(&sm.full[st]);
+        return;
+      }
       const int s = dec[unit / G];
       const int g = unit % G;
       const int h = g * hpg + j;
@@ -292,6 +307,7 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
       const int rblk = p.has_past[s] ? wblk : 0;
       sm.row[st] = row;
       sm.wblk[st] = wblk;
+      sm.unit[st] = unit;
       const unsigned char* rbase = p.layer_base + (size_t)rblk * p.stride;
       const float* src = reinterpret_cast<const float*>(rbase + p.ssm_off) + (size_t)h * DP * DN;
       uint32_t bytes = kDHeadBytes;
@@ -328,8 +344,8 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
         bulk_g2s(ci->dt, reinterpret_cast<const __nv_bfloat16*>(p.dt) + (size_t)row * H + g * hpg,
                  hpg * 2, &sm.full[st]);
       }
+      sm.issued = n + 1;
     }
-    return;
   }
 
   // ======================= compute warps =======================
@@ -338,23 +354,25 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
   const int rg = tid >> 5;   // row group: rows rg + 8 i
   const int lane = tid & 31;
 
-  for (int n = 0; n < n_stages; ++n) {
+  for (int n = 0;; ++n) {
     const int st = n % kDStages;
     const int k = n / hpg, j = n % hpg;
-    const int unit = blockIdx.x + k * gridDim.x;
-    const int g = unit % G;
-    const int h = g * hpg + j;
 
     if (tid == 0) sm.ok = mbar_wait_bounded(&sm.full[st], (n / kDStages) & 1) ? 1 : 0;
     ssd_consumer_sync();
     if (!sm.ok) {
       if (tid == 0) {
-        atomicOr((unsigned*)&p.work.header()[kErr], GDN_FLAG_TIMEOUT);
-        for (int m = n + 1; m < n_stages && m < n + kDStages; ++m)
+        atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_TIMEOUT);
+        // the copies already issued land before the CTA ends
+        for (int m = n + 1; m < sm.issued && m < n + kDStages; ++m)
           mbar_wait_bounded(&sm.full[m % kDStages], (m / kDStages) & 1);
       }
       return;
     }
+    const int unit = sm.unit[st];
+    if (unit < 0) break;
+    const int g = unit % G;
+    const int h = g * hpg + j;
     const int row = sm.row[st];
     unsigned char* wbase = p.layer_base + (size_t)sm.wblk[st] * p.stride;
 
