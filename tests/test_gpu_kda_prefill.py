@@ -59,6 +59,17 @@ def test_long_chains(slow):
     check_against_oracle(wl, run=_run_split(wl))
 
 
+def test_many_decodes_behind_the_prefill():
+    """300 decodes among two prefill continuations: the per-channel-decay
+    decode kernel runs behind the split prefill's recurrence and takes its
+    units from a counter."""
+    rng = np.random.default_rng(47)
+    lens = [1] * 300 + [150, 70]
+    rng.shuffle(lens)
+    wl = _kda("kda_many_dec", lens, [1] * len(lens), len(lens) + 9, 47)
+    check_against_oracle(wl, run=_run_split(wl))
+
+
 def test_split_and_token_serial_agree():
     """The split prefill and the token-serial kernel (a pool without
     prefill scratch) on the same batch."""

@@ -106,6 +106,18 @@ def test_mixed_batch_full(prefill):
     check_against_oracle(synth.mixed_batch(), prefill=prefill)
 
 
+@pytest.mark.parametrize("prefill", ["split", "fused"])
+def test_many_decodes_behind_the_prefill(prefill):
+    """400 decodes among three prefill continuations: the decode kernel runs
+    behind the prefill's recurrence (its CTAs start while the recurrence's last
+    chains run) and takes its units from a counter, many more than its CTAs."""
+    rng = np.random.default_rng(61)
+    lens = [1] * 400 + [200, 130, 65]
+    rng.shuffle(lens)
+    wl = synth.make_workload("many_dec", synth.FULL_DIMS, lens, [1] * len(lens), len(lens) + 9, 61)
+    check_against_oracle(wl, prefill=prefill)
+
+
 def test_long_context_split_equals_single_pass():
     """4 x 32768 tokens then a 4096-token continuation from the saved states
     equals one 36864-token pass; the oracle checks a prefix of sequence 0."""
