@@ -496,8 +496,10 @@ seq_kernel(FwdParams p) {
       }
       tc::fence_before_sync();
       mma_release<kBarS>();  // S += U^T (e^{G_C - G} k~)
-      // ---- O^T columns 64 + i <- e^{G_i} (.) before U^T P^T accumulates onto them
-      {
+      // ---- O^T columns 64 + i <- e^{G_i} (.) before U^T P^T accumulates onto
+      // them (the per-channel-decay tiles carry the scales already; columns
+      // past the chunk's end are never stored)
+      if constexpr (!kKda) {
         float o[32];
         tc::tmem_ld32(tmem + lane + dcol + CH + hf * 32, o);
         tc::tmem_wait_ld();
