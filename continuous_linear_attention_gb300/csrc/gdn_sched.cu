@@ -30,7 +30,12 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
   __shared__ int s_n_items, s_n_dec, s_n_pre, s_pre_tokens;
   __shared__ unsigned s_flags;
   __shared__ int32_t s_counts[kSmemCounts];
-  pdl_wait_then_release();  // launched plainly: lets the next kernel launch early
+  // A programmatic dependent of the stream's previous kernel: the reads of
+  // this call's inputs and the block counts (which only this kernel uses) run
+  // before griddepcontrol.wait, overlapping that kernel's tail; every write
+  // the previous forward's kernels could still read (the header, the lists,
+  // the records) comes after it.  The next kernel may launch at once.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
   int32_t* hdr = work.header();
   int32_t* blk_count = num_blocks <= kSmemCounts ? s_counts : work.blk_count();
@@ -45,6 +50,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     if (cu[s + 1] < cu[s]) s_bad = 1;
   __syncthreads();
   if (s_bad) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) {
       atomicOr((unsigned*)&hdr[kErr], GDN_FLAG_SEQLENS);
       hdr[kNItems] = hdr[kNDec] = hdr[kNPre] = hdr[kPreTokens] = hdr[kPreChunks] = 0;
@@ -66,6 +72,7 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     }
   }
   __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int32_t* items = work.items();
   int32_t* dec = work.dec();
   int32_t* pre_tmp = work.pre_tmp();
@@ -152,10 +159,8 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
 }  // namespace
 
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream) {
-  schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p.cu, p.blk, p.N, p.T, p.num_blocks,
-                                                   p.max_seqlen_hint, p.work,
-                                                   static_cast<int4*>(p.scr_c));
-  return cudaGetLastError();
+  return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), 0, stream, p.cu, p.blk, p.N,
+                    p.T, p.num_blocks, p.max_seqlen_hint, p.work, static_cast<int4*>(p.scr_c));
 }
 
 }  // namespace gdn
