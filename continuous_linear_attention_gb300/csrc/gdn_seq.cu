@@ -6,20 +6,23 @@
 // chunk's last valid token and n its valid tokens, everything runs in the
 // transposed orientation: tensor-memory lane = v, columns = k or tokens.  One
 // 128 x 128 accumulator D^T carries
-//   columns 0..63  : U^T = u^T - S0 w^T            (the chunk's updates u_j)
-//   columns 64..127: O^T = S0 (e^G q~)^T + U^T P^T (the chunk's outputs o_i)
+//   columns 0..63  : U^T = u^T - S0 w^T            (the chunk's updates u_j),
+//                    then U^T P^T
+//   columns 64..127: S0 q~^T
 // as
-//   CUDA  S0 -> fp16 A operand in tensor memory;  S <- e^{G_C} S0, in two
-//         passes over k (0..63, then 64..127)
+//   CUDA  S0 -> fp16 A operand in tensor memory, in two passes over k (0..63,
+//         then 64..127), each released to the tensor core before
+//         S <- e^{G_C} S0 is written back
 //   MMA   D^T  = S0 [-w ; q~]^T (the first pass's K-steps start while the
 //         second pass runs);  D^T[:, j] += u_j  (u^T times an identity)
 //   CUDA  k~_j <- e^{G_C - G_j} k~_j in the staged tile, rows past n zeroed
 //         (while the D product runs)
 //   CUDA  U^T = D^T[:, 0..63] -> fp16 A operand in tensor memory (columns
-//         past n zeroed);  D^T[:, 64 + i] <- e^{G_i} D^T[:, 64 + i]
+//         past n zeroed)
 //   MMA   S  += U^T (e^{G_C - G} k~)             (k~ as an MN-major operand)
-//   MMA   D^T[:, 64..127] += U^T P^T
-//   CUDA  o_i = D^T[:, 64 + i] -> bf16           (while the next chunk's MMAs run)
+//   MMA   D^T[:, 0..63] = U^T P^T               (over the U^T columns, read)
+//   CUDA  o_i = e^{G_i} D^T[:, 64 + i] + D^T[:, i] -> bf16  (while the next
+//         chunk's MMAs run)
 // This is the chunked gated delta rule (Gated Delta Networks, chunkwise WY
 // form) run over cu_seqlens from per-sequence initial states, as a continuous
 // batching engine does for a linear-attention layer.  With the state as the
@@ -58,8 +61,8 @@ constexpr int kIssuer = kCompute + 32;    // first thread of the MMA warp
 constexpr int kThreads = kCompute + 64;
 // named barriers: 1 the compute warps; compute warps -> MMA warp: 5 S0
 // columns k < 64 written, 2 all of S0 written, 3 k~ tile scaled and U^T
-// written, 4 output columns rescaled
-constexpr int kBarC = 1, kBarD = 2, kBarS = 3, kBarO = 4, kBarD1 = 5;
+// written
+constexpr int kBarC = 1, kBarD = 2, kBarS = 3, kBarD1 = 5;
 constexpr int kGate = kCompute + 32;
 constexpr int R = 2;  // v-heads per k-head
 constexpr float kF16Max = 65000.f;
@@ -122,6 +125,15 @@ __device__ __forceinline__ void mul2v(float& a, float& b, float x, float y) {
   b = __uint_as_float((uint32_t)(v >> 32));
 }
 __device__ __forceinline__ void mul2(float& a, float& b, float s) { mul2v(a, b, s, s); }
+// Packed fp32 pair fma (one fma.rn.f32x2): (a, b) = (a, b) * (x, y) + (c, d).
+__device__ __forceinline__ void fma2v(float& a, float& b, float x, float y, float c, float d) {
+  unsigned long long v = (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+  const unsigned long long m = (unsigned long long)__float_as_uint(x) | ((unsigned long long)__float_as_uint(y) << 32);
+  const unsigned long long ad = (unsigned long long)__float_as_uint(c) | ((unsigned long long)__float_as_uint(d) << 32);
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(v) : "l"(m), "l"(ad));
+  a = __uint_as_float((uint32_t)v);
+  b = __uint_as_float((uint32_t)(v >> 32));
+}
 
 __device__ __forceinline__ uint4 pack8(const float* v) {
   uint4 w;
@@ -148,7 +160,9 @@ seq_kernel(FwdParams p) {
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t full[kStages], empty[kStages], mma_y, mma_s;
   __shared__ ChunkDesc desc[kStages];
-  __shared__ __align__(16) float EF[CH];  // e^{G_i} of the current chunk (0 past its end)
+  // e^{G_i} of the chunks with D^T accumulator 0 / 1 (1 for the per-channel
+  // decay, whose tiles carry the scales; 0 past a chunk's end)
+  __shared__ __align__(16) float EF[2][CH];
   __shared__ uint32_t tmem_slot;
   __shared__ int ok_c;
   __shared__ volatile int mma_stop;
@@ -190,11 +204,10 @@ seq_kernel(FwdParams p) {
     // Chunk k: gate kBarD1 (S0, k < 64)      -> D^T  = S0[:, :64] [-w ; q~][:, :64]^T;
     //          gate kBarD (all of S0)        -> D^T += S0[:, 64:] [-w ; q~][:, 64:]^T, + u^T I;
     //          gate kBarS (k~ scaled, U^T)   -> S += U^T (e^{G_C-G} k~);
-    //          gate kBarO (outputs rescaled) -> D^T[:, 64..] += U^T P^T.
-    // mma_s covers the state update only (the next hand-over waits for it),
-    // except on a chain's last chunk, whose outputs are written right away.
-    // The compute warps only ever leave while this warp waits at kBarD1 or
-    // kBarS, so the stop flag is read there.
+    //                                           D^T[:, ..64] = U^T P^T.
+    // mma_s covers both (the next hand-over and a chain's last outputs wait
+    // for it).  The compute warps only ever leave while this warp waits at
+    // kBarD1 or kBarS, so the stop flag is read there.
     for (int k = 0;; ++k) {
       const int b = k % kStages;
       const uint32_t sb = sbase + b * ST_BYTES;
@@ -227,20 +240,15 @@ seq_kernel(FwdParams p) {
       __syncwarp();
       mma_gate<kBarS>();
       if (mma_stop) break;
-      const bool last = (desc[b].flags & 2) != 0;
       if (tid == kIssuer) {
         tc::fence_after_sync();
         tc::mma_op_ts(tmem + TM_S, tmem + TM_UT, tc::Opnd{sb + ST_K, BOX, true}, CH / 16,
                       tc::idesc_f16_f32(128, 128, false, true), true);
-        if (!last) tc::commit(&mma_s);
-      }
-      __syncwarp();
-      mma_gate<kBarO>();
-      if (tid == kIssuer) {
-        tc::fence_after_sync();
-        tc::mma_op_ts(tmem + dcol + CH, tmem + TM_UT, tc::Opnd{sb + ST_P, 0u, false}, CH / 16,
-                      tc::idesc_f16_f32(128, 64), true);
-        if (last) tc::commit(&mma_s);
+        // the outputs' U^T P^T over the U^T columns, which the compute warps
+        // have read
+        tc::mma_op_ts(tmem + dcol, tmem + TM_UT, tc::Opnd{sb + ST_P, 0u, false}, CH / 16,
+                      tc::idesc_f16_f32(128, 64), false);
+        tc::commit(&mma_s);
         tc::commit(&empty[b]);  // the stage is free once these MMAs are done
       }
       __syncwarp();
@@ -332,13 +340,20 @@ seq_kernel(FwdParams p) {
     bool dead = false;
     int next_gate = kBarD1;  // the gate the MMA warp waits at
     float amax = 0.f;
-    // outputs i = 32 hf .. 32 hf + 31 of the pending chunk: column 64 + i of
-    // its D^T at this thread's v (tcgen05.ld and the pair exchange are
-    // warp-collective, the token predicate guards the stores only)
+    // outputs i = 32 hf .. 32 hf + 31 of the pending chunk at this thread's
+    // v: e^{G_i} D^T[:, 64 + i] + D^T[:, i] (tcgen05.ld and the pair exchange
+    // are warp-collective, the token predicate guards the stores only)
     auto flush = [&]() {
-      float o[32];
+      float o[32], y[32];
       tc::tmem_ld32(tmem + lane + TM_D + p_ob * 128 + CH + hf * 32, o);
+      tc::tmem_ld32(tmem + lane + TM_D + p_ob * 128 + hf * 32, y);
       tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(&EF[p_ob][hf * 32 + e]);
+        fma2v(o[e], o[e + 1], f.x, f.y, y[e], y[e + 1]);
+        fma2v(o[e + 2], o[e + 3], f.z, f.w, y[e + 2], y[e + 3]);
+      }
       // a lane pair (v, v ^ 1) writes the two v of one token with one 4-byte
       // store: the even lane the even tokens, the odd lane the odd ones
       const bool odd = (v & 1) != 0;
@@ -389,7 +404,9 @@ seq_kernel(FwdParams p) {
       }
       // ---- state hand-over: S0 -> fp16 A operand, S <- e^{G_C} S0
       // (this thread: row v, k = 32 hf .. 32 hf + 31, then 64 + the same;
-      // the first K-block of the D product starts after the first pass)
+      // each pass releases its K-block of the D product as soon as its fp16
+      // copy is in, and the scaled state goes back while the product runs:
+      // the state update waits for it with the U^T store)
       tc::fence_proxy_async_smem();  // the zeroed u rows
       {
         const float dc = __expf(GC);
@@ -417,6 +434,10 @@ seq_kernel(FwdParams p) {
           }
           amax = fmaxf(amax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
           tc::tmem_st16u(tmem + lane + TM_S0 + k0 / 2, w16);
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          if (hh == 0) mma_release<kBarD1>();  // D^T = S0[:, :64] [-w ; q~][:, :64]^T
+          else mma_release<kBarD>();           // D^T += S0[:, 64:] [-w ; q~][:, 64:]^T + u^T
           if constexpr (kKda) {
 #pragma unroll
             for (int kk = 0; kk < 32; kk += 4) {
@@ -429,12 +450,8 @@ seq_kernel(FwdParams p) {
             for (int kk = 0; kk < 32; kk += 2) mul2(srow[kk], srow[kk + 1], dc);
           }
           tc::tmem_st32(tmem + lane + TM_S + k0, srow);
-          tc::tmem_wait_st();
-          tc::fence_before_sync();
-          if (hh == 0) mma_release<kBarD1>();  // D^T = S0[:, :64] [-w ; q~][:, :64]^T
         }
       }
-      mma_release<kBarD>();  // D^T += S0[:, 64:] [-w ; q~][:, 64:]^T + u^T
       next_gate = kBarS;
       const int ob = k & 1;
       const uint32_t dcol = TM_D + ob * 128;
@@ -470,7 +487,7 @@ seq_kernel(FwdParams p) {
           for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(krow + (((c0 + c + j) & 7) << 4)) = make_uint4(0, 0, 0, 0);
         }
-        if (tid < CH) EF[tid] = tid < n ? (kKda ? 1.f : __expf(GT[tid * 4 + 2 * r2])) : 0.f;
+        if (tid < CH) EF[ob][tid] = tid < n ? (kKda ? 1.f : __expf(GT[tid * 4 + 2 * r2])) : 0.f;
         tc::fence_proxy_async_smem();
       }
       if (!wait_c(&mma_y, ph_y)) { dead = true; break; }
@@ -495,25 +512,7 @@ seq_kernel(FwdParams p) {
         tc::tmem_wait_st();
       }
       tc::fence_before_sync();
-      mma_release<kBarS>();  // S += U^T (e^{G_C - G} k~)
-      // ---- O^T columns 64 + i <- e^{G_i} (.) before U^T P^T accumulates onto
-      // them (the per-channel-decay tiles carry the scales already; columns
-      // past the chunk's end are never stored)
-      if constexpr (!kKda) {
-        float o[32];
-        tc::tmem_ld32(tmem + lane + dcol + CH + hf * 32, o);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(EF + hf * 32 + e);
-          mul2v(o[e], o[e + 1], f.x, f.y);
-          mul2v(o[e + 2], o[e + 3], f.z, f.w);
-        }
-        tc::tmem_st32(tmem + lane + dcol + CH + hf * 32, o);
-        tc::tmem_wait_st();
-      }
-      tc::fence_before_sync();
-      mma_release<kBarO>();  // D^T[:, 64..] += U^T P^T
+      mma_release<kBarS>();  // S += U^T (e^{G_C - G} k~); D^T[:, ..64] = U^T P^T
       next_gate = kBarD1;
       // ---- the previous chunk's outputs (its U^T P^T finished before this
       // chunk's D product)
