@@ -57,6 +57,10 @@ constexpr int CH = 64;
 constexpr int KC = 4;
 constexpr int kThreads = 256;
 constexpr int R = 2;  // v-heads per k-head
+// the thread that fetches the item counter: a global atomic holds its thread
+// for the round trip, so a thread of the warps that sit out the gate
+// computation takes it
+constexpr int kCtr = 224;
 constexpr int XROWS = CH + KC - 1;
 constexpr uint32_t XSUB = 9216;  // one staged box: 72 rows x 128 B, 1024-aligned
 constexpr uint32_t XBOX_BYTES = 64 * XROWS * 2;
@@ -262,13 +266,13 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   const int gidx = item / Hk, kh = item % Hk;
   const int row0 = rec.x, n = rec.y, c = rec.z, kpre = rec.w;
   const int next = s_ni;
-  int nn = 0;  // (thread 0) counter value of the item after next
-  if (tid == 0 && next < n_items) nn = atomicAdd(&hdr[kItemHeadC], 1);
+  int nn = 0;  // (thread kCtr) counter value of the item after next
   if (tid == 0 && next < n_items) {
     mbar_arrive_expect_tx(&rbar, 16);
     bulk_g2s(&s_nx[par ^ 1u], recs + next / Hk, 16, &rbar);
     rpend = 1 + (int)par;
   }
+  if (tid == kCtr && next < n_items) nn = atomicAdd(&hdr[kItemHeadC], 1);
   int rblk = 0;  // the conv state is read on chunk 0 only
   if (c == 0) {
     const int s = p.work.pre()[kpre];
@@ -777,7 +781,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   // redo.  (The next item's staged gate inputs are visible after this barrier.)
   tc::fence_before_sync();
   if (!kConvOnly) asm volatile("cp.async.wait_all;" ::: "memory");
-  if (tid == 0 && next < n_items) s_ni = (int)gridDim.x + nn;  // read after the barrier
+  if (tid == kCtr && next < n_items) s_ni = (int)gridDim.x + nn;  // read after the barrier
   if (__syncthreads_or(!(amax <= kF16Max) || !(vmax <= kF16Max)) && tid == 0) {
     mark_redo(p.work, kpre, kh * R);
     mark_redo(p.work, kpre, kh * R + 1);

@@ -52,6 +52,7 @@ constexpr int D = 128;
 constexpr int CH = 64;
 constexpr int R = 2;  // v-heads per k-head
 constexpr int kThreads = 512;
+constexpr int kCtr = 480;  // the thread that fetches the item counter (a helper warp's)
 constexpr uint32_t BOX = 8192;         // 64 rows x 128 B
 constexpr uint32_t KB_STRIDE = 16384;  // K-blocks of a 128-row [q ; k] tile
 constexpr int AP = solve::AP;
@@ -294,8 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   const int gidx = item / Hv, h = item % Hv, kh = h / R, hl = h % R;
   const int n = rec.y, kpre = rec.w;
   const int next = s_ni;
-  int nn = 0;  // (thread 0) counter value of the item after next
-  if (tid == 0 && next < n_items) nn = atomicAdd(&hdr[kItemHeadK], 1);
+  int nn = 0;  // (thread kCtr) counter value of the item after next
   if (tid == 0 && next < n_items) {
     mbar_arrive_expect_tx(&rbar, 16);
     bulk_g2s(&s_next, recs + next / Hv, 16, &rbar);
@@ -631,6 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
         }
       });
     } else {
+      // a global atomic holds its thread for the round trip: a helper warp,
+      // idle for most of the solve, fetches the item counter
+      if (tid == kCtr && next < n_items) nn = atomicAdd(&hdr[kItemHeadK], 1);
       // zero rows 64..127 (64 x 128 B) and the six blocks above the diagonal
       // (16 rows x 32 B each) of the operand
       for (int q = tid - 192; q < 512 + 6 * 32; q += 320) {
@@ -697,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) kintra_kernel(FwdParams p) {
   // a value out of its range sends this chain to the token-serial redo
   tc::fence_before_sync();
   if (tid >= 2 * CH) cp_async_wait_all();  // the next item's gate inputs, visible after the barrier
-  if (tid == 0 && next < n_items) s_ni = (int)gridDim.x + nn;  // read after the barrier
+  if (tid == kCtr && next < n_items) s_ni = (int)gridDim.x + nn;  // read after the barrier
   if (__syncthreads_or(!(amax <= kF16Max)) && tid == 0) mark_redo(p.work, kpre, h);
   if (next >= n_items) break;
   item = next;
