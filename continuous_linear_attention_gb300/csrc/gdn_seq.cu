@@ -205,9 +205,11 @@ seq_kernel(FwdParams p) {
     //          gate kBarD (all of S0)        -> D^T += S0[:, 64:] [-w ; q~][:, 64:]^T, + u^T I;
     //          gate kBarS (k~ scaled, U^T)   -> S += U^T (e^{G_C-G} k~);
     //                                           D^T[:, ..64] = U^T P^T.
-    // mma_s covers both (the next hand-over and a chain's last outputs wait
-    // for it).  The compute warps only ever leave while this warp waits at
-    // kBarD1 or kBarS, so the stop flag is read there.
+    // mma_s covers the state update only (the next hand-over waits for it;
+    // the outputs are read after the next chunk's D product), except on a
+    // chain's last chunk, whose outputs are written right away.  The compute
+    // warps only ever leave while this warp waits at kBarD1 or kBarS, so the
+    // stop flag is read there.
     for (int k = 0;; ++k) {
       const int b = k % kStages;
       const uint32_t sb = sbase + b * ST_BYTES;
@@ -240,15 +242,17 @@ seq_kernel(FwdParams p) {
       __syncwarp();
       mma_gate<kBarS>();
       if (mma_stop) break;
+      const bool last = (desc[b].flags & 2) != 0;
       if (tid == kIssuer) {
         tc::fence_after_sync();
         tc::mma_op_ts(tmem + TM_S, tmem + TM_UT, tc::Opnd{sb + ST_K, BOX, true}, CH / 16,
                       tc::idesc_f16_f32(128, 128, false, true), true);
+        if (!last) tc::commit(&mma_s);
         // the outputs' U^T P^T over the U^T columns, which the compute warps
         // have read
         tc::mma_op_ts(tmem + dcol, tmem + TM_UT, tc::Opnd{sb + ST_P, 0u, false}, CH / 16,
                       tc::idesc_f16_f32(128, 64), false);
-        tc::commit(&mma_s);
+        if (last) tc::commit(&mma_s);
         tc::commit(&empty[b]);  // the stage is free once these MMAs are done
       }
       __syncwarp();
