@@ -206,7 +206,9 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t xbar1, xbar2, mbar, rbar;
   __shared__ uint32_t tmem_slot;
-  __shared__ int flag;
+  // the outcome of a CTA-wide wait; the record wait has its own, as it comes
+  // right after the X product's wait with no barrier in between
+  __shared__ int flag, rflag;
   __shared__ int s_ni;  // the CTA's next item (a dynamic counter hands them out)
   __shared__ float gtot[R];
   __shared__ int4 s_nx[2];  // the record of the item of each parity (by bulk copy on rbar)
@@ -510,7 +512,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       // the conv-only pass ends here: the two v-heads' v tiles to the scratch
       // (and the next item's record has landed)
       if (next < n_items) {
-        ok = cta_wait(&rbar, par, &flag);
+        ok = cta_wait(&rbar, par, &rflag);
         if (ok && tid == 0) rpend = 0;
       } else {
         __syncthreads();
@@ -533,7 +535,7 @@ cintra_kernel(FwdParams p, const __grid_constant__ CUtensorMap tmx) {
       // this item's start): stage its gate inputs (this item's were read
       // before the first barrier)
       if (ok && next < n_items) {
-        ok = cta_wait(&rbar, par, &flag);
+        ok = cta_wait(&rbar, par, &rflag);
         if (ok && tid == 0) rpend = 0;
         if (ok) stage_gates(p, s_nx[par ^ 1u], next % Hk, tid, sbase + OFF_GIN);
       }

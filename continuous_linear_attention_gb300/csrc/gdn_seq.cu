@@ -164,7 +164,10 @@ seq_kernel(FwdParams p) {
   // decay, whose tiles carry the scales; 0 past a chunk's end)
   __shared__ __align__(16) float EF[2][CH];
   __shared__ uint32_t tmem_slot;
-  __shared__ int ok_c;
+  // outcomes of the compute warps' waits, in two slots used in turn: two waits
+  // in a row have no other barrier between them, and a thread may read a
+  // slot after thread 0 has moved on to the next wait
+  __shared__ int ok_c[2];
   __shared__ volatile int mma_stop;
 
   pdl_wait_then_release();
@@ -332,10 +335,13 @@ seq_kernel(FwdParams p) {
     const int v = tid & 127;                           // TMEM lane = state row v
     const int hf = tid >> 7;                           // column half
     __nv_bfloat16* __restrict__ out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    int okslot = 0;
     auto wait_c = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (tid == 0) ok_c = mbar_wait_bounded(bar, parity) ? 1 : 0;
+      if (tid == 0) ok_c[okslot] = mbar_wait_bounded(bar, parity) ? 1 : 0;
       cbar();
-      return ok_c != 0;
+      const bool r = ok_c[okslot] != 0;
+      okslot ^= 1;
+      return r;
     };
     uint32_t ph_y = 0, ph_s = 0;
     bool s_busy = false;   // an MMA-S commit not waited for yet
@@ -381,10 +387,12 @@ seq_kernel(FwdParams p) {
       if (tid == 0) {
         bool okw = mbar_wait_bounded(&full[b], (k / kStages) & 1);
         if (okw && s_busy) okw = mbar_wait_bounded(&mma_s, ph_s);
-        ok_c = okw ? 1 : 0;
+        ok_c[okslot] = okw ? 1 : 0;
       }
       cbar();
-      if (!ok_c) { dead = true; break; }
+      const bool okt = ok_c[okslot] != 0;
+      okslot ^= 1;
+      if (!okt) { dead = true; break; }
       if (s_busy) {
         ph_s ^= 1;
         s_busy = false;
