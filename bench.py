@@ -53,9 +53,10 @@ def peaks():
                 "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def decode_bytes(wl) -> int:
-    """Algorithmic HBM bytes of one decode forward: per request the recurrent
-    state read + write, the conv state read + write, x, a, b and out; the conv
+def decode_bytes(wl, requests=None) -> int:
+    """Algorithmic HBM bytes of one decode forward (of `requests` decode
+    requests, all of the batch's by default): per request the recurrent state
+    read + write, the conv state read + write, x, a, b and out; the conv
     weight, A_log and dt_bias once.  With one gate per key channel (KDA) a has
     d_k entries per v-head and dt_bias is [Hv][d_k]."""
     d = wl.dims
@@ -64,7 +65,7 @@ def decode_bytes(wl) -> int:
     per_req = (2 * d.Hv * d.dk * d.dv * 4 + 2 * (d.K - 1) * d.C * act + d.C * act
                + d.Hv * gate * act + d.Hv * act + d.Hv * d.dv * act)
     weights = d.C * d.K * act + d.Hv * 4 + d.Hv * gate * 4
-    return wl.N * per_req + weights
+    return (wl.N if requests is None else requests) * per_req + weights
 
 
 def ssd_decode_bytes(wl) -> int:
@@ -217,6 +218,16 @@ def time_secondary(harness, wl, steps, device, pk, graph=False, warmup=3):
            "compute_kernels_ms_median": statistics.median(kall),
            "prefill_tflops": tf, "tensor_frac": tf / pk["bf16_tflops"],
            "algorithmic_flops": fl, "error_flags": flags}
+    n_dec = sum(1 for L in wl.seqlens() if L == 1)
+    if n_dec:
+        # the decode part at the HBM roof and the prefill part at the tensor
+        # roof, one after the other: the time a call could take if each part
+        # ran at its own roofline; its ratio to the measured time
+        dbytes = decode_bytes(wl, n_dec)
+        roof_ms = (dbytes / (pk["hbm_gbs"] * 1e9) + fl / (pk["bf16_tflops"] * 1e12)) * 1e3
+        res.update({"decode_requests": n_dec, "decode_algorithmic_bytes": dbytes,
+                    "decode_gbs_over_call": dbytes / (kms / 1e3) / 1e9,
+                    "roofline_sum_ms": roof_ms, "roofline_sum_frac": roof_ms / kms})
     if gms is not None:
         res["graph_replay_ms_per_step"] = gms
         res["graph_replay_tokens_per_s"] = wl.T / (gms / 1e3)
