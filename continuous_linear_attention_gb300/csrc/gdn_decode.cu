@@ -157,9 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
     // ======================= producer warp =======================
     if (tid != kConsumers) return;
     const int* dec = p.work.dec();
-    // this CTA's units: its index, then from the counter (one fetched ahead)
+    // this CTA's units: its index, then from the counter, each claimed when
+    // its first stage is issued (the ring's lead covers the atomic's round
+    // trip; a unit claimed a whole unit ahead left CTAs up to two units apart
+    // at the end)
     int unit = blockIdx.x;
-    int nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
     sm.issued = 0;
     for (int n = 0;; ++n) {
       const int st = n % kStages;
@@ -168,10 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(FwdParams p) {
         return;
       }
       const int k = n / R, jh = n % R;
-      if (jh == 0 && k > 0) {
-        unit = nxt;
-        if (unit < n_units) nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
-      }
+      if (jh == 0 && k > 0) unit = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
       if (unit >= n_units) {
         // no more units: an empty stage tells the compute warps
         sm.meta[st].unit = -1;

@@ -278,9 +278,9 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
     const int* dec = p.work.dec();
     const uint32_t unit_ch = (uint32_t)(hpg * DP + 2 * DN);
     // this CTA's units (request, group): its index, then from a counter the
-    // scheduler resets (one fetched ahead), so that no CTA ends far behind
+    // scheduler resets, each claimed when its first stage is issued, so that
+    // no CTA ends far behind
     int unit = blockIdx.x;
-    int nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
     sm.issued = 0;
     for (int n = 0;; ++n) {
       const int st = n % kDStages;
@@ -289,10 +289,7 @@ __global__ void __launch_bounds__(kDThreads, 1) ssd_decode_kernel(SsdParams p) {
         return;
       }
       const int k = n / hpg, j = n % hpg;
-      if (j == 0 && k > 0) {
-        unit = nxt;
-        if (unit < n_units) nxt = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
-      }
+      if (j == 0 && k > 0) unit = (int)gridDim.x + atomicAdd(&hdr[kDecHead], 1);
       if (unit >= n_units) {
         // no more units: an empty stage tells the compute warps
         sm.unit[st] = -1;
