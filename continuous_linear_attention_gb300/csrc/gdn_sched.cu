@@ -72,11 +72,56 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     }
   }
   __syncthreads();
+  // A batch of up to kEarly sequences per thread is classified before the
+  // wait (list positions from the shared counters, kept in registers; the
+  // inputs and the block counts are this call's own): after it the lists are
+  // only written, with no global read on the way.
+  constexpr int kEarly = 4;
+  const bool early = N <= kEarly * kSchedThreads;
+  int kind[kEarly], at[kEarly], lat[kEarly];  // 0 none, 1 decode, 2 prefill; item and list positions
+#pragma unroll
+  for (int k = 0; k < kEarly; ++k) kind[k] = 0;
+  if (early) {
+#pragma unroll
+    for (int k = 0; k < kEarly; ++k) {
+      const int s = tid + k * kSchedThreads;
+      if (s >= N) continue;
+      const int len = cu[s + 1] - cu[s];
+      const int b = blk[s];
+      if (b <= 0 || b >= num_blocks || len <= 0) continue;
+      if (atomicAdd(&blk_count[b], 0) > 1) {
+        atomicOr(&s_flags, GDN_FLAG_DUPLICATE);
+        continue;
+      }
+      if (hint > 0 && len > hint) {
+        atomicOr(&s_flags, GDN_FLAG_HINT);
+        continue;
+      }
+      at[k] = atomicAdd(&s_n_items, 1);
+      if (len == 1) {
+        kind[k] = 1;
+        lat[k] = atomicAdd(&s_n_dec, 1);
+      } else {
+        kind[k] = 2;
+        lat[k] = atomicAdd(&s_n_pre, 1);
+        atomicAdd(&s_pre_tokens, len);
+      }
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   int32_t* items = work.items();
   int32_t* dec = work.dec();
   int32_t* pre_tmp = work.pre_tmp();
-  for (int s = tid; s < N; s += kSchedThreads) {
+  if (early) {
+#pragma unroll
+    for (int k = 0; k < kEarly; ++k) {
+      if (!kind[k]) continue;
+      const int s = tid + k * kSchedThreads;
+      items[at[k]] = s;
+      (kind[k] == 1 ? dec : pre_tmp)[lat[k]] = s;
+    }
+  }
+  for (int s = early ? N : tid; s < N; s += kSchedThreads) {
     const int len = cu[s + 1] - cu[s];
     const int b = blk[s];
     if (b <= 0 || b >= num_blocks || len <= 0) continue;
@@ -97,8 +142,22 @@ schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ blk,
     }
   }
   __syncthreads();
-  // Rank sort of the prefill sequences: longest first, ties by sequence id.
   const int n_pre = s_n_pre;
+  if (n_pre == 0) {
+    // no prefill sequence: no sort, no chunk prefix beyond its zero, no records
+    if (tid == 0) {
+      work.pre_cp()[0] = 0;
+      if (s_flags) atomicOr((unsigned*)&hdr[kErr], s_flags);
+      hdr[kPreChunks] = 0;
+      hdr[kNItems] = s_n_items;
+      hdr[kNDec] = s_n_dec;
+      hdr[kNPre] = 0;
+      hdr[kPreTokens] = 0;
+      hdr[kWorkHead] = hdr[kItemHeadC] = hdr[kItemHeadK] = hdr[kDecHead] = 0;
+    }
+    return;
+  }
+  // Rank sort of the prefill sequences: longest first, ties by sequence id.
   int32_t* pre = work.pre();
   for (int i = tid; i < n_pre; i += kSchedThreads) {
     const int si = pre_tmp[i];
