@@ -8,6 +8,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_sessionstart(session):
+    """The library under test is built in-tree; a checkout without it builds it
+    first (nvcc cross-compiles for sm_103a without a GPU)."""
+    from continuous_linear_attention_gb300 import build
+    if not os.path.exists(build.LIB_PATH):
+        build.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long CPU oracle runs")
