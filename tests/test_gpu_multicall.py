@@ -1,0 +1,89 @@
+"""GPU parity over several calls on one pool: every request's tokens arrive
+spread over consecutive calls in segments of mixed kinds — nothing, a single
+token (the decode kernel), a short or a multi-chunk prefill (the chunked
+path), with or without a past — so that one call mixes decodes and prefills
+and a request's state passes from one kernel path to another between calls.
+The concatenated outputs and the final states must equal the oracle's single
+pass over the whole sequences.  This exercises the per-call reset of the
+persistent kernels' counters, the late decode behind the recurrence, and the
+continuation of conv and recurrent states across paths."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from continuous_linear_attention_gb300 import harness, synth
+
+from gpu_check import TOL, log_errs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _calls(whole, bounds):
+    """Split every sequence s of ``whole`` at the offsets bounds[s] (0 = b_0 <=
+    b_1 <= ... <= b_K = length) into K consecutive calls on the same blocks; a
+    request whose earlier segments were all empty keeps its own has_past."""
+    cu = whole.cu_seqlens.tolist()
+    n_calls = len(bounds[0]) - 1
+    calls = []
+    for k in range(n_calls):
+        rows, lens, hp = [], [], []
+        for s in range(whole.N):
+            lo, hi = cu[s] + bounds[s][k], cu[s] + bounds[s][k + 1]
+            rows.extend(range(lo, hi))
+            lens.append(hi - lo)
+            hp.append(int(whole.has_past[s]) if bounds[s][k] == 0 else 1)
+        idx = torch.tensor(rows, dtype=torch.int64)
+        ncu = np.zeros(whole.N + 1, dtype=np.int32)
+        ncu[1:] = np.cumsum(lens)
+        calls.append(dataclasses.replace(
+            whole, name=f"{whole.name}_call{k}", x=whole.x[idx].contiguous(),
+            a=whole.a[idx].contiguous(), b=whole.b[idx].contiguous(),
+            cu_seqlens=torch.from_numpy(ncu), has_past=torch.tensor(hp, dtype=torch.uint8)))
+    return calls
+
+
+@pytest.mark.parametrize("seed", [81, 82])
+def test_requests_spread_over_calls_of_mixed_kinds_match_one_pass(seed):
+    rng = np.random.default_rng(seed)
+    n_req, n_calls = 20, 5
+    # per request and call: 0 tokens, 1 token, a short prefill or one over several chunks
+    kinds = rng.choice(4, size=(n_req, n_calls), p=[0.15, 0.45, 0.25, 0.15])
+    seg = np.where(kinds == 0, 0, np.where(kinds == 1, 1, np.where(
+        kinds == 2, rng.integers(2, 64, size=kinds.shape), rng.integers(64, 300, size=kinds.shape))))
+    seg[seg.sum(axis=1) == 0, 0] = 1  # every request has a token somewhere
+    lens = seg.sum(axis=1).tolist()
+    has_past = rng.integers(0, 2, size=n_req).tolist()
+    dims = synth.Dims(Hk=4, Hv=8, dk=128, dv=128, K=4, act=synth.BF16)
+    whole = synth.make_workload("multicall", dims, lens, has_past, 64, seed)
+    bounds = [[0] + np.cumsum(seg[s]).tolist() for s in range(n_req)]
+    calls = _calls(whole, bounds)
+    ref = oracle.forward(whole)
+
+    run = harness.DeviceRun(calls[0])
+    outs = []
+    for k, wl in enumerate(calls):
+        if k:
+            run.set_inputs(wl)
+        run.run()
+        torch.cuda.synchronize()
+        assert run.pool.error_flags() == 0, k
+        outs.append(run.out.double().cpu().numpy())
+    # each request's rows, call after call, in the whole batch's order
+    got = np.concatenate([
+        np.concatenate([outs[k][int(calls[k].cu_seqlens[s]):int(calls[k].cu_seqlens[s + 1])]
+                        for k in range(n_calls)])
+        for s in range(n_req)])
+    err_out = rel_l2(got, ref["out"])
+    ref_blocks = [int(v) for v in whole.ref_blocks]
+    err_rec = 0.0
+    for s in range(n_req):
+        blk = int(whole.block_idx[s])
+        r = ref_blocks.index(blk)
+        err_rec = max(err_rec, rel_l2(run.rec_view(blk).cpu().numpy(), ref["rec_state"][r]))
+        np.testing.assert_array_equal(run.conv_view(blk).float().cpu().numpy().astype(np.float64),
+                                      ref["conv_state"][r])
+    log_errs({"out": err_out, "rec": err_rec})
+    assert err_out <= TOL["bf16"] and err_rec <= TOL["bf16"], (err_out, err_rec)
