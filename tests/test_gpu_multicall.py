@@ -4,7 +4,8 @@ token (the decode kernel), a short or a multi-chunk prefill (the chunked
 path), with or without a past — so that one call mixes decodes and prefills
 and a request's state passes from one kernel path to another between calls.
 The concatenated outputs and the final states must equal the oracle's single
-pass over the whole sequences.  This exercises the per-call reset of the
+pass over the whole sequences (scalar gate, and one case with the
+per-channel decay).  This exercises the per-call reset of the
 persistent kernels' counters, the late decode behind the recurrence, and the
 continuation of conv and recurrent states across paths."""
 import dataclasses
@@ -45,8 +46,8 @@ def _calls(whole, bounds):
     return calls
 
 
-@pytest.mark.parametrize("seed", [81, 82])
-def test_requests_spread_over_calls_of_mixed_kinds_match_one_pass(seed):
+@pytest.mark.parametrize("seed,channel_gate", [(81, False), (82, False), (83, True)])
+def test_requests_spread_over_calls_of_mixed_kinds_match_one_pass(seed, channel_gate):
     rng = np.random.default_rng(seed)
     n_req, n_calls = 20, 5
     # per request and call: 0 tokens, 1 token, a short prefill or one over several chunks
@@ -57,7 +58,8 @@ def test_requests_spread_over_calls_of_mixed_kinds_match_one_pass(seed):
     lens = seg.sum(axis=1).tolist()
     has_past = rng.integers(0, 2, size=n_req).tolist()
     dims = synth.Dims(Hk=4, Hv=8, dk=128, dv=128, K=4, act=synth.BF16)
-    whole = synth.make_workload("multicall", dims, lens, has_past, 64, seed)
+    whole = synth.make_workload("multicall", dims, lens, has_past, 64, seed,
+                                channel_gate=channel_gate)
     bounds = [[0] + np.cumsum(seg[s]).tolist() for s in range(n_req)]
     calls = _calls(whole, bounds)
     ref = oracle.forward(whole)
