@@ -158,6 +158,16 @@ class SsdDeviceRun:
         return torch.stack([self.mem[self.block_offset(int(b)): self.block_offset(int(b)) +
                                      self.stride] for b in blocks]).cpu()
 
+    def set_inputs(self, wl: SsdWorkload):
+        """Point the run at another batch over the same pool (a continuation)."""
+        dev = self.xbc.device
+        self.wl = wl
+        self.xbc, self.dt = wl.xbc.to(dev), wl.dt.to(dev)
+        self.cu, self.idx, self.has_past = (wl.cu_seqlens.to(dev), wl.block_idx.to(dev),
+                                            wl.has_past.to(dev))
+        act = torch.bfloat16 if wl.dims.act == "bf16" else torch.float32
+        self.y = torch.full((wl.T, wl.dims.H, wl.dims.P), OUT_SENTINEL, dtype=act, device=dev)
+
     def run(self, stream=None, max_seqlen_hint: int = 0):
         binding.ssd_varlen_forward(self.pool, self.layer, self.xbc, self.dt, self.cu, self.idx,
                                    self.has_past, self.conv_w, self.A_log, self.dt_bias, self.D,

@@ -89,3 +89,70 @@ def test_requests_spread_over_calls_of_mixed_kinds_match_one_pass(seed, channel_
                                       ref["conv_state"][r])
     log_errs({"out": err_out, "rec": err_rec})
     assert err_out <= TOL["bf16"] and err_rec <= TOL["bf16"], (err_out, err_rec)
+
+
+def _ssd_calls(whole, bounds):
+    """The Mamba2 workload's sequences split at ``bounds`` into consecutive
+    calls, as ``_calls`` does for the gated delta rule."""
+    cu = whole.cu_seqlens.tolist()
+    n_calls = len(bounds[0]) - 1
+    calls = []
+    for k in range(n_calls):
+        rows, lens, hp = [], [], []
+        for s in range(whole.N):
+            lo, hi = cu[s] + bounds[s][k], cu[s] + bounds[s][k + 1]
+            rows.extend(range(lo, hi))
+            lens.append(hi - lo)
+            hp.append(int(whole.has_past[s]) if bounds[s][k] == 0 else 1)
+        idx = torch.tensor(rows, dtype=torch.int64)
+        ncu = np.zeros(whole.N + 1, dtype=np.int32)
+        ncu[1:] = np.cumsum(lens)
+        calls.append(dataclasses.replace(
+            whole, name=f"{whole.name}_call{k}", xbc=whole.xbc[idx].contiguous(),
+            dt=whole.dt[idx].contiguous(), cu_seqlens=torch.from_numpy(ncu),
+            has_past=torch.tensor(hp, dtype=torch.uint8)))
+    return calls
+
+
+def test_mamba2_requests_spread_over_calls_match_one_pass():
+    """The same over the Mamba2 scan: requests' tokens over five calls in
+    segments of mixed kinds (decode kernel, chunked scan), y and the final
+    conv and SSM states against the oracle's single pass."""
+    rng = np.random.default_rng(91)
+    n_req, n_calls = 12, 5
+    kinds = rng.choice(4, size=(n_req, n_calls), p=[0.15, 0.45, 0.25, 0.15])
+    seg = np.where(kinds == 0, 0, np.where(kinds == 1, 1, np.where(
+        kinds == 2, rng.integers(2, 64, size=kinds.shape), rng.integers(64, 300, size=kinds.shape))))
+    seg[seg.sum(axis=1) == 0, 0] = 1
+    lens = seg.sum(axis=1).tolist()
+    has_past = rng.integers(0, 2, size=n_req).tolist()
+    dims = synth.SsdDims(H=16, P=64, N=128, G=2, K=4, act="bf16")
+    whole = synth.make_ssd_workload("ssd_multicall", dims, lens, has_past, 32, 91)
+    bounds = [[0] + np.cumsum(seg[s]).tolist() for s in range(n_req)]
+    calls = _ssd_calls(whole, bounds)
+    ref = oracle.ssd_forward(whole)
+
+    run = harness.SsdDeviceRun(calls[0])
+    ys = []
+    for k, wl in enumerate(calls):
+        if k:
+            run.set_inputs(wl)
+        run.run()
+        torch.cuda.synchronize()
+        assert run.pool.error_flags() == 0, k
+        ys.append(run.y.float().cpu().numpy().astype(np.float64))
+    got = np.concatenate([
+        np.concatenate([ys[k][int(calls[k].cu_seqlens[s]):int(calls[k].cu_seqlens[s + 1])]
+                        for k in range(n_calls)])
+        for s in range(n_req)])
+    err_y = rel_l2(got, ref["y"])
+    blocks = [int(whole.block_idx[s]) for s in range(n_req)]
+    raw = run.block_bytes(blocks).numpy().reshape(-1)
+    conv, ssm = oracle.read_ssd_pool_states(raw, 0, range(len(blocks)), dims, len(blocks), 1)
+    ref_blocks = [int(v) for v in whole.ref_blocks]
+    idx = [ref_blocks.index(b) for b in blocks]
+    np.testing.assert_array_equal(conv, ref["conv_state"][idx])
+    err_ssm = rel_l2(ssm, ref["ssm_state"][idx])
+    log_errs({"y": err_y, "ssm": err_ssm})
+    assert err_y <= TOL["bf16"] and err_ssm <= TOL["bf16"], (err_y, err_ssm)
+    run.close()
