@@ -156,3 +156,65 @@ def test_mamba2_requests_spread_over_calls_match_one_pass():
     log_errs({"y": err_y, "ssm": err_ssm})
     assert err_y <= TOL["bf16"] and err_ssm <= TOL["bf16"], (err_y, err_ssm)
     run.close()
+
+
+def test_one_captured_graph_replayed_over_changing_batches():
+    """A serving loop's pattern: one CUDA graph captured for a fixed token
+    count and request count (after the prefill scratch is reserved), then
+    replayed over batches of different compositions written into its input
+    buffers — decodes, prefills, a padding request (block -1) taking the
+    leftover rows.  Every replay equals an eager call on the same inputs from
+    the same pool state, bit for bit (outputs of the real requests and the
+    whole pool)."""
+    T, n_req = 512, 8
+    rng = np.random.default_rng(7)
+    dims = synth.FULL_DIMS
+    # requests on blocks 1..7 (with past states), the padding request last
+    base = synth.make_workload("graph_serve", dims, [1] * 7 + [T - 7], [1] * 7 + [0], 16, 71,
+                               block_idx=list(range(1, n_req)) + [-1])
+    steps = []
+    for k in range(4):
+        kinds = rng.choice(3, size=n_req - 1, p=[0.2, 0.5, 0.3])
+        lens = [0 if c == 0 else (1 if c == 1 else int(rng.integers(2, 150))) for c in kinds]
+        if sum(lens) > T:
+            lens = [1] * (n_req - 1)
+        lens.append(T - sum(lens))  # the padding request takes the leftover rows
+        cu = np.zeros(n_req + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lens)
+        g = torch.Generator().manual_seed(100 + k)
+        steps.append(dataclasses.replace(
+            base, name=f"graph_serve_{k}",
+            x=torch.randn(T, dims.C, generator=g).to(base.x.dtype),
+            a=torch.randn(T, dims.Hv, generator=g).to(base.a.dtype),
+            b=torch.randn(T, dims.Hv, generator=g).to(base.b.dtype),
+            cu_seqlens=torch.from_numpy(cu),
+            block_idx=torch.tensor(list(range(1, n_req)) + [-1], dtype=torch.int32),
+            has_past=torch.tensor([1] * (n_req - 1) + [0], dtype=torch.uint8)))
+    eager = harness.DeviceRun(steps[0])
+    graphed = harness.DeviceRun(steps[0])
+    snapshot = graphed.mem.clone()
+    graphed.pool.reserve(T)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graphed.run(stream=s)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=s):
+        graphed.run(stream=s)
+    graphed.mem.copy_(snapshot)
+    torch.cuda.synchronize()
+    for k, st in enumerate(steps):
+        if k:
+            eager.set_inputs(st)
+        eager.run()
+        for dst, src in ((graphed.x, st.x), (graphed.a, st.a), (graphed.b, st.b),
+                         (graphed.cu, st.cu_seqlens), (graphed.idx, st.block_idx),
+                         (graphed.has_past, st.has_past)):
+            dst.copy_(src)
+        cg.replay()
+        torch.cuda.synchronize()
+        assert eager.pool.error_flags() == 0 and graphed.pool.error_flags() == 0
+        real = int(st.cu_seqlens[n_req - 1])  # rows of the real requests
+        assert torch.equal(eager.out[:real], graphed.out[:real]), k
+        assert torch.equal(eager.mem, graphed.mem), k
